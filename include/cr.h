@@ -1,0 +1,248 @@
+/*
+ * cr.h -- C ABI of libcr, the emulated-rank gradient collectives for one
+ * GB300 GPU.
+ *
+ * N data-parallel ranks are emulated as N buffers resident in the HBM of one
+ * GPU.  Each collective is one (or a few) CUDA kernels that read the rank
+ * buffers directly; a "message" of the ring schedule becomes a global load
+ * by the thread that reduces that element.  The ring schedule survives as
+ * the per-chunk order in which the ranks' contributions are summed, so the
+ * result is reproducible and equal, bit for bit, to the ring's.
+ *
+ * Page abbreviations used in the citations:
+ *   [DT]  "Distributed Training for Large Models: Collectives, FSDP/ZeRO,
+ *          DeviceMesh, and Multi-Dimensional Parallelism" (zexinliu.github.io)
+ *   [AIG] "AI Infra Guide, Chapter 6: Distributed Training Basics"
+ *          (theaiera.top, ch06)
+ *   [NX]  nxmr.cn news 160867, the article on collective communication and
+ *          model parallelism (numbered sub-headings 1.1 .. 7)
+ *
+ * Conventions shared by every entry point
+ *  - Pointer arrays (bufs, out_shards, ...) are HOST arrays of DEVICE
+ *    pointers, one per rank; the library copies them into the kernel's
+ *    parameters, so the host arrays may be reused as soon as the call returns.
+ *  - The caller owns every device buffer.  No entry point allocates device
+ *    memory; apart from cr_bucket_plan (which mallocs the host-side plan the
+ *    caller releases with cr_bucket_plan_free) nothing allocates at all, and
+ *    the library keeps no state between calls beyond cached device
+ *    attributes.
+ *  - Every launching call is asynchronous on `stream` (NULL = the legacy
+ *    default stream).  Argument errors are detected on the host before any
+ *    launch and leave all buffers untouched; a failed launch returns
+ *    CR_ERR_CUDA.  cr_last_error() gives the detail of the last failure on
+ *    the calling thread.
+ *  - Chunking (a1): with L = ceil(count/N), chunk j is the element range
+ *    [j*L, min((j+1)*L, count)); trailing chunks may be short or empty, as
+ *    with torch.chunk-style uneven Shard(0) shards ([DT] section 4, FSDP2).
+ *    Shard j of a reduce-scatter is chunk j reduced over all ranks.
+ *  - Reduction order: chunk j is summed starting from rank (j+1) mod N and
+ *    ending at its owner j, as the ring reduce-scatter of [DT] section 2
+ *    (Reduce-Scatter, N=4 schedule) and [NX] 2.2 do:
+ *        y_j = ((x_{j+1} + x_{j+2}) + ... ) + x_j     (ranks mod N)
+ *    Partial sums are fp32 for fp32/bf16 inputs (reduce dtype fp32,
+ *    [AIG] 6.3.4) and int32 with two's-complement wrap for int32.
+ *  - CR_AVG divides the finished fp32 sum by N once ([DT] section 2,
+ *    All-Reduce: G = sum_i G_i / N); bf16 outputs are rounded to nearest
+ *    even once, after the average.
+ *  - Every pointer must be aligned to its element size (CR_ERR_ALIGNMENT).
+ *    16-byte aligned buffers take the 128-bit vector path; others a slower
+ *    element-wise path with identical results.
+ */
+#ifndef CR_H
+#define CR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so that no CUDA header is
+ * needed to use the library. */
+typedef struct CUstream_st* cr_stream_t;
+
+typedef enum {
+  CR_OK = 0,
+  CR_ERR_INVALID_ARG = 1, /* NULL where a pointer is needed, bad N/count,
+                             overlapping buffers that may not overlap    */
+  CR_ERR_UNSUPPORTED = 2, /* legal but unimplemented dtype/op combination */
+  CR_ERR_ALIGNMENT = 3,   /* pointer not aligned to its element size      */
+  CR_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed         */
+  CR_ERR_TIMEOUT = 5      /* reserved for host-side fault harnesses       */
+} cr_status;
+
+typedef enum { CR_F32 = 0, CR_BF16 = 1, CR_I32 = 2 } cr_dtype;
+typedef enum { CR_SUM = 0, CR_AVG = 1 } cr_op;
+
+#define CR_MAX_RANKS 64
+
+/* ---- errors and version ------------------------------------------------ */
+const char* cr_status_string(cr_status status);
+/* Detail of the last non-OK status returned on this thread ("" if none).
+ * The string is owned by the library and valid until the next call. */
+const char* cr_last_error(void);
+/* Library version, major*10000 + minor*100 + patch. */
+int cr_version(void);
+
+/* ---- a1: chunking ---------------------------------------------------------
+ * cr_chunk_len: L = ceil(count/nranks) (0 if nranks < 1).
+ * cr_shard_range: element range [*lo, *hi) of chunk j.  CR_ERR_INVALID_ARG
+ * if nranks is outside [1, CR_MAX_RANKS], j outside [0, nranks) or an output
+ * pointer is NULL.  Host only. */
+size_t cr_chunk_len(size_t count, int nranks);
+cr_status cr_shard_range(size_t count, int nranks, int j, size_t* lo,
+                         size_t* hi);
+
+/* ---- a2/a3: reduce-scatter ------------------------------------------------
+ * [DT] section 2, Reduce-Scatter: y_j = sum over source ranks i of x_{j,i},
+ * where x_{j,i} is chunk j of rank i's buffer; rank j keeps y_j.
+ *   bufs[r]        rank r's input, `count` elements of in_dtype
+ *   out_shards[j]  shard j, cr_shard_range(count, nranks, j) length, of
+ *                  out_dtype (may be NULL when that shard is empty)
+ *   op             CR_SUM or CR_AVG (CR_AVG needs a floating type)
+ * Supported (in, out): (F32,F32), (BF16,BF16), (BF16,F32), (I32,I32).
+ * In place is allowed when in_dtype == out_dtype and
+ * out_shards[j] == (char*)bufs[j] + j*L*esize; any other overlap between an
+ * output and an input, or between two outputs, is CR_ERR_INVALID_ARG.
+ * Vector path: all pointers 16-byte aligned and L*esize(in) and
+ * L*esize(out) multiples of 16. */
+cr_status cr_reduce_scatter(const void* const* bufs, int nranks, size_t count,
+                            cr_dtype in_dtype, cr_op op,
+                            void* const* out_shards, cr_dtype out_dtype,
+                            cr_stream_t stream);
+
+/* ---- a4: all-gather -------------------------------------------------------
+ * [DT] section 2, All-Gather: every rank receives concat(p_0, ..., p_{N-1}).
+ *   shards[j]  shard j, cr_shard_range length, of dtype (NULL if empty)
+ *   bufs[r]    rank r's output, `count` elements:
+ *              bufs[r][j*L + k] = shards[j][k] for every r
+ * In place is allowed when shards[j] == (char*)bufs[j] + j*L*esize (that
+ * store is then skipped); other overlaps are CR_ERR_INVALID_ARG.
+ * Vector path: 16-byte aligned pointers and L*esize a multiple of 16. */
+cr_status cr_all_gather(const void* const* shards, int nranks, size_t count,
+                        cr_dtype dtype, void* const* bufs, cr_stream_t stream);
+
+/* ---- a5: all-reduce -------------------------------------------------------
+ * [DT] section 2, All-Reduce = Reduce-Scatter + All-Gather, fused into one
+ * kernel: every element of every output buffer receives the reduced value
+ * of that element.  in[r] and out[r], `count` elements each.  in == out per
+ * rank (in place) is allowed when in_dtype == out_dtype; other overlaps are
+ * CR_ERR_INVALID_ARG.  Supported pairs as for cr_reduce_scatter.
+ * Vector path: all pointers 16-byte aligned (any L). */
+cr_status cr_all_reduce(const void* const* in, int nranks, size_t count,
+                        cr_dtype in_dtype, cr_op op, void* const* out,
+                        cr_dtype out_dtype, cr_stream_t stream);
+
+/* ---- a6: DDP bucket plan (host) -------------------------------------------
+ * [AIG] 6.2.4: gradients go into buckets (default 25 MB) in the order
+ * backward produces them; [AIG] 6.2.6 Horovod Tensor Fusion; [NX] 5.1.
+ * Tensors are visited from the last index to the first (backward order) and
+ * appended to the current bucket while its bytes plus the tensor's stay
+ * within cap_bytes; otherwise a new bucket starts.  A tensor is never split;
+ * one larger than the cap gets a bucket of its own.  Tensor offsets inside a
+ * bucket are contiguous, in elements, with no padding (the flat layout of
+ * [DT] section 4, FSDP1 FlatParameter).
+ * On success *plan receives a host object the caller releases with
+ * cr_bucket_plan_free.  CR_ERR_INVALID_ARG: ntensors < 0, numels NULL with
+ * ntensors > 0, elem_size 0, cap_bytes 0, plan NULL, or byte sizes that
+ * overflow size_t. */
+typedef struct cr_bucket_plan_t {
+  int ntensors;
+  int nbuckets;
+  size_t elem_size;
+  size_t cap_bytes;
+  size_t* numels;        /* [ntensors], copy of the input                */
+  int* tensor_bucket;    /* [ntensors], bucket holding tensor t          */
+  size_t* tensor_offset; /* [ntensors], element offset inside the bucket */
+  size_t* bucket_numel;  /* [nbuckets], elements in bucket b             */
+} cr_bucket_plan_t;
+
+cr_status cr_bucket_plan(const size_t* numels, int ntensors, size_t elem_size,
+                         size_t cap_bytes, cr_bucket_plan_t** plan);
+void cr_bucket_plan_free(cr_bucket_plan_t* plan);
+
+/* ---- a7: bucket pack / unpack ---------------------------------------------
+ * Byte copies between each rank's tensors and its buckets:
+ *   pack:   buckets[r*B + b][off_t + i] = tensors[r*T + t][i]
+ *   unpack: tensors[r*T + t][i] = buckets[r*B + b][off_t + i]
+ * with b = plan->tensor_bucket[t], off_t = plan->tensor_offset[t],
+ * T = plan->ntensors, B = plan->nbuckets.  Pointers may be NULL only for
+ * empty tensors; every pointer must be aligned to plan->elem_size.
+ * Tensors and buckets must not overlap (not checked).  Any byte offset is
+ * handled; the copies run as 16-byte vectors with funnel shifts when the
+ * source and destination are mutually misaligned. */
+cr_status cr_bucket_pack(const cr_bucket_plan_t* plan, int nranks,
+                         const void* const* tensors, void* const* buckets,
+                         cr_stream_t stream);
+cr_status cr_bucket_unpack(const cr_bucket_plan_t* plan, int nranks,
+                           const void* const* buckets, void* const* tensors,
+                           cr_stream_t stream);
+
+/* DDP middle step: cr_all_reduce in place on every bucket, bucket by bucket
+ * in index order (bucket b of rank r is buckets[r*B + b]). */
+cr_status cr_bucket_all_reduce(const cr_bucket_plan_t* plan, int nranks,
+                               void* const* buckets, cr_dtype dtype, cr_op op,
+                               cr_stream_t stream);
+
+/* ---- a8..a10: fused FSDP / ZeRO-3 step ------------------------------------
+ * One kernel performs the step of [DT] section 4 (ZeRO-3/FSDP flow steps
+ * 5-6; FSDP1 unit lifecycle "backward post-hook" then "optimizer step" then
+ * the next forward's all-gather) for one flat parameter buffer:
+ *   1. reduce-scatter of the bf16 grads, fp32 partials in ring order, / N
+ *      (reduce_dtype fp32, keep_low_precision_grads=False, [AIG] 6.3.4);
+ *   2. AdamW on owner j's fp32 master/m/v shard with that fp32 gradient;
+ *   3. bf16 round-to-nearest-even of the updated master shard;
+ *   4. all-gather of the bf16 shards into every rank's param buffer.
+ * AdamW (decoupled weight decay; the pages name torch.optim.AdamW but do
+ * not print its rule), each operation an individually rounded fp32 op:
+ *   p <- p*(1 - lr*wd);  m <- b1*m + (1-b1)*g;  v <- b2*v + (1-b2)*(g*g);
+ *   p <- p - lr*((m/(1-b1^t)) / (sqrt(v/(1-b2^t)) + eps))
+ * with the scalars 1-lr*wd, 1-b1, 1-b2, 1-b1^t, 1-b2^t formed in double
+ * and rounded once to fp32.
+ *   grads_bf16[r]   rank r's local full gradient, count bf16
+ *   master/m/v[j]   owner j's fp32 shard, cr_shard_range length (in/out)
+ *   params_bf16[r]  rank r's full bf16 parameter buffer, count (output)
+ * No buffer may overlap another (CR_ERR_INVALID_ARG).  cfg->step >= 1.
+ * Vector path: 16-byte aligned pointers and L a multiple of 8. */
+typedef struct {
+  double lr, beta1, beta2, eps, weight_decay;
+  int64_t step;
+} cr_adamw_cfg;
+
+cr_status cr_fsdp_step(const void* const* grads_bf16, int nranks,
+                       size_t count, float* const* master, float* const* m,
+                       float* const* v, const cr_adamw_cfg* cfg,
+                       void* const* params_bf16, cr_stream_t stream);
+
+/* a9 alone: AdamW as above on n fp32 elements with an fp32 gradient
+ * (for example a shard produced by cr_reduce_scatter with out_dtype F32);
+ * param_bf16 (may be NULL) receives the bf16 cast of the updated master.
+ * No overlaps allowed. */
+cr_status cr_adamw_step(size_t n, float* master, float* m, float* v,
+                        const float* grad, const cr_adamw_cfg* cfg,
+                        void* param_bf16, cr_stream_t stream);
+
+/* ---- a11: communication accounting (host) ---------------------------------
+ * Elements rank `rank` sends and receives, and the logical steps taken, in
+ * the ring schedule of [DT] section 2 (reduce-scatter N-1 steps, all-gather
+ * N-1 steps, all-reduce both) or in the naive schedule of [NX] 2.2
+ * (reduce to rank 0, then broadcast from it; all-reduce only).  Multiply by
+ * the element size for bytes: with N | count, ring all-reduce gives
+ * 2(N-1)/N * count per rank and naive gives 2(N-1) * count at the root.
+ * CR_ERR_UNSUPPORTED for a naive reduce-scatter or all-gather. */
+typedef enum {
+  CR_COLL_REDUCE_SCATTER = 0,
+  CR_COLL_ALL_GATHER = 1,
+  CR_COLL_ALL_REDUCE = 2
+} cr_collective;
+typedef enum { CR_SCHED_RING = 0, CR_SCHED_NAIVE = 1 } cr_schedule;
+
+cr_status cr_comm_elems(cr_collective coll, cr_schedule sched, int nranks,
+                        size_t count, int rank, uint64_t* sent,
+                        uint64_t* recv, int* steps);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CR_H */

@@ -1,0 +1,81 @@
+/*
+ * adamw_fsdp.c -- oracle for the sharded AdamW update and the FSDP step
+ * (reduce-scatter -> owner AdamW -> bf16 cast -> all-gather).  Test
+ * infrastructure only (see oracle.h).
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Scalar AdamW with decoupled weight decay; see oracle.h for the rule and
+ * the reading of the pages it follows.  One element at a time, every
+ * operation an individually rounded fp32 operation. */
+void orc_adamw(size_t n, float* p, float* m, float* v, const float* g,
+               const orc_adamw_cfg* c) {
+  const float lr = (float)c->lr;
+  const float eps = (float)c->eps;
+  const float b1 = (float)c->beta1;
+  const float b2 = (float)c->beta2;
+  const float one_minus_b1 = (float)(1.0 - c->beta1);
+  const float one_minus_b2 = (float)(1.0 - c->beta2);
+  const float decay = (float)(1.0 - c->lr * c->weight_decay);
+  const float bc1 = (float)(1.0 - pow(c->beta1, (double)c->step));
+  const float bc2 = (float)(1.0 - pow(c->beta2, (double)c->step));
+  for (size_t i = 0; i < n; ++i) {
+    float gi = g[i];
+    float pi = p[i] * decay;
+    float mi = b1 * m[i] + one_minus_b1 * gi;
+    float vi = b2 * v[i] + one_minus_b2 * (gi * gi);
+    float mh = mi / bc1;
+    float vh = vi / bc2;
+    float denom = sqrtf(vh) + eps;
+    pi = pi - lr * (mh / denom);
+    p[i] = pi;
+    m[i] = mi;
+    v[i] = vi;
+  }
+}
+
+/* FSDP step in the order the pages give for one flat unit:
+ * backward post-hook reduce-scatter (fp32 reduce dtype, averaged), the
+ * optimizer step on the local shard only, then the all-gather that rebuilds
+ * the full bf16 parameter buffer on every rank ([DT] section 4, FSDP1
+ * "unit1 lifecycle"; [AIG] 6.3.2 and 6.3.4). */
+int orc_fsdp_step(int n, size_t count, const uint16_t* const* grads,
+                  float* const* master, float* const* m, float* const* v,
+                  const orc_adamw_cfg* cfg, uint16_t* const* params) {
+  if (n < 1 || n > ORC_MAX_RANKS) return ORC_EINVAL;
+  size_t L = orc_chunk_len(count, n);
+  float* gshard[ORC_MAX_RANKS];
+  uint16_t* pshard[ORC_MAX_RANKS];
+  for (int r = 0; r < n; ++r) {
+    gshard[r] = (float*)malloc((L ? L : 1) * sizeof(float));
+    pshard[r] = (uint16_t*)malloc((L ? L : 1) * sizeof(uint16_t));
+    if (!gshard[r] || !pshard[r]) {
+      for (int q = 0; q <= r; ++q) { free(gshard[q]); free(pshard[q]); }
+      return ORC_ENOMEM;
+    }
+  }
+  /* 1. reduce-scatter: bf16 grads in, fp32 averaged shard out. */
+  int rc = orc_ring_reduce_scatter(n, count, ORC_BF16, ORC_AVG,
+                                   (const void* const*)grads,
+                                   (void* const*)gshard, ORC_F32, NULL, NULL,
+                                   NULL);
+  if (rc == ORC_OK) {
+    /* 2./3. each owner j updates its own shard and casts it to bf16. */
+    for (int j = 0; j < n; ++j) {
+      size_t lo, hi;
+      orc_chunk_bounds(count, n, j, &lo, &hi);
+      orc_adamw(hi - lo, master[j], m[j], v[j], gshard[j], cfg);
+      for (size_t k = 0; k < hi - lo; ++k)
+        pshard[j][k] = orc_f32_to_bf16(master[j][k]);
+    }
+    /* 4. all-gather of the bf16 parameter shards. */
+    rc = orc_ring_all_gather(n, count, ORC_BF16, (const void* const*)pshard,
+                             (void* const*)params, NULL, NULL);
+  }
+  for (int r = 0; r < n; ++r) { free(gshard[r]); free(pshard[r]); }
+  return rc;
+}

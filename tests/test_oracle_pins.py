@@ -1,0 +1,510 @@
+"""Pins of the CPU oracle to facts fixed outside the oracle itself.
+
+Each test checks the oracle against the pages' worked examples (fixtures in
+tests/golden, each with its source), closed forms, exact arithmetic, brute
+force on tiny inputs, or an independent library routine.  A plausible slip in
+the oracle -- a wrong ring direction, a dropped contribution, an off-by-one
+chunk bound, a transposed operand in AdamW -- fails at least one of them.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle as O
+from fsdp_emulated_ranks_gb300 import inputs as I
+
+pytestmark = pytest.mark.filterwarnings("ignore::DeprecationWarning")
+
+
+def load(golden_dir, name):
+    with open(os.path.join(golden_dir, name)) as f:
+        return json.load(f)
+
+
+def bitmask_buffers(n, count_per_chunk=1):
+    """x_{j,i} = 1 << (n*j + i) as int32: every partial sum names its
+    contributors exactly (n*n <= 31 bits)."""
+    bufs = []
+    for i in range(n):
+        b = np.zeros(n * count_per_chunk, np.int32)
+        for j in range(n):
+            b[j * count_per_chunk:(j + 1) * count_per_chunk] = 1 << (n * j + i)
+        bufs.append(b)
+    return bufs
+
+
+def mask_of(contribs, n):
+    return sum(1 << (n * j + i) for j, i in contribs)
+
+
+# ---- a1: chunking ------------------------------------------------------------
+
+def test_uneven_shards_match_pages(golden_dir):
+    g = load(golden_dir, "uneven_shards.json")
+    for case in g["cases"]:
+        got = [list(O.chunk_bounds(case["dim0"], case["world_size"], j))
+               for j in range(case["world_size"])]
+        assert got == case["rows"], case
+
+
+def test_flat_parameter_example(golden_dir):
+    g = load(golden_dir, "flat_parameter_example.json")
+    n = g["world_size"]
+    total = g["total_numel"]
+    assert [list(O.chunk_bounds(total, n, j)) for j in range(n)] == g["shards"]
+    # Contiguous, unpadded offsets in visit order: the planner visits from the
+    # last index, so hand it the parameters reversed to get registration order.
+    numels = [p["numel"] for p in g["params"]][::-1]
+    plan = O.bucket_plan(numels, 4, 1 << 30)
+    assert plan.nbuckets == 1
+    offs = plan.tensor_offset[::-1]
+    for p, off in zip(g["params"], offs):
+        assert [int(off), int(off) + p["numel"]] == p["range"]
+    # The shard boundary splits the named parameter.
+    split = [p for p in g["params"] if p["range"][0] < g["shards"][0][1] < p["range"][1]]
+    assert [p["name"] for p in split] == [g["split_param"]]
+
+
+@pytest.mark.parametrize("count", [0, 1, 7, 8, 13, 64, 1000])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 64])
+def test_chunks_partition_buffer(count, n):
+    bounds = [O.chunk_bounds(count, n, j) for j in range(n)]
+    assert bounds[0][0] == 0 and bounds[-1][1] == count
+    for (a, b), (c, d) in zip(bounds, bounds[1:]):
+        assert b == c and a <= b
+    assert all(b - a <= math.ceil(count / n) for a, b in bounds)
+
+
+# ---- a2: ring reduce-scatter schedule ---------------------------------------
+
+def test_ring_reduce_scatter_trace_n4(golden_dir):
+    g = load(golden_dir, "ring_reduce_scatter_n4.json")
+    n = g["n"]
+    shards, tr, (chunks, values) = O.ring_reduce_scatter(
+        bitmask_buffers(n), "i32", "sum", trace=True)
+    for s, step in enumerate(g["steps"]):
+        assert list(chunks[s]) == step["sends"], f"step {s + 1}"
+        for rank, contribs in step["held_after"].items():
+            assert int(values[s][int(rank)]) == mask_of(contribs, n), (s, rank)
+    final = g["steps"][-1]["held_after"]
+    for j in range(n):
+        assert int(shards[j][0]) == mask_of(final[str(j)], n)
+    assert tr.steps == n - 1
+
+
+def test_ring_reduce_scatter_two_rank_example():
+    # FSDP1 unit1 with world_size 2: y_0 = x_00 + x_01, y_1 = x_10 + x_11.
+    shards, _ = O.ring_reduce_scatter(bitmask_buffers(2, 7), "i32", "sum")
+    assert np.all(shards[0] == (1 << 0) + (1 << 1))
+    assert np.all(shards[1] == (1 << 2) + (1 << 3))
+
+
+def order_from_trace(golden):
+    """For each chunk j, the order in which ranks' contributions were added,
+    read from the page's final partials."""
+    final = golden["steps"][-1]["held_after"]
+    return {int(r): [i for _, i in contribs] for r, contribs in final.items()}
+
+
+def test_fold_order_matches_page_schedule(golden_dir):
+    """Random fp32 inputs: the oracle's shard j must equal the left fold in
+    exactly the page's order of contributions (fp32 addition is not
+    associative, so any other order differs somewhere)."""
+    g = load(golden_dir, "ring_reduce_scatter_n4.json")
+    order = order_from_trace(g)
+    n, count = 4, 4 * 257
+    bufs = I.host_rank_buffers(n, count, "f32", std=1.0, seed0=11)
+    sim, _ = O.ring_reduce_scatter(bufs, "f32", "sum")
+    L = count // n
+    for j in range(n):
+        seg = [b[j * L:(j + 1) * L] for b in bufs]
+        acc = seg[order[j][0]].copy()
+        for i in order[j][1:]:
+            acc = (acc + seg[i]).astype(np.float32)
+        assert np.array_equal(sim[j].view(np.uint32), acc.view(np.uint32)), j
+    # And a different association does give different bits somewhere.
+    naive = [(seg := [b[j * L:(j + 1) * L] for b in bufs])[0] + seg[1] + seg[2] + seg[3]
+             for j in range(n)]
+    assert any(not np.array_equal(naive[j], sim[j]) for j in range(n))
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 8, 13, 16])
+@pytest.mark.parametrize("count", [1, 5, 64, 999])
+@pytest.mark.parametrize("dt", ["f32", "bf16", "i32"])
+def test_simulation_equals_closed_form_fold(n, count, dt):
+    bufs = I.host_rank_buffers(n, count, dt, seed0=100 + n)
+    for op, out in [("sum", dt)] + ([("avg", dt), ("avg", "f32")] if dt != "i32" else []):
+        sim, _ = O.ring_reduce_scatter(bufs, dt, op, out)
+        fold = O.fold_reduce_scatter(bufs, dt, op, out)
+        for a, b in zip(sim, fold):
+            assert a.tobytes() == b.tobytes(), (op, out)
+
+
+@pytest.mark.parametrize("n", [2, 3, 4, 7, 8, 16, 64])
+def test_ring_equals_naive_on_integer_values(n):
+    """Integer-valued fp32 with |x| <= 2^10: every partial is exact, so the
+    ring must reduce to the textbook sum computed by the naive schedule."""
+    count = 3 * n + 5
+    bufs = I.integer_valued_f32(n, count, seed=n)
+    ring, _ = O.ring_all_reduce(bufs, "f32", "sum")
+    naive, _ = O.naive_all_reduce(bufs, "f32", "sum")
+    exact = np.sum(np.stack(bufs).astype(np.float64), axis=0)
+    for r in range(n):
+        assert np.array_equal(ring[r], naive[r])
+        assert np.array_equal(ring[r].astype(np.float64), exact)
+
+
+@pytest.mark.parametrize("n", [2, 3, 4])
+@pytest.mark.parametrize("count", [1, 2, 5, 12])
+def test_brute_force_tiny(n, count):
+    """Exact rational sum, the recursive-summation error bound, and the one
+    association the ring fixes, enumerated by hand for N <= 4."""
+    rng = np.random.default_rng(1000 * n + count)
+    bufs = [(rng.standard_normal(count) * rng.choice([1e-3, 1.0, 1e3], count))
+            .astype(np.float32) for _ in range(n)]
+    shards, _ = O.ring_reduce_scatter(bufs, "f32", "sum")
+    L = math.ceil(count / n)
+    u = 2.0 ** -24
+    f = np.float32
+    for e in range(count):
+        j = e // L
+        got = float(shards[j][e - j * L])
+        xs = [bufs[i][e] for i in range(n)]
+        exact = sum(Fraction(float(x)) for x in xs)
+        bound = (n - 1) * u * sum(abs(float(x)) for x in xs)
+        assert abs(Fraction(got) - exact) <= Fraction(bound) * (1 + 1e-12)
+        x = lambda k: xs[(j + k) % n]
+        if n == 2:
+            want = f(x(1) + x(0))
+        elif n == 3:
+            want = f(f(x(1) + x(2)) + x(0))
+        else:
+            want = f(f(f(x(1) + x(2)) + x(3)) + x(0))
+        assert np.float32(got).tobytes() == np.float32(want).tobytes()
+
+
+# ---- a3: average and cast -----------------------------------------------------
+
+@pytest.mark.parametrize("n", [2, 3, 5, 8])
+def test_avg_is_sum_divided_once(n):
+    bufs = I.host_rank_buffers(n, 40 * n, "f32", seed0=5)
+    s, _ = O.ring_reduce_scatter(bufs, "f32", "sum")
+    a, _ = O.ring_reduce_scatter(bufs, "f32", "avg")
+    for x, y in zip(s, a):
+        want = np.array([np.float32(v) / np.float32(n) for v in x], np.float32)
+        assert np.array_equal(want, y)
+        if n & (n - 1) == 0:   # power of two: exact scaling
+            assert np.array_equal(x * np.float32(1.0 / n), y)
+
+
+def test_bf16_rounding_matches_torch():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(3)
+    x = np.concatenate([
+        rng.standard_normal(100000).astype(np.float32) * 10.0 ** rng.integers(-30, 30, 100000),
+        np.array([0.0, -0.0, 1.0, 1.00390625, 1.01171875, 3.3895313892515355e38,
+                  np.finfo(np.float32).max, np.inf, -np.inf, 1e-40, -1e-45,
+                  np.finfo(np.float32).tiny], np.float32)])
+    # Exact ties: 1 + 2^-8 (round down to even) and 1 + 3*2^-8 (round up).
+    got = O.f32_to_bf16(x)
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, want)
+    assert O.f32_to_bf16(np.array([1.00390625], np.float32))[0] == 0x3F80
+    assert O.f32_to_bf16(np.array([1.01171875], np.float32))[0] == 0x3F82
+    nan = O.f32_to_bf16(np.array([np.nan], np.float32))[0]
+    assert (nan & 0x7F80) == 0x7F80 and (nan & 0x7F) != 0
+
+
+def test_bf16_avg_output_rounds_once():
+    n = 8
+    bufs = I.host_rank_buffers(n, 64 * n, "bf16", std=0.02, seed0=0)
+    f32, _ = O.ring_reduce_scatter(bufs, "bf16", "avg", "f32")
+    b16, _ = O.ring_reduce_scatter(bufs, "bf16", "avg", "bf16")
+    for a, b in zip(f32, b16):
+        assert np.array_equal(O.f32_to_bf16(a), b)
+
+
+# ---- a4 / a5: all-gather and all-reduce -------------------------------------
+
+def test_ring_all_gather_trace_n4(golden_dir):
+    g = load(golden_dir, "ring_all_gather_n4.json")
+    n = g["n"]
+    shards = [np.full(3, 10 + j, np.int32) for j in range(n)]
+    bufs, tr, arrival = O.ring_all_gather(shards, 3 * n, "i32", trace=True)
+    contents = [list(c) for c in g["initial"]]
+    for s, step in enumerate(g["steps"]):
+        for r in range(n):
+            contents[r].append(int(arrival[s][r]))
+            # what r received at step s is what r-1 sent
+            assert int(arrival[s][r]) == step["sends"][(r - 1) % n]
+        assert contents == step["contents_after"], f"step {s + 1}"
+    for r in range(n):
+        assert list(bufs[r][::3] - 10) == g["final_by_shard_index"][r]
+    assert tr.steps == n - 1
+
+
+@pytest.mark.parametrize("n,count", [(1, 9), (2, 9), (4, 1 << 12), (5, 23), (8, 8 * 37 + 3), (64, 200)])
+@pytest.mark.parametrize("dt,op,out", [("f32", "sum", "f32"), ("bf16", "avg", "bf16"),
+                                       ("bf16", "avg", "f32"), ("i32", "sum", "i32")])
+def test_all_reduce_is_all_gather_of_reduce_scatter(n, count, dt, op, out):
+    bufs = I.host_rank_buffers(n, count, dt, seed0=n + count)
+    ar, _ = O.ring_all_reduce(bufs, dt, op, out)
+    rs, _ = O.ring_reduce_scatter(bufs, dt, op, out)
+    ag, _ = O.ring_all_gather(rs, count, out)
+    for r in range(n):
+        assert ar[r].tobytes() == ag[r].tobytes()
+        assert ar[r].tobytes() == np.concatenate(rs).tobytes()
+
+
+# ---- a11: traffic counters and the cost model -------------------------------
+
+@pytest.mark.parametrize("n", [2, 4, 8, 16, 64])
+def test_traffic_ring_vs_naive(n):
+    count = 64 * n
+    bufs = I.integer_valued_f32(n, count, seed=1)
+    _, ring = O.ring_all_reduce(bufs, "f32", "sum")
+    _, naive = O.naive_all_reduce(bufs, "f32", "sum")
+    # ring: every rank sends 2(N-1)/N of the buffer, over 2(N-1) steps
+    assert ring.sent == [2 * (n - 1) * count // n] * n
+    assert ring.recv == ring.sent
+    assert ring.steps == 2 * (n - 1)
+    # naive: the root receives and sends (N-1) full buffers
+    root = naive.sent[0] + naive.recv[0]
+    assert root == 2 * (n - 1) * count
+    assert all(naive.sent[r] == count and naive.recv[r] == count for r in range(1, n))
+    # both move the same total over all links
+    assert sum(ring.sent) == sum(naive.sent) == 2 * (n - 1) * count
+    assert root == n * ring.sent[0]
+
+
+def test_traffic_uneven_chunks():
+    n, count = 4, 10     # chunks of 3, 3, 3, 1
+    bufs = I.integer_valued_f32(n, count, seed=2)
+    _, rs = O.ring_reduce_scatter(bufs, "f32", "sum")
+    lens = [b - a for a, b in (O.chunk_bounds(count, n, j) for j in range(n))]
+    # rank r sends every chunk but its own in reduce-scatter
+    assert rs.sent == [count - lens[r] for r in range(n)]
+
+
+def test_cost_figures(golden_dir):
+    g = load(golden_dir, "cost_figures.json")
+    ab = g["alpha_beta_64MiB_8ranks"]
+    n, S = ab["n"], ab["bytes"]
+    for key in ("intra_node", "inter_node"):
+        c = ab[key]
+        t = O.alpha_beta_ring_allreduce(n, S, c["alpha_s"], c["bw_Bps"])
+        alpha_term = O.alpha_beta_ring_allreduce(n, 0.0, c["alpha_s"], c["bw_Bps"])
+        assert alpha_term == pytest.approx(c["alpha_term_s"], rel=1e-9)
+        assert t - alpha_term == pytest.approx(c["beta_term_s"], rel=0.01)
+        assert t == pytest.approx(c["total_s"], rel=0.01)
+    rv = g["ring_vs_naive_8ranks"]
+    n = rv["n"]
+    count = 8 * 1024
+    bufs = I.integer_valued_f32(n, count, seed=3)
+    _, ring = O.ring_all_reduce(bufs, "f32", "sum")
+    _, naive = O.naive_all_reduce(bufs, "f32", "sum")
+    assert ring.sent[0] / count == rv["ring_per_rank_in_S"]
+    assert (naive.sent[0] + naive.recv[0]) / count == rv["naive_in_S"]
+    d7 = g["ddp_7b_8xh100"]
+    per_card = 2 * (d7["n"] - 1) / d7["n"] * d7["grad_bytes"]
+    assert per_card == pytest.approx(d7["ring_per_card_bytes"], rel=1e-12)
+    assert per_card / d7["bw_Bps"] == pytest.approx(d7["t_comm_s"], rel=0.01)
+    d70 = g["ddp_70b_64gpus"]
+    per_card = 2 * (d70["n"] - 1) / d70["n"] * d70["grad_bytes"]
+    assert per_card == pytest.approx(d70["ring_per_card_bytes_approx"], rel=0.01)
+    assert per_card / d70["bw_Bps"] == pytest.approx(d70["t_comm_s_approx"], rel=0.01)
+    tp = g["tp_allreduce_per_call"]
+    n, S = tp["n"], tp["bytes"]
+    bufs = I.integer_valued_f32(n, S // 4 // 1024, seed=4)
+    _, ring = O.ring_all_reduce(bufs, "f32", "sum")
+    assert ring.sent[0] * 4 * 1024 == tp["ring_per_card_bytes"]
+
+
+# ---- a6 / a7: buckets -----------------------------------------------------------
+
+CAP = 25 * 1024 * 1024
+
+
+def check_plan_rules(numels, esize, cap, plan):
+    t = len(numels)
+    tb, to, bn = plan.tensor_bucket, plan.tensor_offset, plan.bucket_numel
+    # visit order: from the last tensor to the first, buckets in that order
+    order = list(range(t - 1, -1, -1))
+    buckets_seen = [int(tb[i]) for i in order]
+    assert buckets_seen == sorted(buckets_seen)
+    assert (buckets_seen[0] if t else 0) == 0
+    for b in range(plan.nbuckets):
+        members = [i for i in order if tb[i] == b]
+        assert members, "empty bucket"
+        # contiguous, unpadded offsets in visit order
+        off = 0
+        for i in members:
+            assert int(to[i]) == off
+            off += int(numels[i])
+        assert int(bn[b]) == off
+        nbytes = off * esize
+        assert nbytes <= cap or len(members) == 1
+        # greedy: the next bucket's first tensor did not fit here
+        if b + 1 < plan.nbuckets:
+            first_next = [i for i in order if tb[i] == b + 1][0]
+            assert nbytes + int(numels[first_next]) * esize > cap
+            assert nbytes > 0
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_bucket_plan_rules_random(seed):
+    rng = np.random.default_rng(seed)
+    numels = rng.integers(0, 5000, size=rng.integers(0, 60)).astype(np.uint64)
+    for cap in (1, 64, 4000, 10000, 1 << 20):
+        plan = O.bucket_plan(numels, 2, cap)
+        check_plan_rules(numels, 2, cap, plan)
+
+
+def test_bucket_plan_workload_sizes():
+    numels = I.bucket_numels()
+    plan = O.bucket_plan(numels, 2, CAP)
+    check_plan_rules(numels, 2, CAP, plan)
+    assert int(plan.bucket_numel.sum()) == int(numels.sum())
+    # oversize tensors (> 12.5 Mi bf16 elements) sit alone
+    for t in np.nonzero(numels * 2 > CAP)[0]:
+        assert np.sum(plan.tensor_bucket == plan.tensor_bucket[t]) == 1
+
+
+def test_bucket_pack_unpack_identity():
+    n = 3
+    numels = np.array([5, 0, 17, 1, 33, 8], np.uint64)
+    plan = O.bucket_plan(numels, 2, 40)
+    rng = np.random.default_rng(0)
+    tensors = [[rng.integers(0, 65535, int(k)).astype(np.uint16) for k in numels]
+               for _ in range(n)]
+    buckets = O.bucket_pack(plan, tensors)
+    for r in range(n):
+        for t, k in enumerate(numels):
+            b, off = plan.tensor_bucket[t], int(plan.tensor_offset[t])
+            assert np.array_equal(buckets[r][b][off:off + int(k)], tensors[r][t])
+    back = O.bucket_unpack(plan, buckets, np.uint16)
+    for r in range(n):
+        for t in range(len(numels)):
+            assert np.array_equal(back[r][t], tensors[r][t])
+
+
+def test_bucketed_all_reduce_equals_per_tensor_average_on_integers():
+    """On integer-valued data (exact sums) and N = 4 (exact /4), the bucket
+    pipeline equals the plain per-tensor mean."""
+    n = 4
+    numels = np.array([7, 100, 3, 64, 1, 250], np.uint64)
+    plan = O.bucket_plan(numels, 4, 400)
+    rng = np.random.default_rng(1)
+    tensors = [[rng.integers(-512, 512, int(k)).astype(np.float32) for k in numels]
+               for _ in range(n)]
+    out = O.bucketed_all_reduce(plan, tensors, "f32", "avg")
+    for t in range(len(numels)):
+        want = np.mean(np.stack([tensors[r][t] for r in range(n)]).astype(np.float64), axis=0)
+        for r in range(n):
+            assert np.array_equal(out[r][t].astype(np.float64), want)
+
+
+# ---- a9: AdamW ----------------------------------------------------------------
+
+def test_adamw_step1_closed_form():
+    """m = v = 0, t = 1: m = (1-b1) g, v = (1-b2) g^2, the bias corrections
+    cancel, and p1 = p0 (1 - lr wd) - lr g / (|g| + eps)."""
+    cfg = O.AdamWConfig()
+    rng = np.random.default_rng(0)
+    k = 20000
+    g = (rng.standard_normal(k) * 10.0 ** rng.integers(-6, 1, k)).astype(np.float32)
+    g[:3] = [0.0, 1e-9, -1e-9]
+    p0 = (rng.standard_normal(k) * 0.02).astype(np.float32)
+    p, m, v = p0.copy(), np.zeros(k, np.float32), np.zeros(k, np.float32)
+    O.adamw(p, m, v, g, cfg)
+    gd, pd = g.astype(np.float64), p0.astype(np.float64)
+    want_p = pd * (1 - cfg.lr * cfg.weight_decay) - cfg.lr * gd / (np.abs(gd) + cfg.eps)
+    u = 2.0 ** -24
+    assert np.all(np.abs(p - want_p) <= 8 * u * (np.abs(pd) + cfg.lr))
+    assert np.all(np.abs(m - 0.1 * gd) <= 4 * u * np.abs(gd))
+    assert np.all(np.abs(v - 0.001 * gd * gd) <= 6 * u * gd * gd + 1e-45)
+    # g = 0: pure decoupled decay
+    assert p[0] == np.float32(p0[0] * np.float32(1 - cfg.lr * cfg.weight_decay))
+
+
+def test_adamw_matches_torch_over_steps():
+    """Against torch.optim.AdamW in float64, several steps with nonzero
+    state; torch orders the operations differently, so agreement is to fp32
+    rounding, not bitwise."""
+    torch = pytest.importorskip("torch")
+    cfgs = [O.AdamWConfig(), O.AdamWConfig(lr=3e-4, beta1=0.9, beta2=0.95, weight_decay=0.1)]
+    for cfg in cfgs:
+        rng = np.random.default_rng(7)
+        k = 4096
+        p = (rng.standard_normal(k) * 0.02).astype(np.float32)
+        m = np.zeros(k, np.float32)
+        v = np.zeros(k, np.float32)
+        tp = torch.nn.Parameter(torch.from_numpy(p.astype(np.float64)))
+        opt = torch.optim.AdamW([tp], lr=cfg.lr, betas=(cfg.beta1, cfg.beta2),
+                                eps=cfg.eps, weight_decay=cfg.weight_decay)
+        for step in range(1, 6):
+            g = (rng.standard_normal(k) * 1e-3).astype(np.float32)
+            cfg.step = step
+            O.adamw(p, m, v, g, cfg)
+            tp.grad = torch.from_numpy(g.astype(np.float64))
+            opt.step()
+            ref = tp.detach().numpy()
+            st = opt.state[tp]
+            assert np.max(np.abs(p - ref)) <= 1e-6 * np.max(np.abs(ref))
+            assert np.max(np.abs(m - st["exp_avg"].numpy())) <= 1e-5 * np.max(np.abs(m))
+            assert np.max(np.abs(v - st["exp_avg_sq"].numpy())) <= 1e-5 * np.max(np.abs(v))
+
+
+# ---- a8..a10: FSDP step -----------------------------------------------------------
+
+@pytest.mark.parametrize("n,count", [(2, 14), (4, 4 * 100), (8, 8 * 64 + 5), (3, 2)])
+def test_fsdp_step_equals_unsharded_training_step(n, count):
+    """The check the pages state for their FSDP simulation: the sharded
+    update, re-gathered, equals one unsharded step on the full flat buffer
+    (here bit for bit: AdamW is elementwise, so sharding changes no
+    operation)."""
+    cfg = O.AdamWConfig()
+    grads = I.host_rank_buffers(n, count, "bf16", std=1e-3, seed0=1000)
+    master_full = I.np_normal_f32(count, 0.02, 2000)
+    shards = [slice(*O.chunk_bounds(count, n, j)) for j in range(n)]
+    master = [master_full[s].copy() for s in shards]
+    m = [np.zeros(s.stop - s.start, np.float32) for s in shards]
+    v = [np.zeros(s.stop - s.start, np.float32) for s in shards]
+    params = O.fsdp_step(grads, master, m, v, cfg)
+    # unsharded: all-reduce AVG into fp32, AdamW on the whole buffer, cast
+    g_full, _ = O.ring_all_reduce(grads, "bf16", "avg", "f32")
+    p_full = master_full.copy()
+    m_full = np.zeros(count, np.float32)
+    v_full = np.zeros(count, np.float32)
+    O.adamw(p_full, m_full, v_full, g_full[0], cfg)
+    assert np.concatenate(master).tobytes() == p_full.tobytes()
+    assert np.concatenate(m).tobytes() == m_full.tobytes()
+    assert np.concatenate(v).tobytes() == v_full.tobytes()
+    want = O.f32_to_bf16(p_full)
+    for r in range(n):
+        assert params[r].tobytes() == want.tobytes()
+
+
+def test_fsdp_step_gradient_is_mean_of_ranks():
+    """With integer-valued bf16 grads the averaged fp32 gradient is exact;
+    step 1 from m = v = 0 then moves each master weight by
+    -lr*sign(g) (|g| >> eps) after the decay."""
+    n, count = 4, 64
+    cfg = O.AdamWConfig()
+    rng = np.random.default_rng(5)
+    ints = [rng.integers(1, 20, count).astype(np.float32) * rng.choice([-1, 1], count)
+            for _ in range(n)]
+    grads = [O.f32_to_bf16(x) for x in ints]
+    mean = np.mean(np.stack(ints).astype(np.float64), axis=0)
+    master = [np.full(count // n, 0.5, np.float32) for _ in range(n)]
+    m = [np.zeros(count // n, np.float32) for _ in range(n)]
+    v = [np.zeros(count // n, np.float32) for _ in range(n)]
+    O.fsdp_step(grads, master, m, v, cfg)
+    got_m = np.concatenate(m).astype(np.float64)
+    assert np.allclose(got_m, 0.1 * mean, rtol=1e-6, atol=0)
+    want = 0.5 * (1 - cfg.lr * cfg.weight_decay) - cfg.lr * np.sign(mean)
+    assert np.allclose(np.concatenate(master), want, rtol=0, atol=1e-7)
