@@ -1,0 +1,261 @@
+"""ctypes binding of libcr (include/cr.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does
+nothing but turn Python arguments (torch tensors or integer device
+pointers, dtype names, a stream) into the C call and raise on a non-OK
+status.  All computation happens in libcr's CUDA kernels; there is no
+fallback: if libcr.so is missing, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Sequence
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "_build", "libcr.so")
+MAX_RANKS = 64
+
+F32, BF16, I32 = 0, 1, 2
+SUM, AVG = 0, 1
+COLL_REDUCE_SCATTER, COLL_ALL_GATHER, COLL_ALL_REDUCE = 0, 1, 2
+SCHED_RING, SCHED_NAIVE = 0, 1
+
+_DTYPES = {"f32": F32, "float32": F32, "bf16": BF16, "bfloat16": BF16,
+           "i32": I32, "int32": I32}
+_OPS = {"sum": SUM, "avg": AVG}
+STATUS = {0: "CR_OK", 1: "CR_ERR_INVALID_ARG", 2: "CR_ERR_UNSUPPORTED",
+          3: "CR_ERR_ALIGNMENT", 4: "CR_ERR_CUDA", 5: "CR_ERR_TIMEOUT"}
+
+# Every symbol include/cr.h declares.
+EXPORTS = ["cr_status_string", "cr_last_error", "cr_version", "cr_chunk_len",
+           "cr_shard_range", "cr_reduce_scatter", "cr_all_gather",
+           "cr_all_reduce", "cr_bucket_plan", "cr_bucket_plan_free",
+           "cr_bucket_pack", "cr_bucket_unpack", "cr_bucket_all_reduce",
+           "cr_fsdp_step", "cr_adamw_step", "cr_comm_elems"]
+
+_lib = None
+
+
+class CRError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        super().__init__(f"{where}: {STATUS.get(status, status)}: {detail}")
+        self.status = status
+
+
+class AdamWCfg(C.Structure):
+    _fields_ = [("lr", C.c_double), ("beta1", C.c_double),
+                ("beta2", C.c_double), ("eps", C.c_double),
+                ("weight_decay", C.c_double), ("step", C.c_int64)]
+
+
+class BucketPlanT(C.Structure):
+    _fields_ = [("ntensors", C.c_int), ("nbuckets", C.c_int),
+                ("elem_size", C.c_size_t), ("cap_bytes", C.c_size_t),
+                ("numels", C.POINTER(C.c_size_t)),
+                ("tensor_bucket", C.POINTER(C.c_int)),
+                ("tensor_offset", C.POINTER(C.c_size_t)),
+                ("bucket_numel", C.POINTER(C.c_size_t))]
+
+
+def lib() -> C.CDLL:
+    """Open libcr.so (built by fsdp_emulated_ranks_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"libcr.so not found at {LIB_PATH}; build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'`")
+    L = C.CDLL(LIB_PATH)
+    vp, sz, i = C.c_void_p, C.c_size_t, C.c_int
+    L.cr_status_string.restype = C.c_char_p
+    L.cr_status_string.argtypes = [i]
+    L.cr_last_error.restype = C.c_char_p
+    L.cr_last_error.argtypes = []
+    L.cr_version.restype = i
+    L.cr_chunk_len.restype = sz
+    L.cr_chunk_len.argtypes = [sz, i]
+    L.cr_shard_range.argtypes = [sz, i, i, C.POINTER(sz), C.POINTER(sz)]
+    L.cr_reduce_scatter.argtypes = [vp, i, sz, i, i, vp, i, vp]
+    L.cr_all_gather.argtypes = [vp, i, sz, i, vp, vp]
+    L.cr_all_reduce.argtypes = [vp, i, sz, i, i, vp, i, vp]
+    L.cr_bucket_plan.argtypes = [vp, i, sz, sz, C.POINTER(C.POINTER(BucketPlanT))]
+    L.cr_bucket_plan_free.restype = None
+    L.cr_bucket_plan_free.argtypes = [C.POINTER(BucketPlanT)]
+    L.cr_bucket_pack.argtypes = [C.POINTER(BucketPlanT), i, vp, vp, vp]
+    L.cr_bucket_unpack.argtypes = [C.POINTER(BucketPlanT), i, vp, vp, vp]
+    L.cr_bucket_all_reduce.argtypes = [C.POINTER(BucketPlanT), i, vp, i, i, vp]
+    L.cr_fsdp_step.argtypes = [vp, i, sz, vp, vp, vp, C.POINTER(AdamWCfg), vp, vp]
+    L.cr_adamw_step.argtypes = [sz, vp, vp, vp, vp, C.POINTER(AdamWCfg), vp, vp]
+    L.cr_comm_elems.argtypes = [i, i, i, sz, i, C.POINTER(C.c_uint64),
+                                C.POINTER(C.c_uint64), C.POINTER(i)]
+    for name in EXPORTS:
+        getattr(L, name).restype = getattr(L, name).restype or i
+    L.cr_status_string.restype = C.c_char_p
+    L.cr_last_error.restype = C.c_char_p
+    L.cr_chunk_len.restype = sz
+    L.cr_bucket_plan_free.restype = None
+    _lib = L
+    return L
+
+
+# ---- marshalling helpers --------------------------------------------------------
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _ptr_array(xs: Sequence) -> C.Array:
+    arr = (C.c_void_p * max(1, len(xs)))()
+    for k, x in enumerate(xs):
+        arr[k] = _ptr(x)
+    return arr
+
+
+def _dtype(d) -> int:
+    if isinstance(d, int):
+        return d
+    return _DTYPES[str(d).replace("torch.", "")]
+
+
+def _op(o) -> int:
+    return o if isinstance(o, int) else _OPS[o]
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise CRError(status, where, lib().cr_last_error().decode())
+
+
+# ---- entry points -----------------------------------------------------------------
+
+def cr_version() -> int:
+    return lib().cr_version()
+
+
+def cr_chunk_len(count: int, nranks: int) -> int:
+    return lib().cr_chunk_len(count, nranks)
+
+
+def cr_shard_range(count: int, nranks: int, j: int) -> tuple[int, int]:
+    lo, hi = C.c_size_t(), C.c_size_t()
+    _check(lib().cr_shard_range(count, nranks, j, C.byref(lo), C.byref(hi)),
+           "cr_shard_range")
+    return lo.value, hi.value
+
+
+def cr_reduce_scatter(bufs, count, in_dtype, op, out_shards, out_dtype,
+                      stream=None) -> None:
+    _check(lib().cr_reduce_scatter(_ptr_array(bufs), len(bufs), count,
+                                   _dtype(in_dtype), _op(op),
+                                   _ptr_array(out_shards), _dtype(out_dtype),
+                                   _stream(stream)), "cr_reduce_scatter")
+
+
+def cr_all_gather(shards, count, dtype, bufs, stream=None) -> None:
+    _check(lib().cr_all_gather(_ptr_array(shards), len(shards), count,
+                               _dtype(dtype), _ptr_array(bufs),
+                               _stream(stream)), "cr_all_gather")
+
+
+def cr_all_reduce(inbufs, count, in_dtype, op, outbufs, out_dtype,
+                  stream=None) -> None:
+    _check(lib().cr_all_reduce(_ptr_array(inbufs), len(inbufs), count,
+                               _dtype(in_dtype), _op(op), _ptr_array(outbufs),
+                               _dtype(out_dtype), _stream(stream)),
+           "cr_all_reduce")
+
+
+class BucketPlan:
+    """Owns a cr_bucket_plan_t; freed with cr_bucket_plan_free."""
+
+    def __init__(self, ptr):
+        self._ptr = ptr
+        p = ptr.contents
+        self.ntensors = p.ntensors
+        self.nbuckets = p.nbuckets
+        self.elem_size = p.elem_size
+        self.tensor_bucket = [p.tensor_bucket[t] for t in range(p.ntensors)]
+        self.tensor_offset = [p.tensor_offset[t] for t in range(p.ntensors)]
+        self.bucket_numel = [p.bucket_numel[b] for b in range(p.nbuckets)]
+        self.numels = [p.numels[t] for t in range(p.ntensors)]
+
+    @property
+    def ptr(self):
+        return self._ptr
+
+    def __del__(self):
+        if getattr(self, "_ptr", None) is not None and _lib is not None:
+            _lib.cr_bucket_plan_free(self._ptr)
+            self._ptr = None
+
+
+def cr_bucket_plan(numels: Sequence[int], elem_size: int, cap_bytes: int) -> BucketPlan:
+    arr = (C.c_size_t * max(1, len(numels)))(*[int(k) for k in numels])
+    out = C.POINTER(BucketPlanT)()
+    _check(lib().cr_bucket_plan(arr, len(numels), elem_size, cap_bytes,
+                                C.byref(out)), "cr_bucket_plan")
+    return BucketPlan(out)
+
+
+def cr_bucket_pack(plan: BucketPlan, nranks: int, tensors, buckets,
+                   stream=None) -> None:
+    _check(lib().cr_bucket_pack(plan.ptr, nranks, _ptr_array(tensors),
+                                _ptr_array(buckets), _stream(stream)),
+           "cr_bucket_pack")
+
+
+def cr_bucket_unpack(plan: BucketPlan, nranks: int, buckets, tensors,
+                     stream=None) -> None:
+    _check(lib().cr_bucket_unpack(plan.ptr, nranks, _ptr_array(buckets),
+                                  _ptr_array(tensors), _stream(stream)),
+           "cr_bucket_unpack")
+
+
+def cr_bucket_all_reduce(plan: BucketPlan, nranks: int, buckets, dtype, op,
+                         stream=None) -> None:
+    _check(lib().cr_bucket_all_reduce(plan.ptr, nranks, _ptr_array(buckets),
+                                      _dtype(dtype), _op(op), _stream(stream)),
+           "cr_bucket_all_reduce")
+
+
+def adamw_cfg(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01,
+              step=1) -> AdamWCfg:
+    return AdamWCfg(lr, beta1, beta2, eps, weight_decay, step)
+
+
+def cr_fsdp_step(grads, count, master, m, v, cfg: AdamWCfg, params,
+                 stream=None) -> None:
+    _check(lib().cr_fsdp_step(_ptr_array(grads), len(grads), count,
+                              _ptr_array(master), _ptr_array(m), _ptr_array(v),
+                              C.byref(cfg), _ptr_array(params), _stream(stream)),
+           "cr_fsdp_step")
+
+
+def cr_adamw_step(n, master, m, v, grad, cfg: AdamWCfg, param_bf16=None,
+                  stream=None) -> None:
+    _check(lib().cr_adamw_step(n, _ptr(master), _ptr(m), _ptr(v), _ptr(grad),
+                               C.byref(cfg), _ptr(param_bf16), _stream(stream)),
+           "cr_adamw_step")
+
+
+def cr_comm_elems(coll: int, sched: int, nranks: int, count: int,
+                  rank: int) -> tuple[int, int, int]:
+    sent, recv, steps = C.c_uint64(), C.c_uint64(), C.c_int()
+    _check(lib().cr_comm_elems(coll, sched, nranks, count, rank, C.byref(sent),
+                               C.byref(recv), C.byref(steps)), "cr_comm_elems")
+    return sent.value, recv.value, steps.value

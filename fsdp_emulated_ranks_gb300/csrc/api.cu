@@ -1,0 +1,525 @@
+// api.cu -- the extern "C" entry points of libcr (include/cr.h): argument
+// validation on the host, then one launch per call (bucket copies: one per
+// 1024 ranges; bucket all-reduce: one per bucket).
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <vector>
+
+#include "cr_internal.cuh"
+
+using namespace cr;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+cr_status fail(cr_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+cr_status ok() {
+  g_err[0] = '\0';
+  return CR_OK;
+}
+
+cr_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(CR_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e),
+              cudaGetErrorString(e));
+}
+
+size_t esize_of(cr_dtype d) {
+  switch (d) {
+    case CR_F32: return 4;
+    case CR_BF16: return 2;
+    case CR_I32: return 4;
+  }
+  return 0;
+}
+
+bool is_float(cr_dtype d) { return d == CR_F32 || d == CR_BF16; }
+
+// Byte interval of one buffer argument.
+struct Span {
+  uintptr_t a, b;  // [a, b)
+  int kind;        // 0 input, 1 output
+  int rank;
+};
+
+bool overlaps(const Span& x, const Span& y) {
+  return x.a < y.b && y.a < x.b && x.a < x.b && y.a < y.b;
+}
+
+uint64_t chunk_lo(uint64_t count, uint64_t L, int j) {
+  uint64_t a = L * (uint64_t)j;
+  return a < count ? a : count;
+}
+
+uint64_t chunk_size(uint64_t count, uint64_t L, int j) {
+  uint64_t a = chunk_lo(count, L, j);
+  uint64_t b = L * (uint64_t)(j + 1);
+  if (b > count) b = count;
+  return b - a;
+}
+
+bool aligned(const void* p, size_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+// Rejects ranks out of range and counts whose byte size overflows.
+cr_status check_common(int nranks, size_t count, const void* arr1,
+                       const void* arr2) {
+  if (nranks < 1 || nranks > CR_MAX_RANKS)
+    return fail(CR_ERR_INVALID_ARG, "nranks=%d outside [1, %d]", nranks, CR_MAX_RANKS);
+  if (!arr1 || !arr2) return fail(CR_ERR_INVALID_ARG, "pointer array is NULL");
+  if (count > (SIZE_MAX / 8)) return fail(CR_ERR_INVALID_ARG, "count=%zu too large", count);
+  return CR_OK;
+}
+
+cr_status check_pair(cr_dtype in, cr_op op, cr_dtype out) {
+  if (esize_of(in) == 0 || esize_of(out) == 0)
+    return fail(CR_ERR_INVALID_ARG, "unknown dtype (%d, %d)", (int)in, (int)out);
+  if (op != CR_SUM && op != CR_AVG) return fail(CR_ERR_INVALID_ARG, "unknown op %d", (int)op);
+  if (op == CR_AVG && !is_float(in))
+    return fail(CR_ERR_UNSUPPORTED, "AVG needs a floating-point dtype");
+  const bool supported = (in == CR_F32 && out == CR_F32) || (in == CR_BF16 && out == CR_BF16) ||
+                         (in == CR_BF16 && out == CR_F32) || (in == CR_I32 && out == CR_I32);
+  if (!supported)
+    return fail(CR_ERR_UNSUPPORTED, "dtype pair (%d -> %d) not supported", (int)in, (int)out);
+  return CR_OK;
+}
+
+// Every buffer: non-NULL if non-empty and aligned to its element size.
+cr_status check_buf(const void* p, uint64_t nelem, size_t es, const char* what, int r) {
+  if (nelem == 0) return CR_OK;
+  if (!p) return fail(CR_ERR_INVALID_ARG, "%s[%d] is NULL", what, r);
+  if (!aligned(p, es))
+    return fail(CR_ERR_ALIGNMENT, "%s[%d]=%p not aligned to %zu bytes", what, r, p, es);
+  return CR_OK;
+}
+
+// No output may overlap another buffer, except the pairs allow(i, o) marks.
+template <typename Allow>
+cr_status check_overlaps(const std::vector<Span>& spans, Allow allow) {
+  for (size_t x = 0; x < spans.size(); ++x) {
+    if (spans[x].kind != 1) continue;
+    for (size_t y = 0; y < spans.size(); ++y) {
+      if (x == y || !overlaps(spans[x], spans[y])) continue;
+      if (spans[y].kind == 0 && allow(spans[y], spans[x])) continue;
+      return fail(CR_ERR_INVALID_ARG, "%s %d overlaps %s %d",
+                  "output", spans[x].rank, spans[y].kind ? "output" : "input",
+                  spans[y].rank);
+    }
+  }
+  return CR_OK;
+}
+
+Span span_of(const void* p, uint64_t bytes, int kind, int rank) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return Span{a, a + bytes, kind, rank};
+}
+
+float exact_inv_n(int n) {
+  return (n & (n - 1)) == 0 ? 1.0f / (float)n : 0.0f;
+}
+
+AdamScalars adam_scalars(const cr_adamw_cfg& c) {
+  AdamScalars s;
+  s.lr = (float)c.lr;
+  s.eps = (float)c.eps;
+  s.b1 = (float)c.beta1;
+  s.b2 = (float)c.beta2;
+  s.omb1 = (float)(1.0 - c.beta1);
+  s.omb2 = (float)(1.0 - c.beta2);
+  s.decay = (float)(1.0 - c.lr * c.weight_decay);
+  s.bc1 = (float)(1.0 - pow(c.beta1, (double)c.step));
+  s.bc2 = (float)(1.0 - pow(c.beta2, (double)c.step));
+  return s;
+}
+
+cr_status check_adam_cfg(const cr_adamw_cfg* cfg) {
+  if (!cfg) return fail(CR_ERR_INVALID_ARG, "cfg is NULL");
+  if (cfg->step < 1) return fail(CR_ERR_INVALID_ARG, "cfg->step=%lld < 1", (long long)cfg->step);
+  if (!(cfg->beta1 >= 0.0 && cfg->beta1 < 1.0) || !(cfg->beta2 >= 0.0 && cfg->beta2 < 1.0))
+    return fail(CR_ERR_INVALID_ARG, "betas must lie in [0, 1)");
+  if (!(cfg->eps >= 0.0) || !(cfg->lr >= 0.0) || !(cfg->weight_decay >= 0.0))
+    return fail(CR_ERR_INVALID_ARG, "lr, eps and weight_decay must be >= 0");
+  return CR_OK;
+}
+
+cr_status all_reduce_impl(const void* const* in, int nranks, size_t count,
+                          cr_dtype in_dtype, cr_op op, void* const* out,
+                          cr_dtype out_dtype, cudaStream_t stream) {
+  cr_status st = check_common(nranks, count, in, out);
+  if (st) return st;
+  if ((st = check_pair(in_dtype, op, out_dtype))) return st;
+  const size_t is = esize_of(in_dtype), os = esize_of(out_dtype);
+  std::vector<Span> spans;
+  bool vec = true;
+  for (int r = 0; r < nranks; ++r) {
+    if ((st = check_buf(in[r], count, is, "in", r))) return st;
+    if ((st = check_buf(out[r], count, os, "out", r))) return st;
+    if (count) {
+      spans.push_back(span_of(in[r], count * is, 0, r));
+      spans.push_back(span_of(out[r], count * os, 1, r));
+      vec = vec && aligned(in[r], 16) && aligned(out[r], 16);
+    }
+  }
+  const bool same = in_dtype == out_dtype;
+  st = check_overlaps(spans, [&](const Span& i, const Span& o) {
+    return same && i.rank == o.rank && i.a == o.a && i.b == o.b;
+  });
+  if (st) return st;
+  if (count == 0) return ok();
+  FoldArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int r = 0; r < nranks; ++r) {
+    a.in[r] = in[r];
+    a.out[r] = out[r];
+  }
+  a.count = count;
+  a.L = (count + nranks - 1) / nranks;
+  a.n = nranks;
+  a.avg = op == CR_AVG;
+  a.inv_n = exact_inv_n(nranks);
+  cudaError_t e = launch_fold(in_dtype, out_dtype, kAR, a, vec, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "all_reduce launch");
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* cr_status_string(cr_status s) {
+  switch (s) {
+    case CR_OK: return "CR_OK";
+    case CR_ERR_INVALID_ARG: return "CR_ERR_INVALID_ARG";
+    case CR_ERR_UNSUPPORTED: return "CR_ERR_UNSUPPORTED";
+    case CR_ERR_ALIGNMENT: return "CR_ERR_ALIGNMENT";
+    case CR_ERR_CUDA: return "CR_ERR_CUDA";
+    case CR_ERR_TIMEOUT: return "CR_ERR_TIMEOUT";
+  }
+  return "CR_ERR_UNKNOWN";
+}
+
+const char* cr_last_error(void) { return g_err; }
+
+int cr_version(void) { return 100; }
+
+size_t cr_chunk_len(size_t count, int nranks) {
+  if (nranks < 1) return 0;
+  return count / (size_t)nranks + (count % (size_t)nranks ? 1 : 0);
+}
+
+cr_status cr_shard_range(size_t count, int nranks, int j, size_t* lo, size_t* hi) {
+  if (nranks < 1 || nranks > CR_MAX_RANKS)
+    return fail(CR_ERR_INVALID_ARG, "nranks=%d outside [1, %d]", nranks, CR_MAX_RANKS);
+  if (j < 0 || j >= nranks) return fail(CR_ERR_INVALID_ARG, "j=%d outside [0, %d)", j, nranks);
+  if (!lo || !hi) return fail(CR_ERR_INVALID_ARG, "lo/hi is NULL");
+  const uint64_t L = cr_chunk_len(count, nranks);
+  *lo = chunk_lo(count, L, j);
+  *hi = *lo + chunk_size(count, L, j);
+  return ok();
+}
+
+cr_status cr_reduce_scatter(const void* const* bufs, int nranks, size_t count,
+                            cr_dtype in_dtype, cr_op op, void* const* out_shards,
+                            cr_dtype out_dtype, cr_stream_t stream) {
+  cr_status st = check_common(nranks, count, bufs, out_shards);
+  if (st) return st;
+  if ((st = check_pair(in_dtype, op, out_dtype))) return st;
+  const size_t is = esize_of(in_dtype), os = esize_of(out_dtype);
+  const uint64_t L = cr_chunk_len(count, nranks);
+  std::vector<Span> spans;
+  bool vec = (L * is) % 16 == 0 && (L * os) % 16 == 0;
+  for (int r = 0; r < nranks; ++r) {
+    const uint64_t len = chunk_size(count, L, r);
+    if ((st = check_buf(bufs[r], count, is, "bufs", r))) return st;
+    if ((st = check_buf(out_shards[r], len, os, "out_shards", r))) return st;
+    if (count) {
+      spans.push_back(span_of(bufs[r], count * is, 0, r));
+      vec = vec && aligned(bufs[r], 16);
+    }
+    if (len) {
+      spans.push_back(span_of(out_shards[r], len * os, 1, r));
+      vec = vec && aligned(out_shards[r], 16);
+    }
+  }
+  const bool same = in_dtype == out_dtype;
+  st = check_overlaps(spans, [&](const Span& i, const Span& o) {
+    // In place: shard j is exactly chunk j of rank j's own buffer.
+    return same && i.rank == o.rank && o.a == i.a + L * (uint64_t)o.rank * is;
+  });
+  if (st) return st;
+  if (count == 0) return ok();
+  FoldArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int r = 0; r < nranks; ++r) {
+    a.in[r] = bufs[r];
+    a.out[r] = out_shards[r];
+  }
+  a.count = count;
+  a.L = L;
+  a.n = nranks;
+  a.avg = op == CR_AVG;
+  a.inv_n = exact_inv_n(nranks);
+  cudaError_t e = launch_fold(in_dtype, out_dtype, kRS, a, vec, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "reduce_scatter launch");
+  return ok();
+}
+
+cr_status cr_all_gather(const void* const* shards, int nranks, size_t count,
+                        cr_dtype dtype, void* const* bufs, cr_stream_t stream) {
+  cr_status st = check_common(nranks, count, shards, bufs);
+  if (st) return st;
+  const size_t es = esize_of(dtype);
+  if (!es) return fail(CR_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+  const uint64_t L = cr_chunk_len(count, nranks);
+  std::vector<Span> spans;
+  bool vec = (L * es) % 16 == 0;
+  uint64_t inplace = 0;
+  for (int r = 0; r < nranks; ++r) {
+    const uint64_t len = chunk_size(count, L, r);
+    if ((st = check_buf(shards[r], len, es, "shards", r))) return st;
+    if ((st = check_buf(bufs[r], count, es, "bufs", r))) return st;
+    if (len) {
+      spans.push_back(span_of(shards[r], len * es, 0, r));
+      vec = vec && aligned(shards[r], 16);
+      if (count && reinterpret_cast<uintptr_t>(shards[r]) ==
+                       reinterpret_cast<uintptr_t>(bufs[r]) + L * (uint64_t)r * es)
+        inplace |= 1ull << r;
+    }
+    if (count) {
+      spans.push_back(span_of(bufs[r], count * es, 1, r));
+      vec = vec && aligned(bufs[r], 16);
+    }
+  }
+  st = check_overlaps(spans, [&](const Span& i, const Span& o) {
+    return i.rank == o.rank && ((inplace >> i.rank) & 1ull);
+  });
+  if (st) return st;
+  if (count == 0) return ok();
+  GatherArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int r = 0; r < nranks; ++r) {
+    a.shards[r] = shards[r];
+    a.bufs[r] = bufs[r];
+  }
+  a.count = count;
+  a.L = L;
+  a.n = nranks;
+  a.inplace_mask = inplace;
+  cudaError_t e = launch_gather(es, a, vec, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "all_gather launch");
+  return ok();
+}
+
+cr_status cr_all_reduce(const void* const* in, int nranks, size_t count,
+                        cr_dtype in_dtype, cr_op op, void* const* out,
+                        cr_dtype out_dtype, cr_stream_t stream) {
+  return all_reduce_impl(in, nranks, count, in_dtype, op, out, out_dtype,
+                         (cudaStream_t)stream);
+}
+
+cr_status cr_fsdp_step(const void* const* grads_bf16, int nranks, size_t count,
+                       float* const* master, float* const* m, float* const* v,
+                       const cr_adamw_cfg* cfg, void* const* params_bf16,
+                       cr_stream_t stream) {
+  cr_status st = check_common(nranks, count, grads_bf16, params_bf16);
+  if (st) return st;
+  if (!master || !m || !v) return fail(CR_ERR_INVALID_ARG, "master/m/v array is NULL");
+  if ((st = check_adam_cfg(cfg))) return st;
+  const uint64_t L = cr_chunk_len(count, nranks);
+  std::vector<Span> spans;
+  bool vec = L % 8 == 0;
+  for (int r = 0; r < nranks; ++r) {
+    const uint64_t len = chunk_size(count, L, r);
+    if ((st = check_buf(grads_bf16[r], count, 2, "grads", r))) return st;
+    if ((st = check_buf(params_bf16[r], count, 2, "params", r))) return st;
+    if ((st = check_buf(master[r], len, 4, "master", r))) return st;
+    if ((st = check_buf(m[r], len, 4, "m", r))) return st;
+    if ((st = check_buf(v[r], len, 4, "v", r))) return st;
+    if (count) {
+      // Every buffer is written or must not be written, so each is an
+      // "output" span: no two may overlap.
+      spans.push_back(span_of(grads_bf16[r], count * 2, 1, r));
+      spans.push_back(span_of(params_bf16[r], count * 2, 1, r));
+      vec = vec && aligned(grads_bf16[r], 16) && aligned(params_bf16[r], 16);
+    }
+    if (len) {
+      spans.push_back(span_of(master[r], len * 4, 1, r));
+      spans.push_back(span_of(m[r], len * 4, 1, r));
+      spans.push_back(span_of(v[r], len * 4, 1, r));
+      vec = vec && aligned(master[r], 16) && aligned(m[r], 16) && aligned(v[r], 16);
+    }
+  }
+  st = check_overlaps(spans, [](const Span&, const Span&) { return false; });
+  if (st) return st;
+  if (count == 0) return ok();
+  FsdpArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int r = 0; r < nranks; ++r) {
+    a.grads[r] = grads_bf16[r];
+    a.params[r] = params_bf16[r];
+    a.master[r] = master[r];
+    a.m[r] = m[r];
+    a.v[r] = v[r];
+  }
+  a.count = count;
+  a.L = L;
+  a.n = nranks;
+  a.inv_n = exact_inv_n(nranks);
+  a.a = adam_scalars(*cfg);
+  cudaError_t e = launch_fsdp(a, vec, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "fsdp_step launch");
+  return ok();
+}
+
+cr_status cr_adamw_step(size_t n, float* master, float* m, float* v,
+                        const float* grad, const cr_adamw_cfg* cfg,
+                        void* param_bf16, cr_stream_t stream) {
+  cr_status st = check_adam_cfg(cfg);
+  if (st) return st;
+  if (n > SIZE_MAX / 8) return fail(CR_ERR_INVALID_ARG, "n=%zu too large", n);
+  if ((st = check_buf(master, n, 4, "master", 0))) return st;
+  if ((st = check_buf(m, n, 4, "m", 0))) return st;
+  if ((st = check_buf(v, n, 4, "v", 0))) return st;
+  if ((st = check_buf(grad, n, 4, "grad", 0))) return st;
+  if (param_bf16 && (st = check_buf(param_bf16, n, 2, "param_bf16", 0))) return st;
+  if (n == 0) return ok();
+  std::vector<Span> spans = {span_of(master, n * 4, 1, 0), span_of(m, n * 4, 1, 1),
+                             span_of(v, n * 4, 1, 2), span_of(grad, n * 4, 1, 3)};
+  if (param_bf16) spans.push_back(span_of(param_bf16, n * 2, 1, 4));
+  st = check_overlaps(spans, [](const Span&, const Span&) { return false; });
+  if (st) return st;
+  AdamArgs a;
+  a.master = master;
+  a.m = m;
+  a.v = v;
+  a.g = grad;
+  a.param_bf16 = param_bf16;
+  a.n = n;
+  a.a = adam_scalars(*cfg);
+  const bool vec = aligned(master, 16) && aligned(m, 16) && aligned(v, 16) &&
+                   aligned(grad, 16) && (!param_bf16 || aligned(param_bf16, 8));
+  cudaError_t e = launch_adamw(a, vec, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "adamw launch");
+  return ok();
+}
+
+// ---- buckets ---------------------------------------------------------------
+
+static cr_status check_plan(const cr_bucket_plan_t* plan, int nranks) {
+  if (!plan) return fail(CR_ERR_INVALID_ARG, "plan is NULL");
+  if (nranks < 1 || nranks > CR_MAX_RANKS)
+    return fail(CR_ERR_INVALID_ARG, "nranks=%d outside [1, %d]", nranks, CR_MAX_RANKS);
+  if (plan->ntensors < 0 || plan->nbuckets < 0 || plan->elem_size == 0)
+    return fail(CR_ERR_INVALID_ARG, "malformed plan");
+  return CR_OK;
+}
+
+// Copies for pack (to_bucket) or unpack, batched kMaxSegsPerLaunch per launch.
+static cr_status bucket_copy(const cr_bucket_plan_t* plan, int nranks,
+                             const void* const* tensors, void* const* buckets,
+                             bool to_bucket, cudaStream_t stream) {
+  cr_status st = check_plan(plan, nranks);
+  if (st) return st;
+  const int T = plan->ntensors, B = plan->nbuckets;
+  const size_t es = plan->elem_size;
+  if (T > 0 && (!tensors || !buckets)) return fail(CR_ERR_INVALID_ARG, "pointer array is NULL");
+  for (int r = 0; r < nranks; ++r) {
+    for (int b = 0; b < B; ++b)
+      if ((st = check_buf(buckets[(size_t)r * B + b], plan->bucket_numel[b], es, "buckets",
+                          r * B + b)))
+        return st;
+    for (int t = 0; t < T; ++t)
+      if ((st = check_buf(tensors[(size_t)r * T + t], plan->numels[t], es, "tensors",
+                          r * T + t)))
+        return st;
+  }
+  static thread_local CopyArgs args;  // ~28 KB: kept off the stack
+  uint32_t ntiles = 0;
+  args.nseg = 0;
+  auto flush = [&]() -> cr_status {
+    if (args.nseg == 0) return CR_OK;
+    args.tile_start[args.nseg] = ntiles;
+    cudaError_t e = launch_copy(args, ntiles, stream);
+    args.nseg = 0;
+    ntiles = 0;
+    if (e != cudaSuccess) return cuda_fail(e, "bucket copy launch");
+    return CR_OK;
+  };
+  for (int r = 0; r < nranks; ++r) {
+    for (int t = 0; t < T; ++t) {
+      const uint64_t bytes = (uint64_t)plan->numels[t] * es;
+      if (bytes == 0) continue;
+      const int b = plan->tensor_bucket[t];
+      unsigned char* bk = static_cast<unsigned char*>(buckets[(size_t)r * B + b]) +
+                          plan->tensor_offset[t] * es;
+      unsigned char* tp =
+          static_cast<unsigned char*>(const_cast<void*>(tensors[(size_t)r * T + t]));
+      CopySeg sg;
+      sg.src = to_bucket ? tp : bk;
+      sg.dst = to_bucket ? bk : tp;
+      sg.bytes = bytes;
+      const uintptr_t d0 = reinterpret_cast<uintptr_t>(sg.dst);
+      const uintptr_t da = (d0 + 15) & ~uintptr_t(15), de = (d0 + bytes) & ~uintptr_t(15);
+      const uint64_t nint = de > da ? (de - da) / 16 : 0;
+      const uint64_t tiles64 = nint == 0 ? 1 : (nint + kCopyTileBytes / 16 - 1) / (kCopyTileBytes / 16);
+      if (args.nseg == kMaxSegsPerLaunch || (uint64_t)ntiles + tiles64 > 0x7fffffffull) {
+        if ((st = flush())) return st;
+      }
+      args.seg[args.nseg] = sg;
+      args.tile_start[args.nseg] = ntiles;
+      args.nseg += 1;
+      ntiles += (uint32_t)tiles64;
+    }
+  }
+  if ((st = flush())) return st;
+  return ok();
+}
+
+cr_status cr_bucket_pack(const cr_bucket_plan_t* plan, int nranks,
+                         const void* const* tensors, void* const* buckets,
+                         cr_stream_t stream) {
+  return bucket_copy(plan, nranks, tensors, buckets, true, (cudaStream_t)stream);
+}
+
+cr_status cr_bucket_unpack(const cr_bucket_plan_t* plan, int nranks,
+                           const void* const* buckets, void* const* tensors,
+                           cr_stream_t stream) {
+  return bucket_copy(plan, nranks, const_cast<const void* const*>(tensors),
+                     const_cast<void* const*>(buckets), false, (cudaStream_t)stream);
+}
+
+cr_status cr_bucket_all_reduce(const cr_bucket_plan_t* plan, int nranks,
+                               void* const* buckets, cr_dtype dtype, cr_op op,
+                               cr_stream_t stream) {
+  cr_status st = check_plan(plan, nranks);
+  if (st) return st;
+  if (esize_of(dtype) != plan->elem_size)
+    return fail(CR_ERR_INVALID_ARG, "dtype size %zu != plan elem_size %zu", esize_of(dtype),
+                plan->elem_size);
+  if (plan->nbuckets > 0 && !buckets) return fail(CR_ERR_INVALID_ARG, "buckets is NULL");
+  const void* in[CR_MAX_RANKS];
+  void* out[CR_MAX_RANKS];
+  for (int b = 0; b < plan->nbuckets; ++b) {
+    for (int r = 0; r < nranks; ++r) {
+      in[r] = buckets[(size_t)r * plan->nbuckets + b];
+      out[r] = buckets[(size_t)r * plan->nbuckets + b];
+    }
+    st = all_reduce_impl(in, nranks, plan->bucket_numel[b], dtype, op, out, dtype,
+                         (cudaStream_t)stream);
+    if (st) return st;
+  }
+  return ok();
+}
+
+}  // extern "C"

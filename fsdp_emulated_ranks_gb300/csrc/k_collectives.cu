@@ -1,0 +1,219 @@
+// k_collectives.cu -- reduce-scatter, all-reduce and all-gather kernels.
+//
+// Reduce-scatter / all-reduce: k_fold_vec reads element e of every rank
+// buffer with 16-byte streaming loads, folds them in ring order (fold.cuh),
+// applies the AVG / cast epilogue in registers and writes either shard j
+// (reduce-scatter, [DT] section 2 Reduce-Scatter) or every rank buffer
+// (all-reduce = reduce-scatter + all-gather fused, [DT] section 2
+// All-Reduce).  No intermediate touches HBM: per element the kernel moves
+// N input and 1 (RS) or N (AR) output elements, the algorithmic minimum.
+//
+// All-gather: k_gather_vec reads each shard element once and writes it to
+// every rank buffer at its chunk offset ([DT] section 2 All-Gather).
+//
+// [DT] = "Distributed Training for Large Models: Collectives, FSDP/ZeRO,
+// DeviceMesh, and Multi-Dimensional Parallelism".
+//
+// Grids are persistent (SMs x resident CTAs) with a grid-stride loop over
+// 16-byte vectors; the ragged tail (count % VEC) and buffers that are not
+// 16-byte aligned go through the element-wise kernels.
+#include "cr_internal.cuh"
+#include "fold.cuh"
+
+namespace cr {
+
+template <int DI, int DO, int MODE, int NT>
+__global__ void __launch_bounds__(kBlock)
+    k_fold_vec(const __grid_constant__ FoldArgs a) {
+  using Acc = typename Elem<DI>::Acc;
+  constexpr int IS = Elem<DI>::kSize;
+  constexpr int OS = Elem<DO>::kSize;
+  constexpr int VEC = 16 / IS;
+  constexpr int OB = VEC * OS;
+  const int n = NT > 0 ? NT : a.n;
+  const uint64_t nvec = a.count / VEC;
+  const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+
+  for (uint64_t iv = tid; iv < nvec; iv += stride) {
+    const uint64_t e0 = iv * VEC;
+    const uint64_t j64 = e0 / a.L;
+    const int j = (int)j64;
+    if (MODE == kAR && e0 + VEC > (j64 + 1) * a.L) {
+      // The vector straddles a chunk boundary (L % VEC != 0): each element
+      // takes its own chunk's ring order.
+      for (int i = 0; i < VEC; ++i) {
+        const uint64_t e = e0 + i;
+        const int je = (int)(e / a.L);
+        Acc x = fold_elem<DI>(a.in, n, je, e);
+        if constexpr (DI != CR_I32) {
+          if (a.avg) x = finish_avg(x, n, a.inv_n);
+        }
+        for (int r = 0; r < n; ++r) st_elem<DO>(a.out[r], e, x);
+      }
+      continue;
+    }
+    Acc acc[VEC];
+    fold_vec16<DI, NT>(a.in, n, j, e0 * IS, acc);
+    if constexpr (DI != CR_I32) {
+      if (a.avg) {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) acc[i] = finish_avg(acc[i], n, a.inv_n);
+      }
+    }
+    uint32_t w[OB / 4];
+    acc_pack<DI, DO>(acc, w);
+    if constexpr (MODE == kRS) {
+      st_words<OB>(static_cast<unsigned char*>(a.out[j]) + (e0 - j64 * a.L) * OS, w);
+    } else {
+#pragma unroll 8
+      for (int r = 0; r < n; ++r)
+        st_words<OB>(static_cast<unsigned char*>(a.out[r]) + e0 * OS, w);
+    }
+  }
+
+  // Ragged tail: fewer than VEC elements after the last full vector.
+  const uint64_t e = nvec * VEC + tid;
+  if (e < a.count) {
+    const int j = (int)(e / a.L);
+    Acc x = fold_elem<DI>(a.in, n, j, e);
+    if constexpr (DI != CR_I32) {
+      if (a.avg) x = finish_avg(x, n, a.inv_n);
+    }
+    if constexpr (MODE == kRS) {
+      st_elem<DO>(a.out[j], e - (uint64_t)j * a.L, x);
+    } else {
+      for (int r = 0; r < n; ++r) st_elem<DO>(a.out[r], e, x);
+    }
+  }
+}
+
+template <int DI, int DO, int MODE>
+__global__ void __launch_bounds__(kBlock)
+    k_fold_elem(const __grid_constant__ FoldArgs a) {
+  using Acc = typename Elem<DI>::Acc;
+  const int n = a.n;
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+       e < a.count; e += stride) {
+    const int j = (int)(e / a.L);
+    Acc x = fold_elem<DI>(a.in, n, j, e);
+    if constexpr (DI != CR_I32) {
+      if (a.avg) x = finish_avg(x, n, a.inv_n);
+    }
+    if constexpr (MODE == kRS) {
+      st_elem<DO>(a.out[j], e - (uint64_t)j * a.L, x);
+    } else {
+      for (int r = 0; r < n; ++r) st_elem<DO>(a.out[r], e, x);
+    }
+  }
+}
+
+// ---- all-gather ----------------------------------------------------------
+
+template <int ES>
+__global__ void __launch_bounds__(kBlock)
+    k_gather_vec(const __grid_constant__ GatherArgs a) {
+  constexpr int VEC = 16 / ES;
+  const uint64_t nvec = a.count / VEC;
+  const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  const int n = a.n;
+  for (uint64_t iv = tid; iv < nvec; iv += stride) {
+    const uint64_t e0 = iv * VEC;
+    const uint64_t j64 = e0 / a.L;
+    const int j = (int)j64;
+    const uint4 v = ld16(static_cast<const unsigned char*>(a.shards[j]) +
+                         (e0 - j64 * a.L) * ES);
+    const bool skip_own = (a.inplace_mask >> j) & 1ull;
+    for (int r = 0; r < n; ++r) {
+      if (skip_own && r == j) continue;
+      st16(static_cast<unsigned char*>(a.bufs[r]) + e0 * ES, v);
+    }
+  }
+  const uint64_t e = nvec * VEC + tid;
+  if (e < a.count) {
+    const uint64_t j64 = e / a.L;
+    const int j = (int)j64;
+    const unsigned char* src =
+        static_cast<const unsigned char*>(a.shards[j]) + (e - j64 * a.L) * ES;
+    const bool skip_own = (a.inplace_mask >> j) & 1ull;
+    for (int r = 0; r < n; ++r) {
+      if (skip_own && r == j) continue;
+      unsigned char* dst = static_cast<unsigned char*>(a.bufs[r]) + e * ES;
+      if constexpr (ES == 2) *reinterpret_cast<uint16_t*>(dst) = *reinterpret_cast<const uint16_t*>(src);
+      else *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(src);
+    }
+  }
+}
+
+template <int ES>
+__global__ void __launch_bounds__(kBlock)
+    k_gather_elem(const __grid_constant__ GatherArgs a) {
+  using W = typename std::conditional<ES == 2, uint16_t, uint32_t>::type;
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+       e < a.count; e += stride) {
+    const uint64_t j64 = e / a.L;
+    const int j = (int)j64;
+    const W x = static_cast<const W*>(a.shards[j])[e - j64 * a.L];
+    const bool skip_own = (a.inplace_mask >> j) & 1ull;
+    for (int r = 0; r < a.n; ++r) {
+      if (skip_own && r == j) continue;
+      static_cast<W*>(a.bufs[r])[e] = x;
+    }
+  }
+}
+
+// ---- launchers -------------------------------------------------------------
+
+template <typename K, typename A>
+static cudaError_t launch_persistent(K kernel, const A& args, uint64_t threads,
+                                     cudaStream_t s) {
+  int grid = 0;
+  cudaError_t err = persistent_grid(reinterpret_cast<const void*>(kernel), threads, &grid);
+  if (err != cudaSuccess) return err;
+  kernel<<<grid, kBlock, 0, s>>>(args);
+  return cudaGetLastError();
+}
+
+template <int DI, int DO, int MODE>
+static cudaError_t fold_dispatch(const FoldArgs& a, bool vec, cudaStream_t s) {
+  if (!vec) return launch_persistent(k_fold_elem<DI, DO, MODE>, a, a.count, s);
+  constexpr int VEC = 16 / Elem<DI>::kSize;
+  const uint64_t threads = a.count / VEC + 1;
+  switch (a.n) {
+    case 2: return launch_persistent(k_fold_vec<DI, DO, MODE, 2>, a, threads, s);
+    case 4: return launch_persistent(k_fold_vec<DI, DO, MODE, 4>, a, threads, s);
+    case 8: return launch_persistent(k_fold_vec<DI, DO, MODE, 8>, a, threads, s);
+    default: return launch_persistent(k_fold_vec<DI, DO, MODE, 0>, a, threads, s);
+  }
+}
+
+template <int MODE>
+static cudaError_t fold_by_type(cr_dtype in, cr_dtype out, const FoldArgs& a,
+                                bool vec, cudaStream_t s) {
+  if (in == CR_F32 && out == CR_F32) return fold_dispatch<CR_F32, CR_F32, MODE>(a, vec, s);
+  if (in == CR_BF16 && out == CR_BF16) return fold_dispatch<CR_BF16, CR_BF16, MODE>(a, vec, s);
+  if (in == CR_BF16 && out == CR_F32) return fold_dispatch<CR_BF16, CR_F32, MODE>(a, vec, s);
+  if (in == CR_I32 && out == CR_I32) return fold_dispatch<CR_I32, CR_I32, MODE>(a, vec, s);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fold(cr_dtype in, cr_dtype out, FoldMode mode,
+                        const FoldArgs& a, bool vec, cudaStream_t s) {
+  return mode == kRS ? fold_by_type<kRS>(in, out, a, vec, s)
+                     : fold_by_type<kAR>(in, out, a, vec, s);
+}
+
+cudaError_t launch_gather(size_t esize, const GatherArgs& a, bool vec,
+                          cudaStream_t s) {
+  if (esize == 2) {
+    return vec ? launch_persistent(k_gather_vec<2>, a, a.count / 8 + 1, s)
+               : launch_persistent(k_gather_elem<2>, a, a.count, s);
+  }
+  return vec ? launch_persistent(k_gather_vec<4>, a, a.count / 4 + 1, s)
+             : launch_persistent(k_gather_elem<4>, a, a.count, s);
+}
+
+}  // namespace cr

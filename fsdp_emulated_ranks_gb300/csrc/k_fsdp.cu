@@ -1,0 +1,206 @@
+// k_fsdp.cu -- the fused FSDP / ZeRO-3 step and the stand-alone AdamW.
+//
+// One pass over the flat parameter buffer does what the FSDP1 unit lifecycle
+// of "Distributed Training for Large Models: Collectives, FSDP/ZeRO,
+// DeviceMesh, and Multi-Dimensional Parallelism" (section 4; ZeRO-3 flow
+// steps 5-6) spreads over three phases:
+//   backward post-hook  reduce-scatter of the bf16 grads, fp32 partials in
+//                       ring order, / N (reduce_dtype fp32, "AI Infra Guide,
+//                       Chapter 6", 6.3.4);
+//   optimizer step      AdamW on owner j's fp32 master/m/v shard;
+//   next forward        bf16 cast and all-gather to every rank's params.
+// Element e belongs to shard j = e / L, so the thread that folds e's
+// gradient is the one that owns e's optimizer state: nothing is staged in
+// HBM between the phases.  Per element: N bf16 grad loads, 12 B of fp32
+// state read and written, N bf16 param stores -- (4N + 24) bytes.
+//
+// AdamW uses only correctly rounded fp32 operations (__fmul_rn & co. are
+// never contracted into FMAs), in the order of the textbook decoupled-
+// weight-decay rule stated in include/cr.h.
+#include "cr_internal.cuh"
+#include "fold.cuh"
+
+namespace cr {
+
+struct AdamOut {
+  float p, m, v;
+};
+
+__device__ __forceinline__ AdamOut adamw_elem(float p, float m, float v,
+                                              float g, const AdamScalars& a) {
+  AdamOut o;
+  const float pd = __fmul_rn(p, a.decay);
+  o.m = __fadd_rn(__fmul_rn(a.b1, m), __fmul_rn(a.omb1, g));
+  o.v = __fadd_rn(__fmul_rn(a.b2, v), __fmul_rn(a.omb2, __fmul_rn(g, g)));
+  const float mh = __fdiv_rn(o.m, a.bc1);
+  const float vh = __fdiv_rn(o.v, a.bc2);
+  const float denom = __fadd_rn(__fsqrt_rn(vh), a.eps);
+  o.p = __fsub_rn(pd, __fmul_rn(a.lr, __fdiv_rn(mh, denom)));
+  return o;
+}
+
+__device__ __forceinline__ uint4 ld16_f(const float* p) { return ld16(p); }
+
+// Vector path: 8 elements (one 16-byte bf16 vector per rank) per iteration.
+template <int NT>
+__global__ void __launch_bounds__(kBlock)
+    k_fsdp_vec(const __grid_constant__ FsdpArgs a) {
+  const int n = NT > 0 ? NT : a.n;
+  const uint64_t nvec = a.count / 8;
+  const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t iv = tid; iv < nvec; iv += stride) {
+    const uint64_t e0 = iv * 8;
+    const uint64_t j64 = e0 / a.L;
+    const int j = (int)j64;
+    const uint64_t k = e0 - j64 * a.L;  // offset inside shard j
+    float g[8];
+    fold_vec16<CR_BF16, NT>(a.grads, n, j, e0 * 2, g);
+    float* mp = a.master[j] + k;
+    float* mm = a.m[j] + k;
+    float* mv = a.v[j] + k;
+    const uint4 p0 = ld16(mp), p1 = ld16(mp + 4);
+    const uint4 m0 = ld16(mm), m1 = ld16(mm + 4);
+    const uint4 v0 = ld16(mv), v1 = ld16(mv + 4);
+    const uint32_t pw[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    const uint32_t mw[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+    const uint32_t vw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint32_t po[8], mo[8], vo[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float gi = finish_avg(g[i], n, a.inv_n);
+      const AdamOut o = adamw_elem(__uint_as_float(pw[i]), __uint_as_float(mw[i]),
+                                   __uint_as_float(vw[i]), gi, a.a);
+      po[i] = __float_as_uint(o.p);
+      mo[i] = __float_as_uint(o.m);
+      vo[i] = __float_as_uint(o.v);
+    }
+    st16(mp, make_uint4(po[0], po[1], po[2], po[3]));
+    st16(mp + 4, make_uint4(po[4], po[5], po[6], po[7]));
+    st16(mm, make_uint4(mo[0], mo[1], mo[2], mo[3]));
+    st16(mm + 4, make_uint4(mo[4], mo[5], mo[6], mo[7]));
+    st16(mv, make_uint4(vo[0], vo[1], vo[2], vo[3]));
+    st16(mv + 4, make_uint4(vo[4], vo[5], vo[6], vo[7]));
+    const uint4 pb = make_uint4(
+        pack_bf16x2(__uint_as_float(po[0]), __uint_as_float(po[1])),
+        pack_bf16x2(__uint_as_float(po[2]), __uint_as_float(po[3])),
+        pack_bf16x2(__uint_as_float(po[4]), __uint_as_float(po[5])),
+        pack_bf16x2(__uint_as_float(po[6]), __uint_as_float(po[7])));
+#pragma unroll 8
+    for (int r = 0; r < n; ++r)
+      st16(static_cast<unsigned char*>(a.params[r]) + e0 * 2, pb);
+  }
+  // Ragged tail (count % 8 elements).
+  const uint64_t e = nvec * 8 + tid;
+  if (e < a.count) {
+    const uint64_t j64 = e / a.L;
+    const int j = (int)j64;
+    const uint64_t k = e - j64 * a.L;
+    const float gi = finish_avg(fold_elem<CR_BF16>(a.grads, n, j, e), n, a.inv_n);
+    const AdamOut o = adamw_elem(a.master[j][k], a.m[j][k], a.v[j][k], gi, a.a);
+    a.master[j][k] = o.p;
+    a.m[j][k] = o.m;
+    a.v[j][k] = o.v;
+    for (int r = 0; r < n; ++r) st_elem<CR_BF16>(a.params[r], e, o.p);
+  }
+}
+
+__global__ void __launch_bounds__(kBlock)
+    k_fsdp_elem(const __grid_constant__ FsdpArgs a) {
+  const int n = a.n;
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+       e < a.count; e += stride) {
+    const uint64_t j64 = e / a.L;
+    const int j = (int)j64;
+    const uint64_t k = e - j64 * a.L;
+    const float gi = finish_avg(fold_elem<CR_BF16>(a.grads, n, j, e), n, a.inv_n);
+    const AdamOut o = adamw_elem(a.master[j][k], a.m[j][k], a.v[j][k], gi, a.a);
+    a.master[j][k] = o.p;
+    a.m[j][k] = o.m;
+    a.v[j][k] = o.v;
+    for (int r = 0; r < n; ++r) st_elem<CR_BF16>(a.params[r], e, o.p);
+  }
+}
+
+// ---- stand-alone AdamW on an fp32 shard ------------------------------------
+
+__global__ void __launch_bounds__(kBlock)
+    k_adamw_vec(const __grid_constant__ AdamArgs a) {
+  const uint64_t nvec = a.n / 4;
+  const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t iv = tid; iv < nvec; iv += stride) {
+    const uint64_t e0 = iv * 4;
+    const uint4 p = ld16(a.master + e0), m = ld16(a.m + e0), v = ld16(a.v + e0);
+    const uint4 g = ld16(a.g + e0);
+    const uint32_t pw[4] = {p.x, p.y, p.z, p.w}, mw[4] = {m.x, m.y, m.z, m.w};
+    const uint32_t vw[4] = {v.x, v.y, v.z, v.w}, gw[4] = {g.x, g.y, g.z, g.w};
+    uint32_t po[4], mo[4], vo[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const AdamOut o = adamw_elem(__uint_as_float(pw[i]), __uint_as_float(mw[i]),
+                                   __uint_as_float(vw[i]), __uint_as_float(gw[i]), a.a);
+      po[i] = __float_as_uint(o.p);
+      mo[i] = __float_as_uint(o.m);
+      vo[i] = __float_as_uint(o.v);
+    }
+    st16(a.master + e0, make_uint4(po[0], po[1], po[2], po[3]));
+    st16(a.m + e0, make_uint4(mo[0], mo[1], mo[2], mo[3]));
+    st16(a.v + e0, make_uint4(vo[0], vo[1], vo[2], vo[3]));
+    if (a.param_bf16) {
+      const uint32_t w[2] = {pack_bf16x2(__uint_as_float(po[0]), __uint_as_float(po[1])),
+                             pack_bf16x2(__uint_as_float(po[2]), __uint_as_float(po[3]))};
+      st_words<8>(static_cast<unsigned char*>(a.param_bf16) + e0 * 2, w);
+    }
+  }
+  const uint64_t e = nvec * 4 + tid;
+  if (e < a.n) {
+    const AdamOut o = adamw_elem(a.master[e], a.m[e], a.v[e], a.g[e], a.a);
+    a.master[e] = o.p;
+    a.m[e] = o.m;
+    a.v[e] = o.v;
+    if (a.param_bf16) st_elem<CR_BF16>(a.param_bf16, e, o.p);
+  }
+}
+
+__global__ void __launch_bounds__(kBlock)
+    k_adamw_elem(const __grid_constant__ AdamArgs a) {
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; e < a.n;
+       e += stride) {
+    const AdamOut o = adamw_elem(a.master[e], a.m[e], a.v[e], a.g[e], a.a);
+    a.master[e] = o.p;
+    a.m[e] = o.m;
+    a.v[e] = o.v;
+    if (a.param_bf16) st_elem<CR_BF16>(a.param_bf16, e, o.p);
+  }
+}
+
+template <typename K, typename A>
+static cudaError_t launch_persistent(K kernel, const A& args, uint64_t threads,
+                                     cudaStream_t s) {
+  int grid = 0;
+  cudaError_t err = persistent_grid(reinterpret_cast<const void*>(kernel), threads, &grid);
+  if (err != cudaSuccess) return err;
+  kernel<<<grid, kBlock, 0, s>>>(args);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fsdp(const FsdpArgs& a, bool vec, cudaStream_t s) {
+  if (!vec) return launch_persistent(k_fsdp_elem, a, a.count, s);
+  const uint64_t threads = a.count / 8 + 1;
+  switch (a.n) {
+    case 2: return launch_persistent(k_fsdp_vec<2>, a, threads, s);
+    case 4: return launch_persistent(k_fsdp_vec<4>, a, threads, s);
+    case 8: return launch_persistent(k_fsdp_vec<8>, a, threads, s);
+    default: return launch_persistent(k_fsdp_vec<0>, a, threads, s);
+  }
+}
+
+cudaError_t launch_adamw(const AdamArgs& a, bool vec, cudaStream_t s) {
+  return vec ? launch_persistent(k_adamw_vec, a, a.n / 4 + 1, s)
+             : launch_persistent(k_adamw_elem, a, a.n, s);
+}
+
+}  // namespace cr

@@ -1,0 +1,171 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol
+include/cr.h declares, rejects bad arguments on the host with the documented
+status before touching a device, and its host-only parts (bucket plan,
+traffic accounting) match the oracle exactly."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as O
+from fsdp_emulated_ranks_gb300 import build as libbuild
+from fsdp_emulated_ranks_gb300 import cr
+from fsdp_emulated_ranks_gb300 import inputs as I
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    libbuild.build()
+    return cr.lib()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "cr.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = set(re.findall(r"\b(cr_[a-z_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_exports_every_declared_symbol(L):
+    declared = header_functions()
+    assert set(declared) == set(cr.EXPORTS)
+    for name in declared:
+        assert hasattr(L, name), name
+    assert L.cr_version() == 100
+
+
+def test_status_strings(L):
+    for k, v in cr.STATUS.items():
+        assert L.cr_status_string(k).decode() == v
+
+
+def expect(status, fn, *args, **kw):
+    with pytest.raises(cr.CRError) as ei:
+        fn(*args, **kw)
+    assert ei.value.status == status, str(ei.value)
+    return str(ei.value)
+
+
+FAKE = 1 << 40  # an address never dereferenced: validation fails first
+
+
+def test_reduce_scatter_validation(L):
+    n = 4
+    bufs = [FAKE + r * (1 << 20) for r in range(n)]
+    outs = [FAKE + (1 << 30) + r * (1 << 20) for r in range(n)]
+    expect(1, cr.cr_reduce_scatter, bufs * 17, 8, "f32", "sum", outs * 17, "f32", stream=0)
+    expect(1, cr.cr_reduce_scatter, [], 8, "f32", "sum", [], "f32", stream=0)
+    expect(2, cr.cr_reduce_scatter, bufs, 8, "i32", "avg", outs, "i32", stream=0)
+    expect(2, cr.cr_reduce_scatter, bufs, 8, "f32", "sum", outs, "bf16", stream=0)
+    expect(2, cr.cr_reduce_scatter, bufs, 8, "f32", "sum", outs, "i32", stream=0)
+    expect(1, cr.cr_reduce_scatter, bufs[:3] + [0], 8, "f32", "sum", outs, "f32", stream=0)
+    expect(3, cr.cr_reduce_scatter, [bufs[0] + 2] + bufs[1:], 8, "f32", "sum", outs, "f32", stream=0)
+    # overlap: shard 1 inside rank 0's input
+    bad = list(outs)
+    bad[1] = bufs[0] + 4
+    expect(1, cr.cr_reduce_scatter, bufs, 8, "f32", "sum", bad, "f32", stream=0)
+    # two outputs overlapping
+    bad = list(outs)
+    bad[2] = outs[1] + 4
+    expect(1, cr.cr_reduce_scatter, bufs, 64, "f32", "sum", bad, "f32", stream=0)
+    # in place is legal only with equal dtypes: bf16 -> f32 in place is not
+    L_ = cr.cr_chunk_len(64, n)
+    inpl = [bufs[j] + j * L_ * 2 for j in range(n)]
+    expect(1, cr.cr_reduce_scatter, bufs, 64, "bf16", "sum", inpl, "f32", stream=0)
+    # empty count: legal, nothing launched
+    cr.cr_reduce_scatter(bufs, 0, "f32", "sum", [0] * n, "f32", stream=0)
+    # NULL rank buffers with count > 0 are rejected even when every shard
+    # they would feed is empty
+    expect(1, cr.cr_reduce_scatter, [0] * n, 2, "f32", "sum", [0] * n, "f32", stream=0)
+
+
+def test_all_reduce_and_gather_validation(L):
+    n = 3
+    bufs = [FAKE + r * (1 << 20) for r in range(n)]
+    outs = [FAKE + (1 << 30) + r * (1 << 20) for r in range(n)]
+    expect(1, cr.cr_all_reduce, bufs, 16, "f32", "sum", [bufs[1]] + outs[1:], "f32", stream=0)
+    expect(1, cr.cr_all_reduce, bufs, 16, "bf16", "avg", bufs, "f32", stream=0)
+    expect(3, cr.cr_all_reduce, bufs, 16, "bf16", "avg", [outs[0] + 1] + outs[1:], "bf16", stream=0)
+    expect(1, cr.cr_all_reduce, bufs, 16, 7, "sum", outs, "f32", stream=0)
+    # shard 0 lies inside rank 1's output (only rank 0's chunk 0 is in place)
+    expect(1, cr.cr_all_gather, bufs, 16, "f32", [outs[0], bufs[0], outs[2]], stream=0)
+    expect(1, cr.cr_all_gather, bufs, 16, "f32", [outs[0], outs[0], outs[2]], stream=0)
+    expect(3, cr.cr_all_gather, bufs, 16, "bf16", [outs[0] + 1] + outs[1:], stream=0)
+    cr.cr_all_reduce(bufs, 0, "f32", "sum", bufs, "f32", stream=0)
+    cr.cr_all_gather([0] * n, 0, "f32", [0] * n, stream=0)
+
+
+def test_fsdp_and_adamw_validation(L):
+    n, count = 2, 16
+    g = [FAKE + r * (1 << 20) for r in range(n)]
+    p = [FAKE + (1 << 28) + r * (1 << 20) for r in range(n)]
+    ms = [FAKE + (2 << 28) + r * (1 << 20) for r in range(n)]
+    m = [FAKE + (3 << 28) + r * (1 << 20) for r in range(n)]
+    v = [FAKE + (4 << 28) + r * (1 << 20) for r in range(n)]
+    expect(1, cr.cr_fsdp_step, g, count, ms, m, v, cr.adamw_cfg(step=0), p, stream=0)
+    expect(1, cr.cr_fsdp_step, g, count, ms, m, v, cr.adamw_cfg(beta1=1.0), p, stream=0)
+    expect(1, cr.cr_fsdp_step, g, count, ms, m, [m[0], v[1]], cr.adamw_cfg(), p, stream=0)
+    expect(1, cr.cr_fsdp_step, g, count, ms, m, v, cr.adamw_cfg(), g, stream=0)
+    expect(3, cr.cr_fsdp_step, g, count, [ms[0] + 2, ms[1]], m, v, cr.adamw_cfg(), p, stream=0)
+    cr.cr_fsdp_step(g, 0, [0] * n, [0] * n, [0] * n, cr.adamw_cfg(), p, stream=0)
+    expect(1, cr.cr_adamw_step, 8, ms[0], ms[0] + 16, m[0], v[0], cr.adamw_cfg(), stream=0)
+    expect(1, cr.cr_adamw_step, 8, ms[0], 0, m[0], v[0], cr.adamw_cfg(), stream=0)
+    cr.cr_adamw_step(0, 0, 0, 0, 0, cr.adamw_cfg(), stream=0)
+
+
+def test_bucket_validation(L):
+    plan = cr.cr_bucket_plan([4, 8], 2, 64)
+    expect(1, cr.cr_bucket_pack, plan, 0, [FAKE] * 2, [FAKE] * 2, stream=0)
+    expect(1, cr.cr_bucket_pack, plan, 1, [0, FAKE], [FAKE], stream=0)
+    expect(3, cr.cr_bucket_pack, plan, 1, [FAKE + 1, FAKE + 64], [FAKE + 4096], stream=0)
+    expect(1, cr.cr_bucket_all_reduce, plan, 1, [FAKE], "f32", "sum", stream=0)
+    with pytest.raises(cr.CRError):
+        cr.cr_bucket_plan([1, 2], 0, 64)
+    with pytest.raises(cr.CRError):
+        cr.cr_bucket_plan([1, 2], 2, 0)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_bucket_plan_matches_oracle(L, seed):
+    rng = np.random.default_rng(seed)
+    numels = [int(k) for k in rng.integers(0, 3000, size=rng.integers(0, 80))]
+    for esize in (2, 4):
+        for cap in (1, 100, 2048, 10000, 1 << 22):
+            a = cr.cr_bucket_plan(numels, esize, cap)
+            b = O.bucket_plan(numels, esize, cap)
+            assert a.nbuckets == b.nbuckets
+            assert a.tensor_bucket == [int(x) for x in b.tensor_bucket]
+            assert a.tensor_offset == [int(x) for x in b.tensor_offset]
+            assert a.bucket_numel == [int(x) for x in b.bucket_numel]
+
+
+def test_bucket_plan_workload_matches_oracle(L):
+    numels = [int(k) for k in I.bucket_numels()]
+    cap = 25 * 1024 * 1024
+    a = cr.cr_bucket_plan(numels, 2, cap)
+    b = O.bucket_plan(numels, 2, cap)
+    assert a.tensor_bucket == [int(x) for x in b.tensor_bucket]
+    assert a.tensor_offset == [int(x) for x in b.tensor_offset]
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 13, 64])
+@pytest.mark.parametrize("count", [0, 1, 5, 64, 1000, 4097])
+def test_comm_elems_match_oracle_counters(L, n, count):
+    bufs = I.integer_valued_f32(n, count, seed=0)
+    _, rs = O.ring_reduce_scatter(bufs, "f32", "sum")
+    L_ = O.chunk_len(count, n)
+    shards = [np.zeros(b - a, np.float32) for a, b in (O.chunk_bounds(count, n, j) for j in range(n))]
+    _, ag = O.ring_all_gather(shards, count, "f32")
+    _, ar = O.ring_all_reduce(bufs, "f32", "sum")
+    _, nv = O.naive_all_reduce(bufs, "f32", "sum")
+    assert L_ == cr.cr_chunk_len(count, n)
+    for r in range(n):
+        assert cr.cr_shard_range(count, n, r) == O.chunk_bounds(count, n, r)
+        for coll, t in ((0, rs), (1, ag), (2, ar)):
+            assert cr.cr_comm_elems(coll, cr.SCHED_RING, n, count, r) == (t.sent[r], t.recv[r], t.steps)
+        assert cr.cr_comm_elems(2, cr.SCHED_NAIVE, n, count, r) == (nv.sent[r], nv.recv[r], nv.steps)
+    expect(2, cr.cr_comm_elems, 0, cr.SCHED_NAIVE, n, count, 0)

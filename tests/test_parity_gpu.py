@@ -1,0 +1,312 @@
+"""GPU parity: every collective of libcr, called through the C ABI, against
+the CPU oracle on the same seeded inputs, element by element.
+
+fp32 / int32 results and bucket copies must be bit-exact (the kernels fold
+in the ring's order); bf16 results within 1 bf16 ulp; AdamW state within
+1e-6 * max|ref|.  Sizes span several 16-byte vectors and CTAs plus a ragged
+tail; the unaligned variants start a buffer one element into an allocation
+to force the element-wise kernels.  Every output carries canaries that must
+survive the call.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from fsdp_emulated_ranks_gb300 import build as libbuild
+from fsdp_emulated_ranks_gb300 import cr
+from fsdp_emulated_ranks_gb300 import inputs as I
+from gpu_util import Guarded, assert_match, rel_maxabs, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+PAIRS = [("f32", "sum", "f32"), ("bf16", "avg", "bf16"), ("bf16", "avg", "f32"),
+         ("i32", "sum", "i32"), ("f32", "avg", "f32"), ("bf16", "sum", "bf16")]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    libbuild.build()
+    cr.lib()
+
+
+def sizes(n):
+    return [0, 1, 7, 8 * n * 3, 8 * n * 37 + 5, 1000, 4099]
+
+
+def host_inputs(n, count, dt, seed):
+    return I.host_rank_buffers(n, count, dt, std=0.02 if dt == "bf16" else 1.0, seed0=seed)
+
+
+# ---- reduce-scatter -------------------------------------------------------------
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 16, 64])
+@pytest.mark.parametrize("pair", PAIRS)
+@pytest.mark.parametrize("offset", [0, 1])
+def test_reduce_scatter(n, pair, offset):
+    dt, op, out = pair
+    for count in sizes(n):
+        host = host_inputs(n, count, dt, seed=n * 100 + count)
+        want, _ = O.ring_reduce_scatter(host, dt, op, out)
+        bufs = [to_dev(x, dt, offset) for x in host]
+        shards = [Guarded(w.size, out, offset) for w in want]
+        cr.cr_reduce_scatter(bufs, count, dt, op, [s.ptr() for s in shards], out)
+        torch.cuda.synchronize()
+        for j in range(n):
+            shards[j].check()
+            assert_match(shards[j].host(), want[j], out, f"n={n} count={count} shard {j}")
+        for r in range(n):  # inputs untouched
+            assert to_host(bufs[r], dt).tobytes() == host[r].tobytes()
+
+
+@pytest.mark.parametrize("n", [2, 4, 8, 5])
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_reduce_scatter_in_place(n, dt):
+    count = 8 * n * 50
+    host = host_inputs(n, count, dt, seed=7)
+    want, _ = O.ring_reduce_scatter(host, dt, "avg", dt)
+    bufs = [to_dev(x, dt) for x in host]
+    L = cr.cr_chunk_len(count, n)
+    shards = [bufs[j][j * L:(j + 1) * L] for j in range(n)]
+    cr.cr_reduce_scatter(bufs, count, dt, "avg", shards, dt)
+    torch.cuda.synchronize()
+    for j in range(n):
+        assert_match(to_host(shards[j], dt), want[j], dt, f"shard {j}")
+
+
+# ---- all-reduce ----------------------------------------------------------------
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 16, 64])
+@pytest.mark.parametrize("pair", PAIRS)
+@pytest.mark.parametrize("offset", [0, 1])
+def test_all_reduce(n, pair, offset):
+    dt, op, out = pair
+    for count in sizes(n):
+        host = host_inputs(n, count, dt, seed=n * 300 + count)
+        want, _ = O.ring_all_reduce(host, dt, op, out)
+        bufs = [to_dev(x, dt, offset) for x in host]
+        outs = [Guarded(count, out, offset) for _ in range(n)]
+        cr.cr_all_reduce(bufs, count, dt, op, [o.ptr() for o in outs], out)
+        torch.cuda.synchronize()
+        for r in range(n):
+            outs[r].check()
+            assert_match(outs[r].host(), want[r], out, f"n={n} count={count} rank {r}")
+
+
+@pytest.mark.parametrize("n", [2, 3, 4, 8, 13])
+@pytest.mark.parametrize("dt,op", [("bf16", "avg"), ("f32", "sum"), ("i32", "sum")])
+@pytest.mark.parametrize("count_fn", [lambda n: 8 * n * 64, lambda n: 8 * n * 64 + 3 * n + 1])
+def test_all_reduce_in_place(n, dt, op, count_fn):
+    """In place, including L not a multiple of the vector width (vectors
+    straddling a chunk boundary take the element-wise path)."""
+    count = count_fn(n)
+    host = host_inputs(n, count, dt, seed=count)
+    want, _ = O.ring_all_reduce(host, dt, op, dt)
+    bufs = [to_dev(x, dt) for x in host]
+    cr.cr_all_reduce(bufs, count, dt, op, bufs, dt)
+    torch.cuda.synchronize()
+    for r in range(n):
+        assert_match(to_host(bufs[r], dt), want[r], dt, f"rank {r}")
+
+
+# ---- all-gather ----------------------------------------------------------------
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 16, 64])
+@pytest.mark.parametrize("dt", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_all_gather(n, dt, offset):
+    for count in sizes(n):
+        shards = []
+        for j in range(n):
+            lo, hi = O.chunk_bounds(count, n, j)
+            shards.append(host_inputs(1, hi - lo, dt, seed=j + count)[0])
+        want, _ = O.ring_all_gather(shards, count, dt)
+        d_sh = [to_dev(s, dt, offset) if s.size else None for s in shards]
+        outs = [Guarded(count, dt, offset) for _ in range(n)]
+        cr.cr_all_gather([s if s is not None else 0 for s in d_sh], count, dt, [o.ptr() for o in outs])
+        torch.cuda.synchronize()
+        for r in range(n):
+            outs[r].check()
+            assert_match(outs[r].host(), want[r], dt, f"n={n} count={count} rank {r}")
+
+
+@pytest.mark.parametrize("n", [2, 4, 8])
+def test_all_gather_in_place(n):
+    count = 8 * n * 33
+    host = host_inputs(n, count, "bf16", seed=3)
+    L = count // n
+    shards_h = [host[j][j * L:(j + 1) * L].copy() for j in range(n)]
+    want, _ = O.ring_all_gather(shards_h, count, "bf16")
+    bufs = [to_dev(x, "bf16") for x in host]
+    cr.cr_all_gather([bufs[j][j * L:(j + 1) * L] for j in range(n)], count, "bf16", bufs)
+    torch.cuda.synchronize()
+    for r in range(n):
+        assert_match(to_host(bufs[r], "bf16"), want[r], "bf16", f"rank {r}")
+
+
+def test_all_reduce_equals_gather_of_scatter_on_gpu():
+    n, count = 8, 8 * 8 * 1000 + 13
+    host = host_inputs(n, count, "bf16", seed=11)
+    bufs = [to_dev(x, "bf16") for x in host]
+    L = cr.cr_chunk_len(count, n)
+    shards = [torch.empty(min(L, max(0, count - j * L)), dtype=torch.bfloat16, device="cuda")
+              for j in range(n)]
+    outs = [torch.empty(count, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    outs2 = [torch.empty(count, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    cr.cr_reduce_scatter(bufs, count, "bf16", "avg", shards, "bf16")
+    cr.cr_all_gather(shards, count, "bf16", outs)
+    cr.cr_all_reduce(bufs, count, "bf16", "avg", outs2, "bf16")
+    torch.cuda.synchronize()
+    for r in range(n):
+        assert torch.equal(outs[r].view(torch.int16), outs2[r].view(torch.int16))
+
+
+# ---- FSDP step and AdamW ----------------------------------------------------------
+
+def fsdp_case(n, count, seed):
+    grads = I.host_rank_buffers(n, count, "bf16", std=1e-3, seed0=1000 + seed)
+    master_full = I.np_normal_f32(count, 0.02, 2000 + seed)
+    shards = [O.chunk_bounds(count, n, j) for j in range(n)]
+    master = [master_full[a:b].copy() for a, b in shards]
+    m = [np.zeros(b - a, np.float32) for a, b in shards]
+    v = [np.zeros(b - a, np.float32) for a, b in shards]
+    return grads, master, m, v
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("count_fn", [lambda n: 8 * n * 40, lambda n: 8 * n * 40 + 5, lambda n: 1,
+                                      lambda n: 100])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_fsdp_step_three_steps(n, count_fn, offset):
+    count = count_fn(n)
+    grads, master, m, v = fsdp_case(n, count, seed=n)
+    d_master = [Guarded(x.size, "f32", offset) for x in master]
+    d_m = [Guarded(x.size, "f32", offset) for x in m]
+    d_v = [Guarded(x.size, "f32", offset) for x in v]
+    for g, src in ((d_master, master), (d_m, m), (d_v, v)):
+        for gg, x in zip(g, src):
+            if x.size:
+                gg.view.copy_(to_dev(x, "f32"))
+    d_p = [Guarded(count, "bf16", offset) for _ in range(n)]
+    for step in (1, 2, 3):
+        grads = I.host_rank_buffers(n, count, "bf16", std=1e-3, seed0=1000 + 17 * step)
+        d_g = [to_dev(x, "bf16", offset) for x in grads]
+        cfg = O.AdamWConfig(step=step)
+        want_p = O.fsdp_step(grads, master, m, v, cfg)
+        cr.cr_fsdp_step(d_g, count, [x.ptr() for x in d_master], [x.ptr() for x in d_m],
+                        [x.ptr() for x in d_v], cr.adamw_cfg(step=step), [x.ptr() for x in d_p])
+        torch.cuda.synchronize()
+        for j in range(n):
+            for gg, ref, name in ((d_master, master, "master"), (d_m, m, "m"), (d_v, v, "v")):
+                gg[j].check()
+                assert rel_maxabs(gg[j].host(), ref[j]) <= 1e-6, f"{name}[{j}] step {step}"
+        for r in range(n):
+            d_p[r].check()
+            assert_match(d_p[r].host(), want_p[r], "bf16", f"params[{r}] step {step}")
+
+
+@pytest.mark.parametrize("n_elems", [1, 3, 4, 1000, 4096 * 9 + 3])
+@pytest.mark.parametrize("with_param", [True, False])
+def test_adamw_step(n_elems, with_param):
+    rng = np.random.default_rng(n_elems)
+    p = (rng.standard_normal(n_elems) * 0.02).astype(np.float32)
+    m = (rng.standard_normal(n_elems) * 1e-4).astype(np.float32)
+    v = np.abs(rng.standard_normal(n_elems) * 1e-7).astype(np.float32)
+    g = (rng.standard_normal(n_elems) * 1e-3).astype(np.float32)
+    d = [to_dev(x, "f32") for x in (p, m, v, g)]
+    out = Guarded(n_elems, "bf16") if with_param else None
+    cfg = O.AdamWConfig(step=4)
+    O.adamw(p, m, v, g, cfg)
+    cr.cr_adamw_step(n_elems, d[0], d[1], d[2], d[3], cr.adamw_cfg(step=4),
+                     out.ptr() if out else None)
+    torch.cuda.synchronize()
+    for t, ref in zip(d[:3], (p, m, v)):
+        assert rel_maxabs(to_host(t, "f32"), ref) <= 1e-6
+    if out:
+        out.check()
+        assert_match(out.host(), O.f32_to_bf16(p), "bf16")
+
+
+# ---- buckets ------------------------------------------------------------------------
+
+def bucket_case(n, numels, esize, cap, seed, bucket_offset):
+    plan = cr.cr_bucket_plan(numels, esize, cap)
+    oplan = O.bucket_plan(numels, esize, cap)
+    assert plan.tensor_bucket == [int(x) for x in oplan.tensor_bucket]
+    assert plan.tensor_offset == [int(x) for x in oplan.tensor_offset]
+    dt = "bf16" if esize == 2 else "f32"
+    host_t = [[host_inputs(1, int(k), dt, seed=seed + 1000 * r + t)[0] for t, k in enumerate(numels)]
+              for r in range(n)]
+    return plan, oplan, dt, host_t
+
+
+@pytest.mark.parametrize("n", [1, 2, 8])
+@pytest.mark.parametrize("esize", [2, 4])
+@pytest.mark.parametrize("tensor_offset,bucket_offset", [(0, 0), (1, 0), (0, 1), (1, 3)])
+def test_bucket_pack_unpack_all_reduce(n, esize, tensor_offset, bucket_offset):
+    rng = np.random.default_rng(n * 10 + esize)
+    numels = [int(k) for k in rng.integers(0, 20000, size=40)] + [1, 0, 3, 70001]
+    cap = 60000 * esize
+    plan, oplan, dt, host_t = bucket_case(n, numels, esize, cap, seed=5, bucket_offset=bucket_offset)
+    want_b = O.bucket_pack(oplan, host_t)
+    d_t = [[to_dev(x, dt, tensor_offset) if x.size else None for x in row] for row in host_t]
+    g_b = [[Guarded(int(k), dt, bucket_offset) for k in plan.bucket_numel] for _ in range(n)]
+    flat_t = [x if x is not None else 0 for row in d_t for x in row]
+    flat_b = [g.ptr() for row in g_b for g in row]
+    cr.cr_bucket_pack(plan, n, flat_t, flat_b)
+    torch.cuda.synchronize()
+    for r in range(n):
+        for b in range(plan.nbuckets):
+            g_b[r][b].check()
+            assert g_b[r][b].host().tobytes() == want_b[r][b].tobytes(), f"pack r={r} b={b}"
+    # all-reduce AVG per bucket, then unpack into fresh guarded tensors
+    cr.cr_bucket_all_reduce(plan, n, flat_b, dt, "avg")
+    want_t = O.bucketed_all_reduce(oplan, host_t, dt, "avg")
+    g_t = [[Guarded(int(k), dt, tensor_offset) for k in numels] for _ in range(n)]
+    cr.cr_bucket_unpack(plan, n, flat_b, [g.ptr() for row in g_t for g in row])
+    torch.cuda.synchronize()
+    for r in range(n):
+        for t in range(len(numels)):
+            g_t[r][t].check()
+            assert_match(g_t[r][t].host(), want_t[r][t], dt, f"unpack r={r} t={t}")
+
+
+@pytest.mark.parametrize("src_shift", range(16))
+@pytest.mark.parametrize("dst_shift", [0, 1, 6, 15])
+def test_bucket_copy_every_byte_alignment(src_shift, dst_shift):
+    """1-byte elements: source and destination misaligned by every amount
+    0..15 bytes (tensor offsets inside the bucket shift the destination
+    further), ranges shorter than, equal to and longer than one vector."""
+    numels = [1, 7, 8, 9, 15, 16, 17, 31, 33, 1000, 20000, 3]
+    plan = cr.cr_bucket_plan(numels, 1, 1 << 30)
+    oplan = O.bucket_plan(numels, 1, 1 << 30)
+    rng = np.random.default_rng(src_shift * 16 + dst_shift)
+    host = [rng.integers(0, 256, k).astype(np.uint8) for k in numels]
+    want = O.bucket_pack(oplan, [host])[0][0]
+    dev_t = []
+    for x in host:
+        base = torch.empty(x.size + src_shift, dtype=torch.uint8, device="cuda")
+        base[src_shift:].copy_(torch.from_numpy(x).cuda())
+        dev_t.append(base[src_shift:])
+    total = int(plan.bucket_numel[0])
+    G = 64
+    bbase = torch.full((total + 2 * G + dst_shift,), 0xA5, dtype=torch.uint8, device="cuda")
+    lo = G + dst_shift
+    cr.cr_bucket_pack(plan, 1, dev_t, [bbase[lo:lo + total]])
+    torch.cuda.synchronize()
+    h = bbase.cpu().numpy()
+    assert np.all(h[:lo] == 0xA5) and np.all(h[lo + total:] == 0xA5), "canary"
+    assert h[lo:lo + total].tobytes() == want.tobytes()
+    # and back out into fresh tensors shifted the other way
+    outs = []
+    for x in host:
+        base = torch.full((x.size + 2 * G + dst_shift,), 0x5A, dtype=torch.uint8, device="cuda")
+        outs.append((base, G + dst_shift, x.size))
+    cr.cr_bucket_unpack(plan, 1, [bbase[lo:lo + total]], [b[o:o + k] for b, o, k in outs])
+    torch.cuda.synchronize()
+    for (b, o, k), x in zip(outs, host):
+        hb = b.cpu().numpy()
+        assert np.all(hb[:o] == 0x5A) and np.all(hb[o + k:] == 0x5A), "canary"
+        assert hb[o:o + k].tobytes() == x.tobytes()
