@@ -44,7 +44,6 @@ if ROOT not in sys.path:
 
 METRIC = "effective HBM GB/s per collective call and % of GB300 HBM peak (1 GPU)"
 UNIT = "GB/s"
-HEADLINE = "allreduce_avg_bf16_8ranks_64MiB"
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -224,46 +223,236 @@ def ar_bytes(n, count, esize):
     return 2 * n * count * esize
 
 
+class Workload:
+    """One benchmarked call of the hot path: setup() allocates and fills the
+    inputs, step(stream) issues the call(s), nbytes is the algorithmic bytes
+    per step, launches the kernels one step launches."""
+    name = kernel = profile = ""
+    nbytes = 0
+    launches = 1
+
+    def setup(self, device):
+        raise NotImplementedError
+
+    def step(self, stream):
+        raise NotImplementedError
+
+    def teardown(self):
+        import torch
+        for k in list(vars(self)):
+            if k.startswith("t_"):
+                delattr(self, k)
+        torch.cuda.empty_cache()
+
+
+class AllReduce(Workload):
+    def __init__(self, n=8, count=1 << 25, dtype="bf16", op="avg", std=0.02):
+        self.n, self.count, self.dt, self.op, self.std = n, count, dtype, op, std
+        es = 2 if dtype == "bf16" else 4
+        self.nbytes = ar_bytes(n, count, es)
+        mib = count * es >> 20
+        self.name = f"allreduce_{op}_{dtype}_{n}ranks_{mib}MiB"
+        self.kernel = f"k_fold_vec<{dtype},{dtype},AR,{n}>"
+        self.profile = f"k_fold_vec_allreduce_{dtype}_{n}x{mib}MiB"
+
+    def setup(self, device):
+        import torch
+        td = torch.bfloat16 if self.dt == "bf16" else torch.float32
+        self.t_bufs = alloc_ranks(self.n, self.count, td, self.std, 0, device)
+
+    def step(self, stream):
+        from fsdp_emulated_ranks_gb300 import cr
+        cr.cr_all_reduce(self.t_bufs, self.count, self.dt, self.op, self.t_bufs, self.dt, stream)
+
+
+class ReduceScatter(Workload):
+    def __init__(self, n=8, count=1 << 25):
+        self.n, self.count = n, count
+        self.nbytes = n * count * 2 + count * 2
+        self.name = f"reduce_scatter_avg_bf16_{n}ranks_{count * 2 >> 20}MiB"
+        self.kernel = f"k_fold_vec<bf16,bf16,RS,{n}>"
+        self.profile = f"k_fold_vec_reduce_scatter_bf16_{n}x{count * 2 >> 20}MiB"
+
+    def setup(self, device):
+        import torch
+        self.t_bufs = alloc_ranks(self.n, self.count, torch.bfloat16, 0.02, 0, device)
+        L = self.count // self.n
+        self.t_shards = [torch.empty(L, dtype=torch.bfloat16, device=device) for _ in range(self.n)]
+
+    def step(self, stream):
+        from fsdp_emulated_ranks_gb300 import cr
+        cr.cr_reduce_scatter(self.t_bufs, self.count, "bf16", "avg", self.t_shards, "bf16", stream)
+
+
+class AllGather(Workload):
+    def __init__(self, n=8, count=1 << 25):
+        self.n, self.count = n, count
+        self.nbytes = count * 2 + n * count * 2
+        self.name = f"all_gather_bf16_{n}ranks_{count * 2 >> 20}MiB"
+        self.kernel = "k_gather_vec<2>"
+        self.profile = f"k_gather_vec_all_gather_bf16_{n}x{count * 2 >> 20}MiB"
+
+    def setup(self, device):
+        import torch
+        L = self.count // self.n
+        self.t_shards = alloc_ranks(self.n, L, torch.bfloat16, 0.02, 0, device)
+        self.t_bufs = [torch.empty(self.count, dtype=torch.bfloat16, device=device)
+                       for _ in range(self.n)]
+
+    def step(self, stream):
+        from fsdp_emulated_ranks_gb300 import cr
+        cr.cr_all_gather(self.t_shards, self.count, "bf16", self.t_bufs, stream)
+
+
+class Buckets(Workload):
+    """DDP bucket fusion: 300 bf16 tensors per rank (log-uniform numel,
+    seed 7), 25 MiB buckets; mode pack, allreduce, unpack or pipeline."""
+
+    def __init__(self, mode="pipeline", n=8, ntensors=300):
+        from fsdp_emulated_ranks_gb300 import inputs as I
+        self.mode, self.n = mode, n
+        self.numels = [int(k) for k in I.bucket_numels()][:ntensors]
+        self.P = sum(self.numels)
+        one = 2 * 2 * self.P * n
+        self.nbytes = 3 * one if mode == "pipeline" else one
+        self.name = f"ddp_bucket_{mode}_bf16_{n}ranks_{ntensors}tensors"
+        self.kernel = "k_fold_vec<bf16,bf16,AR,8>" if mode == "allreduce" else "k_copy_segments"
+        self.profile = (f"k_fold_vec_bucket_allreduce_bf16_{n}x{ntensors}" if mode == "allreduce"
+                        else f"k_copy_segments_bucket_{mode}_bf16_{n}x{ntensors}")
+
+    def setup(self, device):
+        import torch
+        from fsdp_emulated_ranks_gb300 import cr
+        from fsdp_emulated_ranks_gb300 import inputs as I
+        n = self.n
+        self.plan = cr.cr_bucket_plan(self.numels, 2, 25 * 1024 * 1024)
+        copies = -(-n * len(self.numels) // 1024)
+        self.launches = {"pack": copies, "unpack": copies, "allreduce": self.plan.nbuckets,
+                         "pipeline": 2 * copies + self.plan.nbuckets}[self.mode]
+        tens = []
+        for r in range(n):
+            flat = torch.empty(self.P + 128 * len(self.numels), dtype=torch.bfloat16, device=device)
+            I.torch_fill_normal_(flat, 1e-3, 1000 + r)
+            off, row_t = 0, []
+            for k in self.numels:
+                row_t.append(flat[off:off + k])
+                off += (k + 127) // 128 * 128
+            tens.append(row_t)
+        bks = []
+        for r in range(n):
+            sizes = [(int(k) + 127) // 128 * 128 for k in self.plan.bucket_numel]
+            flat = torch.empty(sum(sizes), dtype=torch.bfloat16, device=device)
+            off, row_b = 0, []
+            for k, sz in zip(self.plan.bucket_numel, sizes):
+                row_b.append(flat[off:off + int(k)])
+                off += sz
+            bks.append(row_b)
+        self.t_flat_t = [x for rr in tens for x in rr]
+        self.t_flat_b = [x for rr in bks for x in rr]
+
+    def step(self, stream):
+        from fsdp_emulated_ranks_gb300 import cr
+        n = self.n
+        if self.mode in ("pack", "pipeline"):
+            cr.cr_bucket_pack(self.plan, n, self.t_flat_t, self.t_flat_b, stream)
+        if self.mode in ("allreduce", "pipeline"):
+            cr.cr_bucket_all_reduce(self.plan, n, self.t_flat_b, "bf16", "avg", stream)
+        if self.mode in ("unpack", "pipeline"):
+            cr.cr_bucket_unpack(self.plan, n, self.t_flat_b, self.t_flat_t, stream)
+
+
+class FsdpStep(Workload):
+    """Fused FSDP step: 8 ranks, flat `count` params (1.3e9 by default)."""
+
+    def __init__(self, n=8, count=1_300_000_000):
+        self.n, self.count = n, count
+        self.nbytes = (4 * n + 24) * count
+        tag = f"{count / 1e9:g}e9" if count >= 10 ** 8 else str(count)
+        self.name = f"fsdp_step_bf16_{n}ranks_{tag}params"
+        self.kernel = f"k_fsdp_vec<{n}>"
+        self.profile = f"k_fsdp_vec_fsdp_step_{n}x{tag}"
+
+    def setup(self, device):
+        import torch
+        from fsdp_emulated_ranks_gb300 import cr
+        from fsdp_emulated_ranks_gb300 import inputs as I
+        n, count = self.n, self.count
+        L = cr.cr_chunk_len(count, n)
+        self.t_grads = alloc_ranks(n, count, torch.bfloat16, 1e-3, 1000, device)
+        self.t_params = [torch.empty(count, dtype=torch.bfloat16, device=device) for _ in range(n)]
+        self.t_master_full = torch.empty(count, dtype=torch.float32, device=device)
+        I.torch_fill_normal_(self.t_master_full, 0.02, 2000)
+        self.t_mv = torch.zeros(2 * count, dtype=torch.float32, device=device)
+        self.t_master = [self.t_master_full[j * L:(j + 1) * L] for j in range(n)]
+        self.t_m = [self.t_mv[j * L:(j + 1) * L] for j in range(n)]
+        self.t_v = [self.t_mv[count + j * L:count + (j + 1) * L] for j in range(n)]
+        self.cfg = cr.adamw_cfg()
+
+    def step(self, stream):
+        from fsdp_emulated_ranks_gb300 import cr
+        cr.cr_fsdp_step(self.t_grads, self.count, self.t_master, self.t_m, self.t_v, self.cfg,
+                        self.t_params, stream)
+
+
+def make_workload(name, args):
+    if name == "allreduce":
+        return AllReduce()
+    if name == "allreduce_f32":
+        return AllReduce(n=4, count=1 << 20, dtype="f32", op="sum", std=1.0)
+    if name == "reduce_scatter":
+        return ReduceScatter()
+    if name == "all_gather":
+        return AllGather()
+    if name.startswith("bucket_"):
+        return Buckets(mode=name[len("bucket_"):], ntensors=args.bucket_ntensors)
+    if name == "fsdp":
+        return FsdpStep(count=args.fsdp_count)
+    raise SystemExit(f"unknown workload {name}")
+
+
+ROW_WORKLOADS = ["reduce_scatter", "all_gather", "allreduce_f32", "bucket_pack",
+                 "bucket_allreduce", "bucket_unpack", "bucket_pipeline", "fsdp"]
+
+
 def run_headline(args, world, rank, device, stream, peak):
     import torch
-    from fsdp_emulated_ranks_gb300 import cr
-    n, count = 8, 1 << 25
-    bufs = alloc_ranks(n, count, torch.bfloat16, 0.02, 0, device)
-    # Sample for the CPU baseline before the in-place calls overwrite it.
+    wl = make_workload(args.workload, args)
+    wl.setup(device)
+    # Sample for the CPU baseline before in-place calls overwrite the inputs.
     sample = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sample = [b[:args.cpu_sample].view(torch.int16).cpu().numpy().view("uint16") for b in bufs]
-
-    def step():
-        cr.cr_all_reduce(bufs, count, "bf16", "avg", bufs, "bf16", stream)
-
+    if (rank == 0 and world == 1 and not args.no_cpu_baseline and isinstance(wl, AllReduce)
+            and wl.dt == "bf16"):
+        k = min(args.cpu_sample, wl.count)
+        sample = [b[:k].view(torch.int16).cpu().numpy().view("uint16") for b in wl.t_bufs]
     sampler = ClockSampler(device)
-    total_ms, per = timed(step, args.steps, args.warmup, world, stream, sampler)
-    nbytes = ar_bytes(n, count, 2)
-    value, ms_step = job_throughput(nbytes, total_ms, args.steps, world, device)
+    total_ms, per = timed(lambda: wl.step(stream), args.steps, args.warmup, world, stream, sampler)
+    value, ms_step = job_throughput(wl.nbytes, total_ms, args.steps, world, device)
     kern_ms = statistics.mean(per)
-    achieved = nbytes / (kern_ms * 1e-3) / 1e9
+    achieved = wl.nbytes / (kern_ms * 1e-3) / 1e9
     out = {
+        "workload": wl,
         "ms_per_step": ms_step,
         "value": value,
         "clocks": sampler.summary(),
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * wl.launches,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak[0],
                      "unit": "GB/s", "frac": round(achieved / peak[0], 4),
-                     "traffic": traffic_per_launch("k_fold_vec_allreduce_bf16_8x64MiB"),
-                     "kernel": "k_fold_vec<bf16,bf16,AR,8>",
-                     "algorithmic_bytes_per_launch": nbytes,
-                     "peak_source": peak[1],
-                     "kernel_ms_median": statistics.median(per)},
+                     "traffic": traffic_per_launch(wl.profile, wl.launches),
+                     "kernel": wl.kernel, "algorithmic_bytes_per_launch": wl.nbytes // wl.launches,
+                     "peak_source": peak[1], "step_ms_median": statistics.median(per)},
     }
-    # End to end through the C ABI from pinned host memory.
-    out["e2e"] = None if args.no_e2e else run_e2e(args, bufs, n, count, world, stream, device)
-    del bufs
-    torch.cuda.empty_cache()
+    out["e2e"] = None
+    if isinstance(wl, AllReduce) and not args.no_e2e:
+        out["e2e"] = run_e2e(args, wl.t_bufs, wl.n, wl.count, world, stream, device)
+    wl.teardown()
     return out, sample
 
 
 def run_e2e(args, bufs, n, count, world, stream, device):
+    """End to end through the C ABI from pinned host memory: every step
+    uploads the 8 rank inputs, all-reduces and downloads the 8 results, in
+    slices pipelined over an upload stream, the compute stream and a
+    download stream (cr_all_reduce_staged)."""
     import torch
     from fsdp_emulated_ranks_gb300 import cr
     host_in = [torch.empty(count, dtype=torch.bfloat16, pin_memory=True) for _ in range(n)]
@@ -271,13 +460,11 @@ def run_e2e(args, bufs, n, count, world, stream, device):
     for h, b in zip(host_in, bufs):
         h.copy_(b)
     torch.cuda.synchronize()
+    up, down = torch.cuda.Stream(device), torch.cuda.Stream(device)
 
     def step():
-        for h, b in zip(host_in, bufs):
-            b.copy_(h, non_blocking=True)
-        cr.cr_all_reduce(bufs, count, "bf16", "avg", bufs, "bf16", stream)
-        for h, b in zip(host_out, bufs):
-            h.copy_(b, non_blocking=True)
+        cr.cr_all_reduce_staged(host_in, host_out, bufs, count, "bf16", "avg",
+                                args.e2e_slice, stream, up, down)
 
     steps = max(3, min(args.steps, 50))
     total_ms, _ = timed(step, steps, max(3, min(args.warmup, 5)), world, stream)
@@ -285,14 +472,15 @@ def run_e2e(args, bufs, n, count, world, stream, device):
     value, ms = job_throughput(nbytes, total_ms, steps, world, device)
     return {"value": round(value, 2), "unit": UNIT,
             "h2d_bytes_per_step": n * count * 2, "d2h_bytes_per_step": n * count * 2,
-            "ms_per_step": ms, "steps": steps}
+            "ms_per_step": ms, "steps": steps, "api": "cr_all_reduce_staged",
+            "slice_elems": args.e2e_slice or "auto"}
 
 
-def traffic_per_launch(name):
+def traffic_per_launch(name, launches=1):
     """DRAM bytes per launch from the committed ncu summary of this kernel,
     or None if absent or taken on a different build of the library."""
     p = os.path.join(ROOT, "profiles", name + ".md")
-    if not os.path.exists(p):
+    if not os.path.exists(p) or launches != 1:
         return None
     vals = {}
     with open(p) as f:
@@ -311,122 +499,41 @@ def traffic_per_launch(name):
 
 # ---- the other rows (N = 1) ------------------------------------------------------------
 
-def row(name, nbytes, per, peak, launches):
-    ms = statistics.mean(per) if per else float("nan")
-    gbs = nbytes / (ms * 1e-3) / 1e9
-    return {"name": name, "ms": round(ms, 4), "GB/s": round(gbs, 1),
-            "frac": round(gbs / peak[0], 4), "algorithmic_bytes": nbytes,
-            "launches_per_call": launches}
-
-
-def run_rows(args, device, stream, peak):
-    import torch
-    from fsdp_emulated_ranks_gb300 import cr
-    from fsdp_emulated_ranks_gb300 import inputs as I
+def run_rows(args, device, stream, peak, skip=None):
     rows = []
-    K, W = args.row_steps, 3
-
-    # a1-a5 on the headline size: reduce-scatter, all-gather.
-    n, count = 8, 1 << 25
-    bufs = alloc_ranks(n, count, torch.bfloat16, 0.02, 0, device)
-    L = count // n
-    shards = [torch.empty(L, dtype=torch.bfloat16, device=device) for _ in range(n)]
-    _, per = timed(lambda: cr.cr_reduce_scatter(bufs, count, "bf16", "avg", shards, "bf16", stream),
-                   K, W, 1, stream)
-    rows.append(row("reduce_scatter_avg_bf16_8x64MiB", n * count * 2 + count * 2, per, peak, 1))
-    _, per = timed(lambda: cr.cr_all_gather(shards, count, "bf16", bufs, stream), K, W, 1, stream)
-    rows.append(row("all_gather_bf16_8x64MiB", count * 2 + n * count * 2, per, peak, 1))
-    del bufs, shards
-    torch.cuda.empty_cache()
-
-    # all-reduce SUM fp32, 4 ranks x 2^20 (fits in L2: latency regime).
-    n, count = 4, 1 << 20
-    bufs = alloc_ranks(n, count, torch.float32, 1.0, 0, device)
-    _, per = timed(lambda: cr.cr_all_reduce(bufs, count, "f32", "sum", bufs, "f32", stream),
-                   K, W, 1, stream)
-    rows.append(row("allreduce_sum_f32_4x4MiB", ar_bytes(n, count, 4), per, peak, 1))
-    del bufs
-    torch.cuda.empty_cache()
-
-    # a6/a7: DDP buckets, 300 bf16 tensors per rank, 25 MiB buckets.
-    n = 8
-    numels = [int(k) for k in I.bucket_numels()]
-    P = sum(numels)
-    plan = cr.cr_bucket_plan(numels, 2, 25 * 1024 * 1024)
-    tens = []
-    for r in range(n):
-        flat = torch.empty(P + 128 * len(numels), dtype=torch.bfloat16, device=device)
-        I.torch_fill_normal_(flat, 1e-3, 1000 + r)
-        off, row_t = 0, []
-        for k in numels:
-            row_t.append(flat[off:off + k])
-            off += (k + 127) // 128 * 128
-        tens.append(row_t)
-    bks = []
-    for r in range(n):
-        sizes = [(int(k) + 127) // 128 * 128 for k in plan.bucket_numel]
-        flat = torch.empty(sum(sizes), dtype=torch.bfloat16, device=device)
-        off, row_b = 0, []
-        for k, s in zip(plan.bucket_numel, sizes):
-            row_b.append(flat[off:off + int(k)])
-            off += s
-        bks.append(row_b)
-    flat_t = [x for rr in tens for x in rr]
-    flat_b = [x for rr in bks for x in rr]
-    copy_launches = -(-n * len(numels) // 1024)
-    _, per = timed(lambda: cr.cr_bucket_pack(plan, n, flat_t, flat_b, stream), K, W, 1, stream)
-    rows.append(row("bucket_pack_bf16_8x300", 2 * 2 * P * n, per, peak, copy_launches))
-    _, per = timed(lambda: cr.cr_bucket_all_reduce(plan, n, flat_b, "bf16", "avg", stream), K, W, 1,
-                   stream)
-    rows.append(row("bucket_allreduce_avg_bf16_8x300", 2 * 2 * P * n, per, peak, plan.nbuckets))
-    _, per = timed(lambda: cr.cr_bucket_unpack(plan, n, flat_b, flat_t, stream), K, W, 1, stream)
-    rows.append(row("bucket_unpack_bf16_8x300", 2 * 2 * P * n, per, peak, copy_launches))
-
-    def pipeline():
-        cr.cr_bucket_pack(plan, n, flat_t, flat_b, stream)
-        cr.cr_bucket_all_reduce(plan, n, flat_b, "bf16", "avg", stream)
-        cr.cr_bucket_unpack(plan, n, flat_b, flat_t, stream)
-    _, per = timed(pipeline, max(3, K // 2), W, 1, stream)
-    rows.append(row("ddp_bucket_pipeline_bf16_8x300", 3 * 2 * 2 * P * n, per, peak,
-                    2 * copy_launches + plan.nbuckets))
-    rows[-1]["total_params"] = P
-    rows[-1]["nbuckets"] = plan.nbuckets
-    del tens, bks, flat_t, flat_b
-    torch.cuda.empty_cache()
-
-    # a8-a10: fused FSDP step, 8 ranks, flat 1.3e9 parameters.
-    if not args.skip_fsdp:
-        n, count = 8, 1_300_000_000
-        L = count // n
-        grads = alloc_ranks(n, count, torch.bfloat16, 1e-3, 1000, device)
-        params = [torch.empty(count, dtype=torch.bfloat16, device=device) for _ in range(n)]
-        master_full = torch.empty(count, dtype=torch.float32, device=device)
-        I.torch_fill_normal_(master_full, 0.02, 2000)
-        master = [master_full[j * L:(j + 1) * L] for j in range(n)]
-        mv = torch.zeros(2 * count, dtype=torch.float32, device=device)
-        m = [mv[j * L:(j + 1) * L] for j in range(n)]
-        v = [mv[count + j * L:count + (j + 1) * L] for j in range(n)]
-        cfg = cr.adamw_cfg()
-        _, per = timed(lambda: cr.cr_fsdp_step(grads, count, master, m, v, cfg, params, stream),
-                       max(3, K // 4), W, 1, stream)
-        rows.append(row("fsdp_step_bf16_8x1.3e9", (4 * n + 24) * count, per, peak, 1))
-        del grads, params, master_full, master, mv, m, v
-        torch.cuda.empty_cache()
+    for name in ROW_WORKLOADS:
+        if (name == "fsdp" and args.skip_fsdp) or name == skip:
+            continue
+        wl = make_workload(name, args)
+        wl.setup(device)
+        steps = args.row_steps if wl.nbytes < (8 << 30) else max(3, args.row_steps // 4)
+        _, per = timed(lambda: wl.step(stream), steps, 3, 1, stream)
+        ms = statistics.mean(per)
+        gbs = wl.nbytes / (ms * 1e-3) / 1e9
+        rows.append({"name": wl.name, "ms": round(ms, 4), "GB/s": round(gbs, 1),
+                     "frac": round(gbs / peak[0], 4), "algorithmic_bytes": wl.nbytes,
+                     "launches_per_call": wl.launches, "kernel": wl.kernel})
+        wl.teardown()
     return rows
 
 
 # ---- CPU oracle -------------------------------------------------------------------------
 
-def cpu_oracle_allreduce(sample):
+def cpu_oracle_allreduce(sample, min_seconds):
     """Ring all-reduce AVG of the sampled bf16 rank buffers by the CPU oracle
-    (single-threaded); returns (GB/s, seconds)."""
+    (single-threaded), repeated until at least `min_seconds` of CPU work;
+    returns (GB/s, seconds, passes)."""
     import oracle as O
     n, count = len(sample), sample[0].size
-    O.ring_all_reduce(sample[:2], "bf16", "avg")  # load and warm the library
-    t0 = time.perf_counter()
-    O.ring_all_reduce(sample, "bf16", "avg")
-    dt = time.perf_counter() - t0
-    return ar_bytes(n, count, 2) / dt / 1e9, dt
+    O.ring_all_reduce([x[:1024] for x in sample], "bf16", "avg")  # load the library
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        O.ring_all_reduce(sample, "bf16", "avg")
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds or passes >= 1000:
+            break
+    return passes * ar_bytes(n, count, 2) / dt / 1e9, dt, passes
 
 
 def run_reference(args):
@@ -454,7 +561,7 @@ def run_reference(args):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32 accumulate, bf16 in/out",
-            "data": "synthetic", "config": {"workload": HEADLINE, "ranks": 8,
+            "data": "synthetic", "config": {"workload": AllReduce().name, "ranks": 8,
                                             "elements_per_rank": 1 << 25,
                                             "sampled_elements_per_rank": count},
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1,
@@ -512,14 +619,23 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--workload", default="allreduce",
+                    help="timed workload: allreduce (headline), allreduce_f32, reduce_scatter, "
+                         "all_gather, bucket_{pack,allreduce,unpack,pipeline}, fsdp")
+    ap.add_argument("--fsdp-count", type=int, default=1_300_000_000)
+    ap.add_argument("--bucket-ntensors", type=int, default=300)
     ap.add_argument("--no-rows", action="store_true")
     ap.add_argument("--skip-fsdp", action="store_true")
     ap.add_argument("--row-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--cpu-sample", type=int, default=1 << 24,
+    ap.add_argument("--e2e-slice", type=int, default=0,
+                    help="elements per slice of the pipelined host all-reduce (0: auto)")
+    ap.add_argument("--cpu-sample", type=int, default=1 << 25,
                     help="elements per rank the CPU oracle reduces for cpu_baseline")
-    ap.add_argument("--ref-sample", type=int, default=1 << 21,
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="minimum CPU time of the cpu_baseline measurement")
+    ap.add_argument("--ref-sample", type=int, default=1 << 22,
                     help="elements per rank per step for --impl reference")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
@@ -553,27 +669,37 @@ def main(argv=None):
         return 0
 
     head, sample = run_headline(args, world, rank, device, stream, peak)
+    wl = head["workload"]
     rows = None
     if world == 1 and not args.no_rows:
-        rows = run_rows(args, device, stream, peak)
+        rows = run_rows(args, device, stream, peak, skip=args.workload)
     cpu = None
     if sample is not None:
-        gbs, secs = cpu_oracle_allreduce(sample)
+        gbs, secs, passes = cpu_oracle_allreduce(sample, args.cpu_seconds)
+        frac = (1 << 25) // sample[0].size
         cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": (f"ring all-reduce AVG of the first {sample[0].size} elements of each "
-                          f"of the 8 rank buffers (1/{(1 << 25) // sample[0].size} of the "
-                          f"workload), single-threaded C oracle, {secs:.1f} s, host has "
+               "sample": (f"{passes} pass(es) of the ring all-reduce AVG over the first "
+                          f"{sample[0].size} elements of each of the 8 rank buffers "
+                          f"({'all' if frac == 1 else '1/%d' % frac} of the workload's bytes), "
+                          f"single-threaded C oracle, {secs:.1f} s; host has "
                           f"{os.cpu_count()} cores")}
     if rank == 0:
+        config = {"workload": wl.name, "parallelism": f"{world} GPU(s) x {wl.n} emulated ranks each"}
+        if isinstance(wl, AllReduce):
+            config.update({"ranks": wl.n, "elements_per_rank": wl.count, "dtype_in_out": wl.dt,
+                           "accumulate": "fp32, ring order" if wl.dt != "i32" else "int32",
+                           "op": f"{wl.op}, in place",
+                           "l2": ("inputs exceed the 129 MB L2, no flush" if wl.nbytes // 2 > (129 << 20)
+                                  else "inputs fit in L2 (latency regime), no flush")})
+        else:
+            config["algorithmic_bytes_per_step"] = wl.nbytes
+            config["l2"] = "inputs exceed the 129 MB L2, no flush"
         line = {"metric": METRIC, "value": round(head["value"], 1), "unit": UNIT,
                 "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": head["ms_per_step"], "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                 "data": "synthetic",
-                "config": {"workload": HEADLINE, "ranks": 8, "elements_per_rank": 1 << 25,
-                           "dtype_in_out": "bf16", "accumulate": "fp32, ring order",
-                           "op": "avg, in place", "l2": "inputs 512 MiB > 129 MB L2, no flush",
-                           "parallelism": f"{world} GPU(s) x 8 emulated ranks each"},
+                "config": config,
                 "roofline": head["roofline"], "cpu_baseline": cpu, "e2e": head["e2e"],
                 "gpu_launches": head["gpu_launches"], "clocks": head["clocks"],
                 "frac_of_peak": round(head["value"] / world / peak[0], 4),

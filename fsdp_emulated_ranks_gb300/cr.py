@@ -30,9 +30,9 @@ STATUS = {0: "CR_OK", 1: "CR_ERR_INVALID_ARG", 2: "CR_ERR_UNSUPPORTED",
 # Every symbol include/cr.h declares.
 EXPORTS = ["cr_status_string", "cr_last_error", "cr_version", "cr_chunk_len",
            "cr_shard_range", "cr_reduce_scatter", "cr_all_gather",
-           "cr_all_reduce", "cr_bucket_plan", "cr_bucket_plan_free",
+           "cr_all_reduce", "cr_all_reduce_staged", "cr_bucket_plan", "cr_bucket_plan_free",
            "cr_bucket_pack", "cr_bucket_unpack", "cr_bucket_all_reduce",
-           "cr_fsdp_step", "cr_adamw_step", "cr_comm_elems"]
+           "cr_bucket_all_reduce_fused", "cr_fsdp_step", "cr_adamw_step", "cr_comm_elems"]
 
 _lib = None
 
@@ -80,12 +80,14 @@ def lib() -> C.CDLL:
     L.cr_reduce_scatter.argtypes = [vp, i, sz, i, i, vp, i, vp]
     L.cr_all_gather.argtypes = [vp, i, sz, i, vp, vp]
     L.cr_all_reduce.argtypes = [vp, i, sz, i, i, vp, i, vp]
+    L.cr_all_reduce_staged.argtypes = [vp, vp, vp, i, sz, i, i, sz, vp, vp, vp]
     L.cr_bucket_plan.argtypes = [vp, i, sz, sz, C.POINTER(C.POINTER(BucketPlanT))]
     L.cr_bucket_plan_free.restype = None
     L.cr_bucket_plan_free.argtypes = [C.POINTER(BucketPlanT)]
     L.cr_bucket_pack.argtypes = [C.POINTER(BucketPlanT), i, vp, vp, vp]
     L.cr_bucket_unpack.argtypes = [C.POINTER(BucketPlanT), i, vp, vp, vp]
     L.cr_bucket_all_reduce.argtypes = [C.POINTER(BucketPlanT), i, vp, i, i, vp]
+    L.cr_bucket_all_reduce_fused.argtypes = [C.POINTER(BucketPlanT), i, vp, i, i, vp]
     L.cr_fsdp_step.argtypes = [vp, i, sz, vp, vp, vp, C.POINTER(AdamWCfg), vp, vp]
     L.cr_adamw_step.argtypes = [sz, vp, vp, vp, vp, C.POINTER(AdamWCfg), vp, vp]
     L.cr_comm_elems.argtypes = [i, i, i, sz, i, C.POINTER(C.c_uint64),
@@ -180,6 +182,18 @@ def cr_all_reduce(inbufs, count, in_dtype, op, outbufs, out_dtype,
            "cr_all_reduce")
 
 
+def cr_all_reduce_staged(host_in, host_out, dev_bufs, count, dtype, op,
+                         slice_elems=0, compute_stream=None, h2d_stream=None,
+                         d2h_stream=None) -> None:
+    sc = _stream(compute_stream)
+    sh = sc if h2d_stream is None else _stream(h2d_stream)
+    sd = sc if d2h_stream is None else _stream(d2h_stream)
+    _check(lib().cr_all_reduce_staged(_ptr_array(host_in), _ptr_array(host_out),
+                                      _ptr_array(dev_bufs), len(dev_bufs), count,
+                                      _dtype(dtype), _op(op), slice_elems, sc, sh, sd),
+           "cr_all_reduce_staged")
+
+
 class BucketPlan:
     """Owns a cr_bucket_plan_t; freed with cr_bucket_plan_free."""
 
@@ -231,6 +245,13 @@ def cr_bucket_all_reduce(plan: BucketPlan, nranks: int, buckets, dtype, op,
     _check(lib().cr_bucket_all_reduce(plan.ptr, nranks, _ptr_array(buckets),
                                       _dtype(dtype), _op(op), _stream(stream)),
            "cr_bucket_all_reduce")
+
+
+def cr_bucket_all_reduce_fused(plan: BucketPlan, nranks: int, tensors, dtype, op,
+                               stream=None) -> None:
+    _check(lib().cr_bucket_all_reduce_fused(plan.ptr, nranks, _ptr_array(tensors),
+                                            _dtype(dtype), _op(op), _stream(stream)),
+           "cr_bucket_all_reduce_fused")
 
 
 def adamw_cfg(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01,

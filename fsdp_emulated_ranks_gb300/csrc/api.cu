@@ -6,6 +6,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <vector>
 
 #include "cr_internal.cuh"
@@ -120,6 +121,16 @@ cr_status check_overlaps(const std::vector<Span>& spans, Allow allow) {
   return CR_OK;
 }
 
+// Many buffers, none of which may overlap another: sort by start address.
+cr_status check_disjoint(std::vector<Span> spans) {
+  std::sort(spans.begin(), spans.end(), [](const Span& x, const Span& y) { return x.a < y.a; });
+  for (size_t k = 1; k < spans.size(); ++k)
+    if (spans[k].a < spans[k - 1].b)
+      return fail(CR_ERR_INVALID_ARG, "buffer %d overlaps buffer %d", spans[k].rank,
+                  spans[k - 1].rank);
+  return CR_OK;
+}
+
 Span span_of(const void* p, uint64_t bytes, int kind, int rank) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(p);
   return Span{a, a + bytes, kind, rank};
@@ -185,6 +196,8 @@ cr_status all_reduce_impl(const void* const* in, int nranks, size_t count,
   }
   a.count = count;
   a.L = (count + nranks - 1) / nranks;
+  a.begin = 0;
+  a.end = count;
   a.n = nranks;
   a.avg = op == CR_AVG;
   a.inv_n = exact_inv_n(nranks);
@@ -267,6 +280,8 @@ cr_status cr_reduce_scatter(const void* const* bufs, int nranks, size_t count,
   }
   a.count = count;
   a.L = L;
+  a.begin = 0;
+  a.end = count;
   a.n = nranks;
   a.avg = op == CR_AVG;
   a.inv_n = exact_inv_n(nranks);
@@ -326,6 +341,106 @@ cr_status cr_all_reduce(const void* const* in, int nranks, size_t count,
                         cr_dtype out_dtype, cr_stream_t stream) {
   return all_reduce_impl(in, nranks, count, in_dtype, op, out, out_dtype,
                          (cudaStream_t)stream);
+}
+
+cr_status cr_all_reduce_staged(const void* const* host_in, void* const* host_out,
+                               void* const* dev_bufs, int nranks, size_t count,
+                               cr_dtype dtype, cr_op op, size_t slice_elems,
+                               cr_stream_t compute_stream, cr_stream_t h2d_stream,
+                               cr_stream_t d2h_stream) {
+  cr_status st = check_common(nranks, count, host_in, dev_bufs);
+  if (st) return st;
+  if (!host_out) return fail(CR_ERR_INVALID_ARG, "host_out is NULL");
+  if ((st = check_pair(dtype, op, dtype))) return st;
+  const size_t es = esize_of(dtype);
+  std::vector<Span> dev_spans, out_spans;
+  bool vec = true;
+  for (int r = 0; r < nranks; ++r) {
+    if ((st = check_buf(host_in[r], count, es, "host_in", r))) return st;
+    if ((st = check_buf(host_out[r], count, es, "host_out", r))) return st;
+    if ((st = check_buf(dev_bufs[r], count, es, "dev_bufs", r))) return st;
+    if (count) {
+      dev_spans.push_back(span_of(dev_bufs[r], count * es, 1, r));
+      out_spans.push_back(span_of(host_out[r], count * es, 1, r));
+      vec = vec && aligned(dev_bufs[r], 16);
+    }
+  }
+  auto never = [](const Span&, const Span&) { return false; };
+  if ((st = check_overlaps(dev_spans, never))) return st;
+  if ((st = check_overlaps(out_spans, never))) return st;
+  if (count == 0) return ok();
+
+  const cudaStream_t sc = (cudaStream_t)compute_stream, sh = (cudaStream_t)h2d_stream,
+                     sd = (cudaStream_t)d2h_stream;
+  uint64_t slice = slice_elems;
+  if (slice == 0) {
+    slice = (count + 15) / 16;
+    if (slice < (1u << 18)) slice = 1u << 18;
+  }
+  slice = (slice + 63) / 64 * 64;
+  const uint64_t nslices = (count + slice - 1) / slice;
+
+  FoldArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int r = 0; r < nranks; ++r) {
+    a.in[r] = dev_bufs[r];
+    a.out[r] = dev_bufs[r];
+  }
+  a.count = count;
+  a.L = (count + nranks - 1) / nranks;
+  a.n = nranks;
+  a.avg = op == CR_AVG;
+  a.inv_n = exact_inv_n(nranks);
+
+  // Events are released with cudaEventDestroy right after being waited on;
+  // the runtime frees each once it has completed.
+  std::vector<cudaEvent_t> events;
+  auto new_event = [&](cudaEvent_t* ev) -> cudaError_t {
+    cudaError_t e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    if (e == cudaSuccess) events.push_back(*ev);
+    return e;
+  };
+  auto release = [&]() {
+    for (cudaEvent_t ev : events) cudaEventDestroy(ev);
+    events.clear();
+  };
+  cudaError_t e = cudaSuccess;
+  cudaEvent_t ev_start;
+  if ((e = new_event(&ev_start)) != cudaSuccess) return cuda_fail(e, "staged: event");
+  e = cudaEventRecord(ev_start, sc);
+  if (e == cudaSuccess && sh != sc) e = cudaStreamWaitEvent(sh, ev_start, 0);
+  if (e == cudaSuccess && sd != sc) e = cudaStreamWaitEvent(sd, ev_start, 0);
+  for (uint64_t k = 0; k < nslices && e == cudaSuccess; ++k) {
+    const uint64_t lo = k * slice, hi = lo + slice < count ? lo + slice : count;
+    const size_t off = lo * es, bytes = (hi - lo) * es;
+    for (int r = 0; r < nranks && e == cudaSuccess; ++r)
+      e = cudaMemcpyAsync(static_cast<unsigned char*>(dev_bufs[r]) + off,
+                          static_cast<const unsigned char*>(host_in[r]) + off, bytes,
+                          cudaMemcpyHostToDevice, sh);
+    cudaEvent_t ev_in, ev_out;
+    if (e == cudaSuccess) e = new_event(&ev_in);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_in, sh);
+    if (e == cudaSuccess && sc != sh) e = cudaStreamWaitEvent(sc, ev_in, 0);
+    if (e == cudaSuccess) {
+      a.begin = lo;
+      a.end = hi;
+      e = launch_fold(dtype, dtype, kAR, a, vec, sc);
+    }
+    if (e == cudaSuccess) e = new_event(&ev_out);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_out, sc);
+    if (e == cudaSuccess && sd != sc) e = cudaStreamWaitEvent(sd, ev_out, 0);
+    for (int r = 0; r < nranks && e == cudaSuccess; ++r)
+      e = cudaMemcpyAsync(static_cast<unsigned char*>(host_out[r]) + off,
+                          static_cast<const unsigned char*>(dev_bufs[r]) + off, bytes,
+                          cudaMemcpyDeviceToHost, sd);
+  }
+  cudaEvent_t ev_done;
+  if (e == cudaSuccess) e = new_event(&ev_done);
+  if (e == cudaSuccess) e = cudaEventRecord(ev_done, sd);
+  if (e == cudaSuccess && sc != sd) e = cudaStreamWaitEvent(sc, ev_done, 0);
+  release();
+  if (e != cudaSuccess) return cuda_fail(e, "all_reduce_staged");
+  return ok();
 }
 
 cr_status cr_fsdp_step(const void* const* grads_bf16, int nranks, size_t count,
@@ -519,6 +634,68 @@ cr_status cr_bucket_all_reduce(const cr_bucket_plan_t* plan, int nranks,
                          (cudaStream_t)stream);
     if (st) return st;
   }
+  return ok();
+}
+
+cr_status cr_bucket_all_reduce_fused(const cr_bucket_plan_t* plan, int nranks,
+                                     void* const* tensors, cr_dtype dtype, cr_op op,
+                                     cr_stream_t stream) {
+  cr_status st = check_plan(plan, nranks);
+  if (st) return st;
+  if ((st = check_pair(dtype, op, dtype))) return st;
+  const size_t es = esize_of(dtype);
+  if (es != plan->elem_size)
+    return fail(CR_ERR_INVALID_ARG, "dtype size %zu != plan elem_size %zu", es, plan->elem_size);
+  const int T = plan->ntensors;
+  if (T > 0 && !tensors) return fail(CR_ERR_INVALID_ARG, "tensors is NULL");
+  std::vector<Span> spans;
+  for (int r = 0; r < nranks; ++r)
+    for (int t = 0; t < T; ++t) {
+      const void* p = tensors[(size_t)r * T + t];
+      if ((st = check_buf(p, plan->numels[t], es, "tensors", r * T + t))) return st;
+      if (plan->numels[t]) spans.push_back(span_of(p, plan->numels[t] * es, 1, r * T + t));
+    }
+  if ((st = check_disjoint(spans))) return st;
+  static thread_local FusedArgs args;  // ~21 KB: kept off the stack
+  const int per_launch = std::min(kFusedMaxTensors, kFusedMaxPtrs / nranks);
+  const uint64_t tile = fused_tile_elems(dtype);
+  uint32_t ntiles = 0;
+  args.ntens = 0;
+  args.n = nranks;
+  args.avg = op == CR_AVG;
+  args.inv_n = exact_inv_n(nranks);
+  auto flush = [&]() -> cr_status {
+    if (args.ntens == 0) return CR_OK;
+    args.tile_start[args.ntens] = ntiles;
+    cudaError_t e = launch_bucket_fused(dtype, args, ntiles, (cudaStream_t)stream);
+    args.ntens = 0;
+    ntiles = 0;
+    if (e != cudaSuccess) return cuda_fail(e, "bucket_all_reduce_fused launch");
+    return CR_OK;
+  };
+  for (int t = 0; t < T; ++t) {
+    const uint64_t numel = plan->numels[t];
+    if (numel == 0) continue;
+    const uint64_t tiles = (numel + tile - 1) / tile;
+    if (args.ntens == per_launch || (uint64_t)ntiles + tiles > 0x7fffffffull)
+      if ((st = flush())) return st;
+    const int k = args.ntens;
+    FusedTensor& d = args.t[k];
+    d.numel = numel;
+    d.off = plan->tensor_offset[t];
+    d.Lb = cr_chunk_len(plan->bucket_numel[plan->tensor_bucket[t]], nranks);
+    d.ptr0 = (uint32_t)(k * nranks);
+    d.vec = 1;
+    for (int r = 0; r < nranks; ++r) {
+      void* p = tensors[(size_t)r * T + t];
+      args.ptrs[k * nranks + r] = p;
+      if (!aligned(p, 16)) d.vec = 0;
+    }
+    args.tile_start[k] = ntiles;
+    args.ntens += 1;
+    ntiles += (uint32_t)tiles;
+  }
+  if ((st = flush())) return st;
   return ok();
 }
 

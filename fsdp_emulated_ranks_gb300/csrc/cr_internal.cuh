@@ -21,6 +21,8 @@ struct FoldArgs {
   void* out[kMaxRanks];
   uint64_t count;  // elements per rank buffer
   uint64_t L;      // chunk length ceil(count / n)
+  uint64_t begin;  // the call covers elements [begin, end) of each buffer
+  uint64_t end;
   int n;           // ranks
   int avg;         // 1: divide the finished sum by n
   float inv_n;     // 1/n when n is a power of two (exact), else 0
@@ -79,6 +81,29 @@ struct CopyArgs {
   CopySeg seg[kMaxSegsPerLaunch];
 };
 
+// Fused bucket all-reduce: one tensor of a launch.
+struct FusedTensor {
+  uint64_t numel;  // elements of the tensor
+  uint64_t off;    // element offset of the tensor inside its bucket
+  uint64_t Lb;     // chunk length of its bucket, ceil(bucket numel / N)
+  uint32_t ptr0;   // index of rank 0's pointer in FusedArgs::ptrs
+  uint32_t vec;    // 1: all N rank pointers are 16-byte aligned
+};
+
+constexpr int kFusedMaxTensors = 128;
+constexpr int kFusedMaxPtrs = 2048;
+constexpr int kFusedVecPerThread = 4;  // 16-byte vectors per thread per tile
+
+struct FusedArgs {
+  int ntens;
+  int n;
+  int avg;
+  float inv_n;
+  uint32_t tile_start[kFusedMaxTensors + 1];
+  FusedTensor t[kFusedMaxTensors];
+  void* ptrs[kFusedMaxPtrs];  // rank q of tensor k at ptrs[t[k].ptr0 + q]
+};
+
 enum FoldMode { kRS = 0, kAR = 1 };
 
 // Launchers (defined next to their kernels).  `vec` selects the 16-byte
@@ -90,6 +115,9 @@ cudaError_t launch_gather(size_t esize, const GatherArgs& a, bool vec,
 cudaError_t launch_fsdp(const FsdpArgs& a, bool vec, cudaStream_t s);
 cudaError_t launch_adamw(const AdamArgs& a, bool vec, cudaStream_t s);
 cudaError_t launch_copy(const CopyArgs& a, uint32_t ntiles, cudaStream_t s);
+cudaError_t launch_bucket_fused(cr_dtype d, const FusedArgs& a, uint32_t ntiles,
+                                cudaStream_t s);
+uint64_t fused_tile_elems(cr_dtype d);  // elements of a tensor per CTA tile
 
 // Persistent-grid size for a kBlock-thread kernel that needs `threads`
 // threads of work: min(SMs on the current device * CTAs of `kernel` resident

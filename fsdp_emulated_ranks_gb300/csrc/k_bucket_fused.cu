@@ -1,0 +1,134 @@
+// k_bucket_fused.cu -- DDP bucket all-reduce straight on the gradient
+// tensors, without packing them into bucket buffers.
+//
+// "AI Infra Guide, Chapter 6", 6.2.4 lets gradients alias bucket storage
+// (gradient_as_bucket_view) so that no copy is made; on one GPU the same
+// idea removes the pack and unpack passes entirely: element i of tensor t
+// sits at bucket position p = off_t + i of bucket b = bucket(t), and is
+// reduced over the ranks in the ring order of p's chunk, j = p / L_b with
+// L_b = ceil(numel_b / N), exactly as the all-reduce of the packed bucket
+// would reduce it.  The result, written back in place into every rank's
+// tensor, is bit-identical to pack -> all-reduce -> unpack, at a third of
+// the HBM traffic (N reads + N writes per element instead of three times
+// that).
+//
+// One launch covers up to kFusedMaxTensors tensors whose N rank pointers
+// (kFusedMaxPtrs in all) travel in the __grid_constant__ parameter block;
+// CTAs walk tiles of one tensor each with a grid stride.
+#include "cr_internal.cuh"
+#include "fold.cuh"
+
+namespace cr {
+
+template <int D>
+__device__ __forceinline__ void fused_elem(const FusedArgs& a, const FusedTensor& t,
+                                           uint64_t i) {
+  using Acc = typename Elem<D>::Acc;
+  const int n = a.n;
+  const int j = (int)((t.off + i) / t.Lb);
+  int r = (j + 1 == n) ? 0 : j + 1;
+  Acc acc = ld_elem<D>(a.ptrs[t.ptr0 + r], i);
+  for (int k = 1; k < n; ++k) {
+    r = (r + 1 == n) ? 0 : r + 1;
+    acc = acc_plus<D>(acc, ld_elem<D>(a.ptrs[t.ptr0 + r], i));
+  }
+  if constexpr (D != CR_I32) {
+    if (a.avg) acc = finish_avg(acc, n, a.inv_n);
+  }
+  for (int q = 0; q < n; ++q) st_elem<D>(a.ptrs[t.ptr0 + q], i, acc);
+}
+
+template <int D, int NT>
+__global__ void __launch_bounds__(kBlock)
+    k_bucket_fused(const __grid_constant__ FusedArgs a, uint32_t ntiles) {
+  using Acc = typename Elem<D>::Acc;
+  constexpr int IS = Elem<D>::kSize;
+  constexpr int VEC = 16 / IS;
+  constexpr uint64_t kTileElems = (uint64_t)kFusedVecPerThread * kBlock * VEC;
+  const int n = NT > 0 ? NT : a.n;
+  for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    int lo = 0, hi = a.ntens;  // tile_start[lo] <= tile < tile_start[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (a.tile_start[mid] <= tile) lo = mid;
+      else hi = mid;
+    }
+    const FusedTensor& t = a.t[lo];
+    const uint64_t e_lo = (uint64_t)(tile - a.tile_start[lo]) * kTileElems;
+    const uint64_t e_hi = e_lo + kTileElems < t.numel ? e_lo + kTileElems : t.numel;
+    if (!t.vec) {
+      for (uint64_t i = e_lo + threadIdx.x; i < e_hi; i += kBlock) fused_elem<D>(a, t, i);
+      continue;
+    }
+    const uint64_t v_hi = e_hi / VEC;  // whole vectors end here; e_lo is a multiple of VEC
+#pragma unroll 1
+    for (int k = 0; k < kFusedVecPerThread; ++k) {
+      const uint64_t iv = e_lo / VEC + (uint64_t)k * kBlock + threadIdx.x;
+      if (iv >= v_hi) break;
+      const uint64_t e0 = iv * VEC;
+      const uint64_t p0 = t.off + e0;
+      const uint64_t j64 = p0 / t.Lb;
+      if (p0 + VEC > (j64 + 1) * t.Lb) {  // straddles a chunk of the bucket
+        for (int q = 0; q < VEC; ++q) fused_elem<D>(a, t, e0 + q);
+        continue;
+      }
+      Acc acc[VEC];
+      fold_vec16<D, NT>(a.ptrs + t.ptr0, n, (int)j64, e0 * IS, acc);
+      if constexpr (D != CR_I32) {
+        if (a.avg) {
+#pragma unroll
+          for (int q = 0; q < VEC; ++q) acc[q] = finish_avg(acc[q], n, a.inv_n);
+        }
+      }
+      uint32_t w[4];
+      acc_pack<D, D>(acc, w);
+#pragma unroll 8
+      for (int q = 0; q < n; ++q)
+        st_words<16>(static_cast<unsigned char*>(a.ptrs[t.ptr0 + q]) + e0 * IS, w);
+    }
+    // Ragged end of the tensor (fewer than VEC elements), in its last tile.
+    if (e_hi == t.numel) {
+      const uint64_t i = v_hi * VEC + threadIdx.x;
+      if (i < e_hi && i >= e_lo) fused_elem<D>(a, t, i);
+    }
+  }
+}
+
+template <int D>
+static cudaError_t fused_dispatch(const FusedArgs& a, uint32_t ntiles, cudaStream_t s) {
+  const void* k;
+  switch (a.n) {
+    case 2: k = reinterpret_cast<const void*>(k_bucket_fused<D, 2>); break;
+    case 4: k = reinterpret_cast<const void*>(k_bucket_fused<D, 4>); break;
+    case 8: k = reinterpret_cast<const void*>(k_bucket_fused<D, 8>); break;
+    default: k = reinterpret_cast<const void*>(k_bucket_fused<D, 0>); break;
+  }
+  int grid = 0;
+  cudaError_t err = persistent_grid(k, (uint64_t)ntiles * kBlock, &grid);
+  if (err != cudaSuccess) return err;
+  switch (a.n) {
+    case 2: k_bucket_fused<D, 2><<<grid, kBlock, 0, s>>>(a, ntiles); break;
+    case 4: k_bucket_fused<D, 4><<<grid, kBlock, 0, s>>>(a, ntiles); break;
+    case 8: k_bucket_fused<D, 8><<<grid, kBlock, 0, s>>>(a, ntiles); break;
+    default: k_bucket_fused<D, 0><<<grid, kBlock, 0, s>>>(a, ntiles); break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bucket_fused(cr_dtype d, const FusedArgs& a, uint32_t ntiles,
+                                cudaStream_t s) {
+  if (ntiles == 0) return cudaSuccess;
+  switch (d) {
+    case CR_F32: return fused_dispatch<CR_F32>(a, ntiles, s);
+    case CR_BF16: return fused_dispatch<CR_BF16>(a, ntiles, s);
+    case CR_I32: return fused_dispatch<CR_I32>(a, ntiles, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+uint64_t fused_tile_elems(cr_dtype d) {
+  const uint64_t vec = d == CR_BF16 ? 8 : 4;
+  return (uint64_t)kFusedVecPerThread * kBlock * vec;
+}
+
+}  // namespace cr

@@ -22,6 +22,24 @@
 
 namespace cr {
 
+// Fold, finish and store element e (any chunk, any alignment).
+template <int DI, int DO, int MODE>
+__device__ __forceinline__ void fold_store_elem(const FoldArgs& a, int n, uint64_t e) {
+  using Acc = typename Elem<DI>::Acc;
+  const int j = (int)(e / a.L);
+  Acc x = fold_elem<DI>(a.in, n, j, e);
+  if constexpr (DI != CR_I32) {
+    if (a.avg) x = finish_avg(x, n, a.inv_n);
+  }
+  if constexpr (MODE == kRS) {
+    st_elem<DO>(a.out[j], e - (uint64_t)j * a.L, x);
+  } else {
+    for (int r = 0; r < n; ++r) st_elem<DO>(a.out[r], e, x);
+  }
+}
+
+// Elements [a.begin, a.end) of every rank buffer; chunks (and so the fold
+// order) are those of the whole buffer of a.count elements.
 template <int DI, int DO, int MODE, int NT>
 __global__ void __launch_bounds__(kBlock)
     k_fold_vec(const __grid_constant__ FoldArgs a) {
@@ -31,26 +49,19 @@ __global__ void __launch_bounds__(kBlock)
   constexpr int VEC = 16 / IS;
   constexpr int OB = VEC * OS;
   const int n = NT > 0 ? NT : a.n;
-  const uint64_t nvec = a.count / VEC;
+  const uint64_t vbeg = (a.begin + VEC - 1) / VEC;
+  const uint64_t vend = a.end / VEC;
   const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
 
-  for (uint64_t iv = tid; iv < nvec; iv += stride) {
+  for (uint64_t iv = vbeg + tid; iv < vend; iv += stride) {
     const uint64_t e0 = iv * VEC;
     const uint64_t j64 = e0 / a.L;
     const int j = (int)j64;
     if (MODE == kAR && e0 + VEC > (j64 + 1) * a.L) {
       // The vector straddles a chunk boundary (L % VEC != 0): each element
       // takes its own chunk's ring order.
-      for (int i = 0; i < VEC; ++i) {
-        const uint64_t e = e0 + i;
-        const int je = (int)(e / a.L);
-        Acc x = fold_elem<DI>(a.in, n, je, e);
-        if constexpr (DI != CR_I32) {
-          if (a.avg) x = finish_avg(x, n, a.inv_n);
-        }
-        for (int r = 0; r < n; ++r) st_elem<DO>(a.out[r], e, x);
-      }
+      for (int i = 0; i < VEC; ++i) fold_store_elem<DI, DO, MODE>(a, n, e0 + i);
       continue;
     }
     Acc acc[VEC];
@@ -72,41 +83,24 @@ __global__ void __launch_bounds__(kBlock)
     }
   }
 
-  // Ragged tail: fewer than VEC elements after the last full vector.
-  const uint64_t e = nvec * VEC + tid;
-  if (e < a.count) {
-    const int j = (int)(e / a.L);
-    Acc x = fold_elem<DI>(a.in, n, j, e);
-    if constexpr (DI != CR_I32) {
-      if (a.avg) x = finish_avg(x, n, a.inv_n);
-    }
-    if constexpr (MODE == kRS) {
-      st_elem<DO>(a.out[j], e - (uint64_t)j * a.L, x);
-    } else {
-      for (int r = 0; r < n; ++r) st_elem<DO>(a.out[r], e, x);
-    }
+  // Ragged ends: fewer than VEC elements before the first and after the
+  // last whole vector of the range.
+  if (vbeg <= vend) {
+    const uint64_t head = vbeg * VEC - a.begin, tail = a.end - vend * VEC;
+    if (tid < head) fold_store_elem<DI, DO, MODE>(a, n, a.begin + tid);
+    if (tid >= VEC && tid - VEC < tail) fold_store_elem<DI, DO, MODE>(a, n, vend * VEC + (tid - VEC));
+  } else if (tid < a.end - a.begin) {
+    fold_store_elem<DI, DO, MODE>(a, n, a.begin + tid);
   }
 }
 
 template <int DI, int DO, int MODE>
 __global__ void __launch_bounds__(kBlock)
     k_fold_elem(const __grid_constant__ FoldArgs a) {
-  using Acc = typename Elem<DI>::Acc;
-  const int n = a.n;
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-  for (uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-       e < a.count; e += stride) {
-    const int j = (int)(e / a.L);
-    Acc x = fold_elem<DI>(a.in, n, j, e);
-    if constexpr (DI != CR_I32) {
-      if (a.avg) x = finish_avg(x, n, a.inv_n);
-    }
-    if constexpr (MODE == kRS) {
-      st_elem<DO>(a.out[j], e - (uint64_t)j * a.L, x);
-    } else {
-      for (int r = 0; r < n; ++r) st_elem<DO>(a.out[r], e, x);
-    }
-  }
+  for (uint64_t e = a.begin + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; e < a.end;
+       e += stride)
+    fold_store_elem<DI, DO, MODE>(a, a.n, e);
 }
 
 // ---- all-gather ----------------------------------------------------------
@@ -179,9 +173,10 @@ static cudaError_t launch_persistent(K kernel, const A& args, uint64_t threads,
 
 template <int DI, int DO, int MODE>
 static cudaError_t fold_dispatch(const FoldArgs& a, bool vec, cudaStream_t s) {
-  if (!vec) return launch_persistent(k_fold_elem<DI, DO, MODE>, a, a.count, s);
+  const uint64_t span = a.end - a.begin;
+  if (!vec) return launch_persistent(k_fold_elem<DI, DO, MODE>, a, span, s);
   constexpr int VEC = 16 / Elem<DI>::kSize;
-  const uint64_t threads = a.count / VEC + 1;
+  const uint64_t threads = span / VEC + 2 * VEC;
   switch (a.n) {
     case 2: return launch_persistent(k_fold_vec<DI, DO, MODE, 2>, a, threads, s);
     case 4: return launch_persistent(k_fold_vec<DI, DO, MODE, 4>, a, threads, s);

@@ -134,6 +134,37 @@ cr_status cr_all_reduce(const void* const* in, int nranks, size_t count,
                         cr_dtype in_dtype, cr_op op, void* const* out,
                         cr_dtype out_dtype, cr_stream_t stream);
 
+/* ---- a5 from host memory: pipelined all-reduce ---------------------------
+ * The all-reduce of cr_all_reduce (in place, in_dtype == out_dtype) for
+ * rank buffers that live in host memory.  The range is cut into slices of
+ * slice_elems elements; for each slice the call enqueues the host-to-device
+ * copies of every rank's slice on h2d_stream, the all-reduce of that slice
+ * (same chunks, same ring order as the whole-buffer call, so the result is
+ * bit-identical) on compute_stream, and the device-to-host copies of the
+ * result on d2h_stream.  Events order the three streams, so slice s+1's
+ * upload, slice s's reduction and slice s-1's download run at once over the
+ * full-duplex host link.  The call first makes h2d_stream and d2h_stream
+ * wait for work already queued on compute_stream, and finally makes
+ * compute_stream wait for the last download: synchronising compute_stream
+ * waits for the whole operation.
+ *   host_in[r]   rank r's input, count elements (pinned host memory for
+ *                asynchronous copies; pageable memory works, serialised)
+ *   host_out[r]  rank r's result, count elements (may equal host_in[r])
+ *   dev_bufs[r]  device staging for rank r, count elements, caller-owned;
+ *                holds the reduced values afterwards
+ *   slice_elems  0 picks about 16 slices (at least 2^18 elements each);
+ *                otherwise rounded up to a multiple of 64
+ * The three streams may be the same stream (no overlap then).  Events are
+ * created per call and released as they complete; no memory is allocated.
+ * Errors as for cr_all_reduce; host buffers must be non-NULL and aligned to
+ * the element size, and no two buffers of the same kind may overlap. */
+cr_status cr_all_reduce_staged(const void* const* host_in,
+                               void* const* host_out, void* const* dev_bufs,
+                               int nranks, size_t count, cr_dtype dtype,
+                               cr_op op, size_t slice_elems,
+                               cr_stream_t compute_stream,
+                               cr_stream_t h2d_stream, cr_stream_t d2h_stream);
+
 /* ---- a6: DDP bucket plan (host) -------------------------------------------
  * [AIG] 6.2.4: gradients go into buckets (default 25 MB) in the order
  * backward produces them; [AIG] 6.2.6 Horovod Tensor Fusion; [NX] 5.1.
@@ -184,6 +215,23 @@ cr_status cr_bucket_unpack(const cr_bucket_plan_t* plan, int nranks,
 cr_status cr_bucket_all_reduce(const cr_bucket_plan_t* plan, int nranks,
                                void* const* buckets, cr_dtype dtype, cr_op op,
                                cr_stream_t stream);
+
+/* DDP bucket all-reduce without packing: the result of cr_bucket_pack,
+ * cr_bucket_all_reduce and cr_bucket_unpack, bit for bit, computed straight
+ * on the gradient tensors ("AI Infra Guide, Chapter 6", 6.2.4,
+ * gradient_as_bucket_view: gradients alias the bucket instead of being
+ * copied into it).  Element i of tensor t is reduced in the ring order of
+ * its bucket position off_t + i within bucket b = plan->tensor_bucket[t]
+ * (chunk length ceil(bucket numel / N)), and written back in place to every
+ * rank's tensor.  HBM traffic: N reads + N writes per element, a third of
+ * the pack / all-reduce / unpack sequence.
+ *   tensors[r*T + t]  rank r's tensor t (NULL only if empty), in/out
+ * dtype's size must equal plan->elem_size; tensors must not overlap
+ * (CR_ERR_INVALID_ARG).  One launch per 128 tensors (per 2048/N tensors
+ * when N > 16). */
+cr_status cr_bucket_all_reduce_fused(const cr_bucket_plan_t* plan, int nranks,
+                                     void* const* tensors, cr_dtype dtype,
+                                     cr_op op, cr_stream_t stream);
 
 /* ---- a8..a10: fused FSDP / ZeRO-3 step ------------------------------------
  * One kernel performs the step of [DT] section 4 (ZeRO-3/FSDP flow steps

@@ -169,3 +169,29 @@ def test_comm_elems_match_oracle_counters(L, n, count):
             assert cr.cr_comm_elems(coll, cr.SCHED_RING, n, count, r) == (t.sent[r], t.recv[r], t.steps)
         assert cr.cr_comm_elems(2, cr.SCHED_NAIVE, n, count, r) == (nv.sent[r], nv.recv[r], nv.steps)
     expect(2, cr.cr_comm_elems, 0, cr.SCHED_NAIVE, n, count, 0)
+
+
+def test_all_reduce_staged_validation(L):
+    n = 2
+    h = [FAKE + r * (1 << 20) for r in range(n)]
+    o = [FAKE + (1 << 30) + r * (1 << 20) for r in range(n)]
+    d = [FAKE + (2 << 30) + r * (1 << 20) for r in range(n)]
+    expect(1, cr.cr_all_reduce_staged, h, o, [d[0], d[0]], 16, "f32", "sum", 0, 0, 0, 0)
+    expect(1, cr.cr_all_reduce_staged, h, [o[0], o[0]], d, 16, "f32", "sum", 0, 0, 0, 0)
+    expect(2, cr.cr_all_reduce_staged, h, o, d, 16, "i32", "avg", 0, 0, 0, 0)
+    expect(3, cr.cr_all_reduce_staged, [h[0] + 2, h[1]], o, d, 16, "f32", "sum", 0, 0, 0, 0)
+    expect(1, cr.cr_all_reduce_staged, [0, h[1]], o, d, 16, "f32", "sum", 0, 0, 0, 0)
+    cr.cr_all_reduce_staged(h, o, d, 0, "f32", "sum", 0, 0, 0, 0)
+
+
+def test_bucket_all_reduce_fused_validation(L):
+    plan = cr.cr_bucket_plan([4, 8, 0], 2, 64)
+    t = [FAKE, FAKE + 4096, 0]
+    expect(1, cr.cr_bucket_all_reduce_fused, plan, 1, t, "f32", "sum", stream=0)
+    expect(1, cr.cr_bucket_all_reduce_fused, plan, 1, [FAKE, FAKE + 4, 0], "bf16", "sum", stream=0)
+    expect(1, cr.cr_bucket_all_reduce_fused, plan, 2, t + [FAKE + 8192, FAKE + 4096, 0], "bf16",
+           "avg", stream=0)
+    expect(3, cr.cr_bucket_all_reduce_fused, plan, 1, [FAKE + 1, FAKE + 4096, 0], "bf16", "sum",
+           stream=0)
+    expect(2, cr.cr_bucket_all_reduce_fused, cr.cr_bucket_plan([4], 4, 64), 1, [FAKE], "i32",
+           "avg", stream=0)

@@ -310,3 +310,76 @@ def test_bucket_copy_every_byte_alignment(src_shift, dst_shift):
         hb = b.cpu().numpy()
         assert np.all(hb[:o] == 0x5A) and np.all(hb[o + k:] == 0x5A), "canary"
         assert hb[o:o + k].tobytes() == x.tobytes()
+
+
+# ---- all-reduce from host memory (pipelined slices) --------------------------------
+
+@pytest.mark.parametrize("n,count", [(8, 8 * 8 * 1000 + 13), (4, 1 << 16), (3, 1000), (1, 77)])
+@pytest.mark.parametrize("dt,op", [("bf16", "avg"), ("f32", "sum"), ("i32", "sum")])
+@pytest.mark.parametrize("slice_elems", [0, 1, 1000, 4096, 1 << 30])
+@pytest.mark.parametrize("streams", ["three", "one"])
+def test_all_reduce_staged(n, count, dt, op, slice_elems, streams):
+    host = host_inputs(n, count, dt, seed=count + n)
+    want, _ = O.ring_all_reduce(host, dt, op, dt)
+    tdt = {"bf16": torch.bfloat16, "f32": torch.float32, "i32": torch.int32}[dt]
+    h_in = [to_dev(x, dt).cpu().pin_memory() for x in host]
+    same = slice_elems == 4096   # host_out == host_in for one variant
+    h_out = h_in if same else [torch.empty(count, dtype=tdt).pin_memory() for _ in range(n)]
+    d = [torch.empty(count, dtype=tdt, device="cuda") for _ in range(n)]
+    sc = torch.cuda.current_stream()
+    sh, sd = (torch.cuda.Stream(), torch.cuda.Stream()) if streams == "three" else (sc, sc)
+    cr.cr_all_reduce_staged(h_in, h_out, d, count, dt, op, slice_elems, sc, sh, sd)
+    sc.synchronize()
+    for r in range(n):
+        got = h_out[r].view(torch.int16).numpy().view(np.uint16) if dt == "bf16" else h_out[r].numpy()
+        assert_match(got, want[r], dt, f"host_out rank {r}")
+        assert_match(to_host(d[r], dt), want[r], dt, f"dev rank {r}")
+
+
+def test_all_reduce_staged_repeated_calls_keep_order():
+    """Back-to-back calls on the same buffers: each call's uploads must wait
+    for the previous call's downloads (host_out == host_in)."""
+    n, count = 8, 1 << 20
+    host = host_inputs(n, count, "f32", seed=5)
+    h = [torch.from_numpy(x).pin_memory() for x in host]
+    d = [torch.empty(count, dtype=torch.float32, device="cuda") for _ in range(n)]
+    sh, sd = torch.cuda.Stream(), torch.cuda.Stream()
+    cur = [x.copy() for x in host]
+    for _ in range(3):
+        cr.cr_all_reduce_staged(h, h, d, count, "f32", "sum", 1 << 16, None, sh, sd)
+        cur, _ = O.ring_all_reduce(cur, "f32", "sum")
+    torch.cuda.synchronize()
+    for r in range(n):
+        assert_match(h[r].numpy(), cur[r], "f32", f"rank {r}")
+
+
+# ---- fused bucket all-reduce (no pack) ---------------------------------------------
+
+@pytest.mark.parametrize("n", [1, 2, 3, 8, 16, 64])
+@pytest.mark.parametrize("dt,op", [("bf16", "avg"), ("f32", "sum"), ("i32", "sum"), ("f32", "avg")])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_bucket_all_reduce_fused(n, dt, op, offset):
+    """Equal, bit for bit, to the oracle's pack -> ring all-reduce per bucket
+    -> unpack, including tensors that straddle chunk boundaries of their
+    bucket and more tensors than one launch takes."""
+    rng = np.random.default_rng(n * 7 + offset)
+    T = 150 if n <= 16 else 40
+    numels = [int(k) for k in rng.integers(0, 3000, size=T)] + [1, 0, 7, 20001]
+    esize = 2 if dt == "bf16" else 4
+    cap = 9000 * esize
+    plan = cr.cr_bucket_plan(numels, esize, cap)
+    oplan = O.bucket_plan(numels, esize, cap)
+    host_t = [[host_inputs(1, k, dt, seed=100 * r + t)[0] for t, k in enumerate(numels)]
+              for r in range(n)]
+    want = O.bucketed_all_reduce(oplan, host_t, dt, op)
+    g = [[Guarded(k, dt, offset) for k in numels] for _ in range(n)]
+    for r in range(n):
+        for t, k in enumerate(numels):
+            if k:
+                g[r][t].view.copy_(to_dev(host_t[r][t], dt))
+    cr.cr_bucket_all_reduce_fused(plan, n, [x.ptr() for row in g for x in row], dt, op)
+    torch.cuda.synchronize()
+    for r in range(n):
+        for t in range(len(numels)):
+            g[r][t].check()
+            assert_match(g[r][t].host(), want[r][t], dt, f"rank {r} tensor {t}")
