@@ -315,8 +315,11 @@ class Buckets(Workload):
         self.P = sum(self.numels)
         one = 2 * 2 * self.P * n
         self.nbytes = 3 * one if mode == "pipeline" else one
+        # The fused all-reduce works on the tensors in place: N reads + N
+        # writes per element, the same bytes as one pass over the buckets.
         self.name = f"ddp_bucket_{mode}_bf16_{n}ranks_{ntensors}tensors"
-        self.kernel = "k_fold_vec<bf16,bf16,AR,8>" if mode == "allreduce" else "k_copy_segments"
+        self.kernel = {"allreduce": "k_fold_vec<bf16,bf16,AR,8>",
+                       "fused": "k_bucket_fused<bf16,8>"}.get(mode, "k_copy_segments")
         self.profile = (f"k_fold_vec_bucket_allreduce_bf16_{n}x{ntensors}" if mode == "allreduce"
                         else f"k_copy_segments_bucket_{mode}_bf16_{n}x{ntensors}")
 
@@ -328,7 +331,8 @@ class Buckets(Workload):
         self.plan = cr.cr_bucket_plan(self.numels, 2, 25 * 1024 * 1024)
         copies = -(-n * len(self.numels) // 1024)
         self.launches = {"pack": copies, "unpack": copies, "allreduce": self.plan.nbuckets,
-                         "pipeline": 2 * copies + self.plan.nbuckets}[self.mode]
+                         "pipeline": 2 * copies + self.plan.nbuckets,
+                         "fused": -(-len(self.numels) // min(128, 2048 // n))}[self.mode]
         tens = []
         for r in range(n):
             flat = torch.empty(self.P + 128 * len(self.numels), dtype=torch.bfloat16, device=device)
@@ -359,18 +363,22 @@ class Buckets(Workload):
             cr.cr_bucket_all_reduce(self.plan, n, self.t_flat_b, "bf16", "avg", stream)
         if self.mode in ("unpack", "pipeline"):
             cr.cr_bucket_unpack(self.plan, n, self.t_flat_b, self.t_flat_t, stream)
+        if self.mode == "fused":
+            cr.cr_bucket_all_reduce_fused(self.plan, n, self.t_flat_t, "bf16", "avg", stream)
 
 
 class FsdpStep(Workload):
-    """Fused FSDP step: 8 ranks, flat `count` params (1.3e9 by default)."""
+    """Fused FSDP step: 8 ranks, flat `count` params (1.3e9 by default);
+    clip=True adds global grad-norm clipping (max_norm 1.0)."""
 
-    def __init__(self, n=8, count=1_300_000_000):
-        self.n, self.count = n, count
-        self.nbytes = (4 * n + 24) * count
+    def __init__(self, n=8, count=1_300_000_000, clip=False):
+        self.n, self.count, self.clip = n, count, clip
+        self.nbytes = ((6 if clip else 4) * n + 24) * count
         tag = f"{count / 1e9:g}e9" if count >= 10 ** 8 else str(count)
-        self.name = f"fsdp_step_bf16_{n}ranks_{tag}params"
-        self.kernel = f"k_fsdp_vec<{n}>"
-        self.profile = f"k_fsdp_vec_fsdp_step_{n}x{tag}"
+        self.name = f"fsdp_step{'_clipped' if clip else ''}_bf16_{n}ranks_{tag}params"
+        self.kernel = f"k_fsdp_vec<{n}>" + (" + k_fsdp_sumsq" if clip else "")
+        self.profile = f"k_fsdp_vec_fsdp_step{'_clipped' if clip else ''}_{n}x{tag}"
+        self.launches = 2 if clip else 1
 
     def setup(self, device):
         import torch
@@ -387,11 +395,19 @@ class FsdpStep(Workload):
         self.t_m = [self.t_mv[j * L:(j + 1) * L] for j in range(n)]
         self.t_v = [self.t_mv[count + j * L:count + (j + 1) * L] for j in range(n)]
         self.cfg = cr.adamw_cfg()
+        self.ws_bytes = cr.cr_fsdp_clip_workspace_bytes()
+        self.t_ws = torch.empty(self.ws_bytes // 8, dtype=torch.float64, device=device)
+        self.t_norm = torch.empty(1, dtype=torch.float32, device=device)
 
     def step(self, stream):
         from fsdp_emulated_ranks_gb300 import cr
-        cr.cr_fsdp_step(self.t_grads, self.count, self.t_master, self.t_m, self.t_v, self.cfg,
-                        self.t_params, stream)
+        if self.clip:
+            cr.cr_fsdp_step_clipped(self.t_grads, self.count, self.t_master, self.t_m, self.t_v,
+                                    self.cfg, 1.0, self.t_ws, self.ws_bytes, self.t_params,
+                                    self.t_norm, stream)
+        else:
+            cr.cr_fsdp_step(self.t_grads, self.count, self.t_master, self.t_m, self.t_v,
+                            self.cfg, self.t_params, stream)
 
 
 def make_workload(name, args):
@@ -407,11 +423,13 @@ def make_workload(name, args):
         return Buckets(mode=name[len("bucket_"):], ntensors=args.bucket_ntensors)
     if name == "fsdp":
         return FsdpStep(count=args.fsdp_count)
+    if name == "fsdp_clipped":
+        return FsdpStep(count=args.fsdp_count, clip=True)
     raise SystemExit(f"unknown workload {name}")
 
 
 ROW_WORKLOADS = ["reduce_scatter", "all_gather", "allreduce_f32", "bucket_pack",
-                 "bucket_allreduce", "bucket_unpack", "bucket_pipeline", "fsdp"]
+                 "bucket_allreduce", "bucket_unpack", "bucket_pipeline", "bucket_fused", "fsdp", "fsdp_clipped"]
 
 
 def run_headline(args, world, rank, device, stream, peak):
@@ -502,7 +520,7 @@ def traffic_per_launch(name, launches=1):
 def run_rows(args, device, stream, peak, skip=None):
     rows = []
     for name in ROW_WORKLOADS:
-        if (name == "fsdp" and args.skip_fsdp) or name == skip:
+        if (name.startswith("fsdp") and args.skip_fsdp) or name == skip:
             continue
         wl = make_workload(name, args)
         wl.setup(device)

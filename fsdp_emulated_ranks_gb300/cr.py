@@ -32,7 +32,8 @@ EXPORTS = ["cr_status_string", "cr_last_error", "cr_version", "cr_chunk_len",
            "cr_shard_range", "cr_reduce_scatter", "cr_all_gather",
            "cr_all_reduce", "cr_all_reduce_staged", "cr_bucket_plan", "cr_bucket_plan_free",
            "cr_bucket_pack", "cr_bucket_unpack", "cr_bucket_all_reduce",
-           "cr_bucket_all_reduce_fused", "cr_fsdp_step", "cr_adamw_step", "cr_comm_elems"]
+           "cr_bucket_all_reduce_fused", "cr_fsdp_step",
+           "cr_fsdp_clip_workspace_bytes", "cr_fsdp_step_clipped", "cr_adamw_step", "cr_comm_elems"]
 
 _lib = None
 
@@ -89,6 +90,10 @@ def lib() -> C.CDLL:
     L.cr_bucket_all_reduce.argtypes = [C.POINTER(BucketPlanT), i, vp, i, i, vp]
     L.cr_bucket_all_reduce_fused.argtypes = [C.POINTER(BucketPlanT), i, vp, i, i, vp]
     L.cr_fsdp_step.argtypes = [vp, i, sz, vp, vp, vp, C.POINTER(AdamWCfg), vp, vp]
+    L.cr_fsdp_clip_workspace_bytes.restype = sz
+    L.cr_fsdp_clip_workspace_bytes.argtypes = []
+    L.cr_fsdp_step_clipped.argtypes = [vp, i, sz, vp, vp, vp, C.POINTER(AdamWCfg), C.c_double,
+                                       vp, sz, vp, vp, vp]
     L.cr_adamw_step.argtypes = [sz, vp, vp, vp, vp, C.POINTER(AdamWCfg), vp, vp]
     L.cr_comm_elems.argtypes = [i, i, i, sz, i, C.POINTER(C.c_uint64),
                                 C.POINTER(C.c_uint64), C.POINTER(i)]
@@ -98,6 +103,7 @@ def lib() -> C.CDLL:
     L.cr_last_error.restype = C.c_char_p
     L.cr_chunk_len.restype = sz
     L.cr_bucket_plan_free.restype = None
+    L.cr_fsdp_clip_workspace_bytes.restype = sz
     _lib = L
     return L
 
@@ -265,6 +271,19 @@ def cr_fsdp_step(grads, count, master, m, v, cfg: AdamWCfg, params,
                               _ptr_array(master), _ptr_array(m), _ptr_array(v),
                               C.byref(cfg), _ptr_array(params), _stream(stream)),
            "cr_fsdp_step")
+
+
+def cr_fsdp_clip_workspace_bytes() -> int:
+    return lib().cr_fsdp_clip_workspace_bytes()
+
+
+def cr_fsdp_step_clipped(grads, count, master, m, v, cfg: AdamWCfg, max_norm, workspace,
+                         workspace_bytes, params, norm_out=None, stream=None) -> None:
+    _check(lib().cr_fsdp_step_clipped(_ptr_array(grads), len(grads), count,
+                                      _ptr_array(master), _ptr_array(m), _ptr_array(v),
+                                      C.byref(cfg), float(max_norm), _ptr(workspace),
+                                      workspace_bytes, _ptr_array(params), _ptr(norm_out),
+                                      _stream(stream)), "cr_fsdp_step_clipped")
 
 
 def cr_adamw_step(n, master, m, v, grad, cfg: AdamWCfg, param_bf16=None,

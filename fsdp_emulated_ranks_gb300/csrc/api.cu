@@ -443,17 +443,21 @@ cr_status cr_all_reduce_staged(const void* const* host_in, void* const* host_out
   return ok();
 }
 
-cr_status cr_fsdp_step(const void* const* grads_bf16, int nranks, size_t count,
+}  // extern "C"
+
+namespace {
+
+// Shared argument checks of the FSDP step entry points; fills `a` and `vec`.
+cr_status fsdp_prepare(const void* const* grads_bf16, int nranks, size_t count,
                        float* const* master, float* const* m, float* const* v,
                        const cr_adamw_cfg* cfg, void* const* params_bf16,
-                       cr_stream_t stream) {
+                       std::vector<Span>& spans, FsdpArgs& a, bool& vec) {
   cr_status st = check_common(nranks, count, grads_bf16, params_bf16);
   if (st) return st;
   if (!master || !m || !v) return fail(CR_ERR_INVALID_ARG, "master/m/v array is NULL");
   if ((st = check_adam_cfg(cfg))) return st;
   const uint64_t L = cr_chunk_len(count, nranks);
-  std::vector<Span> spans;
-  bool vec = L % 8 == 0;
+  vec = L % 8 == 0;
   for (int r = 0; r < nranks; ++r) {
     const uint64_t len = chunk_size(count, L, r);
     if ((st = check_buf(grads_bf16[r], count, 2, "grads", r))) return st;
@@ -475,10 +479,6 @@ cr_status cr_fsdp_step(const void* const* grads_bf16, int nranks, size_t count,
       vec = vec && aligned(master[r], 16) && aligned(m[r], 16) && aligned(v[r], 16);
     }
   }
-  st = check_overlaps(spans, [](const Span&, const Span&) { return false; });
-  if (st) return st;
-  if (count == 0) return ok();
-  FsdpArgs a;
   memset(&a, 0, sizeof(a));
   for (int r = 0; r < nranks; ++r) {
     a.grads[r] = grads_bf16[r];
@@ -492,8 +492,74 @@ cr_status cr_fsdp_step(const void* const* grads_bf16, int nranks, size_t count,
   a.n = nranks;
   a.inv_n = exact_inv_n(nranks);
   a.a = adam_scalars(*cfg);
+  return CR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+cr_status cr_fsdp_step(const void* const* grads_bf16, int nranks, size_t count,
+                       float* const* master, float* const* m, float* const* v,
+                       const cr_adamw_cfg* cfg, void* const* params_bf16,
+                       cr_stream_t stream) {
+  std::vector<Span> spans;
+  FsdpArgs a;
+  bool vec = false;
+  cr_status st = fsdp_prepare(grads_bf16, nranks, count, master, m, v, cfg, params_bf16,
+                              spans, a, vec);
+  if (st) return st;
+  if ((st = check_overlaps(spans, [](const Span&, const Span&) { return false; }))) return st;
+  if (count == 0) return ok();
   cudaError_t e = launch_fsdp(a, vec, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "fsdp_step launch");
+  return ok();
+}
+
+size_t cr_fsdp_clip_workspace_bytes(void) { return (size_t)kMaxNormParts * sizeof(double); }
+
+cr_status cr_fsdp_step_clipped(const void* const* grads_bf16, int nranks, size_t count,
+                               float* const* master, float* const* m, float* const* v,
+                               const cr_adamw_cfg* cfg, double max_norm, void* workspace,
+                               size_t workspace_bytes, void* const* params_bf16,
+                               float* norm_out, cr_stream_t stream) {
+  std::vector<Span> spans;
+  FsdpArgs a;
+  bool vec = false;
+  cr_status st = fsdp_prepare(grads_bf16, nranks, count, master, m, v, cfg, params_bf16,
+                              spans, a, vec);
+  if (st) return st;
+  if (!(max_norm > 0.0) || !isfinite(max_norm))
+    return fail(CR_ERR_INVALID_ARG, "max_norm must be finite and > 0");
+  if (!workspace) return fail(CR_ERR_INVALID_ARG, "workspace is NULL");
+  if (!aligned(workspace, 8)) return fail(CR_ERR_ALIGNMENT, "workspace not 8-byte aligned");
+  if (workspace_bytes < sizeof(double))
+    return fail(CR_ERR_INVALID_ARG, "workspace_bytes=%zu too small", workspace_bytes);
+  if (norm_out && !aligned(norm_out, 4)) return fail(CR_ERR_ALIGNMENT, "norm_out not aligned");
+  const size_t max_parts = workspace_bytes / sizeof(double) < (size_t)kMaxNormParts
+                               ? workspace_bytes / sizeof(double)
+                               : (size_t)kMaxNormParts;
+  spans.push_back(span_of(workspace, max_parts * sizeof(double), 1, 1000));
+  if (norm_out) spans.push_back(span_of(norm_out, sizeof(float), 1, 1001));
+  if ((st = check_overlaps(spans, [](const Span&, const Span&) { return false; }))) return st;
+  if (count == 0) {
+    if (norm_out) {
+      cudaError_t e = cudaMemsetAsync(norm_out, 0, sizeof(float), (cudaStream_t)stream);
+      if (e != cudaSuccess) return cuda_fail(e, "fsdp_step_clipped norm_out");
+    }
+    return ok();
+  }
+  double* partials = static_cast<double*>(workspace);
+  int nparts = 0;
+  cudaError_t e = launch_fsdp_sumsq(a, vec, partials, (int)max_parts, &nparts,
+                                    (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "fsdp_step_clipped sum-of-squares launch");
+  a.partials = partials;
+  a.nparts = nparts;
+  a.max_norm = max_norm;
+  a.norm_out = norm_out;
+  e = launch_fsdp(a, vec, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "fsdp_step_clipped launch");
   return ok();
 }
 

@@ -53,7 +53,17 @@ struct FsdpArgs {
   int n;
   float inv_n;
   AdamScalars a;
+  // Gradient-norm clipping (clip_grad_norm_): when partials is non-null the
+  // step first sums the nparts fp64 partial sums of squares, in index
+  // order, and scales every gradient by min(1, max_norm / (norm + 1e-6)).
+  const double* partials;
+  int nparts;
+  double max_norm;
+  float* norm_out;  // written by CTA 0 when non-null
 };
+
+// Upper bound on the per-CTA partial sums of the sum-of-squares pass.
+constexpr int kMaxNormParts = 4096;
 
 struct AdamArgs {
   float* master;
@@ -113,6 +123,10 @@ cudaError_t launch_fold(cr_dtype in, cr_dtype out, FoldMode mode,
 cudaError_t launch_gather(size_t esize, const GatherArgs& a, bool vec,
                           cudaStream_t s);
 cudaError_t launch_fsdp(const FsdpArgs& a, bool vec, cudaStream_t s);
+// Sum-of-squares pass of the clipped step: writes *nparts (<= max_parts)
+// fp64 partials to `partials`.
+cudaError_t launch_fsdp_sumsq(const FsdpArgs& a, bool vec, double* partials,
+                              int max_parts, int* nparts, cudaStream_t s);
 cudaError_t launch_adamw(const AdamArgs& a, bool vec, cudaStream_t s);
 cudaError_t launch_copy(const CopyArgs& a, uint32_t ntiles, cudaStream_t s);
 cudaError_t launch_bucket_fused(cr_dtype d, const FusedArgs& a, uint32_t ntiles,

@@ -39,13 +39,74 @@ __device__ __forceinline__ AdamOut adamw_elem(float p, float m, float v,
   return o;
 }
 
-__device__ __forceinline__ uint4 ld16_f(const float* p) { return ld16(p); }
+// Clip coefficient of clip_grad_norm_, the same in every CTA: the partial
+// sums are added in a fixed order (lane-strided, then a fixed shuffle tree),
+// so the norm is reproducible run to run.  Returns 1 when not clipping.
+__device__ float clip_coef(const FsdpArgs& a) {
+  __shared__ float s_coef;
+  if (a.partials == nullptr) return 1.0f;
+  if (threadIdx.x < 32) {
+    double t = 0.0;
+    for (int i = threadIdx.x; i < a.nparts; i += 32) t += a.partials[i];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) t += __shfl_down_sync(0xffffffffu, t, off);
+    if (threadIdx.x == 0) {
+      const double norm = sqrt(t);
+      double c = a.max_norm / (norm + 1e-6);
+      if (c > 1.0) c = 1.0;
+      s_coef = (float)c;
+      if (blockIdx.x == 0 && a.norm_out) *a.norm_out = (float)norm;
+    }
+  }
+  __syncthreads();
+  return s_coef;
+}
+
+// Sum of squares of the averaged fp32 gradient, one fp64 partial per CTA.
+template <int NT, bool VEC>
+__global__ void __launch_bounds__(kBlock)
+    k_fsdp_sumsq(const __grid_constant__ FsdpArgs a, double* partials) {
+  __shared__ double s_warp[kBlock / 32];
+  const int n = NT > 0 ? NT : a.n;
+  const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  double t = 0.0;
+  uint64_t e_elem = 0;  // first element the element-wise loop covers
+  if constexpr (VEC) {
+    const uint64_t nvec = a.count / 8;
+    for (uint64_t iv = tid; iv < nvec; iv += stride) {
+      const uint64_t e0 = iv * 8;
+      float g[8];
+      fold_vec16<CR_BF16, NT>(a.grads, n, (int)(e0 / a.L), e0 * 2, g);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const double gi = finish_avg(g[i], n, a.inv_n);
+        t += gi * gi;
+      }
+    }
+    e_elem = nvec * 8;
+  }
+  for (uint64_t e = e_elem + tid; e < a.count; e += stride) {
+    const double gi = finish_avg(fold_elem<CR_BF16>(a.grads, n, (int)(e / a.L), e), n, a.inv_n);
+    t += gi * gi;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) t += __shfl_down_sync(0xffffffffu, t, off);
+  if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = t;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double b = 0.0;
+    for (int w = 0; w < kBlock / 32; ++w) b += s_warp[w];
+    partials[blockIdx.x] = b;
+  }
+}
 
 // Vector path: 8 elements (one 16-byte bf16 vector per rank) per iteration.
 template <int NT>
 __global__ void __launch_bounds__(kBlock)
     k_fsdp_vec(const __grid_constant__ FsdpArgs a) {
   const int n = NT > 0 ? NT : a.n;
+  const float coef = clip_coef(a);
   const uint64_t nvec = a.count / 8;
   const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
@@ -68,7 +129,7 @@ __global__ void __launch_bounds__(kBlock)
     uint32_t po[8], mo[8], vo[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float gi = finish_avg(g[i], n, a.inv_n);
+      const float gi = __fmul_rn(finish_avg(g[i], n, a.inv_n), coef);
       const AdamOut o = adamw_elem(__uint_as_float(pw[i]), __uint_as_float(mw[i]),
                                    __uint_as_float(vw[i]), gi, a.a);
       po[i] = __float_as_uint(o.p);
@@ -96,7 +157,8 @@ __global__ void __launch_bounds__(kBlock)
     const uint64_t j64 = e / a.L;
     const int j = (int)j64;
     const uint64_t k = e - j64 * a.L;
-    const float gi = finish_avg(fold_elem<CR_BF16>(a.grads, n, j, e), n, a.inv_n);
+    const float gi =
+        __fmul_rn(finish_avg(fold_elem<CR_BF16>(a.grads, n, j, e), n, a.inv_n), coef);
     const AdamOut o = adamw_elem(a.master[j][k], a.m[j][k], a.v[j][k], gi, a.a);
     a.master[j][k] = o.p;
     a.m[j][k] = o.m;
@@ -108,13 +170,15 @@ __global__ void __launch_bounds__(kBlock)
 __global__ void __launch_bounds__(kBlock)
     k_fsdp_elem(const __grid_constant__ FsdpArgs a) {
   const int n = a.n;
+  const float coef = clip_coef(a);
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
   for (uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
        e < a.count; e += stride) {
     const uint64_t j64 = e / a.L;
     const int j = (int)j64;
     const uint64_t k = e - j64 * a.L;
-    const float gi = finish_avg(fold_elem<CR_BF16>(a.grads, n, j, e), n, a.inv_n);
+    const float gi =
+        __fmul_rn(finish_avg(fold_elem<CR_BF16>(a.grads, n, j, e), n, a.inv_n), coef);
     const AdamOut o = adamw_elem(a.master[j][k], a.m[j][k], a.v[j][k], gi, a.a);
     a.master[j][k] = o.p;
     a.m[j][k] = o.m;
@@ -195,6 +259,31 @@ cudaError_t launch_fsdp(const FsdpArgs& a, bool vec, cudaStream_t s) {
     case 4: return launch_persistent(k_fsdp_vec<4>, a, threads, s);
     case 8: return launch_persistent(k_fsdp_vec<8>, a, threads, s);
     default: return launch_persistent(k_fsdp_vec<0>, a, threads, s);
+  }
+}
+
+template <int NT, bool VEC>
+static cudaError_t sumsq_launch(const FsdpArgs& a, double* partials, int max_parts,
+                                int* nparts, cudaStream_t s) {
+  const uint64_t threads = VEC ? a.count / 8 + 1 : a.count;
+  int grid = 0;
+  cudaError_t err =
+      persistent_grid(reinterpret_cast<const void*>(k_fsdp_sumsq<NT, VEC>), threads, &grid);
+  if (err != cudaSuccess) return err;
+  if (grid > max_parts) grid = max_parts;
+  *nparts = grid;
+  k_fsdp_sumsq<NT, VEC><<<grid, kBlock, 0, s>>>(a, partials);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fsdp_sumsq(const FsdpArgs& a, bool vec, double* partials,
+                              int max_parts, int* nparts, cudaStream_t s) {
+  if (!vec) return sumsq_launch<0, false>(a, partials, max_parts, nparts, s);
+  switch (a.n) {
+    case 2: return sumsq_launch<2, true>(a, partials, max_parts, nparts, s);
+    case 4: return sumsq_launch<4, true>(a, partials, max_parts, nparts, s);
+    case 8: return sumsq_launch<8, true>(a, partials, max_parts, nparts, s);
+    default: return sumsq_launch<0, true>(a, partials, max_parts, nparts, s);
   }
 }
 

@@ -263,6 +263,33 @@ cr_status cr_fsdp_step(const void* const* grads_bf16, int nranks,
                        float* const* v, const cr_adamw_cfg* cfg,
                        void* const* params_bf16, cr_stream_t stream);
 
+/* cr_fsdp_step with global gradient-norm clipping between the
+ * reduce-scatter and AdamW ("AI Infra Guide, Chapter 6", 6.8: the training
+ * loop calls clip_grad_norm_(max_norm=1.0) on the sharded model before the
+ * optimizer step).  norm = L2 norm of the whole averaged fp32 gradient (all
+ * shards: the global norm), accumulated in fp64; every gradient element is
+ * multiplied (one fp32 multiply) by c = min(1, max_norm / (norm + 1e-6)),
+ * formed in double and rounded to fp32, before AdamW.  Two launches: a
+ * sum-of-squares pass over the grads that writes one fp64 partial per CTA
+ * into `workspace`, then the fused step, whose every CTA adds the partials
+ * in the same fixed order (the norm is reproducible run to run).
+ * Algorithmic bytes: (6N + 24) per parameter (the grads are read twice).
+ *   max_norm        finite, > 0 (CR_ERR_INVALID_ARG otherwise)
+ *   workspace       caller-owned device scratch, 8-byte aligned, of
+ *                   workspace_bytes >= 8 bytes; cr_fsdp_clip_workspace_bytes()
+ *                   bytes are always enough (fewer bytes cap the number of
+ *                   CTAs of the first pass).  Contents on entry are ignored.
+ *   norm_out        device pointer (may be NULL) receiving the norm as fp32
+ * Other arguments and errors as cr_fsdp_step; no buffer may overlap another. */
+size_t cr_fsdp_clip_workspace_bytes(void);
+cr_status cr_fsdp_step_clipped(const void* const* grads_bf16, int nranks,
+                               size_t count, float* const* master,
+                               float* const* m, float* const* v,
+                               const cr_adamw_cfg* cfg, double max_norm,
+                               void* workspace, size_t workspace_bytes,
+                               void* const* params_bf16, float* norm_out,
+                               cr_stream_t stream);
+
 /* a9 alone: AdamW as above on n fp32 elements with an fp32 gradient
  * (for example a shard produced by cr_reduce_scatter with out_dtype F32);
  * param_bf16 (may be NULL) receives the bf16 cast of the updated master.

@@ -81,6 +81,9 @@ def lib() -> C.CDLL:
         L.orc_adamw.argtypes = [sz, vp, vp, vp, vp, C.POINTER(_AdamCfg)]
         L.orc_fsdp_step.argtypes = [C.c_int, sz, vp, vp, vp, vp,
                                     C.POINTER(_AdamCfg), vp]
+        L.orc_fsdp_step_clipped.argtypes = [C.c_int, sz, vp, vp, vp, vp,
+                                            C.POINTER(_AdamCfg), C.c_double, vp,
+                                            C.POINTER(C.c_double)]
         L.orc_bucket_plan.argtypes = [C.c_int, vp, sz, sz, vp, vp, vp,
                                       C.POINTER(C.c_int)]
         L.orc_bucket_pack.argtypes = [C.c_int, C.c_int, vp, sz, vp, vp, vp, vp]
@@ -259,6 +262,20 @@ def fsdp_step(grads, master, m, v, cfg: AdamWConfig):
                                _ptrs(m), _ptrs(v), C.byref(c), _ptrs(params)),
            "fsdp_step")
     return params
+
+
+def fsdp_step_clipped(grads, master, m, v, cfg: AdamWConfig, max_norm: float):
+    """FSDP step with global gradient-norm clipping.  Returns (params, norm)."""
+    n, count = len(grads), grads[0].size
+    grads = [np.ascontiguousarray(g, np.uint16) for g in grads]
+    params = [np.zeros(count, np.uint16) for _ in range(n)]
+    c = _cfg(cfg)
+    norm = C.c_double()
+    _check(lib().orc_fsdp_step_clipped(n, count, _ptrs(grads), _ptrs(master),
+                                       _ptrs(m), _ptrs(v), C.byref(c),
+                                       float(max_norm), _ptrs(params),
+                                       C.byref(norm)), "fsdp_step_clipped")
+    return params, norm.value
 
 
 # ---- a6 / a7 ----------------------------------------------------------------

@@ -79,3 +79,58 @@ int orc_fsdp_step(int n, size_t count, const uint16_t* const* grads,
   for (int r = 0; r < n; ++r) { free(gshard[r]); free(pshard[r]); }
   return rc;
 }
+
+/* FSDP step with clip_grad_norm_ between the reduce-scatter and AdamW; see
+ * oracle.h.  The norm is the global one: every owner's squared shard norm
+ * summed over all shards. */
+int orc_fsdp_step_clipped(int n, size_t count, const uint16_t* const* grads,
+                          float* const* master, float* const* m,
+                          float* const* v, const orc_adamw_cfg* cfg,
+                          double max_norm, uint16_t* const* params,
+                          double* norm_out) {
+  if (n < 1 || n > ORC_MAX_RANKS) return ORC_EINVAL;
+  size_t L = orc_chunk_len(count, n);
+  float* gshard[ORC_MAX_RANKS];
+  uint16_t* pshard[ORC_MAX_RANKS];
+  for (int r = 0; r < n; ++r) {
+    gshard[r] = (float*)malloc((L ? L : 1) * sizeof(float));
+    pshard[r] = (uint16_t*)malloc((L ? L : 1) * sizeof(uint16_t));
+    if (!gshard[r] || !pshard[r]) {
+      for (int q = 0; q <= r; ++q) { free(gshard[q]); free(pshard[q]); }
+      return ORC_ENOMEM;
+    }
+  }
+  int rc = orc_ring_reduce_scatter(n, count, ORC_BF16, ORC_AVG,
+                                   (const void* const*)grads,
+                                   (void* const*)gshard, ORC_F32, NULL, NULL,
+                                   NULL);
+  if (rc == ORC_OK) {
+    /* Global norm: each owner's sum of squares, then the sum over owners. */
+    double total = 0.0;
+    for (int j = 0; j < n; ++j) {
+      size_t lo, hi;
+      orc_chunk_bounds(count, n, j, &lo, &hi);
+      double local = 0.0;
+      for (size_t k = 0; k < hi - lo; ++k)
+        local += (double)gshard[j][k] * (double)gshard[j][k];
+      total += local;
+    }
+    double norm = sqrt(total);
+    double coef = max_norm / (norm + 1e-6);
+    if (coef > 1.0) coef = 1.0;
+    float c = (float)coef;
+    if (norm_out) *norm_out = norm;
+    for (int j = 0; j < n; ++j) {
+      size_t lo, hi;
+      orc_chunk_bounds(count, n, j, &lo, &hi);
+      for (size_t k = 0; k < hi - lo; ++k) gshard[j][k] = gshard[j][k] * c;
+      orc_adamw(hi - lo, master[j], m[j], v[j], gshard[j], cfg);
+      for (size_t k = 0; k < hi - lo; ++k)
+        pshard[j][k] = orc_f32_to_bf16(master[j][k]);
+    }
+    rc = orc_ring_all_gather(n, count, ORC_BF16, (const void* const*)pshard,
+                             (void* const*)params, NULL, NULL);
+  }
+  for (int r = 0; r < n; ++r) { free(gshard[r]); free(pshard[r]); }
+  return rc;
+}

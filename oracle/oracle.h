@@ -147,6 +147,20 @@ int orc_fsdp_step(int n, size_t count, const uint16_t* const* grads,
                   float* const* master, float* const* m, float* const* v,
                   const orc_adamw_cfg* cfg, uint16_t* const* params);
 
+/* FSDP step with global gradient-norm clipping ([AIG] 6.8, the production
+ * loop calls clip_grad_norm_(max_norm=1.0) on the sharded model before the
+ * optimizer step).  After the reduce-scatter, the L2 norm of the whole
+ * averaged fp32 gradient (all shards) is computed in double, shard by shard
+ * in element order; the clip coefficient c = max_norm / (norm + 1e-6),
+ * formed in double, capped at 1 and rounded to fp32, multiplies every
+ * gradient element (one fp32 multiply) before AdamW.  *norm_out receives
+ * the norm. */
+int orc_fsdp_step_clipped(int n, size_t count, const uint16_t* const* grads,
+                          float* const* master, float* const* m,
+                          float* const* v, const orc_adamw_cfg* cfg,
+                          double max_norm, uint16_t* const* params,
+                          double* norm_out);
+
 /* ---- a6/a7: DDP gradient buckets ---------------------------------------
  * Plan: tensors are visited in reverse index order (backward order) and
  * appended to the current bucket while its byte size plus the tensor's stays

@@ -195,3 +195,26 @@ def test_bucket_all_reduce_fused_validation(L):
            stream=0)
     expect(2, cr.cr_bucket_all_reduce_fused, cr.cr_bucket_plan([4], 4, 64), 1, [FAKE], "i32",
            "avg", stream=0)
+
+
+def test_fsdp_step_clipped_validation(L):
+    n, count = 2, 16
+    g = [FAKE + r * (1 << 20) for r in range(n)]
+    p = [FAKE + (1 << 28) + r * (1 << 20) for r in range(n)]
+    ms = [FAKE + (2 << 28) + r * (1 << 20) for r in range(n)]
+    m = [FAKE + (3 << 28) + r * (1 << 20) for r in range(n)]
+    v = [FAKE + (4 << 28) + r * (1 << 20) for r in range(n)]
+    ws = FAKE + (5 << 28)
+    nb = cr.cr_fsdp_clip_workspace_bytes()
+    assert nb >= 8 and nb % 8 == 0
+    expect(1, cr.cr_fsdp_step_clipped, g, count, ms, m, v, cr.adamw_cfg(), 0.0, ws, nb, p, stream=0)
+    expect(1, cr.cr_fsdp_step_clipped, g, count, ms, m, v, cr.adamw_cfg(), float("inf"), ws, nb, p,
+           stream=0)
+    expect(1, cr.cr_fsdp_step_clipped, g, count, ms, m, v, cr.adamw_cfg(), 1.0, 0, nb, p, stream=0)
+    expect(1, cr.cr_fsdp_step_clipped, g, count, ms, m, v, cr.adamw_cfg(), 1.0, ws, 4, p, stream=0)
+    expect(3, cr.cr_fsdp_step_clipped, g, count, ms, m, v, cr.adamw_cfg(), 1.0, ws + 4, nb, p,
+           stream=0)
+    expect(1, cr.cr_fsdp_step_clipped, g, count, ms, m, v, cr.adamw_cfg(), 1.0, ms[0], nb, p,
+           stream=0)
+    expect(1, cr.cr_fsdp_step_clipped, g, count, ms, m, v, cr.adamw_cfg(), 1.0, ws, nb, p,
+           norm_out=ws, stream=0)

@@ -508,3 +508,53 @@ def test_fsdp_step_gradient_is_mean_of_ranks():
     assert np.allclose(got_m, 0.1 * mean, rtol=1e-6, atol=0)
     want = 0.5 * (1 - cfg.lr * cfg.weight_decay) - cfg.lr * np.sign(mean)
     assert np.allclose(np.concatenate(master), want, rtol=0, atol=1e-7)
+
+
+# ---- FSDP step with gradient-norm clipping ---------------------------------------
+
+def clip_case(n, count, seed):
+    grads = I.host_rank_buffers(n, count, "bf16", std=1e-3, seed0=seed)
+    master_full = I.np_normal_f32(count, 0.02, seed + 1)
+    sl = [slice(*O.chunk_bounds(count, n, j)) for j in range(n)]
+    mk = lambda: ([master_full[s].copy() for s in sl],
+                  [np.zeros(s.stop - s.start, np.float32) for s in sl],
+                  [np.zeros(s.stop - s.start, np.float32) for s in sl])
+    return grads, mk
+
+
+@pytest.mark.parametrize("n,count", [(2, 14), (4, 400), (8, 8 * 64 + 5), (3, 2)])
+def test_clip_with_large_max_norm_is_the_plain_step(n, count):
+    grads, mk = clip_case(n, count, 50)
+    cfg = O.AdamWConfig()
+    a_master, a_m, a_v = mk()
+    b_master, b_m, b_v = mk()
+    pa = O.fsdp_step(grads, a_master, a_m, a_v, cfg)
+    pb, norm = O.fsdp_step_clipped(grads, b_master, b_m, b_v, cfg, max_norm=1e30)
+    for x, y in zip(pa + a_master + a_m + a_v, pb + b_master + b_m + b_v):
+        assert x.tobytes() == y.tobytes()
+
+
+@pytest.mark.parametrize("n,count", [(4, 4000), (8, 8 * 1000 + 3)])
+def test_clip_norm_and_scaled_gradient(n, count):
+    """The reported norm is numpy's 2-norm of the averaged fp32 gradient
+    (an independent routine); with max_norm = norm / 4 the clipped gradient,
+    read back from m = (1 - b1) g at step 1, has norm max_norm."""
+    grads, mk = clip_case(n, count, 60)
+    cfg = O.AdamWConfig()
+    g_full, _ = O.ring_all_reduce(grads, "bf16", "avg", "f32")
+    want_norm = float(np.linalg.norm(g_full[0].astype(np.float64)))
+    master, m, v = mk()
+    _, norm = O.fsdp_step_clipped(grads, master, m, v, cfg, max_norm=1e30)
+    assert norm == pytest.approx(want_norm, rel=1e-12)
+    master, m, v = mk()
+    _, norm2 = O.fsdp_step_clipped(grads, master, m, v, cfg, max_norm=want_norm / 4)
+    assert norm2 == norm
+    g_clipped = np.concatenate(m).astype(np.float64) / (1 - cfg.beta1)
+    # the clipped norm is max_norm * norm / (norm + 1e-6): slightly below max_norm
+    want_clipped = (want_norm / 4) * want_norm / (want_norm + 1e-6)
+    assert float(np.linalg.norm(g_clipped)) == pytest.approx(want_clipped, rel=1e-6)
+    # elementwise: g' = fl(g * c) with c = fl32(max_norm / (norm + 1e-6))
+    c = np.float32((want_norm / 4) / (norm + 1e-6))
+    gp = (g_full[0] * c).astype(np.float32)
+    want_m = np.float32(1 - cfg.beta1) * gp
+    assert np.max(np.abs(np.concatenate(m) - want_m)) <= 2 ** -22 * np.max(np.abs(want_m))

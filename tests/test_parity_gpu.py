@@ -383,3 +383,60 @@ def test_bucket_all_reduce_fused(n, dt, op, offset):
         for t in range(len(numels)):
             g[r][t].check()
             assert_match(g[r][t].host(), want[r][t], dt, f"rank {r} tensor {t}")
+
+
+# ---- FSDP step with gradient-norm clipping ----------------------------------------
+
+@pytest.mark.parametrize("n", [1, 2, 3, 8, 16])
+@pytest.mark.parametrize("count_fn", [lambda n: 8 * n * 40, lambda n: 8 * n * 40 + 5, lambda n: 3])
+@pytest.mark.parametrize("clip", ["active", "inactive"])
+@pytest.mark.parametrize("ws_parts", [None, 1, 7])
+def test_fsdp_step_clipped(n, count_fn, clip, ws_parts):
+    count = count_fn(n)
+    grads, master, m, v = fsdp_case(n, count, seed=3 * n)
+    g_full, _ = O.ring_all_reduce(grads, "bf16", "avg", "f32")
+    norm = float(np.linalg.norm(g_full[0].astype(np.float64)))
+    max_norm = norm / 3 if clip == "active" else norm * 10 + 1
+    cfg = O.AdamWConfig()
+    d_master = [to_dev(x, "f32") for x in master]
+    d_m = [to_dev(x, "f32") for x in m]
+    d_v = [to_dev(x, "f32") for x in v]
+    d_g = [to_dev(x, "bf16") for x in grads]
+    d_p = [Guarded(count, "bf16") for _ in range(n)]
+    ws_bytes = cr.cr_fsdp_clip_workspace_bytes() if ws_parts is None else 8 * ws_parts
+    ws = torch.empty(ws_bytes // 8, dtype=torch.float64, device="cuda")
+    norm_out = torch.full((1,), -1.0, dtype=torch.float32, device="cuda")
+    want_p, want_norm = O.fsdp_step_clipped(grads, master, m, v, cfg, max_norm)
+    cr.cr_fsdp_step_clipped(d_g, count, d_master, d_m, d_v, cr.adamw_cfg(), max_norm, ws,
+                            ws_bytes, [x.ptr() for x in d_p], norm_out)
+    torch.cuda.synchronize()
+    assert float(norm_out.item()) == pytest.approx(want_norm, rel=1e-6)
+    for j in range(n):
+        for t, ref, name in ((d_master, master, "master"), (d_m, m, "m"), (d_v, v, "v")):
+            assert rel_maxabs(to_host(t[j], "f32"), ref[j]) <= 1e-6, f"{name}[{j}]"
+    for r in range(n):
+        d_p[r].check()
+        assert_match(d_p[r].host(), want_p[r], "bf16", f"params[{r}]")
+
+
+def test_fsdp_step_clipped_is_deterministic():
+    n, count = 8, 8 * 8 * 5000 + 3
+    grads, master, m, v = fsdp_case(n, count, seed=9)
+    d_g = [to_dev(x, "bf16") for x in grads]
+    ws = torch.empty(cr.cr_fsdp_clip_workspace_bytes() // 8, dtype=torch.float64, device="cuda")
+    outs = []
+    for _ in range(3):
+        d_master = [to_dev(x, "f32") for x in master]
+        d_m = [to_dev(x, "f32") for x in m]
+        d_v = [to_dev(x, "f32") for x in v]
+        d_p = [torch.empty(count, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+        norm_out = torch.empty(1, dtype=torch.float32, device="cuda")
+        cr.cr_fsdp_step_clipped(d_g, count, d_master, d_m, d_v, cr.adamw_cfg(), 1e-3, ws,
+                                ws.numel() * 8, d_p, norm_out)
+        torch.cuda.synchronize()
+        outs.append((norm_out.cpu(), [x.cpu() for x in d_master + d_m + d_v],
+                     [x.view(torch.int16).cpu() for x in d_p]))
+    for o in outs[1:]:
+        assert torch.equal(o[0], outs[0][0])
+        assert all(torch.equal(a, b) for a, b in zip(o[1], outs[0][1]))
+        assert all(torch.equal(a, b) for a, b in zip(o[2], outs[0][2]))
