@@ -33,7 +33,8 @@ EXPORTS = ["cr_status_string", "cr_last_error", "cr_version", "cr_chunk_len",
            "cr_all_reduce", "cr_all_reduce_staged", "cr_bucket_plan", "cr_bucket_plan_free",
            "cr_bucket_pack", "cr_bucket_unpack", "cr_bucket_all_reduce",
            "cr_bucket_all_reduce_fused", "cr_fsdp_step",
-           "cr_fsdp_clip_workspace_bytes", "cr_fsdp_step_clipped", "cr_adamw_step", "cr_comm_elems"]
+           "cr_fsdp_clip_workspace_bytes", "cr_fsdp_step_clipped",
+           "cr_fsdp_step_clipped_noalloc", "cr_adamw_step", "cr_comm_elems"]
 
 _lib = None
 
@@ -94,6 +95,8 @@ def lib() -> C.CDLL:
     L.cr_fsdp_clip_workspace_bytes.argtypes = []
     L.cr_fsdp_step_clipped.argtypes = [vp, i, sz, vp, vp, vp, C.POINTER(AdamWCfg), C.c_double,
                                        vp, sz, vp, vp, vp]
+    L.cr_fsdp_step_clipped_noalloc.argtypes = [vp, i, sz, vp, vp, vp, C.POINTER(AdamWCfg),
+                                               C.c_double, vp, vp, vp]
     L.cr_adamw_step.argtypes = [sz, vp, vp, vp, vp, C.POINTER(AdamWCfg), vp, vp]
     L.cr_comm_elems.argtypes = [i, i, i, sz, i, C.POINTER(C.c_uint64),
                                 C.POINTER(C.c_uint64), C.POINTER(i)]
@@ -284,6 +287,17 @@ def cr_fsdp_step_clipped(grads, count, master, m, v, cfg: AdamWCfg, max_norm, wo
                                       C.byref(cfg), float(max_norm), _ptr(workspace),
                                       workspace_bytes, _ptr_array(params), _ptr(norm_out),
                                       _stream(stream)), "cr_fsdp_step_clipped")
+
+
+def cr_fsdp_step_clipped_noalloc(grads, count, master, m, v, cfg: AdamWCfg, max_norm, params,
+                                 norm_out=None, stream=None) -> None:
+    """cr_fsdp_step_clipped with the library's static scratch instead of a
+    caller workspace, for callers that cannot allocate device memory."""
+    _check(lib().cr_fsdp_step_clipped_noalloc(_ptr_array(grads), len(grads), count,
+                                              _ptr_array(master), _ptr_array(m), _ptr_array(v),
+                                              C.byref(cfg), float(max_norm), _ptr_array(params),
+                                              _ptr(norm_out), _stream(stream)),
+           "cr_fsdp_step_clipped_noalloc")
 
 
 def cr_adamw_step(n, master, m, v, grad, cfg: AdamWCfg, param_bf16=None,

@@ -208,6 +208,8 @@ cr_status all_reduce_impl(const void* const* in, int nranks, size_t count,
 
 }  // namespace
 
+void cr::report_error(cr_status status, const char* msg) { fail(status, "%s", msg); }
+
 extern "C" {
 
 const char* cr_status_string(cr_status s) {

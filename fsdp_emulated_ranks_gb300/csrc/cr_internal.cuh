@@ -133,6 +133,9 @@ cudaError_t launch_bucket_fused(cr_dtype d, const FusedArgs& a, uint32_t ntiles,
                                 cudaStream_t s);
 uint64_t fused_tile_elems(cr_dtype d);  // elements of a tensor per CTA tile
 
+// Records `msg` as the detail cr_last_error() returns on this thread.
+void report_error(cr_status status, const char* msg);
+
 // Persistent-grid size for a kBlock-thread kernel that needs `threads`
 // threads of work: min(SMs on the current device * CTAs of `kernel` resident
 // per SM, ceil(threads / kBlock)), at least 1.  Occupancy is queried once

@@ -290,6 +290,33 @@ cr_status cr_fsdp_step_clipped(const void* const* grads_bf16, int nranks,
                                void* const* params_bf16, float* norm_out,
                                cr_stream_t stream);
 
+/* cr_fsdp_step_clipped for callers that cannot allocate device memory.
+ * The pages have no counterpart: this entry point exists for library users
+ * that are handed only their tensors -- for example a plugin of a framework
+ * whose own allocator owns the whole device budget, or latency-critical code
+ * where a cudaMalloc would synchronise the device -- and so have no
+ * workspace to pass.  It runs exactly cr_fsdp_step_clipped (same arguments
+ * minus workspace/workspace_bytes, same results and errors) with the
+ * sum-of-squares partials kept in a static device array of 4096 doubles
+ * (32 KiB) that the library holds on every GPU that loads it until the
+ * process exits.  The first pass uses one partial per CTA and at most 8 CTAs
+ * per SM, so any GPU with up to 512 SMs fits; on a larger one the call
+ * returns CR_ERR_UNSUPPORTED.  The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current)
+ * and caches it; make that first call before any stream capture.  All calls
+ * share the one array: nothing in it needs to start at zero (the first pass
+ * writes every partial the second pass reads), but calls that overlap on
+ * the GPU -- on different streams, unordered -- race on it and must be
+ * serialised by the caller.  Nothing is allocated. */
+cr_status cr_fsdp_step_clipped_noalloc(const void* const* grads_bf16,
+                                       int nranks, size_t count,
+                                       float* const* master, float* const* m,
+                                       float* const* v,
+                                       const cr_adamw_cfg* cfg,
+                                       double max_norm,
+                                       void* const* params_bf16,
+                                       float* norm_out, cr_stream_t stream);
+
 /* a9 alone: AdamW as above on n fp32 elements with an fp32 gradient
  * (for example a shard produced by cr_reduce_scatter with out_dtype F32);
  * param_bf16 (may be NULL) receives the bf16 cast of the updated master.
