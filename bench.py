@@ -467,10 +467,12 @@ def run_headline(args, world, rank, device, stream, peak):
 
 
 def run_e2e(args, bufs, n, count, world, stream, device):
-    """End to end through the C ABI from pinned host memory: every step
-    uploads the 8 rank inputs, all-reduces and downloads the 8 results, in
-    slices pipelined over an upload stream, the compute stream and a
-    download stream (cr_all_reduce_staged)."""
+    """End to end through the C ABI with the rank buffers in pinned host
+    memory: every step moves the 8 inputs host -> GPU, all-reduces them and
+    moves the 8 results GPU -> host.  Default API cr_all_reduce_host (the
+    kernel reads and writes host memory over the coherent host link, both
+    directions at once); --e2e-api staged uses cr_all_reduce_staged (copy
+    engines, sliced and pipelined over upload / compute / download streams)."""
     import torch
     from fsdp_emulated_ranks_gb300 import cr
     host_in = [torch.empty(count, dtype=torch.bfloat16, pin_memory=True) for _ in range(n)]
@@ -480,18 +482,24 @@ def run_e2e(args, bufs, n, count, world, stream, device):
     torch.cuda.synchronize()
     up, down = torch.cuda.Stream(device), torch.cuda.Stream(device)
 
-    def step():
-        cr.cr_all_reduce_staged(host_in, host_out, bufs, count, "bf16", "avg",
-                                args.e2e_slice, stream, up, down)
+    if args.e2e_api == "host":
+        def step():
+            cr.cr_all_reduce_host(host_in, host_out, count, "bf16", "avg", stream=stream)
+    else:
+        def step():
+            cr.cr_all_reduce_staged(host_in, host_out, bufs, count, "bf16", "avg",
+                                    args.e2e_slice, stream, up, down)
 
     steps = max(3, min(args.steps, 50))
     total_ms, _ = timed(step, steps, max(3, min(args.warmup, 5)), world, stream)
     nbytes = ar_bytes(n, count, 2)
     value, ms = job_throughput(nbytes, total_ms, steps, world, device)
-    return {"value": round(value, 2), "unit": UNIT,
-            "h2d_bytes_per_step": n * count * 2, "d2h_bytes_per_step": n * count * 2,
-            "ms_per_step": ms, "steps": steps, "api": "cr_all_reduce_staged",
-            "slice_elems": args.e2e_slice or "auto"}
+    out = {"value": round(value, 2), "unit": UNIT,
+           "h2d_bytes_per_step": n * count * 2, "d2h_bytes_per_step": n * count * 2,
+           "ms_per_step": ms, "steps": steps, "api": f"cr_all_reduce_{args.e2e_api}"}
+    if args.e2e_api == "staged":
+        out["slice_elems"] = args.e2e_slice or "auto"
+    return out
 
 
 def traffic_per_launch(name, launches=1):
@@ -647,7 +655,8 @@ def main(argv=None):
     ap.add_argument("--row-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--e2e-slice", type=int, default=0,
+    ap.add_argument("--e2e-api", choices=["host", "staged"], default="host")
+    ap.add_argument("--e2e-slice", type=int, default=1 << 22,
                     help="elements per slice of the pipelined host all-reduce (0: auto)")
     ap.add_argument("--cpu-sample", type=int, default=1 << 25,
                     help="elements per rank the CPU oracle reduces for cpu_baseline")

@@ -30,7 +30,7 @@ STATUS = {0: "CR_OK", 1: "CR_ERR_INVALID_ARG", 2: "CR_ERR_UNSUPPORTED",
 # Every symbol include/cr.h declares.
 EXPORTS = ["cr_status_string", "cr_last_error", "cr_version", "cr_chunk_len",
            "cr_shard_range", "cr_reduce_scatter", "cr_all_gather",
-           "cr_all_reduce", "cr_all_reduce_staged", "cr_bucket_plan", "cr_bucket_plan_free",
+           "cr_all_reduce", "cr_all_reduce_host", "cr_all_reduce_staged", "cr_bucket_plan", "cr_bucket_plan_free",
            "cr_bucket_pack", "cr_bucket_unpack", "cr_bucket_all_reduce",
            "cr_bucket_all_reduce_fused", "cr_fsdp_step",
            "cr_fsdp_clip_workspace_bytes", "cr_fsdp_step_clipped",
@@ -82,6 +82,7 @@ def lib() -> C.CDLL:
     L.cr_reduce_scatter.argtypes = [vp, i, sz, i, i, vp, i, vp]
     L.cr_all_gather.argtypes = [vp, i, sz, i, vp, vp]
     L.cr_all_reduce.argtypes = [vp, i, sz, i, i, vp, i, vp]
+    L.cr_all_reduce_host.argtypes = [vp, vp, vp, i, sz, i, i, vp]
     L.cr_all_reduce_staged.argtypes = [vp, vp, vp, i, sz, i, i, sz, vp, vp, vp]
     L.cr_bucket_plan.argtypes = [vp, i, sz, sz, C.POINTER(C.POINTER(BucketPlanT))]
     L.cr_bucket_plan_free.restype = None
@@ -189,6 +190,13 @@ def cr_all_reduce(inbufs, count, in_dtype, op, outbufs, out_dtype,
                                _dtype(in_dtype), _op(op), _ptr_array(outbufs),
                                _dtype(out_dtype), _stream(stream)),
            "cr_all_reduce")
+
+
+def cr_all_reduce_host(host_in, host_out, count, dtype, op, dev_out=None, stream=None) -> None:
+    _check(lib().cr_all_reduce_host(_ptr_array(host_in), _ptr_array(host_out),
+                                    _ptr_array(dev_out) if dev_out is not None else None,
+                                    len(host_in), count, _dtype(dtype), _op(op), _stream(stream)),
+           "cr_all_reduce_host")
 
 
 def cr_all_reduce_staged(host_in, host_out, dev_bufs, count, dtype, op,

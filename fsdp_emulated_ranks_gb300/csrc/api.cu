@@ -199,6 +199,7 @@ cr_status all_reduce_impl(const void* const* in, int nranks, size_t count,
   a.begin = 0;
   a.end = count;
   a.n = nranks;
+  a.n_out = nranks;
   a.avg = op == CR_AVG;
   a.inv_n = exact_inv_n(nranks);
   cudaError_t e = launch_fold(in_dtype, out_dtype, kAR, a, vec, stream);
@@ -285,6 +286,7 @@ cr_status cr_reduce_scatter(const void* const* bufs, int nranks, size_t count,
   a.begin = 0;
   a.end = count;
   a.n = nranks;
+  a.n_out = nranks;
   a.avg = op == CR_AVG;
   a.inv_n = exact_inv_n(nranks);
   cudaError_t e = launch_fold(in_dtype, out_dtype, kRS, a, vec, (cudaStream_t)stream);
@@ -345,6 +347,70 @@ cr_status cr_all_reduce(const void* const* in, int nranks, size_t count,
                          (cudaStream_t)stream);
 }
 
+// Device address of a host buffer the GPU can read and write directly
+// (pinned with cudaHostAlloc / cudaHostRegister, or managed memory).
+static cr_status host_view(const void* p, const char* what, int r, void** dptr) {
+  cudaPointerAttributes at;
+  cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes");
+  if ((at.type != cudaMemoryTypeHost && at.type != cudaMemoryTypeManaged) || !at.devicePointer)
+    return fail(CR_ERR_INVALID_ARG, "%s[%d]=%p is not pinned (page-locked, mapped) host memory",
+                what, r, p);
+  *dptr = at.devicePointer;
+  return CR_OK;
+}
+
+cr_status cr_all_reduce_host(const void* const* host_in, void* const* host_out,
+                             void* const* dev_out, int nranks, size_t count, cr_dtype dtype,
+                             cr_op op, cr_stream_t stream) {
+  cr_status st = check_common(nranks, count, host_in, host_out);
+  if (st) return st;
+  if ((st = check_pair(dtype, op, dtype))) return st;
+  if (dev_out && nranks > CR_MAX_RANKS / 2)
+    return fail(CR_ERR_UNSUPPORTED, "dev_out needs nranks <= %d", CR_MAX_RANKS / 2);
+  const size_t es = esize_of(dtype);
+  std::vector<Span> spans;
+  for (int r = 0; r < nranks; ++r) {
+    if ((st = check_buf(host_in[r], count, es, "host_in", r))) return st;
+    if ((st = check_buf(host_out[r], count, es, "host_out", r))) return st;
+    if (dev_out && (st = check_buf(dev_out[r], count, es, "dev_out", r))) return st;
+    if (count) {
+      spans.push_back(span_of(host_in[r], count * es, 0, r));
+      spans.push_back(span_of(host_out[r], count * es, 1, r));
+      if (dev_out) spans.push_back(span_of(dev_out[r], count * es, 1, 100 + r));
+    }
+  }
+  st = check_overlaps(spans, [](const Span& i, const Span& o) {
+    return i.rank == o.rank && i.a == o.a && i.b == o.b;  // in place per rank
+  });
+  if (st) return st;
+  if (count == 0) return ok();
+  FoldArgs a;
+  memset(&a, 0, sizeof(a));
+  bool vec = true;
+  for (int r = 0; r < nranks; ++r) {
+    void* din = nullptr;
+    void* dout = nullptr;
+    if ((st = host_view(host_in[r], "host_in", r, &din))) return st;
+    if ((st = host_view(host_out[r], "host_out", r, &dout))) return st;
+    a.in[r] = din;
+    a.out[r] = dout;
+    if (dev_out) a.out[nranks + r] = dev_out[r];
+    vec = vec && aligned(din, 16) && aligned(dout, 16) && (!dev_out || aligned(dev_out[r], 16));
+  }
+  a.count = count;
+  a.L = (count + nranks - 1) / nranks;
+  a.begin = 0;
+  a.end = count;
+  a.n = nranks;
+  a.n_out = dev_out ? 2 * nranks : nranks;
+  a.avg = op == CR_AVG;
+  a.inv_n = exact_inv_n(nranks);
+  cudaError_t e = launch_fold(dtype, dtype, kAR, a, vec, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "all_reduce_host launch");
+  return ok();
+}
+
 cr_status cr_all_reduce_staged(const void* const* host_in, void* const* host_out,
                                void* const* dev_bufs, int nranks, size_t count,
                                cr_dtype dtype, cr_op op, size_t slice_elems,
@@ -391,6 +457,7 @@ cr_status cr_all_reduce_staged(const void* const* host_in, void* const* host_out
   a.count = count;
   a.L = (count + nranks - 1) / nranks;
   a.n = nranks;
+  a.n_out = nranks;
   a.avg = op == CR_AVG;
   a.inv_n = exact_inv_n(nranks);
 

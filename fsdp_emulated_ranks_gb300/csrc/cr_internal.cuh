@@ -24,6 +24,8 @@ struct FoldArgs {
   uint64_t begin;  // the call covers elements [begin, end) of each buffer
   uint64_t end;
   int n;           // ranks
+  int n_out;       // all-reduce: output buffers written (n, or 2n when the
+                   // result also goes to a second set of buffers)
   int avg;         // 1: divide the finished sum by n
   float inv_n;     // 1/n when n is a power of two (exact), else 0
 };

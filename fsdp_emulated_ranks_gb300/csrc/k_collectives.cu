@@ -34,7 +34,7 @@ __device__ __forceinline__ void fold_store_elem(const FoldArgs& a, int n, uint64
   if constexpr (MODE == kRS) {
     st_elem<DO>(a.out[j], e - (uint64_t)j * a.L, x);
   } else {
-    for (int r = 0; r < n; ++r) st_elem<DO>(a.out[r], e, x);
+    for (int r = 0; r < a.n_out; ++r) st_elem<DO>(a.out[r], e, x);
   }
 }
 
@@ -77,8 +77,9 @@ __global__ void __launch_bounds__(kBlock)
     if constexpr (MODE == kRS) {
       st_words<OB>(static_cast<unsigned char*>(a.out[j]) + (e0 - j64 * a.L) * OS, w);
     } else {
+      const int n_out = NT > 0 && NT <= 32 && a.n_out == NT ? NT : a.n_out;
 #pragma unroll 8
-      for (int r = 0; r < n; ++r)
+      for (int r = 0; r < n_out; ++r)
         st_words<OB>(static_cast<unsigned char*>(a.out[r]) + e0 * OS, w);
     }
   }

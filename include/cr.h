@@ -165,6 +165,23 @@ cr_status cr_all_reduce_staged(const void* const* host_in,
                                cr_stream_t compute_stream,
                                cr_stream_t h2d_stream, cr_stream_t d2h_stream);
 
+/* The same all-reduce for rank buffers in pinned host memory, read and
+ * written by the kernel itself over the GPU's coherent host link: every
+ * input byte crosses the link once towards the GPU, every result byte once
+ * back, with no staging copy in HBM (the reduced values go to dev_out as
+ * well when it is non-NULL).  On a GB300 the link, not HBM, bounds this
+ * call; it moves the same bytes as upload + all-reduce + download, but
+ * with both directions in flight at once.
+ *   host_in[r], host_out[r]  count elements each, page-locked and mapped
+ *                            (cudaHostAlloc, cudaHostRegister or managed);
+ *                            host_out[r] == host_in[r] is allowed (in place)
+ *   dev_out                  NULL, or nranks device buffers (nranks <= 32)
+ * CR_ERR_INVALID_ARG for host memory the GPU cannot address (pageable
+ * memory: use cr_all_reduce_staged), otherwise errors as cr_all_reduce. */
+cr_status cr_all_reduce_host(const void* const* host_in, void* const* host_out,
+                             void* const* dev_out, int nranks, size_t count,
+                             cr_dtype dtype, cr_op op, cr_stream_t stream);
+
 /* ---- a6: DDP bucket plan (host) -------------------------------------------
  * [AIG] 6.2.4: gradients go into buckets (default 25 MB) in the order
  * backward produces them; [AIG] 6.2.6 Horovod Tensor Fusion; [NX] 5.1.

@@ -218,3 +218,17 @@ def test_fsdp_step_clipped_validation(L):
            stream=0)
     expect(1, cr.cr_fsdp_step_clipped, g, count, ms, m, v, cr.adamw_cfg(), 1.0, ws, nb, p,
            norm_out=ws, stream=0)
+
+
+def test_all_reduce_host_validation(L):
+    n = 2
+    h = [FAKE + r * (1 << 20) for r in range(n)]
+    o = [FAKE + (1 << 30) + r * (1 << 20) for r in range(n)]
+    d = [FAKE + (2 << 30) + r * (1 << 20) for r in range(n)]
+    expect(1, cr.cr_all_reduce_host, h, [o[0], o[0]], 16, "f32", "sum", stream=0)
+    expect(1, cr.cr_all_reduce_host, h, [h[1], o[1]], 16, "f32", "sum", stream=0)
+    expect(1, cr.cr_all_reduce_host, h, o, 16, "f32", "sum", dev_out=[d[0], o[1]], stream=0)
+    expect(2, cr.cr_all_reduce_host, h, o, 16, "i32", "avg", stream=0)
+    expect(3, cr.cr_all_reduce_host, [h[0] + 2, h[1]], o, 16, "f32", "sum", stream=0)
+    expect(2, cr.cr_all_reduce_host, h * 17, o * 17, 16, "f32", "sum", dev_out=d * 17, stream=0)
+    cr.cr_all_reduce_host(h, o, 0, "f32", "sum", stream=0)

@@ -440,3 +440,35 @@ def test_fsdp_step_clipped_is_deterministic():
         assert torch.equal(o[0], outs[0][0])
         assert all(torch.equal(a, b) for a, b in zip(o[1], outs[0][1]))
         assert all(torch.equal(a, b) for a, b in zip(o[2], outs[0][2]))
+
+
+# ---- all-reduce read and written straight from pinned host memory ------------------
+
+@pytest.mark.parametrize("n,count", [(8, 8 * 8 * 1000 + 13), (4, 1 << 16), (3, 1000), (1, 77), (32, 4099)])
+@pytest.mark.parametrize("dt,op", [("bf16", "avg"), ("f32", "sum"), ("i32", "sum")])
+@pytest.mark.parametrize("mode", ["out", "in_place", "with_dev"])
+def test_all_reduce_host(n, count, dt, op, mode):
+    host = host_inputs(n, count, dt, seed=count + 7 * n)
+    want, _ = O.ring_all_reduce(host, dt, op, dt)
+    tdt = {"bf16": torch.bfloat16, "f32": torch.float32, "i32": torch.int32}[dt]
+    h_in = [to_dev(x, dt).cpu().pin_memory() for x in host]
+    h_out = h_in if mode == "in_place" else [torch.empty(count, dtype=tdt).pin_memory()
+                                             for _ in range(n)]
+    d_out = [Guarded(count, dt) for _ in range(n)] if mode == "with_dev" else None
+    cr.cr_all_reduce_host(h_in, h_out, count, dt, op,
+                          dev_out=[g.ptr() for g in d_out] if d_out else None)
+    torch.cuda.synchronize()
+    for r in range(n):
+        got = h_out[r].view(torch.int16).numpy().view(np.uint16) if dt == "bf16" else h_out[r].numpy()
+        assert_match(got, want[r], dt, f"host_out rank {r}")
+        if d_out:
+            d_out[r].check()
+            assert_match(d_out[r].host(), want[r], dt, f"dev_out rank {r}")
+
+
+def test_all_reduce_host_rejects_pageable_memory():
+    n, count = 2, 1024
+    pageable = [torch.zeros(count, dtype=torch.float32) for _ in range(n)]
+    with pytest.raises(cr.CRError) as ei:
+        cr.cr_all_reduce_host(pageable, pageable, count, "f32", "sum")
+    assert ei.value.status == 1 and "pinned" in str(ei.value)
