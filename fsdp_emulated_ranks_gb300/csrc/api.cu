@@ -136,6 +136,21 @@ Span span_of(const void* p, uint64_t bytes, int kind, int rank) {
   return Span{a, a + bytes, kind, rank};
 }
 
+// Widest vector access every buffer of a call allows: 32 or 16 bytes, or
+// 0 for the element-wise kernels.
+struct Width {
+  bool w16 = true, w32 = true;
+  void ptr(const void* p) {
+    w16 = w16 && aligned(p, 16);
+    w32 = w32 && aligned(p, 32);
+  }
+  void bytes(uint64_t b) {
+    w16 = w16 && b % 16 == 0;
+    w32 = w32 && b % 32 == 0;
+  }
+  int get() const { return w32 ? 32 : (w16 ? 16 : 0); }
+};
+
 float exact_inv_n(int n) {
   return (n & (n - 1)) == 0 ? 1.0f / (float)n : 0.0f;
 }
@@ -172,14 +187,15 @@ cr_status all_reduce_impl(const void* const* in, int nranks, size_t count,
   if ((st = check_pair(in_dtype, op, out_dtype))) return st;
   const size_t is = esize_of(in_dtype), os = esize_of(out_dtype);
   std::vector<Span> spans;
-  bool vec = true;
+  Width vw;
   for (int r = 0; r < nranks; ++r) {
     if ((st = check_buf(in[r], count, is, "in", r))) return st;
     if ((st = check_buf(out[r], count, os, "out", r))) return st;
     if (count) {
       spans.push_back(span_of(in[r], count * is, 0, r));
       spans.push_back(span_of(out[r], count * os, 1, r));
-      vec = vec && aligned(in[r], 16) && aligned(out[r], 16);
+      vw.ptr(in[r]);
+      vw.ptr(out[r]);
     }
   }
   const bool same = in_dtype == out_dtype;
@@ -202,7 +218,7 @@ cr_status all_reduce_impl(const void* const* in, int nranks, size_t count,
   a.n_out = nranks;
   a.avg = op == CR_AVG;
   a.inv_n = exact_inv_n(nranks);
-  cudaError_t e = launch_fold(in_dtype, out_dtype, kAR, a, vec, stream);
+  cudaError_t e = launch_fold(in_dtype, out_dtype, kAR, a, vw.get(), stream);
   if (e != cudaSuccess) return cuda_fail(e, "all_reduce launch");
   return ok();
 }
@@ -254,18 +270,20 @@ cr_status cr_reduce_scatter(const void* const* bufs, int nranks, size_t count,
   const size_t is = esize_of(in_dtype), os = esize_of(out_dtype);
   const uint64_t L = cr_chunk_len(count, nranks);
   std::vector<Span> spans;
-  bool vec = (L * is) % 16 == 0 && (L * os) % 16 == 0;
+  Width vw;
+  vw.bytes(L * is);
+  vw.bytes(L * os);
   for (int r = 0; r < nranks; ++r) {
     const uint64_t len = chunk_size(count, L, r);
     if ((st = check_buf(bufs[r], count, is, "bufs", r))) return st;
     if ((st = check_buf(out_shards[r], len, os, "out_shards", r))) return st;
     if (count) {
       spans.push_back(span_of(bufs[r], count * is, 0, r));
-      vec = vec && aligned(bufs[r], 16);
+      vw.ptr(bufs[r]);
     }
     if (len) {
       spans.push_back(span_of(out_shards[r], len * os, 1, r));
-      vec = vec && aligned(out_shards[r], 16);
+      vw.ptr(out_shards[r]);
     }
   }
   const bool same = in_dtype == out_dtype;
@@ -289,7 +307,7 @@ cr_status cr_reduce_scatter(const void* const* bufs, int nranks, size_t count,
   a.n_out = nranks;
   a.avg = op == CR_AVG;
   a.inv_n = exact_inv_n(nranks);
-  cudaError_t e = launch_fold(in_dtype, out_dtype, kRS, a, vec, (cudaStream_t)stream);
+  cudaError_t e = launch_fold(in_dtype, out_dtype, kRS, a, vw.get(), (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "reduce_scatter launch");
   return ok();
 }
@@ -302,7 +320,8 @@ cr_status cr_all_gather(const void* const* shards, int nranks, size_t count,
   if (!es) return fail(CR_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
   const uint64_t L = cr_chunk_len(count, nranks);
   std::vector<Span> spans;
-  bool vec = (L * es) % 16 == 0;
+  Width vw;
+  vw.bytes(L * es);
   uint64_t inplace = 0;
   for (int r = 0; r < nranks; ++r) {
     const uint64_t len = chunk_size(count, L, r);
@@ -310,14 +329,14 @@ cr_status cr_all_gather(const void* const* shards, int nranks, size_t count,
     if ((st = check_buf(bufs[r], count, es, "bufs", r))) return st;
     if (len) {
       spans.push_back(span_of(shards[r], len * es, 0, r));
-      vec = vec && aligned(shards[r], 16);
+      vw.ptr(shards[r]);
       if (count && reinterpret_cast<uintptr_t>(shards[r]) ==
                        reinterpret_cast<uintptr_t>(bufs[r]) + L * (uint64_t)r * es)
         inplace |= 1ull << r;
     }
     if (count) {
       spans.push_back(span_of(bufs[r], count * es, 1, r));
-      vec = vec && aligned(bufs[r], 16);
+      vw.ptr(bufs[r]);
     }
   }
   st = check_overlaps(spans, [&](const Span& i, const Span& o) {
@@ -335,7 +354,7 @@ cr_status cr_all_gather(const void* const* shards, int nranks, size_t count,
   a.L = L;
   a.n = nranks;
   a.inplace_mask = inplace;
-  cudaError_t e = launch_gather(es, a, vec, (cudaStream_t)stream);
+  cudaError_t e = launch_gather(es, a, vw.get(), (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "all_gather launch");
   return ok();
 }
@@ -387,7 +406,7 @@ cr_status cr_all_reduce_host(const void* const* host_in, void* const* host_out,
   if (count == 0) return ok();
   FoldArgs a;
   memset(&a, 0, sizeof(a));
-  bool vec = true;
+  Width vw;
   for (int r = 0; r < nranks; ++r) {
     void* din = nullptr;
     void* dout = nullptr;
@@ -396,7 +415,9 @@ cr_status cr_all_reduce_host(const void* const* host_in, void* const* host_out,
     a.in[r] = din;
     a.out[r] = dout;
     if (dev_out) a.out[nranks + r] = dev_out[r];
-    vec = vec && aligned(din, 16) && aligned(dout, 16) && (!dev_out || aligned(dev_out[r], 16));
+    vw.ptr(din);
+    vw.ptr(dout);
+    if (dev_out) vw.ptr(dev_out[r]);
   }
   a.count = count;
   a.L = (count + nranks - 1) / nranks;
@@ -406,7 +427,7 @@ cr_status cr_all_reduce_host(const void* const* host_in, void* const* host_out,
   a.n_out = dev_out ? 2 * nranks : nranks;
   a.avg = op == CR_AVG;
   a.inv_n = exact_inv_n(nranks);
-  cudaError_t e = launch_fold(dtype, dtype, kAR, a, vec, (cudaStream_t)stream);
+  cudaError_t e = launch_fold(dtype, dtype, kAR, a, vw.get(), (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "all_reduce_host launch");
   return ok();
 }
@@ -422,7 +443,7 @@ cr_status cr_all_reduce_staged(const void* const* host_in, void* const* host_out
   if ((st = check_pair(dtype, op, dtype))) return st;
   const size_t es = esize_of(dtype);
   std::vector<Span> dev_spans, out_spans;
-  bool vec = true;
+  Width vw;
   for (int r = 0; r < nranks; ++r) {
     if ((st = check_buf(host_in[r], count, es, "host_in", r))) return st;
     if ((st = check_buf(host_out[r], count, es, "host_out", r))) return st;
@@ -430,7 +451,7 @@ cr_status cr_all_reduce_staged(const void* const* host_in, void* const* host_out
     if (count) {
       dev_spans.push_back(span_of(dev_bufs[r], count * es, 1, r));
       out_spans.push_back(span_of(host_out[r], count * es, 1, r));
-      vec = vec && aligned(dev_bufs[r], 16);
+      vw.ptr(dev_bufs[r]);
     }
   }
   auto never = [](const Span&, const Span&) { return false; };
@@ -493,7 +514,7 @@ cr_status cr_all_reduce_staged(const void* const* host_in, void* const* host_out
     if (e == cudaSuccess) {
       a.begin = lo;
       a.end = hi;
-      e = launch_fold(dtype, dtype, kAR, a, vec, sc);
+      e = launch_fold(dtype, dtype, kAR, a, vw.get(), sc);
     }
     if (e == cudaSuccess) e = new_event(&ev_out);
     if (e == cudaSuccess) e = cudaEventRecord(ev_out, sc);
@@ -516,17 +537,22 @@ cr_status cr_all_reduce_staged(const void* const* host_in, void* const* host_out
 
 namespace {
 
-// Shared argument checks of the FSDP step entry points; fills `a` and `vec`.
+// Shared argument checks of the FSDP step entry points; fills `a` and the
+// vector width `vw`.
 cr_status fsdp_prepare(const void* const* grads_bf16, int nranks, size_t count,
                        float* const* master, float* const* m, float* const* v,
                        const cr_adamw_cfg* cfg, void* const* params_bf16,
-                       std::vector<Span>& spans, FsdpArgs& a, bool& vec) {
+                       std::vector<Span>& spans, FsdpArgs& a, int& vw) {
   cr_status st = check_common(nranks, count, grads_bf16, params_bf16);
   if (st) return st;
   if (!master || !m || !v) return fail(CR_ERR_INVALID_ARG, "master/m/v array is NULL");
   if ((st = check_adam_cfg(cfg))) return st;
   const uint64_t L = cr_chunk_len(count, nranks);
-  vec = L % 8 == 0;
+  // Vector path: 16-byte bf16 grads/params and 16- (or 32-) byte fp32
+  // state vectors of 8 elements, which needs L % 8 == 0.
+  Width gw, sw;
+  gw.bytes(L * 2);
+  sw.bytes(L * 4);
   for (int r = 0; r < nranks; ++r) {
     const uint64_t len = chunk_size(count, L, r);
     if ((st = check_buf(grads_bf16[r], count, 2, "grads", r))) return st;
@@ -539,15 +565,19 @@ cr_status fsdp_prepare(const void* const* grads_bf16, int nranks, size_t count,
       // "output" span: no two may overlap.
       spans.push_back(span_of(grads_bf16[r], count * 2, 1, r));
       spans.push_back(span_of(params_bf16[r], count * 2, 1, r));
-      vec = vec && aligned(grads_bf16[r], 16) && aligned(params_bf16[r], 16);
+      gw.ptr(grads_bf16[r]);
+      gw.ptr(params_bf16[r]);
     }
     if (len) {
       spans.push_back(span_of(master[r], len * 4, 1, r));
       spans.push_back(span_of(m[r], len * 4, 1, r));
       spans.push_back(span_of(v[r], len * 4, 1, r));
-      vec = vec && aligned(master[r], 16) && aligned(m[r], 16) && aligned(v[r], 16);
+      sw.ptr(master[r]);
+      sw.ptr(m[r]);
+      sw.ptr(v[r]);
     }
   }
+  vw = (gw.w16 && sw.w16) ? (sw.w32 ? 32 : 16) : 0;
   memset(&a, 0, sizeof(a));
   for (int r = 0; r < nranks; ++r) {
     a.grads[r] = grads_bf16[r];
@@ -574,13 +604,13 @@ cr_status cr_fsdp_step(const void* const* grads_bf16, int nranks, size_t count,
                        cr_stream_t stream) {
   std::vector<Span> spans;
   FsdpArgs a;
-  bool vec = false;
+  int vw = 0;
   cr_status st = fsdp_prepare(grads_bf16, nranks, count, master, m, v, cfg, params_bf16,
-                              spans, a, vec);
+                              spans, a, vw);
   if (st) return st;
   if ((st = check_overlaps(spans, [](const Span&, const Span&) { return false; }))) return st;
   if (count == 0) return ok();
-  cudaError_t e = launch_fsdp(a, vec, (cudaStream_t)stream);
+  cudaError_t e = launch_fsdp(a, vw, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "fsdp_step launch");
   return ok();
 }
@@ -594,9 +624,9 @@ cr_status cr_fsdp_step_clipped(const void* const* grads_bf16, int nranks, size_t
                                float* norm_out, cr_stream_t stream) {
   std::vector<Span> spans;
   FsdpArgs a;
-  bool vec = false;
+  int vw = 0;
   cr_status st = fsdp_prepare(grads_bf16, nranks, count, master, m, v, cfg, params_bf16,
-                              spans, a, vec);
+                              spans, a, vw);
   if (st) return st;
   if (!(max_norm > 0.0) || !isfinite(max_norm))
     return fail(CR_ERR_INVALID_ARG, "max_norm must be finite and > 0");
@@ -620,14 +650,14 @@ cr_status cr_fsdp_step_clipped(const void* const* grads_bf16, int nranks, size_t
   }
   double* partials = static_cast<double*>(workspace);
   int nparts = 0;
-  cudaError_t e = launch_fsdp_sumsq(a, vec, partials, (int)max_parts, &nparts,
+  cudaError_t e = launch_fsdp_sumsq(a, vw != 0, partials, (int)max_parts, &nparts,
                                     (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "fsdp_step_clipped sum-of-squares launch");
   a.partials = partials;
   a.nparts = nparts;
   a.max_norm = max_norm;
   a.norm_out = norm_out;
-  e = launch_fsdp(a, vec, (cudaStream_t)stream);
+  e = launch_fsdp(a, vw, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "fsdp_step_clipped launch");
   return ok();
 }
@@ -820,12 +850,13 @@ cr_status cr_bucket_all_reduce_fused(const cr_bucket_plan_t* plan, int nranks,
     d.off = plan->tensor_offset[t];
     d.Lb = cr_chunk_len(plan->bucket_numel[plan->tensor_bucket[t]], nranks);
     d.ptr0 = (uint32_t)(k * nranks);
-    d.vec = 1;
+    Width w;
     for (int r = 0; r < nranks; ++r) {
       void* p = tensors[(size_t)r * T + t];
       args.ptrs[k * nranks + r] = p;
-      if (!aligned(p, 16)) d.vec = 0;
+      w.ptr(p);
     }
+    d.vw = (uint32_t)w.get();
     args.tile_start[k] = ntiles;
     args.ntens += 1;
     ntiles += (uint32_t)tiles;

@@ -85,7 +85,7 @@ struct CopySeg {
 };
 
 constexpr int kMaxSegsPerLaunch = 1024;
-constexpr int kCopyTileBytes = 32768;  // bytes of destination per CTA tile
+constexpr int kCopyTileBytes = 8192;  // bytes of destination per CTA tile
 
 struct CopyArgs {
   int nseg;
@@ -99,12 +99,12 @@ struct FusedTensor {
   uint64_t off;    // element offset of the tensor inside its bucket
   uint64_t Lb;     // chunk length of its bucket, ceil(bucket numel / N)
   uint32_t ptr0;   // index of rank 0's pointer in FusedArgs::ptrs
-  uint32_t vec;    // 1: all N rank pointers are 16-byte aligned
+  uint32_t vw;     // vector bytes all N rank pointers allow: 32, 16 or 0
 };
 
 constexpr int kFusedMaxTensors = 128;
 constexpr int kFusedMaxPtrs = 2048;
-constexpr int kFusedVecPerThread = 4;  // 16-byte vectors per thread per tile
+constexpr uint64_t kFusedTileElems = 4096;  // elements of a tensor per CTA
 
 struct FusedArgs {
   int ntens;
@@ -118,13 +118,14 @@ struct FusedArgs {
 
 enum FoldMode { kRS = 0, kAR = 1 };
 
-// Launchers (defined next to their kernels).  `vec` selects the 16-byte
-// vector kernel; the host layer has checked its preconditions.
+// Launchers (defined next to their kernels).  `vw` is the vector width in
+// bytes the host layer has checked the buffers allow: 32, 16, or 0 for the
+// element-wise kernels.
 cudaError_t launch_fold(cr_dtype in, cr_dtype out, FoldMode mode,
-                        const FoldArgs& a, bool vec, cudaStream_t s);
-cudaError_t launch_gather(size_t esize, const GatherArgs& a, bool vec,
+                        const FoldArgs& a, int vw, cudaStream_t s);
+cudaError_t launch_gather(size_t esize, const GatherArgs& a, int vw,
                           cudaStream_t s);
-cudaError_t launch_fsdp(const FsdpArgs& a, bool vec, cudaStream_t s);
+cudaError_t launch_fsdp(const FsdpArgs& a, int vw, cudaStream_t s);
 // Sum-of-squares pass of the clipped step: writes *nparts (<= max_parts)
 // fp64 partials to `partials`.
 cudaError_t launch_fsdp_sumsq(const FsdpArgs& a, bool vec, double* partials,
@@ -143,5 +144,14 @@ void report_error(cr_status status, const char* msg);
 // per SM, ceil(threads / kBlock)), at least 1.  Occupancy is queried once
 // per (kernel, device) and cached.
 cudaError_t persistent_grid(const void* kernel, uint64_t threads, int* grid);
+
+// Grid of ceil(threads / kBlock) CTAs (at least 1, at most 2^30; kernels
+// keep a grid-stride loop for anything beyond).
+inline unsigned flat_grid(uint64_t threads) {
+  uint64_t g = (threads + kBlock - 1) / kBlock;
+  if (g < 1) g = 1;
+  if (g > (1ull << 30)) g = 1ull << 30;
+  return (unsigned)g;
+}
 
 }  // namespace cr

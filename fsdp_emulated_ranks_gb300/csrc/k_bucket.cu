@@ -5,8 +5,8 @@
 // of many contiguous byte ranges into others.  One launch copies up to
 // kMaxSegsPerLaunch ranges, described in its __grid_constant__ parameter
 // block (no device-side table, no allocation).  Work is cut into tiles of
-// kCopyTileBytes of destination; CTAs walk the tiles with a grid stride and
-// find a tile's range by binary search over the per-range tile prefix sum.
+// kCopyTileBytes of destination, one per CTA; a CTA finds its tile's range
+// by binary search over the per-range tile prefix sum.
 //
 // Inside a range the destination is written in aligned 16-byte vectors.
 // When the source is misaligned relative to the destination (bucket offsets
@@ -119,11 +119,7 @@ __global__ void __launch_bounds__(kBlock)
 
 cudaError_t launch_copy(const CopyArgs& a, uint32_t ntiles, cudaStream_t s) {
   if (ntiles == 0) return cudaSuccess;
-  int grid = 0;
-  cudaError_t err = persistent_grid(reinterpret_cast<const void*>(k_copy_segments),
-                                    (uint64_t)ntiles * kBlock, &grid);
-  if (err != cudaSuccess) return err;
-  k_copy_segments<<<grid, kBlock, 0, s>>>(a, ntiles);
+  k_copy_segments<<<flat_grid((uint64_t)ntiles * kBlock), kBlock, 0, s>>>(a, ntiles);
   return cudaGetLastError();
 }
 

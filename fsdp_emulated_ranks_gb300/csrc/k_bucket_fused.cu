@@ -14,7 +14,8 @@
 //
 // One launch covers up to kFusedMaxTensors tensors whose N rank pointers
 // (kFusedMaxPtrs in all) travel in the __grid_constant__ parameter block;
-// CTAs walk tiles of one tensor each with a grid stride.
+// each CTA takes one tile of kFusedTileElems elements of one tensor, in
+// 32-byte vectors when all of that tensor's rank pointers allow it.
 #include "cr_internal.cuh"
 #include "fold.cuh"
 
@@ -38,13 +39,47 @@ __device__ __forceinline__ void fused_elem(const FusedArgs& a, const FusedTensor
   for (int q = 0; q < n; ++q) st_elem<D>(a.ptrs[t.ptr0 + q], i, acc);
 }
 
+// Vectors of NW words over tensor elements [e_lo, e_hi) of one tile; the
+// ragged end of the tensor (fewer than a vector) goes element by element.
+template <int D, int NT, int NW>
+__device__ __forceinline__ void fused_tile(const FusedArgs& a, const FusedTensor& t, int n,
+                                           uint64_t e_lo, uint64_t e_hi) {
+  using Acc = typename Elem<D>::Acc;
+  constexpr int IS = Elem<D>::kSize;
+  constexpr int VEC = elems_per<D, NW>();
+  constexpr int OB = VEC * IS;
+  const uint64_t v_hi = e_hi / VEC;  // e_lo is a multiple of VEC
+  for (uint64_t iv = e_lo / VEC + threadIdx.x; iv < v_hi; iv += kBlock) {
+    const uint64_t e0 = iv * VEC;
+    const uint64_t p0 = t.off + e0;
+    const uint64_t j64 = p0 / t.Lb;
+    if (p0 + VEC > (j64 + 1) * t.Lb) {  // straddles a chunk of the bucket
+      for (int q = 0; q < VEC; ++q) fused_elem<D>(a, t, e0 + q);
+      continue;
+    }
+    Acc acc[VEC];
+    fold_vec<D, NT, NW>(a.ptrs + t.ptr0, n, (int)j64, e0 * IS, acc);
+    if constexpr (D != CR_I32) {
+      if (a.avg) {
+#pragma unroll
+        for (int q = 0; q < VEC; ++q) acc[q] = finish_avg(acc[q], n, a.inv_n);
+      }
+    }
+    uint32_t w[OB / 4];
+    acc_pack<D, D, VEC>(acc, w);
+#pragma unroll 8
+    for (int q = 0; q < n; ++q)
+      st_words<OB, NW * 4>(static_cast<unsigned char*>(a.ptrs[t.ptr0 + q]) + e0 * IS, w);
+  }
+  if (e_hi == t.numel) {
+    const uint64_t i = v_hi * VEC + threadIdx.x;
+    if (i < e_hi && i >= e_lo) fused_elem<D>(a, t, i);
+  }
+}
+
 template <int D, int NT>
 __global__ void __launch_bounds__(kBlock)
     k_bucket_fused(const __grid_constant__ FusedArgs a, uint32_t ntiles) {
-  using Acc = typename Elem<D>::Acc;
-  constexpr int IS = Elem<D>::kSize;
-  constexpr int VEC = 16 / IS;
-  constexpr uint64_t kTileElems = (uint64_t)kFusedVecPerThread * kBlock * VEC;
   const int n = NT > 0 ? NT : a.n;
   for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     int lo = 0, hi = a.ntens;  // tile_start[lo] <= tile < tile_start[hi]
@@ -54,58 +89,21 @@ __global__ void __launch_bounds__(kBlock)
       else hi = mid;
     }
     const FusedTensor& t = a.t[lo];
-    const uint64_t e_lo = (uint64_t)(tile - a.tile_start[lo]) * kTileElems;
-    const uint64_t e_hi = e_lo + kTileElems < t.numel ? e_lo + kTileElems : t.numel;
-    if (!t.vec) {
+    const uint64_t e_lo = (uint64_t)(tile - a.tile_start[lo]) * kFusedTileElems;
+    const uint64_t e_hi = e_lo + kFusedTileElems < t.numel ? e_lo + kFusedTileElems : t.numel;
+    if (t.vw == 32) {
+      fused_tile<D, NT, 8>(a, t, n, e_lo, e_hi);
+    } else if (t.vw == 16) {
+      fused_tile<D, NT, 4>(a, t, n, e_lo, e_hi);
+    } else {
       for (uint64_t i = e_lo + threadIdx.x; i < e_hi; i += kBlock) fused_elem<D>(a, t, i);
-      continue;
-    }
-    const uint64_t v_hi = e_hi / VEC;  // whole vectors end here; e_lo is a multiple of VEC
-#pragma unroll 1
-    for (int k = 0; k < kFusedVecPerThread; ++k) {
-      const uint64_t iv = e_lo / VEC + (uint64_t)k * kBlock + threadIdx.x;
-      if (iv >= v_hi) break;
-      const uint64_t e0 = iv * VEC;
-      const uint64_t p0 = t.off + e0;
-      const uint64_t j64 = p0 / t.Lb;
-      if (p0 + VEC > (j64 + 1) * t.Lb) {  // straddles a chunk of the bucket
-        for (int q = 0; q < VEC; ++q) fused_elem<D>(a, t, e0 + q);
-        continue;
-      }
-      Acc acc[VEC];
-      fold_vec16<D, NT>(a.ptrs + t.ptr0, n, (int)j64, e0 * IS, acc);
-      if constexpr (D != CR_I32) {
-        if (a.avg) {
-#pragma unroll
-          for (int q = 0; q < VEC; ++q) acc[q] = finish_avg(acc[q], n, a.inv_n);
-        }
-      }
-      uint32_t w[4];
-      acc_pack<D, D>(acc, w);
-#pragma unroll 8
-      for (int q = 0; q < n; ++q)
-        st_words<16>(static_cast<unsigned char*>(a.ptrs[t.ptr0 + q]) + e0 * IS, w);
-    }
-    // Ragged end of the tensor (fewer than VEC elements), in its last tile.
-    if (e_hi == t.numel) {
-      const uint64_t i = v_hi * VEC + threadIdx.x;
-      if (i < e_hi && i >= e_lo) fused_elem<D>(a, t, i);
     }
   }
 }
 
 template <int D>
 static cudaError_t fused_dispatch(const FusedArgs& a, uint32_t ntiles, cudaStream_t s) {
-  const void* k;
-  switch (a.n) {
-    case 2: k = reinterpret_cast<const void*>(k_bucket_fused<D, 2>); break;
-    case 4: k = reinterpret_cast<const void*>(k_bucket_fused<D, 4>); break;
-    case 8: k = reinterpret_cast<const void*>(k_bucket_fused<D, 8>); break;
-    default: k = reinterpret_cast<const void*>(k_bucket_fused<D, 0>); break;
-  }
-  int grid = 0;
-  cudaError_t err = persistent_grid(k, (uint64_t)ntiles * kBlock, &grid);
-  if (err != cudaSuccess) return err;
+  const unsigned grid = flat_grid((uint64_t)ntiles * kBlock);
   switch (a.n) {
     case 2: k_bucket_fused<D, 2><<<grid, kBlock, 0, s>>>(a, ntiles); break;
     case 4: k_bucket_fused<D, 4><<<grid, kBlock, 0, s>>>(a, ntiles); break;
@@ -126,9 +124,6 @@ cudaError_t launch_bucket_fused(cr_dtype d, const FusedArgs& a, uint32_t ntiles,
   return cudaErrorInvalidValue;
 }
 
-uint64_t fused_tile_elems(cr_dtype d) {
-  const uint64_t vec = d == CR_BF16 ? 8 : 4;
-  return (uint64_t)kFusedVecPerThread * kBlock * vec;
-}
+uint64_t fused_tile_elems(cr_dtype) { return kFusedTileElems; }
 
 }  // namespace cr

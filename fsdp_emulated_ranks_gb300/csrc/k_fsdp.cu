@@ -101,8 +101,32 @@ __global__ void __launch_bounds__(kBlock)
   }
 }
 
-// Vector path: 8 elements (one 16-byte bf16 vector per rank) per iteration.
-template <int NT>
+// 8 fp32 state words at p: one 32-byte access (SW == 8) or two 16-byte ones.
+template <int SW>
+__device__ __forceinline__ void ld_state8(const float* p, uint32_t* w) {
+  if constexpr (SW == 8) {
+    const Words<8> v = ldv<8>(p);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = v.w[i];
+  } else {
+    const uint4 a = ld16(p), b = ld16(p + 4);
+    w[0] = a.x, w[1] = a.y, w[2] = a.z, w[3] = a.w;
+    w[4] = b.x, w[5] = b.y, w[6] = b.z, w[7] = b.w;
+  }
+}
+template <int SW>
+__device__ __forceinline__ void st_state8(float* p, const uint32_t* w) {
+  if constexpr (SW == 8) {
+    st32(p, w);
+  } else {
+    st16(p, make_uint4(w[0], w[1], w[2], w[3]));
+    st16(p + 4, make_uint4(w[4], w[5], w[6], w[7]));
+  }
+}
+
+// Vector path: 8 elements (one 16-byte bf16 vector per rank) per thread and
+// iteration; SW = 8 moves the fp32 state in 32-byte accesses.
+template <int NT, int SW>
 __global__ void __launch_bounds__(kBlock)
     k_fsdp_vec(const __grid_constant__ FsdpArgs a) {
   const int n = NT > 0 ? NT : a.n;
@@ -120,12 +144,10 @@ __global__ void __launch_bounds__(kBlock)
     float* mp = a.master[j] + k;
     float* mm = a.m[j] + k;
     float* mv = a.v[j] + k;
-    const uint4 p0 = ld16(mp), p1 = ld16(mp + 4);
-    const uint4 m0 = ld16(mm), m1 = ld16(mm + 4);
-    const uint4 v0 = ld16(mv), v1 = ld16(mv + 4);
-    const uint32_t pw[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-    const uint32_t mw[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-    const uint32_t vw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint32_t pw[8], mw[8], vw[8];
+    ld_state8<SW>(mp, pw);
+    ld_state8<SW>(mm, mw);
+    ld_state8<SW>(mv, vw);
     uint32_t po[8], mo[8], vo[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -136,12 +158,9 @@ __global__ void __launch_bounds__(kBlock)
       mo[i] = __float_as_uint(o.m);
       vo[i] = __float_as_uint(o.v);
     }
-    st16(mp, make_uint4(po[0], po[1], po[2], po[3]));
-    st16(mp + 4, make_uint4(po[4], po[5], po[6], po[7]));
-    st16(mm, make_uint4(mo[0], mo[1], mo[2], mo[3]));
-    st16(mm + 4, make_uint4(mo[4], mo[5], mo[6], mo[7]));
-    st16(mv, make_uint4(vo[0], vo[1], vo[2], vo[3]));
-    st16(mv + 4, make_uint4(vo[4], vo[5], vo[6], vo[7]));
+    st_state8<SW>(mp, po);
+    st_state8<SW>(mm, mo);
+    st_state8<SW>(mv, vo);
     const uint4 pb = make_uint4(
         pack_bf16x2(__uint_as_float(po[0]), __uint_as_float(po[1])),
         pack_bf16x2(__uint_as_float(po[2]), __uint_as_float(po[3])),
@@ -215,7 +234,7 @@ __global__ void __launch_bounds__(kBlock)
     if (a.param_bf16) {
       const uint32_t w[2] = {pack_bf16x2(__uint_as_float(po[0]), __uint_as_float(po[1])),
                              pack_bf16x2(__uint_as_float(po[2]), __uint_as_float(po[3]))};
-      st_words<8>(static_cast<unsigned char*>(a.param_bf16) + e0 * 2, w);
+      st_words<8, 16>(static_cast<unsigned char*>(a.param_bf16) + e0 * 2, w);
     }
   }
   const uint64_t e = nvec * 4 + tid;
@@ -242,24 +261,31 @@ __global__ void __launch_bounds__(kBlock)
 }
 
 template <typename K, typename A>
-static cudaError_t launch_persistent(K kernel, const A& args, uint64_t threads,
-                                     cudaStream_t s) {
-  int grid = 0;
-  cudaError_t err = persistent_grid(reinterpret_cast<const void*>(kernel), threads, &grid);
-  if (err != cudaSuccess) return err;
-  kernel<<<grid, kBlock, 0, s>>>(args);
+static cudaError_t launch_flat(K kernel, const A& args, uint64_t threads, cudaStream_t s) {
+  kernel<<<flat_grid(threads), kBlock, 0, s>>>(args);
   return cudaGetLastError();
 }
 
-cudaError_t launch_fsdp(const FsdpArgs& a, bool vec, cudaStream_t s) {
-  if (!vec) return launch_persistent(k_fsdp_elem, a, a.count, s);
+template <int SW>
+static cudaError_t fsdp_dispatch(const FsdpArgs& a, cudaStream_t s) {
   const uint64_t threads = a.count / 8 + 1;
   switch (a.n) {
-    case 2: return launch_persistent(k_fsdp_vec<2>, a, threads, s);
-    case 4: return launch_persistent(k_fsdp_vec<4>, a, threads, s);
-    case 8: return launch_persistent(k_fsdp_vec<8>, a, threads, s);
-    default: return launch_persistent(k_fsdp_vec<0>, a, threads, s);
+    case 2: return launch_flat(k_fsdp_vec<2, SW>, a, threads, s);
+    case 4: return launch_flat(k_fsdp_vec<4, SW>, a, threads, s);
+    case 8: return launch_flat(k_fsdp_vec<8, SW>, a, threads, s);
+    default: return launch_flat(k_fsdp_vec<0, SW>, a, threads, s);
   }
+}
+
+cudaError_t launch_fsdp(const FsdpArgs& a, int vw, cudaStream_t s) {
+  if (vw == 32) return fsdp_dispatch<8>(a, s);
+  if (vw == 16) return fsdp_dispatch<4>(a, s);
+  return launch_flat(k_fsdp_elem, a, a.count, s);
+}
+
+cudaError_t launch_adamw(const AdamArgs& a, bool vec, cudaStream_t s) {
+  return vec ? launch_flat(k_adamw_vec, a, a.n / 4 + 1, s)
+             : launch_flat(k_adamw_elem, a, a.n, s);
 }
 
 template <int NT, bool VEC>
@@ -287,9 +313,5 @@ cudaError_t launch_fsdp_sumsq(const FsdpArgs& a, bool vec, double* partials,
   }
 }
 
-cudaError_t launch_adamw(const AdamArgs& a, bool vec, cudaStream_t s) {
-  return vec ? launch_persistent(k_adamw_vec, a, a.n / 4 + 1, s)
-             : launch_persistent(k_adamw_elem, a, a.n, s);
-}
 
 }  // namespace cr

@@ -32,6 +32,16 @@ def _lib():
     cr.lib()
 
 
+ESIZE = {"f32": 4, "bf16": 2, "i32": 4}
+
+
+def eoff(offset, dt):
+    """Element offset of a buffer inside its allocation: 0 (32-byte aligned:
+    32-byte vector path), "16B" (16- but not 32-byte aligned: 16-byte
+    path) or 1 (element-wise path)."""
+    return 16 // ESIZE[dt] if offset == "16B" else offset
+
+
 def sizes(n):
     return [0, 1, 7, 8 * n * 3, 8 * n * 37 + 5, 1000, 4099]
 
@@ -44,14 +54,14 @@ def host_inputs(n, count, dt, seed):
 
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 16, 64])
 @pytest.mark.parametrize("pair", PAIRS)
-@pytest.mark.parametrize("offset", [0, 1])
+@pytest.mark.parametrize("offset", [0, 1, "16B"])
 def test_reduce_scatter(n, pair, offset):
     dt, op, out = pair
     for count in sizes(n):
         host = host_inputs(n, count, dt, seed=n * 100 + count)
         want, _ = O.ring_reduce_scatter(host, dt, op, out)
-        bufs = [to_dev(x, dt, offset) for x in host]
-        shards = [Guarded(w.size, out, offset) for w in want]
+        bufs = [to_dev(x, dt, eoff(offset, dt)) for x in host]
+        shards = [Guarded(w.size, out, eoff(offset, out)) for w in want]
         cr.cr_reduce_scatter(bufs, count, dt, op, [s.ptr() for s in shards], out)
         torch.cuda.synchronize()
         for j in range(n):
@@ -80,14 +90,14 @@ def test_reduce_scatter_in_place(n, dt):
 
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 16, 64])
 @pytest.mark.parametrize("pair", PAIRS)
-@pytest.mark.parametrize("offset", [0, 1])
+@pytest.mark.parametrize("offset", [0, 1, "16B"])
 def test_all_reduce(n, pair, offset):
     dt, op, out = pair
     for count in sizes(n):
         host = host_inputs(n, count, dt, seed=n * 300 + count)
         want, _ = O.ring_all_reduce(host, dt, op, out)
-        bufs = [to_dev(x, dt, offset) for x in host]
-        outs = [Guarded(count, out, offset) for _ in range(n)]
+        bufs = [to_dev(x, dt, eoff(offset, dt)) for x in host]
+        outs = [Guarded(count, out, eoff(offset, out)) for _ in range(n)]
         cr.cr_all_reduce(bufs, count, dt, op, [o.ptr() for o in outs], out)
         torch.cuda.synchronize()
         for r in range(n):
@@ -115,7 +125,7 @@ def test_all_reduce_in_place(n, dt, op, count_fn):
 
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 16, 64])
 @pytest.mark.parametrize("dt", ["f32", "bf16", "i32"])
-@pytest.mark.parametrize("offset", [0, 1])
+@pytest.mark.parametrize("offset", [0, 1, "16B"])
 def test_all_gather(n, dt, offset):
     for count in sizes(n):
         shards = []
@@ -123,8 +133,8 @@ def test_all_gather(n, dt, offset):
             lo, hi = O.chunk_bounds(count, n, j)
             shards.append(host_inputs(1, hi - lo, dt, seed=j + count)[0])
         want, _ = O.ring_all_gather(shards, count, dt)
-        d_sh = [to_dev(s, dt, offset) if s.size else None for s in shards]
-        outs = [Guarded(count, dt, offset) for _ in range(n)]
+        d_sh = [to_dev(s, dt, eoff(offset, dt)) if s.size else None for s in shards]
+        outs = [Guarded(count, dt, eoff(offset, dt)) for _ in range(n)]
         cr.cr_all_gather([s if s is not None else 0 for s in d_sh], count, dt, [o.ptr() for o in outs])
         torch.cuda.synchronize()
         for r in range(n):
@@ -178,21 +188,21 @@ def fsdp_case(n, count, seed):
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 16])
 @pytest.mark.parametrize("count_fn", [lambda n: 8 * n * 40, lambda n: 8 * n * 40 + 5, lambda n: 1,
                                       lambda n: 100])
-@pytest.mark.parametrize("offset", [0, 1])
+@pytest.mark.parametrize("offset", [0, 1, "16B"])
 def test_fsdp_step_three_steps(n, count_fn, offset):
     count = count_fn(n)
     grads, master, m, v = fsdp_case(n, count, seed=n)
-    d_master = [Guarded(x.size, "f32", offset) for x in master]
-    d_m = [Guarded(x.size, "f32", offset) for x in m]
-    d_v = [Guarded(x.size, "f32", offset) for x in v]
+    d_master = [Guarded(x.size, "f32", eoff(offset, "f32")) for x in master]
+    d_m = [Guarded(x.size, "f32", eoff(offset, "f32")) for x in m]
+    d_v = [Guarded(x.size, "f32", eoff(offset, "f32")) for x in v]
     for g, src in ((d_master, master), (d_m, m), (d_v, v)):
         for gg, x in zip(g, src):
             if x.size:
                 gg.view.copy_(to_dev(x, "f32"))
-    d_p = [Guarded(count, "bf16", offset) for _ in range(n)]
+    d_p = [Guarded(count, "bf16", eoff(offset, "bf16")) for _ in range(n)]
     for step in (1, 2, 3):
         grads = I.host_rank_buffers(n, count, "bf16", std=1e-3, seed0=1000 + 17 * step)
-        d_g = [to_dev(x, "bf16", offset) for x in grads]
+        d_g = [to_dev(x, "bf16", eoff(offset, "bf16")) for x in grads]
         cfg = O.AdamWConfig(step=step)
         want_p = O.fsdp_step(grads, master, m, v, cfg)
         cr.cr_fsdp_step(d_g, count, [x.ptr() for x in d_master], [x.ptr() for x in d_m],
@@ -357,12 +367,12 @@ def test_all_reduce_staged_repeated_calls_keep_order():
 
 @pytest.mark.parametrize("n", [1, 2, 3, 8, 16, 64])
 @pytest.mark.parametrize("dt,op", [("bf16", "avg"), ("f32", "sum"), ("i32", "sum"), ("f32", "avg")])
-@pytest.mark.parametrize("offset", [0, 1])
+@pytest.mark.parametrize("offset", [0, 1, "16B"])
 def test_bucket_all_reduce_fused(n, dt, op, offset):
     """Equal, bit for bit, to the oracle's pack -> ring all-reduce per bucket
     -> unpack, including tensors that straddle chunk boundaries of their
     bucket and more tensors than one launch takes."""
-    rng = np.random.default_rng(n * 7 + offset)
+    rng = np.random.default_rng(n * 7 + eoff(offset, dt))
     T = 150 if n <= 16 else 40
     numels = [int(k) for k in rng.integers(0, 3000, size=T)] + [1, 0, 7, 20001]
     esize = 2 if dt == "bf16" else 4
@@ -372,7 +382,7 @@ def test_bucket_all_reduce_fused(n, dt, op, offset):
     host_t = [[host_inputs(1, k, dt, seed=100 * r + t)[0] for t, k in enumerate(numels)]
               for r in range(n)]
     want = O.bucketed_all_reduce(oplan, host_t, dt, op)
-    g = [[Guarded(k, dt, offset) for k in numels] for _ in range(n)]
+    g = [[Guarded(k, dt, eoff(offset, dt)) for k in numels] for _ in range(n)]
     for r in range(n):
         for t, k in enumerate(numels):
             if k:
