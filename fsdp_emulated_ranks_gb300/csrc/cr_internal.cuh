@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include "cr.h"
+#include "fastdiv.h"
 
 namespace cr {
 
@@ -21,6 +22,7 @@ struct FoldArgs {
   void* out[kMaxRanks];
   uint64_t count;  // elements per rank buffer
   uint64_t L;      // chunk length ceil(count / n)
+  FastDiv Ld;      // division by L
   uint64_t begin;  // the call covers elements [begin, end) of each buffer
   uint64_t end;
   int n;           // ranks
@@ -28,6 +30,7 @@ struct FoldArgs {
                    // result also goes to a second set of buffers)
   int avg;         // 1: divide the finished sum by n
   float inv_n;     // 1/n when n is a power of two (exact), else 0
+  uint32_t max_ctas;  // cap on the grid (0: one vector per thread)
 };
 
 struct GatherArgs {
@@ -35,6 +38,7 @@ struct GatherArgs {
   void* bufs[kMaxRanks];
   uint64_t count;
   uint64_t L;
+  FastDiv Ld;
   int n;
   uint64_t inplace_mask;  // bit j: shards[j] is chunk j of bufs[j]
 };
@@ -52,6 +56,7 @@ struct FsdpArgs {
   float* v[kMaxRanks];
   uint64_t count;
   uint64_t L;
+  FastDiv Ld;
   int n;
   float inv_n;
   AdamScalars a;
@@ -98,6 +103,7 @@ struct FusedTensor {
   uint64_t numel;  // elements of the tensor
   uint64_t off;    // element offset of the tensor inside its bucket
   uint64_t Lb;     // chunk length of its bucket, ceil(bucket numel / N)
+  FastDiv Lbd;     // division by Lb
   uint32_t ptr0;   // index of rank 0's pointer in FusedArgs::ptrs
   uint32_t vw;     // vector bytes all N rank pointers allow: 32, 16 or 0
 };
@@ -144,6 +150,9 @@ void report_error(cr_status status, const char* msg);
 // per SM, ceil(threads / kBlock)), at least 1.  Occupancy is queried once
 // per (kernel, device) and cached.
 cudaError_t persistent_grid(const void* kernel, uint64_t threads, int* grid);
+
+// Streaming multiprocessors of the current device (cached per device).
+cudaError_t sm_count(int* sms);
 
 // Grid of ceil(threads / kBlock) CTAs (at least 1, at most 2^30; kernels
 // keep a grid-stride loop for anything beyond).

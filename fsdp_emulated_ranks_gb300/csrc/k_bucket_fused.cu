@@ -26,7 +26,7 @@ __device__ __forceinline__ void fused_elem(const FusedArgs& a, const FusedTensor
                                            uint64_t i) {
   using Acc = typename Elem<D>::Acc;
   const int n = a.n;
-  const int j = (int)((t.off + i) / t.Lb);
+  const int j = (int)fastdiv_div(t.Lbd, t.off + i);
   int r = (j + 1 == n) ? 0 : j + 1;
   Acc acc = ld_elem<D>(a.ptrs[t.ptr0 + r], i);
   for (int k = 1; k < n; ++k) {
@@ -52,7 +52,7 @@ __device__ __forceinline__ void fused_tile(const FusedArgs& a, const FusedTensor
   for (uint64_t iv = e_lo / VEC + threadIdx.x; iv < v_hi; iv += kBlock) {
     const uint64_t e0 = iv * VEC;
     const uint64_t p0 = t.off + e0;
-    const uint64_t j64 = p0 / t.Lb;
+    const uint64_t j64 = fastdiv_div(t.Lbd, p0);
     if (p0 + VEC > (j64 + 1) * t.Lb) {  // straddles a chunk of the bucket
       for (int q = 0; q < VEC; ++q) fused_elem<D>(a, t, e0 + q);
       continue;

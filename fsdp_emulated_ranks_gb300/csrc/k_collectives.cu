@@ -31,7 +31,7 @@ namespace cr {
 template <int DI, int DO, int MODE>
 __device__ __forceinline__ void fold_store_elem(const FoldArgs& a, int n, uint64_t e) {
   using Acc = typename Elem<DI>::Acc;
-  const int j = (int)(e / a.L);
+  const int j = (int)(fastdiv_div(a.Ld, e));
   Acc x = fold_elem<DI>(a.in, n, j, e);
   if constexpr (DI != CR_I32) {
     if (a.avg) x = finish_avg(x, n, a.inv_n);
@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kBlock)
 
   for (uint64_t iv = vbeg + tid; iv < vend; iv += stride) {
     const uint64_t e0 = iv * VEC;
-    const uint64_t j64 = e0 / a.L;
+    const uint64_t j64 = fastdiv_div(a.Ld, e0);
     const int j = (int)j64;
     if (MODE == kAR && e0 + VEC > (j64 + 1) * a.L) {
       // The vector straddles a chunk boundary (L % VEC != 0): each element
@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kBlock)
   const int n = a.n;
   for (uint64_t iv = tid; iv < nvec; iv += stride) {
     const uint64_t e0 = iv * VEC;
-    const uint64_t j64 = e0 / a.L;
+    const uint64_t j64 = fastdiv_div(a.Ld, e0);
     const int j = (int)j64;
     const Words<NW> v = ldv<NW>(static_cast<const unsigned char*>(a.shards[j]) +
                                 (e0 - j64 * a.L) * ES);
@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kBlock)
   }
   const uint64_t e = nvec * VEC + tid;
   if (e < a.count) {
-    const uint64_t j64 = e / a.L;
+    const uint64_t j64 = fastdiv_div(a.Ld, e);
     const int j = (int)j64;
     const unsigned char* src =
         static_cast<const unsigned char*>(a.shards[j]) + (e - j64 * a.L) * ES;
@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kBlock)
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
   for (uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
        e < a.count; e += stride) {
-    const uint64_t j64 = e / a.L;
+    const uint64_t j64 = fastdiv_div(a.Ld, e);
     const int j = (int)j64;
     const W x = static_cast<const W*>(a.shards[j])[e - j64 * a.L];
     const bool skip_own = (a.inplace_mask >> j) & 1ull;
@@ -174,15 +174,24 @@ static cudaError_t launch_flat(K kernel, const A& args, uint64_t threads, cudaSt
   return cudaGetLastError();
 }
 
+template <typename K>
+static cudaError_t launch_fold_kernel(K kernel, const FoldArgs& a, uint64_t threads,
+                                      cudaStream_t s) {
+  unsigned grid = flat_grid(threads);
+  if (a.max_ctas && grid > a.max_ctas) grid = a.max_ctas;
+  kernel<<<grid, kBlock, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <int DI, int DO, int MODE, int NW>
 static cudaError_t fold_dispatch_nw(const FoldArgs& a, cudaStream_t s) {
   constexpr int VEC = elems_per<DI, NW>();
   const uint64_t threads = (a.end - a.begin) / VEC + 2 * VEC;
   switch (a.n) {
-    case 2: return launch_flat(k_fold_vec<DI, DO, MODE, 2, NW>, a, threads, s);
-    case 4: return launch_flat(k_fold_vec<DI, DO, MODE, 4, NW>, a, threads, s);
-    case 8: return launch_flat(k_fold_vec<DI, DO, MODE, 8, NW>, a, threads, s);
-    default: return launch_flat(k_fold_vec<DI, DO, MODE, 0, NW>, a, threads, s);
+    case 2: return launch_fold_kernel(k_fold_vec<DI, DO, MODE, 2, NW>, a, threads, s);
+    case 4: return launch_fold_kernel(k_fold_vec<DI, DO, MODE, 4, NW>, a, threads, s);
+    case 8: return launch_fold_kernel(k_fold_vec<DI, DO, MODE, 8, NW>, a, threads, s);
+    default: return launch_fold_kernel(k_fold_vec<DI, DO, MODE, 0, NW>, a, threads, s);
   }
 }
 
@@ -190,7 +199,7 @@ template <int DI, int DO, int MODE>
 static cudaError_t fold_dispatch(const FoldArgs& a, int vw, cudaStream_t s) {
   if (vw == 32) return fold_dispatch_nw<DI, DO, MODE, 8>(a, s);
   if (vw == 16) return fold_dispatch_nw<DI, DO, MODE, 4>(a, s);
-  return launch_flat(k_fold_elem<DI, DO, MODE>, a, a.end - a.begin, s);
+  return launch_fold_kernel(k_fold_elem<DI, DO, MODE>, a, a.end - a.begin, s);
 }
 
 template <int MODE>

@@ -62,7 +62,8 @@ __device__ float clip_coef(const FsdpArgs& a) {
   return s_coef;
 }
 
-// Sum of squares of the averaged fp32 gradient, one fp64 partial per CTA.
+// Sum of squares of the averaged fp32 gradient, one fp64 partial per CTA
+// (fp64 per thread and across threads, fp32 within batches of 8 squares).
 template <int NT, bool VEC>
 __global__ void __launch_bounds__(kBlock)
     k_fsdp_sumsq(const __grid_constant__ FsdpArgs a, double* partials) {
@@ -77,17 +78,21 @@ __global__ void __launch_bounds__(kBlock)
     for (uint64_t iv = tid; iv < nvec; iv += stride) {
       const uint64_t e0 = iv * 8;
       float g[8];
-      fold_vec16<CR_BF16, NT>(a.grads, n, (int)(e0 / a.L), e0 * 2, g);
+      fold_vec16<CR_BF16, NT>(a.grads, n, (int)fastdiv_div(a.Ld, e0), e0 * 2, g);
+      // Eight squares summed in fp32, the batch added in fp64: GB300's fp64
+      // rate is far below its fp32 rate, and the norm only needs ~1e-7.
+      float s8 = 0.0f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const double gi = finish_avg(g[i], n, a.inv_n);
-        t += gi * gi;
+        const float gi = finish_avg(g[i], n, a.inv_n);
+        s8 = fmaf(gi, gi, s8);
       }
+      t += (double)s8;
     }
     e_elem = nvec * 8;
   }
   for (uint64_t e = e_elem + tid; e < a.count; e += stride) {
-    const double gi = finish_avg(fold_elem<CR_BF16>(a.grads, n, (int)(e / a.L), e), n, a.inv_n);
+    const double gi = finish_avg(fold_elem<CR_BF16>(a.grads, n, (int)fastdiv_div(a.Ld, e), e), n, a.inv_n);
     t += gi * gi;
   }
 #pragma unroll
@@ -136,7 +141,7 @@ __global__ void __launch_bounds__(kBlock)
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
   for (uint64_t iv = tid; iv < nvec; iv += stride) {
     const uint64_t e0 = iv * 8;
-    const uint64_t j64 = e0 / a.L;
+    const uint64_t j64 = fastdiv_div(a.Ld, e0);
     const int j = (int)j64;
     const uint64_t k = e0 - j64 * a.L;  // offset inside shard j
     float g[8];
@@ -173,7 +178,7 @@ __global__ void __launch_bounds__(kBlock)
   // Ragged tail (count % 8 elements).
   const uint64_t e = nvec * 8 + tid;
   if (e < a.count) {
-    const uint64_t j64 = e / a.L;
+    const uint64_t j64 = fastdiv_div(a.Ld, e);
     const int j = (int)j64;
     const uint64_t k = e - j64 * a.L;
     const float gi =
@@ -193,7 +198,7 @@ __global__ void __launch_bounds__(kBlock)
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
   for (uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
        e < a.count; e += stride) {
-    const uint64_t j64 = e / a.L;
+    const uint64_t j64 = fastdiv_div(a.Ld, e);
     const int j = (int)j64;
     const uint64_t k = e - j64 * a.L;
     const float gi =

@@ -1,4 +1,5 @@
-// launch_util.cu -- persistent-grid sizing shared by all launchers.
+// launch_util.cu -- grid sizing shared by the launchers (SM counts and
+// occupancy, cached per device).
 #include <map>
 #include <mutex>
 #include <utility>
@@ -12,6 +13,21 @@ std::mutex g_mu;
 std::map<std::pair<const void*, int>, int> g_ctas_per_sm;  // (kernel, device)
 std::map<int, int> g_sms;                                  // device -> SMs
 }  // namespace
+
+cudaError_t sm_count(int* sms) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  std::lock_guard<std::mutex> lock(g_mu);
+  auto it = g_sms.find(dev);
+  if (it != g_sms.end()) {
+    *sms = it->second;
+    return cudaSuccess;
+  }
+  err = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err == cudaSuccess) g_sms[dev] = *sms;
+  return err;
+}
 
 cudaError_t persistent_grid(const void* kernel, uint64_t threads, int* grid) {
   int dev = 0;

@@ -284,7 +284,8 @@ cr_status cr_fsdp_step(const void* const* grads_bf16, int nranks,
  * reduce-scatter and AdamW ("AI Infra Guide, Chapter 6", 6.8: the training
  * loop calls clip_grad_norm_(max_norm=1.0) on the sharded model before the
  * optimizer step).  norm = L2 norm of the whole averaged fp32 gradient (all
- * shards: the global norm), accumulated in fp64; every gradient element is
+ * shards: the global norm), squares summed in fp32 batches of 8 and the
+ * batches in fp64 (relative error ~1e-7); every gradient element is
  * multiplied (one fp32 multiply) by c = min(1, max_norm / (norm + 1e-6)),
  * formed in double and rounded to fp32, before AdamW.  Two launches: a
  * sum-of-squares pass over the grads that writes one fp64 partial per CTA
