@@ -318,9 +318,10 @@ class Buckets(Workload):
         # The fused all-reduce works on the tensors in place: N reads + N
         # writes per element, the same bytes as one pass over the buckets.
         self.name = f"ddp_bucket_{mode}_bf16_{n}ranks_{ntensors}tensors"
-        self.kernel = {"allreduce": "k_fold_vec<bf16,bf16,AR,8>",
+        self.kernel = {"allreduce": "k_bucket_fused<bf16,8>",
                        "fused": "k_bucket_fused<bf16,8>"}.get(mode, "k_copy_segments")
-        self.profile = (f"k_fold_vec_bucket_allreduce_bf16_{n}x{ntensors}" if mode == "allreduce"
+        self.profile = (f"k_bucket_fused_bucket_{mode}_bf16_{n}x{ntensors}"
+                        if mode in ("allreduce", "fused")
                         else f"k_copy_segments_bucket_{mode}_bf16_{n}x{ntensors}")
 
     def setup(self, device):
@@ -330,8 +331,9 @@ class Buckets(Workload):
         n = self.n
         self.plan = cr.cr_bucket_plan(self.numels, 2, 25 * 1024 * 1024)
         copies = -(-n * len(self.numels) // 1024)
-        self.launches = {"pack": copies, "unpack": copies, "allreduce": self.plan.nbuckets,
-                         "pipeline": 2 * copies + self.plan.nbuckets,
+        ar_launches = -(-self.plan.nbuckets // min(128, 2048 // n))
+        self.launches = {"pack": copies, "unpack": copies, "allreduce": ar_launches,
+                         "pipeline": 2 * copies + ar_launches,
                          "fused": -(-len(self.numels) // min(128, 2048 // n))}[self.mode]
         tens = []
         for r in range(n):

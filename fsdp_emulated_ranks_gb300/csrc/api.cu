@@ -792,28 +792,66 @@ cr_status cr_bucket_unpack(const cr_bucket_plan_t* plan, int nranks,
                      const_cast<void* const*>(buckets), false, (cudaStream_t)stream);
 }
 
-cr_status cr_bucket_all_reduce(const cr_bucket_plan_t* plan, int nranks,
-                               void* const* buckets, cr_dtype dtype, cr_op op,
-                               cr_stream_t stream) {
-  cr_status st = check_plan(plan, nranks);
-  if (st) return st;
-  if (esize_of(dtype) != plan->elem_size)
-    return fail(CR_ERR_INVALID_ARG, "dtype size %zu != plan elem_size %zu", esize_of(dtype),
-                plan->elem_size);
-  if (plan->nbuckets > 0 && !buckets) return fail(CR_ERR_INVALID_ARG, "buckets is NULL");
-  const void* in[CR_MAX_RANKS];
-  void* out[CR_MAX_RANKS];
-  for (int b = 0; b < plan->nbuckets; ++b) {
+}  // extern "C"
+
+namespace {
+
+// Runs the fused bucket kernel over `nitems` items (tensors, or whole
+// buckets): item(k, &numel, &offset in bucket, &bucket numel, rank ptrs).
+// One launch per kFusedMaxTensors items (fewer when N > 16).
+template <typename Item>
+cr_status fused_run(int nitems, int nranks, cr_dtype dtype, cr_op op, cudaStream_t stream,
+                    Item item) {
+  static thread_local FusedArgs args;  // ~24 KB: kept off the stack
+  const int per_launch = std::min(kFusedMaxTensors, kFusedMaxPtrs / nranks);
+  const uint64_t tile = fused_tile_elems(dtype);
+  uint32_t ntiles = 0;
+  args.ntens = 0;
+  args.n = nranks;
+  args.avg = op == CR_AVG;
+  args.inv_n = exact_inv_n(nranks);
+  auto flush = [&]() -> cr_status {
+    if (args.ntens == 0) return CR_OK;
+    args.tile_start[args.ntens] = ntiles;
+    cudaError_t e = launch_bucket_fused(dtype, args, ntiles, stream);
+    args.ntens = 0;
+    ntiles = 0;
+    if (e != cudaSuccess) return cuda_fail(e, "fused bucket all-reduce launch");
+    return CR_OK;
+  };
+  cr_status st = CR_OK;
+  void* ptrs[CR_MAX_RANKS];
+  for (int t = 0; t < nitems; ++t) {
+    uint64_t numel = 0, off = 0, bnumel = 0;
+    item(t, &numel, &off, &bnumel, ptrs);
+    if (numel == 0) continue;
+    const uint64_t tiles = (numel + tile - 1) / tile;
+    if (args.ntens == per_launch || (uint64_t)ntiles + tiles > 0x7fffffffull)
+      if ((st = flush())) return st;
+    const int k = args.ntens;
+    FusedTensor& d = args.t[k];
+    d.numel = numel;
+    d.off = off;
+    d.Lb = cr_chunk_len(bnumel, nranks);
+    d.Lbd = fastdiv_make(d.Lb, bnumel ? bnumel - 1 : 0);
+    d.ptr0 = (uint32_t)(k * nranks);
+    Width w;
     for (int r = 0; r < nranks; ++r) {
-      in[r] = buckets[(size_t)r * plan->nbuckets + b];
-      out[r] = buckets[(size_t)r * plan->nbuckets + b];
+      args.ptrs[k * nranks + r] = ptrs[r];
+      w.ptr(ptrs[r]);
     }
-    st = all_reduce_impl(in, nranks, plan->bucket_numel[b], dtype, op, out, dtype,
-                         (cudaStream_t)stream);
-    if (st) return st;
+    d.vw = (uint32_t)w.get();
+    args.tile_start[k] = ntiles;
+    args.ntens += 1;
+    ntiles += (uint32_t)tiles;
   }
+  if ((st = flush())) return st;
   return ok();
 }
+
+}  // namespace
+
+extern "C" {
 
 cr_status cr_bucket_all_reduce_fused(const cr_bucket_plan_t* plan, int nranks,
                                      void* const* tensors, cr_dtype dtype, cr_op op,
@@ -834,50 +872,45 @@ cr_status cr_bucket_all_reduce_fused(const cr_bucket_plan_t* plan, int nranks,
       if (plan->numels[t]) spans.push_back(span_of(p, plan->numels[t] * es, 1, r * T + t));
     }
   if ((st = check_disjoint(spans))) return st;
-  static thread_local FusedArgs args;  // ~21 KB: kept off the stack
-  const int per_launch = std::min(kFusedMaxTensors, kFusedMaxPtrs / nranks);
-  const uint64_t tile = fused_tile_elems(dtype);
-  uint32_t ntiles = 0;
-  args.ntens = 0;
-  args.n = nranks;
-  args.avg = op == CR_AVG;
-  args.inv_n = exact_inv_n(nranks);
-  auto flush = [&]() -> cr_status {
-    if (args.ntens == 0) return CR_OK;
-    args.tile_start[args.ntens] = ntiles;
-    cudaError_t e = launch_bucket_fused(dtype, args, ntiles, (cudaStream_t)stream);
-    args.ntens = 0;
-    ntiles = 0;
-    if (e != cudaSuccess) return cuda_fail(e, "bucket_all_reduce_fused launch");
-    return CR_OK;
-  };
-  for (int t = 0; t < T; ++t) {
-    const uint64_t numel = plan->numels[t];
-    if (numel == 0) continue;
-    const uint64_t tiles = (numel + tile - 1) / tile;
-    if (args.ntens == per_launch || (uint64_t)ntiles + tiles > 0x7fffffffull)
-      if ((st = flush())) return st;
-    const int k = args.ntens;
-    FusedTensor& d = args.t[k];
-    d.numel = numel;
-    d.off = plan->tensor_offset[t];
-    const uint64_t bnumel = plan->bucket_numel[plan->tensor_bucket[t]];
-    d.Lb = cr_chunk_len(bnumel, nranks);
-    d.Lbd = fastdiv_make(d.Lb, bnumel ? bnumel - 1 : 0);
-    d.ptr0 = (uint32_t)(k * nranks);
-    Width w;
-    for (int r = 0; r < nranks; ++r) {
-      void* p = tensors[(size_t)r * T + t];
-      args.ptrs[k * nranks + r] = p;
-      w.ptr(p);
+  return fused_run(T, nranks, dtype, op, (cudaStream_t)stream,
+                   [&](int t, uint64_t* numel, uint64_t* off, uint64_t* bnumel, void** ptrs) {
+                     *numel = plan->numels[t];
+                     *off = plan->tensor_offset[t];
+                     *bnumel = plan->bucket_numel[plan->tensor_bucket[t]];
+                     for (int r = 0; r < nranks; ++r) ptrs[r] = tensors[(size_t)r * T + t];
+                   });
+}
+
+// Every bucket of every rank all-reduced in place, all buckets in one
+// launch (per 128): each bucket is one item of the fused kernel, offset 0,
+// chunked over its own element count -- the same result as one
+// cr_all_reduce per bucket.
+cr_status cr_bucket_all_reduce(const cr_bucket_plan_t* plan, int nranks,
+                               void* const* buckets, cr_dtype dtype, cr_op op,
+                               cr_stream_t stream) {
+  cr_status st = check_plan(plan, nranks);
+  if (st) return st;
+  if ((st = check_pair(dtype, op, dtype))) return st;
+  const size_t es = esize_of(dtype);
+  if (es != plan->elem_size)
+    return fail(CR_ERR_INVALID_ARG, "dtype size %zu != plan elem_size %zu", es, plan->elem_size);
+  const int B = plan->nbuckets;
+  if (B > 0 && !buckets) return fail(CR_ERR_INVALID_ARG, "buckets is NULL");
+  std::vector<Span> spans;
+  for (int r = 0; r < nranks; ++r)
+    for (int b = 0; b < B; ++b) {
+      const void* p = buckets[(size_t)r * B + b];
+      if ((st = check_buf(p, plan->bucket_numel[b], es, "buckets", r * B + b))) return st;
+      if (plan->bucket_numel[b]) spans.push_back(span_of(p, plan->bucket_numel[b] * es, 1, r * B + b));
     }
-    d.vw = (uint32_t)w.get();
-    args.tile_start[k] = ntiles;
-    args.ntens += 1;
-    ntiles += (uint32_t)tiles;
-  }
-  if ((st = flush())) return st;
-  return ok();
+  if ((st = check_disjoint(spans))) return st;
+  return fused_run(B, nranks, dtype, op, (cudaStream_t)stream,
+                   [&](int b, uint64_t* numel, uint64_t* off, uint64_t* bnumel, void** ptrs) {
+                     *numel = plan->bucket_numel[b];
+                     *off = 0;
+                     *bnumel = plan->bucket_numel[b];
+                     for (int r = 0; r < nranks; ++r) ptrs[r] = buckets[(size_t)r * B + b];
+                   });
 }
 
 }  // extern "C"

@@ -227,8 +227,12 @@ cr_status cr_bucket_unpack(const cr_bucket_plan_t* plan, int nranks,
                            const void* const* buckets, void* const* tensors,
                            cr_stream_t stream);
 
-/* DDP middle step: cr_all_reduce in place on every bucket, bucket by bucket
- * in index order (bucket b of rank r is buckets[r*B + b]). */
+/* DDP middle step: every bucket of every rank all-reduced in place, with
+ * the result cr_all_reduce would give on each bucket (chunks of the
+ * bucket's own element count); bucket b of rank r is buckets[r*B + b].
+ * All buckets go in one launch (per 128 buckets).  Buckets must not
+ * overlap (CR_ERR_INVALID_ARG); supported dtype/op pairs as cr_all_reduce
+ * with in == out. */
 cr_status cr_bucket_all_reduce(const cr_bucket_plan_t* plan, int nranks,
                                void* const* buckets, cr_dtype dtype, cr_op op,
                                cr_stream_t stream);

@@ -84,6 +84,13 @@ def lib() -> C.CDLL:
         L.orc_fsdp_step_clipped.argtypes = [C.c_int, sz, vp, vp, vp, vp,
                                             C.POINTER(_AdamCfg), C.c_double, vp,
                                             C.POINTER(C.c_double)]
+        L.orc_ring_reduce_scatter_L.argtypes = [C.c_int, sz, sz, C.c_int, C.c_int,
+                                                vp, vp, C.c_int, vp, vp, vp]
+        L.orc_ring_all_gather_L.argtypes = [C.c_int, sz, sz, C.c_int, vp, vp, vp, vp]
+        L.orc_fsdp2_step.argtypes = [C.c_int, vp, C.c_int, vp, vp, vp, vp,
+                                     C.POINTER(_AdamCfg), vp]
+        L.orc_accumulate.restype = None
+        L.orc_accumulate.argtypes = [sz, vp, vp, C.c_int]
         L.orc_bucket_plan.argtypes = [C.c_int, vp, sz, sz, vp, vp, vp,
                                       C.POINTER(C.c_int)]
         L.orc_bucket_pack.argtypes = [C.c_int, C.c_int, vp, sz, vp, vp, vp, vp]
@@ -276,6 +283,53 @@ def fsdp_step_clipped(grads, master, m, v, cfg: AdamWConfig, max_norm: float):
                                        float(max_norm), _ptrs(params),
                                        C.byref(norm)), "fsdp_step_clipped")
     return params, norm.value
+
+
+def ring_reduce_scatter_L(bufs, L, dtype, op="sum", out_dtype=None):
+    """Ring reduce-scatter with an explicit chunk length L (elements)."""
+    out_dtype = out_dtype or dtype
+    n, count = len(bufs), bufs[0].size
+    bufs = [np.ascontiguousarray(b, _NP[dtype]) for b in bufs]
+    shards = [np.zeros(max(0, min(count, (j + 1) * L) - min(count, j * L)), _NP[out_dtype])
+              for j in range(n)]
+    _check(lib().orc_ring_reduce_scatter_L(n, count, L, _DT[dtype], _OP[op], _ptrs(bufs),
+                                           _ptrs(shards), _DT[out_dtype], None, None, None),
+           "ring_reduce_scatter_L")
+    return shards
+
+
+def fsdp2_shard_rows(dim0: int, n: int, j: int) -> tuple[int, int]:
+    """Rows [lo, hi) of dim 0 that rank j owns (torch.chunk-like)."""
+    Lr = -(-dim0 // n) if n else 0
+    return min(dim0, j * Lr), min(dim0, (j + 1) * Lr)
+
+
+class _Shape(C.Structure):
+    _fields_ = [("dim0", C.c_size_t), ("row_numel", C.c_size_t)]
+
+
+def fsdp2_step(shapes, grads, master, m, v, cfg: AdamWConfig):
+    """shapes: [(dim0, row_numel)] per parameter; grads[p][r]: full bf16
+    gradient of parameter p on rank r; master/m/v[p][j]: fp32 shard j
+    (updated in place).  Returns params[p][r], the all-gathered bf16."""
+    n = len(grads[0]) if grads else 1
+    P = len(shapes)
+    sh = (_Shape * max(1, P))(*[_Shape(d, rn) for d, rn in shapes])
+    flat_g = [np.ascontiguousarray(g, np.uint16) for row in grads for g in row]
+    params = [[np.zeros(d * rn, np.uint16) for _ in range(n)] for d, rn in shapes]
+    flat_p = [x for row in params for x in row]
+    flat = lambda xs: [x for row in xs for x in row]
+    c = _cfg(cfg)
+    _check(lib().orc_fsdp2_step(P, sh, n, _ptrs(flat_g), _ptrs(flat(master)), _ptrs(flat(m)),
+                                _ptrs(flat(v)), C.byref(c), _ptrs(flat_p)), "fsdp2_step")
+    return params
+
+
+def accumulate(acc: np.ndarray, g: np.ndarray, dtype: str) -> None:
+    """acc += g in fp32 (g: f32 or bf16 bits), in place."""
+    assert acc.dtype == np.float32 and acc.flags["C_CONTIGUOUS"]
+    g = np.ascontiguousarray(g, _NP[dtype])
+    lib().orc_accumulate(acc.size, acc.ctypes.data, g.ctypes.data, _DT[dtype])
 
 
 # ---- a6 / a7 ----------------------------------------------------------------

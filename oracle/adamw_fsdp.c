@@ -134,3 +134,48 @@ int orc_fsdp_step_clipped(int n, size_t count, const uint16_t* const* grads,
   for (int r = 0; r < n; ++r) { free(gshard[r]); free(pshard[r]); }
   return rc;
 }
+
+/* FSDP2 step, parameter by parameter; see oracle.h. */
+int orc_fsdp2_step(int nparams, const orc_param_shape* shapes, int n,
+                   const uint16_t* const* grads, float* const* master,
+                   float* const* m, float* const* v, const orc_adamw_cfg* cfg,
+                   uint16_t* const* params) {
+  if (n < 1 || n > ORC_MAX_RANKS || nparams < 0) return ORC_EINVAL;
+  for (int p = 0; p < nparams; ++p) {
+    const size_t count = shapes[p].dim0 * shapes[p].row_numel;
+    const size_t Lr = (shapes[p].dim0 + (size_t)n - 1) / (size_t)n;
+    const size_t L = Lr * shapes[p].row_numel;
+    float* gshard[ORC_MAX_RANKS];
+    uint16_t* pshard[ORC_MAX_RANKS];
+    for (int r = 0; r < n; ++r) {
+      gshard[r] = (float*)malloc((L ? L : 1) * sizeof(float));
+      pshard[r] = (uint16_t*)malloc((L ? L : 1) * sizeof(uint16_t));
+      if (!gshard[r] || !pshard[r]) {
+        for (int q = 0; q <= r; ++q) { free(gshard[q]); free(pshard[q]); }
+        return ORC_ENOMEM;
+      }
+    }
+    int rc = orc_ring_reduce_scatter_L(n, count, L, ORC_BF16, ORC_AVG,
+                                       (const void* const*)(grads + (size_t)p * n),
+                                       (void* const*)gshard, ORC_F32, NULL, NULL,
+                                       NULL);
+    if (rc == ORC_OK) {
+      for (int j = 0; j < n; ++j) {
+        size_t lo = L * (size_t)j, hi = lo + L;
+        if (lo > count) lo = count;
+        if (hi > count) hi = count;
+        const size_t k = (size_t)p * n + j;
+        orc_adamw(hi - lo, master[k], m[k], v[k], gshard[j], cfg);
+        for (size_t i = 0; i < hi - lo; ++i)
+          pshard[j][i] = orc_f32_to_bf16(master[k][i]);
+      }
+      rc = orc_ring_all_gather_L(n, count, L, ORC_BF16,
+                                 (const void* const*)pshard,
+                                 (void* const*)(params + (size_t)p * n), NULL,
+                                 NULL);
+    }
+    for (int r = 0; r < n; ++r) { free(gshard[r]); free(pshard[r]); }
+    if (rc != ORC_OK) return rc;
+  }
+  return ORC_OK;
+}

@@ -25,6 +25,18 @@ void orc_chunk_bounds(size_t count, int n, int j, size_t* lo, size_t* hi) {
   *hi = b;
 }
 
+/* Chunk j of a buffer of count elements cut into chunks of L elements (the
+ * last ones short or empty).  Used with L = ceil(count/N) for flat buffers
+ * and with L = ceil(dim0/N) * row for FSDP2's dim-0 shards. */
+static void bounds_L(size_t count, size_t L, int j, size_t* lo, size_t* hi) {
+  size_t a = L * (size_t)j;
+  size_t b = a + L;
+  if (a > count) a = count;
+  if (b > count) b = count;
+  *lo = a;
+  *hi = b;
+}
+
 /* ---- bf16 ------------------------------------------------------------- */
 
 uint16_t orc_f32_to_bf16(float x) {
@@ -133,14 +145,14 @@ typedef struct {
   acc_t* data;   /* hi - lo accumulators               */
 } partial_t;
 
-int orc_ring_reduce_scatter(int n, size_t count, int in_dt, int op,
-                            const void* const* bufs, void* const* out_shards,
-                            int out_dt, orc_traffic* tr, int* trace_chunk,
-                            double* trace_value) {
+int orc_ring_reduce_scatter_L(int n, size_t count, size_t L, int in_dt, int op,
+                              const void* const* bufs, void* const* out_shards,
+                              int out_dt, orc_traffic* tr, int* trace_chunk,
+                              double* trace_value) {
   int rc = check_types(n, in_dt, op, out_dt);
   if (rc) return rc;
+  if (L * (size_t)n < count) return ORC_EINVAL;
   if (tr) memset(tr, 0, sizeof(*tr));
-  size_t L = orc_chunk_len(count, n);
 
   /* hold[r]: the partial rank r holds and will send next.
    * inbox[r]: the message rank r receives in the current step. */
@@ -159,7 +171,7 @@ int orc_ring_reduce_scatter(int n, size_t count, int in_dt, int op,
   for (int r = 0; r < n; ++r) {
     int c = (r - 1 + n) % n;
     hold[r].chunk = c;
-    orc_chunk_bounds(count, n, c, &hold[r].lo, &hold[r].hi);
+    bounds_L(count, L, c, &hold[r].lo, &hold[r].hi);
     for (size_t e = hold[r].lo; e < hold[r].hi; ++e)
       hold[r].data[e - hold[r].lo] = load_acc(bufs[r], in_dt, e);
   }
@@ -211,6 +223,16 @@ int orc_ring_reduce_scatter(int n, size_t count, int in_dt, int op,
   return rc;
 }
 
+int orc_ring_reduce_scatter(int n, size_t count, int in_dt, int op,
+                            const void* const* bufs, void* const* out_shards,
+                            int out_dt, orc_traffic* tr, int* trace_chunk,
+                            double* trace_value) {
+  if (n < 1 || n > ORC_MAX_RANKS) return ORC_EINVAL;
+  return orc_ring_reduce_scatter_L(n, count, orc_chunk_len(count, n), in_dt, op,
+                                   bufs, out_shards, out_dt, tr, trace_chunk,
+                                   trace_value);
+}
+
 /* ---- closed-form fold --------------------------------------------------- */
 
 int orc_fold_reduce_scatter(int n, size_t count, int in_dt, int op,
@@ -253,13 +275,13 @@ int orc_fold_columns(int n, size_t nsamp, int in_dt, int op, const void* vals,
  * every rank forwards one D/N shard to its right neighbour; after N-1 steps
  * each rank rearranges what it holds by shard index. */
 
-int orc_ring_all_gather(int n, size_t count, int dt, const void* const* shards,
-                        void* const* bufs, orc_traffic* tr,
-                        int* trace_arrival) {
+int orc_ring_all_gather_L(int n, size_t count, size_t L, int dt,
+                          const void* const* shards, void* const* bufs,
+                          orc_traffic* tr, int* trace_arrival) {
   if (n < 1 || n > ORC_MAX_RANKS || orc_esize(dt) == 0) return ORC_EINVAL;
+  if (L * (size_t)n < count) return ORC_EINVAL;
   if (tr) memset(tr, 0, sizeof(*tr));
   size_t es = orc_esize(dt);
-  size_t L = orc_chunk_len(count, n);
 
   /* held[r][k]: the k-th shard rank r came to hold (k = 0 is its own),
    * with its id in held_id[r][k]. */
@@ -272,7 +294,7 @@ int orc_ring_all_gather(int n, size_t count, int dt, const void* const* shards,
       return ORC_ENOMEM;
     }
     size_t lo, hi;
-    orc_chunk_bounds(count, n, r, &lo, &hi);
+    bounds_L(count, L, r, &lo, &hi);
     memcpy(held[r], shards[r], (hi - lo) * es);
     held_id[r][0] = r;
   }
@@ -284,7 +306,7 @@ int orc_ring_all_gather(int n, size_t count, int dt, const void* const* shards,
       int d = (r + 1) % n;
       int id = held_id[r][s - 1];
       size_t lo, hi;
-      orc_chunk_bounds(count, n, id, &lo, &hi);
+      bounds_L(count, L, id, &lo, &hi);
       memcpy(held[d] + (size_t)s * L * es, held[r] + (size_t)(s - 1) * L * es,
              (hi - lo) * es);
       held_id[d][s] = id;
@@ -299,13 +321,21 @@ int orc_ring_all_gather(int n, size_t count, int dt, const void* const* shards,
     for (int k = 0; k < n; ++k) {
       int id = held_id[r][k];
       size_t lo, hi;
-      orc_chunk_bounds(count, n, id, &lo, &hi);
+      bounds_L(count, L, id, &lo, &hi);
       memcpy((unsigned char*)bufs[r] + lo * es, held[r] + (size_t)k * L * es,
              (hi - lo) * es);
     }
     free(held[r]);
   }
   return ORC_OK;
+}
+
+int orc_ring_all_gather(int n, size_t count, int dt, const void* const* shards,
+                        void* const* bufs, orc_traffic* tr,
+                        int* trace_arrival) {
+  if (n < 1 || n > ORC_MAX_RANKS) return ORC_EINVAL;
+  return orc_ring_all_gather_L(n, count, orc_chunk_len(count, n), dt, shards,
+                               bufs, tr, trace_arrival);
 }
 
 /* ---- ring all-reduce = reduce-scatter + all-gather ([DT] section 2) ---- */
@@ -369,6 +399,12 @@ int orc_naive_all_reduce(int n, size_t count, int in_dt, int op,
   }
   free(root);
   return ORC_OK;
+}
+
+/* ---- gradient accumulation ([AIG] 6.2.6, no_sync) ------------------------ */
+
+void orc_accumulate(size_t count, float* acc, const void* g, int g_dtype) {
+  for (size_t e = 0; e < count; ++e) acc[e] = acc[e] + load_acc(g, g_dtype, e).f;
 }
 
 /* ---- alpha-beta model --------------------------------------------------- */

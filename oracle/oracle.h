@@ -83,6 +83,15 @@ int orc_ring_reduce_scatter(int n, size_t count, int in_dtype, int op,
                             int out_dtype, orc_traffic* tr, int* trace_chunk,
                             double* trace_value);
 
+/* The same with an explicit chunk length L (chunk j = [j*L, (j+1)*L) cut
+ * at count; L*N >= count), for FSDP2's dim-0 shards, whose chunks are
+ * whole rows ([DT] section 4, FSDP2 Shard(0)). */
+int orc_ring_reduce_scatter_L(int n, size_t count, size_t L, int in_dtype,
+                              int op, const void* const* bufs,
+                              void* const* out_shards, int out_dtype,
+                              orc_traffic* tr, int* trace_chunk,
+                              double* trace_value);
+
 /* Closed-form fold with the same association:
  * y_j[e] = ((x_{j+1}[e] + x_{j+2}[e]) + ...) + x_j[e], ranks mod N. */
 int orc_fold_reduce_scatter(int n, size_t count, int in_dtype, int op,
@@ -105,6 +114,10 @@ int orc_fold_columns(int n, size_t nsamp, int in_dtype, int op,
 int orc_ring_all_gather(int n, size_t count, int dtype,
                         const void* const* shards, void* const* bufs,
                         orc_traffic* tr, int* trace_arrival);
+
+int orc_ring_all_gather_L(int n, size_t count, size_t L, int dtype,
+                          const void* const* shards, void* const* bufs,
+                          orc_traffic* tr, int* trace_arrival);
 
 /* ---- a5: ring all-reduce = ring reduce-scatter then ring all-gather ----
  * in and out may be the same buffers (in place). */
@@ -183,6 +196,32 @@ void orc_bucket_unpack(int n, int ntensors, const size_t* numels,
                        size_t esize, const int* tensor_bucket,
                        const size_t* tensor_offset,
                        const void* const* buckets, void* const* tensors);
+
+/* ---- FSDP2: per-parameter Shard(0) ([DT] section 4, FSDP2) --------------
+ * Each parameter p is its own DTensor sharded on dim 0: rank j owns rows
+ * [j*Lr, min((j+1)*Lr, dim0)) with Lr = ceil(dim0 / N) (torch.chunk-like,
+ * trailing shards short or empty), i.e. chunk length Lr * row_numel
+ * elements of the flattened parameter.  The step per parameter is the
+ * FSDP step above with that chunking: ring reduce-scatter of the bf16
+ * grads (fp32 partials, AVG), AdamW on owner j's fp32 shard, bf16 cast,
+ * ring all-gather.  Arrays are indexed [p*N + r] (grads, params: full
+ * parameter; master/m/v: shard j of parameter p at [p*N + j]). */
+typedef struct {
+  size_t dim0;
+  size_t row_numel;
+} orc_param_shape;
+
+int orc_fsdp2_step(int nparams, const orc_param_shape* shapes, int n,
+                   const uint16_t* const* grads, float* const* master,
+                   float* const* m, float* const* v, const orc_adamw_cfg* cfg,
+                   uint16_t* const* params);
+
+/* ---- gradient accumulation ([AIG] 6.2.6, DDP no_sync) -------------------
+ * Micro-steps inside no_sync() only add the new local gradient to the
+ * accumulated one, rank by rank, with no communication:
+ * acc[e] <- acc[e] + g[e] in fp32 (g of dtype ORC_F32 or ORC_BF16).  The
+ * last micro-step adds its gradient and then all-reduces the sum. */
+void orc_accumulate(size_t count, float* acc, const void* g, int g_dtype);
 
 /* ---- a11: alpha-beta model ([AIG] 6.1.4; [DT] section 2; [NX] 2.3) ----
  * T_ring_allreduce = 2(N-1)*alpha + 2(N-1)/N * S / B, seconds. */

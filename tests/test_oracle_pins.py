@@ -558,3 +558,111 @@ def test_clip_norm_and_scaled_gradient(n, count):
     gp = (g_full[0] * c).astype(np.float32)
     want_m = np.float32(1 - cfg.beta1) * gp
     assert np.max(np.abs(np.concatenate(m) - want_m)) <= 2 ** -22 * np.max(np.abs(want_m))
+
+
+# ---- FSDP2: per-parameter Shard(0) ----------------------------------------------
+
+def test_fsdp2_unit1_shards_and_reduce_scatter(golden_dir):
+    g = load(golden_dir, "fsdp2_unit1.json")
+    n = g["world_size"]
+    for p in g["params"]:
+        for j in range(n):
+            assert list(O.fsdp2_shard_rows(p["shape"][0], n, j)) == p["rows"][j], p["name"]
+    # reduce-scatter of layer1.weight with bitmask payloads: x_{j,i} = row j
+    # of rank i's gradient
+    shape = [p for p in g["params"] if p["name"] == g["reduce_scatter"]["param"]][0]["shape"]
+    rows, row_numel = shape[0], shape[1]
+    bufs = []
+    for i in range(n):
+        b = np.zeros(rows * row_numel, np.int32)
+        for j in range(rows):
+            b[j * row_numel:(j + 1) * row_numel] = 1 << (2 * j + i)
+        bufs.append(b)
+    Lr = -(-rows // n)
+    shards = O.ring_reduce_scatter_L(bufs, Lr * row_numel, "i32", "sum")
+    rs = g["reduce_scatter"]
+    assert np.all(shards[0] == mask_of(rs["rank0_row0"], 2))
+    assert np.all(shards[1] == mask_of(rs["rank1_row1"], 2))
+
+
+def test_fsdp2_uneven_and_empty_shards(golden_dir):
+    u = load(golden_dir, "uneven_shards.json")
+    for case in u["cases"]:
+        got = [list(O.fsdp2_shard_rows(case["dim0"], case["world_size"], j))
+               for j in range(case["world_size"])]
+        assert got == case["rows"]
+
+
+def fsdp2_case(shapes, n, seed):
+    grads = [I.host_rank_buffers(n, d * rn, "bf16", std=1e-3, seed0=seed + 100 * p)
+             for p, (d, rn) in enumerate(shapes)]
+    master, m, v = [], [], []
+    for p, (d, rn) in enumerate(shapes):
+        full = I.np_normal_f32(d * rn, 0.02, seed + 7 * p + 1)
+        row_m, row_mm, row_v = [], [], []
+        for j in range(n):
+            lo, hi = O.fsdp2_shard_rows(d, n, j)
+            row_m.append(full[lo * rn:hi * rn].copy())
+            row_mm.append(np.zeros((hi - lo) * rn, np.float32))
+            row_v.append(np.zeros((hi - lo) * rn, np.float32))
+        master.append(row_m); m.append(row_mm); v.append(row_v)
+    return grads, master, m, v
+
+
+SHAPES = [(2, 3), (2, 1), (3, 3), (5, 7), (1, 16), (9, 1), (0, 4), (16, 8)]
+
+
+@pytest.mark.parametrize("n", [2, 3, 4])
+def test_fsdp2_equals_unsharded_step_per_parameter(n):
+    """The sharded update, re-gathered, equals one unsharded AdamW step on
+    each full parameter after the averaging all-reduce (bit for bit)."""
+    cfg = O.AdamWConfig()
+    grads, master, m, v = fsdp2_case(SHAPES, n, 70)
+    full0 = [np.concatenate(row) if row else np.zeros(0, np.float32) for row in master]
+    params = O.fsdp2_step(SHAPES, grads, master, m, v, cfg)
+    for p, (d, rn) in enumerate(SHAPES):
+        if d * rn == 0:
+            continue
+        g_full, _ = O.ring_all_reduce(grads[p], "bf16", "avg", "f32")
+        pf = full0[p].copy()
+        mf = np.zeros_like(pf)
+        vf = np.zeros_like(pf)
+        O.adamw(pf, mf, vf, g_full[0], cfg)
+        assert np.concatenate(master[p]).tobytes() == pf.tobytes(), p
+        assert np.concatenate(m[p]).tobytes() == mf.tobytes(), p
+        for r in range(n):
+            assert params[p][r].tobytes() == O.f32_to_bf16(pf).tobytes(), (p, r)
+
+
+@pytest.mark.parametrize("n,count", [(2, 14), (4, 64), (3, 10)])
+def test_fsdp2_with_scalar_rows_is_the_flat_step(n, count):
+    """A 1-D parameter of `count` entries is sharded like the flat buffer of
+    the FSDP1 step, so both give identical bits."""
+    cfg = O.AdamWConfig()
+    grads, master, m, v = fsdp2_case([(count, 1)], n, 90)
+    fm = [x.copy() for x in master[0]]
+    fmm = [x.copy() for x in m[0]]
+    fv = [x.copy() for x in v[0]]
+    params2 = O.fsdp2_step([(count, 1)], grads, master, m, v, cfg)
+    params1 = O.fsdp_step(grads[0], fm, fmm, fv, cfg)
+    for r in range(n):
+        assert params2[0][r].tobytes() == params1[r].tobytes()
+    for a, b in zip(master[0] + m[0] + v[0], fm + fmm + fv):
+        assert a.tobytes() == b.tobytes()
+
+
+# ---- gradient accumulation (no_sync) ------------------------------------------------
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_accumulate_is_fp32_addition(dt):
+    rng = np.random.default_rng(3)
+    acc = rng.standard_normal(1000).astype(np.float32)
+    g = I.host_rank_buffers(1, 1000, dt, std=1e-2, seed0=4)[0]
+    want = acc + (O.bf16_to_f32(g) if dt == "bf16" else g)
+    O.accumulate(acc, g, dt)
+    assert acc.tobytes() == want.astype(np.float32).tobytes()
+    # integer-valued micro-steps accumulate exactly
+    acc = np.zeros(16, np.float32)
+    for k in range(1, 5):
+        O.accumulate(acc, np.full(16, float(k), np.float32), "f32")
+    assert np.all(acc == 10.0)
