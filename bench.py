@@ -412,6 +412,107 @@ class FsdpStep(Workload):
                             self.cfg, self.t_params, stream)
 
 
+def transformer_shapes(hidden=2048, layers=24, vocab=32000, ffn=8192):
+    """Parameter shapes (dim0, row) of a decoder-only transformer: per layer
+    qkv, output, up and down projections and two norms, plus the embedding
+    (1.27e9 parameters with the defaults)."""
+    shapes = [(vocab, hidden)]
+    for _ in range(layers):
+        shapes += [(3 * hidden, hidden), (hidden, hidden), (ffn, hidden), (hidden, ffn),
+                   (hidden, 1), (hidden, 1)]
+    return shapes
+
+
+class Fsdp2Step(Workload):
+    """FSDP2 per-parameter Shard(0) step over a transformer's parameters,
+    8 ranks; each rank's grads and params live in one 256-byte-aligned slab
+    per rank, the shards' fp32 state in one slab per parameter set."""
+
+    def __init__(self, n=8):
+        self.n = n
+        self.shapes = transformer_shapes()
+        self.P = sum(d * r for d, r in self.shapes)
+        self.nbytes = (4 * n + 24) * self.P
+        self.name = f"fsdp2_step_bf16_{n}ranks_{len(self.shapes)}params_{self.P / 1e9:.2f}e9"
+        self.kernel = f"k_fsdp2<{n}>"
+        self.profile = f"k_fsdp2_fsdp2_step_{n}x{len(self.shapes)}params"
+        self.launches = -(-len(self.shapes) // min(64, 2560 // (5 * n)))
+
+    def setup(self, device):
+        import torch
+        from fsdp_emulated_ranks_gb300 import cr
+        from fsdp_emulated_ranks_gb300 import inputs as I
+        n, pad = self.n, 128
+        sizes = [d * r for d, r in self.shapes]
+        offs, o = [], 0
+        for k in sizes:
+            offs.append(o)
+            o += (k + pad - 1) // pad * pad
+        self.t_g = [torch.empty(o, dtype=torch.bfloat16, device=device) for _ in range(n)]
+        for r, t in enumerate(self.t_g):
+            I.torch_fill_normal_(t, 1e-3, 1000 + r)
+        self.t_p = [torch.empty(o, dtype=torch.bfloat16, device=device) for _ in range(n)]
+        shard = []
+        for (d, rn) in self.shapes:
+            Lr = -(-d // n)
+            shard.append([max(0, min(d, (j + 1) * Lr) - min(d, j * Lr)) * rn for j in range(n)])
+        soffs, so = [], 0
+        for row in shard:
+            so_row = []
+            for k in row:
+                so_row.append(so)
+                so += (k + pad - 1) // pad * pad
+            soffs.append(so_row)
+        self.t_state = torch.zeros(3 * so, dtype=torch.float32, device=device)
+        I.torch_fill_normal_(self.t_state[:so], 0.02, 2000)
+        self.grads, self.params, self.master, self.m, self.v = [], [], [], [], []
+        for p, k in enumerate(sizes):
+            for r in range(n):
+                self.grads.append(self.t_g[r][offs[p]:offs[p] + k])
+                self.params.append(self.t_p[r][offs[p]:offs[p] + k])
+                sk, so0 = shard[p][r], soffs[p][r]
+                self.master.append(self.t_state[so0:so0 + sk] if sk else 0)
+                self.m.append(self.t_state[so + so0:so + so0 + sk] if sk else 0)
+                self.v.append(self.t_state[2 * so + so0:2 * so + so0 + sk] if sk else 0)
+        self.cfg = cr.adamw_cfg()
+
+    def step(self, stream):
+        from fsdp_emulated_ranks_gb300 import cr
+        cr.cr_fsdp2_step(self.shapes, self.n, self.grads, self.master, self.m, self.v, self.cfg,
+                         self.params, stream)
+
+    def teardown(self):
+        self.grads = self.params = self.master = self.m = self.v = None
+        super().teardown()
+
+
+class Accumulate(Workload):
+    """DDP no_sync micro-steps: 8 ranks' fp32 accumulators of 2^25 elements
+    plus a bf16 micro-step gradient each; reduce=True fuses the last
+    micro-step's accumulation with the AVG all-reduce."""
+
+    def __init__(self, reduce, n=8, count=1 << 25):
+        self.reduce, self.n, self.count = reduce, n, count
+        self.nbytes = n * count * (4 + 2 + 4)
+        self.name = (f"{'all_reduce_' if reduce else ''}accumulate_bf16_into_f32_{n}ranks_"
+                     f"{count * 2 >> 20}MiB")
+        self.kernel = f"k_accum_vec<bf16,{n if reduce else 0},8>"
+        self.profile = f"k_accum_vec_{'allreduce_' if reduce else ''}accumulate_{n}x{count}"
+
+    def setup(self, device):
+        import torch
+        self.t_acc = [torch.zeros(self.count, dtype=torch.float32, device=device)
+                      for _ in range(self.n)]
+        self.t_g = alloc_ranks(self.n, self.count, torch.bfloat16, 1e-3, 0, device)
+
+    def step(self, stream):
+        from fsdp_emulated_ranks_gb300 import cr
+        if self.reduce:
+            cr.cr_all_reduce_accumulate(self.t_acc, self.count, self.t_g, "bf16", "avg", stream)
+        else:
+            cr.cr_accumulate(self.t_acc, self.count, self.t_g, "bf16", stream)
+
+
 def make_workload(name, args):
     if name == "allreduce":
         return AllReduce()
@@ -427,11 +528,18 @@ def make_workload(name, args):
         return FsdpStep(count=args.fsdp_count)
     if name == "fsdp_clipped":
         return FsdpStep(count=args.fsdp_count, clip=True)
+    if name == "fsdp2":
+        return Fsdp2Step()
+    if name == "accumulate":
+        return Accumulate(reduce=False)
+    if name == "accumulate_allreduce":
+        return Accumulate(reduce=True)
     raise SystemExit(f"unknown workload {name}")
 
 
 ROW_WORKLOADS = ["reduce_scatter", "all_gather", "allreduce_f32", "bucket_pack",
-                 "bucket_allreduce", "bucket_unpack", "bucket_pipeline", "bucket_fused", "fsdp", "fsdp_clipped"]
+                 "bucket_allreduce", "bucket_unpack", "bucket_pipeline", "bucket_fused", "fsdp", "fsdp_clipped", "fsdp2", "accumulate",
+                 "accumulate_allreduce"]
 
 
 def run_headline(args, world, rank, device, stream, peak):

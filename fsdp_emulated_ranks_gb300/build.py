@@ -25,7 +25,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "--expt-relaxed-constexpr", "-I" + INCLUDE, "-I" + CSRC]
 SOURCES = ["api.cu", "launch_util.cu", "k_collectives.cu", "k_fsdp.cu",
-           "k_bucket.cu", "k_bucket_fused.cu", "fsdp_noalloc.cu", "plan.cpp"]
+           "k_bucket.cu", "k_bucket_fused.cu", "k_fsdp2.cu", "k_accum.cu",
+           "fsdp_noalloc.cu", "plan.cpp"]
 
 
 def nvcc() -> str:

@@ -34,7 +34,8 @@ EXPORTS = ["cr_status_string", "cr_last_error", "cr_version", "cr_chunk_len",
            "cr_bucket_pack", "cr_bucket_unpack", "cr_bucket_all_reduce",
            "cr_bucket_all_reduce_fused", "cr_fsdp_step",
            "cr_fsdp_clip_workspace_bytes", "cr_fsdp_step_clipped",
-           "cr_fsdp_step_clipped_noalloc", "cr_adamw_step", "cr_comm_elems"]
+           "cr_fsdp_step_clipped_noalloc", "cr_fsdp2_step", "cr_accumulate",
+           "cr_all_reduce_accumulate", "cr_adamw_step", "cr_comm_elems"]
 
 _lib = None
 
@@ -49,6 +50,10 @@ class AdamWCfg(C.Structure):
     _fields_ = [("lr", C.c_double), ("beta1", C.c_double),
                 ("beta2", C.c_double), ("eps", C.c_double),
                 ("weight_decay", C.c_double), ("step", C.c_int64)]
+
+
+class ParamShape(C.Structure):
+    _fields_ = [("dim0", C.c_size_t), ("row_numel", C.c_size_t)]
 
 
 class BucketPlanT(C.Structure):
@@ -98,6 +103,9 @@ def lib() -> C.CDLL:
                                        vp, sz, vp, vp, vp]
     L.cr_fsdp_step_clipped_noalloc.argtypes = [vp, i, sz, vp, vp, vp, C.POINTER(AdamWCfg),
                                                C.c_double, vp, vp, vp]
+    L.cr_fsdp2_step.argtypes = [vp, i, i, vp, vp, vp, vp, C.POINTER(AdamWCfg), vp, vp]
+    L.cr_accumulate.argtypes = [vp, i, sz, vp, i, vp]
+    L.cr_all_reduce_accumulate.argtypes = [vp, i, sz, vp, i, i, vp]
     L.cr_adamw_step.argtypes = [sz, vp, vp, vp, vp, C.POINTER(AdamWCfg), vp, vp]
     L.cr_comm_elems.argtypes = [i, i, i, sz, i, C.POINTER(C.c_uint64),
                                 C.POINTER(C.c_uint64), C.POINTER(i)]
@@ -306,6 +314,26 @@ def cr_fsdp_step_clipped_noalloc(grads, count, master, m, v, cfg: AdamWCfg, max_
                                               C.byref(cfg), float(max_norm), _ptr_array(params),
                                               _ptr(norm_out), _stream(stream)),
            "cr_fsdp_step_clipped_noalloc")
+
+
+def cr_fsdp2_step(shapes, nranks, grads, master, m, v, cfg: AdamWCfg, params,
+                  stream=None) -> None:
+    """shapes: [(dim0, row_numel)]; the pointer lists are flat, index p*N + r."""
+    arr = (ParamShape * max(1, len(shapes)))(*[ParamShape(d, rn) for d, rn in shapes])
+    _check(lib().cr_fsdp2_step(arr, len(shapes), nranks, _ptr_array(grads), _ptr_array(master),
+                               _ptr_array(m), _ptr_array(v), C.byref(cfg), _ptr_array(params),
+                               _stream(stream)), "cr_fsdp2_step")
+
+
+def cr_accumulate(acc, count, grads, grad_dtype, stream=None) -> None:
+    _check(lib().cr_accumulate(_ptr_array(acc), len(acc), count, _ptr_array(grads),
+                               _dtype(grad_dtype), _stream(stream)), "cr_accumulate")
+
+
+def cr_all_reduce_accumulate(acc, count, grads, grad_dtype, op, stream=None) -> None:
+    _check(lib().cr_all_reduce_accumulate(_ptr_array(acc), len(acc), count, _ptr_array(grads),
+                                          _dtype(grad_dtype), _op(op), _stream(stream)),
+           "cr_all_reduce_accumulate")
 
 
 def cr_adamw_step(n, master, m, v, grad, cfg: AdamWCfg, param_bf16=None,

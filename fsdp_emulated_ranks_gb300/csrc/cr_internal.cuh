@@ -122,6 +122,44 @@ struct FusedArgs {
   void* ptrs[kFusedMaxPtrs];  // rank q of tensor k at ptrs[t[k].ptr0 + q]
 };
 
+// FSDP2 step: one parameter of a launch.  Its 5N pointers sit in
+// Fsdp2Args::ptrs from ptr0: grads[0..N), params[N..2N), master[2N..3N),
+// m[3N..4N), v[4N..5N).
+struct Fsdp2Param {
+  uint64_t numel;  // dim0 * row_numel
+  uint64_t L;      // shard length: ceil(dim0 / N) rows * row_numel
+  FastDiv Ld;      // division by L
+  uint32_t ptr0;
+  uint32_t vw;     // 32: vector path with 32-byte state, 16: 16-byte, 0: elements
+};
+
+constexpr int kFsdp2MaxParams = 64;
+constexpr int kFsdp2MaxPtrs = 2560;
+constexpr uint64_t kFsdp2TileElems = 4096;  // elements of a parameter per CTA
+
+struct Fsdp2Args {
+  int nparams;
+  int n;
+  float inv_n;
+  AdamScalars a;
+  uint32_t tile_start[kFsdp2MaxParams + 1];
+  Fsdp2Param p[kFsdp2MaxParams];
+  void* ptrs[kFsdp2MaxPtrs];
+};
+
+// Gradient accumulation (no_sync) and the fused accumulate + all-reduce.
+struct AccumArgs {
+  float* acc[kMaxRanks];
+  const void* grads[kMaxRanks];
+  uint64_t count;
+  uint64_t L;
+  FastDiv Ld;
+  int n;
+  int reduce;  // 0: acc[r] += g[r] only; 1: then all-reduce the sums in place
+  int avg;
+  float inv_n;
+};
+
 enum FoldMode { kRS = 0, kAR = 1 };
 
 // Launchers (defined next to their kernels).  `vw` is the vector width in
@@ -141,6 +179,10 @@ cudaError_t launch_copy(const CopyArgs& a, uint32_t ntiles, cudaStream_t s);
 cudaError_t launch_bucket_fused(cr_dtype d, const FusedArgs& a, uint32_t ntiles,
                                 cudaStream_t s);
 uint64_t fused_tile_elems(cr_dtype d);  // elements of a tensor per CTA tile
+cudaError_t launch_fsdp2(const Fsdp2Args& a, uint32_t ntiles, cudaStream_t s);
+// grad_dtype CR_F32 or CR_BF16; vw as for the other launchers (16-byte
+// grads and 32- or 16-byte accumulators).
+cudaError_t launch_accum(cr_dtype grad_dtype, const AccumArgs& a, int vw, cudaStream_t s);
 
 // Records `msg` as the detail cr_last_error() returns on this thread.
 void report_error(cr_status status, const char* msg);

@@ -1,0 +1,111 @@
+// fsdp_body.cuh -- per-vector and per-element work of the fused FSDP step,
+// shared by the flat-buffer kernel (k_fsdp.cu) and the per-parameter FSDP2
+// kernel (k_fsdp2.cu).
+#pragma once
+
+#include "cr_internal.cuh"
+#include "fold.cuh"
+
+namespace cr {
+
+struct AdamOut {
+  float p, m, v;
+};
+
+__device__ __forceinline__ AdamOut adamw_elem(float p, float m, float v,
+                                              float g, const AdamScalars& a) {
+  AdamOut o;
+  const float pd = __fmul_rn(p, a.decay);
+  o.m = __fadd_rn(__fmul_rn(a.b1, m), __fmul_rn(a.omb1, g));
+  o.v = __fadd_rn(__fmul_rn(a.b2, v), __fmul_rn(a.omb2, __fmul_rn(g, g)));
+  const float mh = __fdiv_rn(o.m, a.bc1);
+  const float vh = __fdiv_rn(o.v, a.bc2);
+  const float denom = __fadd_rn(__fsqrt_rn(vh), a.eps);
+  o.p = __fsub_rn(pd, __fmul_rn(a.lr, __fdiv_rn(mh, denom)));
+  return o;
+}
+
+// 8 fp32 state words at p: one 32-byte access (SW == 8) or two 16-byte ones.
+template <int SW>
+__device__ __forceinline__ void ld_state8(const float* p, uint32_t* w) {
+  if constexpr (SW == 8) {
+    const Words<8> v = ldv<8>(p);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = v.w[i];
+  } else {
+    const uint4 a = ld16(p), b = ld16(p + 4);
+    w[0] = a.x, w[1] = a.y, w[2] = a.z, w[3] = a.w;
+    w[4] = b.x, w[5] = b.y, w[6] = b.z, w[7] = b.w;
+  }
+}
+template <int SW>
+__device__ __forceinline__ void st_state8(float* p, const uint32_t* w) {
+  if constexpr (SW == 8) {
+    st32(p, w);
+  } else {
+    st16(p, make_uint4(w[0], w[1], w[2], w[3]));
+    st16(p + 4, make_uint4(w[4], w[5], w[6], w[7]));
+  }
+}
+
+// Element e0..e0+7 of a flat buffer (e0 % 8 == 0; the vector lies inside
+// chunk j = e0 / L, i.e. L % 8 == 0): fold the n bf16 gradients in ring
+// order, average, clip, AdamW on owner j's fp32 state, bf16 cast, write
+// the parameter to every rank.  SW = 8: 32-byte state accesses.
+template <int NT, int SW>
+__device__ __forceinline__ void fsdp_vector(const void* const* grads, void* const* params,
+                                            float* const* master, float* const* m,
+                                            float* const* v, int n, uint64_t L,
+                                            const FastDiv& Ld, float inv_n,
+                                            const AdamScalars& as, float coef, uint64_t e0) {
+  const uint64_t j64 = fastdiv_div(Ld, e0);
+  const int j = (int)j64;
+  const uint64_t k = e0 - j64 * L;  // offset inside shard j
+  float g[8];
+  fold_vec16<CR_BF16, NT>(grads, n, j, e0 * 2, g);
+  float* mp = master[j] + k;
+  float* mm = m[j] + k;
+  float* mv = v[j] + k;
+  uint32_t pw[8], mw[8], vw[8];
+  ld_state8<SW>(mp, pw);
+  ld_state8<SW>(mm, mw);
+  ld_state8<SW>(mv, vw);
+  uint32_t po[8], mo[8], vo[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float gi = __fmul_rn(finish_avg(g[i], n, inv_n), coef);
+    const AdamOut o = adamw_elem(__uint_as_float(pw[i]), __uint_as_float(mw[i]),
+                                 __uint_as_float(vw[i]), gi, as);
+    po[i] = __float_as_uint(o.p);
+    mo[i] = __float_as_uint(o.m);
+    vo[i] = __float_as_uint(o.v);
+  }
+  st_state8<SW>(mp, po);
+  st_state8<SW>(mm, mo);
+  st_state8<SW>(mv, vo);
+  const uint4 pb = make_uint4(pack_bf16x2(__uint_as_float(po[0]), __uint_as_float(po[1])),
+                              pack_bf16x2(__uint_as_float(po[2]), __uint_as_float(po[3])),
+                              pack_bf16x2(__uint_as_float(po[4]), __uint_as_float(po[5])),
+                              pack_bf16x2(__uint_as_float(po[6]), __uint_as_float(po[7])));
+#pragma unroll 8
+  for (int r = 0; r < n; ++r) st16(static_cast<unsigned char*>(params[r]) + e0 * 2, pb);
+}
+
+// The same for one element e (any alignment, any chunk).
+__device__ __forceinline__ void fsdp_element(const void* const* grads, void* const* params,
+                                             float* const* master, float* const* m,
+                                             float* const* v, int n, uint64_t L,
+                                             const FastDiv& Ld, float inv_n,
+                                             const AdamScalars& as, float coef, uint64_t e) {
+  const uint64_t j64 = fastdiv_div(Ld, e);
+  const int j = (int)j64;
+  const uint64_t k = e - j64 * L;
+  const float gi = __fmul_rn(finish_avg(fold_elem<CR_BF16>(grads, n, j, e), n, inv_n), coef);
+  const AdamOut o = adamw_elem(master[j][k], m[j][k], v[j][k], gi, as);
+  master[j][k] = o.p;
+  m[j][k] = o.m;
+  v[j][k] = o.v;
+  for (int r = 0; r < n; ++r) st_elem<CR_BF16>(params[r], e, o.p);
+}
+
+}  // namespace cr

@@ -19,25 +19,9 @@
 // weight-decay rule stated in include/cr.h.
 #include "cr_internal.cuh"
 #include "fold.cuh"
+#include "fsdp_body.cuh"
 
 namespace cr {
-
-struct AdamOut {
-  float p, m, v;
-};
-
-__device__ __forceinline__ AdamOut adamw_elem(float p, float m, float v,
-                                              float g, const AdamScalars& a) {
-  AdamOut o;
-  const float pd = __fmul_rn(p, a.decay);
-  o.m = __fadd_rn(__fmul_rn(a.b1, m), __fmul_rn(a.omb1, g));
-  o.v = __fadd_rn(__fmul_rn(a.b2, v), __fmul_rn(a.omb2, __fmul_rn(g, g)));
-  const float mh = __fdiv_rn(o.m, a.bc1);
-  const float vh = __fdiv_rn(o.v, a.bc2);
-  const float denom = __fadd_rn(__fsqrt_rn(vh), a.eps);
-  o.p = __fsub_rn(pd, __fmul_rn(a.lr, __fdiv_rn(mh, denom)));
-  return o;
-}
 
 // Clip coefficient of clip_grad_norm_, the same in every CTA: the partial
 // sums are added in a fixed order (lane-strided, then a fixed shuffle tree),
@@ -106,29 +90,6 @@ __global__ void __launch_bounds__(kBlock)
   }
 }
 
-// 8 fp32 state words at p: one 32-byte access (SW == 8) or two 16-byte ones.
-template <int SW>
-__device__ __forceinline__ void ld_state8(const float* p, uint32_t* w) {
-  if constexpr (SW == 8) {
-    const Words<8> v = ldv<8>(p);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = v.w[i];
-  } else {
-    const uint4 a = ld16(p), b = ld16(p + 4);
-    w[0] = a.x, w[1] = a.y, w[2] = a.z, w[3] = a.w;
-    w[4] = b.x, w[5] = b.y, w[6] = b.z, w[7] = b.w;
-  }
-}
-template <int SW>
-__device__ __forceinline__ void st_state8(float* p, const uint32_t* w) {
-  if constexpr (SW == 8) {
-    st32(p, w);
-  } else {
-    st16(p, make_uint4(w[0], w[1], w[2], w[3]));
-    st16(p + 4, make_uint4(w[4], w[5], w[6], w[7]));
-  }
-}
-
 // Vector path: 8 elements (one 16-byte bf16 vector per rank) per thread and
 // iteration; SW = 8 moves the fp32 state in 32-byte accesses.
 template <int NT, int SW>
@@ -139,76 +100,21 @@ __global__ void __launch_bounds__(kBlock)
   const uint64_t nvec = a.count / 8;
   const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-  for (uint64_t iv = tid; iv < nvec; iv += stride) {
-    const uint64_t e0 = iv * 8;
-    const uint64_t j64 = fastdiv_div(a.Ld, e0);
-    const int j = (int)j64;
-    const uint64_t k = e0 - j64 * a.L;  // offset inside shard j
-    float g[8];
-    fold_vec16<CR_BF16, NT>(a.grads, n, j, e0 * 2, g);
-    float* mp = a.master[j] + k;
-    float* mm = a.m[j] + k;
-    float* mv = a.v[j] + k;
-    uint32_t pw[8], mw[8], vw[8];
-    ld_state8<SW>(mp, pw);
-    ld_state8<SW>(mm, mw);
-    ld_state8<SW>(mv, vw);
-    uint32_t po[8], mo[8], vo[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float gi = __fmul_rn(finish_avg(g[i], n, a.inv_n), coef);
-      const AdamOut o = adamw_elem(__uint_as_float(pw[i]), __uint_as_float(mw[i]),
-                                   __uint_as_float(vw[i]), gi, a.a);
-      po[i] = __float_as_uint(o.p);
-      mo[i] = __float_as_uint(o.m);
-      vo[i] = __float_as_uint(o.v);
-    }
-    st_state8<SW>(mp, po);
-    st_state8<SW>(mm, mo);
-    st_state8<SW>(mv, vo);
-    const uint4 pb = make_uint4(
-        pack_bf16x2(__uint_as_float(po[0]), __uint_as_float(po[1])),
-        pack_bf16x2(__uint_as_float(po[2]), __uint_as_float(po[3])),
-        pack_bf16x2(__uint_as_float(po[4]), __uint_as_float(po[5])),
-        pack_bf16x2(__uint_as_float(po[6]), __uint_as_float(po[7])));
-#pragma unroll 8
-    for (int r = 0; r < n; ++r)
-      st16(static_cast<unsigned char*>(a.params[r]) + e0 * 2, pb);
-  }
+  for (uint64_t iv = tid; iv < nvec; iv += stride)
+    fsdp_vector<NT, SW>(a.grads, a.params, a.master, a.m, a.v, n, a.L, a.Ld, a.inv_n, a.a, coef,
+                        iv * 8);
   // Ragged tail (count % 8 elements).
   const uint64_t e = nvec * 8 + tid;
-  if (e < a.count) {
-    const uint64_t j64 = fastdiv_div(a.Ld, e);
-    const int j = (int)j64;
-    const uint64_t k = e - j64 * a.L;
-    const float gi =
-        __fmul_rn(finish_avg(fold_elem<CR_BF16>(a.grads, n, j, e), n, a.inv_n), coef);
-    const AdamOut o = adamw_elem(a.master[j][k], a.m[j][k], a.v[j][k], gi, a.a);
-    a.master[j][k] = o.p;
-    a.m[j][k] = o.m;
-    a.v[j][k] = o.v;
-    for (int r = 0; r < n; ++r) st_elem<CR_BF16>(a.params[r], e, o.p);
-  }
+  if (e < a.count)
+    fsdp_element(a.grads, a.params, a.master, a.m, a.v, n, a.L, a.Ld, a.inv_n, a.a, coef, e);
 }
 
 __global__ void __launch_bounds__(kBlock)
     k_fsdp_elem(const __grid_constant__ FsdpArgs a) {
-  const int n = a.n;
   const float coef = clip_coef(a);
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-  for (uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-       e < a.count; e += stride) {
-    const uint64_t j64 = fastdiv_div(a.Ld, e);
-    const int j = (int)j64;
-    const uint64_t k = e - j64 * a.L;
-    const float gi =
-        __fmul_rn(finish_avg(fold_elem<CR_BF16>(a.grads, n, j, e), n, a.inv_n), coef);
-    const AdamOut o = adamw_elem(a.master[j][k], a.m[j][k], a.v[j][k], gi, a.a);
-    a.master[j][k] = o.p;
-    a.m[j][k] = o.m;
-    a.v[j][k] = o.v;
-    for (int r = 0; r < n; ++r) st_elem<CR_BF16>(a.params[r], e, o.p);
-  }
+  for (uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; e < a.count; e += stride)
+    fsdp_element(a.grads, a.params, a.master, a.m, a.v, a.n, a.L, a.Ld, a.inv_n, a.a, coef, e);
 }
 
 // ---- stand-alone AdamW on an fp32 shard ------------------------------------

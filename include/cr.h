@@ -339,6 +339,55 @@ cr_status cr_fsdp_step_clipped_noalloc(const void* const* grads_bf16,
                                        void* const* params_bf16,
                                        float* norm_out, cr_stream_t stream);
 
+/* ---- FSDP2: per-parameter Shard(0) ---------------------------------------
+ * [DT] section 4, FSDP2: every parameter is its own DTensor with placement
+ * Shard(0): of a parameter with dim0 rows of row_numel elements, rank j
+ * owns rows [j*Lr, min((j+1)*Lr, dim0)), Lr = ceil(dim0/N) -- uneven, and
+ * empty for trailing ranks when dim0 < N.  The step applies cr_fsdp_step's
+ * arithmetic to each parameter with that chunking (chunk length
+ * Lr*row_numel elements): ring-ordered reduce-scatter of the bf16 grads in
+ * fp32, / N, AdamW on owner j's fp32 shard, bf16 cast, all-gather.
+ *   shapes[p]                  dim0 and row_numel of parameter p
+ *   grads_bf16[p*N + r]        rank r's full gradient of p (dim0*row_numel)
+ *   master/m/v[p*N + j]        owner j's fp32 shard of p (NULL if empty)
+ *   params_bf16[p*N + r]       rank r's full bf16 parameter p (output)
+ * One launch per 64 parameters (per 512/N when N > 8).  No buffer may
+ * overlap another (CR_ERR_INVALID_ARG).  A parameter whose shard length is
+ * a multiple of 8 and whose buffers are 16-byte aligned takes the vector
+ * path; any other takes the element-wise one, with identical results. */
+typedef struct {
+  size_t dim0;
+  size_t row_numel;
+} cr_param_shape;
+
+cr_status cr_fsdp2_step(const cr_param_shape* shapes, int nparams, int nranks,
+                        const void* const* grads_bf16, float* const* master,
+                        float* const* m, float* const* v,
+                        const cr_adamw_cfg* cfg, void* const* params_bf16,
+                        cr_stream_t stream);
+
+/* ---- DDP gradient accumulation (no_sync) ---------------------------------
+ * "AI Infra Guide, Chapter 6", 6.2.6: micro-steps inside model.no_sync()
+ * only accumulate their gradient locally; the last one accumulates and then
+ * all-reduces the sum.
+ * cr_accumulate: acc[r][e] += grads[r][e] for every rank (fp32 addition;
+ * grads CR_F32 or CR_BF16), no communication.
+ * cr_all_reduce_accumulate: the same addition and, in the same pass, the
+ * all-reduce (CR_SUM or CR_AVG) of the N sums in ring order, written back
+ * into every acc[r] -- equal, bit for bit, to cr_accumulate followed by
+ * cr_all_reduce(acc, ..., CR_F32, op, acc, CR_F32), without the
+ * intermediate write and read of the accumulators.
+ *   acc[r]    rank r's fp32 accumulator, count elements (in/out)
+ *   grads[r]  rank r's new micro-step gradient, count elements
+ * Buffers must not overlap (CR_ERR_INVALID_ARG). */
+cr_status cr_accumulate(float* const* acc, int nranks, size_t count,
+                        const void* const* grads, cr_dtype grad_dtype,
+                        cr_stream_t stream);
+cr_status cr_all_reduce_accumulate(float* const* acc, int nranks, size_t count,
+                                   const void* const* grads,
+                                   cr_dtype grad_dtype, cr_op op,
+                                   cr_stream_t stream);
+
 /* a9 alone: AdamW as above on n fp32 elements with an fp32 gradient
  * (for example a shard produced by cr_reduce_scatter with out_dtype F32);
  * param_bf16 (may be NULL) receives the bf16 cast of the updated master.

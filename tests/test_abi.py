@@ -26,7 +26,7 @@ def L():
 def header_functions():
     text = open(os.path.join(ROOT, "include", "cr.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = set(re.findall(r"\b(cr_[a-z_]+)\s*\(", text))
+    names = set(re.findall(r"\b(cr_[a-z0-9_]+)\s*\(", text))
     return sorted(names)
 
 
@@ -50,7 +50,9 @@ def expect(status, fn, *args, **kw):
     return str(ei.value)
 
 
-FAKE = 1 << 40  # an address never dereferenced: validation fails first
+# An address never dereferenced: every call below either fails validation or
+# has nothing to do (count 0), so no kernel is ever launched on it.
+FAKE = 1 << 40
 
 
 def test_reduce_scatter_validation(L):
@@ -232,3 +234,27 @@ def test_all_reduce_host_validation(L):
     expect(3, cr.cr_all_reduce_host, [h[0] + 2, h[1]], o, 16, "f32", "sum", stream=0)
     expect(2, cr.cr_all_reduce_host, h * 17, o * 17, 16, "f32", "sum", dev_out=d * 17, stream=0)
     cr.cr_all_reduce_host(h, o, 0, "f32", "sum", stream=0)
+
+
+def test_fsdp2_and_accumulate_validation(L):
+    n = 2
+    g = [FAKE + k * (1 << 20) for k in range(2 * n)]
+    p = [FAKE + (1 << 28) + k * (1 << 20) for k in range(2 * n)]
+    ms = [FAKE + (2 << 28) + k * (1 << 20) for k in range(2 * n)]
+    mm = [FAKE + (3 << 28) + k * (1 << 20) for k in range(2 * n)]
+    v = [FAKE + (4 << 28) + k * (1 << 20) for k in range(2 * n)]
+    shapes = [(4, 3), (1, 8)]   # second parameter: rank 1's shard is empty
+    expect(1, cr.cr_fsdp2_step, shapes, 65, g, ms, mm, v, cr.adamw_cfg(), p, stream=0)
+    expect(1, cr.cr_fsdp2_step, shapes, n, g, ms, mm, v, cr.adamw_cfg(step=0), p, stream=0)
+    expect(1, cr.cr_fsdp2_step, shapes, n, g, ms, mm, [v[0], ms[0], v[2], v[3]], cr.adamw_cfg(),
+           p, stream=0)
+    expect(1, cr.cr_fsdp2_step, shapes, n, g[:2] + [0, g[3]], ms, mm, v, cr.adamw_cfg(), p, stream=0)
+    expect(3, cr.cr_fsdp2_step, shapes, n, g, [ms[0] + 2] + ms[1:], mm, v, cr.adamw_cfg(), p,
+           stream=0)
+    a = [FAKE + r * (1 << 20) for r in range(n)]
+    gr = [FAKE + (1 << 30) + r * (1 << 20) for r in range(n)]
+    expect(2, cr.cr_accumulate, a, 16, gr, "i32", stream=0)
+    expect(1, cr.cr_accumulate, a, 16, [a[0], gr[1]], "f32", stream=0)
+    expect(3, cr.cr_all_reduce_accumulate, [a[0] + 2, a[1]], 16, gr, "f32", "avg", stream=0)
+    expect(1, cr.cr_all_reduce_accumulate, a, 16, gr, "f32", 9, stream=0)
+    cr.cr_accumulate(a, 0, gr, "bf16", stream=0)

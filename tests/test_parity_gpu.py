@@ -482,3 +482,88 @@ def test_all_reduce_host_rejects_pageable_memory():
     with pytest.raises(cr.CRError) as ei:
         cr.cr_all_reduce_host(pageable, pageable, count, "f32", "sum")
     assert ei.value.status == 1 and "pinned" in str(ei.value)
+
+
+# ---- FSDP2 per-parameter step ----------------------------------------------------
+
+FSDP2_SHAPES = [(2, 3), (2, 1), (3, 3), (5, 7), (1, 16), (9, 1), (0, 4), (16, 8), (64, 24),
+                (7, 129), (33, 64), (4, 1000)]
+
+
+def fsdp2_host(shapes, n, seed):
+    grads = [I.host_rank_buffers(n, d * rn, "bf16", std=1e-3, seed0=seed + 100 * p)
+             for p, (d, rn) in enumerate(shapes)]
+    master, m, v = [], [], []
+    for p, (d, rn) in enumerate(shapes):
+        full = I.np_normal_f32(d * rn, 0.02, seed + 7 * p + 1)
+        rows = [O.fsdp2_shard_rows(d, n, j) for j in range(n)]
+        master.append([full[lo * rn:hi * rn].copy() for lo, hi in rows])
+        m.append([np.zeros((hi - lo) * rn, np.float32) for lo, hi in rows])
+        v.append([np.zeros((hi - lo) * rn, np.float32) for lo, hi in rows])
+    return grads, master, m, v
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("offset", [0, "16B", 1])
+def test_fsdp2_step_two_steps(n, offset):
+    shapes = FSDP2_SHAPES
+    grads, master, m, v = fsdp2_host(shapes, n, 40 + n)
+    gm = [[Guarded(x.size, "f32", eoff(offset, "f32")) for x in row] for row in master]
+    gmm = [[Guarded(x.size, "f32", eoff(offset, "f32")) for x in row] for row in m]
+    gv = [[Guarded(x.size, "f32", eoff(offset, "f32")) for x in row] for row in v]
+    for g, src in ((gm, master), (gmm, m), (gv, v)):
+        for grow, srow in zip(g, src):
+            for gg, x in zip(grow, srow):
+                if x.size:
+                    gg.view.copy_(to_dev(x, "f32"))
+    gp = [[Guarded(d * rn, "bf16", eoff(offset, "bf16")) for _ in range(n)] for d, rn in shapes]
+    for step in (1, 2):
+        if step == 2:
+            grads = [I.host_rank_buffers(n, d * rn, "bf16", std=1e-3, seed0=500 + 100 * p)
+                     for p, (d, rn) in enumerate(shapes)]
+        cfg = O.AdamWConfig(step=step)
+        want = O.fsdp2_step(shapes, grads, master, m, v, cfg)
+        d_g = [to_dev(x, "bf16", eoff(offset, "bf16")) if x.size else None for row in grads for x in row]
+        flat = lambda xs: [x.ptr() for row in xs for x in row]
+        cr.cr_fsdp2_step(shapes, n, [x if x is not None else 0 for x in d_g], flat(gm), flat(gmm),
+                         flat(gv), cr.adamw_cfg(step=step), flat(gp))
+        torch.cuda.synchronize()
+        for p in range(len(shapes)):
+            for j in range(n):
+                for g, ref, name in ((gm, master, "master"), (gmm, m, "m"), (gv, v, "v")):
+                    g[p][j].check()
+                    assert rel_maxabs(g[p][j].host(), ref[p][j]) <= 1e-6, (name, p, j, step)
+            for r in range(n):
+                gp[p][r].check()
+                assert_match(gp[p][r].host(), want[p][r], "bf16", f"param {p} rank {r} step {step}")
+
+
+# ---- gradient accumulation (no_sync) ---------------------------------------------
+
+@pytest.mark.parametrize("n", [1, 2, 3, 8, 16])
+@pytest.mark.parametrize("gdt", ["bf16", "f32"])
+@pytest.mark.parametrize("offset", [0, "16B", 1])
+@pytest.mark.parametrize("op", ["avg", "sum"])
+def test_accumulate_then_all_reduce(n, gdt, offset, op):
+    """Three no_sync micro-steps (cr_accumulate), then the last micro-step
+    fused with the all-reduce (cr_all_reduce_accumulate): equal to the
+    oracle's accumulations followed by its ring all-reduce."""
+    for count in (8 * n * 40, 8 * n * 40 + 5, 7):
+        acc_h = [np.zeros(count, np.float32) for _ in range(n)]
+        g_acc = [Guarded(count, "f32", eoff(offset, "f32")) for _ in range(n)]
+        for x in g_acc:
+            x.view.zero_()
+        for micro in range(4):
+            gh = I.host_rank_buffers(n, count, gdt, std=1e-2, seed0=10 * micro + count)
+            for r in range(n):
+                O.accumulate(acc_h[r], gh[r], gdt)
+            d_g = [to_dev(x, gdt, eoff(offset, gdt)) for x in gh]
+            if micro < 3:
+                cr.cr_accumulate([x.ptr() for x in g_acc], count, d_g, gdt)
+            else:
+                cr.cr_all_reduce_accumulate([x.ptr() for x in g_acc], count, d_g, gdt, op)
+        want, _ = O.ring_all_reduce(acc_h, "f32", op)
+        torch.cuda.synchronize()
+        for r in range(n):
+            g_acc[r].check()
+            assert_match(g_acc[r].host(), want[r], "f32", f"count {count} rank {r}")
