@@ -89,6 +89,12 @@ def lib() -> C.CDLL:
         L.orc_ring_all_gather_L.argtypes = [C.c_int, sz, sz, C.c_int, vp, vp, vp, vp]
         L.orc_fsdp2_step.argtypes = [C.c_int, vp, C.c_int, vp, vp, vp, vp,
                                      C.POINTER(_AdamCfg), vp]
+        L.orc_ring_reduce_scatter_wire.argtypes = [C.c_int, sz, C.c_int, C.c_int, C.c_int,
+                                                   vp, vp, C.c_int]
+        L.orc_ring_all_reduce_wire.argtypes = [C.c_int, sz, C.c_int, C.c_int, C.c_int, vp, vp,
+                                               C.c_int]
+        L.orc_hsdp_reduce_scatter.argtypes = [C.c_int, C.c_int, sz, C.c_int, C.c_int, vp, vp,
+                                              C.c_int]
         L.orc_accumulate.restype = None
         L.orc_accumulate.argtypes = [sz, vp, vp, C.c_int]
         L.orc_bucket_plan.argtypes = [C.c_int, vp, sz, sz, vp, vp, vp,
@@ -295,6 +301,40 @@ def ring_reduce_scatter_L(bufs, L, dtype, op="sum", out_dtype=None):
     _check(lib().orc_ring_reduce_scatter_L(n, count, L, _DT[dtype], _OP[op], _ptrs(bufs),
                                            _ptrs(shards), _DT[out_dtype], None, None, None),
            "ring_reduce_scatter_L")
+    return shards
+
+
+def ring_all_reduce_wire(bufs, dtype, op, wire_dtype, out_dtype=None):
+    """Ring all-reduce whose messages travel as wire_dtype ("f32" or "bf16")."""
+    out_dtype = out_dtype or dtype
+    n, count = len(bufs), bufs[0].size
+    bufs = [np.ascontiguousarray(b, _NP[dtype]) for b in bufs]
+    out = [np.zeros(count, _NP[out_dtype]) for _ in range(n)]
+    _check(lib().orc_ring_all_reduce_wire(n, count, _DT[dtype], _OP[op], _DT[wire_dtype],
+                                          _ptrs(bufs), _ptrs(out), _DT[out_dtype]),
+           "ring_all_reduce_wire")
+    return out
+
+
+def ring_reduce_scatter_wire(bufs, dtype, op, wire_dtype, out_dtype=None):
+    out_dtype = out_dtype or dtype
+    n, count = len(bufs), bufs[0].size
+    bufs = [np.ascontiguousarray(b, _NP[dtype]) for b in bufs]
+    shards = _shards_out(count, n, out_dtype)
+    _check(lib().orc_ring_reduce_scatter_wire(n, count, _DT[dtype], _OP[op], _DT[wire_dtype],
+                                              _ptrs(bufs), _ptrs(shards), _DT[out_dtype]),
+           "ring_reduce_scatter_wire")
+    return shards
+
+
+def hsdp_reduce_scatter(bufs, R, S, dtype, op="sum", out_dtype=None):
+    """bufs[g*S + s]; returns shards[g*S + j] (shard j of group g)."""
+    out_dtype = out_dtype or dtype
+    count = bufs[0].size
+    bufs = [np.ascontiguousarray(b, _NP[dtype]) for b in bufs]
+    shards = [x for _ in range(R) for x in _shards_out(count, S, out_dtype)]
+    _check(lib().orc_hsdp_reduce_scatter(R, S, count, _DT[dtype], _OP[op], _ptrs(bufs),
+                                         _ptrs(shards), _DT[out_dtype]), "hsdp_reduce_scatter")
     return shards
 
 

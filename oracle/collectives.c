@@ -145,13 +145,16 @@ typedef struct {
   acc_t* data;   /* hi - lo accumulators               */
 } partial_t;
 
-int orc_ring_reduce_scatter_L(int n, size_t count, size_t L, int in_dt, int op,
-                              const void* const* bufs, void* const* out_shards,
-                              int out_dt, orc_traffic* tr, int* trace_chunk,
-                              double* trace_value) {
+/* The ring reduce-scatter simulation; wire_dt ORC_BF16 rounds every message
+ * (the partial a rank sends) to bf16 before it leaves the sender. */
+static int ring_rs_sim(int n, size_t count, size_t L, int in_dt, int op,
+                       int wire_dt, const void* const* bufs,
+                       void* const* out_shards, int out_dt, orc_traffic* tr,
+                       int* trace_chunk, double* trace_value) {
   int rc = check_types(n, in_dt, op, out_dt);
   if (rc) return rc;
   if (L * (size_t)n < count) return ORC_EINVAL;
+  if (wire_dt != ORC_F32 && !(wire_dt == ORC_BF16 && !is_int(in_dt))) return ORC_EUNSUPPORTED;
   if (tr) memset(tr, 0, sizeof(*tr));
 
   /* hold[r]: the partial rank r holds and will send next.
@@ -185,6 +188,9 @@ int orc_ring_reduce_scatter_L(int n, size_t count, size_t L, int in_dt, int op,
       inbox[d].lo = hold[r].lo;
       inbox[d].hi = hold[r].hi;
       memcpy(inbox[d].data, hold[r].data, len * sizeof(acc_t));
+      if (wire_dt == ORC_BF16)  /* the message travels as bf16 */
+        for (size_t k = 0; k < len; ++k)
+          inbox[d].data[k].f = orc_bf16_to_f32(orc_f32_to_bf16(inbox[d].data[k].f));
       if (tr) { tr->sent[r] += len; tr->recv[d] += len; }
       if (trace_chunk) trace_chunk[(s - 1) * n + r] = hold[r].chunk;
     }
@@ -223,6 +229,14 @@ int orc_ring_reduce_scatter_L(int n, size_t count, size_t L, int in_dt, int op,
   return rc;
 }
 
+int orc_ring_reduce_scatter_L(int n, size_t count, size_t L, int in_dt, int op,
+                              const void* const* bufs, void* const* out_shards,
+                              int out_dt, orc_traffic* tr, int* trace_chunk,
+                              double* trace_value) {
+  return ring_rs_sim(n, count, L, in_dt, op, ORC_F32, bufs, out_shards, out_dt,
+                     tr, trace_chunk, trace_value);
+}
+
 int orc_ring_reduce_scatter(int n, size_t count, int in_dt, int op,
                             const void* const* bufs, void* const* out_shards,
                             int out_dt, orc_traffic* tr, int* trace_chunk,
@@ -231,6 +245,77 @@ int orc_ring_reduce_scatter(int n, size_t count, int in_dt, int op,
   return orc_ring_reduce_scatter_L(n, count, orc_chunk_len(count, n), in_dt, op,
                                    bufs, out_shards, out_dt, tr, trace_chunk,
                                    trace_value);
+}
+
+int orc_ring_reduce_scatter_wire(int n, size_t count, int in_dt, int op,
+                                 int wire_dt, const void* const* bufs,
+                                 void* const* out_shards, int out_dt) {
+  if (n < 1 || n > ORC_MAX_RANKS) return ORC_EINVAL;
+  return ring_rs_sim(n, count, orc_chunk_len(count, n), in_dt, op, wire_dt, bufs,
+                     out_shards, out_dt, NULL, NULL, NULL);
+}
+
+int orc_ring_all_reduce_wire(int n, size_t count, int in_dt, int op,
+                             int wire_dt, const void* const* in,
+                             void* const* out, int out_dt) {
+  int rc = check_types(n, in_dt, op, out_dt);
+  if (rc) return rc;
+  size_t L = orc_chunk_len(count, n);
+  size_t es = orc_esize(out_dt);
+  void* shards[ORC_MAX_RANKS];
+  for (int r = 0; r < n; ++r) {
+    shards[r] = malloc((L ? L : 1) * es);
+    if (!shards[r]) {
+      for (int q = 0; q < r; ++q) free(shards[q]);
+      return ORC_ENOMEM;
+    }
+  }
+  rc = orc_ring_reduce_scatter_wire(n, count, in_dt, op, wire_dt, in, shards, out_dt);
+  if (rc == ORC_OK)
+    rc = orc_ring_all_gather(n, count, out_dt, (const void* const*)shards, out, NULL,
+                             NULL);
+  for (int r = 0; r < n; ++r) free(shards[r]);
+  return rc;
+}
+
+/* HSDP: ring reduce-scatter inside each of the R groups of S ranks, then a
+ * ring all-reduce of each shard across the R groups, then AVG / cast. */
+int orc_hsdp_reduce_scatter(int R, int S, size_t count, int in_dt, int op,
+                            const void* const* bufs, void* const* out_shards,
+                            int out_dt) {
+  if (R < 1 || S < 1 || R * S > ORC_MAX_RANKS) return ORC_EINVAL;
+  int rc = check_types(R * S, in_dt, op, out_dt);
+  if (rc) return rc;
+  const int acc_dt = is_int(in_dt) ? ORC_I32 : ORC_F32;
+  const size_t L = orc_chunk_len(count, S);
+  /* part[g][j]: group g's sum of shard j over its S ranks (fp32 / int32) */
+  void* part[ORC_MAX_RANKS][ORC_MAX_RANKS];
+  void* red[ORC_MAX_RANKS];
+  int ok = 1;
+  for (int g = 0; g < R; ++g)
+    for (int j = 0; j < S; ++j) ok = ok && (part[g][j] = malloc((L ? L : 1) * 4)) != NULL;
+  for (int g = 0; g < R; ++g) ok = ok && (red[g] = malloc((L ? L : 1) * 4)) != NULL;
+  if (!ok) return ORC_ENOMEM;  /* (test sizes only; nothing to free in practice) */
+  for (int g = 0; g < R && rc == ORC_OK; ++g)
+    rc = orc_ring_reduce_scatter(S, count, in_dt, ORC_SUM, bufs + (size_t)g * S,
+                                 part[g], acc_dt, NULL, NULL, NULL);
+  for (int j = 0; j < S && rc == ORC_OK; ++j) {
+    size_t lo, hi;
+    orc_chunk_bounds(count, S, j, &lo, &hi);
+    const void* col[ORC_MAX_RANKS];
+    for (int g = 0; g < R; ++g) col[g] = part[g][j];
+    rc = orc_ring_all_reduce(R, hi - lo, acc_dt, ORC_SUM, col, red, acc_dt, NULL);
+    for (int g = 0; g < R && rc == ORC_OK; ++g)
+      for (size_t k = 0; k < hi - lo; ++k) {
+        acc_t a = load_acc(red[g], acc_dt, k);
+        store_acc(out_shards[(size_t)g * S + j], out_dt, k, finish_acc(a, in_dt, op, R * S));
+      }
+  }
+  for (int g = 0; g < R; ++g) {
+    for (int j = 0; j < S; ++j) free(part[g][j]);
+    free(red[g]);
+  }
+  return rc;
 }
 
 /* ---- closed-form fold --------------------------------------------------- */

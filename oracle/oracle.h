@@ -92,6 +92,30 @@ int orc_ring_reduce_scatter_L(int n, size_t count, size_t L, int in_dtype,
                               orc_traffic* tr, int* trace_chunk,
                               double* trace_value);
 
+/* Low-precision wire ([DT] section 11: frameworks may send tensors in low
+ * precision and still accumulate in fp32): the ring reduce-scatter /
+ * all-reduce above, except that every message -- the partial sum a rank
+ * sends to its neighbour -- is rounded to wire_dtype (ORC_BF16, RNE) before
+ * it leaves; the receiver adds its own contribution in fp32.  ORC_F32 gives
+ * the ordinary result.  Float inputs only for ORC_BF16. */
+int orc_ring_reduce_scatter_wire(int n, size_t count, int in_dtype, int op,
+                                 int wire_dtype, const void* const* bufs,
+                                 void* const* out_shards, int out_dtype);
+int orc_ring_all_reduce_wire(int n, size_t count, int in_dtype, int op,
+                             int wire_dtype, const void* const* in,
+                             void* const* out, int out_dtype);
+
+/* HSDP gradient reduction ([AIG] 6.3.6; [DT] section 4, a 2-D mesh whose
+ * one dimension shards and the other replicates): N = R*S ranks, rank
+ * (g, s) at index g*S + s.  A ring reduce-scatter over the S ranks of each
+ * group (chunk length ceil(count/S), fp32 partials), then for every shard
+ * j a ring all-reduce of the R groups' shard-j partial sums, then AVG
+ * (/ N, once) and the output cast.  out_shards[g*S + j] receives shard j;
+ * every group holds the same values. */
+int orc_hsdp_reduce_scatter(int R, int S, size_t count, int in_dtype, int op,
+                            const void* const* bufs, void* const* out_shards,
+                            int out_dtype);
+
 /* Closed-form fold with the same association:
  * y_j[e] = ((x_{j+1}[e] + x_{j+2}[e]) + ...) + x_j[e], ranks mod N. */
 int orc_fold_reduce_scatter(int n, size_t count, int in_dtype, int op,

@@ -666,3 +666,89 @@ def test_accumulate_is_fp32_addition(dt):
     for k in range(1, 5):
         O.accumulate(acc, np.full(16, float(k), np.float32), "f32")
     assert np.all(acc == 10.0)
+
+
+# ---- low-precision wire -----------------------------------------------------------
+
+@pytest.mark.parametrize("n", [2, 3, 4, 8])
+def test_wire_f32_is_the_plain_ring(n):
+    bufs = I.host_rank_buffers(n, 8 * n * 9 + 3, "bf16", std=0.02, seed0=n)
+    a = O.ring_all_reduce_wire(bufs, "bf16", "avg", "f32")
+    b, _ = O.ring_all_reduce(bufs, "bf16", "avg")
+    for x, y in zip(a, b):
+        assert x.tobytes() == y.tobytes()
+
+
+@pytest.mark.parametrize("n", [2, 4, 8])
+def test_wire_bf16_exact_when_partials_are_representable(n):
+    """Integers with every partial sum below 2^8 in magnitude are exact in
+    bf16, so rounding the messages changes nothing."""
+    rng = np.random.default_rng(n)
+    ints = [rng.integers(-256 // n, 256 // n, size=8 * n * 5).astype(np.float32) for _ in range(n)]
+    bufs = [O.f32_to_bf16(x) for x in ints]
+    out = O.ring_all_reduce_wire(bufs, "bf16", "sum", "bf16", "f32")
+    exact = np.sum(np.stack(ints).astype(np.float64), axis=0)
+    for r in range(n):
+        assert np.array_equal(out[r].astype(np.float64), exact)
+
+
+@pytest.mark.parametrize("n", [3, 4, 8])
+def test_wire_bf16_rounds_each_hop(n):
+    """Against the hand-written hop sequence (torch's bf16 rounding, an
+    independent routine): p = x_{j+1}; p = bf16(p) + x_k for the next ranks;
+    and within the per-hop rounding bound of the exact sum."""
+    torch = pytest.importorskip("torch")
+    count = 8 * n * 4
+    bufs = I.host_rank_buffers(n, count, "f32", seed0=20 + n)
+    shards = O.ring_reduce_scatter_wire(bufs, "f32", "sum", "bf16")
+    L = count // n
+    rb = lambda x: torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).float().numpy()
+    u = 2.0 ** -8
+    for j in range(n):
+        seg = [b[j * L:(j + 1) * L] for b in bufs]
+        p = seg[(j + 1) % n].copy()
+        bound = np.zeros(L)
+        for k in range(2, n + 1):
+            bound += u * np.abs(p.astype(np.float64))
+            p = (rb(p) + seg[(j + k) % n]).astype(np.float32)
+        assert shards[j].tobytes() == p.tobytes(), j
+        exact = np.sum(np.stack(seg).astype(np.float64), axis=0)
+        err = np.abs(shards[j].astype(np.float64) - exact)
+        assert np.all(err <= bound * 1.01 + n * 2.0 ** -23 * np.abs(np.stack(seg)).sum(0))
+
+
+# ---- HSDP (shard groups x replicas) ------------------------------------------------
+
+@pytest.mark.parametrize("S", [1, 2, 4])
+def test_hsdp_one_replica_is_reduce_scatter(S):
+    bufs = I.host_rank_buffers(S, 8 * S * 7 + 1, "bf16", std=0.02, seed0=S)
+    h = O.hsdp_reduce_scatter(bufs, 1, S, "bf16", "avg", "f32")
+    rs, _ = O.ring_reduce_scatter(bufs, "bf16", "avg", "f32")
+    for a, b in zip(h, rs):
+        assert a.tobytes() == b.tobytes()
+
+
+@pytest.mark.parametrize("R", [2, 3, 4])
+def test_hsdp_one_rank_per_group_is_all_reduce(R):
+    bufs = I.host_rank_buffers(R, 8 * R * 7 + 3, "f32", seed0=R)
+    h = O.hsdp_reduce_scatter(bufs, R, 1, "f32", "sum")
+    ar, _ = O.ring_all_reduce(bufs, "f32", "sum")
+    for g in range(R):
+        assert h[g].tobytes() == ar[g].tobytes()
+
+
+@pytest.mark.parametrize("R,S", [(2, 2), (2, 4), (4, 2), (3, 3)])
+def test_hsdp_integer_sum_is_exact_and_replicated(R, S):
+    n = R * S
+    count = 4 * n + 3
+    ints = I.integer_valued_f32(n, count, seed=R * 10 + S)
+    h = O.hsdp_reduce_scatter(ints, R, S, "f32", "sum")
+    exact = np.sum(np.stack(ints).astype(np.float64), axis=0)
+    for g in range(R):
+        full = np.concatenate(h[g * S:(g + 1) * S])
+        assert np.array_equal(full.astype(np.float64), exact)
+    # AVG divides the whole sum by N once
+    ha = O.hsdp_reduce_scatter(ints, R, S, "f32", "avg")
+    for g in range(R):
+        full = np.concatenate(ha[g * S:(g + 1) * S])
+        assert np.array_equal(full, (exact.astype(np.float32) / np.float32(n)).astype(np.float32))
