@@ -265,6 +265,56 @@ class AllReduce(Workload):
         cr.cr_all_reduce(self.t_bufs, self.count, self.dt, self.op, self.t_bufs, self.dt, stream)
 
 
+class AllReduceWire(Workload):
+    """The headline all-reduce with its ring messages carried in bf16: each
+    forwarded partial rounded before the next rank's fp32 addition."""
+
+    def __init__(self, n=8, count=1 << 25):
+        self.n, self.count = n, count
+        self.nbytes = ar_bytes(n, count, 2)
+        mib = count * 2 >> 20
+        self.name = f"allreduce_avg_bf16_bf16wire_{n}ranks_{mib}MiB"
+        self.kernel = f"k_fold_vec<bf16,bf16,AR,{n},wire>"
+        self.profile = f"k_fold_vec_allreduce_bf16wire_{n}x{mib}MiB"
+
+    def setup(self, device):
+        import torch
+        self.t_bufs = alloc_ranks(self.n, self.count, torch.bfloat16, 0.02, 0, device)
+
+    def step(self, stream):
+        from fsdp_emulated_ranks_gb300 import cr
+        cr.cr_all_reduce_wire(self.t_bufs, self.count, "bf16", "avg", "bf16", self.t_bufs, "bf16",
+                              stream)
+
+
+class Hsdp(Workload):
+    """HSDP gradient reduction on an R x S mesh: reduce-scatter inside each
+    group of S ranks and all-reduce of every shard across the R groups, one
+    pass; reads N*count and writes R*count bf16 elements."""
+
+    def __init__(self, R=2, S=4, count=1 << 25):
+        self.R, self.S, self.count = R, S, count
+        n = R * S
+        self.nbytes = n * count * 2 + R * count * 2
+        mib = count * 2 >> 20
+        self.name = f"hsdp_reduce_scatter_avg_bf16_{R}x{S}mesh_{mib}MiB"
+        self.kernel = f"k_hsdp_vec<bf16,bf16,{R},{S},8>"
+        self.profile = f"k_hsdp_vec_hsdp_bf16_{R}x{S}x{mib}MiB"
+
+    def setup(self, device):
+        import torch
+        self.t_bufs = alloc_ranks(self.R * self.S, self.count, torch.bfloat16, 0.02, 0, device)
+        L = -(-self.count // self.S)
+        self.t_shards = [torch.empty(min(L, self.count - j * L), dtype=torch.bfloat16,
+                                     device=device)
+                         for _ in range(self.R) for j in range(self.S)]
+
+    def step(self, stream):
+        from fsdp_emulated_ranks_gb300 import cr
+        cr.cr_hsdp_reduce_scatter(self.t_bufs, self.R, self.S, self.count, "bf16", "avg",
+                                  self.t_shards, "bf16", stream)
+
+
 class ReduceScatter(Workload):
     def __init__(self, n=8, count=1 << 25):
         self.n, self.count = n, count
@@ -518,6 +568,10 @@ def make_workload(name, args):
         return AllReduce()
     if name == "allreduce_f32":
         return AllReduce(n=4, count=1 << 20, dtype="f32", op="sum", std=1.0)
+    if name == "allreduce_wire":
+        return AllReduceWire()
+    if name == "hsdp":
+        return Hsdp()
     if name == "reduce_scatter":
         return ReduceScatter()
     if name == "all_gather":
@@ -539,7 +593,7 @@ def make_workload(name, args):
 
 ROW_WORKLOADS = ["reduce_scatter", "all_gather", "allreduce_f32", "bucket_pack",
                  "bucket_allreduce", "bucket_unpack", "bucket_pipeline", "bucket_fused", "fsdp", "fsdp_clipped", "fsdp2", "accumulate",
-                 "accumulate_allreduce"]
+                 "accumulate_allreduce", "allreduce_wire", "hsdp"]
 
 
 def run_headline(args, world, rank, device, stream, peak):
@@ -756,8 +810,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--workload", default="allreduce",
-                    help="timed workload: allreduce (headline), allreduce_f32, reduce_scatter, "
-                         "all_gather, bucket_{pack,allreduce,unpack,pipeline}, fsdp")
+                    help="timed workload: allreduce (headline), allreduce_f32, allreduce_wire, "
+                         "reduce_scatter, all_gather, hsdp, "
+                         "bucket_{pack,allreduce,unpack,pipeline,fused}, fsdp, fsdp_clipped, "
+                         "fsdp2, accumulate, accumulate_allreduce")
     ap.add_argument("--fsdp-count", type=int, default=1_300_000_000)
     ap.add_argument("--bucket-ntensors", type=int, default=300)
     ap.add_argument("--no-rows", action="store_true")

@@ -35,7 +35,9 @@ EXPORTS = ["cr_status_string", "cr_last_error", "cr_version", "cr_chunk_len",
            "cr_bucket_all_reduce_fused", "cr_fsdp_step",
            "cr_fsdp_clip_workspace_bytes", "cr_fsdp_step_clipped",
            "cr_fsdp_step_clipped_noalloc", "cr_fsdp2_step", "cr_accumulate",
-           "cr_all_reduce_accumulate", "cr_adamw_step", "cr_comm_elems"]
+           "cr_all_reduce_accumulate", "cr_adamw_step", "cr_comm_elems",
+           "cr_reduce_scatter_wire", "cr_all_reduce_wire",
+           "cr_hsdp_reduce_scatter"]
 
 _lib = None
 
@@ -87,6 +89,9 @@ def lib() -> C.CDLL:
     L.cr_reduce_scatter.argtypes = [vp, i, sz, i, i, vp, i, vp]
     L.cr_all_gather.argtypes = [vp, i, sz, i, vp, vp]
     L.cr_all_reduce.argtypes = [vp, i, sz, i, i, vp, i, vp]
+    L.cr_reduce_scatter_wire.argtypes = [vp, i, sz, i, i, i, vp, i, vp]
+    L.cr_all_reduce_wire.argtypes = [vp, i, sz, i, i, i, vp, i, vp]
+    L.cr_hsdp_reduce_scatter.argtypes = [vp, i, i, sz, i, i, vp, i, vp]
     L.cr_all_reduce_host.argtypes = [vp, vp, vp, i, sz, i, i, vp]
     L.cr_all_reduce_staged.argtypes = [vp, vp, vp, i, sz, i, i, sz, vp, vp, vp]
     L.cr_bucket_plan.argtypes = [vp, i, sz, sz, C.POINTER(C.POINTER(BucketPlanT))]
@@ -198,6 +203,30 @@ def cr_all_reduce(inbufs, count, in_dtype, op, outbufs, out_dtype,
                                _dtype(in_dtype), _op(op), _ptr_array(outbufs),
                                _dtype(out_dtype), _stream(stream)),
            "cr_all_reduce")
+
+
+def cr_reduce_scatter_wire(bufs, count, in_dtype, op, wire_dtype, out_shards, out_dtype,
+                           stream=None) -> None:
+    _check(lib().cr_reduce_scatter_wire(_ptr_array(bufs), len(bufs), count,
+                                        _dtype(in_dtype), _op(op), _dtype(wire_dtype),
+                                        _ptr_array(out_shards), _dtype(out_dtype),
+                                        _stream(stream)), "cr_reduce_scatter_wire")
+
+
+def cr_all_reduce_wire(inbufs, count, in_dtype, op, wire_dtype, outbufs, out_dtype,
+                       stream=None) -> None:
+    _check(lib().cr_all_reduce_wire(_ptr_array(inbufs), len(inbufs), count,
+                                    _dtype(in_dtype), _op(op), _dtype(wire_dtype),
+                                    _ptr_array(outbufs), _dtype(out_dtype),
+                                    _stream(stream)), "cr_all_reduce_wire")
+
+
+def cr_hsdp_reduce_scatter(bufs, R, S, count, in_dtype, op, out_shards, out_dtype,
+                           stream=None) -> None:
+    """bufs[g*S + s]: rank (g, s)'s buffer; out_shards[g*S + j]: shard j of group g."""
+    _check(lib().cr_hsdp_reduce_scatter(_ptr_array(bufs), R, S, count, _dtype(in_dtype),
+                                        _op(op), _ptr_array(out_shards), _dtype(out_dtype),
+                                        _stream(stream)), "cr_hsdp_reduce_scatter")
 
 
 def cr_all_reduce_host(host_in, host_out, count, dtype, op, dev_out=None, stream=None) -> None:

@@ -179,9 +179,23 @@ cr_status check_adam_cfg(const cr_adamw_cfg* cfg) {
   return CR_OK;
 }
 
+// The wire type of a ring whose messages may travel in low precision.
+cr_status check_wire(cr_dtype in, cr_dtype wire, bool* bf16) {
+  if (wire == CR_F32) {
+    *bf16 = false;
+    return CR_OK;
+  }
+  if (wire == CR_BF16) {
+    if (!is_float(in)) return fail(CR_ERR_UNSUPPORTED, "a bf16 wire needs a floating-point dtype");
+    *bf16 = true;
+    return CR_OK;
+  }
+  return fail(CR_ERR_INVALID_ARG, "wire dtype %d is neither CR_F32 nor CR_BF16", (int)wire);
+}
+
 cr_status all_reduce_impl(const void* const* in, int nranks, size_t count,
                           cr_dtype in_dtype, cr_op op, void* const* out,
-                          cr_dtype out_dtype, cudaStream_t stream) {
+                          cr_dtype out_dtype, cudaStream_t stream, bool wire_bf16 = false) {
   cr_status st = check_common(nranks, count, in, out);
   if (st) return st;
   if ((st = check_pair(in_dtype, op, out_dtype))) return st;
@@ -219,6 +233,7 @@ cr_status all_reduce_impl(const void* const* in, int nranks, size_t count,
   a.n_out = nranks;
   a.avg = op == CR_AVG;
   a.inv_n = exact_inv_n(nranks);
+  a.wire_bf16 = wire_bf16 ? 1 : 0;
   cudaError_t e = launch_fold(in_dtype, out_dtype, kAR, a, vw.get(), stream);
   if (e != cudaSuccess) return cuda_fail(e, "all_reduce launch");
   return ok();
@@ -262,9 +277,13 @@ cr_status cr_shard_range(size_t count, int nranks, int j, size_t* lo, size_t* hi
   return ok();
 }
 
-cr_status cr_reduce_scatter(const void* const* bufs, int nranks, size_t count,
-                            cr_dtype in_dtype, cr_op op, void* const* out_shards,
-                            cr_dtype out_dtype, cr_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+cr_status reduce_scatter_impl(const void* const* bufs, int nranks, size_t count,
+                              cr_dtype in_dtype, cr_op op, void* const* out_shards,
+                              cr_dtype out_dtype, cudaStream_t stream, bool wire_bf16) {
   cr_status st = check_common(nranks, count, bufs, out_shards);
   if (st) return st;
   if ((st = check_pair(in_dtype, op, out_dtype))) return st;
@@ -309,8 +328,90 @@ cr_status cr_reduce_scatter(const void* const* bufs, int nranks, size_t count,
   a.n_out = nranks;
   a.avg = op == CR_AVG;
   a.inv_n = exact_inv_n(nranks);
-  cudaError_t e = launch_fold(in_dtype, out_dtype, kRS, a, vw.get(), (cudaStream_t)stream);
+  a.wire_bf16 = wire_bf16 ? 1 : 0;
+  cudaError_t e = launch_fold(in_dtype, out_dtype, kRS, a, vw.get(), stream);
   if (e != cudaSuccess) return cuda_fail(e, "reduce_scatter launch");
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+cr_status cr_reduce_scatter(const void* const* bufs, int nranks, size_t count,
+                            cr_dtype in_dtype, cr_op op, void* const* out_shards,
+                            cr_dtype out_dtype, cr_stream_t stream) {
+  return reduce_scatter_impl(bufs, nranks, count, in_dtype, op, out_shards, out_dtype,
+                             (cudaStream_t)stream, false);
+}
+
+cr_status cr_reduce_scatter_wire(const void* const* bufs, int nranks, size_t count,
+                                 cr_dtype in_dtype, cr_op op, cr_dtype wire_dtype,
+                                 void* const* out_shards, cr_dtype out_dtype,
+                                 cr_stream_t stream) {
+  bool bf16 = false;
+  cr_status st = check_wire(in_dtype, wire_dtype, &bf16);
+  if (st) return st;
+  return reduce_scatter_impl(bufs, nranks, count, in_dtype, op, out_shards, out_dtype,
+                             (cudaStream_t)stream, bf16);
+}
+
+cr_status cr_hsdp_reduce_scatter(const void* const* bufs, int R, int S, size_t count,
+                                 cr_dtype in_dtype, cr_op op, void* const* out_shards,
+                                 cr_dtype out_dtype, cr_stream_t stream) {
+  if (R < 1 || S < 1 || R > CR_MAX_RANKS || S > CR_MAX_RANKS || R * S > CR_MAX_RANKS)
+    return fail(CR_ERR_INVALID_ARG, "mesh %d x %d outside [1, %d] ranks", R, S, CR_MAX_RANKS);
+  const int n = R * S;
+  cr_status st = check_common(n, count, bufs, out_shards);
+  if (st) return st;
+  if ((st = check_pair(in_dtype, op, out_dtype))) return st;
+  const size_t is = esize_of(in_dtype), os = esize_of(out_dtype);
+  const uint64_t L = cr_chunk_len(count, S);
+  std::vector<Span> spans;
+  Width vw;
+  vw.bytes(L * is);
+  vw.bytes(L * os);
+  for (int r = 0; r < n; ++r) {
+    const uint64_t len = chunk_size(count, L, r % S);
+    if ((st = check_buf(bufs[r], count, is, "bufs", r))) return st;
+    if ((st = check_buf(out_shards[r], len, os, "out_shards", r))) return st;
+    if (count) {
+      spans.push_back(span_of(bufs[r], count * is, 0, r));
+      vw.ptr(bufs[r]);
+    }
+    if (len) {
+      spans.push_back(span_of(out_shards[r], len * os, 1, r));
+      vw.ptr(out_shards[r]);
+    }
+  }
+  const bool same = in_dtype == out_dtype;
+  st = check_overlaps(spans, [&](const Span& i, const Span& o) {
+    // In place: shard j of group g is chunk j of rank (g, j)'s own buffer.
+    return same && i.rank == o.rank && o.a == i.a + L * (uint64_t)(o.rank % S) * is;
+  });
+  if (st) return st;
+  if (count == 0) return ok();
+  HsdpArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int r = 0; r < n; ++r) {
+    a.in[r] = bufs[r];
+    a.out[r] = out_shards[r];
+  }
+  a.count = count;
+  a.L = L;
+  a.jlast = (count - 1) / L;
+  const uint64_t len_last = count - a.jlast * L;
+  a.L2 = (L + R - 1) / R;
+  a.L2last = (len_last + R - 1) / R;
+  a.Ld = fastdiv_make(L, count - 1);
+  a.L2d = fastdiv_make(a.L2, L - 1);
+  a.L2lastd = fastdiv_make(a.L2last, len_last - 1);
+  a.R = R;
+  a.S = S;
+  a.avg = op == CR_AVG;
+  a.inv_n = exact_inv_n(n);
+  cudaError_t e = launch_hsdp(in_dtype, out_dtype, a, vw.get(), (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "hsdp_reduce_scatter launch");
   return ok();
 }
 
@@ -367,6 +468,16 @@ cr_status cr_all_reduce(const void* const* in, int nranks, size_t count,
                         cr_dtype out_dtype, cr_stream_t stream) {
   return all_reduce_impl(in, nranks, count, in_dtype, op, out, out_dtype,
                          (cudaStream_t)stream);
+}
+
+cr_status cr_all_reduce_wire(const void* const* in, int nranks, size_t count,
+                             cr_dtype in_dtype, cr_op op, cr_dtype wire_dtype,
+                             void* const* out, cr_dtype out_dtype, cr_stream_t stream) {
+  bool bf16 = false;
+  cr_status st = check_wire(in_dtype, wire_dtype, &bf16);
+  if (st) return st;
+  return all_reduce_impl(in, nranks, count, in_dtype, op, out, out_dtype,
+                         (cudaStream_t)stream, bf16);
 }
 
 // Device address of a host buffer the GPU can read and write directly

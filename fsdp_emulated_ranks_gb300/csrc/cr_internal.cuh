@@ -31,6 +31,7 @@ struct FoldArgs {
   int avg;         // 1: divide the finished sum by n
   float inv_n;     // 1/n when n is a power of two (exact), else 0
   uint32_t max_ctas;  // cap on the grid (0: one vector per thread)
+  int wire_bf16;      // 1: round every forwarded partial to bf16 (a bf16 wire)
 };
 
 struct GatherArgs {
@@ -165,6 +166,25 @@ enum FoldMode { kRS = 0, kAR = 1 };
 // Launchers (defined next to their kernels).  `vw` is the vector width in
 // bytes the host layer has checked the buffers allow: 32, 16, or 0 for the
 // element-wise kernels.
+// HSDP gradient reduction over an R x S mesh (rank (g, s) at g*S + s): the
+// ring reduce-scatter inside each group of S ranks, then the ring
+// all-reduce of every shard across the R groups.
+struct HsdpArgs {
+  const void* in[CR_MAX_RANKS];  // rank g*S + s's full buffer
+  void* out[CR_MAX_RANKS];       // shard j of group g at g*S + j
+  uint64_t count;
+  uint64_t L;       // shard length ceil(count / S)
+  uint64_t L2;      // outer chunk length of a full shard: ceil(L / R)
+  uint64_t L2last;  // outer chunk length of the last non-empty shard
+  uint64_t jlast;   // index of the last non-empty shard
+  FastDiv Ld, L2d, L2lastd;
+  int R, S;
+  int avg;
+  float inv_n;  // 1/(R*S) when exact, else 0 (divide)
+};
+
+cudaError_t launch_hsdp(cr_dtype in, cr_dtype out, const HsdpArgs& a, int vw,
+                        cudaStream_t s);
 cudaError_t launch_fold(cr_dtype in, cr_dtype out, FoldMode mode,
                         const FoldArgs& a, int vw, cudaStream_t s);
 cudaError_t launch_gather(size_t esize, const GatherArgs& a, int vw,

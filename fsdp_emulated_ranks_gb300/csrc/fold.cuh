@@ -176,10 +176,26 @@ __device__ __forceinline__ void acc_pack(const typename Elem<DI>::Acc* acc, uint
   }
 }
 
+// Low-precision wire: the partial sum a rank forwards is rounded to bf16
+// (nearest even) before the next rank adds its contribution in fp32.
+__device__ __forceinline__ float wire_round(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+template <int D, int NW, bool WIRE>
+__device__ __forceinline__ void wire_round_acc(typename Elem<D>::Acc* acc) {
+  if constexpr (WIRE && D != CR_I32) {
+    constexpr int VEC = elems_per<D, NW>();
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) acc[i] = wire_round(acc[i]);
+  }
+}
+
 // Ring-ordered fold of one NW-word vector at byte offset byte_off of chunk
 // j.  NT > 0: the rank count is a compile-time constant and all NT loads are
 // issued before the first add; NT == 0: runtime n, loads in groups of 8.
-template <int D, int NT, int NW>
+// WIRE: the partial is rounded to bf16 before every add (a bf16 wire).
+template <int D, int NT, int NW, bool WIRE = false>
 __device__ __forceinline__ void fold_vec(const void* const* in, int n, int j,
                                          uint64_t byte_off, typename Elem<D>::Acc* acc) {
   if constexpr (NT > 0) {
@@ -192,7 +208,10 @@ __device__ __forceinline__ void fold_vec(const void* const* in, int n, int j,
     }
     acc_init<D, NW>(acc, v[0]);
 #pragma unroll
-    for (int k = 1; k < NT; ++k) acc_add<D, NW>(acc, v[k]);
+    for (int k = 1; k < NT; ++k) {
+      wire_round_acc<D, NW, WIRE>(acc);
+      acc_add<D, NW>(acc, v[k]);
+    }
   } else {
     int r = (j + 1 == n) ? 0 : j + 1;
     for (int k0 = 0; k0 < n; k0 += 8) {
@@ -208,8 +227,12 @@ __device__ __forceinline__ void fold_vec(const void* const* in, int n, int j,
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         if (k < cnt) {
-          if (k0 == 0 && k == 0) acc_init<D, NW>(acc, v[0]);
-          else acc_add<D, NW>(acc, v[k]);
+          if (k0 == 0 && k == 0) {
+            acc_init<D, NW>(acc, v[0]);
+          } else {
+            wire_round_acc<D, NW, WIRE>(acc);
+            acc_add<D, NW>(acc, v[k]);
+          }
         }
       }
     }
@@ -258,14 +281,15 @@ __device__ __forceinline__ typename Elem<D>::Acc acc_plus(
   else return __fadd_rn(a, b);
 }
 
-// Ring-ordered fold of element e (chunk j) over n ranks.
-template <int D>
+// Ring-ordered fold of element e (chunk j) over n ranks (WIRE: a bf16 wire).
+template <int D, bool WIRE = false>
 __device__ __forceinline__ typename Elem<D>::Acc fold_elem(
     const void* const* in, int n, int j, uint64_t e) {
   int r = (j + 1 == n) ? 0 : j + 1;
   typename Elem<D>::Acc acc = ld_elem<D>(in[r], e);
   for (int k = 1; k < n; ++k) {
     r = (r + 1 == n) ? 0 : r + 1;
+    if constexpr (WIRE && D != CR_I32) acc = wire_round(acc);
     acc = acc_plus<D>(acc, ld_elem<D>(in[r], e));
   }
   return acc;

@@ -28,11 +28,11 @@
 namespace cr {
 
 // Fold, finish and store element e (any chunk, any alignment).
-template <int DI, int DO, int MODE>
+template <int DI, int DO, int MODE, bool WIRE>
 __device__ __forceinline__ void fold_store_elem(const FoldArgs& a, int n, uint64_t e) {
   using Acc = typename Elem<DI>::Acc;
   const int j = (int)(fastdiv_div(a.Ld, e));
-  Acc x = fold_elem<DI>(a.in, n, j, e);
+  Acc x = fold_elem<DI, WIRE>(a.in, n, j, e);
   if constexpr (DI != CR_I32) {
     if (a.avg) x = finish_avg(x, n, a.inv_n);
   }
@@ -46,7 +46,7 @@ __device__ __forceinline__ void fold_store_elem(const FoldArgs& a, int n, uint64
 // Elements [a.begin, a.end) of every rank buffer; chunks (and so the fold
 // order) are those of the whole buffer of a.count elements.  NW: 4 or 8
 // words per vector (16 or 32 bytes of input).
-template <int DI, int DO, int MODE, int NT, int NW>
+template <int DI, int DO, int MODE, int NT, int NW, bool WIRE>
 __global__ void __launch_bounds__(kBlock)
     k_fold_vec(const __grid_constant__ FoldArgs a) {
   using Acc = typename Elem<DI>::Acc;
@@ -67,11 +67,11 @@ __global__ void __launch_bounds__(kBlock)
     if (MODE == kAR && e0 + VEC > (j64 + 1) * a.L) {
       // The vector straddles a chunk boundary (L % VEC != 0): each element
       // takes its own chunk's ring order.
-      for (int i = 0; i < VEC; ++i) fold_store_elem<DI, DO, MODE>(a, n, e0 + i);
+      for (int i = 0; i < VEC; ++i) fold_store_elem<DI, DO, MODE, WIRE>(a, n, e0 + i);
       continue;
     }
     Acc acc[VEC];
-    fold_vec<DI, NT, NW>(a.in, n, j, e0 * IS, acc);
+    fold_vec<DI, NT, NW, WIRE>(a.in, n, j, e0 * IS, acc);
     if constexpr (DI != CR_I32) {
       if (a.avg) {
 #pragma unroll
@@ -94,20 +94,20 @@ __global__ void __launch_bounds__(kBlock)
   // last whole vector of the range.
   if (vbeg <= vend) {
     const uint64_t head = vbeg * VEC - a.begin, tail = a.end - vend * VEC;
-    if (tid < head) fold_store_elem<DI, DO, MODE>(a, n, a.begin + tid);
-    if (tid >= VEC && tid - VEC < tail) fold_store_elem<DI, DO, MODE>(a, n, vend * VEC + (tid - VEC));
+    if (tid < head) fold_store_elem<DI, DO, MODE, WIRE>(a, n, a.begin + tid);
+    if (tid >= VEC && tid - VEC < tail) fold_store_elem<DI, DO, MODE, WIRE>(a, n, vend * VEC + (tid - VEC));
   } else if (tid < a.end - a.begin) {
-    fold_store_elem<DI, DO, MODE>(a, n, a.begin + tid);
+    fold_store_elem<DI, DO, MODE, WIRE>(a, n, a.begin + tid);
   }
 }
 
-template <int DI, int DO, int MODE>
+template <int DI, int DO, int MODE, bool WIRE>
 __global__ void __launch_bounds__(kBlock)
     k_fold_elem(const __grid_constant__ FoldArgs a) {
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
   for (uint64_t e = a.begin + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; e < a.end;
        e += stride)
-    fold_store_elem<DI, DO, MODE>(a, a.n, e);
+    fold_store_elem<DI, DO, MODE, WIRE>(a, a.n, e);
 }
 
 // ---- all-gather ----------------------------------------------------------
@@ -183,32 +183,38 @@ static cudaError_t launch_fold_kernel(K kernel, const FoldArgs& a, uint64_t thre
   return cudaGetLastError();
 }
 
-template <int DI, int DO, int MODE, int NW>
+template <int DI, int DO, int MODE, int NW, bool WIRE>
 static cudaError_t fold_dispatch_nw(const FoldArgs& a, cudaStream_t s) {
   constexpr int VEC = elems_per<DI, NW>();
   const uint64_t threads = (a.end - a.begin) / VEC + 2 * VEC;
   switch (a.n) {
-    case 2: return launch_fold_kernel(k_fold_vec<DI, DO, MODE, 2, NW>, a, threads, s);
-    case 4: return launch_fold_kernel(k_fold_vec<DI, DO, MODE, 4, NW>, a, threads, s);
-    case 8: return launch_fold_kernel(k_fold_vec<DI, DO, MODE, 8, NW>, a, threads, s);
-    default: return launch_fold_kernel(k_fold_vec<DI, DO, MODE, 0, NW>, a, threads, s);
+    case 2: return launch_fold_kernel(k_fold_vec<DI, DO, MODE, 2, NW, WIRE>, a, threads, s);
+    case 4: return launch_fold_kernel(k_fold_vec<DI, DO, MODE, 4, NW, WIRE>, a, threads, s);
+    case 8: return launch_fold_kernel(k_fold_vec<DI, DO, MODE, 8, NW, WIRE>, a, threads, s);
+    default: return launch_fold_kernel(k_fold_vec<DI, DO, MODE, 0, NW, WIRE>, a, threads, s);
   }
 }
 
-template <int DI, int DO, int MODE>
+template <int DI, int DO, int MODE, bool WIRE>
 static cudaError_t fold_dispatch(const FoldArgs& a, int vw, cudaStream_t s) {
-  if (vw == 32) return fold_dispatch_nw<DI, DO, MODE, 8>(a, s);
-  if (vw == 16) return fold_dispatch_nw<DI, DO, MODE, 4>(a, s);
-  return launch_fold_kernel(k_fold_elem<DI, DO, MODE>, a, a.end - a.begin, s);
+  if (vw == 32) return fold_dispatch_nw<DI, DO, MODE, 8, WIRE>(a, s);
+  if (vw == 16) return fold_dispatch_nw<DI, DO, MODE, 4, WIRE>(a, s);
+  return launch_fold_kernel(k_fold_elem<DI, DO, MODE, WIRE>, a, a.end - a.begin, s);
 }
 
 template <int MODE>
 static cudaError_t fold_by_type(cr_dtype in, cr_dtype out, const FoldArgs& a,
                                 int vw, cudaStream_t s) {
-  if (in == CR_F32 && out == CR_F32) return fold_dispatch<CR_F32, CR_F32, MODE>(a, vw, s);
-  if (in == CR_BF16 && out == CR_BF16) return fold_dispatch<CR_BF16, CR_BF16, MODE>(a, vw, s);
-  if (in == CR_BF16 && out == CR_F32) return fold_dispatch<CR_BF16, CR_F32, MODE>(a, vw, s);
-  if (in == CR_I32 && out == CR_I32) return fold_dispatch<CR_I32, CR_I32, MODE>(a, vw, s);
+  if (a.wire_bf16) {
+    if (in == CR_F32 && out == CR_F32) return fold_dispatch<CR_F32, CR_F32, MODE, true>(a, vw, s);
+    if (in == CR_BF16 && out == CR_BF16) return fold_dispatch<CR_BF16, CR_BF16, MODE, true>(a, vw, s);
+    if (in == CR_BF16 && out == CR_F32) return fold_dispatch<CR_BF16, CR_F32, MODE, true>(a, vw, s);
+    return cudaErrorInvalidValue;
+  }
+  if (in == CR_F32 && out == CR_F32) return fold_dispatch<CR_F32, CR_F32, MODE, false>(a, vw, s);
+  if (in == CR_BF16 && out == CR_BF16) return fold_dispatch<CR_BF16, CR_BF16, MODE, false>(a, vw, s);
+  if (in == CR_BF16 && out == CR_F32) return fold_dispatch<CR_BF16, CR_F32, MODE, false>(a, vw, s);
+  if (in == CR_I32 && out == CR_I32) return fold_dispatch<CR_I32, CR_I32, MODE, false>(a, vw, s);
   return cudaErrorInvalidValue;
 }
 

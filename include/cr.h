@@ -182,6 +182,56 @@ cr_status cr_all_reduce_host(const void* const* host_in, void* const* host_out,
                              void* const* dev_out, int nranks, size_t count,
                              cr_dtype dtype, cr_op op, cr_stream_t stream);
 
+/* ---- low-precision wire ---------------------------------------------------
+ * [DT] section 11 (precision and distributed communication): a framework
+ * may move gradients in low precision while accumulating in fp32.  These
+ * are cr_reduce_scatter / cr_all_reduce with the ring's messages carried as
+ * wire_dtype: with CR_BF16 the partial sum a rank forwards to its neighbour
+ * is rounded to bf16 (nearest even) before the receiver adds its own
+ * contribution in fp32, so chunk j becomes
+ *     p = x_{j+1};  p = bf16(p) + x_{j+2};  ...;  y_j = bf16(p) + x_j
+ * (the owner's last addition is not rounded; CR_AVG and the output cast
+ * follow as usual).  The all-gather half of cr_all_reduce_wire moves the
+ * finished values in out_dtype, so every rank holds the same result.
+ * wire_dtype CR_F32 gives exactly cr_reduce_scatter / cr_all_reduce.
+ *   wire_dtype  CR_F32 or CR_BF16 (else CR_ERR_INVALID_ARG); CR_BF16 needs a
+ *               floating in_dtype (else CR_ERR_UNSUPPORTED)
+ * Every other argument, rule and error as for cr_reduce_scatter and
+ * cr_all_reduce. */
+cr_status cr_reduce_scatter_wire(const void* const* bufs, int nranks,
+                                 size_t count, cr_dtype in_dtype, cr_op op,
+                                 cr_dtype wire_dtype, void* const* out_shards,
+                                 cr_dtype out_dtype, cr_stream_t stream);
+cr_status cr_all_reduce_wire(const void* const* in, int nranks, size_t count,
+                             cr_dtype in_dtype, cr_op op, cr_dtype wire_dtype,
+                             void* const* out, cr_dtype out_dtype,
+                             cr_stream_t stream);
+
+/* ---- HSDP: shard within a group, replicate across groups -----------------
+ * [AIG] 6.3.6 (hybrid sharding: shard inside a node, replicate across
+ * nodes) and [DT] section 4, FSDP2 (a 2-D mesh, one dimension sharded and the
+ * other replicated).  N = R*S ranks on an R x S mesh; rank (g, s) is index
+ * g*S + s.  The gradient is reduce-scattered in ring order over the S ranks
+ * of each group (shard j = chunk j with L = ceil(count/S)), then each
+ * shard is all-reduced in ring order over the R groups (shard j's len_j
+ * elements in R chunks of ceil(len_j/R), chunk i summed from group i+1 to
+ * group i), all in fp32 partials (int32 wraps); CR_AVG divides by N once.
+ *   bufs[g*S + s]        rank (g, s)'s input, `count` elements of in_dtype
+ *   out_shards[g*S + j]  shard j as group g holds it (every group receives
+ *                        the same values), cr_shard_range(count, S, j)
+ *                        length of out_dtype (NULL if empty)
+ * R, S >= 1 and R*S <= CR_MAX_RANKS (else CR_ERR_INVALID_ARG).  Supported
+ * pairs as for cr_reduce_scatter.  In place is allowed when in_dtype ==
+ * out_dtype and out_shards[g*S + j] == (char*)bufs[g*S + j] + j*L*esize;
+ * any other overlap is CR_ERR_INVALID_ARG.  R == 1 is cr_reduce_scatter
+ * over S ranks; S == 1 is cr_all_reduce over R ranks (outputs only).
+ * Vector path: pointers 16-byte aligned and L*esize(in), L*esize(out)
+ * multiples of 16. */
+cr_status cr_hsdp_reduce_scatter(const void* const* bufs, int R, int S,
+                                 size_t count, cr_dtype in_dtype, cr_op op,
+                                 void* const* out_shards, cr_dtype out_dtype,
+                                 cr_stream_t stream);
+
 /* ---- a6: DDP bucket plan (host) -------------------------------------------
  * [AIG] 6.2.4: gradients go into buckets (default 25 MB) in the order
  * backward produces them; [AIG] 6.2.6 Horovod Tensor Fusion; [NX] 5.1.

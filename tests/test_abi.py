@@ -258,3 +258,52 @@ def test_fsdp2_and_accumulate_validation(L):
     expect(3, cr.cr_all_reduce_accumulate, [a[0] + 2, a[1]], 16, gr, "f32", "avg", stream=0)
     expect(1, cr.cr_all_reduce_accumulate, a, 16, gr, "f32", 9, stream=0)
     cr.cr_accumulate(a, 0, gr, "bf16", stream=0)
+
+
+def test_wire_validation(L):
+    n = 4
+    bufs = [FAKE + r * (1 << 20) for r in range(n)]
+    outs = [FAKE + (1 << 30) + r * (1 << 20) for r in range(n)]
+    # the wire is f32 or bf16, and a bf16 wire needs floating inputs
+    expect(1, cr.cr_all_reduce_wire, bufs, 16, "f32", "sum", "i32", outs, "f32", stream=0)
+    expect(1, cr.cr_reduce_scatter_wire, bufs, 16, "f32", "sum", 7, outs, "f32", stream=0)
+    expect(2, cr.cr_all_reduce_wire, bufs, 16, "i32", "sum", "bf16", outs, "i32", stream=0)
+    expect(2, cr.cr_reduce_scatter_wire, bufs, 16, "i32", "sum", "bf16", outs, "i32", stream=0)
+    # everything else is checked as for the f32-wire collectives
+    expect(2, cr.cr_all_reduce_wire, bufs, 16, "f32", "sum", "bf16", outs, "bf16", stream=0)
+    expect(3, cr.cr_reduce_scatter_wire, [bufs[0] + 1] + bufs[1:], 16, "bf16", "sum", "bf16",
+           outs, "bf16", stream=0)
+    expect(1, cr.cr_all_reduce_wire, bufs, 16, "f32", "sum", "bf16", [bufs[1]] + outs[1:], "f32",
+           stream=0)
+    cr.cr_all_reduce_wire(bufs, 0, "f32", "sum", "bf16", outs, "f32", stream=0)
+    cr.cr_reduce_scatter_wire(bufs, 0, "bf16", "avg", "bf16", [0] * n, "bf16", stream=0)
+
+
+def test_hsdp_validation(L):
+    R, S = 2, 3
+    n = R * S
+    bufs = [FAKE + r * (1 << 20) for r in range(n)]
+    outs = [FAKE + (1 << 30) + r * (1 << 20) for r in range(n)]
+    expect(1, cr.cr_hsdp_reduce_scatter, bufs, 0, S, 16, "f32", "sum", outs, "f32", stream=0)
+    expect(1, cr.cr_hsdp_reduce_scatter, bufs, R, 0, 16, "f32", "sum", outs, "f32", stream=0)
+    expect(1, cr.cr_hsdp_reduce_scatter, bufs * 11, 9, 8, 16, "f32", "sum", outs * 11, "f32",
+           stream=0)
+    expect(2, cr.cr_hsdp_reduce_scatter, bufs, R, S, 16, "i32", "avg", outs, "i32", stream=0)
+    expect(2, cr.cr_hsdp_reduce_scatter, bufs, R, S, 16, "f32", "sum", outs, "bf16", stream=0)
+    expect(3, cr.cr_hsdp_reduce_scatter, [bufs[0] + 2] + bufs[1:], R, S, 16, "f32", "sum", outs,
+           "f32", stream=0)
+    expect(1, cr.cr_hsdp_reduce_scatter, bufs[:5] + [0], R, S, 16, "f32", "sum", outs, "f32",
+           stream=0)
+    # shard 0 of group 1 inside rank (0, 0)'s input
+    bad = list(outs)
+    bad[S] = bufs[0] + 4
+    expect(1, cr.cr_hsdp_reduce_scatter, bufs, R, S, 16, "f32", "sum", bad, "f32", stream=0)
+    # two groups' copies of shard 1 overlapping
+    bad = list(outs)
+    bad[S + 1] = outs[1] + 4
+    expect(1, cr.cr_hsdp_reduce_scatter, bufs, R, S, 16, "f32", "sum", bad, "f32", stream=0)
+    # in place needs equal dtypes
+    L_ = cr.cr_chunk_len(48, S)
+    inpl = [bufs[g * S + j] + j * L_ * 2 for g in range(R) for j in range(S)]
+    expect(1, cr.cr_hsdp_reduce_scatter, bufs, R, S, 48, "bf16", "sum", inpl, "f32", stream=0)
+    cr.cr_hsdp_reduce_scatter(bufs, R, S, 0, "f32", "sum", [0] * n, "f32", stream=0)
