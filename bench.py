@@ -294,7 +294,7 @@ class Hsdp(Workload):
 
     def __init__(self, R=2, S=4, count=1 << 25):
         self.R, self.S, self.count = R, S, count
-        n = R * S
+        self.n = n = R * S
         self.nbytes = n * count * 2 + R * count * 2
         mib = count * 2 >> 20
         self.name = f"hsdp_reduce_scatter_avg_bf16_{R}x{S}mesh_{mib}MiB"
@@ -428,9 +428,9 @@ class FsdpStep(Workload):
         self.nbytes = ((6 if clip else 4) * n + 24) * count
         tag = f"{count / 1e9:g}e9" if count >= 10 ** 8 else str(count)
         self.name = f"fsdp_step{'_clipped' if clip else ''}_bf16_{n}ranks_{tag}params"
-        self.kernel = f"k_fsdp_vec<{n}>" + (" + k_fsdp_sumsq" if clip else "")
+        self.kernel = f"k_fsdp_vec<{n}>" + (" + k_fsdp_sumsq + k_clip_coef" if clip else "")
         self.profile = f"k_fsdp_vec_fsdp_step{'_clipped' if clip else ''}_{n}x{tag}"
-        self.launches = 2 if clip else 1
+        self.launches = 3 if clip else 1
 
     def setup(self, device):
         import torch
@@ -478,9 +478,9 @@ class Fsdp2Step(Workload):
     8 ranks; each rank's grads and params live in one 256-byte-aligned slab
     per rank, the shards' fp32 state in one slab per parameter set."""
 
-    def __init__(self, n=8):
+    def __init__(self, n=8, layers=24, hidden=2048):
         self.n = n
-        self.shapes = transformer_shapes()
+        self.shapes = transformer_shapes(hidden=hidden, layers=layers, ffn=4 * hidden)
         self.P = sum(d * r for d, r in self.shapes)
         self.nbytes = (4 * n + 24) * self.P
         self.name = f"fsdp2_step_bf16_{n}ranks_{len(self.shapes)}params_{self.P / 1e9:.2f}e9"
@@ -583,7 +583,7 @@ def make_workload(name, args):
     if name == "fsdp_clipped":
         return FsdpStep(count=args.fsdp_count, clip=True)
     if name == "fsdp2":
-        return Fsdp2Step()
+        return Fsdp2Step(layers=args.fsdp2_layers, hidden=args.fsdp2_hidden)
     if name == "accumulate":
         return Accumulate(reduce=False)
     if name == "accumulate_allreduce":
@@ -668,22 +668,24 @@ def run_e2e(args, bufs, n, count, world, stream, device):
 
 def traffic_per_launch(name, launches=1):
     """DRAM bytes per launch from the committed ncu summary of this kernel,
-    or None if absent or taken on a different build of the library."""
+    or None if absent or taken on a different build of its kernel code (the
+    summary names the translation unit and its kernel_hash)."""
     p = os.path.join(ROOT, "profiles", name + ".md")
     if not os.path.exists(p) or launches != 1:
         return None
     vals = {}
     with open(p) as f:
         for line in f:
-            if ":" in line and line.strip().startswith(("dram_bytes_per_launch", "libcr_source_hash")):
+            if ":" in line and line.strip().startswith(
+                    ("dram_bytes_per_launch", "kernel_tu", "kernel_source_hash")):
                 k, v = line.split(":", 1)
                 vals[k.strip(" -*`")] = v.strip(" `\n")
     try:
         from fsdp_emulated_ranks_gb300 import build as B
-        if vals.get("libcr_source_hash") != B.source_hash():
+        if vals.get("kernel_source_hash") != B.kernel_hash(vals["kernel_tu"]):
             return None
         return int(vals["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
+    except (KeyError, ValueError, OSError):
         return None
 
 
@@ -702,7 +704,8 @@ def run_rows(args, device, stream, peak, skip=None):
         gbs = wl.nbytes / (ms * 1e-3) / 1e9
         rows.append({"name": wl.name, "ms": round(ms, 4), "GB/s": round(gbs, 1),
                      "frac": round(gbs / peak[0], 4), "algorithmic_bytes": wl.nbytes,
-                     "launches_per_call": wl.launches, "kernel": wl.kernel})
+                     "launches_per_call": wl.launches, "kernel": wl.kernel,
+                     "traffic": traffic_per_launch(wl.profile, wl.launches)})
         wl.teardown()
     return rows
 
@@ -816,6 +819,9 @@ def main(argv=None):
                          "fsdp2, accumulate, accumulate_allreduce")
     ap.add_argument("--fsdp-count", type=int, default=1_300_000_000)
     ap.add_argument("--bucket-ntensors", type=int, default=300)
+    ap.add_argument("--fsdp2-layers", type=int, default=24,
+                    help="transformer layers of the fsdp2 workload (1.27e9 parameters at 24)")
+    ap.add_argument("--fsdp2-hidden", type=int, default=2048)
     ap.add_argument("--no-rows", action="store_true")
     ap.add_argument("--skip-fsdp", action="store_true")
     ap.add_argument("--row-steps", type=int, default=20)

@@ -54,6 +54,21 @@ def source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def kernel_hash(tu: str) -> str:
+    """Hash of what the kernels of one translation unit are compiled from:
+    that file, every shared header of the library and the compiler flags.
+    A profile of a kernel stays valid while this hash is unchanged."""
+    h = hashlib.sha256()
+    h.update(" ".join(ARCH + NVCC_FLAGS).encode())
+    heads = sorted(f for f in os.listdir(CSRC) if f.endswith((".cuh", ".h")))
+    for f in [os.path.join(CSRC, tu)] + [os.path.join(CSRC, x) for x in heads] + [
+            os.path.join(INCLUDE, "cr.h")]:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def _stamp() -> str:
     return os.path.join(BUILD_DIR, "libcr.hash")
 

@@ -739,7 +739,9 @@ cr_status cr_fsdp_step(const void* const* grads_bf16, int nranks, size_t count,
   return ok();
 }
 
-size_t cr_fsdp_clip_workspace_bytes(void) { return (size_t)kMaxNormParts * sizeof(double); }
+size_t cr_fsdp_clip_workspace_bytes(void) {
+  return (size_t)(kMaxNormParts + 1) * sizeof(double);
+}
 
 cr_status cr_fsdp_step_clipped(const void* const* grads_bf16, int nranks, size_t count,
                                float* const* master, float* const* m, float* const* v,
@@ -756,13 +758,14 @@ cr_status cr_fsdp_step_clipped(const void* const* grads_bf16, int nranks, size_t
     return fail(CR_ERR_INVALID_ARG, "max_norm must be finite and > 0");
   if (!workspace) return fail(CR_ERR_INVALID_ARG, "workspace is NULL");
   if (!aligned(workspace, 8)) return fail(CR_ERR_ALIGNMENT, "workspace not 8-byte aligned");
-  if (workspace_bytes < sizeof(double))
+  if (workspace_bytes < 2 * sizeof(double))
     return fail(CR_ERR_INVALID_ARG, "workspace_bytes=%zu too small", workspace_bytes);
   if (norm_out && !aligned(norm_out, 4)) return fail(CR_ERR_ALIGNMENT, "norm_out not aligned");
-  const size_t max_parts = workspace_bytes / sizeof(double) < (size_t)kMaxNormParts
-                               ? workspace_bytes / sizeof(double)
+  // Slot 0: the clip coefficient; slots 1..max_parts: the partial sums.
+  const size_t max_parts = workspace_bytes / sizeof(double) - 1 < (size_t)kMaxNormParts
+                               ? workspace_bytes / sizeof(double) - 1
                                : (size_t)kMaxNormParts;
-  spans.push_back(span_of(workspace, max_parts * sizeof(double), 1, 1000));
+  spans.push_back(span_of(workspace, (max_parts + 1) * sizeof(double), 1, 1000));
   if (norm_out) spans.push_back(span_of(norm_out, sizeof(float), 1, 1001));
   if ((st = check_overlaps(spans, [](const Span&, const Span&) { return false; }))) return st;
   if (count == 0) {
@@ -772,15 +775,15 @@ cr_status cr_fsdp_step_clipped(const void* const* grads_bf16, int nranks, size_t
     }
     return ok();
   }
-  double* partials = static_cast<double*>(workspace);
+  float* coef = static_cast<float*>(workspace);
+  double* partials = static_cast<double*>(workspace) + 1;
   int nparts = 0;
   cudaError_t e = launch_fsdp_sumsq(a, vw != 0, partials, (int)max_parts, &nparts,
                                     (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "fsdp_step_clipped sum-of-squares launch");
-  a.partials = partials;
-  a.nparts = nparts;
-  a.max_norm = max_norm;
-  a.norm_out = norm_out;
+  e = launch_clip_coef(partials, nparts, max_norm, coef, norm_out, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "fsdp_step_clipped coefficient launch");
+  a.coef = coef;
   e = launch_fsdp(a, vw, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "fsdp_step_clipped launch");
   return ok();

@@ -61,17 +61,15 @@ struct FsdpArgs {
   int n;
   float inv_n;
   AdamScalars a;
-  // Gradient-norm clipping (clip_grad_norm_): when partials is non-null the
-  // step first sums the nparts fp64 partial sums of squares, in index
-  // order, and scales every gradient by min(1, max_norm / (norm + 1e-6)).
-  const double* partials;
-  int nparts;
-  double max_norm;
-  float* norm_out;  // written by CTA 0 when non-null
+  // Gradient-norm clipping (clip_grad_norm_): when non-null, the device
+  // address of the coefficient min(1, max_norm / (norm + 1e-6)) by which
+  // every averaged gradient is scaled (written by k_clip_coef).
+  const float* coef;
 };
 
-// Upper bound on the per-CTA partial sums of the sum-of-squares pass.
-constexpr int kMaxNormParts = 4096;
+// Upper bound on the per-CTA partial sums of the sum-of-squares pass; the
+// clip workspace holds the coefficient in its first 8 bytes, then these.
+constexpr int kMaxNormParts = 4095;
 
 struct AdamArgs {
   float* master;
@@ -194,6 +192,10 @@ cudaError_t launch_fsdp(const FsdpArgs& a, int vw, cudaStream_t s);
 // fp64 partials to `partials`.
 cudaError_t launch_fsdp_sumsq(const FsdpArgs& a, bool vec, double* partials,
                               int max_parts, int* nparts, cudaStream_t s);
+// One warp: sums the nparts partials in a fixed order, writes the clip
+// coefficient to *coef and the norm to *norm_out (if non-null).
+cudaError_t launch_clip_coef(const double* partials, int nparts, double max_norm, float* coef,
+                             float* norm_out, cudaStream_t s);
 cudaError_t launch_adamw(const AdamArgs& a, bool vec, cudaStream_t s);
 cudaError_t launch_copy(const CopyArgs& a, uint32_t ntiles, cudaStream_t s);
 cudaError_t launch_bucket_fused(cr_dtype d, const FusedArgs& a, uint32_t ntiles,

@@ -15,8 +15,9 @@
 
 namespace {
 
-// One fp64 partial sum per CTA of the first pass: 4096 x 8 B = 32 KiB,
-// resident on every GPU that loads the library until the process exits.
+// The clip coefficient (first 8 bytes) and one fp64 partial sum per CTA of
+// the first pass: 4096 x 8 B = 32 KiB, resident on every GPU that loads the
+// library until the process exits.
 constexpr int kScratchParts = 4096;
 static __device__ __align__(256) double g_clip_scratch[kScratchParts];
 
@@ -61,10 +62,10 @@ extern "C" cr_status cr_fsdp_step_clipped_noalloc(
     cr::report_error(CR_ERR_CUDA, "fsdp_step_clipped_noalloc: SM count query failed");
     return CR_ERR_CUDA;
   }
-  if ((long long)sms * kMaxCtasPerSm > kScratchParts) {
+  if ((long long)sms * kMaxCtasPerSm > kScratchParts - 1) {
     cr::report_error(CR_ERR_UNSUPPORTED,
                      "fsdp_step_clipped_noalloc: this GPU's first pass may need more "
-                     "partial sums than the 4096 the static scratch holds");
+                     "partial sums than the 4095 the static scratch holds");
     return CR_ERR_UNSUPPORTED;
   }
   void* scratch = nullptr;

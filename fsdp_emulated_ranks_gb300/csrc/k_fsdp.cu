@@ -23,27 +23,32 @@
 
 namespace cr {
 
-// Clip coefficient of clip_grad_norm_, the same in every CTA: the partial
-// sums are added in a fixed order (lane-strided, then a fixed shuffle tree),
-// so the norm is reproducible run to run.  Returns 1 when not clipping.
-__device__ float clip_coef(const FsdpArgs& a) {
-  __shared__ float s_coef;
-  if (a.partials == nullptr) return 1.0f;
-  if (threadIdx.x < 32) {
-    double t = 0.0;
-    for (int i = threadIdx.x; i < a.nparts; i += 32) t += a.partials[i];
+// Clip coefficient of clip_grad_norm_, computed once per step by one warp:
+// the partial sums are added in a fixed order (lane-strided, then a fixed
+// shuffle tree), so the norm is reproducible run to run.
+__global__ void k_clip_coef(const double* partials, int nparts, double max_norm, float* coef,
+                            float* norm_out) {
+  double t = 0.0;
+  for (int i = threadIdx.x; i < nparts; i += 32) t += partials[i];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) t += __shfl_down_sync(0xffffffffu, t, off);
-    if (threadIdx.x == 0) {
-      const double norm = sqrt(t);
-      double c = a.max_norm / (norm + 1e-6);
-      if (c > 1.0) c = 1.0;
-      s_coef = (float)c;
-      if (blockIdx.x == 0 && a.norm_out) *a.norm_out = (float)norm;
-    }
+  for (int off = 16; off > 0; off >>= 1) t += __shfl_down_sync(0xffffffffu, t, off);
+  if (threadIdx.x == 0) {
+    const double norm = sqrt(t);
+    double c = max_norm / (norm + 1e-6);
+    if (c > 1.0) c = 1.0;
+    *coef = (float)c;
+    if (norm_out) *norm_out = (float)norm;
   }
-  __syncthreads();
-  return s_coef;
+}
+
+cudaError_t launch_clip_coef(const double* partials, int nparts, double max_norm, float* coef,
+                             float* norm_out, cudaStream_t s) {
+  k_clip_coef<<<1, 32, 0, s>>>(partials, nparts, max_norm, coef, norm_out);
+  return cudaGetLastError();
+}
+
+__device__ __forceinline__ float clip_coef(const FsdpArgs& a) {
+  return a.coef ? __ldg(a.coef) : 1.0f;
 }
 
 // Sum of squares of the averaged fp32 gradient, one fp64 partial per CTA

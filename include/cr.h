@@ -341,14 +341,15 @@ cr_status cr_fsdp_step(const void* const* grads_bf16, int nranks,
  * shards: the global norm), squares summed in fp32 batches of 8 and the
  * batches in fp64 (relative error ~1e-7); every gradient element is
  * multiplied (one fp32 multiply) by c = min(1, max_norm / (norm + 1e-6)),
- * formed in double and rounded to fp32, before AdamW.  Two launches: a
+ * formed in double and rounded to fp32, before AdamW.  Three launches: a
  * sum-of-squares pass over the grads that writes one fp64 partial per CTA
- * into `workspace`, then the fused step, whose every CTA adds the partials
- * in the same fixed order (the norm is reproducible run to run).
+ * into `workspace`, one warp that adds the partials in a fixed order (the
+ * norm is reproducible run to run) and stores c in the workspace's first 8
+ * bytes, then the fused step, which reads c.
  * Algorithmic bytes: (6N + 24) per parameter (the grads are read twice).
  *   max_norm        finite, > 0 (CR_ERR_INVALID_ARG otherwise)
  *   workspace       caller-owned device scratch, 8-byte aligned, of
- *                   workspace_bytes >= 8 bytes; cr_fsdp_clip_workspace_bytes()
+ *                   workspace_bytes >= 16 bytes; cr_fsdp_clip_workspace_bytes()
  *                   bytes are always enough (fewer bytes cap the number of
  *                   CTAs of the first pass).  Contents on entry are ignored.
  *   norm_out        device pointer (may be NULL) receiving the norm as fp32
@@ -369,11 +370,11 @@ cr_status cr_fsdp_step_clipped(const void* const* grads_bf16, int nranks,
  * where a cudaMalloc would synchronise the device -- and so have no
  * workspace to pass.  It runs exactly cr_fsdp_step_clipped (same arguments
  * minus workspace/workspace_bytes, same results and errors) with the
- * sum-of-squares partials kept in a static device array of 4096 doubles
- * (32 KiB) that the library holds on every GPU that loads it until the
- * process exits.  The first pass uses one partial per CTA and at most 8 CTAs
- * per SM, so any GPU with up to 512 SMs fits; on a larger one the call
- * returns CR_ERR_UNSUPPORTED.  The first call on each device looks up the
+ * workspace (coefficient and sum-of-squares partials) kept in a static
+ * device array of 4096 doubles (32 KiB) that the library holds on every GPU
+ * that loads it until the process exits.  The first pass uses one partial
+ * per CTA and at most 8 CTAs per SM, so any GPU with up to 511 SMs fits; on
+ * a larger one the call returns CR_ERR_UNSUPPORTED.  The first call on each device looks up the
  * array's device address (cudaGetSymbolAddress, with that device current)
  * and caches it; make that first call before any stream capture.  All calls
  * share the one array: nothing in it needs to start at zero (the first pass

@@ -208,12 +208,14 @@ def test_fsdp_step_clipped_validation(L):
     v = [FAKE + (4 << 28) + r * (1 << 20) for r in range(n)]
     ws = FAKE + (5 << 28)
     nb = cr.cr_fsdp_clip_workspace_bytes()
-    assert nb >= 8 and nb % 8 == 0
+    assert nb >= 16 and nb % 8 == 0
     expect(1, cr.cr_fsdp_step_clipped, g, count, ms, m, v, cr.adamw_cfg(), 0.0, ws, nb, p, stream=0)
     expect(1, cr.cr_fsdp_step_clipped, g, count, ms, m, v, cr.adamw_cfg(), float("inf"), ws, nb, p,
            stream=0)
     expect(1, cr.cr_fsdp_step_clipped, g, count, ms, m, v, cr.adamw_cfg(), 1.0, 0, nb, p, stream=0)
     expect(1, cr.cr_fsdp_step_clipped, g, count, ms, m, v, cr.adamw_cfg(), 1.0, ws, 4, p, stream=0)
+    # the coefficient slot alone leaves no room for a partial sum
+    expect(1, cr.cr_fsdp_step_clipped, g, count, ms, m, v, cr.adamw_cfg(), 1.0, ws, 8, p, stream=0)
     expect(3, cr.cr_fsdp_step_clipped, g, count, ms, m, v, cr.adamw_cfg(), 1.0, ws + 4, nb, p,
            stream=0)
     expect(1, cr.cr_fsdp_step_clipped, g, count, ms, m, v, cr.adamw_cfg(), 1.0, ms[0], nb, p,

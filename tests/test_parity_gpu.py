@@ -413,7 +413,8 @@ def test_fsdp_step_clipped(n, count_fn, clip, ws_parts):
     d_v = [to_dev(x, "f32") for x in v]
     d_g = [to_dev(x, "bf16") for x in grads]
     d_p = [Guarded(count, "bf16") for _ in range(n)]
-    ws_bytes = cr.cr_fsdp_clip_workspace_bytes() if ws_parts is None else 8 * ws_parts
+    # the coefficient's 8 bytes, then room for ws_parts partial sums
+    ws_bytes = cr.cr_fsdp_clip_workspace_bytes() if ws_parts is None else 8 * (ws_parts + 1)
     ws = torch.empty(ws_bytes // 8, dtype=torch.float64, device="cuda")
     norm_out = torch.full((1,), -1.0, dtype=torch.float32, device="cuda")
     want_p, want_norm = O.fsdp_step_clipped(grads, master, m, v, cfg, max_norm)
