@@ -710,6 +710,73 @@ def run_rows(args, device, stream, peak, skip=None):
     return rows
 
 
+# ---- DDP backward / all-reduce overlap ---------------------------------------------------
+
+def run_overlap(args, device, caps=(0, 38)):
+    """The reducer's overlap of bucket all-reduces with backward ("AI Infra
+    Guide, Chapter 6", 6.2.5): the 300-tensor bucket workload, 8 ranks; the
+    emulated backward runs, per bucket, k bf16 4096^3 GEMMs (cuBLAS through
+    torch: the stand-in for layer backward, not part of the library) on a
+    compute stream and then marks the bucket's tensors ready; the reducer
+    all-reduces each bucket on a comm stream with at most `cap` CTAs.  k is
+    chosen so that compute alone takes about as long as the all-reduces
+    alone, the case where overlap matters most.  hidden = (t_compute +
+    t_comm - t_both) / min(t_compute, t_comm)."""
+    import torch
+    from fsdp_emulated_ranks_gb300 import cr
+    wl = Buckets(mode="fused", ntensors=args.bucket_ntensors)
+    wl.setup(device)
+    plan, n, T = wl.plan, wl.n, wl.plan.ntensors
+    members = [[] for _ in range(plan.nbuckets)]
+    for t in range(T - 1, -1, -1):
+        members[plan.tensor_bucket[t]].append(t)
+    compute, comm = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    a = torch.randn(4096, 4096, device=device, dtype=torch.bfloat16)
+    b = torch.randn(4096, 4096, device=device, dtype=torch.bfloat16)
+    c = torch.empty(4096, 4096, device=device, dtype=torch.bfloat16)
+
+    def timed_on(stream, fn, reps):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    def backward(red, k):
+        with torch.cuda.stream(compute):
+            for bk in range(plan.nbuckets):
+                for _ in range(k):
+                    torch.mm(a, b, out=c)
+                if red is not None:
+                    for t in members[bk]:
+                        cr.cr_reducer_mark_ready(red, t, compute)
+            if red is not None:
+                cr.cr_reducer_finalize(red, compute)
+
+    t_gemm = timed_on(compute, lambda: torch.mm(a, b, out=c), 50)
+    out = {"workload": wl.name, "buckets": plan.nbuckets, "gemm": "bf16 4096x4096x4096",
+           "gemm_ms": round(t_gemm, 4), "caps": []}
+    for cap in caps:
+        red = cr.cr_reducer_create(plan, n, wl.t_flat_t, "bf16", "avg", cap, comm)
+        t_comm = timed_on(compute, lambda: backward(red, 0), 5)
+        k = max(1, round(t_comm / (plan.nbuckets * t_gemm)))
+        t_comp = timed_on(compute, lambda: backward(None, k), 5)
+        t_both = timed_on(compute, lambda: backward(red, k), 5)
+        cr.cr_reducer_destroy(red)
+        hidden = (t_comp + t_comm - t_both) / min(t_comp, t_comm)
+        out["caps"].append({"comm_ctas": cap, "gemms_per_bucket": k,
+                            "t_comm_ms": round(t_comm, 3), "t_compute_ms": round(t_comp, 3),
+                            "t_both_ms": round(t_both, 3), "hidden": round(hidden, 3),
+                            "comm_GBs_alone": round(wl.nbytes / (t_comm * 1e-3) / 1e9, 1)})
+    wl.teardown()
+    return out
+
+
 # ---- CPU oracle -------------------------------------------------------------------------
 
 def cpu_oracle_allreduce(sample, min_seconds):
@@ -870,8 +937,10 @@ def main(argv=None):
     head, sample = run_headline(args, world, rank, device, stream, peak)
     wl = head["workload"]
     rows = None
+    overlap = None
     if world == 1 and not args.no_rows:
         rows = run_rows(args, device, stream, peak, skip=args.workload)
+        overlap = run_overlap(args, device)
     cpu = None
     if sample is not None:
         gbs, secs, passes = cpu_oracle_allreduce(sample, args.cpu_seconds)
@@ -902,7 +971,7 @@ def main(argv=None):
                 "roofline": head["roofline"], "cpu_baseline": cpu, "e2e": head["e2e"],
                 "gpu_launches": head["gpu_launches"], "clocks": head["clocks"],
                 "frac_of_peak": round(head["value"] / world / peak[0], 4),
-                "rows": rows}
+                "rows": rows, "ddp_overlap": overlap}
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist

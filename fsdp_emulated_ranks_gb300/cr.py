@@ -37,7 +37,8 @@ EXPORTS = ["cr_status_string", "cr_last_error", "cr_version", "cr_chunk_len",
            "cr_fsdp_step_clipped_noalloc", "cr_fsdp2_step", "cr_accumulate",
            "cr_all_reduce_accumulate", "cr_adamw_step", "cr_comm_elems",
            "cr_reduce_scatter_wire", "cr_all_reduce_wire",
-           "cr_hsdp_reduce_scatter"]
+           "cr_hsdp_reduce_scatter", "cr_reducer_create", "cr_reducer_mark_ready",
+           "cr_reducer_launched", "cr_reducer_finalize", "cr_reducer_destroy"]
 
 _lib = None
 
@@ -78,6 +79,7 @@ def lib() -> C.CDLL:
             "`python -c 'import __graft_entry__ as g; g.build()'`")
     L = C.CDLL(LIB_PATH)
     vp, sz, i = C.c_void_p, C.c_size_t, C.c_int
+    L.cr_reducer_destroy.restype = None
     L.cr_status_string.restype = C.c_char_p
     L.cr_status_string.argtypes = [i]
     L.cr_last_error.restype = C.c_char_p
@@ -92,6 +94,13 @@ def lib() -> C.CDLL:
     L.cr_reduce_scatter_wire.argtypes = [vp, i, sz, i, i, i, vp, i, vp]
     L.cr_all_reduce_wire.argtypes = [vp, i, sz, i, i, i, vp, i, vp]
     L.cr_hsdp_reduce_scatter.argtypes = [vp, i, i, sz, i, i, vp, i, vp]
+    L.cr_reducer_create.argtypes = [C.POINTER(BucketPlanT), i, vp, i, i, i, vp,
+                                    C.POINTER(vp)]
+    L.cr_reducer_mark_ready.argtypes = [vp, i, vp]
+    L.cr_reducer_launched.argtypes = [vp]
+    L.cr_reducer_launched.restype = i
+    L.cr_reducer_finalize.argtypes = [vp, vp]
+    L.cr_reducer_destroy.argtypes = [vp]
     L.cr_all_reduce_host.argtypes = [vp, vp, vp, i, sz, i, i, vp]
     L.cr_all_reduce_staged.argtypes = [vp, vp, vp, i, sz, i, i, sz, vp, vp, vp]
     L.cr_bucket_plan.argtypes = [vp, i, sz, sz, C.POINTER(C.POINTER(BucketPlanT))]
@@ -306,6 +315,53 @@ def cr_bucket_all_reduce_fused(plan: BucketPlan, nranks: int, tensors, dtype, op
     _check(lib().cr_bucket_all_reduce_fused(plan.ptr, nranks, _ptr_array(tensors),
                                             _dtype(dtype), _op(op), _stream(stream)),
            "cr_bucket_all_reduce_fused")
+
+
+class Reducer:
+    """Owns a cr_reducer_t, the DDP reducer (bucket all-reduces started as
+    gradients become ready); released by cr_reducer_destroy or when
+    collected."""
+
+    def __init__(self, ptr: int):
+        self._ptr = ptr
+
+    @property
+    def ptr(self):
+        return self._ptr
+
+    def __del__(self):
+        if getattr(self, "_ptr", None) and _lib is not None:
+            _lib.cr_reducer_destroy(self._ptr)
+            self._ptr = None
+
+
+def cr_reducer_create(plan: BucketPlan, nranks: int, tensors, dtype, op, comm_ctas=0,
+                      comm_stream=None) -> Reducer:
+    """tensors[r*T + t]: rank r's tensor t."""
+    out = C.c_void_p()
+    _check(lib().cr_reducer_create(plan.ptr, nranks, _ptr_array(tensors), _dtype(dtype),
+                                   _op(op), comm_ctas, _stream(comm_stream), C.byref(out)),
+           "cr_reducer_create")
+    return Reducer(out.value)
+
+
+def cr_reducer_mark_ready(red: Reducer, tensor: int, compute_stream=None) -> None:
+    _check(lib().cr_reducer_mark_ready(red.ptr, tensor, _stream(compute_stream)),
+           "cr_reducer_mark_ready")
+
+
+def cr_reducer_launched(red: Reducer) -> int:
+    return lib().cr_reducer_launched(red.ptr)
+
+
+def cr_reducer_finalize(red: Reducer, compute_stream=None) -> None:
+    _check(lib().cr_reducer_finalize(red.ptr, _stream(compute_stream)), "cr_reducer_finalize")
+
+
+def cr_reducer_destroy(red: Reducer) -> None:
+    if red.ptr:
+        lib().cr_reducer_destroy(red.ptr)
+        red._ptr = None
 
 
 def adamw_cfg(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01,

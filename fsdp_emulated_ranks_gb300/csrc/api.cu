@@ -915,12 +915,13 @@ namespace {
 // One launch per kFusedMaxTensors items (fewer when N > 16).
 template <typename Item>
 cr_status fused_run(int nitems, int nranks, cr_dtype dtype, cr_op op, cudaStream_t stream,
-                    Item item) {
+                    Item item, uint32_t max_ctas = 0) {
   static thread_local FusedArgs args;  // ~24 KB: kept off the stack
   const int per_launch = std::min(kFusedMaxTensors, kFusedMaxPtrs / nranks);
   const uint64_t tile = fused_tile_elems(dtype);
   uint32_t ntiles = 0;
   args.ntens = 0;
+  args.max_ctas = max_ctas;
   args.n = nranks;
   args.avg = op == CR_AVG;
   args.inv_n = exact_inv_n(nranks);
@@ -965,11 +966,10 @@ cr_status fused_run(int nitems, int nranks, cr_dtype dtype, cr_op op, cudaStream
 
 }  // namespace
 
-extern "C" {
-
-cr_status cr_bucket_all_reduce_fused(const cr_bucket_plan_t* plan, int nranks,
-                                     void* const* tensors, cr_dtype dtype, cr_op op,
-                                     cr_stream_t stream) {
+// Arguments of cr_bucket_all_reduce_fused: plan, dtype, and N*T aligned,
+// pairwise disjoint tensors.
+cr_status cr::bucket_fused_check(const cr_bucket_plan_t* plan, int nranks, void* const* tensors,
+                                 cr_dtype dtype, cr_op op) {
   cr_status st = check_plan(plan, nranks);
   if (st) return st;
   if ((st = check_pair(dtype, op, dtype))) return st;
@@ -985,14 +985,36 @@ cr_status cr_bucket_all_reduce_fused(const cr_bucket_plan_t* plan, int nranks,
       if ((st = check_buf(p, plan->numels[t], es, "tensors", r * T + t))) return st;
       if (plan->numels[t]) spans.push_back(span_of(p, plan->numels[t] * es, 1, r * T + t));
     }
-  if ((st = check_disjoint(spans))) return st;
-  return fused_run(T, nranks, dtype, op, (cudaStream_t)stream,
-                   [&](int t, uint64_t* numel, uint64_t* off, uint64_t* bnumel, void** ptrs) {
+  return check_disjoint(spans);
+}
+
+// The fused in-place all-reduce of tensors list[0..nlist) of the plan (all
+// T tensors when list is NULL), on at most max_ctas CTAs (0: no cap).
+cr_status cr::bucket_fused_tensors(const cr_bucket_plan_t* plan, int nranks,
+                                   void* const* tensors, cr_dtype dtype, cr_op op,
+                                   const int* list, int nlist, uint32_t max_ctas,
+                                   cudaStream_t stream) {
+  const int T = plan->ntensors;
+  return fused_run(nlist, nranks, dtype, op, stream,
+                   [&](int i, uint64_t* numel, uint64_t* off, uint64_t* bnumel, void** ptrs) {
+                     const int t = list ? list[i] : i;
                      *numel = plan->numels[t];
                      *off = plan->tensor_offset[t];
                      *bnumel = plan->bucket_numel[plan->tensor_bucket[t]];
                      for (int r = 0; r < nranks; ++r) ptrs[r] = tensors[(size_t)r * T + t];
-                   });
+                   },
+                   max_ctas);
+}
+
+extern "C" {
+
+cr_status cr_bucket_all_reduce_fused(const cr_bucket_plan_t* plan, int nranks,
+                                     void* const* tensors, cr_dtype dtype, cr_op op,
+                                     cr_stream_t stream) {
+  cr_status st = cr::bucket_fused_check(plan, nranks, tensors, dtype, op);
+  if (st) return st;
+  return cr::bucket_fused_tensors(plan, nranks, tensors, dtype, op, nullptr, plan->ntensors, 0,
+                                  (cudaStream_t)stream);
 }
 
 // Every bucket of every rank all-reduced in place, all buckets in one

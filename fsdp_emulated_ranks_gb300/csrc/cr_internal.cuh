@@ -116,6 +116,7 @@ struct FusedArgs {
   int n;
   int avg;
   float inv_n;
+  uint32_t max_ctas;  // cap on the grid (0: one CTA per tile)
   uint32_t tile_start[kFusedMaxTensors + 1];
   FusedTensor t[kFusedMaxTensors];
   void* ptrs[kFusedMaxPtrs];  // rank q of tensor k at ptrs[t[k].ptr0 + q]
@@ -180,6 +181,14 @@ struct HsdpArgs {
   int avg;
   float inv_n;  // 1/(R*S) when exact, else 0 (divide)
 };
+
+// The fused bucket all-reduce (api.cu), for the DDP reducer: argument
+// checks, and the launch over a list of the plan's tensors.
+cr_status bucket_fused_check(const cr_bucket_plan_t* plan, int nranks, void* const* tensors,
+                             cr_dtype dtype, cr_op op);
+cr_status bucket_fused_tensors(const cr_bucket_plan_t* plan, int nranks, void* const* tensors,
+                               cr_dtype dtype, cr_op op, const int* list, int nlist,
+                               uint32_t max_ctas, cudaStream_t stream);
 
 cudaError_t launch_hsdp(cr_dtype in, cr_dtype out, const HsdpArgs& a, int vw,
                         cudaStream_t s);

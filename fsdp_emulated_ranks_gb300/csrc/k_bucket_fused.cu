@@ -103,7 +103,8 @@ __global__ void __launch_bounds__(kBlock)
 
 template <int D>
 static cudaError_t fused_dispatch(const FusedArgs& a, uint32_t ntiles, cudaStream_t s) {
-  const unsigned grid = flat_grid((uint64_t)ntiles * kBlock);
+  unsigned grid = flat_grid((uint64_t)ntiles * kBlock);
+  if (a.max_ctas && grid > a.max_ctas) grid = a.max_ctas;  // tiles are grid-strided
   switch (a.n) {
     case 2: k_bucket_fused<D, 2><<<grid, kBlock, 0, s>>>(a, ntiles); break;
     case 4: k_bucket_fused<D, 4><<<grid, kBlock, 0, s>>>(a, ntiles); break;

@@ -22,9 +22,10 @@
  *    pointers, one per rank; the library copies them into the kernel's
  *    parameters, so the host arrays may be reused as soon as the call returns.
  *  - The caller owns every device buffer.  No entry point allocates device
- *    memory; apart from cr_bucket_plan (which mallocs the host-side plan the
- *    caller releases with cr_bucket_plan_free) nothing allocates at all, and
- *    the library keeps no state between calls beyond cached device
+ *    memory; apart from cr_bucket_plan (the host-side plan the caller
+ *    releases with cr_bucket_plan_free) and cr_reducer_create (a host object
+ *    and CUDA events, released with cr_reducer_destroy) nothing allocates at
+ *    all, and the library keeps no state between calls beyond cached device
  *    attributes.
  *  - Every launching call is asynchronous on `stream` (NULL = the legacy
  *    default stream).  Argument errors are detected on the host before any
@@ -303,6 +304,48 @@ cr_status cr_bucket_all_reduce(const cr_bucket_plan_t* plan, int nranks,
 cr_status cr_bucket_all_reduce_fused(const cr_bucket_plan_t* plan, int nranks,
                                      void* const* tensors, cr_dtype dtype,
                                      cr_op op, cr_stream_t stream);
+
+/* ---- DDP reducer: bucket all-reduce overlapped with backward ---------------
+ * [AIG] 6.2.4-6.2.5 (figure 6-2): backward produces gradients last layer
+ * first; as soon as every gradient of a bucket is ready, that bucket's
+ * all-reduce starts on the communication stream while backward goes on.
+ * Buckets start strictly in bucket-index order (a bucket that fills early
+ * waits for its predecessors), as every rank must issue its collectives in
+ * the same order.  Each bucket's all-reduce is cr_bucket_all_reduce_fused
+ * restricted to that bucket's tensors, so after a full iteration every
+ * tensor holds exactly what cr_bucket_all_reduce_fused gives.
+ *
+ * cr_reducer_create: validates as cr_bucket_all_reduce_fused (tensors
+ *   [r*T + t], N*T pairwise disjoint, aligned), copies the plan and the
+ *   pointer table (the caller may free its plan), and creates one CUDA event
+ *   per bucket on the current device (host memory and events only; no
+ *   device memory).  comm_ctas >= 0 caps the CTAs of every bucket launch
+ *   (0: no cap) so that communication leaves SMs to the compute kernels;
+ *   results do not depend on it.  comm_stream: where the all-reduces run.
+ * cr_reducer_mark_ready: the gradient of tensor t (on all N ranks) has been
+ *   enqueued on compute_stream.  For each bucket this makes launchable, in
+ *   order: an event is recorded on compute_stream, comm_stream waits for
+ *   it, and the bucket's all-reduce is enqueued on comm_stream.
+ *   CR_ERR_INVALID_ARG: t outside [0, T), t already marked this iteration.
+ * cr_reducer_launched: buckets started so far this iteration (-1 if NULL).
+ * cr_reducer_finalize: every tensor must have been marked
+ *   (CR_ERR_INVALID_ARG otherwise, nothing enqueued); compute_stream then
+ *   waits for all of comm_stream's work, and the next iteration begins.
+ * cr_reducer_destroy: releases the object and its events (work already
+ *   enqueued is unaffected).
+ * The reducer's device must be current for every call.  Not thread-safe.
+ * On CR_ERR_CUDA the iteration's state is undefined: destroy the reducer. */
+typedef struct cr_reducer cr_reducer_t;
+
+cr_status cr_reducer_create(const cr_bucket_plan_t* plan, int nranks,
+                            void* const* tensors, cr_dtype dtype, cr_op op,
+                            int comm_ctas, cr_stream_t comm_stream,
+                            cr_reducer_t** out);
+cr_status cr_reducer_mark_ready(cr_reducer_t* red, int tensor,
+                                cr_stream_t compute_stream);
+int cr_reducer_launched(const cr_reducer_t* red);
+cr_status cr_reducer_finalize(cr_reducer_t* red, cr_stream_t compute_stream);
+void cr_reducer_destroy(cr_reducer_t* red);
 
 /* ---- a8..a10: fused FSDP / ZeRO-3 step ------------------------------------
  * One kernel performs the step of [DT] section 4 (ZeRO-3/FSDP flow steps

@@ -309,3 +309,24 @@ def test_hsdp_validation(L):
     inpl = [bufs[g * S + j] + j * L_ * 2 for g in range(R) for j in range(S)]
     expect(1, cr.cr_hsdp_reduce_scatter, bufs, R, S, 48, "bf16", "sum", inpl, "f32", stream=0)
     cr.cr_hsdp_reduce_scatter(bufs, R, S, 0, "f32", "sum", [0] * n, "f32", stream=0)
+
+
+def test_reducer_validation(L):
+    """Argument errors of the DDP reducer, all detected before any CUDA
+    call (no reducer is ever created on FAKE pointers)."""
+    plan = cr.cr_bucket_plan([8, 16, 4], 2, 40)
+    T = plan.ntensors
+    t = [FAKE + k * 4096 for k in range(2 * T)]
+    expect(1, cr.cr_reducer_create, plan, 2, t, "bf16", "avg", comm_ctas=-1, comm_stream=0)
+    expect(1, cr.cr_reducer_create, plan, 0, t, "bf16", "avg", comm_stream=0)
+    expect(1, cr.cr_reducer_create, plan, 2, t, "f32", "avg", comm_stream=0)   # elem size 4 != 2
+    expect(2, cr.cr_reducer_create, plan, 2, t, "i32", "avg", comm_stream=0)
+    expect(3, cr.cr_reducer_create, plan, 2, [t[0] + 1] + t[1:], "bf16", "sum", comm_stream=0)
+    expect(1, cr.cr_reducer_create, plan, 2, [t[0], t[0]] + t[2:], "bf16", "sum", comm_stream=0)
+    expect(1, cr.cr_reducer_create, plan, 2, t[:-1] + [0], "bf16", "sum", comm_stream=0)
+    null = cr.Reducer(0)
+    expect(1, cr.cr_reducer_mark_ready, null, 0, compute_stream=0)
+    expect(1, cr.cr_reducer_finalize, null, compute_stream=0)
+    assert cr.cr_reducer_launched(null) == -1
+    cr.cr_reducer_destroy(null)
+    L.cr_reducer_destroy(None)
