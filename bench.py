@@ -368,6 +368,13 @@ class Buckets(Workload):
         # The fused all-reduce works on the tensors in place: N reads + N
         # writes per element, the same bytes as one pass over the buckets.
         self.name = f"ddp_bucket_{mode}_bf16_{n}ranks_{ntensors}tensors"
+        from fsdp_emulated_ranks_gb300 import cr
+        self.plan = cr.cr_bucket_plan(self.numels, 2, 25 * 1024 * 1024)
+        copies = -(-n * len(self.numels) // 1024)
+        ar_launches = -(-self.plan.nbuckets // min(128, 2048 // n))
+        self.launches = {"pack": copies, "unpack": copies, "allreduce": ar_launches,
+                         "pipeline": 2 * copies + ar_launches,
+                         "fused": -(-len(self.numels) // min(128, 2048 // n))}[mode]
         self.kernel = {"allreduce": "k_bucket_fused<bf16,8>",
                        "fused": "k_bucket_fused<bf16,8>"}.get(mode, "k_copy_segments")
         self.profile = (f"k_bucket_fused_bucket_{mode}_bf16_{n}x{ntensors}"
@@ -376,15 +383,8 @@ class Buckets(Workload):
 
     def setup(self, device):
         import torch
-        from fsdp_emulated_ranks_gb300 import cr
         from fsdp_emulated_ranks_gb300 import inputs as I
         n = self.n
-        self.plan = cr.cr_bucket_plan(self.numels, 2, 25 * 1024 * 1024)
-        copies = -(-n * len(self.numels) // 1024)
-        ar_launches = -(-self.plan.nbuckets // min(128, 2048 // n))
-        self.launches = {"pack": copies, "unpack": copies, "allreduce": ar_launches,
-                         "pipeline": 2 * copies + ar_launches,
-                         "fused": -(-len(self.numels) // min(128, 2048 // n))}[self.mode]
         tens = []
         for r in range(n):
             flat = torch.empty(self.P + 128 * len(self.numels), dtype=torch.bfloat16, device=device)

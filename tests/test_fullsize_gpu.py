@@ -226,3 +226,74 @@ def test_fsdp_step_1p3b_sampled():
         assert torch.equal(params[r].view(torch.int16), params[0].view(torch.int16))
     del grads, params, master_full, mv
     torch.cuda.empty_cache()
+
+
+def embed(vals, keys, nkeys):
+    """Place sampled columns (vals [k, n]) into small rank buffers of nkeys
+    equal blocks, each sample in the block of its key (its chunk of the
+    full-size problem), so that a ring over the small buffers reduces every
+    sample in the same order as the full-size ring.  Returns the buffers,
+    the block size M and each sample's position."""
+    k, n = vals.shape
+    counts = np.bincount(keys, minlength=nkeys)
+    M = max(1, int(counts.max()))
+    pos = np.empty(k, np.int64)
+    fill = np.zeros(nkeys, np.int64)
+    for s, key in enumerate(keys):
+        pos[s] = key * M + fill[key]
+        fill[key] += 1
+    bufs = [np.zeros(nkeys * M, vals.dtype) for _ in range(n)]
+    for r in range(n):
+        bufs[r][pos] = vals[:, r]
+    return bufs, M, pos
+
+
+def test_allreduce_bf16_wire_full_sampled():
+    """The bf16-wire all-reduce of 8 x 64 MiB, as benchmarked (in place),
+    sampled and reduced by the oracle's literal ring with bf16 messages."""
+    n, count = 8, 1 << 25
+    bufs = ranks(n, count, torch.bfloat16, 0.02, 0)
+    idx = sample_idx(count, seed=123, k=1 << 16)
+    vals = gather(bufs, idx, "bf16")
+    L = cr.cr_chunk_len(count, n)
+    chunk = (idx.cpu().numpy() // L).astype(np.int64)
+    small, M, pos = embed(vals, chunk, n)
+    want = O.ring_all_reduce_wire(small, "bf16", "avg", "bf16", "bf16")[0][pos]
+    cr.cr_all_reduce_wire(bufs, count, "bf16", "avg", "bf16", bufs, "bf16")
+    torch.cuda.synchronize()
+    got = gather(bufs, idx, "bf16")
+    for r in range(n):
+        assert_match(got[:, r].copy(), want, "bf16", f"rank {r}")
+    del bufs
+    torch.cuda.empty_cache()
+
+
+def test_hsdp_2x4_full_sampled():
+    """HSDP on the 2 x 4 mesh, 64 MiB bf16 per rank, as benchmarked: each
+    sample keeps its shard j and outer chunk i in the embedded problem."""
+    R, S, count = 2, 4, 1 << 25
+    n = R * S
+    bufs = ranks(n, count, torch.bfloat16, 0.02, 0)
+    L = -(-count // S)
+    shards = [torch.empty(min(L, count - j * L), dtype=torch.bfloat16, device="cuda")
+              for _ in range(R) for j in range(S)]
+    idx = sample_idx(count, seed=321, k=1 << 16)
+    vals = gather(bufs, idx, "bf16")
+    e = idx.cpu().numpy().astype(np.int64)
+    j = e // L
+    k = e - j * L
+    L2 = -(-L // R)   # every shard is full: count = S * L
+    i = k // L2
+    small, M, pos = embed(vals, j * R + i, S * R)
+    want = O.hsdp_reduce_scatter(small, R, S, "bf16", "avg", "bf16")
+    cr.cr_hsdp_reduce_scatter(bufs, R, S, count, "bf16", "avg", shards, "bf16")
+    torch.cuda.synchronize()
+    Ls = R * M  # shard length of the embedded problem
+    for g in range(R):
+        flat = torch.cat(shards[g * S:(g + 1) * S])
+        got = to_host(flat[idx], "bf16")
+        ref = np.concatenate(want[g * S:(g + 1) * S])[pos]
+        assert_match(got, ref, "bf16", f"group {g}")
+        assert Ls * S == sum(w.size for w in want[g * S:(g + 1) * S])
+    del bufs, shards
+    torch.cuda.empty_cache()

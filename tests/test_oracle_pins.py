@@ -752,3 +752,79 @@ def test_hsdp_integer_sum_is_exact_and_replicated(R, S):
     for g in range(R):
         full = np.concatenate(ha[g * S:(g + 1) * S])
         assert np.array_equal(full, (exact.astype(np.float32) / np.float32(n)).astype(np.float32))
+
+
+def _hsdp_by_hand(x, R, S, count):
+    """HSDP's association written out element by element from the two
+    rings' conventions (reading of [AIG] 6.3.6 / [DT] section 4): shard
+    j = e // L (L = ceil(count/S)); inside group g the ranks are added from
+    s = j+1 round to s = j; the R group sums of shard j's offset k are added
+    from group i+1 round to group i, where i = k // ceil(len_j / R).  x is
+    [R*S][count] float32; returns [count] float32 sums."""
+    f = np.float32
+    L = -(-count // S)
+    out = np.zeros(count, np.float32)
+    for e in range(count):
+        j, k = e // L, e % L
+        len_j = min(L, count - j * L)
+        i = k // -(-len_j // R)
+        def inner(g):
+            acc = f(x[g * S + (j + 1) % S][e])
+            for t in range(2, S + 1):
+                acc = f(acc + f(x[g * S + (j + t) % S][e]))
+            return acc
+        acc = inner((i + 1) % R)
+        for t in range(2, R + 1):
+            acc = f(acc + inner((i + t) % R))
+        out[e] = acc
+    return out
+
+
+def _hsdp_slip(x, R, S, count, outer_from_shard, inner_from_zero):
+    """_hsdp_by_hand with one plausible slip: the outer ring started at
+    group j+1 (the shard index) instead of i+1, or the inner ring started
+    at rank 0 instead of j+1."""
+    f = np.float32
+    L = -(-count // S)
+    out = np.zeros(count, np.float32)
+    for e in range(count):
+        j, k = e // L, e % L
+        len_j = min(L, count - j * L)
+        i = k // -(-len_j // R)
+        s0 = 0 if inner_from_zero else (j + 1) % S
+        def inner(g):
+            acc = f(x[g * S + s0][e])
+            for t in range(1, S):
+                acc = f(acc + f(x[g * S + (s0 + t) % S][e]))
+            return acc
+        g0 = (j + 1) % R if outer_from_shard else (i + 1) % R
+        acc = inner(g0)
+        for t in range(1, R):
+            acc = f(acc + inner((g0 + t) % R))
+        out[e] = acc
+    return out
+
+
+@pytest.mark.parametrize("R,S,count", [(2, 2, 4), (2, 3, 7), (3, 2, 11), (2, 2, 9), (3, 3, 13),
+                                       (4, 3, 25)])
+def test_hsdp_fold_order_by_hand(R, S, count):
+    """The oracle's HSDP equals the hand-enumerated parenthesisation on
+    random fp32 values, bit for bit.  With three or more operands the order
+    matters (two-operand sums are commutative), and there each plausible
+    slip -- outer ring started at the shard's index, inner ring started at
+    rank 0 -- gives a different answer somewhere: the pin has teeth."""
+    rng = np.random.default_rng(R * 100 + S * 10 + count)
+    outer_hits = inner_hits = 0
+    for trial in range(40):
+        x = [(rng.standard_normal(count) * np.exp2(rng.integers(-12, 12, count))).astype(np.float32)
+             for _ in range(R * S)]
+        got = O.hsdp_reduce_scatter(x, R, S, "f32", "sum")
+        want = _hsdp_by_hand(x, R, S, count)
+        for g in range(R):
+            assert np.concatenate(got[g * S:(g + 1) * S]).tobytes() == want.tobytes()
+        outer_hits += _hsdp_slip(x, R, S, count, True, False).tobytes() != want.tobytes()
+        inner_hits += _hsdp_slip(x, R, S, count, False, True).tobytes() != want.tobytes()
+    if R >= 3:
+        assert outer_hits > 0
+    if S >= 3:
+        assert inner_hits > 0
