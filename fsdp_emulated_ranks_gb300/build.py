@@ -58,7 +58,8 @@ def kernel_hash(tu: str) -> str:
     that file, every shared header of the library and the compiler flags.
     A profile of a kernel stays valid while this hash is unchanged."""
     h = hashlib.sha256()
-    h.update(" ".join(ARCH + NVCC_FLAGS).encode())
+    # the flags without the include paths, which differ between checkouts
+    h.update(" ".join(f for f in ARCH + NVCC_FLAGS if not f.startswith("-I")).encode())
     heads = sorted(f for f in os.listdir(CSRC) if f.endswith((".cuh", ".h")))
     for f in [os.path.join(CSRC, tu)] + [os.path.join(CSRC, x) for x in heads] + [
             os.path.join(INCLUDE, "cr.h")]:
