@@ -144,27 +144,50 @@ def _ptr(x) -> int:
     return x.data_ptr()
 
 
+_VP_ARRAY = {}  # length -> ctypes array type of void pointers
+
+
 def _ptr_array(xs: Sequence) -> C.Array:
-    arr = (C.c_void_p * max(1, len(xs)))()
-    for k, x in enumerate(xs):
-        arr[k] = _ptr(x)
-    return arr
+    n = max(1, len(xs))
+    t = _VP_ARRAY.get(n)
+    if t is None:
+        t = _VP_ARRAY[n] = C.c_void_p * n
+    return t(*[x if type(x) is int else _ptr(x) for x in xs])
 
 
 def _dtype(d) -> int:
     if isinstance(d, int):
         return d
-    return _DTYPES[str(d).replace("torch.", "")]
+    k = _DTYPES.get(d)
+    return k if k is not None else _DTYPES[str(d).replace("torch.", "")]
 
 
 def _op(o) -> int:
     return o if isinstance(o, int) else _OPS[o]
 
 
+_torch = None
+_raw_stream = None  # torch's C-level current-stream query, when it has one
+
+
+def _current_stream() -> int:
+    """Handle of torch's current CUDA stream on the current device."""
+    global _torch, _raw_stream
+    if _torch is None:
+        import torch
+        _torch = torch
+        get_raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        get_dev = getattr(torch._C, "_cuda_getDevice", None)
+        if get_raw is not None and get_dev is not None:
+            _raw_stream = lambda: get_raw(get_dev())
+    if _raw_stream is not None:
+        return _raw_stream()
+    return _torch.cuda.current_stream().cuda_stream
+
+
 def _stream(stream) -> int:
     if stream is None:
-        import torch
-        return torch.cuda.current_stream().cuda_stream
+        return _current_stream()
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
