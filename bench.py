@@ -854,9 +854,22 @@ def run_sweep(args, device, stream, peak):
                        steps, 3, 1, stream)
         ms = statistics.median(per)
         sent, _, _ = cr.cr_comm_elems(cr.COLL_ALL_REDUCE, cr.SCHED_RING, n, count, 0)
-        out.append({"n": n, "bytes_per_rank": count * 2, "us": round(ms * 1e3, 2),
-                    "GB/s": round(ar_bytes(n, count, 2) / (ms * 1e-3) / 1e9, 1),
-                    "ring_bytes_per_rank": sent * 2})
+        pt = {"n": n, "bytes_per_rank": count * 2, "us": round(ms * 1e3, 2),
+              "GB/s": round(ar_bytes(n, count, 2) / (ms * 1e-3) / 1e9, 1),
+              "ring_bytes_per_rank": sent * 2}
+        if count * 2 <= (16 << 20):
+            # the same calls captured in a CUDA graph: no host work per call
+            reps = 50
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream(device)
+            side.wait_stream(torch.cuda.current_stream(device))
+            with torch.cuda.graph(g, stream=side):
+                for _ in range(reps):
+                    cr.cr_all_reduce(bufs, count, "bf16", "avg", bufs, "bf16")
+            _, gper = timed(g.replay, 10, 3, 1, stream)
+            pt["graph_us"] = round(statistics.median(gper) * 1e3 / reps, 2)
+            del g
+        out.append(pt)
         del bufs
         torch.cuda.empty_cache()
     # least squares on the 8-rank points: t = a + x / B, x = algorithmic bytes
@@ -866,8 +879,10 @@ def run_sweep(args, device, stream, peak):
     slope = sum((x - mx) * (t - mt) for x, t in zip(xs, ts)) / sum((x - mx) ** 2 for x in xs)
     a = mt - slope * mx
     bw = 1 / slope
+    g8 = [p["graph_us"] for p in out if p["n"] == 8 and "graph_us" in p]
     return {"points": out, "alpha_us": round(a * 1e6, 3), "bw_GBs": round(bw / 1e9, 1),
-            "crossover_bytes": round(a * bw)}
+            "crossover_bytes": round(a * bw),
+            "graph_latency_us_min": min(g8) if g8 else None}
 
 
 # ---- main ---------------------------------------------------------------------------------

@@ -297,3 +297,95 @@ def test_hsdp_2x4_full_sampled():
         assert Ls * S == sum(w.size for w in want[g * S:(g + 1) * S])
     del bufs, shards
     torch.cuda.empty_cache()
+
+
+# ---- beyond 2^32 elements per buffer ----------------------------------------
+# Element indices and chunk divisions switch to 64-bit arithmetic once a
+# buffer holds 2^32 elements or more (the multiply-shift division covers
+# dividends below 2^32 only).  N = 2 keeps the footprint at tens of GB.
+
+BIG_RAGGED = (1 << 32) + 301            # odd: vector path plus an element tail
+BIG_EVEN = 2 * ((1 << 31) + 80)         # shard length a multiple of 16
+
+
+def edge_idx(count, extra=(), seed=0):
+    L = -(-count // 2)
+    fixed = [0, 1, L - 1, L, L + 1, (1 << 32) - 1, 1 << 32, (1 << 32) + 1, count - 17,
+             count - 16, count - 1, *extra]
+    idx = torch.cat([sample_idx(count, seed, k=1 << 14).cpu(),
+                     torch.tensor([i for i in fixed if 0 <= i < count])])
+    return torch.unique(idx).cuda()
+
+
+def pick(shards, L, idx):
+    """Elements idx of the concatenation of equal-length shards, without
+    building the concatenation."""
+    out = torch.empty(idx.numel(), dtype=shards[0].dtype, device="cuda")
+    which = idx // L
+    for j, sh in enumerate(shards):
+        m = which == j
+        out[m] = sh[idx[m] - j * L]
+    return out
+
+
+def test_allreduce_bf16_beyond_2_32_elements():
+    n, count = 2, BIG_RAGGED
+    bufs = ranks(n, count, torch.bfloat16, 0.02, 40)
+    idx = edge_idx(count, seed=1)
+    vals = gather(bufs, idx, "bf16")
+    L = cr.cr_chunk_len(count, n)
+    chunk = (idx.cpu().numpy() // L).astype(np.int32)
+    want = O.fold_columns(vals, chunk, "bf16", "avg", "bf16")
+    cr.cr_all_reduce(bufs, count, "bf16", "avg", bufs, "bf16")
+    torch.cuda.synchronize()
+    got = gather(bufs, idx, "bf16")
+    for r in range(n):
+        assert_match(got[:, r].copy(), want, "bf16", f"rank {r}")
+    assert torch.equal(bufs[0].view(torch.int16), bufs[1].view(torch.int16))
+    del bufs
+    torch.cuda.empty_cache()
+
+
+def test_reduce_scatter_and_all_gather_beyond_2_32_elements():
+    n, count = 2, BIG_EVEN
+    L = count // n
+    bufs = ranks(n, count, torch.bfloat16, 0.02, 50)
+    idx = edge_idx(count, seed=2)
+    vals = gather(bufs, idx, "bf16")
+    chunk = (idx.cpu().numpy() // L).astype(np.int32)
+    want = O.fold_columns(vals, chunk, "bf16", "avg", "bf16")
+    shards = [torch.empty(L, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    cr.cr_reduce_scatter(bufs, count, "bf16", "avg", shards, "bf16")
+    torch.cuda.synchronize()
+    assert_match(to_host(pick(shards, L, idx), "bf16"), want, "bf16", "reduce-scatter")
+    cr.cr_all_gather(shards, count, "bf16", bufs)
+    torch.cuda.synchronize()
+    for r in range(n):
+        for j in range(n):
+            assert torch.equal(bufs[r][j * L:(j + 1) * L].view(torch.int16),
+                               shards[j].view(torch.int16)), (r, j)
+    del bufs, shards
+    torch.cuda.empty_cache()
+
+
+def test_hsdp_2x2_beyond_2_32_elements():
+    R, S, count = 2, 2, BIG_EVEN
+    n = R * S
+    L = count // S
+    bufs = ranks(n, count, torch.bfloat16, 0.02, 60)
+    shards = [torch.empty(L, dtype=torch.bfloat16, device="cuda") for _ in range(R * S)]
+    idx = edge_idx(count, seed=3)
+    vals = gather(bufs, idx, "bf16")
+    e = idx.cpu().numpy().astype(np.int64)
+    j = e // L
+    i = (e - j * L) // (-(-L // R))
+    small, M, pos = embed(vals, j * R + i, S * R)
+    want = O.hsdp_reduce_scatter(small, R, S, "bf16", "avg", "bf16")
+    cr.cr_hsdp_reduce_scatter(bufs, R, S, count, "bf16", "avg", shards, "bf16")
+    torch.cuda.synchronize()
+    for g in range(R):
+        got = to_host(pick(shards[g * S:(g + 1) * S], L, idx), "bf16")
+        ref = np.concatenate(want[g * S:(g + 1) * S])[pos]
+        assert_match(got, ref, "bf16", f"group {g}")
+    del bufs, shards
+    torch.cuda.empty_cache()
