@@ -53,16 +53,34 @@ def source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def _local_includes(path: str, seen: set) -> None:
+    """Files under csrc/ or include/ that `path` includes, transitively."""
+    with open(path) as fh:
+        for line in fh:
+            line = line.strip()
+            if not line.startswith("#include \""):
+                continue
+            name = line.split('"')[1]
+            for d in (CSRC, INCLUDE):
+                q = os.path.join(d, name)
+                if os.path.exists(q) and q not in seen:
+                    seen.add(q)
+                    _local_includes(q, seen)
+                    break
+
+
 def kernel_hash(tu: str) -> str:
     """Hash of what the kernels of one translation unit are compiled from:
-    that file, every shared header of the library and the compiler flags.
-    A profile of a kernel stays valid while this hash is unchanged."""
+    that file, the library headers it includes (transitively) and the
+    compiler flags.  A profile of a kernel stays valid while this hash is
+    unchanged."""
     h = hashlib.sha256()
     # the flags without the include paths, which differ between checkouts
     h.update(" ".join(f for f in ARCH + NVCC_FLAGS if not f.startswith("-I")).encode())
-    heads = sorted(f for f in os.listdir(CSRC) if f.endswith((".cuh", ".h")))
-    for f in [os.path.join(CSRC, tu)] + [os.path.join(CSRC, x) for x in heads] + [
-            os.path.join(INCLUDE, "cr.h")]:
+    src = os.path.join(CSRC, tu)
+    deps: set = set()
+    _local_includes(src, deps)
+    for f in [src] + sorted(deps, key=os.path.basename):
         h.update(os.path.basename(f).encode())
         with open(f, "rb") as fh:
             h.update(fh.read())

@@ -853,11 +853,12 @@ static cr_status bucket_copy(const cr_bucket_plan_t* plan, int nranks,
   }
   static thread_local CopyArgs args;  // ~28 KB: kept off the stack
   uint32_t ntiles = 0;
+  int launches = 0;  // launches after the first are chained to their predecessor
   args.nseg = 0;
   auto flush = [&]() -> cr_status {
     if (args.nseg == 0) return CR_OK;
     args.tile_start[args.nseg] = ntiles;
-    cudaError_t e = launch_copy(args, ntiles, stream);
+    cudaError_t e = launch_copy(args, ntiles, launches++ > 0, stream);
     args.nseg = 0;
     ntiles = 0;
     if (e != cudaSuccess) return cuda_fail(e, "bucket copy launch");
@@ -920,6 +921,7 @@ cr_status fused_run(int nitems, int nranks, cr_dtype dtype, cr_op op, cudaStream
   const int per_launch = std::min(kFusedMaxTensors, kFusedMaxPtrs / nranks);
   const uint64_t tile = fused_tile_elems(dtype);
   uint32_t ntiles = 0;
+  int launches = 0;  // launches after the first are chained to their predecessor
   args.ntens = 0;
   args.max_ctas = max_ctas;
   args.n = nranks;
@@ -928,7 +930,7 @@ cr_status fused_run(int nitems, int nranks, cr_dtype dtype, cr_op op, cudaStream
   auto flush = [&]() -> cr_status {
     if (args.ntens == 0) return CR_OK;
     args.tile_start[args.ntens] = ntiles;
-    cudaError_t e = launch_bucket_fused(dtype, args, ntiles, stream);
+    cudaError_t e = launch_bucket_fused(dtype, args, ntiles, launches++ > 0, stream);
     args.ntens = 0;
     ntiles = 0;
     if (e != cudaSuccess) return cuda_fail(e, "fused bucket all-reduce launch");
@@ -1092,6 +1094,7 @@ cr_status cr_fsdp2_step(const cr_param_shape* shapes, int nparams, int nranks,
   static thread_local Fsdp2Args args;  // ~24 KB: kept off the stack
   const int per_launch = std::min(kFsdp2MaxParams, kFsdp2MaxPtrs / (5 * n));
   uint32_t ntiles = 0;
+  int launches = 0;  // launches after the first are chained to their predecessor
   args.nparams = 0;
   args.n = n;
   args.inv_n = exact_inv_n(n);
@@ -1099,7 +1102,7 @@ cr_status cr_fsdp2_step(const cr_param_shape* shapes, int nparams, int nranks,
   auto flush = [&]() -> cr_status {
     if (args.nparams == 0) return CR_OK;
     args.tile_start[args.nparams] = ntiles;
-    cudaError_t e = launch_fsdp2(args, ntiles, (cudaStream_t)stream);
+    cudaError_t e = launch_fsdp2(args, ntiles, launches++ > 0, (cudaStream_t)stream);
     args.nparams = 0;
     ntiles = 0;
     if (e != cudaSuccess) return cuda_fail(e, "fsdp2_step launch");

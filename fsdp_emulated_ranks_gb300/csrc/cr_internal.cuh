@@ -206,11 +206,13 @@ cudaError_t launch_fsdp_sumsq(const FsdpArgs& a, bool vec, double* partials,
 cudaError_t launch_clip_coef(const double* partials, int nparts, double max_norm, float* coef,
                              float* norm_out, cudaStream_t s);
 cudaError_t launch_adamw(const AdamArgs& a, bool vec, cudaStream_t s);
-cudaError_t launch_copy(const CopyArgs& a, uint32_t ntiles, cudaStream_t s);
-cudaError_t launch_bucket_fused(cr_dtype d, const FusedArgs& a, uint32_t ntiles,
+// chained: launched as the programmatic dependent of the call's previous
+// launch (pdl.cuh).
+cudaError_t launch_copy(const CopyArgs& a, uint32_t ntiles, bool chained, cudaStream_t s);
+cudaError_t launch_bucket_fused(cr_dtype d, const FusedArgs& a, uint32_t ntiles, bool chained,
                                 cudaStream_t s);
 uint64_t fused_tile_elems(cr_dtype d);  // elements of a tensor per CTA tile
-cudaError_t launch_fsdp2(const Fsdp2Args& a, uint32_t ntiles, cudaStream_t s);
+cudaError_t launch_fsdp2(const Fsdp2Args& a, uint32_t ntiles, bool chained, cudaStream_t s);
 // grad_dtype CR_F32 or CR_BF16; vw as for the other launchers (16-byte
 // grads and 32- or 16-byte accumulators).
 cudaError_t launch_accum(cr_dtype grad_dtype, const AccumArgs& a, int vw, cudaStream_t s);

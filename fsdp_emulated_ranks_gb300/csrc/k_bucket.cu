@@ -17,6 +17,7 @@
 // one byte at a time by the range's first tile.
 #include "cr_internal.cuh"
 #include "fold.cuh"
+#include "pdl.cuh"
 
 namespace cr {
 
@@ -51,6 +52,7 @@ __device__ __forceinline__ uint4 ld16_ro(const void* p) {
 
 __global__ void __launch_bounds__(kBlock)
     k_copy_segments(const __grid_constant__ CopyArgs a, uint32_t ntiles) {
+  pdl_launch_dependents();
   for (uint32_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
     // Range s holds tile t iff tile_start[s] <= t < tile_start[s + 1].
     int lo = 0, hi = a.nseg;  // invariant: tile_start[lo] <= t < tile_start[hi]
@@ -115,12 +117,13 @@ __global__ void __launch_bounds__(kBlock)
       }
     }
   }
+  pdl_wait_prerequisites();
 }
 
-cudaError_t launch_copy(const CopyArgs& a, uint32_t ntiles, cudaStream_t s) {
+cudaError_t launch_copy(const CopyArgs& a, uint32_t ntiles, bool chained, cudaStream_t s) {
   if (ntiles == 0) return cudaSuccess;
-  k_copy_segments<<<flat_grid((uint64_t)ntiles * kBlock), kBlock, 0, s>>>(a, ntiles);
-  return cudaGetLastError();
+  return launch_chained(k_copy_segments, flat_grid((uint64_t)ntiles * kBlock), kBlock, s, chained,
+                        a, ntiles);
 }
 
 }  // namespace cr

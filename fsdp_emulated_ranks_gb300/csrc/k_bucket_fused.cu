@@ -18,6 +18,7 @@
 // 32-byte vectors when all of that tensor's rank pointers allow it.
 #include "cr_internal.cuh"
 #include "fold.cuh"
+#include "pdl.cuh"
 
 namespace cr {
 
@@ -80,6 +81,7 @@ __device__ __forceinline__ void fused_tile(const FusedArgs& a, const FusedTensor
 template <int D, int NT>
 __global__ void __launch_bounds__(kBlock)
     k_bucket_fused(const __grid_constant__ FusedArgs a, uint32_t ntiles) {
+  pdl_launch_dependents();
   const int n = NT > 0 ? NT : a.n;
   for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     int lo = 0, hi = a.ntens;  // tile_start[lo] <= tile < tile_start[hi]
@@ -99,28 +101,29 @@ __global__ void __launch_bounds__(kBlock)
       for (uint64_t i = e_lo + threadIdx.x; i < e_hi; i += kBlock) fused_elem<D>(a, t, i);
     }
   }
+  pdl_wait_prerequisites();
 }
 
 template <int D>
-static cudaError_t fused_dispatch(const FusedArgs& a, uint32_t ntiles, cudaStream_t s) {
+static cudaError_t fused_dispatch(const FusedArgs& a, uint32_t ntiles, bool chained,
+                                  cudaStream_t s) {
   unsigned grid = flat_grid((uint64_t)ntiles * kBlock);
   if (a.max_ctas && grid > a.max_ctas) grid = a.max_ctas;  // tiles are grid-strided
   switch (a.n) {
-    case 2: k_bucket_fused<D, 2><<<grid, kBlock, 0, s>>>(a, ntiles); break;
-    case 4: k_bucket_fused<D, 4><<<grid, kBlock, 0, s>>>(a, ntiles); break;
-    case 8: k_bucket_fused<D, 8><<<grid, kBlock, 0, s>>>(a, ntiles); break;
-    default: k_bucket_fused<D, 0><<<grid, kBlock, 0, s>>>(a, ntiles); break;
+    case 2: return launch_chained(k_bucket_fused<D, 2>, grid, kBlock, s, chained, a, ntiles);
+    case 4: return launch_chained(k_bucket_fused<D, 4>, grid, kBlock, s, chained, a, ntiles);
+    case 8: return launch_chained(k_bucket_fused<D, 8>, grid, kBlock, s, chained, a, ntiles);
+    default: return launch_chained(k_bucket_fused<D, 0>, grid, kBlock, s, chained, a, ntiles);
   }
-  return cudaGetLastError();
 }
 
-cudaError_t launch_bucket_fused(cr_dtype d, const FusedArgs& a, uint32_t ntiles,
+cudaError_t launch_bucket_fused(cr_dtype d, const FusedArgs& a, uint32_t ntiles, bool chained,
                                 cudaStream_t s) {
   if (ntiles == 0) return cudaSuccess;
   switch (d) {
-    case CR_F32: return fused_dispatch<CR_F32>(a, ntiles, s);
-    case CR_BF16: return fused_dispatch<CR_BF16>(a, ntiles, s);
-    case CR_I32: return fused_dispatch<CR_I32>(a, ntiles, s);
+    case CR_F32: return fused_dispatch<CR_F32>(a, ntiles, chained, s);
+    case CR_BF16: return fused_dispatch<CR_BF16>(a, ntiles, chained, s);
+    case CR_I32: return fused_dispatch<CR_I32>(a, ntiles, chained, s);
   }
   return cudaErrorInvalidValue;
 }

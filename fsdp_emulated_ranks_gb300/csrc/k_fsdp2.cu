@@ -13,12 +13,14 @@
 #include "cr_internal.cuh"
 #include "fold.cuh"
 #include "fsdp_body.cuh"
+#include "pdl.cuh"
 
 namespace cr {
 
 template <int NT>
 __global__ void __launch_bounds__(kBlock)
     k_fsdp2(const __grid_constant__ Fsdp2Args a, uint32_t ntiles) {
+  pdl_launch_dependents();
   const int n = NT > 0 ? NT : a.n;
   for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     int lo = 0, hi = a.nparams;  // tile_start[lo] <= tile < tile_start[hi]
@@ -51,18 +53,18 @@ __global__ void __launch_bounds__(kBlock)
         fsdp_element(grads, params, master, m, v, n, p.L, p.Ld, a.inv_n, a.a, 1.0f, e);
     }
   }
+  pdl_wait_prerequisites();
 }
 
-cudaError_t launch_fsdp2(const Fsdp2Args& a, uint32_t ntiles, cudaStream_t s) {
+cudaError_t launch_fsdp2(const Fsdp2Args& a, uint32_t ntiles, bool chained, cudaStream_t s) {
   if (ntiles == 0) return cudaSuccess;
   const unsigned grid = flat_grid((uint64_t)ntiles * kBlock);
   switch (a.n) {
-    case 2: k_fsdp2<2><<<grid, kBlock, 0, s>>>(a, ntiles); break;
-    case 4: k_fsdp2<4><<<grid, kBlock, 0, s>>>(a, ntiles); break;
-    case 8: k_fsdp2<8><<<grid, kBlock, 0, s>>>(a, ntiles); break;
-    default: k_fsdp2<0><<<grid, kBlock, 0, s>>>(a, ntiles); break;
+    case 2: return launch_chained(k_fsdp2<2>, grid, kBlock, s, chained, a, ntiles);
+    case 4: return launch_chained(k_fsdp2<4>, grid, kBlock, s, chained, a, ntiles);
+    case 8: return launch_chained(k_fsdp2<8>, grid, kBlock, s, chained, a, ntiles);
+    default: return launch_chained(k_fsdp2<0>, grid, kBlock, s, chained, a, ntiles);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace cr

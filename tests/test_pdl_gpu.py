@@ -1,0 +1,132 @@
+"""Calls that need several launches (fused bucket all-reduce, bucket pack,
+FSDP2 step) chain them with programmatic dependent launch.  The chain must
+still look like one stream-ordered operation to the caller: work the caller
+enqueues next on the same stream sees every launch's results, the first
+launch's included; and a captured CUDA graph of a chained call replays
+the same results."""
+import numpy as np
+import pytest
+import torch
+
+from fsdp_emulated_ranks_gb300 import build as libbuild
+from fsdp_emulated_ranks_gb300 import cr
+from fsdp_emulated_ranks_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    libbuild.build()
+    cr.lib()
+
+
+def tensors(n, numels, seed):
+    out = []
+    for r in range(n):
+        for t, k in enumerate(numels):
+            x = torch.empty(k, dtype=torch.bfloat16, device="cuda")
+            I.torch_fill_normal_(x, 0.02, seed + 1000 * r + t)
+            out.append(x)
+    return out
+
+
+def big_case(seed, T=300):
+    rng = np.random.default_rng(seed)
+    # large first tensors: the first launch runs long, so a broken chain
+    # would let the caller's next kernel read its tensors too early
+    numels = [int(x) for x in rng.integers(1 << 10, 1 << 20, T)]
+    numels[:20] = [1 << 22] * 20
+    return numels
+
+
+def test_fused_chain_is_stream_ordered():
+    n = 8
+    numels = big_case(1)
+    plan = cr.cr_bucket_plan(numels, 2, 25 << 20)
+    t = tensors(n, numels, 0)
+    ref = [x.clone() for x in t]
+    cr.cr_bucket_all_reduce_fused(plan, n, ref, "bf16", "avg")
+    torch.cuda.synchronize()
+    cr.cr_bucket_all_reduce_fused(plan, n, t, "bf16", "avg")
+    snap = [x.clone() for x in t]          # same stream, right behind the chain
+    torch.cuda.synchronize()
+    for k in range(len(t)):
+        assert torch.equal(snap[k].view(torch.int16), ref[k].view(torch.int16)), k
+
+
+def test_pack_chain_is_stream_ordered():
+    n = 8
+    numels = big_case(2)
+    plan = cr.cr_bucket_plan(numels, 2, 25 << 20)
+    t = tensors(n, numels, 10)
+    B = plan.nbuckets
+    buckets = [torch.empty(int(plan.bucket_numel[b]), dtype=torch.bfloat16, device="cuda")
+               for _ in range(n) for b in range(B)]
+    torch.cuda.synchronize()
+    cr.cr_bucket_pack(plan, n, t, buckets)
+    snap = [x.clone() for x in buckets]
+    torch.cuda.synchronize()
+    T = plan.ntensors
+    for r in range(n):
+        for k in range(T):
+            b, off = plan.tensor_bucket[k], plan.tensor_offset[k]
+            got = snap[r * B + b][off:off + numels[k]]
+            assert torch.equal(got.view(torch.int16), t[r * T + k].view(torch.int16)), (r, k)
+
+
+def test_fsdp2_chain_is_stream_ordered():
+    n = 8
+    shapes = [(4096, 1024)] * 10 + [(257, 33)] * 150   # more than one launch of 64
+    cfg = cr.adamw_cfg()
+
+    def state(seed):
+        g, m_, mm, v, p = [], [], [], [], []
+        for i, (d0, row) in enumerate(shapes):
+            for r in range(n):
+                x = torch.empty(d0 * row, dtype=torch.bfloat16, device="cuda")
+                I.torch_fill_normal_(x, 1e-3, seed + 100 * i + r)
+                g.append(x)
+                p.append(torch.empty(d0 * row, dtype=torch.bfloat16, device="cuda"))
+            Lr = -(-d0 // n)
+            for j in range(n):
+                k = max(0, min(d0, (j + 1) * Lr) - min(d0, j * Lr)) * row
+                x = torch.empty(k, dtype=torch.float32, device="cuda")
+                I.torch_fill_normal_(x, 0.02, seed + 7 * i + j + 5000)
+                m_.append(x if k else 0)
+                mm.append(torch.zeros(k, dtype=torch.float32, device="cuda") if k else 0)
+                v.append(torch.zeros(k, dtype=torch.float32, device="cuda") if k else 0)
+        return g, m_, mm, v, p
+
+    a, b = state(3), state(3)
+    cr.cr_fsdp2_step(shapes, n, a[0], a[1], a[2], a[3], cfg, a[4])
+    torch.cuda.synchronize()
+    cr.cr_fsdp2_step(shapes, n, b[0], b[1], b[2], b[3], cfg, b[4])
+    snap = [x.clone() for x in b[4]]
+    torch.cuda.synchronize()
+    for k in range(len(snap)):
+        assert torch.equal(snap[k].view(torch.int16), a[4][k].view(torch.int16)), k
+
+
+def test_chained_call_replays_from_a_graph():
+    n = 8
+    numels = big_case(4)
+    plan = cr.cr_bucket_plan(numels, 2, 25 << 20)
+    src = tensors(n, numels, 20)
+    ref = [x.clone() for x in src]
+    cr.cr_bucket_all_reduce_fused(plan, n, ref, "bf16", "avg")
+    work = [torch.empty_like(x) for x in src]
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        cr.cr_bucket_all_reduce_fused(plan, n, work, "bf16", "avg")
+    for w, x in zip(work, src):
+        w.copy_(x)
+    g.replay()
+    torch.cuda.synchronize()
+    for k in range(len(work)):
+        assert torch.equal(work[k].view(torch.int16), ref[k].view(torch.int16)), k
