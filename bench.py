@@ -405,18 +405,22 @@ class Buckets(Workload):
             bks.append(row_b)
         self.t_flat_t = [x for rr in tens for x in rr]
         self.t_flat_b = [x for rr in bks for x in rr]
+        # Device addresses taken once, as a framework with static gradient
+        # buffers would: the calls then marshal integers, not 2400 tensors.
+        self.p_flat_t = [x.data_ptr() for x in self.t_flat_t]
+        self.p_flat_b = [x.data_ptr() for x in self.t_flat_b]
 
     def step(self, stream):
         from fsdp_emulated_ranks_gb300 import cr
         n = self.n
         if self.mode in ("pack", "pipeline"):
-            cr.cr_bucket_pack(self.plan, n, self.t_flat_t, self.t_flat_b, stream)
+            cr.cr_bucket_pack(self.plan, n, self.p_flat_t, self.p_flat_b, stream)
         if self.mode in ("allreduce", "pipeline"):
-            cr.cr_bucket_all_reduce(self.plan, n, self.t_flat_b, "bf16", "avg", stream)
+            cr.cr_bucket_all_reduce(self.plan, n, self.p_flat_b, "bf16", "avg", stream)
         if self.mode in ("unpack", "pipeline"):
-            cr.cr_bucket_unpack(self.plan, n, self.t_flat_b, self.t_flat_t, stream)
+            cr.cr_bucket_unpack(self.plan, n, self.p_flat_b, self.p_flat_t, stream)
         if self.mode == "fused":
-            cr.cr_bucket_all_reduce_fused(self.plan, n, self.t_flat_t, "bf16", "avg", stream)
+            cr.cr_bucket_all_reduce_fused(self.plan, n, self.p_flat_t, "bf16", "avg", stream)
 
 
 class FsdpStep(Workload):
@@ -524,6 +528,10 @@ class Fsdp2Step(Workload):
                 self.master.append(self.t_state[so0:so0 + sk] if sk else 0)
                 self.m.append(self.t_state[so + so0:so + so0 + sk] if sk else 0)
                 self.v.append(self.t_state[2 * so + so0:2 * so + so0 + sk] if sk else 0)
+        # Device addresses taken once (the slabs t_g, t_p, t_state stay alive).
+        addr = lambda xs: [x if isinstance(x, int) else x.data_ptr() for x in xs]
+        self.grads, self.params = addr(self.grads), addr(self.params)
+        self.master, self.m, self.v = addr(self.master), addr(self.m), addr(self.v)
         self.cfg = cr.adamw_cfg()
 
     def step(self, stream):
@@ -698,7 +706,7 @@ def run_rows(args, device, stream, peak, skip=None):
             continue
         wl = make_workload(name, args)
         wl.setup(device)
-        steps = args.row_steps if wl.nbytes < (8 << 30) else max(3, args.row_steps // 4)
+        steps = args.row_steps if wl.nbytes < (8 << 30) else max(5, args.row_steps // 2)
         _, per = timed(lambda: wl.step(stream), steps, 3, 1, stream)
         ms = statistics.mean(per)
         gbs = wl.nbytes / (ms * 1e-3) / 1e9
