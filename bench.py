@@ -718,6 +718,39 @@ def run_rows(args, device, stream, peak, skip=None):
     return rows
 
 
+# ---- bf16 wire error ----------------------------------------------------------------------
+
+def wire_error(device, n=8, count=1 << 24):
+    """What the bf16 wire costs in accuracy, measured on the GPU: the same 8
+    bf16 rank buffers (N(0, 0.02^2)) all-reduced (AVG) into fp32, once with
+    fp32 partials and once with every forwarded partial rounded to bf16.
+    The fp32-partial result is within ~1e-7 relative of the exact sum, so
+    the difference is the wire's error; it is reported in bf16 ulps of the
+    fp32-partial result, next to the 0.5 ulp that rounding that result to
+    bf16 once costs."""
+    import torch
+    from fsdp_emulated_ranks_gb300 import cr
+    bufs = alloc_ranks(n, count, torch.bfloat16, 0.02, 100, device)
+    a = [torch.empty(count, dtype=torch.float32, device=device) for _ in range(n)]
+    b = [torch.empty(count, dtype=torch.float32, device=device) for _ in range(n)]
+    cr.cr_all_reduce(bufs, count, "bf16", "avg", a, "f32")
+    cr.cr_all_reduce_wire(bufs, count, "bf16", "avg", "bf16", b, "f32")
+    torch.cuda.synchronize()
+    ref, got = a[0].double(), b[0].double()
+    nz = ref != 0
+    ulp = torch.exp2(torch.floor(torch.log2(ref[nz].abs())) - 7)
+    err = ((got[nz] - ref[nz]).abs() / ulp).float()
+    q = torch.quantile(err[:1 << 20], torch.tensor([0.5, 0.99], device=device)).tolist()
+    rel_rms = float(((got - ref) ** 2).mean().sqrt() / (ref ** 2).mean().sqrt())
+    out = {"ranks": n, "elements": count, "inputs": "bf16 N(0, 0.02^2), AVG, fp32 output",
+           "bf16_ulps_median": round(q[0], 4), "bf16_ulps_p99": round(q[1], 4),
+           "bf16_ulps_max": round(float(err.max()), 4), "relative_rms": rel_rms,
+           "same_as_fp32_wire_fraction": round(float((err == 0).float().mean()), 4)}
+    del bufs, a, b
+    torch.cuda.empty_cache()
+    return out
+
+
 # ---- DDP backward / all-reduce overlap ---------------------------------------------------
 
 def run_overlap(args, device, caps=(0, 38)):
@@ -960,10 +993,11 @@ def main(argv=None):
     head, sample = run_headline(args, world, rank, device, stream, peak)
     wl = head["workload"]
     rows = None
-    overlap = None
+    overlap = wire = None
     if world == 1 and not args.no_rows:
         rows = run_rows(args, device, stream, peak, skip=args.workload)
         overlap = run_overlap(args, device)
+        wire = wire_error(device)
     cpu = None
     if sample is not None:
         gbs, secs, passes = cpu_oracle_allreduce(sample, args.cpu_seconds)
@@ -994,7 +1028,7 @@ def main(argv=None):
                 "roofline": head["roofline"], "cpu_baseline": cpu, "e2e": head["e2e"],
                 "gpu_launches": head["gpu_launches"], "clocks": head["clocks"],
                 "frac_of_peak": round(head["value"] / world / peak[0], 4),
-                "rows": rows, "ddp_overlap": overlap}
+                "rows": rows, "ddp_overlap": overlap, "wire_error": wire}
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
