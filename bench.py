@@ -753,7 +753,7 @@ def wire_error(device, n=8, count=1 << 24):
 
 # ---- DDP backward / all-reduce overlap ---------------------------------------------------
 
-def run_overlap(args, device, caps=(0, 38)):
+def run_overlap(args, device, caps=(0, 38, 304)):
     """The reducer's overlap of bucket all-reduces with backward ("AI Infra
     Guide, Chapter 6", 6.2.5): the 300-tensor bucket workload, 8 ranks; the
     emulated backward runs, per bucket, k bf16 4096^3 GEMMs (cuBLAS through
