@@ -1,0 +1,225 @@
+"""Seeded random cases for every collective, through the C ABI, against the
+oracle.  Unlike the structured parity tests, each rank's buffer gets its own
+element offset inside its allocation (0, 1, 2, 3, 8, 16, 17 ...), so a call
+mixes 32-byte, 16-byte and unaligned buffers and must take the widest path
+that all of them allow; rank counts, sizes (around vector and chunk
+boundaries), dtype pairs, ops and in-place forms are drawn too.  Same bars
+as the parity tests: fp32/int32 bit-exact, bf16 within 1 ulp."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from fsdp_emulated_ranks_gb300 import build as libbuild
+from fsdp_emulated_ranks_gb300 import cr
+from fsdp_emulated_ranks_gb300 import inputs as I
+from gpu_util import Guarded, assert_match, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+PAIRS = [("f32", "sum", "f32"), ("bf16", "avg", "bf16"), ("bf16", "avg", "f32"),
+         ("i32", "sum", "i32"), ("f32", "avg", "f32"), ("bf16", "sum", "bf16")]
+OFFSETS = [0, 0, 0, 1, 2, 3, 8, 16, 17]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    libbuild.build()
+    cr.lib()
+
+
+def draw_count(rng, n):
+    base = int(rng.choice([0, 1, 7, 16 * n, 32 * n * 5, 1000, 4099, 16 * n * 37]))
+    return max(0, base + int(rng.integers(-3, 4)))
+
+
+def host_inputs(n, count, dt, seed):
+    return I.host_rank_buffers(n, count, dt, std=0.02 if dt == "bf16" else 1.0, seed0=seed)
+
+
+def offs(rng, k, dt):
+    """Element offsets of k buffers inside their allocations (element
+    alignment always holds; 16- and 32-byte alignment only for some)."""
+    return [int(rng.choice(OFFSETS)) for _ in range(k)]
+
+
+@pytest.mark.parametrize("case", range(60))
+def test_fuzz_reduce_scatter_all_reduce(case):
+    rng = np.random.default_rng(1000 + case)
+    n = int(rng.integers(1, 13))
+    dt, op, out = PAIRS[int(rng.integers(len(PAIRS)))]
+    count = draw_count(rng, n)
+    host = host_inputs(n, count, dt, seed=case)
+    oi, oo = offs(rng, n, dt), offs(rng, n, out)
+    # reduce-scatter
+    want, _ = O.ring_reduce_scatter(host, dt, op, out)
+    bufs = [to_dev(x, dt, o) for x, o in zip(host, oi)]
+    shards = [Guarded(w.size, out, o) for w, o in zip(want, oo)]
+    cr.cr_reduce_scatter(bufs, count, dt, op, [s.ptr() for s in shards], out)
+    torch.cuda.synchronize()
+    for j in range(n):
+        shards[j].check()
+        assert_match(shards[j].host(), want[j], out, f"RS n={n} count={count} offs={oi}/{oo} j={j}")
+    # all-reduce, in place when the dtypes allow and the draw says so
+    want, _ = O.ring_all_reduce(host, dt, op, out)
+    if dt == out and rng.random() < 0.5:
+        cr.cr_all_reduce(bufs, count, dt, op, bufs, out)
+        torch.cuda.synchronize()
+        got = [to_host(b, out) for b in bufs]
+    else:
+        outs = [Guarded(count, out, o) for o in oo]
+        cr.cr_all_reduce(bufs, count, dt, op, [x.ptr() for x in outs], out)
+        torch.cuda.synchronize()
+        for x in outs:
+            x.check()
+        got = [x.host() for x in outs]
+    for r in range(n):
+        assert_match(got[r], want[r], out, f"AR n={n} count={count} offs={oi}/{oo} r={r}")
+
+
+@pytest.mark.parametrize("case", range(40))
+def test_fuzz_all_gather_and_wire(case):
+    rng = np.random.default_rng(2000 + case)
+    n = int(rng.integers(1, 13))
+    dt = ["f32", "bf16", "i32"][int(rng.integers(3))]
+    count = draw_count(rng, n)
+    shards = []
+    for j in range(n):
+        lo, hi = O.chunk_bounds(count, n, j)
+        shards.append(host_inputs(1, hi - lo, dt, seed=case * 31 + j)[0])
+    want, _ = O.ring_all_gather(shards, count, dt)
+    osh, ob = offs(rng, n, dt), offs(rng, n, dt)
+    d_sh = [to_dev(s, dt, o) if s.size else 0 for s, o in zip(shards, osh)]
+    outs = [Guarded(count, dt, o) for o in ob]
+    cr.cr_all_gather(d_sh, count, dt, [o.ptr() for o in outs])
+    torch.cuda.synchronize()
+    for r in range(n):
+        outs[r].check()
+        assert_match(outs[r].host(), want[r], dt, f"AG n={n} count={count} offs={osh}/{ob}")
+    # bf16-wire all-reduce on float inputs
+    fdt, op, fout = PAIRS[int(rng.choice([0, 1, 2, 4, 5]))]
+    host = host_inputs(n, count, fdt, seed=case + 77)
+    want = O.ring_all_reduce_wire(host, fdt, op, "bf16", fout)
+    oi, oo = offs(rng, n, fdt), offs(rng, n, fout)
+    bufs = [to_dev(x, fdt, o) for x, o in zip(host, oi)]
+    outs = [Guarded(count, fout, o) for o in oo]
+    cr.cr_all_reduce_wire(bufs, count, fdt, op, "bf16", [o.ptr() for o in outs], fout)
+    torch.cuda.synchronize()
+    for r in range(n):
+        outs[r].check()
+        assert_match(outs[r].host(), want[r], fout, f"wire n={n} count={count} offs={oi}/{oo}")
+
+
+@pytest.mark.parametrize("case", range(40))
+def test_fuzz_hsdp(case):
+    rng = np.random.default_rng(3000 + case)
+    R, S = int(rng.integers(1, 5)), int(rng.integers(1, 6))
+    n = R * S
+    dt, op, out = PAIRS[int(rng.integers(len(PAIRS)))]
+    count = draw_count(rng, S)
+    host = host_inputs(n, count, dt, seed=case * 7)
+    want = O.hsdp_reduce_scatter(host, R, S, dt, op, out)
+    oi, oo = offs(rng, n, dt), offs(rng, n, out)
+    bufs = [to_dev(x, dt, o) for x, o in zip(host, oi)]
+    shards = [Guarded(w.size, out, o) for w, o in zip(want, oo)]
+    cr.cr_hsdp_reduce_scatter(bufs, R, S, count, dt, op, [s.ptr() for s in shards], out)
+    torch.cuda.synchronize()
+    for q in range(n):
+        shards[q].check()
+        assert_match(shards[q].host(), want[q], out, f"{R}x{S} count={count} offs={oi}/{oo} q={q}")
+
+
+@pytest.mark.parametrize("case", range(30))
+def test_fuzz_fused_buckets_and_accumulate(case):
+    rng = np.random.default_rng(4000 + case)
+    n = int(rng.integers(1, 9))
+    dt = ["bf16", "f32"][int(rng.integers(2))]
+    es = 2 if dt == "bf16" else 4
+    T = int(rng.integers(1, 25))
+    numels = [int(x) for x in rng.integers(0, 3000, T)]
+    cap = int(rng.integers(64, 20000))
+    plan = cr.cr_bucket_plan(numels, es, cap)
+    oplan = O.bucket_plan(numels, es, cap)
+    host = [[host_inputs(1, k, dt, seed=case * 1000 + r * 50 + t)[0] for t, k in enumerate(numels)]
+            for r in range(n)]
+    want = O.bucketed_all_reduce(oplan, host, dt, "avg")
+    ot = offs(rng, n * T, dt)
+    dev_t = [to_dev(host[r][t], dt, ot[r * T + t]) if numels[t] else 0
+             for r in range(n) for t in range(T)]
+    cr.cr_bucket_all_reduce_fused(plan, n, dev_t, dt, "avg")
+    torch.cuda.synchronize()
+    for r in range(n):
+        for t in range(T):
+            if numels[t]:
+                assert_match(to_host(dev_t[r * T + t], dt), want[r][t], dt,
+                             f"fused n={n} T={T} cap={cap} r={r} t={t}")
+    # fused accumulate + all-reduce: fp32 accumulators, grads of dt
+    count = draw_count(rng, n)
+    acc = host_inputs(n, count, "f32", seed=case + 5)
+    g = host_inputs(n, count, dt, seed=case + 9)
+    sums = [a.copy() for a in acc]
+    for a, x in zip(sums, g):
+        O.accumulate(a, x, dt)
+    want, _ = O.ring_all_reduce(sums, "f32", "sum")
+    oa, og = offs(rng, n, "f32"), offs(rng, n, dt)
+    d_acc = [to_dev(x, "f32", o) for x, o in zip(acc, oa)]
+    d_g = [to_dev(x, dt, o) for x, o in zip(g, og)]
+    cr.cr_all_reduce_accumulate(d_acc, count, d_g, dt, "sum")
+    torch.cuda.synchronize()
+    for r in range(n):
+        assert_match(to_host(d_acc[r], "f32"), want[r], "f32", f"acc n={n} count={count} offs={oa}/{og}")
+
+
+def rel_maxabs(got, want):
+    d = np.max(np.abs(got.astype(np.float64) - want.astype(np.float64))) if got.size else 0.0
+    s = np.max(np.abs(want.astype(np.float64))) if want.size else 0.0
+    return d / s if s else d
+
+
+@pytest.mark.parametrize("case", range(30))
+def test_fuzz_fsdp_step(case):
+    """FSDP step, plain or clipped, with every grad, param and state buffer
+    at its own offset; two consecutive steps (t = 1, 2)."""
+    rng = np.random.default_rng(5000 + case)
+    n = int(rng.integers(1, 11))
+    count = draw_count(rng, n)
+    clipped = bool(rng.random() < 0.5)
+    grads0 = I.host_rank_buffers(n, count, "bf16", std=1e-3, seed0=case)
+    master_full = I.np_normal_f32(count, 0.02, 77 + case)
+    bounds = [O.chunk_bounds(count, n, j) for j in range(n)]
+    master = [master_full[a:b].copy() for a, b in bounds]
+    m = [np.zeros(b - a, np.float32) for a, b in bounds]
+    v = [np.zeros(b - a, np.float32) for a, b in bounds]
+    ostate = offs(rng, 3 * n, "f32")
+    d_state = [Guarded(x.size, "f32", o) for x, o in zip(master + m + v, ostate)]
+    for gg, x in zip(d_state, master + m + v):
+        if x.size:
+            gg.view.copy_(to_dev(x, "f32"))
+    d_master, d_m, d_v = d_state[:n], d_state[n:2 * n], d_state[2 * n:]
+    d_p = [Guarded(count, "bf16", o) for o in offs(rng, n, "bf16")]
+    ws = torch.empty(cr.cr_fsdp_clip_workspace_bytes() // 8, dtype=torch.float64, device="cuda")
+    max_norm = 1e-3
+    for step in (1, 2):
+        grads = grads0 if step == 1 else I.host_rank_buffers(n, count, "bf16", std=1e-3,
+                                                             seed0=case + 500)
+        d_g = [to_dev(x, "bf16", o) for x, o in zip(grads, offs(rng, n, "bf16"))]
+        cfg = O.AdamWConfig(step=step)
+        if clipped:
+            want_p, _ = O.fsdp_step_clipped(grads, master, m, v, cfg, max_norm)
+            cr.cr_fsdp_step_clipped(d_g, count, [x.ptr() for x in d_master], [x.ptr() for x in d_m],
+                                    [x.ptr() for x in d_v], cr.adamw_cfg(step=step), max_norm, ws,
+                                    ws.numel() * 8, [x.ptr() for x in d_p], None)
+        else:
+            want_p = O.fsdp_step(grads, master, m, v, cfg)
+            cr.cr_fsdp_step(d_g, count, [x.ptr() for x in d_master], [x.ptr() for x in d_m],
+                            [x.ptr() for x in d_v], cr.adamw_cfg(step=step), [x.ptr() for x in d_p])
+        torch.cuda.synchronize()
+        for j in range(n):
+            for gg, ref, name in ((d_master, master, "master"), (d_m, m, "m"), (d_v, v, "v")):
+                gg[j].check()
+                assert rel_maxabs(gg[j].host(), ref[j]) <= 1e-6, f"{name}[{j}] step {step}"
+        for r in range(n):
+            d_p[r].check()
+            assert_match(d_p[r].host(), want_p[r], "bf16", f"n={n} count={count} params[{r}]")
