@@ -54,11 +54,16 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
-def init_dist(world, backend):
+def init_dist(world, backend, timeout_s=600):
+    """Process group of the N > 1 run.  Its timeout bounds every barrier and
+    collective: a rank that dies or never arrives makes the others fail with
+    an error after at most timeout_s instead of waiting forever."""
+    import datetime
     import torch.distributed as dist
     if world > 1 and not dist.is_initialized():
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-        dist.init_process_group(backend=backend)
+        dist.init_process_group(backend=backend,
+                                timeout=datetime.timedelta(seconds=timeout_s))
     return dist
 
 
@@ -945,6 +950,9 @@ def main(argv=None):
     ap.add_argument("--fsdp2-layers", type=int, default=24,
                     help="transformer layers of the fsdp2 workload (1.27e9 parameters at 24)")
     ap.add_argument("--fsdp2-hidden", type=int, default=2048)
+    ap.add_argument("--pg-timeout", type=int, default=600,
+                    help="seconds after which a barrier or collective of an N > 1 run fails "
+                         "when a rank is missing")
     ap.add_argument("--no-rows", action="store_true")
     ap.add_argument("--skip-fsdp", action="store_true")
     ap.add_argument("--row-steps", type=int, default=20)
@@ -974,7 +982,7 @@ def main(argv=None):
         raise SystemExit("bench.py needs a CUDA device (libcr has no CPU path)")
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    init_dist(world, "nccl")
+    init_dist(world, "nccl", args.pg_timeout)
     if rank == 0:
         B.build()
     barrier(world)

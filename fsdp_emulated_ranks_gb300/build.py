@@ -26,7 +26,7 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "--expt-relaxed-constexpr", "-I" + INCLUDE, "-I" + CSRC]
 SOURCES = ["api.cu", "launch_util.cu", "k_collectives.cu", "k_fsdp.cu",
            "k_bucket.cu", "k_bucket_fused.cu", "k_fsdp2.cu", "k_accum.cu",
-           "k_hsdp.cu", "reducer.cu", "fsdp_noalloc.cu", "plan.cpp"]
+           "k_hsdp.cu", "reducer.cu", "fsdp_noalloc.cu", "plan.cpp", "comm.cpp"]
 
 
 def nvcc() -> str:

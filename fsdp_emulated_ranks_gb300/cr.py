@@ -38,7 +38,9 @@ EXPORTS = ["cr_status_string", "cr_last_error", "cr_version", "cr_chunk_len",
            "cr_all_reduce_accumulate", "cr_adamw_step", "cr_comm_elems",
            "cr_reduce_scatter_wire", "cr_all_reduce_wire",
            "cr_hsdp_reduce_scatter", "cr_reducer_create", "cr_reducer_mark_ready",
-           "cr_reducer_launched", "cr_reducer_finalize", "cr_reducer_destroy"]
+           "cr_reducer_launched", "cr_reducer_finalize", "cr_reducer_destroy",
+           "cr_comm_create", "cr_comm_all_reduce", "cr_comm_reduce_scatter",
+           "cr_comm_all_gather", "cr_comm_broken", "cr_comm_destroy"]
 
 _lib = None
 
@@ -80,6 +82,7 @@ def lib() -> C.CDLL:
     L = C.CDLL(LIB_PATH)
     vp, sz, i = C.c_void_p, C.c_size_t, C.c_int
     L.cr_reducer_destroy.restype = None
+    L.cr_comm_destroy.restype = None
     L.cr_status_string.restype = C.c_char_p
     L.cr_status_string.argtypes = [i]
     L.cr_last_error.restype = C.c_char_p
@@ -101,6 +104,12 @@ def lib() -> C.CDLL:
     L.cr_reducer_launched.restype = i
     L.cr_reducer_finalize.argtypes = [vp, vp]
     L.cr_reducer_destroy.argtypes = [vp]
+    L.cr_comm_create.argtypes = [i, i, vp, C.POINTER(vp)]
+    L.cr_comm_all_reduce.argtypes = [vp, i, vp, sz, i, i]
+    L.cr_comm_reduce_scatter.argtypes = [vp, i, vp, vp, sz, i, i, i]
+    L.cr_comm_all_gather.argtypes = [vp, i, vp, vp, sz, i]
+    L.cr_comm_broken.argtypes = [vp]
+    L.cr_comm_destroy.argtypes = [vp]
     L.cr_all_reduce_host.argtypes = [vp, vp, vp, i, sz, i, i, vp]
     L.cr_all_reduce_staged.argtypes = [vp, vp, vp, i, sz, i, i, sz, vp, vp, vp]
     L.cr_bucket_plan.argtypes = [vp, i, sz, sz, C.POINTER(C.POINTER(BucketPlanT))]
@@ -385,6 +394,57 @@ def cr_reducer_destroy(red: Reducer) -> None:
     if red.ptr:
         lib().cr_reducer_destroy(red.ptr)
         red._ptr = None
+
+
+class Comm:
+    """Owns a cr_comm_t: N emulated ranks, one host thread each (ctypes
+    releases the GIL during the blocking calls)."""
+
+    def __init__(self, ptr: int):
+        self._ptr = ptr
+
+    @property
+    def ptr(self):
+        return self._ptr
+
+    def __del__(self):
+        if getattr(self, "_ptr", None) and _lib is not None:
+            _lib.cr_comm_destroy(self._ptr)
+            self._ptr = None
+
+
+def cr_comm_create(nranks: int, timeout_ms: int, stream=None) -> Comm:
+    out = C.c_void_p()
+    _check(lib().cr_comm_create(nranks, timeout_ms, _stream(stream), C.byref(out)),
+           "cr_comm_create")
+    return Comm(out.value)
+
+
+def cr_comm_all_reduce(comm: Comm, rank: int, buf, count, dtype, op) -> None:
+    _check(lib().cr_comm_all_reduce(comm.ptr, rank, _ptr(buf), count, _dtype(dtype), _op(op)),
+           "cr_comm_all_reduce")
+
+
+def cr_comm_reduce_scatter(comm: Comm, rank: int, buf, shard, count, in_dtype, op,
+                           out_dtype) -> None:
+    _check(lib().cr_comm_reduce_scatter(comm.ptr, rank, _ptr(buf), _ptr(shard), count,
+                                        _dtype(in_dtype), _op(op), _dtype(out_dtype)),
+           "cr_comm_reduce_scatter")
+
+
+def cr_comm_all_gather(comm: Comm, rank: int, shard, buf, count, dtype) -> None:
+    _check(lib().cr_comm_all_gather(comm.ptr, rank, _ptr(shard), _ptr(buf), count,
+                                    _dtype(dtype)), "cr_comm_all_gather")
+
+
+def cr_comm_broken(comm: Comm) -> int:
+    return lib().cr_comm_broken(comm.ptr)
+
+
+def cr_comm_destroy(comm: Comm) -> None:
+    if comm.ptr:
+        lib().cr_comm_destroy(comm.ptr)
+        comm._ptr = None
 
 
 def adamw_cfg(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01,

@@ -23,8 +23,9 @@
  *    parameters, so the host arrays may be reused as soon as the call returns.
  *  - The caller owns every device buffer.  No entry point allocates device
  *    memory; apart from cr_bucket_plan (the host-side plan the caller
- *    releases with cr_bucket_plan_free) and cr_reducer_create (a host object
- *    and CUDA events, released with cr_reducer_destroy) nothing allocates at
+ *    releases with cr_bucket_plan_free), cr_reducer_create (a host object
+ *    and CUDA events, released with cr_reducer_destroy) and cr_comm_create
+ *    (a host object, released with cr_comm_destroy) nothing allocates at
  *    all, and the library keeps no state between calls beyond cached device
  *    attributes.
  *  - Every launching call is asynchronous on `stream` (NULL = the legacy
@@ -346,6 +347,47 @@ cr_status cr_reducer_mark_ready(cr_reducer_t* red, int tensor,
 int cr_reducer_launched(const cr_reducer_t* red);
 cr_status cr_reducer_finalize(cr_reducer_t* red, cr_stream_t compute_stream);
 void cr_reducer_destroy(cr_reducer_t* red);
+
+/* ---- thread-per-rank communicator --------------------------------------------
+ * [DT] section 2 and [AIG] 6.1: with real ranks, every rank calls a
+ * collective on its own tensor and the collective runs once all ranks have
+ * called it.  cr_comm_t gives the emulated ranks that form: each rank's host
+ * thread calls cr_comm_<collective>(comm, rank, its buffers...) and blocks
+ * until all nranks ranks have joined the same collective; the last to
+ * arrive checks that all calls agree (collective, count, dtypes, op) and
+ * enqueues the single-kernel collective (cr_all_reduce in place,
+ * cr_reduce_scatter, cr_all_gather) over the N ranks' buffers on the
+ * communicator's stream.  Every rank then returns that call's status; the
+ * work is asynchronous on the stream, as with NCCL.
+ * Failures ([AIG] 6.8 and the pages' troubleshooting notes: the NCCL timeout
+ * and watchdog, hangs from mismatched calls), decided on the host before
+ * any launch:
+ *  - a rank that does not join within timeout_ms: every waiting rank returns
+ *    CR_ERR_TIMEOUT, nothing is launched, and the communicator is broken --
+ *    every later call returns CR_ERR_TIMEOUT at once (cr_comm_broken
+ *    reports 1); destroy it, as an aborted NCCL communicator;
+ *  - calls that disagree: every rank returns CR_ERR_INVALID_ARG, nothing is
+ *    launched, and the next collective may be joined;
+ *  - rank outside [0, nranks), or a rank joining the same collective twice:
+ *    CR_ERR_INVALID_ARG for that call.
+ * The argument checks of the underlying entry point (alignment, overlaps)
+ * apply at launch and their status is returned to every rank.  Buffers are
+ * device pointers owned by the caller.  cr_comm_create allocates a host
+ * object (no CUDA call); cr_comm_destroy releases it (no rank may be inside
+ * a call). */
+typedef struct cr_comm cr_comm_t;
+
+cr_status cr_comm_create(int nranks, int timeout_ms, cr_stream_t stream,
+                         cr_comm_t** out);
+cr_status cr_comm_all_reduce(cr_comm_t* comm, int rank, void* buf,
+                             size_t count, cr_dtype dtype, cr_op op);
+cr_status cr_comm_reduce_scatter(cr_comm_t* comm, int rank, const void* buf,
+                                 void* shard, size_t count, cr_dtype in_dtype,
+                                 cr_op op, cr_dtype out_dtype);
+cr_status cr_comm_all_gather(cr_comm_t* comm, int rank, const void* shard,
+                             void* buf, size_t count, cr_dtype dtype);
+int cr_comm_broken(const cr_comm_t* comm);
+void cr_comm_destroy(cr_comm_t* comm);
 
 /* ---- a8..a10: fused FSDP / ZeRO-3 step ------------------------------------
  * One kernel performs the step of [DT] section 4 (ZeRO-3/FSDP flow steps

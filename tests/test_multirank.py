@@ -44,3 +44,33 @@ def test_two_rank_timing_uses_slowest_rank():
         assert ms == pytest.approx(slowest_ms)
         assert gbs == pytest.approx(world * 1e9 / (slowest_ms * 1e-3) / 1e9)
         assert mx == world - 1
+
+
+def _worker_one_dies(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE=str(world),
+                      RANK=str(rank), LOCAL_RANK=str(rank))
+    import time
+    import bench
+    bench.init_dist(world, "gloo", timeout_s=5)
+    if rank == 1:
+        os._exit(0)          # the rank dies between steps, without a word
+    t0 = time.monotonic()
+    try:
+        bench.barrier(world)
+        out[rank] = ("no error", time.monotonic() - t0)
+    except Exception as e:   # the survivor learns of it from the process group
+        out[rank] = (type(e).__name__, time.monotonic() - t0)
+
+
+def test_dead_rank_fails_the_barrier_instead_of_hanging():
+    """A rank that exits between steps: the other rank's next barrier fails
+    with an error within the process-group timeout (5 s here), so an N > 1
+    benchmark run ends instead of waiting forever."""
+    world = 2
+    port = _free_port()
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_worker_one_dies, args=(world, port, out), nprocs=world, join=True)
+    kind, secs = out[0]
+    assert kind != "no error"
+    assert secs < 20.0
