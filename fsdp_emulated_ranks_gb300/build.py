@@ -20,13 +20,18 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libcr.so")
+# The checked variant (device-side index checks, csrc/check.cuh), for tests.
+CHECKED_DIR = os.path.join(PKG, "_build_checked")
+CHECKED_LIB_PATH = os.path.join(CHECKED_DIR, "libcr.so")
+CHECKED_FLAGS = ["-DCR_DEVICE_CHECKS", "-rdc=true"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "--expt-relaxed-constexpr", "-I" + INCLUDE, "-I" + CSRC]
 SOURCES = ["api.cu", "launch_util.cu", "k_collectives.cu", "k_fsdp.cu",
            "k_bucket.cu", "k_bucket_fused.cu", "k_fsdp2.cu", "k_accum.cu",
-           "k_hsdp.cu", "reducer.cu", "fsdp_noalloc.cu", "plan.cpp", "comm.cpp"]
+           "k_hsdp.cu", "reducer.cu", "fsdp_noalloc.cu", "check.cu", "plan.cpp",
+           "comm.cpp"]
 
 
 def nvcc() -> str:
@@ -87,20 +92,26 @@ def kernel_hash(tu: str) -> str:
     return h.hexdigest()[:16]
 
 
-def _stamp() -> str:
-    return os.path.join(BUILD_DIR, "libcr.hash")
+def _dir(checked: bool) -> str:
+    return CHECKED_DIR if checked else BUILD_DIR
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH) or not os.path.exists(_stamp()):
+def _stamp(checked: bool = False) -> str:
+    return os.path.join(_dir(checked), "libcr.hash")
+
+
+def up_to_date(checked: bool = False) -> bool:
+    lib = CHECKED_LIB_PATH if checked else LIB_PATH
+    if not os.path.exists(lib) or not os.path.exists(_stamp(checked)):
         return False
-    with open(_stamp()) as f:
+    with open(_stamp(checked)) as f:
         return f.read().strip() == source_hash()
 
 
-def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
-    cmd = [nvcc()] + ARCH + NVCC_FLAGS + ["-c", src, "-o", obj]
+def _compile(src: str, verbose_ptxas: bool, checked: bool) -> str:
+    obj = os.path.join(_dir(checked), os.path.basename(src) + ".o")
+    extra = CHECKED_FLAGS if checked else []
+    cmd = [nvcc()] + ARCH + NVCC_FLAGS + extra + ["-c", src, "-o", obj]
     if src.endswith(".cpp"):
         cmd = [nvcc()] + ["-x", "c++"] + NVCC_FLAGS + ["-c", src, "-o", obj]
     elif verbose_ptxas:
@@ -113,23 +124,27 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile libcr.so if it is missing or stale; return its path."""
-    if not force and up_to_date():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, checked: bool = False) -> str:
+    """Compile libcr.so if it is missing or stale; return its path.
+    checked=True builds the variant with device-side index checks into its
+    own directory (tests only)."""
+    lib = CHECKED_LIB_PATH if checked else LIB_PATH
+    if not force and up_to_date(checked):
+        return lib
+    os.makedirs(_dir(checked), exist_ok=True)
     srcs = [os.path.join(CSRC, s) for s in SOURCES]
     with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), srcs))
-    tmp = LIB_PATH + ".tmp.%d" % os.getpid()
-    cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
+        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas, checked), srcs))
+    tmp = lib + ".tmp.%d" % os.getpid()
+    extra = ["-rdc=true"] if checked else []
+    cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static"] + extra + ["-o", tmp] + objs
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB_PATH)
-    with open(_stamp(), "w") as f:
+    os.replace(tmp, lib)
+    with open(_stamp(checked), "w") as f:
         f.write(source_hash())
-    return LIB_PATH
+    return lib
 
 
 if __name__ == "__main__":

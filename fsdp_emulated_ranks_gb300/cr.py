@@ -14,6 +14,9 @@ from typing import Sequence
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "_build", "libcr.so")
+# CR_LIBRARY=<path> loads another build of the library (the tests' checked
+# variant, with device-side index checks).
+LIB_PATH = os.environ.get("CR_LIBRARY", LIB_PATH)
 MAX_RANKS = 64
 
 F32, BF16, I32 = 0, 1, 2
@@ -40,7 +43,8 @@ EXPORTS = ["cr_status_string", "cr_last_error", "cr_version", "cr_chunk_len",
            "cr_hsdp_reduce_scatter", "cr_reducer_create", "cr_reducer_mark_ready",
            "cr_reducer_launched", "cr_reducer_finalize", "cr_reducer_destroy",
            "cr_comm_create", "cr_comm_all_reduce", "cr_comm_reduce_scatter",
-           "cr_comm_all_gather", "cr_comm_broken", "cr_comm_destroy"]
+           "cr_comm_all_gather", "cr_comm_broken", "cr_comm_destroy",
+           "cr_check_word", "cr_check_selftest"]
 
 _lib = None
 
@@ -110,6 +114,9 @@ def lib() -> C.CDLL:
     L.cr_comm_all_gather.argtypes = [vp, i, vp, vp, sz, i]
     L.cr_comm_broken.argtypes = [vp]
     L.cr_comm_destroy.argtypes = [vp]
+    L.cr_check_word.argtypes = [i]
+    L.cr_check_word.restype = C.c_longlong
+    L.cr_check_selftest.argtypes = [vp]
     L.cr_all_reduce_host.argtypes = [vp, vp, vp, i, sz, i, i, vp]
     L.cr_all_reduce_staged.argtypes = [vp, vp, vp, i, sz, i, i, sz, vp, vp, vp]
     L.cr_bucket_plan.argtypes = [vp, i, sz, sz, C.POINTER(C.POINTER(BucketPlanT))]
@@ -445,6 +452,16 @@ def cr_comm_destroy(comm: Comm) -> None:
     if comm.ptr:
         lib().cr_comm_destroy(comm.ptr)
         comm._ptr = None
+
+
+def cr_check_word(clear: bool = False) -> int:
+    """Device error word of the checked build (-1: this build has no device
+    checks; -2: reading it failed)."""
+    return lib().cr_check_word(1 if clear else 0)
+
+
+def cr_check_selftest(stream=None) -> None:
+    _check(lib().cr_check_selftest(_stream(stream)), "cr_check_selftest")
 
 
 def adamw_cfg(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01,

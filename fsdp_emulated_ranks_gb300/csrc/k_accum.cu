@@ -10,6 +10,7 @@
 // written back to every rank's accumulator -- the result of accumulating
 // and then all-reducing, bit for bit, without writing and re-reading the
 // accumulators in between.
+#include "check.cuh"
 #include "cr_internal.cuh"
 #include "fold.cuh"
 
@@ -72,6 +73,7 @@ __device__ __forceinline__ void accum_elem(const AccumArgs& a, int n, uint64_t e
     return;
   }
   const int j = (int)fastdiv_div(a.Ld, e);
+  CR_DCHECK(e < a.count && (uint64_t)j == e / a.L && j < n, kChkAccum);
   int r = (j + 1 == n) ? 0 : j + 1;
   float sum = __fadd_rn(a.acc[r][e], grad_elem<GD>(a.grads[r], e));
   for (int k = 1; k < n; ++k) {
@@ -113,6 +115,7 @@ __global__ void __launch_bounds__(kBlock)
       continue;
     }
     const int j = (int)j64;
+    CR_DCHECK(e0 + 8 <= a.count && j64 == e0 / a.L && j < n, kChkAccum);
     int r = (j + 1 == n) ? 0 : j + 1;
     float sum[8];
 #pragma unroll

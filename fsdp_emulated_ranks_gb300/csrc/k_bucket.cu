@@ -15,6 +15,7 @@
 // shift; both granules hold bytes of the range, so no load leaves it.  The
 // unaligned head and tail bytes of the destination (< 16 each) are copied
 // one byte at a time by the range's first tile.
+#include "check.cuh"
 #include "cr_internal.cuh"
 #include "fold.cuh"
 #include "pdl.cuh"
@@ -61,6 +62,7 @@ __global__ void __launch_bounds__(kBlock)
       if (a.tile_start[mid] <= t) lo = mid;
       else hi = mid;
     }
+    CR_DCHECK(lo < a.nseg && a.tile_start[lo] <= t && t < a.tile_start[lo + 1], kChkCopy);
     const CopySeg sg = a.seg[lo];
     const uint32_t tile = t - a.tile_start[lo];
     const uintptr_t d0 = reinterpret_cast<uintptr_t>(sg.dst);
@@ -106,6 +108,8 @@ __global__ void __launch_bounds__(kBlock)
       for (int k = 0; k < kVecPerThread; ++k) {
         const uint64_t i = v0 + (uint64_t)k * kBlock + threadIdx.x;
         if (i < nint) {
+          // both granules hold bytes of the source range
+          CR_DCHECK(sa + i * 16 + 16 < sg.src + sg.bytes && sa + i * 16 + 16 > sg.src, kChkCopy);
           lo_v[k] = ld16_ro(sa + i * 16);
           hi_v[k] = ld16_ro(sa + i * 16 + 16);
         }

@@ -16,6 +16,7 @@
 // (kFusedMaxPtrs in all) travel in the __grid_constant__ parameter block;
 // each CTA takes one tile of kFusedTileElems elements of one tensor, in
 // 32-byte vectors when all of that tensor's rank pointers allow it.
+#include "check.cuh"
 #include "cr_internal.cuh"
 #include "fold.cuh"
 #include "pdl.cuh"
@@ -28,6 +29,7 @@ __device__ __forceinline__ void fused_elem(const FusedArgs& a, const FusedTensor
   using Acc = typename Elem<D>::Acc;
   const int n = a.n;
   const int j = (int)fastdiv_div(t.Lbd, t.off + i);
+  CR_DCHECK(i < t.numel && (uint64_t)j == (t.off + i) / t.Lb && j < n, kChkFused);
   int r = (j + 1 == n) ? 0 : j + 1;
   Acc acc = ld_elem<D>(a.ptrs[t.ptr0 + r], i);
   for (int k = 1; k < n; ++k) {
@@ -58,6 +60,7 @@ __device__ __forceinline__ void fused_tile(const FusedArgs& a, const FusedTensor
       for (int q = 0; q < VEC; ++q) fused_elem<D>(a, t, e0 + q);
       continue;
     }
+    CR_DCHECK(e0 + VEC <= t.numel && j64 == p0 / t.Lb && j64 < (uint64_t)n, kChkFused);
     Acc acc[VEC];
     fold_vec<D, NT, NW>(a.ptrs + t.ptr0, n, (int)j64, e0 * IS, acc);
     if constexpr (D != CR_I32) {
@@ -90,6 +93,7 @@ __global__ void __launch_bounds__(kBlock)
       if (a.tile_start[mid] <= tile) lo = mid;
       else hi = mid;
     }
+    CR_DCHECK(lo < a.ntens && a.tile_start[lo] <= tile && tile < a.tile_start[lo + 1], kChkFused);
     const FusedTensor& t = a.t[lo];
     const uint64_t e_lo = (uint64_t)(tile - a.tile_start[lo]) * kFusedTileElems;
     const uint64_t e_hi = e_lo + kFusedTileElems < t.numel ? e_lo + kFusedTileElems : t.numel;

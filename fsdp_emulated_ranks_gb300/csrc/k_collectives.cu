@@ -22,6 +22,7 @@
 // element-wise kernels.
 #include <type_traits>
 
+#include "check.cuh"
 #include "cr_internal.cuh"
 #include "fold.cuh"
 
@@ -32,6 +33,7 @@ template <int DI, int DO, int MODE, bool WIRE>
 __device__ __forceinline__ void fold_store_elem(const FoldArgs& a, int n, uint64_t e) {
   using Acc = typename Elem<DI>::Acc;
   const int j = (int)(fastdiv_div(a.Ld, e));
+  CR_DCHECK(e < a.count && (uint64_t)j == e / a.L && j < n, kChkFoldChunk);
   Acc x = fold_elem<DI, WIRE>(a.in, n, j, e);
   if constexpr (DI != CR_I32) {
     if (a.avg) x = finish_avg(x, n, a.inv_n);
@@ -64,6 +66,9 @@ __global__ void __launch_bounds__(kBlock)
     const uint64_t e0 = iv * VEC;
     const uint64_t j64 = fastdiv_div(a.Ld, e0);
     const int j = (int)j64;
+    CR_DCHECK(e0 + VEC <= a.end && j64 == e0 / a.L && j < n, kChkFoldChunk);
+    // The reduce-scatter takes vectors only when L is a multiple of VEC.
+    CR_DCHECK(MODE == kAR || e0 + VEC <= (j64 + 1) * a.L, kChkFoldShard);
     if (MODE == kAR && e0 + VEC > (j64 + 1) * a.L) {
       // The vector straddles a chunk boundary (L % VEC != 0): each element
       // takes its own chunk's ring order.
@@ -124,6 +129,8 @@ __global__ void __launch_bounds__(kBlock)
     const uint64_t e0 = iv * VEC;
     const uint64_t j64 = fastdiv_div(a.Ld, e0);
     const int j = (int)j64;
+    CR_DCHECK(j64 == e0 / a.L && j < n && e0 + VEC <= (j64 + 1) * a.L && e0 + VEC <= a.count,
+              kChkGather);
     const Words<NW> v = ldv<NW>(static_cast<const unsigned char*>(a.shards[j]) +
                                 (e0 - j64 * a.L) * ES);
     const bool skip_own = (a.inplace_mask >> j) & 1ull;
@@ -136,6 +143,7 @@ __global__ void __launch_bounds__(kBlock)
   if (e < a.count) {
     const uint64_t j64 = fastdiv_div(a.Ld, e);
     const int j = (int)j64;
+    CR_DCHECK(j64 == e / a.L && j < n, kChkGather);
     const unsigned char* src =
         static_cast<const unsigned char*>(a.shards[j]) + (e - j64 * a.L) * ES;
     const bool skip_own = (a.inplace_mask >> j) & 1ull;
@@ -157,6 +165,7 @@ __global__ void __launch_bounds__(kBlock)
        e < a.count; e += stride) {
     const uint64_t j64 = fastdiv_div(a.Ld, e);
     const int j = (int)j64;
+    CR_DCHECK(j64 == e / a.L && j < a.n, kChkGather);
     const W x = static_cast<const W*>(a.shards[j])[e - j64 * a.L];
     const bool skip_own = (a.inplace_mask >> j) & 1ull;
     for (int r = 0; r < a.n; ++r) {

@@ -17,6 +17,7 @@
 // AdamW uses only correctly rounded fp32 operations (__fmul_rn & co. are
 // never contracted into FMAs), in the order of the textbook decoupled-
 // weight-decay rule stated in include/cr.h.
+#include "check.cuh"
 #include "cr_internal.cuh"
 #include "fold.cuh"
 #include "fsdp_body.cuh"
@@ -107,21 +108,30 @@ __global__ void __launch_bounds__(kBlock, 4)
   const uint64_t nvec = a.count / 8;
   const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-  for (uint64_t iv = tid; iv < nvec; iv += stride)
+  for (uint64_t iv = tid; iv < nvec; iv += stride) {
+    // the 8 elements lie in one shard, inside that shard's length
+    CR_DCHECK(fastdiv_div(a.Ld, iv * 8) == iv * 8 / a.L && iv * 8 / a.L < (uint64_t)n &&
+                  iv * 8 % a.L + 8 <= a.L && iv * 8 + 8 <= a.count,
+              kChkFsdp);
     fsdp_vector<NT, SW>(a.grads, a.params, a.master, a.m, a.v, n, a.L, a.Ld, a.inv_n, a.a, coef,
                         iv * 8);
+  }
   // Ragged tail (count % 8 elements).
   const uint64_t e = nvec * 8 + tid;
-  if (e < a.count)
+  if (e < a.count) {
+    CR_DCHECK(fastdiv_div(a.Ld, e) == e / a.L && e / a.L < (uint64_t)n, kChkFsdp);
     fsdp_element(a.grads, a.params, a.master, a.m, a.v, n, a.L, a.Ld, a.inv_n, a.a, coef, e);
+  }
 }
 
 __global__ void __launch_bounds__(kBlock)
     k_fsdp_elem(const __grid_constant__ FsdpArgs a) {
   const float coef = clip_coef(a);
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-  for (uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; e < a.count; e += stride)
+  for (uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; e < a.count; e += stride) {
+    CR_DCHECK(fastdiv_div(a.Ld, e) == e / a.L && e / a.L < (uint64_t)a.n, kChkFsdp);
     fsdp_element(a.grads, a.params, a.master, a.m, a.v, a.n, a.L, a.Ld, a.inv_n, a.a, coef, e);
+  }
 }
 
 // ---- stand-alone AdamW on an fp32 shard ------------------------------------

@@ -10,6 +10,7 @@
 // to kFsdp2MaxParams parameters, whose 5N pointers travel in the
 // __grid_constant__ parameter block.  Each CTA takes one tile of
 // kFsdp2TileElems elements of one parameter.
+#include "check.cuh"
 #include "cr_internal.cuh"
 #include "fold.cuh"
 #include "fsdp_body.cuh"
@@ -29,6 +30,8 @@ __global__ void __launch_bounds__(kBlock)
       if (a.tile_start[mid] <= tile) lo = mid;
       else hi = mid;
     }
+    CR_DCHECK(lo < a.nparams && a.tile_start[lo] <= tile && tile < a.tile_start[lo + 1],
+              kChkFsdp2);
     const Fsdp2Param& p = a.p[lo];
     const void* const* grads = a.ptrs + p.ptr0;
     void* const* params = a.ptrs + p.ptr0 + n;
@@ -40,6 +43,9 @@ __global__ void __launch_bounds__(kBlock)
     if (p.vw) {
       const uint64_t v_hi = e_hi / 8;  // e_lo is a multiple of 8
       for (uint64_t iv = e_lo / 8 + threadIdx.x; iv < v_hi; iv += kBlock) {
+        CR_DCHECK(fastdiv_div(p.Ld, iv * 8) == iv * 8 / p.L && iv * 8 / p.L < (uint64_t)n &&
+                      iv * 8 % p.L + 8 <= p.L && iv * 8 + 8 <= p.numel,
+                  kChkFsdp2);
         if (p.vw == 32)
           fsdp_vector<NT, 8>(grads, params, master, m, v, n, p.L, p.Ld, a.inv_n, a.a, 1.0f, iv * 8);
         else

@@ -19,6 +19,7 @@
 // AVG (one division by N) and the output cast, stored at k in every
 // group's shard j.  Each element is read once from every rank and written
 // once per group: N*in + R*out bytes, the roofline bound of this pass.
+#include "check.cuh"
 #include "cr_internal.cuh"
 #include "fold.cuh"
 
@@ -35,6 +36,9 @@ __device__ __forceinline__ void hsdp_elem(const HsdpArgs& a, int R, int S, uint6
   const uint64_t j = fastdiv_div(a.Ld, e);
   const uint64_t k = e - j * a.L;
   const int i = (int)hsdp_outer_chunk(a, j, k);
+  CR_DCHECK(e < a.count && j == e / a.L && j < (uint64_t)S && i < R &&
+                (uint64_t)i == k / (j == a.jlast ? a.L2last : a.L2),
+            kChkHsdp);
   int g = (i + 1 == R) ? 0 : i + 1;
   Acc acc = fold_elem<DI>(a.in + g * S, S, (int)j, e);
   for (int q = 1; q < R; ++q) {
@@ -76,6 +80,9 @@ __global__ void __launch_bounds__(kBlock, 4)
       for (int q = 0; q < VEC; ++q) hsdp_elem<DI, DO>(a, R, S, e0 + q);
       continue;
     }
+    CR_DCHECK(e0 + VEC <= a.count && j == e0 / a.L && j < (uint64_t)S && i < (uint64_t)R &&
+                  i == k0 / L2,
+              kChkHsdp);
     Acc acc[VEC], part[VEC];
     int g = ((int)i + 1 == R) ? 0 : (int)i + 1;
     fold_vec<DI, ST, NW>(a.in + g * S, S, (int)j, e0 * IS, acc);

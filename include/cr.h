@@ -532,6 +532,20 @@ cr_status cr_adamw_step(size_t n, float* master, float* m, float* v,
                         const float* grad, const cr_adamw_cfg* cfg,
                         void* param_bf16, cr_stream_t stream);
 
+/* ---- device-side checks (test builds) --------------------------------------
+ * The library can be built as a checked variant whose kernels verify, before
+ * touching memory, the index arithmetic their accesses rest on (the chunk of
+ * an element is a rank, its offset lies inside that rank's shard, a tile
+ * belongs to its tensor...).  A failed check sets one bit of a device error
+ * word and skips the rest of that thread's work; nothing traps.
+ * cr_check_word: the word (0 = no check has failed), cleared afterwards if
+ * clear != 0; -1 in the normal build, which has no checks; -2 if reading it
+ * failed.  Synchronises with the device.
+ * cr_check_selftest: sets bit 31 through the failing-check path (checked
+ * build); CR_ERR_UNSUPPORTED in the normal build. */
+long long cr_check_word(int clear);
+cr_status cr_check_selftest(cr_stream_t stream);
+
 /* ---- a11: communication accounting (host) ---------------------------------
  * Elements rank `rank` sends and receives, and the logical steps taken, in
  * the ring schedule of [DT] section 2 (reduce-scatter N-1 steps, all-gather
