@@ -679,6 +679,29 @@ def run_e2e(args, bufs, n, count, world, stream, device):
     return out
 
 
+def traffic_per_step(name):
+    """DRAM bytes of one step (all its launches) from the committed ncu
+    summary, or None if absent or taken on a different build of the kernel."""
+    p = os.path.join(ROOT, "profiles", name + ".md")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    with open(p) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith(
+                    ("dram_bytes_per_launch", "dram_bytes_per_step", "kernel_tu",
+                     "kernel_source_hash")):
+                k, v = line.split(":", 1)
+                vals[k.strip(" -*`")] = v.strip(" `\n")
+    try:
+        from fsdp_emulated_ranks_gb300 import build as B
+        if vals.get("kernel_source_hash") != B.kernel_hash(vals["kernel_tu"]):
+            return None
+        return int(vals.get("dram_bytes_per_step") or vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError, OSError):
+        return None
+
+
 def traffic_per_launch(name, launches=1):
     """DRAM bytes per launch from the committed ncu summary of this kernel,
     or None if absent or taken on a different build of its kernel code (the
@@ -718,7 +741,8 @@ def run_rows(args, device, stream, peak, skip=None):
         rows.append({"name": wl.name, "ms": round(ms, 4), "GB/s": round(gbs, 1),
                      "frac": round(gbs / peak[0], 4), "algorithmic_bytes": wl.nbytes,
                      "launches_per_call": wl.launches, "kernel": wl.kernel,
-                     "traffic": traffic_per_launch(wl.profile, wl.launches)})
+                     "traffic": traffic_per_launch(wl.profile, wl.launches),
+                     "traffic_per_step": traffic_per_step(wl.profile)})
         wl.teardown()
     return rows
 
