@@ -629,7 +629,8 @@ def run_headline(args, world, rank, device, stream, peak):
         "ms_per_step": ms_step,
         "value": value,
         "clocks": sampler.summary(),
-        "gpu_launches": args.steps * wl.launches,
+        # every GPU launches the same kernels: the job's count, like `value`
+        "gpu_launches": world * args.steps * wl.launches,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak[0],
                      "unit": "GB/s", "frac": round(achieved / peak[0], 4),
                      "traffic": traffic_per_launch(wl.profile, wl.launches),
