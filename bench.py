@@ -1049,6 +1049,12 @@ def main(argv=None):
                            "op": f"{wl.op}, in place",
                            "l2": ("inputs exceed the 129 MB L2, no flush" if wl.nbytes // 2 > (129 << 20)
                                   else "inputs fit in L2 (latency regime), no flush")})
+            # what a real ring and a naive reduce + broadcast would move
+            es = 2 if wl.dt == "bf16" else 4
+            ring, _, _ = cr.cr_comm_elems(cr.COLL_ALL_REDUCE, cr.SCHED_RING, wl.n, wl.count, 0)
+            rs, rr, _ = cr.cr_comm_elems(cr.COLL_ALL_REDUCE, cr.SCHED_NAIVE, wl.n, wl.count, 0)
+            config["ring_bytes_sent_per_rank"] = ring * es            # 2(N-1)/N S
+            config["naive_root_bytes_sent_and_received"] = (rs + rr) * es   # 2(N-1) S
         else:
             config["algorithmic_bytes_per_step"] = wl.nbytes
             config["l2"] = "inputs exceed the 129 MB L2, no flush"
