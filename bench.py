@@ -891,7 +891,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32 accumulate, bf16 in/out",
+            "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "config": {"workload": AllReduce().name, "ranks": 8,
                                             "elements_per_rank": 1 << 25,
                                             "sampled_elements_per_rank": count},
@@ -1061,7 +1061,8 @@ def main(argv=None):
         line = {"metric": METRIC, "value": round(head["value"], 1), "unit": UNIT,
                 "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": head["ms_per_step"], "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                # the arithmetic: fp32 partial sums (bf16 in and out, see config)
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32",
                 "data": "synthetic",
                 "config": config,
                 "roofline": head["roofline"], "cpu_baseline": cpu, "e2e": head["e2e"],
