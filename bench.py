@@ -609,6 +609,27 @@ ROW_WORKLOADS = ["reduce_scatter", "all_gather", "allreduce_f32", "bucket_pack",
                  "accumulate_allreduce", "allreduce_wire", "hsdp"]
 
 
+def workload_config(wl, world):
+    """The JSON line's config for workload wl on `world` GPUs (both arms)."""
+    config = {"workload": wl.name, "parallelism": f"{world} GPU(s) x {wl.n} emulated ranks each"}
+    if isinstance(wl, AllReduce):
+        es = 2 if wl.dt == "bf16" else 4
+        S = wl.count * es
+        config.update({"ranks": wl.n, "elements_per_rank": wl.count, "dtype_in_out": wl.dt,
+                       "accumulate": "fp32, ring order" if wl.dt != "i32" else "int32",
+                       "op": f"{wl.op}, in place",
+                       "l2": ("inputs exceed the 129 MB L2, no flush" if wl.nbytes // 2 > (129 << 20)
+                              else "inputs fit in L2 (latency regime), no flush"),
+                       # what a real ring and a naive reduce + broadcast would move
+                       # (N divides the count): 2(N-1)/N S per rank, 2(N-1) S at the root
+                       "ring_bytes_sent_per_rank": 2 * (wl.n - 1) * S // wl.n,
+                       "naive_root_bytes_sent_and_received": 2 * (wl.n - 1) * S})
+    else:
+        config["algorithmic_bytes_per_step"] = wl.nbytes
+        config["l2"] = "inputs exceed the 129 MB L2, no flush"
+    return config
+
+
 def run_headline(args, world, rank, device, stream, peak):
     import torch
     wl = make_workload(args.workload, args)
@@ -892,9 +913,8 @@ def run_reference(args):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": {"workload": AllReduce().name, "ranks": 8,
-                                            "elements_per_rank": 1 << 25,
-                                            "sampled_elements_per_rank": count},
+            "data": "synthetic", "config": dict(workload_config(AllReduce(), world),
+                                           sampled_elements_per_rank=count),
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -1042,22 +1062,7 @@ def main(argv=None):
                           f"single-threaded C oracle, {secs:.1f} s; host has "
                           f"{os.cpu_count()} cores")}
     if rank == 0:
-        config = {"workload": wl.name, "parallelism": f"{world} GPU(s) x {wl.n} emulated ranks each"}
-        if isinstance(wl, AllReduce):
-            config.update({"ranks": wl.n, "elements_per_rank": wl.count, "dtype_in_out": wl.dt,
-                           "accumulate": "fp32, ring order" if wl.dt != "i32" else "int32",
-                           "op": f"{wl.op}, in place",
-                           "l2": ("inputs exceed the 129 MB L2, no flush" if wl.nbytes // 2 > (129 << 20)
-                                  else "inputs fit in L2 (latency regime), no flush")})
-            # what a real ring and a naive reduce + broadcast would move
-            es = 2 if wl.dt == "bf16" else 4
-            ring, _, _ = cr.cr_comm_elems(cr.COLL_ALL_REDUCE, cr.SCHED_RING, wl.n, wl.count, 0)
-            rs, rr, _ = cr.cr_comm_elems(cr.COLL_ALL_REDUCE, cr.SCHED_NAIVE, wl.n, wl.count, 0)
-            config["ring_bytes_sent_per_rank"] = ring * es            # 2(N-1)/N S
-            config["naive_root_bytes_sent_and_received"] = (rs + rr) * es   # 2(N-1) S
-        else:
-            config["algorithmic_bytes_per_step"] = wl.nbytes
-            config["l2"] = "inputs exceed the 129 MB L2, no flush"
+        config = workload_config(wl, world)
         line = {"metric": METRIC, "value": round(head["value"], 1), "unit": UNIT,
                 "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": head["ms_per_step"], "higher_is_better": True,
