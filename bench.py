@@ -656,7 +656,8 @@ def run_headline(args, world, rank, device, stream, peak):
                      "unit": "GB/s", "frac": round(achieved / peak[0], 4),
                      "traffic": traffic_per_launch(wl.profile, wl.launches),
                      "kernel": wl.kernel, "algorithmic_bytes_per_launch": wl.nbytes // wl.launches,
-                     "peak_source": peak[1], "step_ms_median": statistics.median(per)},
+                     "peak_source": peak[1], "step_ms_median": statistics.median(per),
+                     **step_quantiles(per)},
     }
     out["e2e"] = None
     if isinstance(wl, AllReduce) and not args.no_e2e:
@@ -762,11 +763,20 @@ def run_rows(args, device, stream, peak, skip=None):
         gbs = wl.nbytes / (ms * 1e-3) / 1e9
         rows.append({"name": wl.name, "ms": round(ms, 4), "GB/s": round(gbs, 1),
                      "frac": round(gbs / peak[0], 4), "algorithmic_bytes": wl.nbytes,
+                     "steps": steps, **step_quantiles(per),
                      "launches_per_call": wl.launches, "kernel": wl.kernel,
                      "traffic": traffic_per_launch(wl.profile, wl.launches),
                      "traffic_per_step": traffic_per_step(wl.profile)})
         wl.teardown()
     return rows
+
+
+def step_quantiles(per):
+    """Median, 10th and 90th percentile of the per-step event times (ms)."""
+    q = sorted(per)
+    at = lambda f: q[min(len(q) - 1, int(round(f * (len(q) - 1))))]
+    return {"ms_median": round(statistics.median(q), 4), "ms_p10": round(at(0.1), 4),
+            "ms_p90": round(at(0.9), 4)}
 
 
 # ---- bf16 wire error ----------------------------------------------------------------------
@@ -998,6 +1008,8 @@ def main(argv=None):
     ap.add_argument("--pg-timeout", type=int, default=600,
                     help="seconds after which a barrier or collective of an N > 1 run fails "
                          "when a rank is missing")
+    ap.add_argument("--jsonl", default=None,
+                    help="also append one JSON record per measured row to this file")
     ap.add_argument("--no-rows", action="store_true")
     ap.add_argument("--skip-fsdp", action="store_true")
     ap.add_argument("--row-steps", type=int, default=20)
@@ -1075,6 +1087,14 @@ def main(argv=None):
                 "frac_of_peak": round(head["value"] / world / peak[0], 4),
                 "rows": rows, "ddp_overlap": overlap, "wire_error": wire}
         print(json.dumps(line))
+        if args.jsonl:
+            with open(args.jsonl, "a") as f:
+                head_rec = {"name": wl.name, "ms": round(head["ms_per_step"], 4),
+                            "GB/s": round(head["value"], 1), "frac": head["roofline"]["frac"],
+                            "kernel": head["roofline"]["kernel"],
+                            "traffic": head["roofline"]["traffic"], "n_gpus": world}
+                for rec in [head_rec] + (rows or []):
+                    f.write(json.dumps(dict(rec, peak_GBs=peak[0], clocks=head["clocks"])) + "\n")
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
