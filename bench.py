@@ -533,6 +533,10 @@ class Fsdp2Step(Workload):
                 self.master.append(self.t_state[so0:so0 + sk] if sk else 0)
                 self.m.append(self.t_state[so + so0:so + so0 + sk] if sk else 0)
                 self.v.append(self.t_state[2 * so + so0:2 * so + so0 + sk] if sk else 0)
+        # Layout kept for tests that sample elements: parameter p of rank r at
+        # t_g/t_p[r][offs[p]:], owner j's shard at t_state[soffs[p][j]:] (m at
+        # +so, v at +2 so).
+        self.offs, self.soffs, self.so = offs, soffs, so
         # Device addresses taken once (the slabs t_g, t_p, t_state stay alive).
         addr = lambda xs: [x if isinstance(x, int) else x.data_ptr() for x in xs]
         self.grads, self.params = addr(self.grads), addr(self.params)

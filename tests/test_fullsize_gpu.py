@@ -389,3 +389,55 @@ def test_hsdp_2x2_beyond_2_32_elements():
         assert_match(got, ref, "bf16", f"group {g}")
     del bufs, shards
     torch.cuda.empty_cache()
+
+
+def test_fsdp2_transformer_full_sampled():
+    """The FSDP2 step over the benchmark's transformer (145 parameters,
+    1.27e9 elements, 8 ranks), laid out and called as benchmarked.  Each
+    sampled element's result depends only on its 8 gradients, its state and
+    the rank that owns its row (the fold order): grouped by owner, the
+    samples are embedded into a small parameter of N rows whose row j is
+    owned by rank j, and that is stepped by the oracle."""
+    import bench
+    n = 8
+    wl = bench.Fsdp2Step()
+    wl.setup(torch.device("cuda"))
+    rng = np.random.default_rng(7)
+    P, I_, J, K = [], [], [], []
+    for p, (d0, row) in enumerate(wl.shapes):
+        k = d0 * row
+        Lr = -(-d0 // n)
+        for i in sorted(set(rng.integers(0, k, 48).tolist()) | {0, k - 1}):
+            j = (i // row) // Lr
+            P.append(p), I_.append(i), J.append(j), K.append(i - j * Lr * row)
+    gidx = torch.tensor([wl.offs[p] + i for p, i in zip(P, I_)], device="cuda")
+    sidx = torch.tensor([wl.soffs[p][j] + k for p, j, k in zip(P, J, K)], device="cuda")
+    g = np.stack([to_host(wl.t_g[r][gidx], "bf16") for r in range(n)], axis=1)   # [s, n]
+    st0 = [wl.t_state[sidx + q * wl.so].cpu().numpy() for q in range(3)]       # master, m, v
+    wl.step(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    st1 = [wl.t_state[sidx + q * wl.so].cpu().numpy() for q in range(3)]
+    par = np.stack([to_host(wl.t_p[r][gidx], "bf16") for r in range(n)], axis=1)
+    wl.teardown()
+    # embed: owner j's samples at row j of an (n x M) parameter
+    J = np.array(J)
+    M = max(1, int(np.bincount(J, minlength=n).max()))
+    col = np.zeros(len(J), np.int64)
+    fill = np.zeros(n, np.int64)
+    for s, j in enumerate(J):
+        col[s] = fill[j]
+        fill[j] += 1
+    grads = [np.zeros(n * M, np.uint16) for _ in range(n)]
+    for r in range(n):
+        grads[r][J * M + col] = g[:, r]
+    state = [[np.zeros(M, np.float32) for _ in range(n)] for _ in range(3)]
+    for q in range(3):
+        for s in range(len(J)):
+            state[q][J[s]][col[s]] = st0[q][s]
+    want_p = O.fsdp2_step([(n, M)], [grads], [state[0]], [state[1]], [state[2]], O.AdamWConfig())
+    for q, name in enumerate(("master", "m", "v")):
+        ref = np.array([state[q][J[s]][col[s]] for s in range(len(J))], np.float32)
+        assert rel_maxabs(st1[q], ref) <= 1e-6, name
+    for r in range(n):
+        ref = want_p[0][r][J * M + col]
+        assert_match(par[:, r].copy(), ref, "bf16", f"params rank {r}")
