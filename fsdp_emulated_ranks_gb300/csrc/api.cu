@@ -59,6 +59,7 @@ cr_status all_reduce_impl(const void* const* in, int nranks, size_t count,
 
 
 void cr::report_error(cr_status status, const char* msg) { fail(status, "%s", msg); }
+cr_status cr::report_cuda_error(cudaError_t e, const char* what) { return cuda_fail(e, what); }
 
 extern "C" {
 

@@ -32,11 +32,10 @@ long long cr_check_word(int clear) {
 
 cr_status cr_check_selftest(cr_stream_t stream) {
 #if defined(CR_DEVICE_CHECKS)
+  cr::clear_stale_error();
   cr::k_check_selftest<<<1, 1, 0, (cudaStream_t)stream>>>();
-  if (cudaGetLastError() != cudaSuccess) {
-    cr::report_error(CR_ERR_CUDA, "check self-test launch failed");
-    return CR_ERR_CUDA;
-  }
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cr::report_cuda_error(e, "check self-test launch");
   return CR_OK;
 #else
   (void)stream;

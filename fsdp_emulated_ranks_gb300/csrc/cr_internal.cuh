@@ -219,6 +219,8 @@ cudaError_t launch_accum(cr_dtype grad_dtype, const AccumArgs& a, int vw, cudaSt
 
 // Records `msg` as the detail cr_last_error() returns on this thread.
 void report_error(cr_status status, const char* msg);
+// CR_ERR_CUDA with `what` and the CUDA error's name and text as the detail.
+cr_status report_cuda_error(cudaError_t e, const char* what);
 
 // Persistent-grid size for a kBlock-thread kernel that needs `threads`
 // threads of work: min(SMs on the current device * CTAs of `kernel` resident
@@ -237,5 +239,13 @@ inline unsigned flat_grid(uint64_t threads) {
   if (g > (1ull << 30)) g = 1ull << 30;
   return (unsigned)g;
 }
+
+// cudart is linked statically, so its last-error word belongs to this
+// library alone, but it also keeps errors that earlier calls returned
+// directly (a failed cudaLaunchKernelEx, cudaEventRecord, ...).  Every
+// <<<>>> launch clears it first, so that cudaGetLastError() after the
+// launch reports that launch alone.  A sticky error of the context is
+// reported again whatever is cleared.
+inline void clear_stale_error() { (void)cudaGetLastError(); }
 
 }  // namespace cr

@@ -53,14 +53,12 @@ extern "C" cr_status cr_fsdp_step_clipped_noalloc(
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) {
-    cr::report_error(CR_ERR_CUDA, "fsdp_step_clipped_noalloc: cudaGetDevice failed");
-    return CR_ERR_CUDA;
+    return cr::report_cuda_error(e, "fsdp_step_clipped_noalloc: cudaGetDevice");
   }
   int sms = 0;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) {
-    cr::report_error(CR_ERR_CUDA, "fsdp_step_clipped_noalloc: SM count query failed");
-    return CR_ERR_CUDA;
+    return cr::report_cuda_error(e, "fsdp_step_clipped_noalloc: SM count query");
   }
   if ((long long)sms * kMaxCtasPerSm > kScratchParts - 1) {
     cr::report_error(CR_ERR_UNSUPPORTED,
@@ -71,8 +69,7 @@ extern "C" cr_status cr_fsdp_step_clipped_noalloc(
   void* scratch = nullptr;
   e = scratch_address(dev, &scratch);
   if (e != cudaSuccess) {
-    cr::report_error(CR_ERR_CUDA, "fsdp_step_clipped_noalloc: cudaGetSymbolAddress failed");
-    return CR_ERR_CUDA;
+    return cr::report_cuda_error(e, "fsdp_step_clipped_noalloc: cudaGetSymbolAddress");
   }
   return cr_fsdp_step_clipped(grads_bf16, nranks, count, master, m, v, cfg, max_norm, scratch,
                               sizeof(g_clip_scratch), params_bf16, norm_out, stream);

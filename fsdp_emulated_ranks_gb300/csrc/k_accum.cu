@@ -153,6 +153,7 @@ __global__ void __launch_bounds__(kBlock)
 template <int GD, int SW>
 static cudaError_t accum_dispatch(const AccumArgs& a, cudaStream_t s) {
   const dim3 grid(flat_grid(a.count / 8 + 1), a.reduce ? 1 : a.n);
+  clear_stale_error();
   switch (a.reduce ? a.n : 0) {
     case 2: k_accum_vec<GD, 2, SW><<<grid, kBlock, 0, s>>>(a); break;
     case 4: k_accum_vec<GD, 4, SW><<<grid, kBlock, 0, s>>>(a); break;
@@ -166,6 +167,7 @@ template <int GD>
 static cudaError_t accum_by_width(const AccumArgs& a, int vw, cudaStream_t s) {
   if (vw == 32) return accum_dispatch<GD, 8>(a, s);
   if (vw == 16) return accum_dispatch<GD, 4>(a, s);
+  clear_stale_error();
   k_accum_elem<GD><<<flat_grid(a.count), kBlock, 0, s>>>(a);
   return cudaGetLastError();
 }

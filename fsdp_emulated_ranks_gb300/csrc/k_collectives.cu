@@ -179,6 +179,7 @@ __global__ void __launch_bounds__(kBlock)
 
 template <typename K, typename A>
 static cudaError_t launch_flat(K kernel, const A& args, uint64_t threads, cudaStream_t s) {
+  clear_stale_error();
   kernel<<<flat_grid(threads), kBlock, 0, s>>>(args);
   return cudaGetLastError();
 }
@@ -188,6 +189,7 @@ static cudaError_t launch_fold_kernel(K kernel, const FoldArgs& a, uint64_t thre
                                       cudaStream_t s) {
   unsigned grid = flat_grid(threads);
   if (a.max_ctas && grid > a.max_ctas) grid = a.max_ctas;
+  clear_stale_error();
   kernel<<<grid, kBlock, 0, s>>>(a);
   return cudaGetLastError();
 }

@@ -44,6 +44,7 @@ __global__ void k_clip_coef(const double* partials, int nparts, double max_norm,
 
 cudaError_t launch_clip_coef(const double* partials, int nparts, double max_norm, float* coef,
                              float* norm_out, cudaStream_t s) {
+  clear_stale_error();
   k_clip_coef<<<1, 32, 0, s>>>(partials, nparts, max_norm, coef, norm_out);
   return cudaGetLastError();
 }
@@ -190,6 +191,7 @@ __global__ void __launch_bounds__(kBlock)
 
 template <typename K, typename A>
 static cudaError_t launch_flat(K kernel, const A& args, uint64_t threads, cudaStream_t s) {
+  clear_stale_error();
   kernel<<<flat_grid(threads), kBlock, 0, s>>>(args);
   return cudaGetLastError();
 }
@@ -226,6 +228,7 @@ static cudaError_t sumsq_launch(const FsdpArgs& a, double* partials, int max_par
   if (err != cudaSuccess) return err;
   if (grid > max_parts) grid = max_parts;
   *nparts = grid;
+  clear_stale_error();
   k_fsdp_sumsq<NT, VEC><<<grid, kBlock, 0, s>>>(a, partials);
   return cudaGetLastError();
 }

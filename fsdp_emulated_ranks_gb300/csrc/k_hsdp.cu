@@ -126,6 +126,7 @@ __global__ void __launch_bounds__(kBlock)
 template <typename K>
 static cudaError_t launch_flat_hsdp(K kernel, const HsdpArgs& a, uint64_t threads,
                                     cudaStream_t s) {
+  clear_stale_error();
   kernel<<<flat_grid(threads), kBlock, 0, s>>>(a);
   return cudaGetLastError();
 }

@@ -66,8 +66,7 @@ cr_status check_device(const cr_reducer* red) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) {
-    cr::report_error(CR_ERR_CUDA, "cudaGetDevice failed");
-    return CR_ERR_CUDA;
+    return cr::report_cuda_error(e, "reducer: cudaGetDevice");
   }
   if (dev != red->device) {
     cr::report_error(CR_ERR_INVALID_ARG, "the reducer's device is not the current device");
@@ -95,10 +94,8 @@ cr_status cr_reducer_create(const cr_bucket_plan_t* plan, int nranks, void* cons
   cr_status st = cr::bucket_fused_check(plan, nranks, tensors, dtype, op);
   if (st) return st;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    cr::report_error(CR_ERR_CUDA, "cudaGetDevice failed");
-    return CR_ERR_CUDA;
-  }
+  const cudaError_t de = cudaGetDevice(&dev);
+  if (de != cudaSuccess) return cr::report_cuda_error(de, "reducer: cudaGetDevice");
   cr_reducer* red = new cr_reducer(plan);
   red->tensors.assign(tensors, tensors + (size_t)nranks * plan->ntensors);
   red->nranks = nranks;
@@ -116,8 +113,7 @@ cr_status cr_reducer_create(const cr_bucket_plan_t* plan, int nranks, void* cons
   if (e != cudaSuccess) {
     destroy_events(red);
     delete red;
-    cr::report_error(CR_ERR_CUDA, "cudaEventCreateWithFlags failed");
-    return CR_ERR_CUDA;
+    return cr::report_cuda_error(e, "reducer: cudaEventCreateWithFlags");
   }
   *out = red;
   return CR_OK;
@@ -146,8 +142,7 @@ cr_status cr_reducer_mark_ready(cr_reducer_t* red, int tensor, cr_stream_t compu
     cudaError_t e = cudaEventRecord(red->ready[b], (cudaStream_t)compute_stream);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(red->comm, red->ready[b], 0);
     if (e != cudaSuccess) {
-      cr::report_error(CR_ERR_CUDA, "event record / stream wait failed");
-      return CR_ERR_CUDA;
+      return cr::report_cuda_error(e, "reducer: event record / stream wait");
     }
     const std::vector<int>& ts = red->bucket_tensors[b];
     st = cr::bucket_fused_tensors(&red->plan, red->nranks, red->tensors.data(), red->dtype,
@@ -177,8 +172,7 @@ cr_status cr_reducer_finalize(cr_reducer_t* red, cr_stream_t compute_stream) {
   cudaError_t e = cudaEventRecord(red->done, red->comm);
   if (e == cudaSuccess) e = cudaStreamWaitEvent((cudaStream_t)compute_stream, red->done, 0);
   if (e != cudaSuccess) {
-    cr::report_error(CR_ERR_CUDA, "event record / stream wait failed");
-    return CR_ERR_CUDA;
+    return cr::report_cuda_error(e, "reducer: event record / stream wait");
   }
   red->state.reset();
   return CR_OK;

@@ -27,12 +27,18 @@
  *    and CUDA events, released with cr_reducer_destroy) and cr_comm_create
  *    (a host object, released with cr_comm_destroy) nothing allocates at
  *    all, and the library keeps no state between calls beyond cached device
- *    attributes.
+ *    attributes, the static array of cr_fsdp_step_clipped_noalloc and the
+ *    device error word of the checked build (cr_check_word).
  *  - Every launching call is asynchronous on `stream` (NULL = the legacy
  *    default stream).  Argument errors are detected on the host before any
- *    launch and leave all buffers untouched; a failed launch returns
- *    CR_ERR_CUDA.  cr_last_error() gives the detail of the last failure on
- *    the calling thread.
+ *    launch and leave all buffers untouched; a launch (or event record, or
+ *    copy) that CUDA refuses returns CR_ERR_CUDA with CUDA's error name and
+ *    text in the detail.  If the call's first launch is refused nothing of
+ *    the call runs; if a later one is (calls of several launches), the
+ *    call's outputs -- and its inputs, where it works in place -- are
+ *    undefined.  A refused launch leaves the library usable: the next call
+ *    does not see the old error.  cr_last_error() gives the detail of the
+ *    last failure on the calling thread.
  *  - Chunking (a1): with L = ceil(count/N), chunk j is the element range
  *    [j*L, min((j+1)*L, count)); trailing chunks may be short or empty, as
  *    with torch.chunk-style uneven Shard(0) shards ([DT] section 4, FSDP2).
@@ -71,7 +77,7 @@ typedef enum {
   CR_ERR_UNSUPPORTED = 2, /* legal but unimplemented dtype/op combination */
   CR_ERR_ALIGNMENT = 3,   /* pointer not aligned to its element size      */
   CR_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed         */
-  CR_ERR_TIMEOUT = 5      /* reserved for host-side fault harnesses       */
+  CR_ERR_TIMEOUT = 5      /* a rank of a cr_comm_t collective never joined */
 } cr_status;
 
 typedef enum { CR_F32 = 0, CR_BF16 = 1, CR_I32 = 2 } cr_dtype;
