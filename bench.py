@@ -219,7 +219,7 @@ def alloc_ranks(n, count, dtype, std, seed0, device):
     bufs = []
     for r in range(n):
         t = torch.empty(count, dtype=dtype, device=device)
-        I.torch_fill_normal_(t, std, seed0 + r)
+        I.torch_fill_normal_(t, std, SEED_OFFSET + seed0 + r)
         bufs.append(t)
     return bufs
 
@@ -363,7 +363,7 @@ class Buckets(Workload):
     """DDP bucket fusion: 300 bf16 tensors per rank (log-uniform numel,
     seed 7), 25 MiB buckets; mode pack, allreduce, unpack or pipeline."""
 
-    def __init__(self, mode="pipeline", n=8, ntensors=300):
+    def __init__(self, mode="pipeline", n=8, ntensors=300, plan=True):
         from fsdp_emulated_ranks_gb300 import inputs as I
         self.mode, self.n = mode, n
         self.numels = [int(k) for k in I.bucket_numels()][:ntensors]
@@ -373,6 +373,8 @@ class Buckets(Workload):
         # The fused all-reduce works on the tensors in place: N reads + N
         # writes per element, the same bytes as one pass over the buckets.
         self.name = f"ddp_bucket_{mode}_bf16_{n}ranks_{ntensors}tensors"
+        if not plan:  # name and bytes only (the reference arm)
+            return
         from fsdp_emulated_ranks_gb300 import cr
         self.plan = cr.cr_bucket_plan(self.numels, 2, 25 * 1024 * 1024)
         copies = -(-n * len(self.numels) // 1024)
@@ -393,7 +395,7 @@ class Buckets(Workload):
         tens = []
         for r in range(n):
             flat = torch.empty(self.P + 128 * len(self.numels), dtype=torch.bfloat16, device=device)
-            I.torch_fill_normal_(flat, 1e-3, 1000 + r)
+            I.torch_fill_normal_(flat, 1e-3, SEED_OFFSET + 1000 + r)
             off, row_t = 0, []
             for k in self.numels:
                 row_t.append(flat[off:off + k])
@@ -450,7 +452,7 @@ class FsdpStep(Workload):
         self.t_grads = alloc_ranks(n, count, torch.bfloat16, 1e-3, 1000, device)
         self.t_params = [torch.empty(count, dtype=torch.bfloat16, device=device) for _ in range(n)]
         self.t_master_full = torch.empty(count, dtype=torch.float32, device=device)
-        I.torch_fill_normal_(self.t_master_full, 0.02, 2000)
+        I.torch_fill_normal_(self.t_master_full, 0.02, SEED_OFFSET + 2000)
         self.t_mv = torch.zeros(2 * count, dtype=torch.float32, device=device)
         self.t_master = [self.t_master_full[j * L:(j + 1) * L] for j in range(n)]
         self.t_m = [self.t_mv[j * L:(j + 1) * L] for j in range(n)]
@@ -509,7 +511,7 @@ class Fsdp2Step(Workload):
             o += (k + pad - 1) // pad * pad
         self.t_g = [torch.empty(o, dtype=torch.bfloat16, device=device) for _ in range(n)]
         for r, t in enumerate(self.t_g):
-            I.torch_fill_normal_(t, 1e-3, 1000 + r)
+            I.torch_fill_normal_(t, 1e-3, SEED_OFFSET + 1000 + r)
         self.t_p = [torch.empty(o, dtype=torch.bfloat16, device=device) for _ in range(n)]
         shard = []
         for (d, rn) in self.shapes:
@@ -523,7 +525,7 @@ class Fsdp2Step(Workload):
                 so += (k + pad - 1) // pad * pad
             soffs.append(so_row)
         self.t_state = torch.zeros(3 * so, dtype=torch.float32, device=device)
-        I.torch_fill_normal_(self.t_state[:so], 0.02, 2000)
+        I.torch_fill_normal_(self.t_state[:so], 0.02, SEED_OFFSET + 2000)
         self.grads, self.params, self.master, self.m, self.v = [], [], [], [], []
         for p, k in enumerate(sizes):
             for r in range(n):
@@ -580,7 +582,16 @@ class Accumulate(Workload):
             cr.cr_accumulate(self.t_acc, self.count, self.t_g, "bf16", stream)
 
 
-def make_workload(name, args):
+# Added to every seed of a value draw (--seed); the recipe's seeds at 0.  The
+# seeded draw of the bucket workload's tensor sizes is not shifted: the
+# workload keeps its shape.
+SEED_OFFSET = 0
+
+# --config: the five benchmark configurations (1-4 a workload, 5 the sweep).
+CONFIGS = {1: "allreduce_f32", 2: "allreduce", 3: "bucket_pipeline", 4: "fsdp", 5: "sweep"}
+
+
+def make_workload(name, args, plan=True):
     if name == "allreduce":
         return AllReduce()
     if name == "allreduce_f32":
@@ -594,7 +605,7 @@ def make_workload(name, args):
     if name == "all_gather":
         return AllGather()
     if name.startswith("bucket_"):
-        return Buckets(mode=name[len("bucket_"):], ntensors=args.bucket_ntensors)
+        return Buckets(mode=name[len("bucket_"):], ntensors=args.bucket_ntensors, plan=plan)
     if name == "fsdp":
         return FsdpStep(count=args.fsdp_count)
     if name == "fsdp_clipped":
@@ -902,39 +913,189 @@ def cpu_oracle_allreduce(sample, min_seconds):
     return passes * ar_bytes(n, count, 2) / dt / 1e9, dt, passes
 
 
+class OracleSample:
+    """A bounded sample of workload `name` for the CPU oracle, drawn by the
+    workload's recipe (numpy's generator on the host): k elements per rank,
+    or for the bucket and FSDP2 workloads the same structure scaled down to
+    about k elements per rank.  step() runs one step of the workload's
+    computation in the oracle; nbytes is that step's algorithmic bytes by
+    the workload's own formula; desc says what the sample is."""
+
+    def __init__(self, name, args, k):
+        import numpy as np
+        import oracle as O
+        from fsdp_emulated_ranks_gb300 import inputs as I
+        self.full = full = make_workload(name, args, plan=False)
+        n = full.n
+
+        def bf16(count, std, seed):
+            return I.np_to_bf16_bits(I.np_normal_f32(count, std, SEED_OFFSET + seed))
+
+        def shards(x, parts):
+            L = O.chunk_len(x.size, parts)
+            return [np.ascontiguousarray(x[min(j * L, x.size):min((j + 1) * L, x.size)])
+                    for j in range(parts)]
+
+        if isinstance(full, (AllReduce, AllReduceWire, ReduceScatter, AllGather, Hsdp)):
+            k = min(k, full.count)
+            dt = getattr(full, "dt", "bf16")
+            if dt == "bf16":
+                x = [bf16(k, getattr(full, "std", 0.02), r) for r in range(n)]
+            else:
+                x = [I.np_normal_f32(k, full.std, SEED_OFFSET + r) for r in range(n)]
+            if isinstance(full, AllReduce):
+                self.step = lambda: O.ring_all_reduce(x, dt, full.op)
+                sample = AllReduce(n, k, dt, full.op)
+            elif isinstance(full, AllReduceWire):
+                self.step = lambda: O.ring_all_reduce_wire(x, "bf16", "avg", "bf16")
+                sample = AllReduceWire(n, k)
+            elif isinstance(full, ReduceScatter):
+                self.step = lambda: O.ring_reduce_scatter(x, "bf16", "avg")
+                sample = ReduceScatter(n, k)
+            elif isinstance(full, AllGather):
+                sh = shards(x[0], n)
+                self.step = lambda: O.ring_all_gather(sh, k, "bf16")
+                sample = AllGather(n, k)
+            else:
+                self.step = lambda: O.hsdp_reduce_scatter(x, full.R, full.S, "bf16", "avg")
+                sample = Hsdp(full.R, full.S, k)
+            self.desc = f"{n} rank buffers of {k} elements"
+        elif isinstance(full, Accumulate):
+            k = min(k, full.count)
+            acc = [np.zeros(k, np.float32) for _ in range(n)]
+            g = [bf16(k, 1e-3, r) for r in range(n)]
+
+            def step():
+                for r in range(n):
+                    O.accumulate(acc[r], g[r], "bf16")
+                if full.reduce:
+                    out, _ = O.ring_all_reduce(acc, "f32", "avg")
+                    for r in range(n):
+                        acc[r][:] = out[r]
+            self.step = step
+            sample = Accumulate(full.reduce, n, k)
+            self.desc = f"{n} fp32 accumulators and bf16 gradients of {k} elements"
+        elif isinstance(full, FsdpStep):
+            k = min(k, full.count)
+            grads = [bf16(k, 1e-3, 1000 + r) for r in range(n)]
+            master = shards(I.np_normal_f32(k, 0.02, SEED_OFFSET + 2000), n)
+            m = [np.zeros_like(a) for a in master]
+            v = [np.zeros_like(a) for a in master]
+            cfg = O.AdamWConfig()
+            if full.clip:
+                self.step = lambda: O.fsdp_step_clipped(grads, master, m, v, cfg, 1.0)
+            else:
+                self.step = lambda: O.fsdp_step(grads, master, m, v, cfg)
+            sample = FsdpStep(n, k, full.clip)
+            self.desc = f"{k} flat parameters"
+        elif isinstance(full, Fsdp2Step):
+            # The same architecture at a width whose parameter count is about k.
+            hidden = 64
+            while hidden < 2048 and Fsdp2Step(n, 1, 2 * hidden).P <= k:
+                hidden *= 2
+            sample = Fsdp2Step(n, 1, hidden)
+            grads = [[bf16(d * rn, 1e-3, 1000 + 8 * p + r) for r in range(n)]
+                     for p, (d, rn) in enumerate(sample.shapes)]
+            master, m, v = [], [], []
+            for p, (d, rn) in enumerate(sample.shapes):
+                Lr = O.chunk_len(d, n)
+                st = [I.np_normal_f32(max(0, min(d, (j + 1) * Lr) - min(d, j * Lr)) * rn, 0.02,
+                                      SEED_OFFSET + 2000 + 8 * p + j) for j in range(n)]
+                master.append(st)
+                m.append([np.zeros_like(a) for a in st])
+                v.append([np.zeros_like(a) for a in st])
+            cfg = O.AdamWConfig()
+            self.step = lambda: O.fsdp2_step(sample.shapes, grads, master, m, v, cfg)
+            self.desc = (f"the same transformer at 1 layer of hidden {hidden} "
+                         f"({len(sample.shapes)} parameters, {sample.P} elements)")
+        elif isinstance(full, Buckets):
+            scale = k / full.P
+            numels = [max(1, round(t * scale)) for t in full.numels]
+            cap = max(2, round(25 * 1024 * 1024 * scale))
+            plan = O.bucket_plan(numels, 2, cap)
+            tens = [[bf16(t, 1e-3, 1000 + 1000 * r + i) for i, t in enumerate(numels)]
+                    for r in range(n)]
+            bks = O.bucket_pack(plan, tens)
+            mode = full.mode
+
+            def step():
+                if mode == "pack":
+                    O.bucket_pack(plan, tens)
+                elif mode == "unpack":
+                    O.bucket_unpack(plan, bks, np.uint16)
+                elif mode == "allreduce":
+                    for b in range(plan.nbuckets):
+                        O.ring_all_reduce([bks[r][b] for r in range(n)], "bf16", "avg")
+                else:  # pipeline, fused: pack, all-reduce per bucket, unpack
+                    O.bucketed_all_reduce(plan, tens, "bf16", "avg")
+            self.step = step
+            P = sum(numels)
+            one = 2 * 2 * P * n
+            sample = None
+            self.nbytes = 3 * one if mode == "pipeline" else one
+            self.desc = (f"the {len(numels)} tensor sizes scaled by {scale:.3g} "
+                         f"({P} elements per rank, {plan.nbuckets} buckets of a {cap}-byte cap)")
+        else:
+            raise SystemExit(f"no oracle sample for workload {name}")
+        if sample is not None:
+            self.nbytes = sample.nbytes
+        self.fraction = self.nbytes / full.nbytes
+
+
+def time_oracle(smp, steps, warmup):
+    """Mean seconds per oracle step after `warmup` untimed steps."""
+    for _ in range(warmup):
+        smp.step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        smp.step()
+    return (time.perf_counter() - t0) / steps
+
+
 def run_reference(args):
-    """--impl reference: the CPU oracle on this host, bounded samples of the
-    headline workload, same metric and unit."""
+    """--impl reference: the CPU oracle on this host, timed on a bounded
+    sample of the selected workload (the headline by default), with the
+    same metric, unit and config as this workload's line."""
     world, rank, _ = dist_env()
     if world > 1 and rank != 0:
         return 0
-    import numpy as np
-    from fsdp_emulated_ranks_gb300 import inputs as I
-    import oracle as O
-    n, count = 8, args.ref_sample
-    host = [I.np_to_bf16_bits(I.np_normal_f32(count, 0.02, r)) for r in range(n)]
-    for _ in range(args.warmup):
-        O.ring_all_reduce(host, "bf16", "avg")
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        out, _ = O.ring_all_reduce(host, "bf16", "avg")
-    dt = time.perf_counter() - t0
-    ms = dt * 1e3 / args.steps
-    value = ar_bytes(n, count, 2) / (ms * 1e-3) / 1e9
-    sample = (f"ring all-reduce AVG of 8 bf16 buffers of {count} elements per step "
-              f"(1/{(1 << 25) // count} of the 64 MiB-per-rank workload), oracle/ C code")
+    smp = OracleSample(args.workload, args, args.ref_sample)
+    sec = time_oracle(smp, args.steps, args.warmup)
+    value = smp.nbytes / sec / 1e9
+    sample = (f"{smp.desc} per step ({smp.fraction:.3g} of the workload's bytes), "
+              f"single-threaded C oracle (oracle/); host has {os.cpu_count()} cores")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": dict(workload_config(AllReduce(), world),
-                                           sampled_elements_per_rank=count),
+            "data": "synthetic", "config": dict(workload_config(smp.full, world),
+                                           sample=smp.desc),
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
+
+
+def cpu_baseline_sampled(args):
+    """cpu_baseline of a workload other than the headline all-reduce: the
+    oracle on a bounded sample of it (OracleSample), repeated for at least
+    --cpu-seconds."""
+    smp = OracleSample(args.workload, args, args.ref_sample)
+    smp.step()  # loads the library, touches the buffers
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        smp.step()
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= args.cpu_seconds or passes >= 1000:
+            break
+    return {"value": round(passes * smp.nbytes / dt / 1e9, 4), "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": (f"{passes} step(s) of the workload on {smp.desc} "
+                       f"({smp.fraction:.3g} of its bytes), single-threaded C oracle, "
+                       f"{dt:.1f} s; host has {os.cpu_count()} cores")}
 
 
 # ---- sweep ----------------------------------------------------------------------------------
@@ -1004,6 +1165,12 @@ def main(argv=None):
                          "reduce_scatter, all_gather, hsdp, "
                          "bucket_{pack,allreduce,unpack,pipeline,fused}, fsdp, fsdp_clipped, "
                          "fsdp2, accumulate, accumulate_allreduce")
+    ap.add_argument("--config", type=int, choices=sorted(CONFIGS), default=None,
+                    help="1: all-reduce SUM fp32 4 ranks x 2^20; 2: all-reduce AVG bf16 8 x 64 MiB "
+                         "(the headline); 3: bucket pack -> all-reduce -> unpack; 4: FSDP step "
+                         "1.3e9 x 8; 5: the sweep")
+    ap.add_argument("--seed", type=int, default=0,
+                    help="offset added to every seed of the input values (0: the recipe)")
     ap.add_argument("--fsdp-count", type=int, default=1_300_000_000)
     ap.add_argument("--bucket-ntensors", type=int, default=300)
     ap.add_argument("--fsdp2-layers", type=int, default=24,
@@ -1030,6 +1197,13 @@ def main(argv=None):
                     help="elements per rank per step for --impl reference")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
+    global SEED_OFFSET
+    SEED_OFFSET = args.seed
+    if args.config is not None:
+        if CONFIGS[args.config] == "sweep":
+            args.sweep = True
+        else:
+            args.workload = CONFIGS[args.config]
 
     if args.impl == "reference":
         return run_reference(args)
@@ -1077,6 +1251,8 @@ def main(argv=None):
                           f"({'all' if frac == 1 else '1/%d' % frac} of the workload's bytes), "
                           f"single-threaded C oracle, {secs:.1f} s; host has "
                           f"{os.cpu_count()} cores")}
+    elif rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_sampled(args)
     if rank == 0:
         config = workload_config(wl, world)
         line = {"metric": METRIC, "value": round(head["value"], 1), "unit": UNIT,

@@ -1,0 +1,75 @@
+"""bench.py's reference arm (the CPU oracle) on every workload, on the CPU.
+
+--impl reference times the oracle on a bounded sample of the workload the
+other arm measures: the line names that workload, counts the sample's bytes
+by the workload's own formula, and says what the sample was.  --config picks
+the benchmark configurations by number and --seed shifts the input values
+only.
+"""
+import argparse
+import json
+
+import pytest
+
+import bench
+
+NS = argparse.Namespace(bucket_ntensors=300, fsdp_count=1_300_000_000, fsdp2_layers=24,
+                        fsdp2_hidden=2048)
+WORKLOADS = ["allreduce", "allreduce_f32", "allreduce_wire", "reduce_scatter", "all_gather",
+             "hsdp", "accumulate", "accumulate_allreduce", "fsdp", "fsdp_clipped", "fsdp2",
+             "bucket_pack", "bucket_allreduce", "bucket_unpack", "bucket_pipeline",
+             "bucket_fused"]
+
+
+def reference_line(capsys, *extra):
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3",
+                       "--ref-sample", "4096", *extra]) == 0
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    return json.loads(lines[0])
+
+
+@pytest.mark.parametrize("workload", WORKLOADS)
+def test_reference_arm_times_the_selected_workload(capsys, workload):
+    d = reference_line(capsys, "--workload", workload)
+    full = bench.make_workload(workload, NS, plan=False)
+    assert d["impl"] == "reference" and d["config"]["workload"] == full.name
+    assert d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["higher_is_better"] is True and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["sample"]
+
+
+def test_sample_bytes_follow_the_workload_formula():
+    ns, k = NS, 4096
+    assert bench.OracleSample("allreduce", ns, k).nbytes == 2 * 8 * k * 2
+    assert bench.OracleSample("reduce_scatter", ns, k).nbytes == 8 * k * 2 + k * 2
+    assert bench.OracleSample("all_gather", ns, k).nbytes == k * 2 + 8 * k * 2
+    assert bench.OracleSample("hsdp", ns, k).nbytes == 8 * k * 2 + 2 * k * 2
+    assert bench.OracleSample("fsdp", ns, k).nbytes == (4 * 8 + 24) * k
+    assert bench.OracleSample("fsdp_clipped", ns, k).nbytes == (6 * 8 + 24) * k
+    assert bench.OracleSample("accumulate", ns, k).nbytes == 8 * k * 10
+    smp = bench.OracleSample("bucket_pipeline", ns, k)
+    P = round(smp.nbytes / (3 * 2 * 2 * 8))
+    assert smp.nbytes == 3 * 2 * 2 * 8 * P and abs(P - k) <= 300
+
+
+def test_config_numbers_and_seed(capsys):
+    assert bench.CONFIGS[2] == "allreduce" and bench.CONFIGS[5] == "sweep"
+    d4 = reference_line(capsys, "--config", "4")
+    assert d4["config"]["workload"].startswith("fsdp_step_bf16_8ranks")
+    d1 = reference_line(capsys, "--config", "1")
+    assert d1["config"]["workload"] == "allreduce_sum_f32_4ranks_4MiB"
+    # --seed shifts the values, not the workload or its bytes
+    ns = NS
+    a = bench.OracleSample("allreduce", ns, 256)
+    out_a, _ = a.step()
+    bench.SEED_OFFSET = 5
+    try:
+        b = bench.OracleSample("allreduce", ns, 256)
+        out_b, _ = b.step()
+    finally:
+        bench.SEED_OFFSET = 0
+    assert a.nbytes == b.nbytes
+    assert any((x != y).any() for x, y in zip(out_a, out_b))

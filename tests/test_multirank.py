@@ -35,7 +35,7 @@ def _worker(rank, world, port, out):
 def test_two_rank_timing_uses_slowest_rank():
     world = 2
     port = _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
     slowest_ms = world * 10.0 / 5
@@ -68,7 +68,7 @@ def test_dead_rank_fails_the_barrier_instead_of_hanging():
     benchmark run ends instead of waiting forever."""
     world = 2
     port = _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.spawn(_worker_one_dies, args=(world, port, out), nprocs=world, join=True)
     kind, secs = out[0]
