@@ -1124,6 +1124,11 @@ def run_sweep(args, device, stream, peak):
               "GB/s": round(ar_bytes(n, count, 2) / (ms * 1e-3) / 1e9, 1),
               "ring_bytes_per_rank": sent * 2}
         if count * 2 <= (16 << 20):
+            # the same call prepared once (cr.prepare): the C call alone per step
+            prep = cr.prepare(cr.cr_all_reduce, bufs, count, "bf16", "avg", bufs, "bf16", stream)
+            _, pper = timed(prep, steps, 3, 1, stream)
+            pt["prepared_us"] = round(statistics.median(pper) * 1e3, 2)
+            del prep
             # the same calls captured in a CUDA graph: no host work per call
             reps = 50
             g = torch.cuda.CUDAGraph()

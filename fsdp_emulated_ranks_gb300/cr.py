@@ -10,6 +10,7 @@ from __future__ import annotations
 
 import ctypes as C
 import os
+import threading
 from typing import Sequence
 
 PKG = os.path.dirname(os.path.abspath(__file__))
@@ -74,9 +75,15 @@ class BucketPlanT(C.Structure):
                 ("bucket_numel", C.POINTER(C.c_size_t))]
 
 
+_tls = threading.local()  # .recorder: set while prepare() runs a wrapper
+
+
 def lib() -> C.CDLL:
     """Open libcr.so (built by fsdp_emulated_ranks_gb300.build)."""
     global _lib
+    rec = getattr(_tls, "recorder", None)
+    if rec is not None:
+        return rec
     if _lib is not None:
         return _lib
     if not os.path.exists(LIB_PATH):
@@ -542,3 +549,86 @@ def cr_comm_elems(coll: int, sched: int, nranks: int, count: int,
     _check(lib().cr_comm_elems(coll, sched, nranks, count, rank, C.byref(sent),
                                C.byref(recv), C.byref(steps)), "cr_comm_elems")
     return sent.value, recv.value, steps.value
+
+
+# ---- prepared calls -----------------------------------------------------------------
+
+# Entry points that launch work on a stream: the ones prepare() can record.
+_PREPARABLE = frozenset([
+    "cr_reduce_scatter", "cr_all_gather", "cr_all_reduce", "cr_reduce_scatter_wire",
+    "cr_all_reduce_wire", "cr_hsdp_reduce_scatter", "cr_all_reduce_host",
+    "cr_all_reduce_staged", "cr_bucket_pack", "cr_bucket_unpack", "cr_bucket_all_reduce",
+    "cr_bucket_all_reduce_fused", "cr_fsdp_step", "cr_fsdp_step_clipped",
+    "cr_fsdp_step_clipped_noalloc", "cr_fsdp2_step", "cr_accumulate",
+    "cr_all_reduce_accumulate", "cr_adamw_step"])
+# Functions without side effects that a wrapper may call while it marshals.
+_PURE = frozenset(["cr_last_error", "cr_status_string", "cr_chunk_len", "cr_version",
+                   "cr_fsdp_clip_workspace_bytes"])
+
+
+class _Recorder:
+    """Stands in for the library while prepare() runs a wrapper: a launching
+    entry point is recorded with its marshalled arguments instead of being
+    called, the pure helpers are the library's, and anything else (a call
+    with side effects that prepare() must not make) raises."""
+
+    def __init__(self, real):
+        self._real = real
+        self.calls = []
+
+    def __getattr__(self, name):
+        fn = getattr(self._real, name)
+        if name in _PURE:
+            return fn
+        if name not in _PREPARABLE:
+            raise TypeError(f"prepare() records launching entry points only, not {name}")
+
+        def record(*args):
+            self.calls.append((name, fn, args))
+            return 0
+        return record
+
+
+class Prepared:
+    """One marshalled call of a launching entry point; see prepare()."""
+
+    __slots__ = ("name", "_calls", "_keep")
+
+    def __init__(self, name, calls, keep):
+        # keep: the wrapper's arguments, so that the tensors and the bucket
+        # plan whose addresses were recorded outlive the prepared call
+        self.name, self._calls, self._keep = name, calls, keep
+
+    def __call__(self) -> None:
+        for name, fn, args in self._calls:
+            status = fn(*args)
+            if status != 0:
+                _check(status, name)
+
+
+def prepare(wrapper, *args, **kwargs) -> Prepared:
+    """Marshal one call of a launching wrapper (cr_all_reduce, cr_fsdp_step,
+    ...) once and return a callable that issues the same C call again: the
+    same device pointers, sizes, dtypes and stream, with none of the Python
+    argument conversion per invocation.  Meant for loops that repeat a call
+    on fixed buffers (a training step on static gradient buffers, a latency
+    measurement).
+
+    The stream is fixed at preparation: the one given, else the current
+    stream then.  The library validates every invocation as it does a
+    direct call.  A cr_adamw_cfg is passed by reference and read at each
+    invocation, so advancing cfg.step between invocations takes effect.
+    The prepared call holds references to the arguments, so the tensors and
+    the bucket plan it addresses stay allocated while it exists."""
+    if getattr(_tls, "recorder", None) is not None:
+        raise RuntimeError("prepare() cannot be nested")
+    rec = _Recorder(lib())
+    _tls.recorder = rec
+    try:
+        wrapper(*args, **kwargs)
+    finally:
+        _tls.recorder = None
+    name = getattr(wrapper, "__name__", "call")
+    if not rec.calls:
+        raise ValueError(f"{name} launches nothing that prepare() could record")
+    return Prepared(name, rec.calls, (args, kwargs))
