@@ -470,8 +470,8 @@ def cr_comm_destroy(comm: Comm) -> None:
 
 
 def cr_check_word(clear: bool = False) -> int:
-    """Device error word of the checked build (-1: this build has no device
-    checks; -2: reading it failed)."""
+    """Device error word of the checked build (-1: the loaded library was
+    built without device checks; -2: reading it failed)."""
     return lib().cr_check_word(1 if clear else 0)
 
 

@@ -39,7 +39,7 @@ cr_status cr_check_selftest(cr_stream_t stream) {
   return CR_OK;
 #else
   (void)stream;
-  cr::report_error(CR_ERR_UNSUPPORTED, "this build has no device checks");
+  cr::report_error(CR_ERR_UNSUPPORTED, "the library was built without device checks");
   return CR_ERR_UNSUPPORTED;
 #endif
 }
