@@ -74,11 +74,40 @@ def _local_includes(path: str, seen: set) -> None:
                     break
 
 
+def code_tokens(text: str) -> str:
+    """C/C++ source with its comments removed and every run of whitespace
+    made one space: what the compiler sees of it, up to the preprocessor.
+    String and character literals are kept as they are."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    # keep line structure for preprocessor directives, squeeze the rest
+    lines = (" ".join(l.split()) for l in "".join(out).splitlines())
+    return "\n".join(l for l in lines if l)
+
+
 def kernel_hash(tu: str) -> str:
     """Hash of what the kernels of one translation unit are compiled from:
-    that file, the library headers it includes (transitively) and the
-    compiler flags.  A profile of a kernel stays valid while this hash is
-    unchanged."""
+    the code of that file and of the library headers it includes
+    (transitively), comments and layout aside, and the compiler flags.  A
+    profile of a kernel stays valid while this hash is unchanged; editing a
+    comment does not change it."""
     h = hashlib.sha256()
     # the flags without the include paths, which differ between checkouts
     h.update(" ".join(f for f in ARCH + NVCC_FLAGS if not f.startswith("-I")).encode())
@@ -87,8 +116,8 @@ def kernel_hash(tu: str) -> str:
     _local_includes(src, deps)
     for f in [src] + sorted(deps, key=os.path.basename):
         h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(code_tokens(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -29,6 +29,11 @@
  *    all, and the library keeps no state between calls beyond cached device
  *    attributes, the static array of cr_fsdp_step_clipped_noalloc and the
  *    device error word of the checked build (cr_check_word).
+ *  - Entry points may be called from several host threads at once, on
+ *    different buffers: each call's marshalled state and error detail are
+ *    per thread, and the cached device attributes are locked.  A reducer
+ *    is used by one thread at a time, and calls of
+ *    cr_fsdp_step_clipped_noalloc share one static array (see there).
  *  - Every launching call is asynchronous on `stream` (NULL = the legacy
  *    default stream).  Argument errors are detected on the host before any
  *    launch and leave all buffers untouched; a launch (or event record, or
