@@ -19,7 +19,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 SUITES = ["tests/test_parity_gpu.py", "tests/test_parity_wire_hsdp_gpu.py",
           "tests/test_fuzz_gpu.py", "tests/test_pdl_gpu.py", "tests/test_reducer_gpu.py",
-          "tests/test_graph_gpu.py", "tests/test_comm_gpu.py", "tests/test_cuda_error_gpu.py"]
+          "tests/test_graph_gpu.py", "tests/test_comm_gpu.py", "tests/test_cuda_error_gpu.py",
+          "tests/test_fullsize_gpu.py", "tests/test_threads_gpu.py", "tests/test_zero_stages_gpu.py"]
 
 
 @pytest.fixture(scope="module")
@@ -49,6 +50,9 @@ def test_error_word_reports_a_failed_check(checked_lib):
 
 
 def test_gpu_suites_pass_with_device_checks(checked_lib):
+    # the suites include the full-size cases: leave them this process's cached memory
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     res = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu",
                           "-p", "no:cacheprovider"] + SUITES,
                          cwd=ROOT, env=_env(checked_lib), capture_output=True, text=True,
