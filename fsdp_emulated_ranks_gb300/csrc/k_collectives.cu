@@ -8,8 +8,10 @@
 // All-Reduce).  No intermediate touches HBM: per element the kernel moves
 // N input and 1 (RS) or N (AR) output elements, the algorithmic minimum.
 //
-// All-gather: k_gather_vec reads each shard element once and writes it to
-// every rank buffer at its chunk offset ([DT] section 2 All-Gather).
+// All-gather: k_gather_vec writes each shard element to every rank buffer
+// at its chunk offset ([DT] section 2 All-Gather), one CTA per span and
+// destination buffer; the CTAs of a span share its shard reads through L2,
+// so each shard byte comes from DRAM once.
 //
 // [DT] = "Distributed Training for Large Models: Collectives, FSDP/ZeRO,
 // DeviceMesh, and Multi-Dimensional Parallelism".
@@ -117,41 +119,62 @@ __global__ void __launch_bounds__(kBlock)
 
 // ---- all-gather ----------------------------------------------------------
 
+// Vectors per span: each CTA writes one span of one destination buffer,
+// two vectors per thread.
+constexpr int kGatherSpanVecs = 2 * kBlock;
+
+// Grid (n, spans): CTA x of span (y + z * gridDim.y) writes that span of
+// destination buffer x.  Blocks start x-fastest, so the n CTAs of a span
+// run together and the shard data they all read comes from DRAM once and
+// from L2 for the rest; each CTA writes one contiguous run into one
+// buffer.  On a GB300 this is 1.7 % faster than one thread writing its
+// vector to all n buffers (8 x 64 MiB bf16: 90.3 against 91.8 us),
+// provided 8 CTAs stay resident per SM (32 registers).  Vectors never
+// straddle a shard (L is a whole number of vectors on this path); the last
+// count % VEC elements are written by the CTAs of span 0, each for its own
+// destination.
 template <int ES, int NW>
-__global__ void __launch_bounds__(kBlock)
+__global__ void __launch_bounds__(kBlock, 8)
     k_gather_vec(const __grid_constant__ GatherArgs a) {
   constexpr int VEC = NW * 4 / ES;
   const uint64_t nvec = a.count / VEC;
-  const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-  const int n = a.n;
-  for (uint64_t iv = tid; iv < nvec; iv += stride) {
-    const uint64_t e0 = iv * VEC;
-    const uint64_t j64 = fastdiv_div(a.Ld, e0);
-    const int j = (int)j64;
-    CR_DCHECK(j64 == e0 / a.L && j < n && e0 + VEC <= (j64 + 1) * a.L && e0 + VEC <= a.count,
-              kChkGather);
-    const Words<NW> v = ldv<NW>(static_cast<const unsigned char*>(a.shards[j]) +
-                                (e0 - j64 * a.L) * ES);
-    const bool skip_own = (a.inplace_mask >> j) & 1ull;
-    for (int r = 0; r < n; ++r) {
-      if (skip_own && r == j) continue;
-      st_words<NW * 4, NW * 4>(static_cast<unsigned char*>(a.bufs[r]) + e0 * ES, v.w);
+  const int dest = blockIdx.x;
+  const uint64_t span = (uint64_t)blockIdx.z * gridDim.y + blockIdx.y;
+  const bool own_inplace = (a.inplace_mask >> dest) & 1ull;
+  unsigned char* const out = static_cast<unsigned char*>(a.bufs[dest]);
+  Words<NW> v[2];
+  uint64_t e0[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const uint64_t iv = span * kGatherSpanVecs + (uint64_t)k * kBlock + threadIdx.x;
+    e0[k] = iv < nvec ? iv * VEC : a.count;  // a.count: nothing to do
+    if (e0[k] < a.count) {
+      const uint64_t j64 = fastdiv_div(a.Ld, e0[k]);
+      CR_DCHECK(j64 == e0[k] / a.L && j64 < (uint64_t)a.n && e0[k] + VEC <= (j64 + 1) * a.L &&
+                    e0[k] + VEC <= a.count,
+                kChkGather);
+      if ((int)j64 == dest && own_inplace) {
+        e0[k] = a.count;  // rank dest's own chunk is already in place
+      } else {
+        v[k] = ldv<NW>(static_cast<const unsigned char*>(a.shards[j64]) +
+                       (e0[k] - j64 * a.L) * ES);
+      }
     }
   }
-  const uint64_t e = nvec * VEC + tid;
-  if (e < a.count) {
+#pragma unroll
+  for (int k = 0; k < 2; ++k)
+    if (e0[k] < a.count) st_words<NW * 4, NW * 4>(out + e0[k] * ES, v[k].w);
+  const uint64_t e = nvec * VEC + threadIdx.x;
+  if (span == 0 && e < a.count) {
     const uint64_t j64 = fastdiv_div(a.Ld, e);
-    const int j = (int)j64;
-    CR_DCHECK(j64 == e / a.L && j < n, kChkGather);
-    const unsigned char* src =
-        static_cast<const unsigned char*>(a.shards[j]) + (e - j64 * a.L) * ES;
-    const bool skip_own = (a.inplace_mask >> j) & 1ull;
-    for (int r = 0; r < n; ++r) {
-      if (skip_own && r == j) continue;
-      unsigned char* dst = static_cast<unsigned char*>(a.bufs[r]) + e * ES;
-      if constexpr (ES == 2) *reinterpret_cast<uint16_t*>(dst) = *reinterpret_cast<const uint16_t*>(src);
-      else *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(src);
+    CR_DCHECK(j64 == e / a.L && j64 < (uint64_t)a.n, kChkGather);
+    if (!((int)j64 == dest && own_inplace)) {
+      const unsigned char* src =
+          static_cast<const unsigned char*>(a.shards[j64]) + (e - j64 * a.L) * ES;
+      if constexpr (ES == 2)
+        *reinterpret_cast<uint16_t*>(out + e * ES) = *reinterpret_cast<const uint16_t*>(src);
+      else
+        *reinterpret_cast<uint32_t*>(out + e * ES) = *reinterpret_cast<const uint32_t*>(src);
     }
   }
 }
@@ -235,15 +258,31 @@ cudaError_t launch_fold(cr_dtype in, cr_dtype out, FoldMode mode,
                      : fold_by_type<kAR>(in, out, a, vw, s);
 }
 
+// One CTA per destination and span: grid (n, ny, nz) with ny * nz >= the
+// number of spans (at least one, whose CTAs write the tail); CTAs of a
+// span past the last do nothing.
+template <int ES, int NW>
+static cudaError_t launch_gather_vec(const GatherArgs& a, cudaStream_t s) {
+  constexpr int VEC = NW * 4 / ES;
+  const uint64_t nvec = a.count / VEC;
+  const uint64_t nspans = nvec ? (nvec + kGatherSpanVecs - 1) / kGatherSpanVecs : 1;
+  const uint64_t ny = nspans < 65535 ? nspans : 65535, nz = (nspans + ny - 1) / ny;
+  if (nz > 65535) return cudaErrorInvalidValue;  // beyond 2^52 elements
+  const dim3 grid((unsigned)a.n, (unsigned)ny, (unsigned)nz);
+  clear_stale_error();
+  k_gather_vec<ES, NW><<<grid, kBlock, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gather(size_t esize, const GatherArgs& a, int vw,
                           cudaStream_t s) {
   if (esize == 2) {
-    if (vw == 32) return launch_flat(k_gather_vec<2, 8>, a, a.count / 16 + 1, s);
-    if (vw == 16) return launch_flat(k_gather_vec<2, 4>, a, a.count / 8 + 1, s);
+    if (vw == 32) return launch_gather_vec<2, 8>(a, s);
+    if (vw == 16) return launch_gather_vec<2, 4>(a, s);
     return launch_flat(k_gather_elem<2>, a, a.count, s);
   }
-  if (vw == 32) return launch_flat(k_gather_vec<4, 8>, a, a.count / 8 + 1, s);
-  if (vw == 16) return launch_flat(k_gather_vec<4, 4>, a, a.count / 4 + 1, s);
+  if (vw == 32) return launch_gather_vec<4, 8>(a, s);
+  if (vw == 16) return launch_gather_vec<4, 4>(a, s);
   return launch_flat(k_gather_elem<4>, a, a.count, s);
 }
 
