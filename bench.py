@@ -1274,12 +1274,16 @@ def main(argv=None):
         print(json.dumps(line))
         if args.jsonl:
             with open(args.jsonl, "a") as f:
+                rl = head["roofline"]
                 head_rec = {"name": wl.name, "ms": round(head["ms_per_step"], 4),
-                            "GB/s": round(head["value"], 1), "frac": head["roofline"]["frac"],
-                            "kernel": head["roofline"]["kernel"],
-                            "traffic": head["roofline"]["traffic"], "n_gpus": world}
+                            "ms_median": rl["ms_median"], "ms_p10": rl["ms_p10"],
+                            "ms_p90": rl["ms_p90"], "GB/s": round(head["value"], 1),
+                            "frac": rl["frac"], "algorithmic_bytes": wl.nbytes,
+                            "kernel": rl["kernel"], "traffic": rl["traffic"], "n_gpus": world,
+                            "cpu_baseline": cpu}
                 for rec in [head_rec] + (rows or []):
-                    f.write(json.dumps(dict(rec, peak_GBs=peak[0], clocks=head["clocks"])) + "\n")
+                    f.write(json.dumps(dict(rec, peak_GBs=peak[0], clocks=head["clocks"],
+                                            host_cores=os.cpu_count())) + "\n")
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

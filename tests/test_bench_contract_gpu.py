@@ -58,6 +58,9 @@ def test_headline_line_has_every_key(tmp_path):
         assert row["ms_p10"] <= row["ms_median"] <= row["ms_p90"]
     recs = [json.loads(l) for l in jsonl.read_text().splitlines()]
     assert len(recs) == 1 + len(d["rows"]) and recs[0]["name"] == d["config"]["workload"]
+    for k in ("ms_median", "ms_p10", "ms_p90", "algorithmic_bytes", "cpu_baseline"):
+        assert k in recs[0], k
+    assert all(r["host_cores"] >= 1 and r["peak_GBs"] > 0 for r in recs)
 
 
 def test_reference_arm_matches_the_metric():
