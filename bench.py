@@ -782,6 +782,15 @@ def run_rows(args, device, stream, peak, skip=None):
                      "launches_per_call": wl.launches, "kernel": wl.kernel,
                      "traffic": traffic_per_launch(wl.profile, wl.launches),
                      "traffic_per_step": traffic_per_step(wl.profile)})
+        if ms < 0.05:
+            # host-bound: also the same call prepared once (the C call alone)
+            from fsdp_emulated_ranks_gb300 import cr
+            prep = cr.prepare(wl.step, stream)
+            _, pper = timed(prep, steps, 3, 1, stream)
+            pms = statistics.median(pper)
+            rows[-1].update({"ms_prepared_median": round(pms, 4),
+                             "GB/s_prepared": round(wl.nbytes / (pms * 1e-3) / 1e9, 1)})
+            del prep
         wl.teardown()
     return rows
 
