@@ -674,11 +674,37 @@ def run_headline(args, world, rank, device, stream, peak):
                      "peak_source": peak[1], "step_ms_median": statistics.median(per),
                      **step_quantiles(per)},
     }
+    out["l2_flushed"] = l2_flushed(wl, stream, device, peak)
     out["e2e"] = None
     if isinstance(wl, AllReduce) and not args.no_e2e:
         out["e2e"] = run_e2e(args, wl.t_bufs, wl.n, wl.count, world, stream, device)
     wl.teardown()
     return out, sample
+
+
+def l2_flushed(wl, stream, device, peak, steps=20):
+    """The workload's step timed one call at a time with L2 flushed before
+    each (a write of twice the 129 MB L2 on the same stream, outside the
+    timed events): the median step time, as a cross-check that L2 residency
+    between back-to-back steps does not inflate the headline figure."""
+    import torch
+    scratch = torch.empty(2 * (129 << 20), dtype=torch.uint8, device=device)
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(steps + 3):
+            scratch.fill_(i & 0xff)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            wl.step(stream)
+            e1.record(stream)
+            e1.synchronize()
+            if i >= 3:
+                times.append(e0.elapsed_time(e1))
+    del scratch
+    ms = statistics.median(times)
+    gbs = wl.nbytes / (ms * 1e-3) / 1e9
+    return {"steps": steps, "flush_bytes": 2 * (129 << 20), "ms_median": round(ms, 4),
+            "GB/s": round(gbs, 1), "frac": round(gbs / peak[0], 4)}
 
 
 def run_e2e(args, bufs, n, count, world, stream, device):
@@ -1276,7 +1302,8 @@ def main(argv=None):
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32",
                 "data": "synthetic",
                 "config": config,
-                "roofline": head["roofline"], "cpu_baseline": cpu, "e2e": head["e2e"],
+                "roofline": head["roofline"], "l2_flushed": head["l2_flushed"],
+                "cpu_baseline": cpu, "e2e": head["e2e"],
                 "gpu_launches": head["gpu_launches"], "clocks": head["clocks"],
                 "frac_of_peak": round(head["value"] / world / peak[0], 4),
                 "rows": rows, "ddp_overlap": overlap, "wire_error": wire}

@@ -51,6 +51,8 @@ def test_headline_line_has_every_key(tmp_path):
     c = d["cpu_baseline"]
     assert c["kind"] == "oracle" and c["cores"] == 1 and c["value"] > 0
     assert d["clocks"]["sm_mhz"] > 0 and "reasons" in d["clocks"]
+    f = d["l2_flushed"]  # the same step with L2 flushed before each call
+    assert f["steps"] >= 20 and f["flush_bytes"] > 2 * (128 << 20) and f["GB/s"] > 0
     assert d["config"]["workload"] == "allreduce_avg_bf16_8ranks_64MiB"
     names = [row["name"] for row in d["rows"]]
     assert "reduce_scatter_avg_bf16_8ranks_64MiB" in names and len(names) >= 10
