@@ -2,7 +2,9 @@
 configuration the benchmark times: the fused bucket all-reduce over the 300
 seeded tensors (three chained launches), the clipped FSDP step over 1.3e9
 parameters with max_norm 1.0 (the norm is about 12.7, so clipping is
-active), and the no_sync accumulation rows over 8 x 2^25 elements.
+active), the no_sync accumulation rows over 8 x 2^25 elements, and the
+end-to-end leg: the 8 x 64 MiB all-reduce over rank buffers in pinned host
+memory, through both host entry points.
 
 As in test_fullsize_gpu.py, the oracle computes a seeded random sample of
 output elements one by one from the same elements' inputs.  The clipped
@@ -172,4 +174,35 @@ def test_accumulate_rows_sampled(reduce):
     for r in range(n):
         assert_match(got[:, r].copy(), want if reduce else sums[:, r].copy(), "f32", f"rank {r}")
     del acc, grads
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("api", ["host", "staged"])
+def test_all_reduce_from_host_memory_full_sampled(api):
+    """The benchmark's end-to-end leg: 8 x 64 MiB bf16 rank buffers in
+    pinned host memory, all-reduced AVG by cr_all_reduce_host (the kernel
+    reads and writes host memory) or cr_all_reduce_staged (copy engines,
+    sliced over three streams, 2^22-element slices as benchmarked)."""
+    n, count = 8, 1 << 25
+    dev_bufs = ranks(n, count, torch.bfloat16, 0.02, 0)
+    host_in = [b.cpu().pin_memory() for b in dev_bufs]
+    host_out = [torch.empty(count, dtype=torch.bfloat16).pin_memory() for _ in range(n)]
+    idx = sample_idx(count, seed=8, k=1 << 18)
+    L = count // n
+    want = O.fold_columns(gather(dev_bufs, idx, "bf16"), (idx.cpu().numpy() // L).astype(np.int32),
+                          "bf16", "avg", "bf16")
+    if api == "host":
+        cr.cr_all_reduce_host(host_in, host_out, count, "bf16", "avg")
+    else:
+        up, down = torch.cuda.Stream(), torch.cuda.Stream()
+        cr.cr_all_reduce_staged(host_in, host_out, dev_bufs, count, "bf16", "avg", 1 << 22,
+                                torch.cuda.current_stream(), up, down)
+    torch.cuda.synchronize()
+    hidx = idx.cpu()
+    for r in range(n):
+        got = host_out[r][hidx].view(torch.int16).numpy().view(np.uint16).copy()
+        assert_match(got, want, "bf16", f"{api} rank {r}")
+    for r in range(1, n):
+        assert torch.equal(host_out[r].view(torch.int16), host_out[0].view(torch.int16))
+    del dev_bufs, host_in, host_out
     torch.cuda.empty_cache()
