@@ -257,7 +257,7 @@ class AllReduce(Workload):
         self.nbytes = ar_bytes(n, count, es)
         mib = count * es >> 20
         self.name = f"allreduce_{op}_{dtype}_{n}ranks_{mib}MiB"
-        self.kernel = f"k_fold_vec<{dtype},{dtype},AR,{n}>"
+        self.kernel = f"k_fold_vec3<{dtype},{dtype},AR,{n}>"
         self.profile = f"k_fold_vec_allreduce_{dtype}_{n}x{mib}MiB"
 
     def setup(self, device):
@@ -279,7 +279,7 @@ class AllReduceWire(Workload):
         self.nbytes = ar_bytes(n, count, 2)
         mib = count * 2 >> 20
         self.name = f"allreduce_avg_bf16_bf16wire_{n}ranks_{mib}MiB"
-        self.kernel = f"k_fold_vec<bf16,bf16,AR,{n},wire>"
+        self.kernel = f"k_fold_vec3<bf16,bf16,AR,{n},wire>"
         self.profile = f"k_fold_vec_allreduce_bf16wire_{n}x{mib}MiB"
 
     def setup(self, device):
@@ -325,7 +325,7 @@ class ReduceScatter(Workload):
         self.n, self.count = n, count
         self.nbytes = n * count * 2 + count * 2
         self.name = f"reduce_scatter_avg_bf16_{n}ranks_{count * 2 >> 20}MiB"
-        self.kernel = f"k_fold_vec<bf16,bf16,RS,{n}>"
+        self.kernel = f"k_fold_vec3<bf16,bf16,RS,{n}>"
         self.profile = f"k_fold_vec_reduce_scatter_bf16_{n}x{count * 2 >> 20}MiB"
 
     def setup(self, device):

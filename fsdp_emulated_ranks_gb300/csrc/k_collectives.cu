@@ -49,19 +49,10 @@ __device__ __forceinline__ void fold_store_elem(const FoldArgs& a, int n, uint64
 
 // Elements [a.begin, a.end) of every rank buffer; chunks (and so the fold
 // order) are those of the whole buffer of a.count elements.  NW: 4 or 8
-// words per vector (16 or 32 bytes of input).
-//
-// Occupancy: with a compile-time rank count and 32-byte vectors the kernel
-// is built for 3 resident CTAs per SM (up to 85 registers).  Left to
-// itself ptxas picks 42-48 registers and interleaves the adds with the N
-// loads; at the larger budget it keeps more of them in flight, and the
-// 8 x 64 MiB bf16 reduce-scatter runs 2.4 % faster on a GB300 (86.3
-// against 88.5 us, all-reduce unchanged).  The runtime-N kernels, which
-// would spill, and the 16-byte ones, which the host-memory path runs at
-// 4 CTAs per SM, keep the default.
+// words per vector (16 or 32 bytes of input).  The body of k_fold_vec and
+// k_fold_vec3, which differ only in their launch bounds.
 template <int DI, int DO, int MODE, int NT, int NW, bool WIRE>
-__global__ void __launch_bounds__(kBlock, (NT > 0 && NW == 8) ? 3 : 1)
-    k_fold_vec(const __grid_constant__ FoldArgs a) {
+__device__ __forceinline__ void fold_range(const FoldArgs& a) {
   using Acc = typename Elem<DI>::Acc;
   constexpr int IS = Elem<DI>::kSize;
   constexpr int OS = Elem<DO>::kSize;
@@ -115,6 +106,25 @@ __global__ void __launch_bounds__(kBlock, (NT > 0 && NW == 8) ? 3 : 1)
   } else if (tid < a.end - a.begin) {
     fold_store_elem<DI, DO, MODE, WIRE>(a, n, a.begin + tid);
   }
+}
+
+template <int DI, int DO, int MODE, int NT, int NW, bool WIRE>
+__global__ void __launch_bounds__(kBlock) k_fold_vec(const __grid_constant__ FoldArgs a) {
+  fold_range<DI, DO, MODE, NT, NW, WIRE>(a);
+}
+
+// The same kernel built for 3 resident CTAs per SM (up to 85 registers),
+// for a compile-time rank count and 32-byte vectors.  Left to itself
+// ptxas gives the kernel 42-48 registers and interleaves the adds with the
+// N loads; at the larger budget it keeps more of them in flight, and the
+// 8 x 64 MiB bf16 reduce-scatter runs 2.4 % faster on a GB300 (86.3
+// against 88.5 us; the all-reduce is unchanged).  The runtime-N kernels,
+// which would spill, and the 16-byte ones, which the host-memory path runs
+// at 4 CTAs per SM, keep the default bounds (an explicit minimum of one
+// CTA is not the same to ptxas: it raises their registers).
+template <int DI, int DO, int MODE, int NT, int NW, bool WIRE>
+__global__ void __launch_bounds__(kBlock, 3) k_fold_vec3(const __grid_constant__ FoldArgs a) {
+  fold_range<DI, DO, MODE, NT, NW, WIRE>(a);
 }
 
 template <int DI, int DO, int MODE, bool WIRE>
@@ -226,14 +236,24 @@ static cudaError_t launch_fold_kernel(K kernel, const FoldArgs& a, uint64_t thre
   return cudaGetLastError();
 }
 
+// A compile-time rank count: 32-byte vectors take the kernel built for 3
+// CTAs per SM, 16-byte ones the default.
+template <int DI, int DO, int MODE, int NT, int NW, bool WIRE>
+static cudaError_t launch_fixed_n(const FoldArgs& a, uint64_t threads, cudaStream_t s) {
+  if constexpr (NW == 8)
+    return launch_fold_kernel(k_fold_vec3<DI, DO, MODE, NT, NW, WIRE>, a, threads, s);
+  else
+    return launch_fold_kernel(k_fold_vec<DI, DO, MODE, NT, NW, WIRE>, a, threads, s);
+}
+
 template <int DI, int DO, int MODE, int NW, bool WIRE>
 static cudaError_t fold_dispatch_nw(const FoldArgs& a, cudaStream_t s) {
   constexpr int VEC = elems_per<DI, NW>();
   const uint64_t threads = (a.end - a.begin) / VEC + 2 * VEC;
   switch (a.n) {
-    case 2: return launch_fold_kernel(k_fold_vec<DI, DO, MODE, 2, NW, WIRE>, a, threads, s);
-    case 4: return launch_fold_kernel(k_fold_vec<DI, DO, MODE, 4, NW, WIRE>, a, threads, s);
-    case 8: return launch_fold_kernel(k_fold_vec<DI, DO, MODE, 8, NW, WIRE>, a, threads, s);
+    case 2: return launch_fixed_n<DI, DO, MODE, 2, NW, WIRE>(a, threads, s);
+    case 4: return launch_fixed_n<DI, DO, MODE, 4, NW, WIRE>(a, threads, s);
+    case 8: return launch_fixed_n<DI, DO, MODE, 8, NW, WIRE>(a, threads, s);
     default: return launch_fold_kernel(k_fold_vec<DI, DO, MODE, 0, NW, WIRE>, a, threads, s);
   }
 }
