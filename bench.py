@@ -382,8 +382,8 @@ class Buckets(Workload):
         self.launches = {"pack": copies, "unpack": copies, "allreduce": ar_launches,
                          "pipeline": 2 * copies + ar_launches,
                          "fused": -(-len(self.numels) // min(128, 2048 // n))}[mode]
-        self.kernel = {"allreduce": "k_bucket_fused<bf16,8>",
-                       "fused": "k_bucket_fused<bf16,8>"}.get(mode, "k_copy_segments")
+        self.kernel = {"allreduce": "k_bucket_fused3<bf16,8>",
+                       "fused": "k_bucket_fused3<bf16,8>"}.get(mode, "k_copy_segments")
         self.profile = (f"k_bucket_fused_bucket_{mode}_bf16_{n}x{ntensors}"
                         if mode in ("allreduce", "fused")
                         else f"k_copy_segments_bucket_{mode}_bf16_{n}x{ntensors}")
