@@ -303,7 +303,7 @@ class Hsdp(Workload):
         self.nbytes = n * count * 2 + R * count * 2
         mib = count * 2 >> 20
         self.name = f"hsdp_reduce_scatter_avg_bf16_{R}x{S}mesh_{mib}MiB"
-        self.kernel = f"k_hsdp_vec<bf16,bf16,{R},{S},8>"
+        self.kernel = f"k_hsdp_vec4<bf16,bf16,{R},{S},8>"
         self.profile = f"k_hsdp_vec_hsdp_bf16_{R}x{S}x{mib}MiB"
 
     def setup(self, device):
@@ -439,7 +439,7 @@ class FsdpStep(Workload):
         self.nbytes = ((6 if clip else 4) * n + 24) * count
         tag = f"{count / 1e9:g}e9" if count >= 10 ** 8 else str(count)
         self.name = f"fsdp_step{'_clipped' if clip else ''}_bf16_{n}ranks_{tag}params"
-        self.kernel = f"k_fsdp_vec<{n}>" + (" + k_fsdp_sumsq + k_clip_coef" if clip else "")
+        self.kernel = f"k_fsdp_vec4<{n}>" + (" + k_fsdp_sumsq + k_clip_coef" if clip else "")
         self.profile = f"k_fsdp_vec_fsdp_step{'_clipped' if clip else ''}_{n}x{tag}"
         self.launches = 3 if clip else 1
 

@@ -98,12 +98,10 @@ __global__ void __launch_bounds__(kBlock)
 }
 
 // Vector path: 8 elements (one 16-byte bf16 vector per rank) per thread and
-// iteration; SW = 8 moves the fp32 state in 32-byte accesses.  Registers
-// are capped for 4 resident CTAs per SM (63 per thread, no spills), which
-// GB300 runs about 1 % faster than the 3 CTAs that 70 registers allow.
+// iteration; SW = 8 moves the fp32 state in 32-byte accesses.  The body of
+// k_fsdp_vec and k_fsdp_vec4, which differ only in their launch bounds.
 template <int NT, int SW>
-__global__ void __launch_bounds__(kBlock, 4)
-    k_fsdp_vec(const __grid_constant__ FsdpArgs a) {
+__device__ __forceinline__ void fsdp_range(const FsdpArgs& a) {
   const int n = NT > 0 ? NT : a.n;
   const float coef = clip_coef(a);
   const uint64_t nvec = a.count / 8;
@@ -123,6 +121,20 @@ __global__ void __launch_bounds__(kBlock, 4)
     CR_DCHECK(fastdiv_div(a.Ld, e) == e / a.L && e / a.L < (uint64_t)n, kChkFsdp);
     fsdp_element(a.grads, a.params, a.master, a.m, a.v, n, a.L, a.Ld, a.inv_n, a.a, coef, e);
   }
+}
+
+// A runtime rank count: default bounds (the 4-CTA bound would spill it).
+template <int NT, int SW>
+__global__ void __launch_bounds__(kBlock) k_fsdp_vec(const __grid_constant__ FsdpArgs a) {
+  fsdp_range<NT, SW>(a);
+}
+
+// A compile-time rank count, registers capped for 4 resident CTAs per SM
+// (63 per thread, no spills), which GB300 runs about 1 % faster than the
+// 3 CTAs that 70 registers allow.
+template <int NT, int SW>
+__global__ void __launch_bounds__(kBlock, 4) k_fsdp_vec4(const __grid_constant__ FsdpArgs a) {
+  fsdp_range<NT, SW>(a);
 }
 
 __global__ void __launch_bounds__(kBlock)
@@ -200,9 +212,9 @@ template <int SW>
 static cudaError_t fsdp_dispatch(const FsdpArgs& a, cudaStream_t s) {
   const uint64_t threads = a.count / 8 + 1;
   switch (a.n) {
-    case 2: return launch_flat(k_fsdp_vec<2, SW>, a, threads, s);
-    case 4: return launch_flat(k_fsdp_vec<4, SW>, a, threads, s);
-    case 8: return launch_flat(k_fsdp_vec<8, SW>, a, threads, s);
+    case 2: return launch_flat(k_fsdp_vec4<2, SW>, a, threads, s);
+    case 4: return launch_flat(k_fsdp_vec4<4, SW>, a, threads, s);
+    case 8: return launch_flat(k_fsdp_vec4<8, SW>, a, threads, s);
     default: return launch_flat(k_fsdp_vec<0, SW>, a, threads, s);
   }
 }

@@ -52,12 +52,10 @@ __device__ __forceinline__ void hsdp_elem(const HsdpArgs& a, int R, int S, uint6
 }
 
 // One vector of VEC elements per thread over [0, count); RT/ST > 0 fix the
-// mesh shape at compile time so that all N loads are issued together.
-// Registers are capped for 4 resident CTAs per SM (64 per thread, no
-// spills): on GB300 that is 6 % faster than the 3 CTAs that 68 allow.
+// mesh shape at compile time so that all N loads are issued together.  The
+// body of k_hsdp_vec and k_hsdp_vec4, which differ only in launch bounds.
 template <int DI, int DO, int RT, int ST, int NW>
-__global__ void __launch_bounds__(kBlock, 4)
-    k_hsdp_vec(const __grid_constant__ HsdpArgs a) {
+__device__ __forceinline__ void hsdp_range(const HsdpArgs& a) {
   using Acc = typename Elem<DI>::Acc;
   constexpr int IS = Elem<DI>::kSize;
   constexpr int OS = Elem<DO>::kSize;
@@ -115,6 +113,20 @@ __global__ void __launch_bounds__(kBlock, 4)
   if (tid < tail) hsdp_elem<DI, DO>(a, R, S, nvec * VEC + tid);
 }
 
+// A runtime mesh shape: default bounds (the 4-CTA bound would spill it).
+template <int DI, int DO, int RT, int ST, int NW>
+__global__ void __launch_bounds__(kBlock) k_hsdp_vec(const __grid_constant__ HsdpArgs a) {
+  hsdp_range<DI, DO, RT, ST, NW>(a);
+}
+
+// A compile-time mesh shape, registers capped for 4 resident CTAs per SM
+// (64 per thread, no spills): on GB300 that is 6 % faster than the 3 CTAs
+// that 68 allow.
+template <int DI, int DO, int RT, int ST, int NW>
+__global__ void __launch_bounds__(kBlock, 4) k_hsdp_vec4(const __grid_constant__ HsdpArgs a) {
+  hsdp_range<DI, DO, RT, ST, NW>(a);
+}
+
 template <int DI, int DO>
 __global__ void __launch_bounds__(kBlock)
     k_hsdp_elem(const __grid_constant__ HsdpArgs a) {
@@ -135,9 +147,9 @@ template <int DI, int DO, int NW>
 static cudaError_t hsdp_dispatch_nw(const HsdpArgs& a, cudaStream_t s) {
   constexpr int VEC = elems_per<DI, NW>();
   const uint64_t threads = a.count / VEC + VEC;
-  if (a.R == 2 && a.S == 4) return launch_flat_hsdp(k_hsdp_vec<DI, DO, 2, 4, NW>, a, threads, s);
-  if (a.R == 4 && a.S == 2) return launch_flat_hsdp(k_hsdp_vec<DI, DO, 4, 2, NW>, a, threads, s);
-  if (a.R == 2 && a.S == 2) return launch_flat_hsdp(k_hsdp_vec<DI, DO, 2, 2, NW>, a, threads, s);
+  if (a.R == 2 && a.S == 4) return launch_flat_hsdp(k_hsdp_vec4<DI, DO, 2, 4, NW>, a, threads, s);
+  if (a.R == 4 && a.S == 2) return launch_flat_hsdp(k_hsdp_vec4<DI, DO, 4, 2, NW>, a, threads, s);
+  if (a.R == 2 && a.S == 2) return launch_flat_hsdp(k_hsdp_vec4<DI, DO, 2, 2, NW>, a, threads, s);
   return launch_flat_hsdp(k_hsdp_vec<DI, DO, 0, 0, NW>, a, threads, s);
 }
 
