@@ -1,7 +1,9 @@
 // k_collectives.cu -- reduce-scatter, all-reduce and all-gather kernels.
 //
-// Reduce-scatter / all-reduce: k_fold_vec reads element e of every rank
-// buffer with 16- or 32-byte streaming loads, folds them in ring order
+// Reduce-scatter / all-reduce: k_fold_vec (k_fold_vec3 for a compile-time
+// rank count with 32-byte vectors, the same body built for 3 CTAs per SM)
+// reads element e of every rank buffer with 16- or 32-byte streaming
+// loads, folds them in ring order
 // (fold.cuh), applies the AVG / cast epilogue in registers and writes either
 // shard j (reduce-scatter, [DT] section 2 Reduce-Scatter) or every rank
 // buffer (all-reduce = reduce-scatter + all-gather fused, [DT] section 2
@@ -16,8 +18,8 @@
 // [DT] = "Distributed Training for Large Models: Collectives, FSDP/ZeRO,
 // DeviceMesh, and Multi-Dimensional Parallelism".
 //
-// Launch shape: one vector per thread, as many CTAs as vectors need (a
-// grid-stride loop covers any remainder).  On a GB300 this beats a
+// Launch shape (fold): one vector per thread, as many CTAs as vectors need
+// (a grid-stride loop covers any remainder).  On a GB300 this beats a
 // persistent grid of resident CTAs by 5-8 %: there is no per-thread
 // sequence of dependent iterations and the last wave is short.  Ragged
 // ends and buffers that are not 16-byte aligned go through the
