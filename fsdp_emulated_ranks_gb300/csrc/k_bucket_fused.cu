@@ -109,8 +109,13 @@ __device__ __forceinline__ void fused_tiles(const FusedArgs& a, uint32_t ntiles)
   pdl_wait_prerequisites();
 }
 
+// A runtime rank count: built for 2 CTAs per SM (126-128 registers, 128-160
+// bytes of spills).  At
+// N = 16 (100 tensors of the DDP workload) GB300 runs it at 6,690 GB/s,
+// against 6,240 with default bounds (162-164 registers, 1 CTA per SM) and
+// 5,210 when built for 3.
 template <int D, int NT>
-__global__ void __launch_bounds__(kBlock)
+__global__ void __launch_bounds__(kBlock, 2)
     k_bucket_fused(const __grid_constant__ FusedArgs a, uint32_t ntiles) {
   fused_tiles<D, NT>(a, ntiles);
 }
@@ -120,8 +125,8 @@ __global__ void __launch_bounds__(kBlock)
 // budget keeps more of the N loads in flight: on a GB300 the 52-bucket
 // all-reduce of the DDP workload runs at 7,046 against 6,803 GB/s, the
 // fused all-reduce of its 300 tensors at 6,982 against 6,752 (A/B on one
-// box).  The runtime-N kernel would spill under the bound and keeps the
-// default.
+// box).  The runtime-N kernel, above, spills too much under this bound
+// and is built for 2.
 template <int D, int NT>
 __global__ void __launch_bounds__(kBlock, 3)
     k_bucket_fused3(const __grid_constant__ FusedArgs a, uint32_t ntiles) {
