@@ -74,3 +74,18 @@ def test_reference_arm_matches_the_metric():
         assert ref[k] == mine[k], k
     assert ref["config"]["workload"] == mine["config"]["workload"]
     assert ref["e2e"]["h2d_bytes_per_step"] == 0 and ref["cpu_baseline"]["kind"] == "oracle"
+
+
+@pytest.mark.parametrize("config,workload", [(1, "allreduce_sum_f32_4ranks_4MiB"),
+                                             (3, "_bucket_pipeline_bf16_8ranks")])
+def test_config_flag_selects_the_same_workload_in_both_arms(config, workload):
+    mine = run(["--config", str(config), "--steps", "5", "--warmup", "3", "--no-rows",
+                "--no-e2e", "--no-cpu-baseline"])
+    ref = run(["--impl", "reference", "--config", str(config), "--steps", "1", "--warmup", "3",
+               "--ref-sample", str(1 << 16)])
+    assert workload in mine["config"]["workload"]
+    assert ref["config"]["workload"] == mine["config"]["workload"]
+    assert mine["value"] > 0 and mine["gpu_launches"] >= 5
+    assert mine["roofline"]["bound"] == "hbm" and mine["roofline"]["achieved"] > 0
+    for k in ("metric", "unit", "higher_is_better", "dtype"):
+        assert ref[k] == mine[k], k
