@@ -1196,7 +1196,8 @@ def run_sweep(args, device, stream, peak):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", "--iters", dest="steps", type=int, default=200,
+                    help="timed steps (--iters is the same flag)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--sweep", action="store_true")

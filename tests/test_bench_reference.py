@@ -4,7 +4,7 @@
 other arm measures: the line names that workload, counts the sample's bytes
 by the workload's own formula, and says what the sample was.  --config picks
 the benchmark configurations by number and --seed shifts the input values
-only.
+only.  --iters is another name for --steps.
 """
 import argparse
 import json
@@ -73,3 +73,8 @@ def test_config_numbers_and_seed(capsys):
         bench.SEED_OFFSET = 0
     assert a.nbytes == b.nbytes
     assert any((x != y).any() for x, y in zip(out_a, out_b))
+
+
+def test_iters_is_steps(capsys):
+    d = reference_line(capsys, "--iters", "2")  # the later flag wins, as for --steps twice
+    assert d["steps"] == 2
