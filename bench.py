@@ -32,6 +32,7 @@ import argparse
 import ctypes
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -89,6 +90,27 @@ def job_throughput(bytes_per_rank: float, total_ms: float, steps: int, world: in
     step; the job's time is the slowest rank's.  Returns (GB/s, ms/step)."""
     ms = max_over_ranks(total_ms, world, device) / steps
     return world * bytes_per_rank / (ms * 1e-3) / 1e9, ms
+
+
+def host_cpu_model():
+    """The host CPU's name for the oracle's report: /proc/cpuinfo's model
+    name (x86), else lscpu's (Arm, whose /proc/cpuinfo lists part numbers
+    only), else the machine type."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine()
 
 
 def measured_peaks():
@@ -1106,7 +1128,8 @@ def run_reference(args):
             "data": "synthetic", "config": dict(workload_config(smp.full, world),
                                            sample=smp.desc),
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample,
+                             "cpu_model": host_cpu_model()},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -1128,6 +1151,7 @@ def cpu_baseline_sampled(args):
             break
     return {"value": round(passes * smp.nbytes / dt / 1e9, 4), "unit": UNIT, "cores": 1,
             "kind": "oracle",
+            "cpu_model": host_cpu_model(),
             "sample": (f"{passes} step(s) of the workload on {smp.desc} "
                        f"({smp.fraction:.3g} of its bytes), single-threaded C oracle, "
                        f"{dt:.1f} s; host has {os.cpu_count()} cores")}
@@ -1287,6 +1311,7 @@ def main(argv=None):
         gbs, secs, passes = cpu_oracle_allreduce(sample, args.cpu_seconds)
         frac = (1 << 25) // sample[0].size
         cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "cpu_model": host_cpu_model(),
                "sample": (f"{passes} pass(es) of the ring all-reduce AVG over the first "
                           f"{sample[0].size} elements of each of the 8 rank buffers "
                           f"({'all' if frac == 1 else '1/%d' % frac} of the workload's bytes), "

@@ -50,6 +50,7 @@ def test_headline_line_has_every_key(tmp_path):
     assert 0 < e["value"] < d["value"]
     c = d["cpu_baseline"]
     assert c["kind"] == "oracle" and c["cores"] == 1 and c["value"] > 0
+    assert c["cpu_model"]
     assert d["clocks"]["sm_mhz"] > 0 and "reasons" in d["clocks"]
     f = d["l2_flushed"]  # the same step with L2 flushed before each call
     assert f["steps"] >= 20 and f["flush_bytes"] > 2 * (128 << 20) and f["GB/s"] > 0

@@ -78,3 +78,4 @@ def test_config_numbers_and_seed(capsys):
 def test_iters_is_steps(capsys):
     d = reference_line(capsys, "--iters", "2")  # the later flag wins, as for --steps twice
     assert d["steps"] == 2
+    assert d["cpu_baseline"]["cpu_model"]  # the host CPU is named beside the core count
