@@ -44,7 +44,7 @@
  *    undefined.  A refused launch leaves the library usable: the next call
  *    does not see the old error.  cr_last_error() gives the detail of the
  *    last failure on the calling thread.
- *  - Chunking (a1): with L = ceil(count/N), chunk j is the element range
+ *  - Chunking: with L = ceil(count/N), chunk j is the element range
  *    [j*L, min((j+1)*L, count)); trailing chunks may be short or empty, as
  *    with torch.chunk-style uneven Shard(0) shards ([DT] section 4, FSDP2).
  *    Shard j of a reduce-scatter is chunk j reduced over all ranks.
@@ -98,7 +98,7 @@ const char* cr_last_error(void);
 /* Library version, major*10000 + minor*100 + patch. */
 int cr_version(void);
 
-/* ---- a1: chunking ---------------------------------------------------------
+/* ---- chunking -------------------------------------------------------------
  * cr_chunk_len: L = ceil(count/nranks) (0 if nranks < 1).
  * cr_shard_range: element range [*lo, *hi) of chunk j.  CR_ERR_INVALID_ARG
  * if nranks is outside [1, CR_MAX_RANKS], j outside [0, nranks) or an output
@@ -107,7 +107,7 @@ size_t cr_chunk_len(size_t count, int nranks);
 cr_status cr_shard_range(size_t count, int nranks, int j, size_t* lo,
                          size_t* hi);
 
-/* ---- a2/a3: reduce-scatter ------------------------------------------------
+/* ---- reduce-scatter -------------------------------------------------------
  * [DT] section 2, Reduce-Scatter: y_j = sum over source ranks i of x_{j,i},
  * where x_{j,i} is chunk j of rank i's buffer; rank j keeps y_j.
  *   bufs[r]        rank r's input, `count` elements of in_dtype
@@ -125,7 +125,7 @@ cr_status cr_reduce_scatter(const void* const* bufs, int nranks, size_t count,
                             void* const* out_shards, cr_dtype out_dtype,
                             cr_stream_t stream);
 
-/* ---- a4: all-gather -------------------------------------------------------
+/* ---- all-gather -----------------------------------------------------------
  * [DT] section 2, All-Gather: every rank receives concat(p_0, ..., p_{N-1}).
  *   shards[j]  shard j, cr_shard_range length, of dtype (NULL if empty)
  *   bufs[r]    rank r's output, `count` elements:
@@ -136,7 +136,7 @@ cr_status cr_reduce_scatter(const void* const* bufs, int nranks, size_t count,
 cr_status cr_all_gather(const void* const* shards, int nranks, size_t count,
                         cr_dtype dtype, void* const* bufs, cr_stream_t stream);
 
-/* ---- a5: all-reduce -------------------------------------------------------
+/* ---- all-reduce -----------------------------------------------------------
  * [DT] section 2, All-Reduce = Reduce-Scatter + All-Gather, fused into one
  * kernel: every element of every output buffer receives the reduced value
  * of that element.  in[r] and out[r], `count` elements each.  in == out per
@@ -147,7 +147,7 @@ cr_status cr_all_reduce(const void* const* in, int nranks, size_t count,
                         cr_dtype in_dtype, cr_op op, void* const* out,
                         cr_dtype out_dtype, cr_stream_t stream);
 
-/* ---- a5 from host memory: pipelined all-reduce ---------------------------
+/* ---- all-reduce from host memory, pipelined -------------------------------
  * The all-reduce of cr_all_reduce (in place, in_dtype == out_dtype) for
  * rank buffers that live in host memory.  The range is cut into slices of
  * slice_elems elements; for each slice the call enqueues the host-to-device
@@ -220,7 +220,7 @@ cr_status cr_all_reduce_wire(const void* const* in, int nranks, size_t count,
                              void* const* out, cr_dtype out_dtype,
                              cr_stream_t stream);
 
-/* ---- HSDP: shard within a group, replicate across groups -----------------
+/* ---- HSDP: shard within a group, replicate across groups ------------------
  * [AIG] 6.3.6 (hybrid sharding: shard inside a node, replicate across
  * nodes) and [DT] section 4, FSDP2 (a 2-D mesh, one dimension sharded and the
  * other replicated).  N = R*S ranks on an R x S mesh; rank (g, s) is index
@@ -245,7 +245,7 @@ cr_status cr_hsdp_reduce_scatter(const void* const* bufs, int R, int S,
                                  void* const* out_shards, cr_dtype out_dtype,
                                  cr_stream_t stream);
 
-/* ---- a6: DDP bucket plan (host) -------------------------------------------
+/* ---- DDP bucket plan (host) -----------------------------------------------
  * [AIG] 6.2.4: gradients go into buckets (default 25 MB) in the order
  * backward produces them; [AIG] 6.2.6 Horovod Tensor Fusion; [NX] 5.1.
  * Tensors are visited from the last index to the first (backward order) and
@@ -273,7 +273,7 @@ cr_status cr_bucket_plan(const size_t* numels, int ntensors, size_t elem_size,
                          size_t cap_bytes, cr_bucket_plan_t** plan);
 void cr_bucket_plan_free(cr_bucket_plan_t* plan);
 
-/* ---- a7: bucket pack / unpack ---------------------------------------------
+/* ---- bucket pack / unpack -------------------------------------------------
  * Byte copies between each rank's tensors and its buckets:
  *   pack:   buckets[r*B + b][off_t + i] = tensors[r*T + t][i]
  *   unpack: tensors[r*T + t][i] = buckets[r*B + b][off_t + i]
@@ -317,7 +317,7 @@ cr_status cr_bucket_all_reduce_fused(const cr_bucket_plan_t* plan, int nranks,
                                      void* const* tensors, cr_dtype dtype,
                                      cr_op op, cr_stream_t stream);
 
-/* ---- DDP reducer: bucket all-reduce overlapped with backward ---------------
+/* ---- DDP reducer: bucket all-reduce overlapped with backward --------------
  * [AIG] 6.2.4-6.2.5 (figure 6-2): backward produces gradients last layer
  * first; as soon as every gradient of a bucket is ready, that bucket's
  * all-reduce starts on the communication stream while backward goes on.
@@ -359,7 +359,7 @@ int cr_reducer_launched(const cr_reducer_t* red);
 cr_status cr_reducer_finalize(cr_reducer_t* red, cr_stream_t compute_stream);
 void cr_reducer_destroy(cr_reducer_t* red);
 
-/* ---- thread-per-rank communicator --------------------------------------------
+/* ---- thread-per-rank communicator -----------------------------------------
  * [DT] section 2 and [AIG] 6.1: with real ranks, every rank calls a
  * collective on its own tensor and the collective runs once all ranks have
  * called it.  cr_comm_t gives the emulated ranks that form: each rank's host
@@ -400,7 +400,7 @@ cr_status cr_comm_all_gather(cr_comm_t* comm, int rank, const void* shard,
 int cr_comm_broken(const cr_comm_t* comm);
 void cr_comm_destroy(cr_comm_t* comm);
 
-/* ---- a8..a10: fused FSDP / ZeRO-3 step ------------------------------------
+/* ---- fused FSDP / ZeRO-3 step ---------------------------------------------
  * One kernel performs the step of [DT] section 4 (ZeRO-3/FSDP flow steps
  * 5-6; FSDP1 unit lifecycle "backward post-hook" then "optimizer step" then
  * the next forward's all-gather) for one flat parameter buffer:
@@ -486,7 +486,7 @@ cr_status cr_fsdp_step_clipped_noalloc(const void* const* grads_bf16,
                                        void* const* params_bf16,
                                        float* norm_out, cr_stream_t stream);
 
-/* ---- FSDP2: per-parameter Shard(0) ---------------------------------------
+/* ---- FSDP2: per-parameter Shard(0) ----------------------------------------
  * [DT] section 4, FSDP2: every parameter is its own DTensor with placement
  * Shard(0): of a parameter with dim0 rows of row_numel elements, rank j
  * owns rows [j*Lr, min((j+1)*Lr, dim0)), Lr = ceil(dim0/N) -- uneven, and
@@ -513,7 +513,7 @@ cr_status cr_fsdp2_step(const cr_param_shape* shapes, int nparams, int nranks,
                         const cr_adamw_cfg* cfg, void* const* params_bf16,
                         cr_stream_t stream);
 
-/* ---- DDP gradient accumulation (no_sync) ---------------------------------
+/* ---- DDP gradient accumulation (no_sync) ----------------------------------
  * "AI Infra Guide, Chapter 6", 6.2.6: micro-steps inside model.no_sync()
  * only accumulate their gradient locally; the last one accumulates and then
  * all-reduces the sum.
@@ -535,7 +535,7 @@ cr_status cr_all_reduce_accumulate(float* const* acc, int nranks, size_t count,
                                    cr_dtype grad_dtype, cr_op op,
                                    cr_stream_t stream);
 
-/* a9 alone: AdamW as above on n fp32 elements with an fp32 gradient
+/* AdamW alone: as above, on n fp32 elements with an fp32 gradient
  * (for example a shard produced by cr_reduce_scatter with out_dtype F32);
  * param_bf16 (may be NULL) receives the bf16 cast of the updated master.
  * No overlaps allowed. */
@@ -543,7 +543,7 @@ cr_status cr_adamw_step(size_t n, float* master, float* m, float* v,
                         const float* grad, const cr_adamw_cfg* cfg,
                         void* param_bf16, cr_stream_t stream);
 
-/* ---- device-side checks (test builds) --------------------------------------
+/* ---- device-side checks (test builds) -------------------------------------
  * The library can be built as a checked variant whose kernels verify, before
  * touching memory, the index arithmetic their accesses rest on (the chunk of
  * an element is a rank, its offset lies inside that rank's shard, a tile
@@ -557,7 +557,7 @@ cr_status cr_adamw_step(size_t n, float* master, float* m, float* v,
 long long cr_check_word(int clear);
 cr_status cr_check_selftest(cr_stream_t stream);
 
-/* ---- a11: communication accounting (host) ---------------------------------
+/* ---- communication accounting (host) --------------------------------------
  * Elements rank `rank` sends and receives, and the logical steps taken, in
  * the ring schedule of [DT] section 2 (reduce-scatter N-1 steps, all-gather
  * N-1 steps, all-reduce both) or in the naive schedule of [NX] 2.2

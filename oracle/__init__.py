@@ -134,7 +134,7 @@ def _cfg(c: AdamWConfig) -> _AdamCfg:
     return _AdamCfg(c.lr, c.beta1, c.beta2, c.eps, c.weight_decay, c.step)
 
 
-# ---- a1 -------------------------------------------------------------------
+# ---- chunking ---------------------------------------------------------------
 
 def chunk_len(count: int, n: int) -> int:
     return lib().orc_chunk_len(count, n)
@@ -157,7 +157,7 @@ def bf16_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.asarray(b, np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
-# ---- a2..a5 ---------------------------------------------------------------
+# ---- ring collectives -------------------------------------------------------
 
 def _shards_out(count, n, dtype):
     out = []
@@ -253,7 +253,7 @@ def naive_all_reduce(bufs, dtype, op="sum", out_dtype=None):
     return out, _traffic(tr, n)
 
 
-# ---- a9 / a8..a10 -----------------------------------------------------------
+# ---- AdamW and the FSDP step ------------------------------------------------
 
 def adamw(p, m, v, g, cfg: AdamWConfig) -> None:
     """In-place scalar AdamW on float32 arrays."""
@@ -372,7 +372,7 @@ def accumulate(acc: np.ndarray, g: np.ndarray, dtype: str) -> None:
     lib().orc_accumulate(acc.size, acc.ctypes.data, g.ctypes.data, _DT[dtype])
 
 
-# ---- a6 / a7 ----------------------------------------------------------------
+# ---- DDP buckets ------------------------------------------------------------
 
 @dataclass
 class BucketPlan:
@@ -439,7 +439,7 @@ def bucketed_all_reduce(plan: BucketPlan, tensors_per_rank, dtype, op="avg"):
     return bucket_unpack(plan, buckets, _NP[dtype])
 
 
-# ---- a11 ----------------------------------------------------------------------
+# ---- communication accounting -----------------------------------------------
 
 def alpha_beta_ring_allreduce(n: int, nbytes: float, alpha_s: float,
                               bw_bytes_per_s: float) -> float:

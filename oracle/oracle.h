@@ -46,7 +46,7 @@ enum { ORC_OK = 0, ORC_EINVAL = 1, ORC_EUNSUPPORTED = 2, ORC_ENOMEM = 3 };
 
 #define ORC_MAX_RANKS 64
 
-/* ---- a1: chunking ---------------------------------------------------- */
+/* ---- chunking -------------------------------------------------------- */
 size_t orc_chunk_len(size_t count, int n);
 void orc_chunk_bounds(size_t count, int n, int j, size_t* lo, size_t* hi);
 
@@ -64,7 +64,7 @@ typedef struct {
   int steps;                     /* logical communication steps taken    */
 } orc_traffic;
 
-/* ---- a2/a3: ring reduce-scatter, literal message-passing simulation ----
+/* ---- ring reduce-scatter, literal message-passing simulation ------------
  * Ring direction r -> r+1.  At step s (1..N-1) rank r sends the partial sum
  * it holds for chunk (r-s) mod N; the receiver adds its own contribution to
  * the same chunk (partial + local).  Chunk j therefore starts at rank j+1
@@ -128,7 +128,7 @@ int orc_fold_columns(int n, size_t nsamp, int in_dtype, int op,
                      const void* vals, const int* chunk, void* out,
                      int out_dtype);
 
-/* ---- a4: ring all-gather, literal simulation ---------------------------
+/* ---- ring all-gather, literal simulation --------------------------------
  * Rank r starts with shard r.  At step s (1..N-1) every rank forwards the
  * shard it received at the previous step (its own at step 1) to r+1
  * ([DT] section 2, All-Reduce second phase, N=4 ring).  Each rank keeps its
@@ -143,7 +143,7 @@ int orc_ring_all_gather_L(int n, size_t count, size_t L, int dtype,
                           const void* const* shards, void* const* bufs,
                           orc_traffic* tr, int* trace_arrival);
 
-/* ---- a5: ring all-reduce = ring reduce-scatter then ring all-gather ----
+/* ---- ring all-reduce = ring reduce-scatter then ring all-gather ---------
  * in and out may be the same buffers (in place). */
 int orc_ring_all_reduce(int n, size_t count, int in_dtype, int op,
                         const void* const* in, void* const* out,
@@ -155,7 +155,7 @@ int orc_naive_all_reduce(int n, size_t count, int in_dtype, int op,
                          const void* const* in, void* const* out,
                          int out_dtype, orc_traffic* tr);
 
-/* ---- a9: scalar AdamW --------------------------------------------------
+/* ---- scalar AdamW -------------------------------------------------------
  * Decoupled weight decay (Loshchilov & Hutter; torch.optim.AdamW named in
  * [AIG] 6.8 (FSDP production config) and [DT] section 4 FSDP2 code skeleton).  The pages never print
  * the rule; the textbook form is used, all in fp32:
@@ -173,7 +173,7 @@ typedef struct {
 void orc_adamw(size_t n, float* p, float* m, float* v, const float* g,
                const orc_adamw_cfg* cfg);
 
-/* ---- a8..a10: FSDP step -------------------------------------------------
+/* ---- FSDP step ----------------------------------------------------------
  * The FSDP1 flat-parameter lifecycle restricted to one step ([DT] section 4,
  * FSDP1 lifecycle; ZeRO-3 flow steps 5-6): ring reduce-scatter of the bf16
  * grads with fp32 partials and AVG (reduce_dtype fp32, [AIG] 6.3.4), AdamW on
@@ -198,7 +198,7 @@ int orc_fsdp_step_clipped(int n, size_t count, const uint16_t* const* grads,
                           double max_norm, uint16_t* const* params,
                           double* norm_out);
 
-/* ---- a6/a7: DDP gradient buckets ---------------------------------------
+/* ---- DDP gradient buckets -----------------------------------------------
  * Plan: tensors are visited in reverse index order (backward order) and
  * appended to the current bucket while its byte size plus the tensor's stays
  * within cap_bytes; otherwise a new bucket starts.  A tensor is never split;
@@ -247,7 +247,7 @@ int orc_fsdp2_step(int nparams, const orc_param_shape* shapes, int n,
  * last micro-step adds its gradient and then all-reduces the sum. */
 void orc_accumulate(size_t count, float* acc, const void* g, int g_dtype);
 
-/* ---- a11: alpha-beta model ([AIG] 6.1.4; [DT] section 2; [NX] 2.3) ----
+/* ---- alpha-beta model ([AIG] 6.1.4; [DT] section 2; [NX] 2.3) -----------
  * T_ring_allreduce = 2(N-1)*alpha + 2(N-1)/N * S / B, seconds. */
 double orc_alpha_beta_ring_allreduce(int n, double bytes, double alpha_s,
                                      double bw_bytes_per_s);
