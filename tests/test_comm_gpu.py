@@ -1,7 +1,7 @@
 """The thread-per-rank communicator on the GPU: each of N host threads is a
 rank that calls the collectives on its own tensors, in the same order, for
 several rounds; results must equal the oracle's ring collectives exactly
-as the single-call entry points are (bf16 within 1 ulp, fp32 bit-exact)."""
+as the single-call entry points do (bitwise, every dtype)."""
 import threading
 
 import numpy as np

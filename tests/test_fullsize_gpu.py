@@ -15,7 +15,7 @@ import oracle as O
 from fsdp_emulated_ranks_gb300 import build as libbuild
 from fsdp_emulated_ranks_gb300 import cr
 from fsdp_emulated_ranks_gb300 import inputs as I
-from gpu_util import assert_match, rel_maxabs, to_host
+from gpu_util import assert_match, to_host
 
 pytestmark = pytest.mark.gpu
 NSAMP = 1 << 18
@@ -215,9 +215,9 @@ def test_fsdp_step_1p3b_sampled():
     O.adamw(pm, mm, vm, gavg, cfg)
     cr.cr_fsdp_step(grads, count, master, m, v, cr.adamw_cfg(), params)
     torch.cuda.synchronize()
-    assert rel_maxabs(to_host(master_full[idx], "f32"), pm) <= 1e-6
-    assert rel_maxabs(to_host(mv[:count][idx], "f32"), mm) <= 1e-6
-    assert rel_maxabs(to_host(mv[count:][idx], "f32"), vm) <= 1e-6
+    assert_match(to_host(master_full[idx], "f32"), pm, "f32", "master")
+    assert_match(to_host(mv[:count][idx], "f32"), mm, "f32", "m")
+    assert_match(to_host(mv[count:][idx], "f32"), vm, "f32", "v")
     want_p = O.f32_to_bf16(pm)
     got_p = gather(params, idx, "bf16")
     for r in range(n):
@@ -437,7 +437,7 @@ def test_fsdp2_transformer_full_sampled():
     want_p = O.fsdp2_step([(n, M)], [grads], [state[0]], [state[1]], [state[2]], O.AdamWConfig())
     for q, name in enumerate(("master", "m", "v")):
         ref = np.array([state[q][J[s]][col[s]] for s in range(len(J))], np.float32)
-        assert rel_maxabs(st1[q], ref) <= 1e-6, name
+        assert_match(st1[q], ref, "f32", name)
     for r in range(n):
         ref = want_p[0][r][J * M + col]
         assert_match(par[:, r].copy(), ref, "bf16", f"params rank {r}")

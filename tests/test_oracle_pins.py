@@ -144,6 +144,82 @@ def test_simulation_equals_closed_form_fold(n, count, dt):
             assert a.tobytes() == b.tobytes(), (op, out)
 
 
+def _columns(bufs, count, n, L, idx):
+    """The sampled elements' values on ranks 0..n-1 and the chunk each
+    element belongs to, as the full-size checks gather them."""
+    vals = np.stack([b[idx] for b in bufs], axis=1)
+    return vals, (idx // L).astype(np.int32)
+
+
+@pytest.mark.parametrize("n", [2, 3, 4, 8, 13, 64])
+@pytest.mark.parametrize("dt,op,out", [("f32", "sum", "f32"), ("f32", "avg", "f32"),
+                                       ("bf16", "sum", "bf16"), ("bf16", "avg", "bf16"),
+                                       ("bf16", "avg", "f32"), ("bf16", "sum", "f32"),
+                                       ("i32", "sum", "i32")])
+def test_fold_columns_equals_ring_simulation(n, dt, op, out):
+    """The per-element checker used at full size must give, for every
+    sampled element, the bytes the literal ring simulation gives for that
+    element: same chunk owner, same starting rank, same association, same
+    single AVG division and bf16 rounding.  count is chosen so L = ceil(C/N)
+    leaves a short last chunk (and empty ones for large N)."""
+    count = 5 * n + 3 if n < 64 else 200
+    L = math.ceil(count / n)
+    bufs = I.host_rank_buffers(n, count, dt, std=1.0, seed0=300 + n)
+    sim, _ = O.ring_reduce_scatter(bufs, dt, op, out)
+    flat = np.concatenate(sim)
+    assert flat.size == count
+    idx = np.arange(count)
+    vals, chunk = _columns(bufs, count, n, L, idx)
+    got = O.fold_columns(vals, chunk, dt, op, out)
+    assert got.tobytes() == flat.tobytes()
+    # A random subset in shuffled order, as the sampled checks use it.
+    rng = np.random.default_rng(n)
+    sub = rng.permutation(count)[: max(1, count // 3)]
+    vals, chunk = _columns(bufs, count, n, L, sub)
+    assert O.fold_columns(vals, chunk, dt, op, out).tobytes() == flat[sub].tobytes()
+
+
+def test_fold_columns_follows_page_schedule_n4(golden_dir):
+    """Against the N=4 ring schedule of the reduce-scatter figure: for each
+    chunk, the left fold in the order the trace's final partials list."""
+    order = order_from_trace(load(golden_dir, "ring_reduce_scatter_n4.json"))
+    n, count = 4, 4 * 301
+    L = count // n
+    bufs = I.host_rank_buffers(n, count, "f32", std=1.0, seed0=21)
+    vals, chunk = _columns(bufs, count, n, L, np.arange(count))
+    got = O.fold_columns(vals, chunk, "f32", "sum")
+    for e in range(count):
+        j = e // L
+        acc = np.float32(vals[e, order[j][0]])
+        for i in order[j][1:]:
+            acc = np.float32(acc + vals[e, i])
+        assert got[e].tobytes() == acc.tobytes(), e
+
+
+@pytest.mark.parametrize("n", [4, 5, 8])
+def test_fold_columns_detects_rotated_start(n):
+    """Negative check: giving each element the chunk of its neighbour (a
+    fold that starts one rank later) changes fp32 bits somewhere, and so do
+    a reversed rank order and a divide-by-N applied per addend.  So a slip
+    in the checker's (j + k) mod N indexing or in its AVG cannot pass the
+    pin above by accident."""
+    count = 64 * n
+    L = count // n
+    bufs = I.host_rank_buffers(n, count, "f32", std=1.0, seed0=700 + n)
+    vals, chunk = _columns(bufs, count, n, L, np.arange(count))
+    right = O.fold_columns(vals, chunk, "f32", "sum")
+    rotated = O.fold_columns(vals, (chunk + 1) % n, "f32", "sum")
+    assert np.any(right.view(np.uint32) != rotated.view(np.uint32))
+    reversed_order = O.fold_columns(vals[:, ::-1].copy(), (n - 1 - chunk) % n, "f32", "sum")
+    assert np.any(right.view(np.uint32) != reversed_order.view(np.uint32))
+    avg = O.fold_columns(vals, chunk, "f32", "avg")
+    per_addend = O.fold_columns((vals / np.float32(n)).astype(np.float32), chunk, "f32", "sum")
+    if n & (n - 1):   # for powers of two both forms are exact scalings
+        assert np.any(avg.view(np.uint32) != per_addend.view(np.uint32))
+    else:
+        assert avg.tobytes() == per_addend.tobytes()
+
+
 @pytest.mark.parametrize("n", [2, 3, 4, 7, 8, 16, 64])
 def test_ring_equals_naive_on_integer_values(n):
     """Integer-valued fp32 with |x| <= 2^10: every partial is exact, so the
@@ -558,6 +634,39 @@ def test_clip_norm_and_scaled_gradient(n, count):
     gp = (g_full[0] * c).astype(np.float32)
     want_m = np.float32(1 - cfg.beta1) * gp
     assert np.max(np.abs(np.concatenate(m) - want_m)) <= 2 ** -22 * np.max(np.abs(want_m))
+
+
+@pytest.mark.parametrize("n,count", [(1, 37), (3, 3 * 40 + 2), (8, 8 * 64 + 5)])
+@pytest.mark.parametrize("frac", [0.25, 10.0])
+def test_clipped_step_at_its_own_coefficient(n, count, frac):
+    """The GPU tests check the clipped step at every fp32 coefficient in the
+    norm's tolerance window by composing oracle pieces (reduce-scatter,
+    g * c, AdamW, cast, all-gather).  At the oracle's own coefficient that
+    composition must be orc_fsdp_step_clipped, bit for bit, and the window
+    must list that coefficient first."""
+    from gpu_util import clip_coefficients, oracle_clipped_at
+    grads, mk = clip_case(n, count, 90 + n)
+    cfg = O.AdamWConfig()
+    g_full, _ = O.ring_all_reduce(grads, "bf16", "avg", "f32")
+    max_norm = frac * float(np.linalg.norm(g_full[0].astype(np.float64)))
+    master, m, v = mk()
+    want_p, norm = O.fsdp_step_clipped(grads, master, m, v, cfg, max_norm)
+    coefs = clip_coefficients(max_norm, norm)
+    assert coefs[0] == np.float32(min(1.0, max_norm / (norm + 1e-6)))
+    assert len(set(float(c) for c in coefs)) == len(coefs)
+    if frac > 1:
+        assert coefs == [np.float32(1.0)]
+    ms, mm, vv = mk()
+    params = oracle_clipped_at(grads, ms, mm, vv, cfg, coefs[0])
+    for a, b in zip(ms + mm + vv, master + m + v):
+        assert a.tobytes() == b.tobytes()
+    for a, b in zip(params, want_p):
+        assert a.tobytes() == b.tobytes()
+    # a neighbouring coefficient gives different state bits
+    if frac < 1:
+        ms, mm, vv = mk()
+        oracle_clipped_at(grads, ms, mm, vv, cfg, np.nextafter(coefs[0], np.float32(2)))
+        assert any(a.tobytes() != b.tobytes() for a, b in zip(mm, m))
 
 
 # ---- FSDP2: per-parameter Shard(0) ----------------------------------------------

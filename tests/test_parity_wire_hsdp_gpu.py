@@ -4,8 +4,8 @@ seeded inputs.
 
 The bf16 wire rounds each forwarded partial exactly where the oracle's ring
 rounds its message, and HSDP folds the S ranks of a group and then the R
-groups in the two rings' orders, so fp32 / int32 results are bit-exact and
-bf16 outputs within 1 bf16 ulp (the bar of the other collectives).  Sizes
+groups in the two rings' orders, so every result is bitwise equal to the
+oracle's (the bar of the other collectives).  Sizes
 span several vectors and CTAs plus ragged tails; offsets 1 and "16B" force
 the element-wise and 16-byte kernels.
 """

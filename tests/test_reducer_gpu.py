@@ -3,7 +3,7 @@ compute stream and marked ready one by one (in backward order and in random
 orders), bucket all-reduces run on a separate communication stream with and
 without a CTA cap.  After finalize every tensor must hold, bit for bit,
 what cr_bucket_all_reduce_fused gives on the same inputs, and the oracle's
-bucketed all-reduce (fp32 results bit-exact, bf16 within 1 ulp)."""
+bucketed all-reduce (bitwise)."""
 import numpy as np
 import pytest
 import torch
