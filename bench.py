@@ -458,10 +458,17 @@ class FsdpStep(Workload):
 
     def __init__(self, n=8, count=1_300_000_000, clip=False):
         self.n, self.count, self.clip = n, count, clip
-        self.nbytes = ((6 if clip else 4) * n + 24) * count
+        # clipped, N >= 5: the first pass parks the averaged fp32 gradient in
+        # two of the parameter outputs (4 B written, 4 B read back) instead of
+        # the update pass folding the N bf16 gradients again (2N B)
+        self.stash = clip and n >= 5
+        self.nbytes = ((4 * n + 32) if self.stash else ((6 if clip else 4) * n + 24)) * count
         tag = f"{count / 1e9:g}e9" if count >= 10 ** 8 else str(count)
         self.name = f"fsdp_step{'_clipped' if clip else ''}_bf16_{n}ranks_{tag}params"
-        self.kernel = f"k_fsdp_vec4<{n}>" + (" + k_fsdp_sumsq + k_clip_coef" if clip else "")
+        if self.stash:
+            self.kernel = f"k_fsdp_sumsq<{n},stash> + k_clip_coef + k_fsdp_vec<stash>"
+        else:
+            self.kernel = f"k_fsdp_vec4<{n}>" + (" + k_fsdp_sumsq + k_clip_coef" if clip else "")
         self.profile = f"k_fsdp_vec_fsdp_step{'_clipped' if clip else ''}_{n}x{tag}"
         self.launches = 3 if clip else 1
 
@@ -696,6 +703,12 @@ def run_headline(args, world, rank, device, stream, peak):
                      "peak_source": peak[1], "step_ms_median": statistics.median(per),
                      **step_quantiles(per)},
     }
+    # the same figure from the median step (achieved/frac above: the mean)
+    med = statistics.median(per)
+    out["roofline"].update({"achieved_median": round(wl.nbytes / (med * 1e-3) / 1e9, 1),
+                            "frac_median": round(wl.nbytes / (med * 1e-3) / 1e9 / peak[0], 4)})
+    if wl.launches > 1:
+        out["roofline"]["launches"] = wl.launches
     out["l2_flushed"] = l2_flushed(wl, stream, device, peak)
     out["e2e"] = None
     if isinstance(wl, AllReduce) and not args.no_e2e:
@@ -830,6 +843,7 @@ def run_rows(args, device, stream, peak, skip=None):
                      "launches_per_call": wl.launches, "kernel": wl.kernel,
                      "traffic": traffic_per_launch(wl.profile, wl.launches),
                      "traffic_per_step": traffic_per_step(wl.profile)})
+        rows[-1]["key"] = name
         if ms < 0.05:
             # host-bound: also the same call prepared once (the C call alone)
             from fsdp_emulated_ranks_gb300 import cr
@@ -839,8 +853,47 @@ def run_rows(args, device, stream, peak, skip=None):
             rows[-1].update({"ms_prepared_median": round(pms, 4),
                              "GB/s_prepared": round(wl.nbytes / (pms * 1e-3) / 1e9, 1)})
             del prep
+            # and captured in a CUDA graph: device time per call, no host work
+            gus = graph_replay_us(wl, device, stream)
+            rows[-1].update({"graph_us": round(gus, 2),
+                             "GB/s_graph": round(wl.nbytes / (gus * 1e-6) / 1e9, 1),
+                             "frac_graph": round(wl.nbytes / (gus * 1e-6) / 1e9 / peak[0], 4)})
         wl.teardown()
     return rows
+
+
+def graph_replay_us(wl, device, stream, reps=50, replays=10):
+    """Per-call time of `reps` back-to-back calls of wl.step captured in one
+    CUDA graph (median over `replays` replays): the device time of a call
+    whose host work (argument checks, marshalling, launch) would otherwise
+    dominate."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.graph(g, stream=side):
+        for _ in range(reps):
+            wl.step(side)
+    torch.cuda.current_stream(device).wait_stream(side)
+    _, gper = timed(g.replay, replays, 3, 1, stream)
+    del g
+    return statistics.median(gper) * 1e3 / reps
+
+
+def rows_summary(head_key, head_roofline, rows, peak):
+    """One compact entry per measured row, [ms median, GB/s at the median,
+    fraction of the peak at the median, fraction at the mean], keyed by
+    workload; host-bound rows add their graph-replay figures
+    [us per call, fraction]."""
+    out = {head_key: [head_roofline["ms_median"], head_roofline["achieved_median"],
+                      head_roofline["frac_median"], head_roofline["frac"]]}
+    for r in rows or []:
+        gbs = r["algorithmic_bytes"] / (r["ms_median"] * 1e-3) / 1e9
+        e = [r["ms_median"], round(gbs, 1), round(gbs / peak[0], 4), r["frac"]]
+        if "graph_us" in r:
+            e += [r["graph_us"], r["frac_graph"]]
+        out[r["key"]] = e
+    return out
 
 
 def step_quantiles(per):
@@ -1118,6 +1171,9 @@ def run_reference(args):
         return 0
     smp = OracleSample(args.workload, args, args.ref_sample)
     sec = time_oracle(smp, args.steps, args.warmup)
+    config = workload_config(smp.full, world)
+    if smp.fraction < 1:
+        config["sample"] = smp.desc   # a bounded sample, not the whole workload
     value = smp.nbytes / sec / 1e9
     sample = (f"{smp.desc} per step ({smp.fraction:.3g} of the workload's bytes), "
               f"single-threaded C oracle (oracle/); host has {os.cpu_count()} cores")
@@ -1125,8 +1181,7 @@ def run_reference(args):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": dict(workload_config(smp.full, world),
-                                           sample=smp.desc),
+            "data": "synthetic", "config": config,
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1,
                              "kind": "oracle", "sample": sample,
                              "cpu_model": host_cpu_model()},
@@ -1258,8 +1313,9 @@ def main(argv=None):
                     help="elements per rank the CPU oracle reduces for cpu_baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="minimum CPU time of the cpu_baseline measurement")
-    ap.add_argument("--ref-sample", type=int, default=1 << 22,
-                    help="elements per rank per step for --impl reference")
+    ap.add_argument("--ref-sample", type=int, default=1 << 25,
+                    help="elements per rank per step for --impl reference (default: the "
+                         "headline's whole 2^25, so both arms time the same workload)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     global SEED_OFFSET
@@ -1333,6 +1389,9 @@ def main(argv=None):
                 "gpu_launches": head["gpu_launches"], "clocks": head["clocks"],
                 "frac_of_peak": round(head["value"] / world / peak[0], 4),
                 "rows": rows, "ddp_overlap": overlap, "wire_error": wire}
+        if rows is not None:
+            # last on the line, so that the end of stdout carries every row
+            line["rows_summary"] = rows_summary(args.workload, head["roofline"], rows, peak)
         print(json.dumps(line))
         if args.jsonl:
             with open(args.jsonl, "a") as f:

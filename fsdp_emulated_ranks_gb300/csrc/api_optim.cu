@@ -125,6 +125,9 @@ cr_status cr_fsdp_step_clipped(const void* const* grads_bf16, int nranks, size_t
   }
   float* coef = static_cast<float*>(workspace);
   double* partials = static_cast<double*>(workspace) + 1;
+  // Park the averaged gradient in params[0]/params[1] between the passes
+  // when that moves fewer bytes: 4N + 32 per element against 6N + 24.
+  a.stash = (vw != 0 && nranks >= 5) ? 1 : 0;
   int nparts = 0;
   cudaError_t e = launch_fsdp_sumsq(a, vw != 0, partials, (int)max_parts, &nparts,
                                     (cudaStream_t)stream);

@@ -65,6 +65,12 @@ struct FsdpArgs {
   // address of the coefficient min(1, max_norm / (norm + 1e-6)) by which
   // every averaged gradient is scaled (written by k_clip_coef).
   const float* coef;
+  // Clipped step only (n >= 2, vector path): 1 when the sum-of-squares pass
+  // parks each averaged fp32 gradient in the parameter outputs -- its low
+  // 16 bits at element e of params[0], its high 16 bits at element e of
+  // params[1] -- and the update pass reads it back from there instead of
+  // folding the n bf16 gradients a second time.
+  int stash;
 };
 
 // Upper bound on the per-CTA partial sums of the sum-of-squares pass; the

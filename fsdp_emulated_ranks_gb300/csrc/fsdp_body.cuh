@@ -48,11 +48,40 @@ __device__ __forceinline__ void st_state8(float* p, const uint32_t* w) {
   }
 }
 
+// The averaged fp32 gradient parked in two bf16 parameter buffers: its low
+// half in `lo`, its high half in `hi`, at the element's own index.
+__device__ __forceinline__ void stash_split(const float* g, uint32_t* lo, uint32_t* hi) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    lo[i] = __byte_perm(__float_as_uint(g[2 * i]), __float_as_uint(g[2 * i + 1]), 0x5410);
+    hi[i] = __byte_perm(__float_as_uint(g[2 * i]), __float_as_uint(g[2 * i + 1]), 0x7632);
+  }
+}
+__device__ __forceinline__ void stash_join(uint4 lo, uint4 hi, float* g) {
+  const uint32_t l[4] = {lo.x, lo.y, lo.z, lo.w}, h[4] = {hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    g[2 * i] = __uint_as_float(__byte_perm(l[i], h[i], 0x5410));
+    g[2 * i + 1] = __uint_as_float(__byte_perm(l[i], h[i], 0x7632));
+  }
+}
+__device__ __forceinline__ void stash_put(void* const* params, uint64_t e, float g) {
+  static_cast<uint16_t*>(params[0])[e] = (uint16_t)(__float_as_uint(g) & 0xffffu);
+  static_cast<uint16_t*>(params[1])[e] = (uint16_t)(__float_as_uint(g) >> 16);
+}
+__device__ __forceinline__ float stash_get(void* const* params, uint64_t e) {
+  const uint32_t lo = static_cast<const uint16_t*>(params[0])[e];
+  const uint32_t hi = static_cast<const uint16_t*>(params[1])[e];
+  return __uint_as_float(lo | (hi << 16));
+}
+
 // Element e0..e0+7 of a flat buffer (e0 % 8 == 0; the vector lies inside
 // chunk j = e0 / L, i.e. L % 8 == 0): fold the n bf16 gradients in ring
 // order, average, clip, AdamW on owner j's fp32 state, bf16 cast, write
-// the parameter to every rank.  SW = 8: 32-byte state accesses.
-template <int NT, int SW>
+// the parameter to every rank.  SW = 8: 32-byte state accesses.  STASH:
+// the averaged gradient is read back from params[0] / params[1], where the
+// sum-of-squares pass of the clipped step parked it, instead of folded.
+template <int NT, int SW, bool STASH = false>
 __device__ __forceinline__ void fsdp_vector(const void* const* grads, void* const* params,
                                             float* const* master, float* const* m,
                                             float* const* v, int n, uint64_t L,
@@ -62,7 +91,14 @@ __device__ __forceinline__ void fsdp_vector(const void* const* grads, void* cons
   const int j = (int)j64;
   const uint64_t k = e0 - j64 * L;  // offset inside shard j
   float g[8];
-  fold_vec16<CR_BF16, NT>(grads, n, j, e0 * 2, g);
+  if constexpr (STASH) {
+    stash_join(ld16(static_cast<const unsigned char*>(params[0]) + e0 * 2),
+               ld16(static_cast<const unsigned char*>(params[1]) + e0 * 2), g);
+  } else {
+    fold_vec16<CR_BF16, NT>(grads, n, j, e0 * 2, g);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) g[i] = finish_avg(g[i], n, inv_n);
+  }
   float* mp = master[j] + k;
   float* mm = m[j] + k;
   float* mv = v[j] + k;
@@ -73,7 +109,7 @@ __device__ __forceinline__ void fsdp_vector(const void* const* grads, void* cons
   uint32_t po[8], mo[8], vo[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float gi = __fmul_rn(finish_avg(g[i], n, inv_n), coef);
+    const float gi = __fmul_rn(g[i], coef);
     const AdamOut o = adamw_elem(__uint_as_float(pw[i]), __uint_as_float(mw[i]),
                                  __uint_as_float(vw[i]), gi, as);
     po[i] = __float_as_uint(o.p);
@@ -92,6 +128,7 @@ __device__ __forceinline__ void fsdp_vector(const void* const* grads, void* cons
 }
 
 // The same for one element e (any alignment, any chunk).
+template <bool STASH = false>
 __device__ __forceinline__ void fsdp_element(const void* const* grads, void* const* params,
                                              float* const* master, float* const* m,
                                              float* const* v, int n, uint64_t L,
@@ -100,7 +137,9 @@ __device__ __forceinline__ void fsdp_element(const void* const* grads, void* con
   const uint64_t j64 = fastdiv_div(Ld, e);
   const int j = (int)j64;
   const uint64_t k = e - j64 * L;
-  const float gi = __fmul_rn(finish_avg(fold_elem<CR_BF16>(grads, n, j, e), n, inv_n), coef);
+  const float gavg = STASH ? stash_get(params, e)
+                           : finish_avg(fold_elem<CR_BF16>(grads, n, j, e), n, inv_n);
+  const float gi = __fmul_rn(gavg, coef);
   const AdamOut o = adamw_elem(master[j][k], m[j][k], v[j][k], gi, as);
   master[j][k] = o.p;
   m[j][k] = o.m;

@@ -14,6 +14,13 @@
 // HBM between the phases.  Per element: N bf16 grad loads, 12 B of fp32
 // state read and written, N bf16 param stores -- (4N + 24) bytes.
 //
+// The clipped step needs the global gradient norm before any update, so it
+// makes two passes: a sum-of-squares pass, then this one with the clip
+// coefficient.  For N >= 5 the first pass parks each averaged fp32 gradient
+// in two of the parameter outputs (16 bits in each) and this pass reads it
+// back, (4N + 32) bytes per element in all instead of the (6N + 24) of
+// folding the N gradients twice.
+//
 // AdamW uses only correctly rounded fp32 operations (__fmul_rn & co. are
 // never contracted into FMAs), in the order of the textbook decoupled-
 // weight-decay rule stated in include/cr.h.
@@ -55,7 +62,10 @@ __device__ __forceinline__ float clip_coef(const FsdpArgs& a) {
 
 // Sum of squares of the averaged fp32 gradient, one fp64 partial per CTA
 // (fp64 per thread and across threads, fp32 within batches of 8 squares).
-template <int NT, bool VEC>
+// STASH: also park every averaged gradient in params[0] / params[1] (low /
+// high 16 bits) for the update pass -- 4 bytes written per element so that
+// the update pass reads 4 bytes instead of the 2N of a second fold.
+template <int NT, bool VEC, bool STASH = false>
 __global__ void __launch_bounds__(kBlock)
     k_fsdp_sumsq(const __grid_constant__ FsdpArgs a, double* partials) {
   __shared__ double s_warp[kBlock / 32];
@@ -75,15 +85,23 @@ __global__ void __launch_bounds__(kBlock)
       float s8 = 0.0f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float gi = finish_avg(g[i], n, a.inv_n);
-        s8 = fmaf(gi, gi, s8);
+        g[i] = finish_avg(g[i], n, a.inv_n);
+        s8 = fmaf(g[i], g[i], s8);
       }
       t += (double)s8;
+      if constexpr (STASH) {
+        uint32_t lo[4], hi[4];
+        stash_split(g, lo, hi);
+        st16(static_cast<unsigned char*>(a.params[0]) + e0 * 2, make_uint4(lo[0], lo[1], lo[2], lo[3]));
+        st16(static_cast<unsigned char*>(a.params[1]) + e0 * 2, make_uint4(hi[0], hi[1], hi[2], hi[3]));
+      }
     }
     e_elem = nvec * 8;
   }
   for (uint64_t e = e_elem + tid; e < a.count; e += stride) {
-    const double gi = finish_avg(fold_elem<CR_BF16>(a.grads, n, (int)fastdiv_div(a.Ld, e), e), n, a.inv_n);
+    const float gf = finish_avg(fold_elem<CR_BF16>(a.grads, n, (int)fastdiv_div(a.Ld, e), e), n, a.inv_n);
+    if constexpr (STASH) stash_put(a.params, e, gf);
+    const double gi = gf;
     t += gi * gi;
   }
 #pragma unroll
@@ -100,7 +118,7 @@ __global__ void __launch_bounds__(kBlock)
 // Vector path: 8 elements (one 16-byte bf16 vector per rank) per thread and
 // iteration; SW = 8 moves the fp32 state in 32-byte accesses.  The body of
 // k_fsdp_vec and k_fsdp_vec4, which differ only in their launch bounds.
-template <int NT, int SW>
+template <int NT, int SW, bool STASH>
 __device__ __forceinline__ void fsdp_range(const FsdpArgs& a) {
   const int n = NT > 0 ? NT : a.n;
   const float coef = clip_coef(a);
@@ -112,14 +130,15 @@ __device__ __forceinline__ void fsdp_range(const FsdpArgs& a) {
     CR_DCHECK(fastdiv_div(a.Ld, iv * 8) == iv * 8 / a.L && iv * 8 / a.L < (uint64_t)n &&
                   iv * 8 % a.L + 8 <= a.L && iv * 8 + 8 <= a.count,
               kChkFsdp);
-    fsdp_vector<NT, SW>(a.grads, a.params, a.master, a.m, a.v, n, a.L, a.Ld, a.inv_n, a.a, coef,
-                        iv * 8);
+    fsdp_vector<NT, SW, STASH>(a.grads, a.params, a.master, a.m, a.v, n, a.L, a.Ld, a.inv_n, a.a,
+                               coef, iv * 8);
   }
   // Ragged tail (count % 8 elements).
   const uint64_t e = nvec * 8 + tid;
   if (e < a.count) {
     CR_DCHECK(fastdiv_div(a.Ld, e) == e / a.L && e / a.L < (uint64_t)n, kChkFsdp);
-    fsdp_element(a.grads, a.params, a.master, a.m, a.v, n, a.L, a.Ld, a.inv_n, a.a, coef, e);
+    fsdp_element<STASH>(a.grads, a.params, a.master, a.m, a.v, n, a.L, a.Ld, a.inv_n, a.a, coef,
+                        e);
   }
 }
 
@@ -127,17 +146,17 @@ __device__ __forceinline__ void fsdp_range(const FsdpArgs& a) {
 // of spills).  At N = 16 and 2^27 parameters GB300 runs it at 6,600 GB/s,
 // against 6,190 under the 4-CTA bound (216-260 bytes of spills) and 5,710
 // with default bounds (87-89 registers, 2 CTAs per SM).
-template <int NT, int SW>
+template <int NT, int SW, bool STASH = false>
 __global__ void __launch_bounds__(kBlock, 3) k_fsdp_vec(const __grid_constant__ FsdpArgs a) {
-  fsdp_range<NT, SW>(a);
+  fsdp_range<NT, SW, STASH>(a);
 }
 
 // A compile-time rank count, registers capped for 4 resident CTAs per SM
 // (63 per thread, no spills), which GB300 runs about 1 % faster than the
 // 3 CTAs that 70 registers allow.
-template <int NT, int SW>
+template <int NT, int SW, bool STASH = false>
 __global__ void __launch_bounds__(kBlock, 4) k_fsdp_vec4(const __grid_constant__ FsdpArgs a) {
-  fsdp_range<NT, SW>(a);
+  fsdp_range<NT, SW, STASH>(a);
 }
 
 __global__ void __launch_bounds__(kBlock)
@@ -214,6 +233,9 @@ static cudaError_t launch_flat(K kernel, const A& args, uint64_t threads, cudaSt
 template <int SW>
 static cudaError_t fsdp_dispatch(const FsdpArgs& a, cudaStream_t s) {
   const uint64_t threads = a.count / 8 + 1;
+  // The update pass of the parked gradient folds nothing, so one runtime-N
+  // build serves every N (the 4-CTA bound would spill here).
+  if (a.stash) return launch_flat(k_fsdp_vec<0, SW, true>, a, threads, s);
   switch (a.n) {
     case 2: return launch_flat(k_fsdp_vec4<2, SW>, a, threads, s);
     case 4: return launch_flat(k_fsdp_vec4<4, SW>, a, threads, s);
@@ -233,24 +255,28 @@ cudaError_t launch_adamw(const AdamArgs& a, bool vec, cudaStream_t s) {
              : launch_flat(k_adamw_elem, a, a.n, s);
 }
 
-template <int NT, bool VEC>
+template <int NT, bool VEC, bool STASH = false>
 static cudaError_t sumsq_launch(const FsdpArgs& a, double* partials, int max_parts,
                                 int* nparts, cudaStream_t s) {
   const uint64_t threads = VEC ? a.count / 8 + 1 : a.count;
   int grid = 0;
-  cudaError_t err =
-      persistent_grid(reinterpret_cast<const void*>(k_fsdp_sumsq<NT, VEC>), threads, &grid);
+  cudaError_t err = persistent_grid(
+      reinterpret_cast<const void*>(k_fsdp_sumsq<NT, VEC, STASH>), threads, &grid);
   if (err != cudaSuccess) return err;
   if (grid > max_parts) grid = max_parts;
   *nparts = grid;
   clear_stale_error();
-  k_fsdp_sumsq<NT, VEC><<<grid, kBlock, 0, s>>>(a, partials);
+  k_fsdp_sumsq<NT, VEC, STASH><<<grid, kBlock, 0, s>>>(a, partials);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fsdp_sumsq(const FsdpArgs& a, bool vec, double* partials,
                               int max_parts, int* nparts, cudaStream_t s) {
   if (!vec) return sumsq_launch<0, false>(a, partials, max_parts, nparts, s);
+  if (a.stash) {
+    if (a.n == 8) return sumsq_launch<8, true, true>(a, partials, max_parts, nparts, s);
+    return sumsq_launch<0, true, true>(a, partials, max_parts, nparts, s);
+  }
   switch (a.n) {
     case 2: return sumsq_launch<2, true>(a, partials, max_parts, nparts, s);
     case 4: return sumsq_launch<4, true>(a, partials, max_parts, nparts, s);

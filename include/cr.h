@@ -442,7 +442,19 @@ cr_status cr_fsdp_step(const void* const* grads_bf16, int nranks,
  * into `workspace`, one warp that adds the partials in a fixed order (the
  * norm is reproducible run to run) and stores c in the workspace's first 8
  * bytes, then the fused step, which reads c.
- * Algorithmic bytes: (6N + 24) per parameter (the grads are read twice).
+ * For N >= 5 on the 128-bit vector path, the first pass also parks every
+ * averaged fp32 gradient in the parameter outputs: its low 16 bits at
+ * element e of params_bf16[0], its high 16 bits at element e of
+ * params_bf16[1] (4 bytes per element).  The update pass reads it back from
+ * there, before it overwrites those elements with the bf16 parameters,
+ * instead of reading the N bf16 gradients a second time.  The parked value
+ * is the fold's own fp32 result, so the update does the same arithmetic on
+ * the same values.  The parameters are outputs only -- their contents on
+ * entry are ignored -- so nothing else may read params_bf16[0] or [1]
+ * while the call runs.
+ * Algorithmic bytes per parameter: (4N + 32) with the parked gradient
+ * (N >= 5, vector path: 64 at N = 8), else (6N + 24) (the grads are read
+ * twice; for N <= 4 this is no more than 4N + 32).
  *   max_norm        finite, > 0 (CR_ERR_INVALID_ARG otherwise)
  *   workspace       caller-owned device scratch, 8-byte aligned, of
  *                   workspace_bytes >= 16 bytes; cr_fsdp_clip_workspace_bytes()

@@ -48,7 +48,7 @@ def test_sample_bytes_follow_the_workload_formula():
     assert bench.OracleSample("all_gather", ns, k).nbytes == k * 2 + 8 * k * 2
     assert bench.OracleSample("hsdp", ns, k).nbytes == 8 * k * 2 + 2 * k * 2
     assert bench.OracleSample("fsdp", ns, k).nbytes == (4 * 8 + 24) * k
-    assert bench.OracleSample("fsdp_clipped", ns, k).nbytes == (6 * 8 + 24) * k
+    assert bench.OracleSample("fsdp_clipped", ns, k).nbytes == (4 * 8 + 32) * k
     assert bench.OracleSample("accumulate", ns, k).nbytes == 8 * k * 10
     smp = bench.OracleSample("bucket_pipeline", ns, k)
     P = round(smp.nbytes / (3 * 2 * 2 * 8))
@@ -79,3 +79,28 @@ def test_iters_is_steps(capsys):
     d = reference_line(capsys, "--iters", "2")  # the later flag wins, as for --steps twice
     assert d["steps"] == 2
     assert d["cpu_baseline"]["cpu_model"]  # the host CPU is named beside the core count
+
+
+def test_full_size_reference_has_the_other_arm_config(capsys):
+    """At the workload's full size (here the 4 x 2^20 fp32 all-reduce) the
+    reference line's config is the workload's own, with no sample key: both
+    arms time the same configuration."""
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3",
+                       "--workload", "allreduce_f32", "--ref-sample", str(1 << 20)]) == 0
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    d = json.loads(lines[0])
+    full = bench.make_workload("allreduce_f32", NS, plan=False)
+    assert d["config"] == bench.workload_config(full, 1)
+    assert "sample" not in d["config"]
+    assert "4 rank buffers of 1048576 elements" in d["cpu_baseline"]["sample"]
+
+
+def test_fsdp_row_bytes():
+    """(4N + 24) bytes per parameter for the plain step; the clipped step
+    parks the averaged gradient for N >= 5, (4N + 32), and reads the
+    gradients twice below that, (6N + 24)."""
+    assert bench.FsdpStep(8, 100).nbytes == 56 * 100
+    assert bench.FsdpStep(8, 100, clip=True).nbytes == 64 * 100
+    assert bench.FsdpStep(5, 100, clip=True).nbytes == 52 * 100
+    assert bench.FsdpStep(4, 100, clip=True).nbytes == 48 * 100
+    assert bench.FsdpStep(2, 100, clip=True).nbytes == 36 * 100
