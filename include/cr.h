@@ -481,10 +481,13 @@ cr_status cr_fsdp_step_clipped(const void* const* grads_bf16, int nranks,
  * workspace (coefficient and sum-of-squares partials) kept in a static
  * device array of 4096 doubles (32 KiB) that the library holds on every GPU
  * that loads it until the process exits.  The first pass uses one partial
- * per CTA and at most 8 CTAs per SM, so any GPU with up to 511 SMs fits; on
- * a larger one the call returns CR_ERR_UNSUPPORTED.  The first call on each device looks up the
- * array's device address (cudaGetSymbolAddress, with that device current)
- * and caches it; make that first call before any stream capture.  All calls
+ * per CTA and at most 4095 CTAs (the array's partial slots), so any GPU
+ * fits.  The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it for that
+ * device's current context, keyed on the driver's context ID; a context
+ * created later on the device (after cudaDeviceReset, say) gets its own
+ * lookup at its first call.  Make each such first call before any stream
+ * capture.  All calls
  * share the one array: nothing in it needs to start at zero (the first pass
  * writes every partial the second pass reads), but calls that overlap on
  * the GPU -- on different streams, unordered -- race on it and must be
