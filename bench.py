@@ -18,9 +18,15 @@ inside the timed region ("e2e"), SM clocks sampled during the timed region
 ("clocks"), the roofline of the dominant kernel, and the CPU oracle timed on
 a bounded sample of the workload on this host ("cpu_baseline").
 
-Multi-GPU (torchrun, one process per GPU): every rank runs its own instance
-of the workload (its own 8 emulated ranks); nothing is exchanged on the data
-path, so scaling is weak and value = sum of all ranks' bytes / max time.
+Multi-GPU (torchrun, one process per GPU), two modes:
+  --split replicas (default): every rank runs its own instance of the
+      workload (its own 8 emulated ranks); nothing is exchanged on the data
+      path, so scaling is weak and value = sum of all ranks' bytes / max time;
+  --split slab: the G ranks share ONE all-reduce workload, rank g holding and
+      reducing only slab g of every buffer's element range (cr_slab_range,
+      whole chunks while G <= 8) through cr_all_reduce_range, which keeps the
+      whole buffers' chunking and so their fold order; nothing is exchanged
+      either, scaling is strong and value = the workload's bytes / max time.
 
 --impl reference times the CPU oracle (the only reference implementation
 this method has) on bounded samples of the same workload.
@@ -273,10 +279,17 @@ class Workload:
 
 
 class AllReduce(Workload):
-    def __init__(self, n=8, count=1 << 25, dtype="bf16", op="avg", std=0.02):
+    """All-reduce of n rank buffers of `count` elements, in place.  slab =
+    (lo, hi): this GPU holds and reduces only elements [lo, hi) of every
+    rank buffer (cr_all_reduce_range, the whole buffers' chunking); nbytes
+    is then this GPU's share and full_nbytes the whole workload's."""
+
+    def __init__(self, n=8, count=1 << 25, dtype="bf16", op="avg", std=0.02, slab=None):
         self.n, self.count, self.dt, self.op, self.std = n, count, dtype, op, std
         es = 2 if dtype == "bf16" else 4
-        self.nbytes = ar_bytes(n, count, es)
+        self.slab = slab
+        self.full_nbytes = ar_bytes(n, count, es)
+        self.nbytes = ar_bytes(n, slab[1] - slab[0], es) if slab else self.full_nbytes
         mib = count * es >> 20
         self.name = f"allreduce_{op}_{dtype}_{n}ranks_{mib}MiB"
         self.kernel = f"k_fold_vec3<{dtype},{dtype},AR,{n}>"
@@ -286,10 +299,27 @@ class AllReduce(Workload):
         import torch
         td = torch.bfloat16 if self.dt == "bf16" else torch.float32
         self.t_bufs = alloc_ranks(self.n, self.count, td, self.std, 0, device)
+        if self.slab:
+            lo, hi = self.slab
+            self.t_bufs = [b[lo:hi].clone() for b in self.t_bufs]
+            torch.cuda.empty_cache()
 
     def step(self, stream):
         from fsdp_emulated_ranks_gb300 import cr
-        cr.cr_all_reduce(self.t_bufs, self.count, self.dt, self.op, self.t_bufs, self.dt, stream)
+        if self.slab:
+            lo, hi = self.slab
+            cr.cr_all_reduce_range(self.t_bufs, self.count, lo, hi, self.dt, self.op, self.t_bufs,
+                                   self.dt, stream)
+        else:
+            cr.cr_all_reduce(self.t_bufs, self.count, self.dt, self.op, self.t_bufs, self.dt,
+                             stream)
+
+
+def slab_bounds(count, n, world, rank):
+    """This GPU's slab of the element range under --split slab: slab `rank`
+    of `world` (whole chunks while world <= n)."""
+    from fsdp_emulated_ranks_gb300 import cr
+    return cr.cr_slab_range(count, n, world, rank)
 
 
 class AllReduceWire(Workload):
@@ -518,15 +548,23 @@ class Fsdp2Step(Workload):
     8 ranks; each rank's grads and params live in one 256-byte-aligned slab
     per rank, the shards' fp32 state in one slab per parameter set."""
 
-    def __init__(self, n=8, layers=24, hidden=2048):
-        self.n = n
+    def __init__(self, n=8, layers=24, hidden=2048, planned=True):
+        self.n, self.planned = n, planned
         self.shapes = transformer_shapes(hidden=hidden, layers=layers, ffn=4 * hidden)
         self.P = sum(d * r for d, r in self.shapes)
         self.nbytes = (4 * n + 24) * self.P
-        self.name = f"fsdp2_step_bf16_{n}ranks_{len(self.shapes)}params_{self.P / 1e9:.2f}e9"
-        self.kernel = f"k_fsdp2<{n}>"
-        self.profile = f"k_fsdp2_fsdp2_step_{n}x{len(self.shapes)}params"
-        self.launches = -(-len(self.shapes) // min(64, 2560 // (5 * n)))
+        tag = "" if planned else "_chained"
+        self.name = f"fsdp2{tag}_step_bf16_{n}ranks_{len(self.shapes)}params_{self.P / 1e9:.2f}e9"
+        if planned:
+            # one launch over the plan's table, uploaded once at setup
+            self.kernel = f"k_fsdp2_table<{n}>"
+            self.profile = f"k_fsdp2_table_fsdp2_step_{n}x{len(self.shapes)}params"
+            self.launches = 1
+        else:
+            # the pointers in the kernel's parameter block: 64 parameters a launch
+            self.kernel = f"k_fsdp2<{n}>"
+            self.profile = f"k_fsdp2_fsdp2_step_{n}x{len(self.shapes)}params"
+            self.launches = -(-len(self.shapes) // min(64, 2560 // (5 * n)))
 
     def setup(self, device):
         import torch
@@ -573,14 +611,25 @@ class Fsdp2Step(Workload):
         self.grads, self.params = addr(self.grads), addr(self.params)
         self.master, self.m, self.v = addr(self.master), addr(self.m), addr(self.v)
         self.cfg = cr.adamw_cfg()
+        self.plan = self.t_table = None
+        if self.planned:
+            self.plan = cr.cr_fsdp2_plan_create(self.shapes, n, self.grads, self.master, self.m,
+                                                self.v, self.params)
+            self.t_table = torch.empty(self.plan.table_bytes, dtype=torch.uint8, device=device)
+            cr.cr_fsdp2_plan_upload(self.plan, self.t_table)
+            torch.cuda.synchronize(device)
 
     def step(self, stream):
         from fsdp_emulated_ranks_gb300 import cr
-        cr.cr_fsdp2_step(self.shapes, self.n, self.grads, self.master, self.m, self.v, self.cfg,
-                         self.params, stream)
+        if self.planned:
+            cr.cr_fsdp2_step_planned(self.plan, self.t_table, self.cfg, stream)
+        else:
+            cr.cr_fsdp2_step(self.shapes, self.n, self.grads, self.master, self.m, self.v,
+                             self.cfg, self.params, stream)
 
     def teardown(self):
         self.grads = self.params = self.master = self.m = self.v = None
+        self.plan = self.t_table = None
         super().teardown()
 
 
@@ -641,6 +690,8 @@ def make_workload(name, args, plan=True):
         return FsdpStep(count=args.fsdp_count, clip=True)
     if name == "fsdp2":
         return Fsdp2Step(layers=args.fsdp2_layers, hidden=args.fsdp2_hidden)
+    if name == "fsdp2_chained":
+        return Fsdp2Step(layers=args.fsdp2_layers, hidden=args.fsdp2_hidden, planned=False)
     if name == "accumulate":
         return Accumulate(reduce=False)
     if name == "accumulate_allreduce":
@@ -649,7 +700,7 @@ def make_workload(name, args, plan=True):
 
 
 ROW_WORKLOADS = ["reduce_scatter", "all_gather", "allreduce_f32", "bucket_pack",
-                 "bucket_allreduce", "bucket_unpack", "bucket_pipeline", "bucket_fused", "fsdp", "fsdp_clipped", "fsdp2", "accumulate",
+                 "bucket_allreduce", "bucket_unpack", "bucket_pipeline", "bucket_fused", "fsdp", "fsdp_clipped", "fsdp2", "fsdp2_chained", "accumulate",
                  "accumulate_allreduce", "allreduce_wire", "hsdp"]
 
 
@@ -677,6 +728,11 @@ def workload_config(wl, world):
 def run_headline(args, world, rank, device, stream, peak):
     import torch
     wl = make_workload(args.workload, args)
+    if args.split == "slab":
+        if not isinstance(wl, AllReduce):
+            raise SystemExit("--split slab is built for the all-reduce workloads")
+        wl = AllReduce(wl.n, wl.count, wl.dt, wl.op, wl.std,
+                       slab=slab_bounds(wl.count, wl.n, world, rank))
     wl.setup(device)
     # Sample for the CPU baseline before in-place calls overwrite the inputs.
     sample = None
@@ -686,7 +742,12 @@ def run_headline(args, world, rank, device, stream, peak):
         sample = [b[:k].view(torch.int16).cpu().numpy().view("uint16") for b in wl.t_bufs]
     sampler = ClockSampler(device)
     total_ms, per = timed(lambda: wl.step(stream), args.steps, args.warmup, world, stream, sampler)
-    value, ms_step = job_throughput(wl.nbytes, total_ms, args.steps, world, device)
+    if getattr(wl, "slab", None):
+        # the ranks' slabs make up one workload: its bytes over the slowest rank's time
+        ms_step = max_over_ranks(total_ms, world, device) / args.steps
+        value = wl.full_nbytes / (ms_step * 1e-3) / 1e9
+    else:
+        value, ms_step = job_throughput(wl.nbytes, total_ms, args.steps, world, device)
     kern_ms = statistics.mean(per)
     achieved = wl.nbytes / (kern_ms * 1e-3) / 1e9
     out = {
@@ -1301,6 +1362,9 @@ def main(argv=None):
                          "when a rank is missing")
     ap.add_argument("--jsonl", default=None,
                     help="also append one JSON record per measured row to this file")
+    ap.add_argument("--split", choices=["replicas", "slab"], default="replicas",
+                    help="N > 1: every GPU runs the whole workload (replicas, weak scaling) "
+                         "or one slab of its element range (slab, strong scaling)")
     ap.add_argument("--no-rows", action="store_true")
     ap.add_argument("--skip-fsdp", action="store_true")
     ap.add_argument("--row-steps", type=int, default=20)
@@ -1363,6 +1427,8 @@ def main(argv=None):
         overlap = run_overlap(args, device)
         wire = wire_error(device)
     cpu = None
+    if sample is not None and args.split == "slab":
+        sample = None   # the slab run's baseline is the whole workload's; not sampled here
     if sample is not None:
         gbs, secs, passes = cpu_oracle_allreduce(sample, args.cpu_seconds)
         frac = (1 << 25) // sample[0].size
@@ -1377,11 +1443,15 @@ def main(argv=None):
         cpu = cpu_baseline_sampled(args)
     if rank == 0:
         config = workload_config(wl, world)
+        if args.split == "slab":
+            config["parallelism"] = (f"{world} GPU(s), each the slab of the element range "
+                                     f"cr_slab_range gives it, of the same {wl.n} emulated ranks")
         line = {"metric": METRIC, "value": round(head["value"], 1), "unit": UNIT,
                 "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": head["ms_per_step"], "higher_is_better": True,
                 # the arithmetic: fp32 partial sums (bf16 in and out, see config)
-                "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                "scaling": "strong" if args.split == "slab" else "weak",
+                "vs_baseline": None, "dtype": "f32",
                 "data": "synthetic",
                 "config": config,
                 "roofline": head["roofline"], "l2_flushed": head["l2_flushed"],

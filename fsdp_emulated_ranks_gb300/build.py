@@ -28,7 +28,7 @@ CHECKED_FLAGS = ["-DCR_DEVICE_CHECKS", "-rdc=true"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "--expt-relaxed-constexpr", "-I" + INCLUDE, "-I" + CSRC]
-SOURCES = ["api.cu", "api_buckets.cu", "api_optim.cu", "launch_util.cu", "k_collectives.cu", "k_fsdp.cu",
+SOURCES = ["api.cu", "api_buckets.cu", "api_optim.cu", "api_range.cu", "launch_util.cu", "k_collectives.cu", "k_fsdp.cu",
            "k_bucket.cu", "k_bucket_fused.cu", "k_fsdp2.cu", "k_accum.cu",
            "k_hsdp.cu", "reducer.cu", "fsdp_noalloc.cu", "check.cu", "plan.cpp",
            "comm.cpp"]

@@ -38,7 +38,10 @@ EXPORTS = ["cr_status_string", "cr_last_error", "cr_version", "cr_chunk_len",
            "cr_bucket_pack", "cr_bucket_unpack", "cr_bucket_all_reduce",
            "cr_bucket_all_reduce_fused", "cr_fsdp_step",
            "cr_fsdp_clip_workspace_bytes", "cr_fsdp_step_clipped",
-           "cr_fsdp_step_clipped_noalloc", "cr_fsdp2_step", "cr_accumulate",
+           "cr_fsdp_step_clipped_noalloc", "cr_fsdp2_step", "cr_fsdp2_plan_create",
+           "cr_fsdp2_plan_table_bytes", "cr_fsdp2_plan_upload", "cr_fsdp2_step_planned",
+           "cr_fsdp2_plan_free", "cr_slab_range", "cr_all_reduce_range",
+           "cr_reduce_scatter_range", "cr_fsdp_step_range", "cr_accumulate",
            "cr_all_reduce_accumulate", "cr_adamw_step", "cr_comm_elems",
            "cr_reduce_scatter_wire", "cr_all_reduce_wire",
            "cr_hsdp_reduce_scatter", "cr_reducer_create", "cr_reducer_mark_ready",
@@ -141,6 +144,17 @@ def lib() -> C.CDLL:
     L.cr_fsdp_step_clipped_noalloc.argtypes = [vp, i, sz, vp, vp, vp, C.POINTER(AdamWCfg),
                                                C.c_double, vp, vp, vp]
     L.cr_fsdp2_step.argtypes = [vp, i, i, vp, vp, vp, vp, C.POINTER(AdamWCfg), vp, vp]
+    L.cr_fsdp2_plan_create.argtypes = [vp, i, i, vp, vp, vp, vp, vp, C.POINTER(vp)]
+    L.cr_fsdp2_plan_table_bytes.restype = sz
+    L.cr_fsdp2_plan_table_bytes.argtypes = [vp]
+    L.cr_fsdp2_plan_upload.argtypes = [vp, vp, sz, vp]
+    L.cr_fsdp2_step_planned.argtypes = [vp, vp, C.POINTER(AdamWCfg), vp]
+    L.cr_fsdp2_plan_free.restype = None
+    L.cr_fsdp2_plan_free.argtypes = [vp]
+    L.cr_slab_range.argtypes = [sz, i, i, i, C.POINTER(sz), C.POINTER(sz)]
+    L.cr_all_reduce_range.argtypes = [vp, i, sz, sz, sz, i, i, vp, i, vp]
+    L.cr_reduce_scatter_range.argtypes = [vp, i, sz, sz, sz, i, i, vp, i, vp]
+    L.cr_fsdp_step_range.argtypes = [vp, i, sz, sz, sz, vp, vp, vp, C.POINTER(AdamWCfg), vp, vp]
     L.cr_accumulate.argtypes = [vp, i, sz, vp, i, vp]
     L.cr_all_reduce_accumulate.argtypes = [vp, i, sz, vp, i, i, vp]
     L.cr_adamw_step.argtypes = [sz, vp, vp, vp, vp, C.POINTER(AdamWCfg), vp, vp]
@@ -153,6 +167,8 @@ def lib() -> C.CDLL:
     L.cr_chunk_len.restype = sz
     L.cr_bucket_plan_free.restype = None
     L.cr_fsdp_clip_workspace_bytes.restype = sz
+    L.cr_fsdp2_plan_table_bytes.restype = sz
+    L.cr_fsdp2_plan_free.restype = None
     _lib = L
     return L
 
@@ -523,6 +539,81 @@ def cr_fsdp2_step(shapes, nranks, grads, master, m, v, cfg: AdamWCfg, params,
     _check(lib().cr_fsdp2_step(arr, len(shapes), nranks, _ptr_array(grads), _ptr_array(master),
                                _ptr_array(m), _ptr_array(v), C.byref(cfg), _ptr_array(params),
                                _stream(stream)), "cr_fsdp2_step")
+
+
+def cr_slab_range(count: int, nranks: int, nslabs: int, g: int) -> tuple[int, int]:
+    lo, hi = C.c_size_t(), C.c_size_t()
+    _check(lib().cr_slab_range(count, nranks, nslabs, g, C.byref(lo), C.byref(hi)),
+           "cr_slab_range")
+    return lo.value, hi.value
+
+
+def cr_all_reduce_range(inp, count, begin, end, in_dtype, op, out, out_dtype,
+                        stream=None) -> None:
+    """inp/out: per-rank slab buffers (element `begin` first)."""
+    _check(lib().cr_all_reduce_range(_ptr_array(inp), len(inp), count, begin, end,
+                                     _dtype(in_dtype), _op(op), _ptr_array(out),
+                                     _dtype(out_dtype), _stream(stream)), "cr_all_reduce_range")
+
+
+def cr_reduce_scatter_range(bufs, count, begin, end, in_dtype, op, out_shards, out_dtype,
+                            stream=None) -> None:
+    """out_shards[j]: shard j's part inside [begin, end) (or 0 if none)."""
+    _check(lib().cr_reduce_scatter_range(_ptr_array(bufs), len(bufs), count, begin, end,
+                                         _dtype(in_dtype), _op(op), _ptr_array(out_shards),
+                                         _dtype(out_dtype), _stream(stream)),
+           "cr_reduce_scatter_range")
+
+
+def cr_fsdp_step_range(grads, count, begin, end, master, m, v, cfg: AdamWCfg, params,
+                       stream=None) -> None:
+    _check(lib().cr_fsdp_step_range(_ptr_array(grads), len(grads), count, begin, end,
+                                    _ptr_array(master), _ptr_array(m), _ptr_array(v),
+                                    C.byref(cfg), _ptr_array(params), _stream(stream)),
+           "cr_fsdp_step_range")
+
+
+class Fsdp2Plan:
+    """Owns a cr_fsdp2_plan_t; freed with cr_fsdp2_plan_free."""
+
+    def __init__(self, ptr: int):
+        self._ptr = ptr
+        self.table_bytes = int(lib().cr_fsdp2_plan_table_bytes(ptr))
+
+    @property
+    def ptr(self):
+        return self._ptr
+
+    def __del__(self):
+        if getattr(self, "_ptr", None) and _lib is not None:
+            _lib.cr_fsdp2_plan_free(self._ptr)
+            self._ptr = None
+
+
+def cr_fsdp2_plan_create(shapes, nranks, grads, master, m, v, params) -> Fsdp2Plan:
+    """shapes: [(dim0, row_numel)]; the pointer lists are flat, index p*N + r."""
+    arr = (ParamShape * max(1, len(shapes)))(*[ParamShape(d, rn) for d, rn in shapes])
+    out = C.c_void_p()
+    _check(lib().cr_fsdp2_plan_create(arr, len(shapes), nranks, _ptr_array(grads),
+                                      _ptr_array(master), _ptr_array(m), _ptr_array(v),
+                                      _ptr_array(params), C.byref(out)), "cr_fsdp2_plan_create")
+    return Fsdp2Plan(out.value)
+
+
+def cr_fsdp2_plan_table_bytes(plan: Fsdp2Plan) -> int:
+    return int(lib().cr_fsdp2_plan_table_bytes(plan.ptr if plan is not None else None))
+
+
+def cr_fsdp2_plan_upload(plan: Fsdp2Plan, table, table_bytes=None, stream=None) -> None:
+    """table: a device tensor or pointer of at least plan.table_bytes bytes."""
+    nbytes = table_bytes if table_bytes is not None else table.numel() * table.element_size()
+    _check(lib().cr_fsdp2_plan_upload(plan.ptr, _ptr(table), nbytes, _stream(stream)),
+           "cr_fsdp2_plan_upload")
+
+
+def cr_fsdp2_step_planned(plan: Fsdp2Plan, table, cfg: AdamWCfg, stream=None) -> None:
+    _check(lib().cr_fsdp2_step_planned(plan.ptr if plan is not None else None, _ptr(table),
+                                       C.byref(cfg), _stream(stream)), "cr_fsdp2_step_planned")
 
 
 def cr_accumulate(acc, count, grads, grad_dtype, stream=None) -> None:

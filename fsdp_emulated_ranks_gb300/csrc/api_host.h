@@ -74,6 +74,14 @@ inline uint64_t chunk_size(uint64_t count, uint64_t L, int j) {
   return b - a;
 }
 
+// p moved back by `elems` elements of `es` bytes: the address element 0 of
+// a buffer would have if p is where its element `elems` sits.  Range calls
+// hand kernels such addresses; the kernels only touch elements >= elems.
+template <typename T>
+inline T* shift_back(T* p, uint64_t elems, size_t es) {
+  return reinterpret_cast<T*>(reinterpret_cast<uintptr_t>(p) - elems * es);
+}
+
 inline bool aligned(const void* p, size_t a) {
   return (reinterpret_cast<uintptr_t>(p) % a) == 0;
 }

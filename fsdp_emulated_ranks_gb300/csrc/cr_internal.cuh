@@ -58,6 +58,8 @@ struct FsdpArgs {
   uint64_t count;
   uint64_t L;
   FastDiv Ld;
+  uint64_t begin;  // the update covers elements [begin, end) of the flat
+  uint64_t end;    // buffer (the whole buffer's chunks and fold order)
   int n;
   float inv_n;
   AdamScalars a;
@@ -153,6 +155,24 @@ struct Fsdp2Args {
   void* ptrs[kFsdp2MaxPtrs];
 };
 
+// FSDP2 step over a plan's table in device memory.  Table layout (built on
+// the host by cr_fsdp2_plan_create, uploaded by cr_fsdp2_plan_upload):
+//   [0, p_off)          uint32 tile_start[nparams + 1] (prefix sums of the
+//                       parameters' tiles), zero-padded to 16 bytes
+//   [p_off, ptr_off)    Fsdp2Param p[nparams], 48 bytes each
+//   [ptr_off, ...)      void* ptrs[5 * n * nparams], parameter q's from
+//                       p[q].ptr0 in the order of Fsdp2Param
+struct Fsdp2TableArgs {
+  const unsigned char* table;
+  uint64_t p_off;
+  uint64_t ptr_off;
+  uint32_t nparams;  // parameters in the table (empty ones left out)
+  uint32_t ntiles;   // tile_start[nparams]
+  int n;
+  float inv_n;
+  AdamScalars a;
+};
+
 // Gradient accumulation (no_sync) and the fused accumulate + all-reduce.
 struct AccumArgs {
   float* acc[kMaxRanks];
@@ -219,6 +239,7 @@ cudaError_t launch_bucket_fused(cr_dtype d, const FusedArgs& a, uint32_t ntiles,
                                 cudaStream_t s);
 uint64_t fused_tile_elems(cr_dtype d);  // elements of a tensor per CTA tile
 cudaError_t launch_fsdp2(const Fsdp2Args& a, uint32_t ntiles, bool chained, cudaStream_t s);
+cudaError_t launch_fsdp2_table(const Fsdp2TableArgs& a, cudaStream_t s);
 // grad_dtype CR_F32 or CR_BF16; vw as for the other launchers (16-byte
 // grads and 32- or 16-byte accumulators).
 cudaError_t launch_accum(cr_dtype grad_dtype, const AccumArgs& a, int vw, cudaStream_t s);

@@ -118,27 +118,36 @@ __global__ void __launch_bounds__(kBlock)
 // Vector path: 8 elements (one 16-byte bf16 vector per rank) per thread and
 // iteration; SW = 8 moves the fp32 state in 32-byte accesses.  The body of
 // k_fsdp_vec and k_fsdp_vec4, which differ only in their launch bounds.
+template <int NT, bool STASH>
+__device__ __forceinline__ void fsdp_one(const FsdpArgs& a, int n, float coef, uint64_t e) {
+  CR_DCHECK(e >= a.begin && e < a.end && fastdiv_div(a.Ld, e) == e / a.L && e / a.L < (uint64_t)n,
+            kChkFsdp);
+  fsdp_element<STASH>(a.grads, a.params, a.master, a.m, a.v, n, a.L, a.Ld, a.inv_n, a.a, coef, e);
+}
+
 template <int NT, int SW, bool STASH>
 __device__ __forceinline__ void fsdp_range(const FsdpArgs& a) {
   const int n = NT > 0 ? NT : a.n;
   const float coef = clip_coef(a);
-  const uint64_t nvec = a.count / 8;
+  const uint64_t vbeg = (a.begin + 7) / 8, vend = a.end / 8;
   const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-  for (uint64_t iv = tid; iv < nvec; iv += stride) {
+  for (uint64_t iv = vbeg + tid; iv < vend; iv += stride) {
     // the 8 elements lie in one shard, inside that shard's length
     CR_DCHECK(fastdiv_div(a.Ld, iv * 8) == iv * 8 / a.L && iv * 8 / a.L < (uint64_t)n &&
-                  iv * 8 % a.L + 8 <= a.L && iv * 8 + 8 <= a.count,
+                  iv * 8 % a.L + 8 <= a.L && iv * 8 + 8 <= a.end,
               kChkFsdp);
     fsdp_vector<NT, SW, STASH>(a.grads, a.params, a.master, a.m, a.v, n, a.L, a.Ld, a.inv_n, a.a,
                                coef, iv * 8);
   }
-  // Ragged tail (count % 8 elements).
-  const uint64_t e = nvec * 8 + tid;
-  if (e < a.count) {
-    CR_DCHECK(fastdiv_div(a.Ld, e) == e / a.L && e / a.L < (uint64_t)n, kChkFsdp);
-    fsdp_element<STASH>(a.grads, a.params, a.master, a.m, a.v, n, a.L, a.Ld, a.inv_n, a.a, coef,
-                        e);
+  // Ragged ends: fewer than 8 elements before the first and after the last
+  // whole vector of the range (threads 0-7 and 8-15).
+  if (vbeg <= vend) {
+    const uint64_t head = vbeg * 8 - a.begin, tail = a.end - vend * 8;
+    if (tid < head) fsdp_one<NT, STASH>(a, n, coef, a.begin + tid);
+    if (tid >= 8 && tid - 8 < tail) fsdp_one<NT, STASH>(a, n, coef, vend * 8 + (tid - 8));
+  } else if (tid < a.end - a.begin) {
+    fsdp_one<NT, STASH>(a, n, coef, a.begin + tid);
   }
 }
 
@@ -163,7 +172,8 @@ __global__ void __launch_bounds__(kBlock)
     k_fsdp_elem(const __grid_constant__ FsdpArgs a) {
   const float coef = clip_coef(a);
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-  for (uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; e < a.count; e += stride) {
+  for (uint64_t e = a.begin + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; e < a.end;
+       e += stride) {
     CR_DCHECK(fastdiv_div(a.Ld, e) == e / a.L && e / a.L < (uint64_t)a.n, kChkFsdp);
     fsdp_element(a.grads, a.params, a.master, a.m, a.v, a.n, a.L, a.Ld, a.inv_n, a.a, coef, e);
   }
@@ -232,7 +242,7 @@ static cudaError_t launch_flat(K kernel, const A& args, uint64_t threads, cudaSt
 
 template <int SW>
 static cudaError_t fsdp_dispatch(const FsdpArgs& a, cudaStream_t s) {
-  const uint64_t threads = a.count / 8 + 1;
+  const uint64_t threads = (a.end - a.begin) / 8 + 16;
   // The update pass of the parked gradient folds nothing, so one runtime-N
   // build serves every N (the 4-CTA bound would spill here).
   if (a.stash) return launch_flat(k_fsdp_vec<0, SW, true>, a, threads, s);
@@ -247,7 +257,7 @@ static cudaError_t fsdp_dispatch(const FsdpArgs& a, cudaStream_t s) {
 cudaError_t launch_fsdp(const FsdpArgs& a, int vw, cudaStream_t s) {
   if (vw == 32) return fsdp_dispatch<8>(a, s);
   if (vw == 16) return fsdp_dispatch<4>(a, s);
-  return launch_flat(k_fsdp_elem, a, a.count, s);
+  return launch_flat(k_fsdp_elem, a, a.end - a.begin, s);
 }
 
 cudaError_t launch_adamw(const AdamArgs& a, bool vec, cudaStream_t s) {

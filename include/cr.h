@@ -430,6 +430,51 @@ cr_status cr_fsdp_step(const void* const* grads_bf16, int nranks,
                        float* const* v, const cr_adamw_cfg* cfg,
                        void* const* params_bf16, cr_stream_t stream);
 
+/* ---- range forms: one slab of the element range per GPU -------------------
+ * Every output element of a reduce-scatter, all-reduce or FSDP step depends
+ * only on the same element of every rank ([DT] section 2, All-Reduce: the
+ * sum is element-wise across ranks; AdamW is element-wise too), so the
+ * element range [0, count) may be cut into slabs processed independently,
+ * e.g. one per GPU, with no exchange between them.  The range calls do the
+ * work of the whole-buffer call for elements [begin, end) only, with the
+ * WHOLE buffer's chunking -- L = ceil(count / N), element e in chunk e / L,
+ * folded in that chunk's ring order -- so every element they write equals,
+ * bit for bit, what the whole-buffer call writes there.  (Calling the
+ * whole-buffer entry points on a slab would chunk the slab instead, and
+ * change the fold order.)  Pointers are slab-local:
+ *   in/out/bufs/grads_bf16/params_bf16[r]  rank r's element `begin`; the
+ *                    buffer holds end - begin elements
+ *   out_shards/master/m/v[j]  the first element of shard j that lies in
+ *                    [begin, end), i.e. shard element max(begin, jL) - jL;
+ *                    the part holds |[begin, end) intersected with chunk j|
+ *                    elements; ignored (may be NULL) if that is empty
+ * Dtypes, ops, in-place rules, alignment and errors as the whole-buffer
+ * calls; begin <= end <= count (CR_ERR_INVALID_ARG otherwise).  A buffer
+ * takes the vector path when its element-0 address (pointer - offset
+ * * element size) is 16-byte aligned, as for the whole-buffer calls.
+ * The clipped FSDP step has no range form: its global gradient norm needs
+ * every slab's sum of squares (one scalar exchange between GPUs).
+ * cr_slab_range: slab g of `nslabs` that partition [0, count): whole chunks
+ * when nslabs <= nranks (slab g starts at chunk floor(g * N / nslabs)),
+ * else 16-element boundaries (slab g starts at element 16 * floor(g *
+ * ceil(count / 16) / nslabs)); bounds clamped to count.  Host only. */
+cr_status cr_slab_range(size_t count, int nranks, int nslabs, int g,
+                        size_t* begin, size_t* end);
+cr_status cr_all_reduce_range(const void* const* in, int nranks, size_t count,
+                              size_t begin, size_t end, cr_dtype in_dtype,
+                              cr_op op, void* const* out, cr_dtype out_dtype,
+                              cr_stream_t stream);
+cr_status cr_reduce_scatter_range(const void* const* bufs, int nranks,
+                                  size_t count, size_t begin, size_t end,
+                                  cr_dtype in_dtype, cr_op op,
+                                  void* const* out_shards, cr_dtype out_dtype,
+                                  cr_stream_t stream);
+cr_status cr_fsdp_step_range(const void* const* grads_bf16, int nranks,
+                             size_t count, size_t begin, size_t end,
+                             float* const* master, float* const* m,
+                             float* const* v, const cr_adamw_cfg* cfg,
+                             void* const* params_bf16, cr_stream_t stream);
+
 /* cr_fsdp_step with global gradient-norm clipping between the
  * reduce-scatter and AdamW ("AI Infra Guide, Chapter 6", 6.8: the training
  * loop calls clip_grad_norm_(max_norm=1.0) on the sharded model before the
@@ -513,8 +558,10 @@ cr_status cr_fsdp_step_clipped_noalloc(const void* const* grads_bf16,
  *   grads_bf16[p*N + r]        rank r's full gradient of p (dim0*row_numel)
  *   master/m/v[p*N + j]        owner j's fp32 shard of p (NULL if empty)
  *   params_bf16[p*N + r]       rank r's full bf16 parameter p (output)
- * One launch per 64 parameters (per 512/N when N > 8).  No buffer may
- * overlap another (CR_ERR_INVALID_ARG).  A parameter whose shard length is
+ * One launch per 64 parameters (per 512/N when N > 8): the pointers travel
+ * in the kernel's parameter block; cr_fsdp2_step_planned below makes the
+ * whole model one launch.  No buffer may overlap another
+ * (CR_ERR_INVALID_ARG).  A parameter whose shard length is
  * a multiple of 8 and whose buffers are 16-byte aligned takes the vector
  * path; any other takes the element-wise one, with identical results. */
 typedef struct {
@@ -527,6 +574,45 @@ cr_status cr_fsdp2_step(const cr_param_shape* shapes, int nparams, int nranks,
                         float* const* m, float* const* v,
                         const cr_adamw_cfg* cfg, void* const* params_bf16,
                         cr_stream_t stream);
+
+/* FSDP2 step in one launch, for a parameter set that stays fixed across
+ * steps ([DT] section 4, FSDP2: the sharded parameters and their optimizer
+ * state are created once and stepped every iteration).  Same arithmetic and
+ * results, bit for bit, as cr_fsdp2_step.
+ * cr_fsdp2_plan_create checks every buffer exactly as cr_fsdp2_step does
+ * (same arguments, same errors) and builds, on the host, the table the
+ * kernel reads: the tile prefix sums, a 48-byte descriptor per non-empty
+ * parameter and its 5N device pointers.  On success *plan receives a host
+ * object that the caller releases with cr_fsdp2_plan_free; it holds the
+ * buffers' addresses, so those buffers must stay allocated, and unmoved,
+ * while the plan's table is used.
+ * cr_fsdp2_plan_table_bytes: the table's size (0 for a NULL plan).
+ * cr_fsdp2_plan_upload copies the table, with one cudaMemcpyAsync on
+ * `stream`, into a caller-owned device buffer `table` of table_bytes >=
+ * cr_fsdp2_plan_table_bytes(plan), 16-byte aligned (CR_ERR_ALIGNMENT).  The
+ * copy is from pageable host memory: the call returns once the bytes are
+ * staged, so the plan may be freed right after it.  Upload once per
+ * parameter set, not per step.
+ * cr_fsdp2_step_planned launches the step for the plan's parameters, with
+ * the table read from `table` (which must hold this plan's uploaded bytes,
+ * unchanged, until the launch completes) and the AdamW configuration given
+ * here (the step count may change every call).  One launch, any number of
+ * parameters.  The library checks the plan, the table's alignment and cfg;
+ * the buffers were checked when the plan was made. */
+typedef struct cr_fsdp2_plan cr_fsdp2_plan_t;
+
+cr_status cr_fsdp2_plan_create(const cr_param_shape* shapes, int nparams,
+                               int nranks, const void* const* grads_bf16,
+                               float* const* master, float* const* m,
+                               float* const* v, void* const* params_bf16,
+                               cr_fsdp2_plan_t** plan);
+size_t cr_fsdp2_plan_table_bytes(const cr_fsdp2_plan_t* plan);
+cr_status cr_fsdp2_plan_upload(const cr_fsdp2_plan_t* plan, void* table,
+                               size_t table_bytes, cr_stream_t stream);
+cr_status cr_fsdp2_step_planned(const cr_fsdp2_plan_t* plan,
+                                const void* table, const cr_adamw_cfg* cfg,
+                                cr_stream_t stream);
+void cr_fsdp2_plan_free(cr_fsdp2_plan_t* plan);
 
 /* ---- DDP gradient accumulation (no_sync) ----------------------------------
  * "AI Infra Guide, Chapter 6", 6.2.6: micro-steps inside model.no_sync()

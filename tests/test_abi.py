@@ -262,6 +262,40 @@ def test_fsdp2_and_accumulate_validation(L):
     cr.cr_accumulate(a, 0, gr, "bf16", stream=0)
 
 
+def test_fsdp2_plan_host_side(L):
+    """cr_fsdp2_plan_create checks what cr_fsdp2_step checks and builds the
+    table on the host; the table's size follows its layout (tile prefix
+    sums padded to 16 bytes, 48 bytes per non-empty parameter, 5N pointers
+    each).  Upload and the planned step reject a NULL or misaligned table, a
+    short table_bytes and a bad AdamW configuration before any copy or
+    launch (every pointer here is fake)."""
+    n = 2
+    g = [FAKE + k * (1 << 20) for k in range(3 * n)]
+    p = [FAKE + (1 << 28) + k * (1 << 20) for k in range(3 * n)]
+    ms = [FAKE + (2 << 28) + k * (1 << 20) for k in range(3 * n)]
+    mm = [FAKE + (3 << 28) + k * (1 << 20) for k in range(3 * n)]
+    v = [FAKE + (4 << 28) + k * (1 << 20) for k in range(3 * n)]
+    shapes = [(4, 3), (0, 5), (1, 8)]   # an empty parameter; rank 1's shard of the last is empty
+    expect(1, cr.cr_fsdp2_plan_create, shapes, 65, g, ms, mm, v, p)
+    expect(1, cr.cr_fsdp2_plan_create, shapes, n, g[:1] + [0] + g[2:], ms, mm, v, p)
+    expect(3, cr.cr_fsdp2_plan_create, shapes, n, g, [ms[0] + 2] + ms[1:], mm, v, p)
+    expect(1, cr.cr_fsdp2_plan_create, shapes, n, g, ms, mm, [v[0], ms[0]] + v[2:], p)
+    plan = cr.cr_fsdp2_plan_create(shapes, n, g, ms, mm, v, p)
+    nonempty = 2
+    assert plan.table_bytes == 16 + 48 * nonempty + 8 * 5 * n * nonempty
+    assert cr.cr_fsdp2_plan_table_bytes(None) == 0
+    expect(1, cr.cr_fsdp2_plan_upload, plan, 0, plan.table_bytes, stream=0)
+    expect(3, cr.cr_fsdp2_plan_upload, plan, FAKE + 8, plan.table_bytes, stream=0)
+    expect(1, cr.cr_fsdp2_plan_upload, plan, FAKE, plan.table_bytes - 1, stream=0)
+    expect(1, cr.cr_fsdp2_step_planned, plan, 0, cr.adamw_cfg(), stream=0)
+    expect(3, cr.cr_fsdp2_step_planned, plan, FAKE + 8, cr.adamw_cfg(), stream=0)
+    expect(1, cr.cr_fsdp2_step_planned, plan, FAKE, cr.adamw_cfg(step=0), stream=0)
+    expect(1, cr.cr_fsdp2_step_planned, None, FAKE, cr.adamw_cfg(), stream=0)
+    empty = cr.cr_fsdp2_plan_create([], n, [], [], [], [], [])
+    assert empty.table_bytes == 16
+    del plan, empty
+
+
 def test_wire_validation(L):
     n = 4
     bufs = [FAKE + r * (1 << 20) for r in range(n)]

@@ -21,7 +21,7 @@ SUITES = ["tests/test_parity_gpu.py", "tests/test_parity_wire_hsdp_gpu.py",
           "tests/test_fuzz_gpu.py", "tests/test_pdl_gpu.py", "tests/test_reducer_gpu.py",
           "tests/test_graph_gpu.py", "tests/test_comm_gpu.py", "tests/test_cuda_error_gpu.py",
           "tests/test_fullsize_gpu.py", "tests/test_fullsize_more_gpu.py",
-          "tests/test_threads_gpu.py", "tests/test_zero_stages_gpu.py"]
+          "tests/test_threads_gpu.py", "tests/test_zero_stages_gpu.py", "tests/test_range_gpu.py"]
 
 
 @pytest.fixture(scope="module")

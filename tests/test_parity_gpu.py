@@ -592,6 +592,86 @@ def test_fsdp2_step_two_steps(n, offset):
                 assert_match(gp[p][r].host(), want[p][r], "bf16", f"param {p} rank {r} step {step}")
 
 
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("offset", [0, "16B", 1])
+def test_fsdp2_step_planned_two_steps(n, offset):
+    """cr_fsdp2_step_planned: the plan made and its table uploaded once,
+    then two steps (t = 1, 2) launched from the table, against the oracle."""
+    shapes = FSDP2_SHAPES
+    grads, master, m, v = fsdp2_host(shapes, n, 80 + n)
+    gm = [[Guarded(x.size, "f32", eoff(offset, "f32")) for x in row] for row in master]
+    gmm = [[Guarded(x.size, "f32", eoff(offset, "f32")) for x in row] for row in m]
+    gv = [[Guarded(x.size, "f32", eoff(offset, "f32")) for x in row] for row in v]
+    for g, src in ((gm, master), (gmm, m), (gv, v)):
+        for grow, srow in zip(g, src):
+            for gg, x in zip(grow, srow):
+                if x.size:
+                    gg.view.copy_(to_dev(x, "f32"))
+    gp = [[Guarded(d * rn, "bf16", eoff(offset, "bf16")) for _ in range(n)] for d, rn in shapes]
+    gg_ = [[Guarded(d * rn, "bf16", eoff(offset, "bf16")) for _ in range(n)] for d, rn in shapes]
+    flat = lambda xs: [x.ptr() for row in xs for x in row]
+    plan = cr.cr_fsdp2_plan_create(shapes, n, flat(gg_), flat(gm), flat(gmm), flat(gv), flat(gp))
+    table = Guarded(plan.table_bytes // 4 + 1, "i32")
+    cr.cr_fsdp2_plan_upload(plan, table.ptr(), plan.table_bytes)
+    del plan  # the uploaded table is all the step needs besides the plan's sizes
+    plan = cr.cr_fsdp2_plan_create(shapes, n, flat(gg_), flat(gm), flat(gmm), flat(gv), flat(gp))
+    for step in (1, 2):
+        if step == 2:
+            grads = [I.host_rank_buffers(n, d * rn, "bf16", std=1e-3, seed0=900 + 100 * p)
+                     for p, (d, rn) in enumerate(shapes)]
+        for grow, srow in zip(gg_, grads):
+            for x, h in zip(grow, srow):
+                if h.size:
+                    x.view.copy_(to_dev(h, "bf16"))
+        cfg = O.AdamWConfig(step=step)
+        want = O.fsdp2_step(shapes, grads, master, m, v, cfg)
+        cr.cr_fsdp2_step_planned(plan, table.ptr(), cr.adamw_cfg(step=step))
+        torch.cuda.synchronize()
+        table.check()
+        for p in range(len(shapes)):
+            for j in range(n):
+                for g, ref, name in ((gm, master, "master"), (gmm, m, "m"), (gv, v, "v")):
+                    g[p][j].check()
+                    assert_match(g[p][j].host(), ref[p][j], "f32", f"{name} {p} {j} step {step}")
+            for r in range(n):
+                gp[p][r].check()
+                gg_[p][r].check()
+                assert_match(gp[p][r].host(), want[p][r], "bf16", f"param {p} rank {r} step {step}")
+
+
+@pytest.mark.parametrize("n", [2, 8])
+def test_fsdp2_planned_equals_chained_launches(n):
+    """300 parameters (more than the 64 one chained launch takes): the single
+    planned launch and cr_fsdp2_step's chained launches give the same bits,
+    on the same inputs."""
+    rng = np.random.default_rng(n)
+    shapes = [(int(rng.integers(0, 40)), int(rng.integers(1, 300))) for _ in range(300)]
+    grads, master, m, v = fsdp2_host(shapes, n, 7)
+    outs = []
+    for planned in (False, True):
+        d_g = [to_dev(x, "bf16") if x.size else 0 for row in grads for x in row]
+        d_st = [[to_dev(x, "f32") if x.size else 0 for row in t for x in row] for t in (master, m, v)]
+        d_p = [torch.empty(d * rn, dtype=torch.bfloat16, device="cuda") for d, rn in shapes
+               for _ in range(n)]
+        if planned:
+            plan = cr.cr_fsdp2_plan_create(shapes, n, d_g, *d_st, d_p)
+            table = torch.empty(plan.table_bytes, dtype=torch.uint8, device="cuda")
+            cr.cr_fsdp2_plan_upload(plan, table)
+            cr.cr_fsdp2_step_planned(plan, table, cr.adamw_cfg())
+        else:
+            cr.cr_fsdp2_step(shapes, n, d_g, *d_st, cr.adamw_cfg(), d_p)
+        torch.cuda.synchronize()
+        outs.append(([x.cpu() for t in d_st for x in t if not isinstance(x, int)],
+                     [x.view(torch.int16).cpu() for x in d_p]))
+    for a, b in zip(outs[0][0] + outs[0][1], outs[1][0] + outs[1][1]):
+        assert torch.equal(a, b)
+    want = O.fsdp2_step(shapes, grads, master, m, v, O.AdamWConfig())
+    for p in range(len(shapes)):
+        for r in range(n):
+            assert_match(to_host(outs[1][1][p * n + r].view(torch.bfloat16), "bf16"), want[p][r],
+                         "bf16", f"param {p} rank {r}")
+
+
 # ---- gradient accumulation (no_sync) ---------------------------------------------
 
 @pytest.mark.parametrize("n", [1, 2, 3, 8, 16])
