@@ -22,11 +22,12 @@ Multi-GPU (torchrun, one process per GPU), two modes:
   --split replicas (default): every rank runs its own instance of the
       workload (its own 8 emulated ranks); nothing is exchanged on the data
       path, so scaling is weak and value = sum of all ranks' bytes / max time;
-  --split slab: the G ranks share ONE all-reduce workload, rank g holding and
-      reducing only slab g of every buffer's element range (cr_slab_range,
-      whole chunks while G <= 8) through cr_all_reduce_range, which keeps the
-      whole buffers' chunking and so their fold order; nothing is exchanged
-      either, scaling is strong and value = the workload's bytes / max time.
+  --split slab: the G ranks share ONE workload (the all-reduce or the
+      unclipped FSDP step), rank g holding and processing only slab g of
+      every buffer's element range (cr_slab_range, whole chunks while G <= 8)
+      through cr_all_reduce_range / cr_fsdp_step_range, which keep the whole
+      buffers' chunking and so their fold order; nothing is exchanged either,
+      scaling is strong and value = the workload's bytes / max time.
 
 --impl reference times the CPU oracle (the only reference implementation
 this method has) on bounded samples of the same workload.
@@ -211,16 +212,23 @@ class ClockSampler:
 def timed(fn, steps, warmup, world, stream, sampler=None):
     """W untimed calls, then exactly `steps` calls between CUDA events on the
     launching stream, bracketed by barrier + synchronize.  Returns
-    (total_ms, per_step_ms list)."""
+    (total_ms, per_step_ms list).
+
+    The clock sampler starts before the warm-up, so that its thread start
+    does not delay the first timed launch, and samples throughout.  Right
+    before the first event the stream gets a short device-side wait (no
+    memory traffic): the host enqueues the first steps behind it, so the
+    events time back-to-back device work, not the host's first launch."""
     import torch
-    for _ in range(warmup):
-        fn()
-    torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     ctx = sampler if sampler is not None else _Null()
     with ctx:
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        device_wait(stream)
         ev[0].record(stream)
         for i in range(steps):
             fn()
@@ -229,6 +237,16 @@ def timed(fn, steps, warmup, world, stream, sampler=None):
     barrier(world)
     per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
     return ev[0].elapsed_time(ev[steps]), per
+
+
+def device_wait(stream, cycles=200_000):
+    """About 0.1 ms of device-side spinning on `stream` (torch's sleep kernel;
+    nothing if this torch has none)."""
+    import torch
+    sleep = getattr(torch.cuda, "_sleep", None)
+    if sleep is not None:
+        with torch.cuda.stream(stream):
+            sleep(cycles)
 
 
 class _Null:
@@ -486,8 +504,13 @@ class FsdpStep(Workload):
     """Fused FSDP step: 8 ranks, flat `count` params (1.3e9 by default);
     clip=True adds global grad-norm clipping (max_norm 1.0)."""
 
-    def __init__(self, n=8, count=1_300_000_000, clip=False):
+    def __init__(self, n=8, count=1_300_000_000, clip=False, slab=None):
         self.n, self.count, self.clip = n, count, clip
+        if slab is not None and clip:
+            raise SystemExit("the clipped step has no slab form (its norm needs every slab)")
+        # slab = (lo, hi): this GPU holds and steps only parameters [lo, hi)
+        # of the flat buffer (cr_fsdp_step_range); nbytes is its share
+        self.slab = slab
         # clipped, N >= 5: the first pass parks the averaged fp32 gradient in
         # two of the parameter outputs (4 B written, 4 B read back) instead of
         # the update pass folding the N bf16 gradients again (2N B)
@@ -501,6 +524,9 @@ class FsdpStep(Workload):
             self.kernel = f"k_fsdp_vec4<{n}>" + (" + k_fsdp_sumsq + k_clip_coef" if clip else "")
         self.profile = f"k_fsdp_vec_fsdp_step{'_clipped' if clip else ''}_{n}x{tag}"
         self.launches = 3 if clip else 1
+        self.full_nbytes = self.nbytes
+        if slab is not None:
+            self.nbytes = self.nbytes // count * (slab[1] - slab[0])
 
     def setup(self, device):
         import torch
@@ -508,6 +534,8 @@ class FsdpStep(Workload):
         from fsdp_emulated_ranks_gb300 import inputs as I
         n, count = self.n, self.count
         L = cr.cr_chunk_len(count, n)
+        if self.slab is not None:
+            return self._setup_slab(device, L)
         self.t_grads = alloc_ranks(n, count, torch.bfloat16, 1e-3, 1000, device)
         self.t_params = [torch.empty(count, dtype=torch.bfloat16, device=device) for _ in range(n)]
         self.t_master_full = torch.empty(count, dtype=torch.float32, device=device)
@@ -521,9 +549,39 @@ class FsdpStep(Workload):
         self.t_ws = torch.empty(self.ws_bytes // 8, dtype=torch.float64, device=device)
         self.t_norm = torch.empty(1, dtype=torch.float32, device=device)
 
+    def _setup_slab(self, device, L):
+        """The whole workload's values, then only this GPU's slab of the
+        grads and params and its parts of the owners' state shards."""
+        import torch
+        from fsdp_emulated_ranks_gb300 import cr
+        from fsdp_emulated_ranks_gb300 import inputs as I
+        n, count = self.n, self.count
+        lo, hi = self.slab
+        self.t_grads = [g[lo:hi].clone() for g in
+                        alloc_ranks(n, count, torch.bfloat16, 1e-3, 1000, device)]
+        torch.cuda.empty_cache()
+        self.t_params = [torch.empty(hi - lo, dtype=torch.bfloat16, device=device)
+                         for _ in range(n)]
+        full = torch.empty(count, dtype=torch.float32, device=device)
+        I.torch_fill_normal_(full, 0.02, SEED_OFFSET + 2000)
+        self.t_master, self.t_m, self.t_v = [], [], []
+        for j in range(n):
+            a, b = max(lo, j * L), min(hi, (j + 1) * L, count)
+            k = max(0, b - a)
+            self.t_master.append(full[a:a + k].clone() if k else 0)
+            self.t_m.append(torch.zeros(k, dtype=torch.float32, device=device) if k else 0)
+            self.t_v.append(torch.zeros(k, dtype=torch.float32, device=device) if k else 0)
+        del full
+        torch.cuda.empty_cache()
+        self.cfg = cr.adamw_cfg()
+
     def step(self, stream):
         from fsdp_emulated_ranks_gb300 import cr
-        if self.clip:
+        if self.slab is not None:
+            lo, hi = self.slab
+            cr.cr_fsdp_step_range(self.t_grads, self.count, lo, hi, self.t_master, self.t_m,
+                                  self.t_v, self.cfg, self.t_params, stream)
+        elif self.clip:
             cr.cr_fsdp_step_clipped(self.t_grads, self.count, self.t_master, self.t_m, self.t_v,
                                     self.cfg, 1.0, self.t_ws, self.ws_bytes, self.t_params,
                                     self.t_norm, stream)
@@ -729,10 +787,13 @@ def run_headline(args, world, rank, device, stream, peak):
     import torch
     wl = make_workload(args.workload, args)
     if args.split == "slab":
-        if not isinstance(wl, AllReduce):
-            raise SystemExit("--split slab is built for the all-reduce workloads")
-        wl = AllReduce(wl.n, wl.count, wl.dt, wl.op, wl.std,
-                       slab=slab_bounds(wl.count, wl.n, world, rank))
+        if isinstance(wl, AllReduce):
+            wl = AllReduce(wl.n, wl.count, wl.dt, wl.op, wl.std,
+                           slab=slab_bounds(wl.count, wl.n, world, rank))
+        elif isinstance(wl, FsdpStep) and not wl.clip:
+            wl = FsdpStep(wl.n, wl.count, slab=slab_bounds(wl.count, wl.n, world, rank))
+        else:
+            raise SystemExit("--split slab is built for the all-reduce and FSDP step workloads")
     wl.setup(device)
     # Sample for the CPU baseline before in-place calls overwrite the inputs.
     sample = None
@@ -742,7 +803,7 @@ def run_headline(args, world, rank, device, stream, peak):
         sample = [b[:k].view(torch.int16).cpu().numpy().view("uint16") for b in wl.t_bufs]
     sampler = ClockSampler(device)
     total_ms, per = timed(lambda: wl.step(stream), args.steps, args.warmup, world, stream, sampler)
-    if getattr(wl, "slab", None):
+    if getattr(wl, "slab", None) is not None:
         # the ranks' slabs make up one workload: its bytes over the slowest rank's time
         ms_step = max_over_ranks(total_ms, world, device) / args.steps
         value = wl.full_nbytes / (ms_step * 1e-3) / 1e9

@@ -59,6 +59,11 @@ def test_headline_line_has_every_key(tmp_path):
     assert "reduce_scatter_avg_bf16_8ranks_64MiB" in names and len(names) >= 10
     for row in d["rows"]:
         assert row["ms_p10"] <= row["ms_median"] <= row["ms_p90"]
+    summ = d["rows_summary"]   # every row, compactly, as the line's last key
+    assert list(d)[-1] == "rows_summary"
+    assert "allreduce" in summ and len(summ) == 1 + len(d["rows"])
+    assert summ["allreduce"][2] == r["frac_median"] and summ["allreduce"][3] == r["frac"]
+    assert "graph_us" in next(row for row in d["rows"] if row["key"] == "allreduce_f32")
     recs = [json.loads(l) for l in jsonl.read_text().splitlines()]
     assert len(recs) == 1 + len(d["rows"]) and recs[0]["name"] == d["config"]["workload"]
     for k in ("ms_median", "ms_p10", "ms_p90", "algorithmic_bytes", "cpu_baseline"):
@@ -90,3 +95,20 @@ def test_config_flag_selects_the_same_workload_in_both_arms(config, workload):
     assert mine["roofline"]["bound"] == "hbm" and mine["roofline"]["achieved"] > 0
     for k in ("metric", "unit", "higher_is_better", "dtype"):
         assert ref[k] == mine[k], k
+
+
+@pytest.mark.parametrize("workload", ["allreduce", "fsdp"])
+def test_slab_split_on_one_gpu(workload):
+    """--split slab on one GPU: the single slab is the whole element range,
+    run through the range entry point; same workload and bytes, strong
+    scaling."""
+    extra = ["--fsdp-count", str(8 * 1000 * 1000)] if workload == "fsdp" else []
+    d = run(["--workload", workload, "--split", "slab", "--steps", "5", "--warmup", "3",
+             "--no-rows", "--no-e2e", "--no-cpu-baseline"] + extra)
+    whole = run(["--workload", workload, "--steps", "5", "--warmup", "3", "--no-rows",
+                 "--no-e2e", "--no-cpu-baseline"] + extra)
+    assert d["scaling"] == "strong" and whole["scaling"] == "weak"
+    assert d["config"]["workload"] == whole["config"]["workload"]
+    assert d["roofline"]["algorithmic_bytes_per_launch"] == \
+        whole["roofline"]["algorithmic_bytes_per_launch"]
+    assert d["value"] > 0

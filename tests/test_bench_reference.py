@@ -104,3 +104,17 @@ def test_fsdp_row_bytes():
     assert bench.FsdpStep(5, 100, clip=True).nbytes == 52 * 100
     assert bench.FsdpStep(4, 100, clip=True).nbytes == 48 * 100
     assert bench.FsdpStep(2, 100, clip=True).nbytes == 36 * 100
+
+
+def test_slab_workload_bytes():
+    """--split slab: a GPU's share of the bytes is its slab's; the slabs of
+    all GPUs add up to the whole workload's bytes."""
+    for G in (1, 2, 3, 8):
+        ar = [bench.AllReduce(slab=(lo, hi)) for lo, hi in
+              (bench.slab_bounds(1 << 25, 8, G, g) for g in range(G))]
+        assert sum(w.nbytes for w in ar) == ar[0].full_nbytes == bench.AllReduce().nbytes
+        fs = [bench.FsdpStep(8, 1000, slab=(lo, hi)) for lo, hi in
+              (bench.slab_bounds(1000, 8, G, g) for g in range(G))]
+        assert sum(w.nbytes for w in fs) == fs[0].full_nbytes == 56 * 1000
+    with pytest.raises(SystemExit):
+        bench.FsdpStep(8, 1000, clip=True, slab=(0, 500))
