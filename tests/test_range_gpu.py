@@ -189,3 +189,79 @@ def test_range_rejects_bad_bounds():
         with pytest.raises(cr.CRError) as ei:
             cr.cr_all_reduce_range(bufs, count, lo, hi, "f32", "sum", bufs, "f32")
         assert ei.value.status == 1
+
+
+@pytest.mark.parametrize("G", [2, 3, 8])
+def test_headline_split_into_slabs_full_size(G):
+    """The benchmark's --split slab at full size, each slab in buffers of its
+    own as on its own GPU: 8 ranks x 2^25 bf16, AVG, in place.  The slabs
+    put side by side equal the whole-buffer call on every element of every
+    rank, bit for bit (the whole-buffer call is itself checked against the
+    oracle at this size in test_fullsize_gpu.py)."""
+    n, count = 8, 1 << 25
+    bufs = []
+    for r in range(n):
+        t = torch.empty(count, dtype=torch.bfloat16, device="cuda")
+        I.torch_fill_normal_(t, 0.02, r)
+        bufs.append(t)
+    slabs = [cr.cr_slab_range(count, n, G, g) for g in range(G)]
+    parts = [[b[lo:hi].clone() for b in bufs] for lo, hi in slabs]
+    cr.cr_all_reduce(bufs, count, "bf16", "avg", bufs, "bf16")
+    for (lo, hi), p in zip(slabs, parts):
+        cr.cr_all_reduce_range(p, count, lo, hi, "bf16", "avg", p, "bf16")
+    torch.cuda.synchronize()
+    for r in range(n):
+        whole = bufs[r].view(torch.int16)
+        for (lo, hi), p in zip(slabs, parts):
+            assert torch.equal(p[r].view(torch.int16), whole[lo:hi]), (r, lo, hi)
+    del bufs, parts
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("G", [2, 8])
+def test_fsdp_step_split_into_slabs_large(G):
+    """The unclipped FSDP step over 8 x 2^26 parameters split into G slabs,
+    each holding its slab of the grads/params and its parts of the owners'
+    state: equal, bit for bit, to the whole-buffer step."""
+    n, count = 8, 1 << 26
+    L = count // n
+    grads = []
+    for r in range(n):
+        t = torch.empty(count, dtype=torch.bfloat16, device="cuda")
+        I.torch_fill_normal_(t, 1e-3, 1000 + r)
+        grads.append(t)
+    master_full = torch.empty(count, dtype=torch.float32, device="cuda")
+    I.torch_fill_normal_(master_full, 0.02, 2000)
+    state0 = master_full.clone()
+    m_full = torch.zeros(count, dtype=torch.float32, device="cuda")
+    v_full = torch.zeros(count, dtype=torch.float32, device="cuda")
+    params = [torch.empty(count, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    slabs = [cr.cr_slab_range(count, n, G, g) for g in range(G)]
+    own = []
+    for lo, hi in slabs:
+        sg = [g[lo:hi].clone() for g in grads]
+        st = []
+        for src in (state0, m_full, v_full):
+            row = []
+            for j in range(n):
+                a, b = max(lo, j * L), min(hi, (j + 1) * L)
+                row.append(src[a:b].clone() if b > a else 0)
+            st.append(row)
+        sp = [torch.empty(hi - lo, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+        own.append((sg, st, sp))
+    cr.cr_fsdp_step(grads, count, [master_full[j * L:(j + 1) * L] for j in range(n)],
+                    [m_full[j * L:(j + 1) * L] for j in range(n)],
+                    [v_full[j * L:(j + 1) * L] for j in range(n)], cr.adamw_cfg(), params)
+    for (lo, hi), (sg, st, sp) in zip(slabs, own):
+        cr.cr_fsdp_step_range(sg, count, lo, hi, *st, cr.adamw_cfg(), sp)
+    torch.cuda.synchronize()
+    for (lo, hi), (sg, st, sp) in zip(slabs, own):
+        for r in range(n):
+            assert torch.equal(sp[r].view(torch.int16), params[r][lo:hi].view(torch.int16))
+        for q, full in enumerate((master_full, m_full, v_full)):
+            for j in range(n):
+                a, b = max(lo, j * L), min(hi, (j + 1) * L)
+                if b > a:
+                    assert torch.equal(st[q][j], full[a:b]), (q, j, lo, hi)
+    del grads, params, own
+    torch.cuda.empty_cache()
