@@ -210,13 +210,21 @@ class ClockSampler:
 # ---- timing ------------------------------------------------------------------------
 
 def timed(fn, steps, warmup, world, stream, sampler=None):
-    """W untimed calls, then exactly `steps` calls between CUDA events on the
-    launching stream, bracketed by barrier + synchronize.  Returns
-    (total_ms, per_step_ms list).
+    """W untimed calls, then exactly `steps` calls between two CUDA events on
+    the launching stream, bracketed by barrier + synchronize: the total is
+    the time of `steps` back-to-back calls, as a caller issues them.
+    Returns (total_ms, per_step_ms list).
+
+    The per-step list comes from a second pass of `steps` calls with an
+    event recorded after each (outside the bracketed region).  An event
+    between two calls keeps the second call's grid from being dispatched
+    during the first one's last wave (the kernels are launched as
+    programmatic dependents of their predecessor), so per-step times are
+    each call on its own, slightly above total / steps.
 
     The clock sampler starts before the warm-up, so that its thread start
     does not delay the first timed launch, and samples throughout.  Right
-    before the first event the stream gets a short device-side wait (no
+    before each first event the stream gets a short device-side wait (no
     memory traffic): the host enqueues the first steps behind it, so the
     events time back-to-back device work, not the host's first launch."""
     import torch
@@ -227,16 +235,24 @@ def timed(fn, steps, warmup, world, stream, sampler=None):
         torch.cuda.synchronize()
         barrier(world)
         torch.cuda.synchronize()
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         device_wait(stream)
-        ev[0].record(stream)
-        for i in range(steps):
+        t0.record(stream)
+        for _ in range(steps):
             fn()
-            ev[i + 1].record(stream)
+        t1.record(stream)
         torch.cuda.synchronize()
     barrier(world)
+    total = t0.elapsed_time(t1)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    device_wait(stream)
+    ev[0].record(stream)
+    for i in range(steps):
+        fn()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
     per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
-    return ev[0].elapsed_time(ev[steps]), per
+    return total, per
 
 
 def device_wait(stream, cycles=200_000):
@@ -809,7 +825,7 @@ def run_headline(args, world, rank, device, stream, peak):
         value = wl.full_nbytes / (ms_step * 1e-3) / 1e9
     else:
         value, ms_step = job_throughput(wl.nbytes, total_ms, args.steps, world, device)
-    kern_ms = statistics.mean(per)
+    kern_ms = total_ms / args.steps   # this GPU's mean launch, back to back
     achieved = wl.nbytes / (kern_ms * 1e-3) / 1e9
     out = {
         "workload": wl,
@@ -825,7 +841,8 @@ def run_headline(args, world, rank, device, stream, peak):
                      "peak_source": peak[1], "step_ms_median": statistics.median(per),
                      **step_quantiles(per)},
     }
-    # the same figure from the median step (achieved/frac above: the mean)
+    # the same figure from the median of the per-step pass (achieved/frac above:
+    # the mean of the back-to-back steps)
     med = statistics.median(per)
     out["roofline"].update({"achieved_median": round(wl.nbytes / (med * 1e-3) / 1e9, 1),
                             "frac_median": round(wl.nbytes / (med * 1e-3) / 1e9 / peak[0], 4)})
@@ -956,8 +973,8 @@ def run_rows(args, device, stream, peak, skip=None):
         wl = make_workload(name, args)
         wl.setup(device)
         steps = args.row_steps if wl.nbytes < (8 << 30) else max(5, args.row_steps // 2)
-        _, per = timed(lambda: wl.step(stream), steps, 3, 1, stream)
-        ms = statistics.mean(per)
+        total, per = timed(lambda: wl.step(stream), steps, 3, 1, stream)
+        ms = total / steps
         gbs = wl.nbytes / (ms * 1e-3) / 1e9
         rows.append({"name": wl.name, "ms": round(ms, 4), "GB/s": round(gbs, 1),
                      "frac": round(gbs / peak[0], 4), "algorithmic_bytes": wl.nbytes,

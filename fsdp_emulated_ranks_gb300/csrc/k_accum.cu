@@ -13,6 +13,7 @@
 #include "check.cuh"
 #include "cr_internal.cuh"
 #include "fold.cuh"
+#include "pdl.cuh"
 
 namespace cr {
 
@@ -87,6 +88,7 @@ __device__ __forceinline__ void accum_elem(const AccumArgs& a, int n, uint64_t e
 template <int GD, int NT, int SW>
 __global__ void __launch_bounds__(kBlock)
     k_accum_vec(const __grid_constant__ AccumArgs a) {
+  pdl_enter();
   const int n = NT > 0 ? NT : a.n;
   const uint64_t nvec = a.count / 8;
   const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -145,6 +147,7 @@ __global__ void __launch_bounds__(kBlock)
 template <int GD>
 __global__ void __launch_bounds__(kBlock)
     k_accum_elem(const __grid_constant__ AccumArgs a) {
+  pdl_enter();
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
   for (uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; e < a.count; e += stride)
     accum_elem<GD>(a, a.n, e);
@@ -155,12 +158,11 @@ static cudaError_t accum_dispatch(const AccumArgs& a, cudaStream_t s) {
   const dim3 grid(flat_grid(a.count / 8 + 1), a.reduce ? 1 : a.n);
   clear_stale_error();
   switch (a.reduce ? a.n : 0) {
-    case 2: k_accum_vec<GD, 2, SW><<<grid, kBlock, 0, s>>>(a); break;
-    case 4: k_accum_vec<GD, 4, SW><<<grid, kBlock, 0, s>>>(a); break;
-    case 8: k_accum_vec<GD, 8, SW><<<grid, kBlock, 0, s>>>(a); break;
-    default: k_accum_vec<GD, 0, SW><<<grid, kBlock, 0, s>>>(a); break;
+    case 2: return launch_pdl(k_accum_vec<GD, 2, SW>, grid, kBlock, s, a);
+    case 4: return launch_pdl(k_accum_vec<GD, 4, SW>, grid, kBlock, s, a);
+    case 8: return launch_pdl(k_accum_vec<GD, 8, SW>, grid, kBlock, s, a);
+    default: return launch_pdl(k_accum_vec<GD, 0, SW>, grid, kBlock, s, a);
   }
-  return cudaGetLastError();
 }
 
 template <int GD>
@@ -168,8 +170,7 @@ static cudaError_t accum_by_width(const AccumArgs& a, int vw, cudaStream_t s) {
   if (vw == 32) return accum_dispatch<GD, 8>(a, s);
   if (vw == 16) return accum_dispatch<GD, 4>(a, s);
   clear_stale_error();
-  k_accum_elem<GD><<<flat_grid(a.count), kBlock, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_accum_elem<GD>, dim3(flat_grid(a.count)), kBlock, s, a);
 }
 
 cudaError_t launch_accum(cr_dtype grad_dtype, const AccumArgs& a, int vw, cudaStream_t s) {

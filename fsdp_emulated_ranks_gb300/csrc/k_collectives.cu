@@ -29,6 +29,7 @@
 #include "check.cuh"
 #include "cr_internal.cuh"
 #include "fold.cuh"
+#include "pdl.cuh"
 
 namespace cr {
 
@@ -60,6 +61,7 @@ __device__ __forceinline__ void fold_range(const FoldArgs& a) {
   constexpr int OS = Elem<DO>::kSize;
   constexpr int VEC = elems_per<DI, NW>();
   constexpr int OB = VEC * OS;
+  pdl_enter();
   const int n = NT > 0 ? NT : a.n;
   const uint64_t vbeg = (a.begin + VEC - 1) / VEC;
   const uint64_t vend = a.end / VEC;
@@ -132,6 +134,7 @@ __global__ void __launch_bounds__(kBlock, 3) k_fold_vec3(const __grid_constant__
 template <int DI, int DO, int MODE, bool WIRE>
 __global__ void __launch_bounds__(kBlock)
     k_fold_elem(const __grid_constant__ FoldArgs a) {
+  pdl_enter();
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
   for (uint64_t e = a.begin + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; e < a.end;
        e += stride)
@@ -157,6 +160,7 @@ constexpr int kGatherSpanVecs = 2 * kBlock;
 template <int ES, int NW>
 __global__ void __launch_bounds__(kBlock, 8)
     k_gather_vec(const __grid_constant__ GatherArgs a) {
+  pdl_enter();
   constexpr int VEC = NW * 4 / ES;
   const uint64_t nvec = a.count / VEC;
   const int dest = blockIdx.x;
@@ -203,6 +207,7 @@ __global__ void __launch_bounds__(kBlock, 8)
 template <int ES>
 __global__ void __launch_bounds__(kBlock)
     k_gather_elem(const __grid_constant__ GatherArgs a) {
+  pdl_enter();
   using W = typename std::conditional<ES == 2, uint16_t, uint32_t>::type;
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
   for (uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -224,8 +229,7 @@ __global__ void __launch_bounds__(kBlock)
 template <typename K, typename A>
 static cudaError_t launch_flat(K kernel, const A& args, uint64_t threads, cudaStream_t s) {
   clear_stale_error();
-  kernel<<<flat_grid(threads), kBlock, 0, s>>>(args);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(flat_grid(threads)), kBlock, s, args);
 }
 
 template <typename K>
@@ -234,8 +238,7 @@ static cudaError_t launch_fold_kernel(K kernel, const FoldArgs& a, uint64_t thre
   unsigned grid = flat_grid(threads);
   if (a.max_ctas && grid > a.max_ctas) grid = a.max_ctas;
   clear_stale_error();
-  kernel<<<grid, kBlock, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(grid), kBlock, s, a);
 }
 
 // A compile-time rank count: 32-byte vectors take the kernel built for 3
@@ -301,8 +304,7 @@ static cudaError_t launch_gather_vec(const GatherArgs& a, cudaStream_t s) {
   if (nz > 65535) return cudaErrorInvalidValue;  // beyond 2^52 elements
   const dim3 grid((unsigned)a.n, (unsigned)ny, (unsigned)nz);
   clear_stale_error();
-  k_gather_vec<ES, NW><<<grid, kBlock, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_gather_vec<ES, NW>, grid, kBlock, s, a);
 }
 
 cudaError_t launch_gather(size_t esize, const GatherArgs& a, int vw,

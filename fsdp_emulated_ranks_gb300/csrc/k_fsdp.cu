@@ -27,6 +27,7 @@
 #include "check.cuh"
 #include "cr_internal.cuh"
 #include "fold.cuh"
+#include "pdl.cuh"
 #include "fsdp_body.cuh"
 
 namespace cr {
@@ -36,6 +37,7 @@ namespace cr {
 // shuffle tree), so the norm is reproducible run to run.
 __global__ void k_clip_coef(const double* partials, int nparts, double max_norm, float* coef,
                             float* norm_out) {
+  pdl_enter();
   double t = 0.0;
   for (int i = threadIdx.x; i < nparts; i += 32) t += partials[i];
 #pragma unroll
@@ -52,8 +54,7 @@ __global__ void k_clip_coef(const double* partials, int nparts, double max_norm,
 cudaError_t launch_clip_coef(const double* partials, int nparts, double max_norm, float* coef,
                              float* norm_out, cudaStream_t s) {
   clear_stale_error();
-  k_clip_coef<<<1, 32, 0, s>>>(partials, nparts, max_norm, coef, norm_out);
-  return cudaGetLastError();
+  return launch_pdl(k_clip_coef, dim3(1), 32, s, partials, nparts, max_norm, coef, norm_out);
 }
 
 __device__ __forceinline__ float clip_coef(const FsdpArgs& a) {
@@ -69,6 +70,7 @@ template <int NT, bool VEC, bool STASH = false>
 __global__ void __launch_bounds__(kBlock)
     k_fsdp_sumsq(const __grid_constant__ FsdpArgs a, double* partials) {
   __shared__ double s_warp[kBlock / 32];
+  pdl_enter();
   const int n = NT > 0 ? NT : a.n;
   const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
@@ -127,6 +129,7 @@ __device__ __forceinline__ void fsdp_one(const FsdpArgs& a, int n, float coef, u
 
 template <int NT, int SW, bool STASH>
 __device__ __forceinline__ void fsdp_range(const FsdpArgs& a) {
+  pdl_enter();
   const int n = NT > 0 ? NT : a.n;
   const float coef = clip_coef(a);
   const uint64_t vbeg = (a.begin + 7) / 8, vend = a.end / 8;
@@ -170,6 +173,7 @@ __global__ void __launch_bounds__(kBlock, 4) k_fsdp_vec4(const __grid_constant__
 
 __global__ void __launch_bounds__(kBlock)
     k_fsdp_elem(const __grid_constant__ FsdpArgs a) {
+  pdl_enter();
   const float coef = clip_coef(a);
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
   for (uint64_t e = a.begin + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; e < a.end;
@@ -183,6 +187,7 @@ __global__ void __launch_bounds__(kBlock)
 
 __global__ void __launch_bounds__(kBlock)
     k_adamw_vec(const __grid_constant__ AdamArgs a) {
+  pdl_enter();
   const uint64_t nvec = a.n / 4;
   const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
@@ -222,6 +227,7 @@ __global__ void __launch_bounds__(kBlock)
 
 __global__ void __launch_bounds__(kBlock)
     k_adamw_elem(const __grid_constant__ AdamArgs a) {
+  pdl_enter();
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
   for (uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; e < a.n;
        e += stride) {
@@ -236,8 +242,7 @@ __global__ void __launch_bounds__(kBlock)
 template <typename K, typename A>
 static cudaError_t launch_flat(K kernel, const A& args, uint64_t threads, cudaStream_t s) {
   clear_stale_error();
-  kernel<<<flat_grid(threads), kBlock, 0, s>>>(args);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(flat_grid(threads)), kBlock, s, args);
 }
 
 template <int SW>
@@ -276,8 +281,7 @@ static cudaError_t sumsq_launch(const FsdpArgs& a, double* partials, int max_par
   if (grid > max_parts) grid = max_parts;
   *nparts = grid;
   clear_stale_error();
-  k_fsdp_sumsq<NT, VEC, STASH><<<grid, kBlock, 0, s>>>(a, partials);
-  return cudaGetLastError();
+  return launch_pdl(k_fsdp_sumsq<NT, VEC, STASH>, dim3(grid), kBlock, s, a, partials);
 }
 
 cudaError_t launch_fsdp_sumsq(const FsdpArgs& a, bool vec, double* partials,

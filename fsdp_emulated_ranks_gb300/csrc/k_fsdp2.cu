@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(kBlock)
 template <int NT>
 __global__ void __launch_bounds__(kBlock, NT > 0 ? 4 : 2)
     k_fsdp2_table(const __grid_constant__ Fsdp2TableArgs a) {
+  pdl_enter();
   __shared__ void* s_ptr[5 * kMaxRanks];
   __shared__ uint4 s_desc[3];  // the tile's Fsdp2Param (48 bytes)
   static_assert(sizeof(Fsdp2Param) == sizeof(s_desc), "descriptor size");
@@ -139,12 +140,11 @@ cudaError_t launch_fsdp2_table(const Fsdp2TableArgs& a, cudaStream_t s) {
   const unsigned grid = flat_grid((uint64_t)a.ntiles * kBlock);
   clear_stale_error();
   switch (a.n) {
-    case 2: k_fsdp2_table<2><<<grid, kBlock, 0, s>>>(a); break;
-    case 4: k_fsdp2_table<4><<<grid, kBlock, 0, s>>>(a); break;
-    case 8: k_fsdp2_table<8><<<grid, kBlock, 0, s>>>(a); break;
-    default: k_fsdp2_table<0><<<grid, kBlock, 0, s>>>(a); break;
+    case 2: return launch_pdl(k_fsdp2_table<2>, dim3(grid), kBlock, s, a);
+    case 4: return launch_pdl(k_fsdp2_table<4>, dim3(grid), kBlock, s, a);
+    case 8: return launch_pdl(k_fsdp2_table<8>, dim3(grid), kBlock, s, a);
+    default: return launch_pdl(k_fsdp2_table<0>, dim3(grid), kBlock, s, a);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace cr

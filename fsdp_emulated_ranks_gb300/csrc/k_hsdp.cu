@@ -22,6 +22,7 @@
 #include "check.cuh"
 #include "cr_internal.cuh"
 #include "fold.cuh"
+#include "pdl.cuh"
 
 namespace cr {
 
@@ -120,6 +121,7 @@ __device__ __forceinline__ void hsdp_range(const HsdpArgs& a) {
 // under the 4-CTA bound (which spills over a kilobyte).
 template <int DI, int DO, int RT, int ST, int NW>
 __global__ void __launch_bounds__(kBlock, 2) k_hsdp_vec(const __grid_constant__ HsdpArgs a) {
+  pdl_enter();
   hsdp_range<DI, DO, RT, ST, NW>(a);
 }
 
@@ -128,12 +130,14 @@ __global__ void __launch_bounds__(kBlock, 2) k_hsdp_vec(const __grid_constant__ 
 // that 68 allow.
 template <int DI, int DO, int RT, int ST, int NW>
 __global__ void __launch_bounds__(kBlock, 4) k_hsdp_vec4(const __grid_constant__ HsdpArgs a) {
+  pdl_enter();
   hsdp_range<DI, DO, RT, ST, NW>(a);
 }
 
 template <int DI, int DO>
 __global__ void __launch_bounds__(kBlock)
     k_hsdp_elem(const __grid_constant__ HsdpArgs a) {
+  pdl_enter();
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
   for (uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; e < a.count; e += stride)
     hsdp_elem<DI, DO>(a, a.R, a.S, e);
@@ -143,8 +147,7 @@ template <typename K>
 static cudaError_t launch_flat_hsdp(K kernel, const HsdpArgs& a, uint64_t threads,
                                     cudaStream_t s) {
   clear_stale_error();
-  kernel<<<flat_grid(threads), kBlock, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(flat_grid(threads)), kBlock, s, a);
 }
 
 template <int DI, int DO, int NW>

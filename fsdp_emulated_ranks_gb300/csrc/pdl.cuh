@@ -1,20 +1,36 @@
-// pdl.cuh -- chaining the launches of one call with programmatic dependent
-// launch (sm_90 and later).
+// pdl.cuh -- programmatic dependent launch (sm_90 and later), in two uses.
 //
-// A call whose work does not fit one launch (the tensor and pointer tables
-// are passed by value, at most 32 KB per launch) issues several launches of
-// the same kernel over disjoint data.  Plain stream order makes each launch
-// wait for the previous one to drain completely, leaving SMs idle during
-// its last wave.  Chained, launch k+1 (launched with programmatic stream
-// serialisation) may start once every CTA of launch k has started
-// (launch_dependents is the first thing each CTA does), so its CTAs fill the
-// SMs that launch k's last wave frees.  Each CTA of a chained launch waits
-// for the previous launch to complete before it exits (griddepcontrol.wait),
-// so the last launch completes only after all earlier ones have: to the
-// stream, and to the caller, the call still ends when all its work has.
-// The wait cannot deadlock: launch k's CTAs have all started before any CTA
-// of launch k+1 exists, and none of them waits on anything.  In a launch
-// without the attribute griddepcontrol.wait returns at once.
+// 1. Chaining the launches of one call.  A call whose work does not fit one
+// launch (the tensor and pointer tables are passed by value, at most 32 KB
+// per launch) issues several launches of the same kernel over disjoint
+// data.  Plain stream order makes each launch wait for the previous one to
+// drain completely, leaving SMs idle during its last wave.  Chained, launch
+// k+1 (launched with programmatic stream serialisation) may start once every
+// CTA of launch k has started (launch_dependents is the first thing each CTA
+// does), so its CTAs fill the SMs that launch k's last wave frees.  Each CTA
+// of a chained launch waits for the previous launch to complete before it
+// exits (griddepcontrol.wait), so the last launch completes only after all
+// earlier ones have: to the stream, and to the caller, the call still ends
+// when all its work has.  The first launch of a call is a plain launch.
+//
+// 2. Overlapping consecutive calls.  Every single-launch kernel (the folds,
+// the all-gather, HSDP, accumulation, the FSDP and AdamW kernels, the FSDP2
+// table kernel) is launched with programmatic stream serialisation and
+// begins with pdl_enter(): it lets its own dependents start, then waits for
+// its prerequisite grid to complete -- with that grid's memory visible --
+// before its first load or store.  When the previous kernel on the stream
+// is one of these, the new grid's CTAs are dispatched during the previous
+// grid's last wave and start their loads the moment it completes, instead
+// of after a launch gap.  Data dependences between calls (an in-place
+// all-reduce reading what the last one wrote) are kept: nothing is touched
+// before the wait returns.  After any other kernel (no early trigger) or a
+// stream operation that is not a kernel, the launch waits in plain stream
+// order.  A kernel that follows one of these without the attribute waits for
+// it to complete, as usual.
+//
+// No wait can deadlock: a grid's dependents start only after all of its
+// CTAs have started, and none of them waits on anything but earlier grids.
+// In a launch without the attribute griddepcontrol.wait returns at once.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -29,13 +45,19 @@ __device__ __forceinline__ void pdl_wait_prerequisites() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// The first statement of every kernel launched with launch_pdl.
+__device__ __forceinline__ void pdl_enter() {
+  pdl_launch_dependents();
+  pdl_wait_prerequisites();
+}
+
 // Launch `kernel` on `grid` CTAs of `block` threads; `chained` launches it
 // as the programmatic dependent of the previous launch on the stream.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_chained(void (*kernel)(KArgs...), unsigned grid, unsigned block,
+cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, unsigned block,
                            cudaStream_t s, bool chained, Args... args) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = grid;
   cfg.blockDim = dim3(block);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
@@ -45,6 +67,14 @@ cudaError_t launch_chained(void (*kernel)(KArgs...), unsigned grid, unsigned blo
   cfg.attrs = chained ? attr : nullptr;
   cfg.numAttrs = chained ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// A single-launch kernel that begins with pdl_enter(): launched as the
+// programmatic dependent of whatever precedes it on the stream.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, unsigned block, cudaStream_t s,
+                       Args... args) {
+  return launch_chained(kernel, grid, block, s, true, args...);
 }
 
 }  // namespace cr
