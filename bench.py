@@ -224,19 +224,27 @@ def timed(fn, steps, warmup, world, stream, sampler=None):
 
     The clock sampler starts before the warm-up, so that its thread start
     does not delay the first timed launch, and samples throughout.  Right
-    before each first event the stream gets a short device-side wait (no
-    memory traffic): the host enqueues the first steps behind it, so the
-    events time back-to-back device work, not the host's first launch."""
+    before each first event the stream gets a device-side wait (no memory
+    traffic) as long as one host enqueue of a step plus 10 us (the last
+    warm-up step's host time; 20-100 us): the first step is queued behind
+    it, so the events time device work from the first step on, and a
+    host-bound step gets no head start beyond its first enqueue.  (For the
+    headline all-reduce the time per call is flat, 153.7-153.8 us, for any
+    wait of 20 us or more, and 154.6 us at 5 us.)"""
     import torch
     ctx = sampler if sampler is not None else _Null()
     with ctx:
+        host_s = 0.0
         for _ in range(warmup):
+            t = time.perf_counter()
             fn()
+            host_s = time.perf_counter() - t
+        wait_s = min(max(host_s + 10e-6, 20e-6), 100e-6)
         torch.cuda.synchronize()
         barrier(world)
         torch.cuda.synchronize()
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        device_wait(stream)
+        device_wait(stream, wait_s)
         t0.record(stream)
         for _ in range(steps):
             fn()
@@ -245,7 +253,7 @@ def timed(fn, steps, warmup, world, stream, sampler=None):
     barrier(world)
     total = t0.elapsed_time(t1)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
-    device_wait(stream)
+    device_wait(stream, wait_s)
     ev[0].record(stream)
     for i in range(steps):
         fn()
@@ -255,14 +263,15 @@ def timed(fn, steps, warmup, world, stream, sampler=None):
     return total, per
 
 
-def device_wait(stream, cycles=200_000):
-    """About 0.1 ms of device-side spinning on `stream` (torch's sleep kernel;
-    nothing if this torch has none)."""
+def device_wait(stream, seconds):
+    """About `seconds` of device-side spinning on `stream` (torch's sleep
+    kernel, counted in SM cycles at about 2 GHz; nothing if this torch has
+    none)."""
     import torch
     sleep = getattr(torch.cuda, "_sleep", None)
     if sleep is not None:
         with torch.cuda.stream(stream):
-            sleep(cycles)
+            sleep(max(1, int(seconds * 2.0e9)))
 
 
 class _Null:

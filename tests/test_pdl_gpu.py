@@ -130,3 +130,30 @@ def test_chained_call_replays_from_a_graph():
     torch.cuda.synchronize()
     for k in range(len(work)):
         assert torch.equal(work[k].view(torch.int16), ref[k].view(torch.int16)), k
+
+
+@pytest.mark.parametrize("n", [3, 8])
+def test_back_to_back_dependent_calls_overlap_safely(n):
+    """Single-launch kernels are dispatched during the previous kernel's last
+    wave and wait for it before their first access.  A long chain of calls
+    that each read what the one before wrote -- in-place all-reduce, then
+    reduce-scatter into shards that are rank j's own chunk, then all-gather
+    back in place, 30 times over -- must give exactly what the arithmetic
+    says: int32 SUM multiplies every element by n per all-reduce (the
+    reduce-scatter + all-gather pair is one more), with wrap modulo 2^32."""
+    count = 8 * n * 50000 + 8 * n
+    rng = np.random.default_rng(n)
+    x = rng.integers(-1000, 1000, size=count, dtype=np.int32)
+    bufs = [torch.from_numpy(x.copy()).cuda() for _ in range(n)]
+    L = cr.cr_chunk_len(count, n)
+    shards = [bufs[j][j * L:min((j + 1) * L, count)] for j in range(n)]
+    rounds = 30
+    for _ in range(rounds):
+        cr.cr_all_reduce(bufs, count, "i32", "sum", bufs, "i32")
+        cr.cr_reduce_scatter(bufs, count, "i32", "sum", shards, "i32")
+        cr.cr_all_gather(shards, count, "i32", bufs)
+    torch.cuda.synchronize()
+    factor = pow(n, 2 * rounds, 1 << 32)
+    want = ((x.astype(np.int64) % (1 << 32)) * factor % (1 << 32)).astype(np.uint32).view(np.int32)
+    for r in range(n):
+        assert np.array_equal(bufs[r].cpu().numpy(), want), r
