@@ -169,6 +169,34 @@ int main() {
     }
   }
 
+  // The FSDP2 plan of the same parameters and its device table.
+  cr_fsdp2_plan_t* plan2 = nullptr;
+  if (cr_fsdp2_plan_create(shapes, 2, N, (const void* const*)g2, m2, mm2, mv2, p2, &plan2) !=
+      CR_OK) {
+    printf("SETUP: cr_fsdp2_plan_create: %s\n", cr_last_error());
+    return 2;
+  }
+  const size_t tb = cr_fsdp2_plan_table_bytes(plan2);
+  void* table = A.get(tb);
+
+  // Range forms: the slab [RB, RE) of every buffer, which cuts chunks 0 and 3.
+  constexpr size_t RB = L / 2 + 1, RE = C - 3;
+  void *rin[N], *rout[N], *rsh[N], *rg[N], *rp[N];
+  float *rms[N], *rmm[N], *rmv[N];
+  for (int r = 0; r < N; ++r) {
+    const size_t lo = RB > L * r ? RB : L * r;
+    const size_t hi0 = L * (r + 1) < C ? L * (r + 1) : C;
+    const size_t hi = RE < hi0 ? RE : hi0;
+    rin[r] = static_cast<char*>(xi[r]) + RB * 4;    // int32 slabs
+    rout[r] = static_cast<char*>(gi[r]) + RB * 4;
+    rsh[r] = hi > lo ? static_cast<char*>(shi[r]) + (lo - L * r) * 4 : nullptr;
+    rg[r] = static_cast<char*>(gb[r]) + RB * 2;     // bf16 slabs
+    rp[r] = static_cast<char*>(pb[r]) + RB * 2;
+    rms[r] = hi > lo ? ms[r] + (lo - L * r) : nullptr;
+    rmm[r] = hi > lo ? mm[r] + (lo - L * r) : nullptr;
+    rmv[r] = hi > lo ? mv[r] + (lo - L * r) : nullptr;
+  }
+
   // Buckets: three bf16 tensors, a 4096-byte cap -> buckets {t2, t1}, {t0}.
   const size_t numels[3] = {1000, 37, 2000};
   cr_bucket_plan_t* plan = nullptr;
@@ -205,6 +233,9 @@ int main() {
   cudaStream_t bad, good;
   CK(cudaStreamCreateWithFlags(&bad, cudaStreamNonBlocking));
   CK(cudaStreamCreateWithFlags(&good, cudaStreamNonBlocking));
+  // The FSDP2 table, uploaded once before the capture.
+  expect_ok(cr_fsdp2_plan_upload(plan2, table, tb, (cr_stream_t)good), "cr_fsdp2_plan_upload");
+  CK(cudaStreamSynchronize(good));
   // The no-alloc step looks its static array up on its first call on a
   // device; that call has to come before any capture (as documented).
   expect_ok(cr_fsdp_step_clipped_noalloc((const void* const*)gb, N, C, ms, mm, mv, &cfg, 1.0,
@@ -313,8 +344,19 @@ int main() {
     }
     EXPECT(cr_comm_broken(comm) == 0, "a refused launch must not break the communicator");
   }
-  // Last: a chained launch (cudaLaunchKernelEx) refused, so that the next
-  // call -- a <<<>>> launch -- would see a stale error if one were kept.
+  expect_cuda_error(cr_all_reduce_range((const void* const*)rin, N, C, RB, RE, CR_I32, CR_SUM,
+                                        rout, CR_I32, sb),
+                    "cr_all_reduce_range");
+  expect_cuda_error(cr_reduce_scatter_range((const void* const*)rin, N, C, RB, RE, CR_I32, CR_SUM,
+                                            rsh, CR_I32, sb),
+                    "cr_reduce_scatter_range");
+  expect_cuda_error(cr_fsdp_step_range((const void* const*)rg, N, C, RB, RE, rms, rmm, rmv, &cfg,
+                                       rp, sb),
+                    "cr_fsdp_step_range");
+  expect_cuda_error(cr_fsdp2_plan_upload(plan2, table, tb, sb), "cr_fsdp2_plan_upload");
+  expect_cuda_error(cr_fsdp2_step_planned(plan2, table, &cfg, sb), "cr_fsdp2_step_planned");
+  // Last: a chained launch refused, so that the next call's launch would
+  // see a stale error in the runtime's last-error word if one were kept.
   expect_cuda_error(cr_fsdp2_step(shapes, 2, N, (const void* const*)g2, m2, mm2, mv2, &cfg, p2, sb),
                     "cr_fsdp2_step");
 
@@ -346,6 +388,23 @@ int main() {
   EXPECT(wrong == 0, "%zu all-reduce results differ from the closed form", wrong);
   expect_ok(cr_fsdp2_step(shapes, 2, N, (const void* const*)g2, m2, mm2, mv2, &cfg, p2, sg),
             "cr_fsdp2_step");
+  expect_ok(cr_fsdp2_step_planned(plan2, table, &cfg, sg), "cr_fsdp2_step_planned");
+  expect_ok(cr_fsdp_step_range((const void* const*)rg, N, C, RB, RE, rms, rmm, rmv, &cfg, rp, sg),
+            "cr_fsdp_step_range");
+  {
+    // the range all-reduce of the closed-form inputs: 10 * (e % 7 + 1)
+    // after the all-reduce above, so the slab sums to 40 * (e % 7 + 1)
+    expect_ok(cr_all_reduce_range((const void* const*)rin, N, C, RB, RE, CR_I32, CR_SUM, rout,
+                                  CR_I32, sg),
+              "cr_all_reduce_range");
+    CK(cudaStreamSynchronize(good));
+    size_t bad_range = 0;
+    for (int r = 0; r < N; ++r) {
+      CK(cudaMemcpy(hx.data(), gi[r], C * 4, cudaMemcpyDeviceToHost));
+      for (size_t e = RB; e < RE; ++e) bad_range += hx[e] != (int32_t)(40 * (e % 7 + 1));
+    }
+    EXPECT(bad_range == 0, "%zu range all-reduce results differ from the closed form", bad_range);
+  }
   expect_ok(cr_bucket_all_reduce_fused(plan, N, bt.data(), CR_BF16, CR_AVG, sg),
             "cr_bucket_all_reduce_fused");
   expect_ok(cr_fsdp_step_clipped(cgb, N, C, ms, mm, mv, &cfg, 1.0, ws, wsb, pb, nullptr, sg),
@@ -384,6 +443,7 @@ int main() {
   CK(cudaDeviceSynchronize());
 
   cr_bucket_plan_free(plan);
+  cr_fsdp2_plan_free(plan2);
   for (int r = 0; r < N; ++r) cudaFreeHost(hin[r]);
   cudaStreamDestroy(bad);
   cudaStreamDestroy(good);
