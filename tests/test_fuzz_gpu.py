@@ -224,3 +224,40 @@ def test_fuzz_fsdp_step(case):
                 assert_match(gg[j].host(), ref[j], "f32", f"{name}[{j}] step {step}")
         for r in range(n):
             assert_match(d_p[r].host(), want_p[r], "bf16", f"n={n} count={count} params[{r}]")
+
+
+@pytest.mark.parametrize("case", range(40))
+def test_fuzz_range_forms(case):
+    """Range all-reduce and reduce-scatter over a random slab [lo, hi) of a
+    random workload, every slab buffer and shard part at its own offset:
+    the slab's elements of the oracle's whole-buffer results, bit for bit,
+    with canaries intact."""
+    rng = np.random.default_rng(9000 + case)
+    n = int(rng.integers(1, 13))
+    dt, op, out = PAIRS[int(rng.integers(len(PAIRS)))]
+    count = max(1, draw_count(rng, n))
+    lo = int(rng.integers(0, count + 1))
+    hi = int(rng.integers(lo, count + 1))
+    host = host_inputs(n, count, dt, seed=500 + case)
+    L = O.chunk_len(count, n)
+    oi, oo = offs(rng, n, dt), offs(rng, n, out)
+    ar, _ = O.ring_all_reduce(host, dt, op, out)
+    slab = [to_dev(np.ascontiguousarray(x[lo:hi]), dt, o) if hi > lo else 0
+            for x, o in zip(host, oi)]
+    outs = [Guarded(hi - lo, out, o) for o in oo]
+    cr.cr_all_reduce_range(slab, count, lo, hi, dt, op, [g.ptr() for g in outs], out)
+    torch.cuda.synchronize()
+    for r in range(n):
+        outs[r].check()
+        assert_match(outs[r].host(), ar[r][lo:hi], out, f"AR range n={n} [{lo},{hi}) of {count}")
+    rs, _ = O.ring_reduce_scatter(host, dt, op, out)
+    parts = []
+    for j in range(n):
+        a, b = max(lo, j * L), min(hi, (j + 1) * L, count)
+        parts.append((a - j * L, max(0, b - a)))
+    sh = [Guarded(k, out, o) for (_, k), o in zip(parts, offs(rng, n, out))]
+    cr.cr_reduce_scatter_range(slab, count, lo, hi, dt, op, [g.ptr() for g in sh], out)
+    torch.cuda.synchronize()
+    for j, ((a, k), g) in enumerate(zip(parts, sh)):
+        g.check()
+        assert_match(g.host(), rs[j][a:a + k], out, f"RS range n={n} shard {j}")
