@@ -592,7 +592,8 @@ cr_status cr_fsdp2_step(const cr_param_shape* shapes, int nparams, int nranks,
  * cr_fsdp2_plan_table_bytes(plan), 16-byte aligned (CR_ERR_ALIGNMENT).  The
  * copy is from pageable host memory: the call returns once the bytes are
  * staged, so the plan may be freed right after it.  Upload once per
- * parameter set, not per step.
+ * parameter set, not per step, and outside any stream capture: a captured
+ * copy would read the plan's host memory again at every replay.
  * cr_fsdp2_step_planned launches the step for the plan's parameters, with
  * the table read from `table` (which must hold this plan's uploaded bytes,
  * unchanged, until the launch completes) and the AdamW configuration given
