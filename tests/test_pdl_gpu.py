@@ -157,3 +157,29 @@ def test_back_to_back_dependent_calls_overlap_safely(n):
     want = ((x.astype(np.int64) % (1 << 32)) * factor % (1 << 32)).astype(np.uint32).view(np.int32)
     for r in range(n):
         assert np.array_equal(bufs[r].cpu().numpy(), want), r
+
+
+def test_overlapped_calls_interleaved_with_torch_kernels():
+    """Library calls launched as programmatic dependents, with ordinary torch
+    kernels between them on the same stream: each torch kernel must see the
+    finished all-reduce, and the next all-reduce must see what the torch
+    kernel wrote (a kernel without the early trigger releases its dependent
+    only when it completes).  int32 SUM over 4 ranks, exact closed form."""
+    n = 4
+    count = 8 * n * 40000 + 12
+    rng = np.random.default_rng(11)
+    x = rng.integers(-50, 50, size=count).astype(np.int64)
+    bufs = [torch.from_numpy(x.astype(np.int32)).cuda() for _ in range(n)]
+    want = [x.copy() for _ in range(n)]
+    for k in range(12):
+        cr.cr_all_reduce(bufs, count, "i32", "sum", bufs, "i32")
+        tot = sum(want)
+        want = [tot.copy() for _ in range(n)]
+        bufs[k % n].add_(k + 1)            # a torch kernel on rank k % n's buffer
+        want[k % n] = want[k % n] + (k + 1)
+        bufs[(k + 1) % n].mul_(-1)         # and another on the next rank's
+        want[(k + 1) % n] = -want[(k + 1) % n]
+    torch.cuda.synchronize()
+    for r in range(n):
+        w = ((want[r] % (1 << 32)).astype(np.uint64) % (1 << 32)).astype(np.uint32).view(np.int32)
+        assert np.array_equal(bufs[r].cpu().numpy(), w), r
