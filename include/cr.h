@@ -526,8 +526,10 @@ cr_status cr_fsdp_step_clipped(const void* const* grads_bf16, int nranks,
  * workspace (coefficient and sum-of-squares partials) kept in a static
  * device array of 4096 doubles (32 KiB) that the library holds on every GPU
  * that loads it until the process exits.  The first pass uses one partial
- * per CTA and at most 4095 CTAs (the array's partial slots), so any GPU
- * fits.  The first call on each device looks up the array's device address
+ * per CTA and at most 4095 CTAs (the array's partial slots) whatever the
+ * element count and the GPU, so no call can need more scratch than the
+ * array holds and no size is refused on that account; other arguments are
+ * checked and refused exactly as cr_fsdp_step_clipped does.  The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and caches it for that
  * device's current context, keyed on the driver's context ID; a context
  * created later on the device (after cudaDeviceReset, say) gets its own
