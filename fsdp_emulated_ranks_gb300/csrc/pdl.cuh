@@ -16,20 +16,27 @@
 // 2. Overlapping consecutive calls.  Every single-launch kernel (the folds,
 // the all-gather, HSDP, accumulation, the FSDP and AdamW kernels, the FSDP2
 // table kernel) is launched with programmatic stream serialisation and
-// begins with pdl_enter(): it lets its own dependents start, then waits for
-// its prerequisite grid to complete -- with that grid's memory visible --
-// before its first load or store.  When the previous kernel on the stream
-// is one of these, the new grid's CTAs are dispatched during the previous
-// grid's last wave and start their loads the moment it completes, instead
-// of after a launch gap.  Data dependences between calls (an in-place
+// begins with pdl_enter(): it waits for its prerequisite grid to complete
+// -- with that grid's memory visible -- before its first load or store,
+// then lets its own dependent start.  When the previous kernel on the
+// stream is one of these, the new grid's CTAs are dispatched during the
+// previous grid's last wave and start their loads the moment it completes,
+// instead of after a launch gap.  Waiting before triggering keeps at most
+// one grid waiting ahead: a grid's dependent can start only once every CTA
+// of the grid has passed its own wait.  Triggering first let the small
+// grids of a stream of short calls release grid after grid, which then sat
+// waiting in SM slots.  In graph replay of 8-rank bf16 all-reduces that
+// cost 3.2 against 2.8 us per call at 256 KiB per rank, and 5.2 against
+// 3.3 us at 1 MiB.  Data dependences between calls (an in-place
 // all-reduce reading what the last one wrote) are kept: nothing is touched
 // before the wait returns.  After any other kernel (no early trigger) or a
 // stream operation that is not a kernel, the launch waits in plain stream
 // order.  A kernel that follows one of these without the attribute waits for
 // it to complete, as usual.
 //
-// No wait can deadlock: a grid's dependents start only after all of its
-// CTAs have started, and none of them waits on anything but earlier grids.
+// No wait can deadlock: a grid's dependent starts only after all of its
+// CTAs have started (for pdl_enter kernels, after each has also passed its
+// wait), and no CTA waits on anything but earlier grids.
 // In a launch without the attribute griddepcontrol.wait returns at once.
 #pragma once
 
@@ -47,8 +54,8 @@ __device__ __forceinline__ void pdl_wait_prerequisites() {
 
 // The first statement of every kernel launched with launch_pdl.
 __device__ __forceinline__ void pdl_enter() {
-  pdl_launch_dependents();
   pdl_wait_prerequisites();
+  pdl_launch_dependents();
 }
 
 // Launch `kernel` on `grid` CTAs of `block` threads; `chained` launches it
