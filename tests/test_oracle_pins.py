@@ -201,7 +201,7 @@ def test_fold_columns_detects_rotated_start(n):
     """Negative check: giving each element the chunk of its neighbour (a
     fold that starts one rank later) changes fp32 bits somewhere, and so do
     a reversed rank order and a divide-by-N applied per addend.  So a slip
-    in the checker's (j + k) mod N indexing or in its AVG cannot pass the
+    in the per-element fold's (j + k) mod N indexing or in its AVG cannot pass the
     pin above by accident."""
     count = 64 * n
     L = count // n
