@@ -23,7 +23,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 
 
 @pytest.fixture(scope="module")
-def checker(tmp_path_factory):
+def error_check_bin(tmp_path_factory):
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA device")
     cr.lib()  # fails loudly if the library is missing
@@ -37,8 +37,8 @@ def checker(tmp_path_factory):
     return exe
 
 
-def test_refused_launches_report_cuda_error_and_leave_the_library_usable(checker):
-    res = subprocess.run([checker], capture_output=True, text=True, timeout=300)
+def test_refused_launches_report_cuda_error_and_leave_the_library_usable(error_check_bin):
+    res = subprocess.run([error_check_bin], capture_output=True, text=True, timeout=300)
     out = res.stdout + res.stderr
     assert res.returncode == 0, out[-4000:]
     assert "ALL OK" in out, out[-4000:]

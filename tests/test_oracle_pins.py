@@ -157,7 +157,7 @@ def _columns(bufs, count, n, L, idx):
                                        ("bf16", "avg", "f32"), ("bf16", "sum", "f32"),
                                        ("i32", "sum", "i32")])
 def test_fold_columns_equals_ring_simulation(n, dt, op, out):
-    """The per-element checker used at full size must give, for every
+    """The per-element fold used at full size must give, for every
     sampled element, the bytes the literal ring simulation gives for that
     element: same chunk owner, same starting rank, same association, same
     single AVG division and bf16 rounding.  count is chosen so L = ceil(C/N)
