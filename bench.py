@@ -1324,7 +1324,7 @@ def run_reference(args):
         config["sample"] = smp.desc   # a bounded sample, not the whole workload
     value = smp.nbytes / sec / 1e9
     sample = (f"{smp.desc} per step ({smp.fraction:.3g} of the workload's bytes), "
-              f"single-threaded C oracle (oracle/); host has {os.cpu_count()} cores")
+              f"single-threaded C++ oracle (oracle/); host has {os.cpu_count()} cores")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -1356,7 +1356,7 @@ def cpu_baseline_sampled(args):
             "kind": "oracle",
             "cpu_model": host_cpu_model(),
             "sample": (f"{passes} step(s) of the workload on {smp.desc} "
-                       f"({smp.fraction:.3g} of its bytes), single-threaded C oracle, "
+                       f"({smp.fraction:.3g} of its bytes), single-threaded C++ oracle, "
                        f"{dt:.1f} s; host has {os.cpu_count()} cores")}
 
 
@@ -1524,7 +1524,7 @@ def main(argv=None):
                "sample": (f"{passes} pass(es) of the ring all-reduce AVG over the first "
                           f"{sample[0].size} elements of each of the 8 rank buffers "
                           f"({'all' if frac == 1 else '1/%d' % frac} of the workload's bytes), "
-                          f"single-threaded C oracle, {secs:.1f} s; host has "
+                          f"single-threaded C++ oracle, {secs:.1f} s; host has "
                           f"{os.cpu_count()} cores")}
     elif rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_sampled(args)

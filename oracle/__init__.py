@@ -1,4 +1,4 @@
-"""ctypes bindings to the C oracle (``oracle/*.c``).
+"""ctypes bindings to the C++ oracle (``oracle/*.cpp``).
 
 TEST INFRASTRUCTURE ONLY.  This is the plain, slow, single-threaded CPU
 statement of what the emulated-rank collectives compute; only ``tests/``, the

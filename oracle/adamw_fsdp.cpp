@@ -1,5 +1,5 @@
 /*
- * adamw_fsdp.c -- oracle for the sharded AdamW update and the FSDP step
+ * adamw_fsdp.cpp -- oracle for the sharded AdamW update and the FSDP step
  * (reduce-scatter -> owner AdamW -> bf16 cast -> all-gather).  Test
  * infrastructure only (see oracle.h).
  */

@@ -1,5 +1,5 @@
 /*
- * buckets.c -- oracle for DDP gradient bucketing: the bucket plan and the
+ * buckets.cpp -- oracle for DDP gradient bucketing: the bucket plan and the
  * pack / unpack copies.  Test infrastructure only (see oracle.h).
  *
  * [AIG] 6.2.4: gradients are grouped into buckets (default 25 MB) in the

@@ -1,5 +1,5 @@
 /*
- * collectives.c -- oracle for chunking, ring reduce-scatter / all-gather /
+ * collectives.cpp -- oracle for chunking, ring reduce-scatter / all-gather /
  * all-reduce and naive reduce+broadcast.  Test infrastructure only (see
  * oracle.h).  Written for obviousness, not speed: every rank's buffers and
  * every ring message are materialised.
