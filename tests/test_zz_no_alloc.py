@@ -6,16 +6,19 @@ code that must not trigger a synchronising cudaMalloc) that have no
 workspace to pass.  Called through the C ABI, it must give what
 cr_fsdp_step_clipped gives with a caller workspace, on two calls in a row
 (the second starting from the state the first left, and reusing the static
-array the first call filled).  This file is collected last on purpose.
+array the first call filled), and both calls must equal the oracle's clipped
+step bit for bit at a clip coefficient the oracle's norm allows.  This file
+is collected last on purpose.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle as O
 from fsdp_emulated_ranks_gb300 import build as libbuild
 from fsdp_emulated_ranks_gb300 import cr
 from fsdp_emulated_ranks_gb300 import inputs as I
-from gpu_util import assert_match, to_host
+from gpu_util import assert_clipped_match, assert_match, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -47,6 +50,8 @@ def test_noalloc_matches_workspace_call_twice(n, count, max_norm):
     b_state = make_state(n, count, L)   # static-scratch entry point
     a_norm = torch.empty(1, dtype=torch.float32, device="cuda")
     b_norm = torch.empty(1, dtype=torch.float32, device="cuda")
+    # The oracle's copy of the state, advanced alongside the GPU's.
+    h_state = [[to_host(x, "f32") for x in t] for t in b_state[:3]]
     for step in (1, 2):
         grads = []
         for r in range(n):
@@ -66,6 +71,17 @@ def test_noalloc_matches_workspace_call_twice(n, count, max_norm):
             assert_match(to_host(y, "f32"), to_host(x, "f32"), "f32", f"state, step {step}")
         for x, y in zip(ap, bp):
             assert_match(to_host(y, "bf16"), to_host(x, "bf16"), "bf16", f"params, step {step}")
+        # And against the oracle: the norm to its summation-order tolerance,
+        # everything after the coefficient bitwise.
+        h_grads = [to_host(g, "bf16") for g in grads]
+        ocfg = O.AdamWConfig(step=step)
+        _, want_norm = O.fsdp_step_clipped(h_grads, [x.copy() for x in h_state[0]],
+                                           [x.copy() for x in h_state[1]],
+                                           [x.copy() for x in h_state[2]], ocfg, max_norm)
+        assert float(b_norm.item()) == pytest.approx(want_norm, rel=1e-6)
+        got_state = [[to_host(x, "f32") for x in t] for t in (bm, bmm, bv)]
+        assert_clipped_match(got_state, [to_host(x, "bf16") for x in bp], h_grads, *h_state,
+                             ocfg, max_norm, want_norm, f"step {step}")
 
 
 def test_noalloc_rejects_bad_arguments_before_launch():
