@@ -529,16 +529,16 @@ cr_status cr_fsdp_step_clipped(const void* const* grads_bf16, int nranks,
  * per CTA and at most 4095 CTAs (the array's partial slots) whatever the
  * element count and the GPU, so no call can need more scratch than the
  * array holds and no size is refused on that account; other arguments are
- * checked and refused exactly as cr_fsdp_step_clipped does.  The first call on each device looks up the array's device address
+ * checked and refused exactly as cr_fsdp_step_clipped does.  The first
+ * call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and caches it for that
  * device's current context, keyed on the driver's context ID; a context
  * created later on the device (after cudaDeviceReset, say) gets its own
  * lookup at its first call.  Make each such first call before any stream
- * capture.  All calls
- * share the one array: nothing in it needs to start at zero (the first pass
- * writes every partial the second pass reads), but calls that overlap on
- * the GPU -- on different streams, unordered -- race on it and must be
- * serialised by the caller.  Nothing is allocated. */
+ * capture.  All calls share the one array: nothing in it needs to start at
+ * zero (the first pass writes every partial the second pass reads), but
+ * calls that overlap on the GPU -- on different streams, unordered -- race
+ * on it and must be serialised by the caller.  Nothing is allocated. */
 cr_status cr_fsdp_step_clipped_noalloc(const void* const* grads_bf16,
                                        int nranks, size_t count,
                                        float* const* master, float* const* m,
