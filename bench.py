@@ -869,25 +869,42 @@ def l2_flushed(wl, stream, device, peak, steps=20):
     """The workload's step timed one call at a time with L2 flushed before
     each (a write of twice the 129 MB L2 on the same stream, outside the
     timed events): the median step time, as a cross-check that L2 residency
-    between back-to-back steps does not inflate the headline figure."""
+    between back-to-back steps does not inflate the headline figure.
+
+    The write leaves L2 full of dirty lines, which the timed call then
+    writes back as its own accesses evict them.  "clean" repeats the
+    measurement with an untimed read of the same scratch after the write:
+    that read takes the write-backs, and the call starts from an L2 of
+    clean lines that hold none of its data."""
     import torch
     scratch = torch.empty(2 * (129 << 20), dtype=torch.uint8, device=device)
-    times = []
-    with torch.cuda.stream(stream):
-        for i in range(steps + 3):
-            scratch.fill_(i & 0xff)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            wl.step(stream)
-            e1.record(stream)
-            e1.synchronize()
-            if i >= 3:
-                times.append(e0.elapsed_time(e1))
-    del scratch
-    ms = statistics.median(times)
-    gbs = wl.nbytes / (ms * 1e-3) / 1e9
-    return {"steps": steps, "flush_bytes": 2 * (129 << 20), "ms_median": round(ms, 4),
-            "GB/s": round(gbs, 1), "frac": round(gbs / peak[0], 4)}
+    words = scratch.view(torch.int32)
+
+    def median_ms(clean):
+        times = []
+        with torch.cuda.stream(stream):
+            for i in range(steps + 3):
+                scratch.fill_(i & 0xff)
+                if clean:
+                    words.amax()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                wl.step(stream)
+                e1.record(stream)
+                e1.synchronize()
+                if i >= 3:
+                    times.append(e0.elapsed_time(e1))
+        return statistics.median(times)
+
+    def figures(ms):
+        gbs = wl.nbytes / (ms * 1e-3) / 1e9
+        return {"ms_median": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / peak[0], 4)}
+
+    out = {"steps": steps, "flush_bytes": 2 * (129 << 20), **figures(median_ms(False))}
+    out["clean"] = figures(median_ms(True))
+    del words, scratch
+    return out
 
 
 def run_e2e(args, bufs, n, count, world, stream, device):
@@ -996,16 +1013,24 @@ def run_rows(args, device, stream, peak, skip=None):
             # host-bound: also the same call prepared once (the C call alone)
             from fsdp_emulated_ranks_gb300 import cr
             prep = cr.prepare(wl.step, stream)
-            _, pper = timed(prep, steps, 3, 1, stream)
+            psteps = max(steps, 200)
+            ptot, pper = timed(prep, psteps, 3, 1, stream)
             pms = statistics.median(pper)
             rows[-1].update({"ms_prepared_median": round(pms, 4),
-                             "GB/s_prepared": round(wl.nbytes / (pms * 1e-3) / 1e9, 1)})
+                             "GB/s_prepared": round(wl.nbytes / (pms * 1e-3) / 1e9, 1),
+                             # back to back: the host issues the next call
+                             # while the device runs this one
+                             "ms_prepared": round(ptot / psteps, 4),
+                             "frac_prepared": round(wl.nbytes / (ptot / psteps * 1e-3) / 1e9
+                                                    / peak[0], 4)})
             del prep
             # and captured in a CUDA graph: device time per call, no host work
             gus = graph_replay_us(wl, device, stream)
             rows[-1].update({"graph_us": round(gus, 2),
                              "GB/s_graph": round(wl.nbytes / (gus * 1e-6) / 1e9, 1),
                              "frac_graph": round(wl.nbytes / (gus * 1e-6) / 1e9 / peak[0], 4)})
+            # and one call at a time from cold L2: its inputs come from HBM
+            rows[-1]["l2_flushed"] = l2_flushed(wl, stream, device, peak)
         wl.teardown()
     return rows
 
@@ -1032,7 +1057,8 @@ def rows_summary(head_key, head_roofline, rows, peak):
     """One compact entry per measured row, [ms median, GB/s at the median,
     fraction of the peak at the median, fraction at the mean], keyed by
     workload; host-bound rows add their graph-replay figures
-    [us per call, fraction]."""
+    [us per call, fraction] and their cold-L2 single-call figures
+    [ms median, fraction]."""
     out = {head_key: [head_roofline["ms_median"], head_roofline["achieved_median"],
                       head_roofline["frac_median"], head_roofline["frac"]]}
     for r in rows or []:
@@ -1040,6 +1066,8 @@ def rows_summary(head_key, head_roofline, rows, peak):
         e = [r["ms_median"], round(gbs, 1), round(gbs / peak[0], 4), r["frac"]]
         if "graph_us" in r:
             e += [r["graph_us"], r["frac_graph"]]
+        if "l2_flushed" in r:
+            e += [r["l2_flushed"]["ms_median"], r["l2_flushed"]["frac"]]
         out[r["key"]] = e
     return out
 

@@ -54,6 +54,7 @@ def test_headline_line_has_every_key(tmp_path):
     assert d["clocks"]["sm_mhz"] > 0 and "reasons" in d["clocks"]
     f = d["l2_flushed"]  # the same step with L2 flushed before each call
     assert f["steps"] >= 20 and f["flush_bytes"] > 2 * (128 << 20) and f["GB/s"] > 0
+    assert f["clean"]["ms_median"] > 0   # and with the flush's dirty lines written back first
     assert d["config"]["workload"] == "allreduce_avg_bf16_8ranks_64MiB"
     names = [row["name"] for row in d["rows"]]
     assert "reduce_scatter_avg_bf16_8ranks_64MiB" in names and len(names) >= 10
@@ -63,7 +64,10 @@ def test_headline_line_has_every_key(tmp_path):
     assert list(d)[-1] == "rows_summary"
     assert "allreduce" in summ and len(summ) == 1 + len(d["rows"])
     assert summ["allreduce"][2] == r["frac_median"] and summ["allreduce"][3] == r["frac"]
-    assert "graph_us" in next(row for row in d["rows"] if row["key"] == "allreduce_f32")
+    cfg1 = next(row for row in d["rows"] if row["key"] == "allreduce_f32")
+    assert "graph_us" in cfg1 and cfg1["l2_flushed"]["ms_median"] > 0
+    assert summ["allreduce_f32"][-2:] == [cfg1["l2_flushed"]["ms_median"],
+                                          cfg1["l2_flushed"]["frac"]]
     recs = [json.loads(l) for l in jsonl.read_text().splitlines()]
     assert len(recs) == 1 + len(d["rows"]) and recs[0]["name"] == d["config"]["workload"]
     for k in ("ms_median", "ms_p10", "ms_p90", "algorithmic_bytes", "cpu_baseline"):

@@ -391,16 +391,19 @@ def test_hsdp_2x2_beyond_2_32_elements():
     torch.cuda.empty_cache()
 
 
-def test_fsdp2_transformer_full_sampled():
+@pytest.mark.parametrize("planned", [True, False], ids=["planned", "chained"])
+def test_fsdp2_transformer_full_sampled(planned):
     """The FSDP2 step over the benchmark's transformer (145 parameters,
-    1.27e9 elements, 8 ranks), laid out and called as benchmarked.  Each
+    1.27e9 elements, 8 ranks), laid out and called as benchmarked: one
+    launch over the plan's table, or the pointers in the parameter blocks
+    of three chained launches.  Each
     sampled element's result depends only on its 8 gradients, its state and
     the rank that owns its row (the fold order): grouped by owner, the
     samples are embedded into a small parameter of N rows whose row j is
     owned by rank j, and that is stepped by the oracle."""
     import bench
     n = 8
-    wl = bench.Fsdp2Step()
+    wl = bench.Fsdp2Step(planned=planned)
     wl.setup(torch.device("cuda"))
     rng = np.random.default_rng(7)
     P, I_, J, K = [], [], [], []
