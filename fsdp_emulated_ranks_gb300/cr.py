@@ -10,6 +10,7 @@ from __future__ import annotations
 
 import ctypes as C
 import os
+import struct
 import threading
 from typing import Sequence
 
@@ -183,23 +184,25 @@ def _ptr(x) -> int:
     return x.data_ptr()
 
 
-_VP_ARRAY = {}  # length -> ctypes array type of void pointers
+_PACK = {}  # length -> struct packer of that many native 64-bit pointers
 
 
 def _ptr_array(xs: Sequence):
-    """Host array of device pointers for a call.  Long tables (the bucket
-    and FSDP2 calls pass thousands) are built through numpy, 3x faster than
-    ctypes element by element; the returned pointer keeps the array alive
-    for the duration of the call."""
-    ptrs = [x if type(x) is int else _ptr(x) for x in xs]
-    if len(ptrs) > 64:
-        import numpy as np
-        return np.array(ptrs, dtype=np.uint64).ctypes.data_as(C.c_void_p)
-    n = max(1, len(ptrs))
-    t = _VP_ARRAY.get(n)
-    if t is None:
-        t = _VP_ARRAY[n] = C.c_void_p * n
-    return t(*ptrs)
+    """Host array of device pointers for a call, as a bytes object of native
+    64-bit words: ctypes passes a bytes argument to a void* parameter as the
+    address of its buffer, which lives until the call returns (the library
+    copies the table before returning).  Packing with struct is about three
+    times faster than filling a ctypes array element by element, which
+    matters for short calls whose host cost is the call itself.  An empty
+    list still yields a valid (one zero entry) table."""
+    ptrs = [x if type(x) is int else (0 if x is None else x.data_ptr()) for x in xs]
+    n = len(ptrs)
+    if n == 0:
+        ptrs, n = [0], 1
+    pack = _PACK.get(n)
+    if pack is None:
+        pack = _PACK[n] = struct.Struct(f"={n}Q").pack
+    return pack(*ptrs)
 
 
 def _dtype(d) -> int:
