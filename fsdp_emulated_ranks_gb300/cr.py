@@ -80,14 +80,17 @@ class BucketPlanT(C.Structure):
 
 
 _tls = threading.local()  # .recorder: set while prepare() runs a wrapper
+_recording = 0            # threads inside prepare(); lib() skips _tls while 0
+_recording_lock = threading.Lock()
 
 
 def lib() -> C.CDLL:
     """Open libcr.so (built by fsdp_emulated_ranks_gb300.build)."""
     global _lib
-    rec = getattr(_tls, "recorder", None)
-    if rec is not None:
-        return rec
+    if _recording:
+        rec = getattr(_tls, "recorder", None)
+        if rec is not None:
+            return rec
     if _lib is not None:
         return _lib
     if not os.path.exists(LIB_PATH):
@@ -714,14 +717,19 @@ def prepare(wrapper, *args, **kwargs) -> Prepared:
     invocation, so advancing cfg.step between invocations takes effect.
     The prepared call holds references to the arguments, so the tensors and
     the bucket plan it addresses stay allocated while it exists."""
+    global _recording
     if getattr(_tls, "recorder", None) is not None:
         raise RuntimeError("prepare() cannot be nested")
     rec = _Recorder(lib())
+    with _recording_lock:
+        _recording += 1
     _tls.recorder = rec
     try:
         wrapper(*args, **kwargs)
     finally:
         _tls.recorder = None
+        with _recording_lock:
+            _recording -= 1
     name = getattr(wrapper, "__name__", "call")
     if not rec.calls:
         raise ValueError(f"{name} launches nothing that prepare() could record")
