@@ -656,8 +656,9 @@ _PREPARABLE = frozenset([
     "cr_all_reduce_wire", "cr_hsdp_reduce_scatter", "cr_all_reduce_host",
     "cr_all_reduce_staged", "cr_bucket_pack", "cr_bucket_unpack", "cr_bucket_all_reduce",
     "cr_bucket_all_reduce_fused", "cr_fsdp_step", "cr_fsdp_step_clipped",
-    "cr_fsdp_step_clipped_noalloc", "cr_fsdp2_step", "cr_accumulate",
-    "cr_all_reduce_accumulate", "cr_adamw_step"])
+    "cr_fsdp_step_clipped_noalloc", "cr_fsdp2_step", "cr_fsdp2_plan_upload",
+    "cr_fsdp2_step_planned", "cr_all_reduce_range", "cr_reduce_scatter_range",
+    "cr_fsdp_step_range", "cr_accumulate", "cr_all_reduce_accumulate", "cr_adamw_step"])
 # Functions without side effects that a wrapper may call while it marshals.
 _PURE = frozenset(["cr_last_error", "cr_status_string", "cr_chunk_len", "cr_version",
                    "cr_fsdp_clip_workspace_bytes"])

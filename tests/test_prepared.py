@@ -28,3 +28,21 @@ def test_prepare_is_not_reentrant_and_leaves_the_library_usable():
     with pytest.raises(RuntimeError, match="nested"):
         cr.prepare(lambda: (nested(), cr.cr_all_reduce([], 16, "bf16", "avg", [], "bf16", 0)))
     assert cr.cr_chunk_len(10, 4) == 3
+
+
+def test_every_stream_entry_point_is_preparable_unless_it_keeps_host_state():
+    """Every entry point of the C ABI that enqueues work on a stream can be
+    prepared, except those whose host-side state a replay would corrupt:
+    the reducer's and communicator's, which track calls between invocations,
+    and the checked build's self-test."""
+    import os
+    import re
+    header = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                          "include", "cr.h")
+    decls = re.findall(r"\bcr_status\s+(cr_\w+)\s*\(([^;]*?)\);", open(header).read(), re.S)
+    streamed = {name for name, params in decls if "cr_stream_t" in params}
+    stateful = {"cr_reducer_create", "cr_reducer_mark_ready", "cr_reducer_finalize",
+                "cr_comm_create", "cr_check_selftest"}
+    assert len(streamed) > 20
+    assert sorted(streamed - stateful - cr._PREPARABLE) == []
+    assert not (stateful & cr._PREPARABLE)
