@@ -661,7 +661,8 @@ _PREPARABLE = frozenset([
     "cr_fsdp_step_range", "cr_accumulate", "cr_all_reduce_accumulate", "cr_adamw_step"])
 # Functions without side effects that a wrapper may call while it marshals.
 _PURE = frozenset(["cr_last_error", "cr_status_string", "cr_chunk_len", "cr_version",
-                   "cr_fsdp_clip_workspace_bytes"])
+                   "cr_fsdp_clip_workspace_bytes", "cr_shard_range", "cr_slab_range",
+                   "cr_comm_elems", "cr_fsdp2_plan_table_bytes"])
 
 
 class _Recorder:

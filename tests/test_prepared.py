@@ -46,3 +46,16 @@ def test_every_stream_entry_point_is_preparable_unless_it_keeps_host_state():
     assert len(streamed) > 20
     assert sorted(streamed - stateful - cr._PREPARABLE) == []
     assert not (stateful & cr._PREPARABLE)
+
+
+def test_a_prepared_slab_split_may_compute_its_slabs_while_recording():
+    # host-only helpers run for real while prepare() records; the range calls
+    # are recorded (and rejected at invocation: no ranks, no pointers)
+    def split():
+        for g in range(3):
+            lo, hi = cr.cr_slab_range(1000, 4, 3, g)
+            cr.cr_all_reduce_range([], 1000, lo, hi, "bf16", "avg", [], "bf16", 0)
+    p = cr.prepare(split)
+    assert len(p._calls) == 3 and {c[0] for c in p._calls} == {"cr_all_reduce_range"}
+    with pytest.raises(cr.CRError, match="INVALID_ARG"):
+        p()
