@@ -261,3 +261,74 @@ def test_fuzz_range_forms(case):
     for j, ((a, k), g) in enumerate(zip(parts, sh)):
         g.check()
         assert_match(g.host(), rs[j][a:a + k], out, f"RS range n={n} shard {j}")
+
+
+@pytest.mark.parametrize("case", range(30))
+def test_fuzz_fsdp2(case):
+    """FSDP2 over a random parameter set -- dim0 from 0 to a few times N
+    (uneven, empty and one-row shards), rows of 1 to 200 elements -- with
+    every grad, param and state buffer at its own offset, so parameters mix
+    the vector and the element-wise paths in one launch.  Half the cases
+    step through a plan's table (one plan, two steps), half pass the
+    pointers per call; both must equal the oracle bitwise at t = 1 and 2."""
+    rng = np.random.default_rng(11000 + case)
+    n = int(rng.integers(1, 11))
+    P = int(rng.integers(1, 13))
+    shapes = []
+    for _ in range(P):
+        d0 = int(rng.choice([0, 1, max(1, n - 1), n, 2 * n + 1, int(rng.integers(1, 4 * n + 8))]))
+        row = int(rng.choice([1, 3, 8, 16, 64, 100, int(rng.integers(1, 201))]))
+        shapes.append((d0, row))
+    planned = bool(rng.random() < 0.5)
+    cfgs = [O.AdamWConfig(step=1), O.AdamWConfig(step=2)]
+    master, m, v = [], [], []
+    for p, (d0, row) in enumerate(shapes):
+        Lr = -(-d0 // n) if d0 else 0
+        ks = [max(0, min(d0, (j + 1) * Lr) - min(d0, j * Lr)) * row for j in range(n)]
+        master.append([I.np_normal_f32(k, 0.02, 100 * case + 10 * p + j) for j, k in enumerate(ks)])
+        m.append([np.zeros(k, np.float32) for k in ks])
+        v.append([np.zeros(k, np.float32) for k in ks])
+    d_state = [[Guarded(x.size, "f32", o) if x.size else None
+                for x, o in zip([x for row in t for x in row], offs(rng, P * n, "f32"))]
+               for t in (master, m, v)]
+    for dd, t in zip(d_state, (master, m, v)):
+        for gg, x in zip(dd, [x for row in t for x in row]):
+            if gg is not None:
+                gg.view.copy_(to_dev(x, "f32"))
+    ptrs = [[gg.ptr() if gg is not None else 0 for gg in dd] for dd in d_state]
+    d_p = [Guarded(d0 * row, "bf16", o) if d0 * row else None
+           for (d0, row) in shapes for o in offs(rng, n, "bf16")]
+    p_ptrs = [gg.ptr() if gg is not None else 0 for gg in d_p]
+    # the gradient buffers stay put across the two steps: refilled in place
+    g_off = offs(rng, P * n, "bf16")
+    d_g = [Guarded(d0 * row, "bf16", o) if d0 * row else None
+           for (d0, row), o in zip([s for s in shapes for _ in range(n)], g_off)]
+    g_ptrs = [gg.ptr() if gg is not None else 0 for gg in d_g]
+    plan = table = None
+    if planned:
+        plan = cr.cr_fsdp2_plan_create(shapes, n, g_ptrs, *ptrs, p_ptrs)
+        table = torch.empty(max(16, plan.table_bytes), dtype=torch.uint8, device="cuda")
+        cr.cr_fsdp2_plan_upload(plan, table)
+    for step, cfg in ((1, cfgs[0]), (2, cfgs[1])):
+        grads = [[I.np_to_bf16_bits(I.np_normal_f32(d0 * row, 1e-3, 7000 * step + 50 * case
+                                                    + 7 * p + r)) for r in range(n)]
+                 for p, (d0, row) in enumerate(shapes)]
+        for gg, x in zip(d_g, [x for row in grads for x in row]):
+            if gg is not None:
+                gg.view.copy_(to_dev(x, "bf16"))
+        want_p = O.fsdp2_step(shapes, grads, master, m, v, cfg)
+        if planned:
+            cr.cr_fsdp2_step_planned(plan, table, cr.adamw_cfg(step=step))
+        else:
+            cr.cr_fsdp2_step(shapes, n, g_ptrs, *ptrs, cr.adamw_cfg(step=step), p_ptrs)
+        torch.cuda.synchronize()
+        what = f"n={n} shapes={shapes} planned={planned} step {step}"
+        for dd, t, name in zip(d_state, (master, m, v), ("master", "m", "v")):
+            for gg, x in zip(dd, [x for row in t for x in row]):
+                if gg is not None:
+                    gg.check()
+                    assert_match(gg.host(), x, "f32", f"{name}: {what}")
+        for q, gg in enumerate(d_p):
+            if gg is not None:
+                gg.check()
+                assert_match(gg.host(), want_p[q // n][q % n], "bf16", f"params[{q}]: {what}")
