@@ -332,3 +332,52 @@ def test_fuzz_fsdp2(case):
             if gg is not None:
                 gg.check()
                 assert_match(gg.host(), want_p[q // n][q % n], "bf16", f"params[{q}]: {what}")
+
+
+@pytest.mark.parametrize("case", range(30))
+def test_fuzz_fsdp_step_range(case):
+    """The FSDP step over a random slab [lo, hi) of a random workload, every
+    slab buffer and shard part at its own offset: the slab's elements of
+    the oracle's whole step (state and params), bit for bit, with canaries
+    intact."""
+    rng = np.random.default_rng(13000 + case)
+    n = int(rng.integers(1, 11))
+    count = max(1, draw_count(rng, n))
+    lo = int(rng.integers(0, count + 1))
+    hi = int(rng.integers(lo, count + 1))
+    L = O.chunk_len(count, n)
+    grads = I.host_rank_buffers(n, count, "bf16", std=1e-3, seed0=600 + case)
+    bounds = [O.chunk_bounds(count, n, j) for j in range(n)]
+    master = [I.np_normal_f32(b - a, 0.02, 700 + case + j) for j, (a, b) in enumerate(bounds)]
+    m = [np.zeros(b - a, np.float32) for a, b in bounds]
+    v = [np.zeros(b - a, np.float32) for a, b in bounds]
+    parts = []  # (first shard element in the slab, elements) per shard
+    for j in range(n):
+        a, b = max(lo, j * L), min(hi, (j + 1) * L, count)
+        parts.append((a - j * L, max(0, b - a)))
+    d_state = []
+    for t in (master, m, v):
+        row = []
+        for (a, k), x, o in zip(parts, t, offs(rng, n, "f32")):
+            g = Guarded(k, "f32", o) if k else None
+            if g is not None:
+                g.view.copy_(to_dev(np.ascontiguousarray(x[a:a + k]), "f32"))
+            row.append(g)
+        d_state.append(row)
+    d_g = [to_dev(np.ascontiguousarray(x[lo:hi]), "bf16", o) if hi > lo else 0
+           for x, o in zip(grads, offs(rng, n, "bf16"))]
+    d_p = [Guarded(hi - lo, "bf16", o) for o in offs(rng, n, "bf16")]
+    want_p = O.fsdp_step(grads, master, m, v, O.AdamWConfig())
+    cr.cr_fsdp_step_range(d_g, count, lo, hi,
+                          *[[g.ptr() if g is not None else 0 for g in row] for row in d_state],
+                          cr.adamw_cfg(), [g.ptr() for g in d_p])
+    torch.cuda.synchronize()
+    what = f"n={n} [{lo},{hi}) of {count}"
+    for row, t, name in zip(d_state, (master, m, v), ("master", "m", "v")):
+        for j, (g, (a, k)) in enumerate(zip(row, parts)):
+            if g is not None:
+                g.check()
+                assert_match(g.host(), t[j][a:a + k], "f32", f"{name}[{j}] {what}")
+    for r in range(n):
+        d_p[r].check()
+        assert_match(d_p[r].host(), want_p[r][lo:hi], "bf16", f"params[{r}] {what}")
