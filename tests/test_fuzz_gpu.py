@@ -381,3 +381,50 @@ def test_fuzz_fsdp_step_range(case):
     for r in range(n):
         d_p[r].check()
         assert_match(d_p[r].host(), want_p[r][lo:hi], "bf16", f"params[{r}] {what}")
+
+
+@pytest.mark.parametrize("case", range(30))
+def test_fuzz_bucket_pack_all_reduce_unpack(case):
+    """The unfused DDP pipeline -- pack, per-bucket all-reduce, unpack --
+    over a random plan, with every tensor and every bucket at its own
+    offset (the copies then take the funnel-shift and element paths as well
+    as the vector one): the buckets after pack equal the oracle's pack bit
+    for bit, and the tensors after unpack the oracle's bucketed all-reduce,
+    with canaries intact."""
+    rng = np.random.default_rng(15000 + case)
+    n = int(rng.integers(1, 9))
+    dt = ["bf16", "f32", "i32"][int(rng.integers(3))]
+    op = "sum" if dt == "i32" else ["sum", "avg"][int(rng.integers(2))]
+    es = 2 if dt == "bf16" else 4
+    T = int(rng.integers(1, 31))
+    numels = [int(x) if rng.random() > 0.1 else 0 for x in rng.integers(1, 3000, T)]
+    cap = int(rng.integers(64, 20000))
+    plan = cr.cr_bucket_plan(numels, es, cap)
+    oplan = O.bucket_plan(numels, es, cap)
+    B = plan.nbuckets
+    assert list(plan.bucket_numel) == [int(x) for x in oplan.bucket_numel]
+    host = [[host_inputs(1, k, dt, seed=case * 1000 + r * 50 + t)[0] for t, k in enumerate(numels)]
+            for r in range(n)]
+    ot = offs(rng, n * T, dt)
+    dev_t = [to_dev(host[r][t], dt, ot[r * T + t]) if numels[t] else 0
+             for r in range(n) for t in range(T)]
+    d_b = [Guarded(int(k), dt, o) for _ in range(n)
+           for k, o in zip(plan.bucket_numel, offs(rng, B, dt))]
+    cr.cr_bucket_pack(plan, n, dev_t, [g.ptr() for g in d_b])
+    torch.cuda.synchronize()
+    want_b = O.bucket_pack(oplan, host)
+    what = f"n={n} {dt} T={T} cap={cap}"
+    for r in range(n):
+        for b in range(B):
+            d_b[r * B + b].check()
+            assert_match(d_b[r * B + b].host(), want_b[r][b], dt, f"pack r={r} b={b} {what}")
+    cr.cr_bucket_all_reduce(plan, n, [g.ptr() for g in d_b], dt, op)
+    d_out = [Guarded(k, dt, o) for _ in range(n) for k, o in zip(numels, offs(rng, T, dt))]
+    cr.cr_bucket_unpack(plan, n, [g.ptr() for g in d_b], [g.ptr() for g in d_out])
+    torch.cuda.synchronize()
+    want = O.bucketed_all_reduce(oplan, host, dt, op)
+    for r in range(n):
+        for t in range(T):
+            g = d_out[r * T + t]
+            g.check()
+            assert_match(g.host(), want[r][t], dt, f"unpack r={r} t={t} {what}")
