@@ -265,3 +265,69 @@ def test_fsdp_step_split_into_slabs_large(G):
                     assert torch.equal(st[q][j], full[a:b]), (q, j, lo, hi)
     del grads, params, own
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("k", [33, 41, 60])
+@pytest.mark.parametrize("n", [3, 8, 64])
+def test_range_forms_at_counts_no_buffer_could_hold(k, n):
+    """The range calls take slab-local buffers, so a slab of a buffer of
+    2^k + 12345 elements per rank (k up to 60) needs only the slab's memory.
+    That runs the index arithmetic of the kernels -- the chunk of an element
+    (a 64-bit division), its offset inside its shard, the byte offsets from
+    the shifted-back pointers -- at element indices far beyond 2^32: a slab
+    across the boundary between chunks n/2 - 1 and n/2 and a slab at the
+    end of the last chunk.  All-reduce, reduce-scatter (bf16 in, fp32
+    shards) and the FSDP step against the oracle, bit for bit."""
+    count = (1 << k) + 12345
+    L = O.chunk_len(count, n)
+    cfg = O.AdamWConfig()
+    for lo, hi in ((n // 2 * L - 37, n // 2 * L + 203), (count - 150, count)):
+        m = hi - lo
+        e = np.arange(m, dtype=object) + lo
+        chunk = np.array([int(x // L) for x in e], np.int32)
+        host = I.host_rank_buffers(n, m, "bf16", std=0.02, seed0=k * 100 + n)
+        vals = np.stack(host, axis=1)
+        what = f"count=2^{k}+12345 n={n} [{lo}, {hi})"
+        # all-reduce AVG in place
+        bufs = [to_dev(x, "bf16") for x in host]
+        cr.cr_all_reduce_range(bufs, count, lo, hi, "bf16", "avg", bufs, "bf16")
+        torch.cuda.synchronize()
+        want = O.fold_columns(vals, chunk, "bf16", "avg", "bf16")
+        for r in range(n):
+            assert_match(to_host(bufs[r], "bf16"), want, "bf16", f"all-reduce rank {r}, {what}")
+        # reduce-scatter to fp32 shard parts
+        bufs = [to_dev(x, "bf16") for x in host]
+        parts = [shard_part(count, n, j, lo, hi) for j in range(n)]
+        outs = [torch.full((max(1, ln),), -1.0, dtype=torch.float32, device="cuda")
+                for _, ln in parts]
+        cr.cr_reduce_scatter_range(bufs, count, lo, hi, "bf16", "avg",
+                                   [o if ln else 0 for o, (_, ln) in zip(outs, parts)], "f32")
+        torch.cuda.synchronize()
+        gavg = O.fold_columns(vals, chunk, "bf16", "avg", "f32")
+        for j, ((a, ln), o) in enumerate(zip(parts, outs)):
+            if ln:
+                first = j * L + a - lo  # the part's first element, slab-local
+                assert_match(to_host(o[:ln], "f32"), gavg[first:first + ln], "f32",
+                             f"shard {j}, {what}")
+        # the FSDP step: state parts per owner, params slab per rank
+        p0 = I.np_normal_f32(m, 0.02, k * 10 + n)
+        pm, mm, vm = p0.copy(), np.zeros(m, np.float32), np.zeros(m, np.float32)
+        O.adamw(pm, mm, vm, gavg.copy(), cfg)
+        st = {name: [] for name in ("master", "m", "v")}
+        for j, (a, ln) in enumerate(parts):
+            first = j * L + a - lo
+            for name, x in (("master", p0), ("m", np.zeros(m, np.float32)),
+                            ("v", np.zeros(m, np.float32))):
+                st[name].append(to_dev(np.ascontiguousarray(x[first:first + ln]), "f32")
+                                if ln else 0)
+        grads = [to_dev(x, "bf16") for x in host]
+        params = [torch.empty(m, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+        cr.cr_fsdp_step_range(grads, count, lo, hi, st["master"], st["m"], st["v"],
+                              cr.adamw_cfg(), params)
+        torch.cuda.synchronize()
+        for name, ref in (("master", pm), ("m", mm), ("v", vm)):
+            got = np.concatenate([to_host(t, "f32") for t in st[name] if isinstance(t, torch.Tensor)])
+            assert_match(got, ref, "f32", f"FSDP {name}, {what}")
+        for r in range(n):
+            assert_match(to_host(params[r], "bf16"), O.f32_to_bf16(pm), "bf16",
+                         f"FSDP params rank {r}, {what}")
