@@ -557,7 +557,7 @@ def fsdp2_host(shapes, n, seed):
     return grads, master, m, v
 
 
-@pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 16, 33, 64])
 @pytest.mark.parametrize("offset", [0, "16B", 1])
 def test_fsdp2_step_two_steps(n, offset):
     shapes = FSDP2_SHAPES
@@ -592,7 +592,7 @@ def test_fsdp2_step_two_steps(n, offset):
                 assert_match(gp[p][r].host(), want[p][r], "bf16", f"param {p} rank {r} step {step}")
 
 
-@pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 16, 33, 64])
 @pytest.mark.parametrize("offset", [0, "16B", 1])
 def test_fsdp2_step_planned_two_steps(n, offset):
     """cr_fsdp2_step_planned: the plan made and its table uploaded once,
