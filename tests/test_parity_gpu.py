@@ -188,7 +188,7 @@ def fsdp_case(n, count, seed):
     return grads, master, m, v
 
 
-@pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 16, 33, 64])
 @pytest.mark.parametrize("count_fn", [lambda n: 8 * n * 40, lambda n: 8 * n * 40 + 5, lambda n: 1,
                                       lambda n: 100])
 @pytest.mark.parametrize("offset", [0, 1, "16B"])
@@ -255,7 +255,7 @@ def bucket_case(n, numels, esize, cap, seed, bucket_offset):
     return plan, oplan, dt, host_t
 
 
-@pytest.mark.parametrize("n", [1, 2, 8])
+@pytest.mark.parametrize("n", [1, 2, 8, 64])
 @pytest.mark.parametrize("esize", [2, 4])
 @pytest.mark.parametrize("tensor_offset,bucket_offset", [(0, 0), (1, 0), (0, 1), (1, 3)])
 def test_bucket_pack_unpack_all_reduce(n, esize, tensor_offset, bucket_offset):
@@ -400,7 +400,7 @@ def test_bucket_all_reduce_fused(n, dt, op, offset):
 
 # ---- FSDP step with gradient-norm clipping ----------------------------------------
 
-@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 8, 16])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 8, 16, 33, 64])
 @pytest.mark.parametrize("count_fn", [lambda n: 8 * n * 40, lambda n: 8 * n * 40 + 5,
                                       lambda n: 8 * n * 40 - 3, lambda n: 3])
 @pytest.mark.parametrize("clip", ["active", "inactive"])
@@ -674,7 +674,7 @@ def test_fsdp2_planned_equals_chained_launches(n):
 
 # ---- gradient accumulation (no_sync) ---------------------------------------------
 
-@pytest.mark.parametrize("n", [1, 2, 3, 8, 16])
+@pytest.mark.parametrize("n", [1, 2, 3, 8, 16, 64])
 @pytest.mark.parametrize("gdt", ["bf16", "f32"])
 @pytest.mark.parametrize("offset", [0, "16B", 1])
 @pytest.mark.parametrize("op", ["avg", "sum"])
