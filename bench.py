@@ -1393,7 +1393,8 @@ def cpu_baseline_sampled(args):
 def run_sweep(args, device, stream, peak):
     """All-reduce AVG bf16: N = 8 over 1 KiB .. 1 GiB per rank (powers of 4)
     and N in {2,4,8,16,32,64} at 256 MiB per rank; fits T = a + bytes / B to
-    the 8-rank points and reports the crossover S* = a * B."""
+    the 8-rank points and reports the crossover S* = a * B.  Then the FSDP
+    step over the same rank counts (fsdp_rank_sweep)."""
     import torch
     from fsdp_emulated_ranks_gb300 import cr
     pts = []
@@ -1443,7 +1444,31 @@ def run_sweep(args, device, stream, peak):
     g8 = [p["graph_us"] for p in out if p["n"] == 8 and "graph_us" in p]
     return {"points": out, "alpha_us": round(a * 1e6, 3), "bw_GBs": round(bw / 1e9, 1),
             "crossover_bytes": round(a * bw),
-            "graph_latency_us_min": min(g8) if g8 else None}
+            "graph_latency_us_min": min(g8) if g8 else None,
+            "fsdp_ranks": fsdp_rank_sweep(device, stream, peak)}
+
+
+def fsdp_rank_sweep(device, stream, peak):
+    """The FSDP step, plain and clipped, at N in {2,4,8,16,32,64}: 2, 4 and
+    8 ranks run the kernels built for that rank count, the others the
+    runtime-N ones.  Parameters per step: 1.3e9 up to 4 ranks, then 2^33 / N
+    (every point holds 26-47 GB on the device)."""
+    import torch
+    out = []
+    for clip in (False, True):
+        for n in (2, 4, 8, 16, 32, 64):
+            count = min((1 << 33) // n, 1_300_000_000)
+            wl = FsdpStep(n=n, count=count, clip=clip)
+            wl.setup(device)
+            total, per = timed(lambda: wl.step(stream), 10, 3, 1, stream)
+            ms = total / 10
+            gbs = wl.nbytes / (ms * 1e-3) / 1e9
+            out.append({"n": n, "clipped": clip, "params": count, "ms": round(ms, 3),
+                        "GB/s": round(gbs, 1), "frac": round(gbs / peak[0], 4),
+                        "ms_median": round(statistics.median(per), 3)})
+            wl.teardown()
+            torch.cuda.empty_cache()
+    return out
 
 
 # ---- main ---------------------------------------------------------------------------------
