@@ -1445,7 +1445,56 @@ def run_sweep(args, device, stream, peak):
     return {"points": out, "alpha_us": round(a * 1e6, 3), "bw_GBs": round(bw / 1e9, 1),
             "crossover_bytes": round(a * bw),
             "graph_latency_us_min": min(g8) if g8 else None,
-            "fsdp_ranks": fsdp_rank_sweep(device, stream, peak)}
+            "fsdp_ranks": fsdp_rank_sweep(device, stream, peak),
+            "uneven": uneven_sweep(device, stream, peak)}
+
+
+def uneven_sweep(device, stream, peak):
+    """Shard lengths on and off the vector grid.  The reduce-scatter (bf16
+    AVG) and the FSDP step at N = 3, 5 and 8, each once with a count whose
+    chunk length L is a multiple of 16 and once with an odd L; and the HSDP
+    reduce-scatter (bf16 AVG, 64 MiB per rank) over mesh shapes beyond the
+    ones built for a fixed shape."""
+    import torch
+    from fsdp_emulated_ranks_gb300 import cr
+    out = []
+
+    def add(kind, n, count, ms, nbytes, chunks=None, **kw):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out.append({"op": kind, "n": n, "count": count,
+                    "L": cr.cr_chunk_len(count, chunks or n), **kw,
+                    "ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / peak[0], 4)})
+
+    for n in (3, 5, 8):
+        for count in (n << 22, (n << 22) + n):   # L = 2^22, then 2^22 + 1
+            bufs = alloc_ranks(n, count, torch.bfloat16, 0.02, 0, device)
+            L = cr.cr_chunk_len(count, n)
+            shards = [torch.empty(L, dtype=torch.bfloat16, device=device) for _ in range(n)]
+            total, _ = timed(lambda: cr.cr_reduce_scatter(bufs, count, "bf16", "avg", shards, "bf16",
+                                                          stream), 20, 3, 1, stream)
+            add("reduce_scatter", n, count, total / 20, (n + 1) * count * 2)
+            del bufs, shards
+            torch.cuda.empty_cache()
+    for n in (3, 5, 8):
+        for count in (n << 24, (n << 24) + n):
+            wl = FsdpStep(n=n, count=count)
+            wl.setup(device)
+            total, _ = timed(lambda: wl.step(stream), 10, 3, 1, stream)
+            add("fsdp_step", n, count, total / 10, wl.nbytes)
+            wl.teardown()
+            torch.cuda.empty_cache()
+    count = 1 << 25
+    for R, S in ((2, 4), (4, 4), (8, 8), (8, 2), (3, 5)):
+        n = R * S
+        bufs = alloc_ranks(n, count, torch.bfloat16, 0.02, 0, device)
+        L = cr.cr_chunk_len(count, S)
+        shards = [torch.empty(L, dtype=torch.bfloat16, device=device) for _ in range(n)]
+        total, _ = timed(lambda: cr.cr_hsdp_reduce_scatter(bufs, R, S, count, "bf16", "avg", shards,
+                                                           "bf16", stream), 20, 3, 1, stream)
+        add("hsdp", n, count, total / 20, (n + R) * count * 2, chunks=S, mesh=f"{R}x{S}")
+        del bufs, shards
+        torch.cuda.empty_cache()
+    return out
 
 
 def fsdp_rank_sweep(device, stream, peak):

@@ -108,7 +108,7 @@ cr_status reduce_scatter_impl(const void* const* bufs, int nranks, size_t count,
   const size_t is = esize_of(in_dtype), os = esize_of(out_dtype);
   const uint64_t L = cr_chunk_len(count, nranks);
   std::vector<Span> spans;
-  Width vw;
+  Width vw, vin;  // every buffer and L; the inputs alone
   vw.bytes(L * is);
   vw.bytes(L * os);
   for (int r = 0; r < nranks; ++r) {
@@ -118,6 +118,7 @@ cr_status reduce_scatter_impl(const void* const* bufs, int nranks, size_t count,
     if (count) {
       spans.push_back(span_of(bufs[r], count * is, 0, r));
       vw.ptr(bufs[r]);
+      vin.ptr(bufs[r]);
     }
     if (len) {
       spans.push_back(span_of(out_shards[r], len * os, 1, r));
@@ -147,7 +148,14 @@ cr_status reduce_scatter_impl(const void* const* bufs, int nranks, size_t count,
   a.avg = op == CR_AVG;
   a.inv_n = exact_inv_n(nranks);
   a.wire_bf16 = wire_bf16 ? 1 : 0;
-  cudaError_t e = launch_fold(in_dtype, out_dtype, kRS, a, vw.get(), stream);
+  // Shards off the vector grid (L or a shard pointer): vector loads, element
+  // stores, rather than element loads too.
+  int w = vw.get();
+  if (w == 0 && vin.get() != 0) {
+    w = vin.get();
+    a.out_scalar = 1;
+  }
+  cudaError_t e = launch_fold(in_dtype, out_dtype, kRS, a, w, stream);
   if (e != cudaSuccess) return cuda_fail(e, "reduce_scatter launch");
   return ok();
 }
@@ -186,7 +194,7 @@ cr_status cr_hsdp_reduce_scatter(const void* const* bufs, int R, int S, size_t c
   const size_t is = esize_of(in_dtype), os = esize_of(out_dtype);
   const uint64_t L = cr_chunk_len(count, S);
   std::vector<Span> spans;
-  Width vw;
+  Width vw, vin;  // every buffer and L; the inputs alone
   vw.bytes(L * is);
   vw.bytes(L * os);
   for (int r = 0; r < n; ++r) {
@@ -196,6 +204,7 @@ cr_status cr_hsdp_reduce_scatter(const void* const* bufs, int R, int S, size_t c
     if (count) {
       spans.push_back(span_of(bufs[r], count * is, 0, r));
       vw.ptr(bufs[r]);
+      vin.ptr(bufs[r]);
     }
     if (len) {
       spans.push_back(span_of(out_shards[r], len * os, 1, r));
@@ -228,7 +237,12 @@ cr_status cr_hsdp_reduce_scatter(const void* const* bufs, int R, int S, size_t c
   a.S = S;
   a.avg = op == CR_AVG;
   a.inv_n = exact_inv_n(n);
-  cudaError_t e = launch_hsdp(in_dtype, out_dtype, a, vw.get(), (cudaStream_t)stream);
+  int w = vw.get();
+  if (w == 0 && vin.get() != 0) {  // shards off the vector grid: element stores
+    w = vin.get();
+    a.out_scalar = 1;
+  }
+  cudaError_t e = launch_hsdp(in_dtype, out_dtype, a, w, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "hsdp_reduce_scatter launch");
   return ok();
 }

@@ -229,7 +229,8 @@ cr_status cr_bucket_all_reduce(const cr_bucket_plan_t* plan, int nranks,
       if ((st = check_buf(p, plan->bucket_numel[b], es, "buckets", r * B + b))) return st;
       if (plan->bucket_numel[b]) spans.push_back(span_of(p, plan->bucket_numel[b] * es, 1, r * B + b));
     }
-  if ((st = check_disjoint(spans))) return st;
+  st = check_disjoint(spans);
+  if (st) return st;
   return fused_run(B, nranks, dtype, op, (cudaStream_t)stream,
                    [&](int b, uint64_t* numel, uint64_t* off, uint64_t* bnumel, void** ptrs) {
                      *numel = plan->bucket_numel[b];

@@ -34,8 +34,10 @@ cr_status fsdp_prepare(const void* const* grads_bf16, int nranks, size_t count,
   const uint64_t L = cr_chunk_len(count, nranks);
   const uint64_t nslab = end - begin;
   // Vector path: 16-byte bf16 grads/params and 16- (or 32-) byte fp32
-  // state vectors of 8 elements, which needs L % 8 == 0.
-  Width gw, sw;
+  // state vectors of 8 elements, which needs L % 8 == 0.  With L (or a
+  // state pointer) off that grid, the grads/params still move as vectors
+  // and the state element by element (vw = 1).
+  Width gw, sw, gp;
   gw.bytes(L * 2);
   sw.bytes(L * 4);
   memset(&a, 0, sizeof(a));
@@ -62,6 +64,8 @@ cr_status fsdp_prepare(const void* const* grads_bf16, int nranks, size_t count,
       spans.push_back(span_of(params_bf16[r], nslab * 2, 1, r));
       gw.ptr(a.grads[r]);
       gw.ptr(a.params[r]);
+      gp.ptr(a.grads[r]);
+      gp.ptr(a.params[r]);
     }
     if (len) {
       spans.push_back(span_of(master[r], len * 4, 1, r));
@@ -72,7 +76,7 @@ cr_status fsdp_prepare(const void* const* grads_bf16, int nranks, size_t count,
       sw.ptr(a.v[r]);
     }
   }
-  vw = (gw.w16 && sw.w16) ? (sw.w32 ? 32 : 16) : 0;
+  vw = (gw.w16 && sw.w16) ? (sw.w32 ? 32 : 16) : (gp.w16 ? 1 : 0);
   a.count = count;
   a.L = L;
   a.Ld = fastdiv_make(L, count ? count - 1 : 0);
@@ -456,7 +460,8 @@ static cr_status accumulate_impl(float* const* acc, int nranks, size_t count,
       gw.ptr(grads[r]);
     }
   }
-  if ((st = check_disjoint(spans))) return st;
+  st = check_disjoint(spans);
+  if (st) return st;
   if (count == 0) return ok();
   AccumArgs a;
   memset(&a, 0, sizeof(a));

@@ -105,7 +105,7 @@ cr_status cr_reduce_scatter_range(const void* const* bufs, int nranks, size_t co
   const uint64_t nslab = end - begin;
   std::vector<Span> spans;
   std::vector<uint64_t> part_lo(nranks, 0);  // first element of shard j's part
-  Width vw;
+  Width vw, vin;  // every buffer and L; the inputs alone
   vw.bytes(L * is);
   vw.bytes(L * os);
   FoldArgs a;
@@ -124,6 +124,7 @@ cr_status cr_reduce_scatter_range(const void* const* bufs, int nranks, size_t co
     if (nslab) {
       spans.push_back(span_of(bufs[j], nslab * is, 0, j));
       vw.ptr(a.in[j]);
+      vin.ptr(a.in[j]);
     }
     if (len) {
       spans.push_back(span_of(out_shards[j], len * os, 1, j));
@@ -147,7 +148,12 @@ cr_status cr_reduce_scatter_range(const void* const* bufs, int nranks, size_t co
   a.n_out = nranks;
   a.avg = op == CR_AVG;
   a.inv_n = exact_inv_n(nranks);
-  cudaError_t e = launch_fold(in_dtype, out_dtype, kRS, a, vw.get(), (cudaStream_t)stream);
+  int w = vw.get();
+  if (w == 0 && vin.get() != 0) {  // as cr_reduce_scatter: element stores
+    w = vin.get();
+    a.out_scalar = 1;
+  }
+  cudaError_t e = launch_fold(in_dtype, out_dtype, kRS, a, w, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "reduce_scatter_range launch");
   return ok();
 }

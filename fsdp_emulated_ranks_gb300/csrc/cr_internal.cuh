@@ -32,6 +32,9 @@ struct FoldArgs {
   float inv_n;     // 1/n when n is a power of two (exact), else 0
   uint32_t max_ctas;  // cap on the grid (0: one vector per thread)
   int wire_bf16;      // 1: round every forwarded partial to bf16 (a bf16 wire)
+  int out_scalar;     // reduce-scatter: 1 when the chunk length or the shard
+                      // pointers are off the vector grid; the inputs still
+                      // take vector loads, each shard element its own store
 };
 
 struct GatherArgs {
@@ -190,7 +193,8 @@ enum FoldMode { kRS = 0, kAR = 1 };
 
 // Launchers (defined next to their kernels).  `vw` is the vector width in
 // bytes the host layer has checked the buffers allow: 32, 16, or 0 for the
-// element-wise kernels.
+// element-wise kernels; launch_fsdp also takes 1 (vector grads and params,
+// fp32 state element by element).
 // HSDP gradient reduction over an R x S mesh (rank (g, s) at g*S + s): the
 // ring reduce-scatter inside each group of S ranks, then the ring
 // all-reduce of every shard across the R groups.
@@ -205,7 +209,8 @@ struct HsdpArgs {
   FastDiv Ld, L2d, L2lastd;
   int R, S;
   int avg;
-  float inv_n;  // 1/(R*S) when exact, else 0 (divide)
+  float inv_n;     // 1/(R*S) when exact, else 0 (divide)
+  int out_scalar;  // 1: shard offsets off the vector grid, element stores
 };
 
 // The fused bucket all-reduce (api.cu), for the DDP reducer: argument

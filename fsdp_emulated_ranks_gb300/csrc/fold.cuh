@@ -10,11 +10,14 @@
 // and bf16 inputs, uint32 (two's-complement wrap) for int32.
 #pragma once
 
+#include <type_traits>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "cr.h"
+#include "cr_internal.cuh"
 
 namespace cr {
 
@@ -272,6 +275,49 @@ __device__ __forceinline__ void st_elem(void* p, uint64_t e,
   } else {
     static_cast<int32_t*>(p)[e] = (int32_t)x;
   }
+}
+
+// Store of one vector's VEC results into a shard whose offsets are off the
+// vector grid (the reduce-scatters' out_scalar: L or a shard pointer not a
+// multiple of the vector).  Element stores from each thread
+// would hit a different 32-byte sector per lane; when the whole warp holds
+// VEC-element vectors that follow one another in one shard, the warp
+// instead passes its 32 * VEC results through shared memory and writes
+// them lane by lane, each store instruction covering 32 consecutive
+// elements.  Otherwise (a partial warp, a warp across a chunk boundary)
+// each thread stores its own elements.
+template <int DI, int DO, int NW>
+__device__ __forceinline__ void store_offgrid(void* out, uint64_t e0, uint64_t k0, int j,
+                                                 const typename Elem<DI>::Acc* acc) {
+  constexpr int VEC = elems_per<DI, NW>();
+  constexpr int OB = VEC * Elem<DO>::kSize;
+  static_assert(OB % 16 == 0, "whole 16-byte words per thread in the staging buffer");
+  using T = typename std::conditional<DO == CR_BF16, uint16_t, uint32_t>::type;
+  __shared__ __align__(16) T s_out[kBlock / 32][32 * VEC];
+  const unsigned act = __activemask();
+  const int lane = threadIdx.x & 31;
+  bool whole = act == 0xffffffffu;
+  if (whole) {
+    const uint64_t e_first = __shfl_sync(0xffffffffu, e0, 0);
+    const int j_first = __shfl_sync(0xffffffffu, j, 0);
+    whole = __all_sync(0xffffffffu, j == j_first && e0 == e_first + (uint64_t)lane * VEC);
+  }
+  if (!whole) {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) st_elem<DO>(out, k0 + i, acc[i]);
+    return;
+  }
+  uint32_t w[OB / 4];
+  acc_pack<DI, DO, VEC>(acc, w);
+  T* buf = s_out[threadIdx.x >> 5];
+  uint4* bv = reinterpret_cast<uint4*>(buf) + lane * (OB / 16);
+#pragma unroll
+  for (int q = 0; q < OB / 16; ++q) bv[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  __syncwarp();
+  T* dst = static_cast<T*>(out) + __shfl_sync(0xffffffffu, k0, 0);
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) dst[i * 32 + lane] = buf[i * 32 + lane];
+  __syncwarp();  // the buffer is reused by this warp's next vector
 }
 
 template <int D>

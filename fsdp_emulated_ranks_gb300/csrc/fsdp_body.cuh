@@ -25,26 +25,78 @@ __device__ __forceinline__ AdamOut adamw_elem(float p, float m, float v,
   return o;
 }
 
-// 8 fp32 state words at p: one 32-byte access (SW == 8) or two 16-byte ones.
+// 8 fp32 state words at p: one 32-byte access (SW == 8), two 16-byte ones
+// (SW == 4), or eight 4-byte ones (SW == 1: a shard length off the vector
+// grid puts the state of a vector at any 4-byte offset).
 template <int SW>
 __device__ __forceinline__ void ld_state8(const float* p, uint32_t* w) {
   if constexpr (SW == 8) {
     const Words<8> v = ldv<8>(p);
 #pragma unroll
     for (int i = 0; i < 8; ++i) w[i] = v.w[i];
-  } else {
+  } else if constexpr (SW == 4) {
     const uint4 a = ld16(p), b = ld16(p + 4);
     w[0] = a.x, w[1] = a.y, w[2] = a.z, w[3] = a.w;
     w[4] = b.x, w[5] = b.y, w[6] = b.z, w[7] = b.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(p[i]);
   }
 }
 template <int SW>
 __device__ __forceinline__ void st_state8(float* p, const uint32_t* w) {
   if constexpr (SW == 8) {
     st32(p, w);
-  } else {
+  } else if constexpr (SW == 4) {
     st16(p, make_uint4(w[0], w[1], w[2], w[3]));
     st16(p + 4, make_uint4(w[4], w[5], w[6], w[7]));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) p[i] = __uint_as_float(w[i]);
+  }
+}
+
+// The master/m/v stores of one 8-element vector whose shard offset is off
+// the vector grid (SW == 1).  Each thread's 8 floats sit in one 32-byte
+// sector at most two sectors apart from its neighbour's, so plain stores
+// would split every warp store across 32 sectors.  When the whole warp
+// holds consecutive vectors of one shard, each array goes through shared
+// memory and the warp writes 32 consecutive floats per store instruction;
+// otherwise each thread stores its own elements.
+__device__ __forceinline__ void st_state3_offgrid(float* mp, float* mm, float* mv,
+                                                  const uint32_t* po, const uint32_t* mo,
+                                                  const uint32_t* vo, int j, uint64_t e0) {
+  __shared__ __align__(16) uint32_t s_st[kBlock / 32][32 * 8];
+  const unsigned act = __activemask();
+  const int lane = threadIdx.x & 31;
+  bool whole = act == 0xffffffffu;
+  if (whole) {
+    const uint64_t e_first = __shfl_sync(0xffffffffu, e0, 0);
+    const int j_first = __shfl_sync(0xffffffffu, j, 0);
+    whole = __all_sync(0xffffffffu, j == j_first && e0 == e_first + 8ull * lane);
+  }
+  float* const dst[3] = {mp, mm, mv};
+  const uint32_t* const src[3] = {po, mo, vo};
+  if (!whole) {
+#pragma unroll
+    for (int t = 0; t < 3; ++t) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dst[t][i] = __uint_as_float(src[t][i]);
+    }
+    return;
+  }
+  uint32_t* buf = s_st[threadIdx.x >> 5];
+#pragma unroll
+  for (int t = 0; t < 3; ++t) {
+    uint4* bv = reinterpret_cast<uint4*>(buf) + lane * 2;
+    bv[0] = make_uint4(src[t][0], src[t][1], src[t][2], src[t][3]);
+    bv[1] = make_uint4(src[t][4], src[t][5], src[t][6], src[t][7]);
+    __syncwarp();
+    float* d0 = reinterpret_cast<float*>(
+        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(dst[t]), 0));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d0[i * 32 + lane] = __uint_as_float(buf[i * 32 + lane]);
+    __syncwarp();  // the buffer is reused for the next array
   }
 }
 
@@ -116,9 +168,13 @@ __device__ __forceinline__ void fsdp_vector(const void* const* grads, void* cons
     mo[i] = __float_as_uint(o.m);
     vo[i] = __float_as_uint(o.v);
   }
-  st_state8<SW>(mp, po);
-  st_state8<SW>(mm, mo);
-  st_state8<SW>(mv, vo);
+  if constexpr (SW == 1) {
+    st_state3_offgrid(mp, mm, mv, po, mo, vo, j, e0);
+  } else {
+    st_state8<SW>(mp, po);
+    st_state8<SW>(mm, mo);
+    st_state8<SW>(mv, vo);
+  }
   const uint4 pb = make_uint4(pack_bf16x2(__uint_as_float(po[0]), __uint_as_float(po[1])),
                               pack_bf16x2(__uint_as_float(po[2]), __uint_as_float(po[3])),
                               pack_bf16x2(__uint_as_float(po[4]), __uint_as_float(po[5])),

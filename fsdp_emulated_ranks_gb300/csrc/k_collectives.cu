@@ -24,8 +24,6 @@
 // sequence of dependent iterations and the last wave is short.  Ragged
 // ends and buffers that are not 16-byte aligned go through the
 // element-wise kernels.
-#include <type_traits>
-
 #include "check.cuh"
 #include "cr_internal.cuh"
 #include "fold.cuh"
@@ -73,9 +71,9 @@ __device__ __forceinline__ void fold_range(const FoldArgs& a) {
     const uint64_t j64 = fastdiv_div(a.Ld, e0);
     const int j = (int)j64;
     CR_DCHECK(e0 + VEC <= a.end && j64 == e0 / a.L && j < n, kChkFoldChunk);
-    // The reduce-scatter takes vectors only when L is a multiple of VEC.
-    CR_DCHECK(MODE == kAR || e0 + VEC <= (j64 + 1) * a.L, kChkFoldShard);
-    if (MODE == kAR && e0 + VEC > (j64 + 1) * a.L) {
+    // A reduce-scatter with vector stores has L a multiple of VEC.
+    CR_DCHECK(MODE == kAR || a.out_scalar || e0 + VEC <= (j64 + 1) * a.L, kChkFoldShard);
+    if ((MODE == kAR || a.out_scalar) && e0 + VEC > (j64 + 1) * a.L) {
       // The vector straddles a chunk boundary (L % VEC != 0): each element
       // takes its own chunk's ring order.
       for (int i = 0; i < VEC; ++i) fold_store_elem<DI, DO, MODE, WIRE>(a, n, e0 + i);
@@ -87,6 +85,12 @@ __device__ __forceinline__ void fold_range(const FoldArgs& a) {
       if (a.avg) {
 #pragma unroll
         for (int i = 0; i < VEC; ++i) acc[i] = finish_avg(acc[i], n, a.inv_n);
+      }
+    }
+    if constexpr (MODE == kRS) {
+      if (a.out_scalar) {  // the shard offset of e0 is off the vector grid
+        store_offgrid<DI, DO, NW>(a.out[j], e0, e0 - j64 * a.L, j, acc);
+        continue;
       }
     }
     uint32_t w[OB / 4];

@@ -66,7 +66,8 @@ __device__ __forceinline__ float clip_coef(const FsdpArgs& a) {
 // STASH: also park every averaged gradient in params[0] / params[1] (low /
 // high 16 bits) for the update pass -- 4 bytes written per element so that
 // the update pass reads 4 bytes instead of the 2N of a second fold.
-template <int NT, bool VEC, bool STASH = false>
+// STRADDLE: L is not a multiple of 8, so a vector may straddle two shards.
+template <int NT, bool VEC, bool STASH = false, bool STRADDLE = false>
 __global__ void __launch_bounds__(kBlock)
     k_fsdp_sumsq(const __grid_constant__ FsdpArgs a, double* partials) {
   __shared__ double s_warp[kBlock / 32];
@@ -80,8 +81,21 @@ __global__ void __launch_bounds__(kBlock)
     const uint64_t nvec = a.count / 8;
     for (uint64_t iv = tid; iv < nvec; iv += stride) {
       const uint64_t e0 = iv * 8;
+      const uint64_t j64 = fastdiv_div(a.Ld, e0);
+      if (STRADDLE && e0 + 8 > (j64 + 1) * a.L) {
+        // the vector straddles two shards (L not a multiple of 8): each
+        // element in its own shard's fold order
+        for (int i = 0; i < 8; ++i) {
+          const uint64_t e = e0 + i;
+          const float gf =
+              finish_avg(fold_elem<CR_BF16>(a.grads, n, (int)fastdiv_div(a.Ld, e), e), n, a.inv_n);
+          if constexpr (STASH) stash_put(a.params, e, gf);
+          t += (double)gf * (double)gf;
+        }
+        continue;
+      }
       float g[8];
-      fold_vec16<CR_BF16, NT>(a.grads, n, (int)fastdiv_div(a.Ld, e0), e0 * 2, g);
+      fold_vec16<CR_BF16, NT>(a.grads, n, (int)j64, e0 * 2, g);
       // Eight squares summed in fp32, the batch added in fp64: GB300's fp64
       // rate is far below its fp32 rate, and the norm only needs ~1e-7.
       float s8 = 0.0f;
@@ -118,8 +132,10 @@ __global__ void __launch_bounds__(kBlock)
 }
 
 // Vector path: 8 elements (one 16-byte bf16 vector per rank) per thread and
-// iteration; SW = 8 moves the fp32 state in 32-byte accesses.  The body of
-// k_fsdp_vec and k_fsdp_vec4, which differ only in their launch bounds.
+// iteration; SW = 8 moves the fp32 state in 32-byte accesses, SW = 4 in
+// 16-byte ones, SW = 1 element by element (a shard length that is not a
+// multiple of 8).  The body of k_fsdp_vec and k_fsdp_vec4, which differ
+// only in their launch bounds.
 template <int NT, bool STASH>
 __device__ __forceinline__ void fsdp_one(const FsdpArgs& a, int n, float coef, uint64_t e) {
   CR_DCHECK(e >= a.begin && e < a.end && fastdiv_div(a.Ld, e) == e / a.L && e / a.L < (uint64_t)n,
@@ -136,6 +152,15 @@ __device__ __forceinline__ void fsdp_range(const FsdpArgs& a) {
   const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
   for (uint64_t iv = vbeg + tid; iv < vend; iv += stride) {
+    if constexpr (SW == 1) {
+      // L off the vector grid: a vector may straddle two shards, and then
+      // each element takes its own shard's fold order and state
+      const uint64_t e0 = iv * 8;
+      if (e0 + 8 > (fastdiv_div(a.Ld, e0) + 1) * a.L) {
+        for (int i = 0; i < 8; ++i) fsdp_one<NT, STASH>(a, n, coef, e0 + i);
+        continue;
+      }
+    }
     // the 8 elements lie in one shard, inside that shard's length
     CR_DCHECK(fastdiv_div(a.Ld, iv * 8) == iv * 8 / a.L && iv * 8 / a.L < (uint64_t)n &&
                   iv * 8 % a.L + 8 <= a.L && iv * 8 + 8 <= a.end,
@@ -262,6 +287,7 @@ static cudaError_t fsdp_dispatch(const FsdpArgs& a, cudaStream_t s) {
 cudaError_t launch_fsdp(const FsdpArgs& a, int vw, cudaStream_t s) {
   if (vw == 32) return fsdp_dispatch<8>(a, s);
   if (vw == 16) return fsdp_dispatch<4>(a, s);
+  if (vw == 1) return fsdp_dispatch<1>(a, s);
   return launch_flat(k_fsdp_elem, a, a.end - a.begin, s);
 }
 
@@ -270,23 +296,27 @@ cudaError_t launch_adamw(const AdamArgs& a, bool vec, cudaStream_t s) {
              : launch_flat(k_adamw_elem, a, a.n, s);
 }
 
-template <int NT, bool VEC, bool STASH = false>
+template <int NT, bool VEC, bool STASH = false, bool STRADDLE = false>
 static cudaError_t sumsq_launch(const FsdpArgs& a, double* partials, int max_parts,
                                 int* nparts, cudaStream_t s) {
   const uint64_t threads = VEC ? a.count / 8 + 1 : a.count;
   int grid = 0;
   cudaError_t err = persistent_grid(
-      reinterpret_cast<const void*>(k_fsdp_sumsq<NT, VEC, STASH>), threads, &grid);
+      reinterpret_cast<const void*>(k_fsdp_sumsq<NT, VEC, STASH, STRADDLE>), threads, &grid);
   if (err != cudaSuccess) return err;
   if (grid > max_parts) grid = max_parts;
   *nparts = grid;
   clear_stale_error();
-  return launch_pdl(k_fsdp_sumsq<NT, VEC, STASH>, dim3(grid), kBlock, s, a, partials);
+  return launch_pdl(k_fsdp_sumsq<NT, VEC, STASH, STRADDLE>, dim3(grid), kBlock, s, a, partials);
 }
 
 cudaError_t launch_fsdp_sumsq(const FsdpArgs& a, bool vec, double* partials,
                               int max_parts, int* nparts, cudaStream_t s) {
   if (!vec) return sumsq_launch<0, false>(a, partials, max_parts, nparts, s);
+  if (a.L % 8 != 0) {  // vectors may straddle shards: the runtime-N builds
+    return a.stash ? sumsq_launch<0, true, true, true>(a, partials, max_parts, nparts, s)
+                   : sumsq_launch<0, true, false, true>(a, partials, max_parts, nparts, s);
+  }
   if (a.stash) {
     if (a.n == 8) return sumsq_launch<8, true, true>(a, partials, max_parts, nparts, s);
     return sumsq_launch<0, true, true>(a, partials, max_parts, nparts, s);

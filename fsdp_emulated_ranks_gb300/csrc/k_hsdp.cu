@@ -53,8 +53,9 @@ __device__ __forceinline__ void hsdp_elem(const HsdpArgs& a, int R, int S, uint6
 }
 
 // One vector of VEC elements per thread over [0, count); RT/ST > 0 fix the
-// mesh shape at compile time so that all N loads are issued together.  The
-// body of k_hsdp_vec and k_hsdp_vec4, which differ only in launch bounds.
+// mesh shape at compile time (ST > 0 alone: the group size, so that the S
+// loads of each group are issued together).  The body of k_hsdp_vec,
+// k_hsdp_vec3 and k_hsdp_vec4, which differ only in their launch bounds.
 template <int DI, int DO, int RT, int ST, int NW>
 __device__ __forceinline__ void hsdp_range(const HsdpArgs& a) {
   using Acc = typename Elem<DI>::Acc;
@@ -103,6 +104,11 @@ __device__ __forceinline__ void hsdp_range(const HsdpArgs& a) {
         for (int t = 0; t < VEC; ++t) acc[t] = finish_avg(acc[t], R * S, a.inv_n);
       }
     }
+    if (a.out_scalar) {
+      // shard offsets off the vector grid (L or a shard pointer)
+      for (int q = 0; q < R; ++q) store_offgrid<DI, DO, NW>(a.out[q * S + (int)j], e0, k0, (int)j, acc);
+      continue;
+    }
     uint32_t w[OB / 4];
     acc_pack<DI, DO, VEC>(acc, w);
 #pragma unroll 4
@@ -116,11 +122,24 @@ __device__ __forceinline__ void hsdp_range(const HsdpArgs& a) {
 
 // A runtime mesh shape: built for 2 CTAs per SM (125-128 registers; the
 // 32-byte versions spill up to 576 bytes and are still the fastest).  On
-// a 4 x 4 mesh of 64 MiB bf16 ranks GB300 runs it at 5,160 GB/s, against
+// a 4 x 4 mesh of 64 MiB bf16 ranks GB300 ran it at 5,160 GB/s, against
 // 4,550 with default bounds (200-240 registers, 1 CTA per SM) and 2,450
-// under the 4-CTA bound (which spills over a kilobyte).
+// under the 4-CTA bound (which spills over a kilobyte).  Only group sizes
+// other than 2, 4 and 8 take it now (k_hsdp_vec3).
 template <int DI, int DO, int RT, int ST, int NW>
 __global__ void __launch_bounds__(kBlock, 2) k_hsdp_vec(const __grid_constant__ HsdpArgs a) {
+  pdl_enter();
+  hsdp_range<DI, DO, RT, ST, NW>(a);
+}
+
+// A compile-time group size S with a runtime group count R, for 3 CTAs per
+// SM: the S loads of the inner fold are issued together, and the R groups
+// are added one after another into one partial, so the registers do not
+// grow with R (60-80, no spills).  On 64 MiB bf16 ranks GB300 runs meshes
+// of 4 x 4, 8 x 8, 2 x 8, 4 x 8 and 16 x 4 at 7,070-7,330 GB/s (8 x 2:
+// 6,870), against 4,900-6,130 for the runtime-shape kernel.
+template <int DI, int DO, int RT, int ST, int NW>
+__global__ void __launch_bounds__(kBlock, 3) k_hsdp_vec3(const __grid_constant__ HsdpArgs a) {
   pdl_enter();
   hsdp_range<DI, DO, RT, ST, NW>(a);
 }
@@ -157,6 +176,9 @@ static cudaError_t hsdp_dispatch_nw(const HsdpArgs& a, cudaStream_t s) {
   if (a.R == 2 && a.S == 4) return launch_flat_hsdp(k_hsdp_vec4<DI, DO, 2, 4, NW>, a, threads, s);
   if (a.R == 4 && a.S == 2) return launch_flat_hsdp(k_hsdp_vec4<DI, DO, 4, 2, NW>, a, threads, s);
   if (a.R == 2 && a.S == 2) return launch_flat_hsdp(k_hsdp_vec4<DI, DO, 2, 2, NW>, a, threads, s);
+  if (a.S == 2) return launch_flat_hsdp(k_hsdp_vec3<DI, DO, 0, 2, NW>, a, threads, s);
+  if (a.S == 4) return launch_flat_hsdp(k_hsdp_vec3<DI, DO, 0, 4, NW>, a, threads, s);
+  if (a.S == 8) return launch_flat_hsdp(k_hsdp_vec3<DI, DO, 0, 8, NW>, a, threads, s);
   return launch_flat_hsdp(k_hsdp_vec<DI, DO, 0, 0, NW>, a, threads, s);
 }
 
