@@ -59,7 +59,11 @@
  *    even once, after the average.
  *  - Every pointer must be aligned to its element size (CR_ERR_ALIGNMENT).
  *    16-byte aligned buffers take the 128-bit vector path; others a slower
- *    element-wise path with identical results.
+ *    element-wise path with identical results.  Where only the shards are
+ *    off the vector grid (a chunk length that is not a multiple of the
+ *    vector, or an unaligned shard pointer) the rank buffers are still read
+ *    as vectors and the shard elements stored one by one, staged per warp
+ *    so that every store covers 32 consecutive elements.
  */
 #ifndef CR_H
 #define CR_H

@@ -2,7 +2,6 @@
 include/cr.h declares, rejects bad arguments on the host with the documented
 status before touching a device, and its host-only parts (bucket plan,
 traffic accounting) match the oracle exactly."""
-import ctypes as C
 import os
 import re
 

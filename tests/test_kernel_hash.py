@@ -2,7 +2,6 @@
 code of a kernel's translation unit and of the library headers it includes,
 and ignores comments and layout, so documenting a header does not orphan the
 measured profiles while any change of code does."""
-import os
 import shutil
 
 import pytest

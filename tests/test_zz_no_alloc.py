@@ -10,7 +10,6 @@ array the first call filled), and both calls must equal the oracle's clipped
 step bit for bit at a clip coefficient the oracle's norm allows.  This file
 is collected last on purpose.
 """
-import numpy as np
 import pytest
 import torch
 
