@@ -45,7 +45,7 @@ def offs(rng, k, dt):
     return [int(rng.choice(OFFSETS)) for _ in range(k)]
 
 
-@pytest.mark.parametrize("case", range(60))
+@pytest.mark.parametrize("case", range(200))
 def test_fuzz_reduce_scatter_all_reduce(case):
     rng = np.random.default_rng(1000 + case)
     n = int(rng.integers(1, 13))
@@ -79,7 +79,7 @@ def test_fuzz_reduce_scatter_all_reduce(case):
         assert_match(got[r], want[r], out, f"AR n={n} count={count} offs={oi}/{oo} r={r}")
 
 
-@pytest.mark.parametrize("case", range(40))
+@pytest.mark.parametrize("case", range(120))
 def test_fuzz_all_gather_and_wire(case):
     rng = np.random.default_rng(2000 + case)
     n = int(rng.integers(1, 13))
@@ -112,7 +112,7 @@ def test_fuzz_all_gather_and_wire(case):
         assert_match(outs[r].host(), want[r], fout, f"wire n={n} count={count} offs={oi}/{oo}")
 
 
-@pytest.mark.parametrize("case", range(40))
+@pytest.mark.parametrize("case", range(120))
 def test_fuzz_hsdp(case):
     rng = np.random.default_rng(3000 + case)
     R, S = int(rng.integers(1, 5)), int(rng.integers(1, 6))
@@ -131,7 +131,7 @@ def test_fuzz_hsdp(case):
         assert_match(shards[q].host(), want[q], out, f"{R}x{S} count={count} offs={oi}/{oo} q={q}")
 
 
-@pytest.mark.parametrize("case", range(30))
+@pytest.mark.parametrize("case", range(100))
 def test_fuzz_fused_buckets_and_accumulate(case):
     rng = np.random.default_rng(4000 + case)
     n = int(rng.integers(1, 9))
@@ -172,7 +172,7 @@ def test_fuzz_fused_buckets_and_accumulate(case):
         assert_match(to_host(d_acc[r], "f32"), want[r], "f32", f"acc n={n} count={count} offs={oa}/{og}")
 
 
-@pytest.mark.parametrize("case", range(30))
+@pytest.mark.parametrize("case", range(100))
 def test_fuzz_fsdp_step(case):
     """FSDP step, plain or clipped, with every grad, param and state buffer
     at its own offset; two consecutive steps (t = 1, 2)."""
@@ -226,7 +226,7 @@ def test_fuzz_fsdp_step(case):
             assert_match(d_p[r].host(), want_p[r], "bf16", f"n={n} count={count} params[{r}]")
 
 
-@pytest.mark.parametrize("case", range(40))
+@pytest.mark.parametrize("case", range(120))
 def test_fuzz_range_forms(case):
     """Range all-reduce and reduce-scatter over a random slab [lo, hi) of a
     random workload, every slab buffer and shard part at its own offset:
@@ -263,7 +263,7 @@ def test_fuzz_range_forms(case):
         assert_match(g.host(), rs[j][a:a + k], out, f"RS range n={n} shard {j}")
 
 
-@pytest.mark.parametrize("case", range(30))
+@pytest.mark.parametrize("case", range(100))
 def test_fuzz_fsdp2(case):
     """FSDP2 over a random parameter set -- dim0 from 0 to a few times N
     (uneven, empty and one-row shards), rows of 1 to 200 elements -- with
@@ -334,7 +334,7 @@ def test_fuzz_fsdp2(case):
                 assert_match(gg.host(), want_p[q // n][q % n], "bf16", f"params[{q}]: {what}")
 
 
-@pytest.mark.parametrize("case", range(30))
+@pytest.mark.parametrize("case", range(100))
 def test_fuzz_fsdp_step_range(case):
     """The FSDP step over a random slab [lo, hi) of a random workload, every
     slab buffer and shard part at its own offset: the slab's elements of
@@ -383,7 +383,7 @@ def test_fuzz_fsdp_step_range(case):
         assert_match(d_p[r].host(), want_p[r][lo:hi], "bf16", f"params[{r}] {what}")
 
 
-@pytest.mark.parametrize("case", range(30))
+@pytest.mark.parametrize("case", range(100))
 def test_fuzz_bucket_pack_all_reduce_unpack(case):
     """The unfused DDP pipeline -- pack, per-bucket all-reduce, unpack --
     over a random plan, with every tensor and every bucket at its own
