@@ -259,6 +259,18 @@ template <int DI, int DO, int MODE, int NW, bool WIRE>
 static cudaError_t fold_dispatch_nw(const FoldArgs& a, cudaStream_t s) {
   constexpr int VEC = elems_per<DI, NW>();
   const uint64_t threads = (a.end - a.begin) / VEC + 2 * VEC;
+  if constexpr (NW == 8) {
+    // Rank counts below 8 that are not a power of two: with the rank count
+    // a runtime value a thread has only its 3-7 loads in flight at 2 CTAs
+    // per SM; built for the count, at 3 CTAs per SM.
+    switch (a.n) {
+      case 3: return launch_fixed_n<DI, DO, MODE, 3, NW, WIRE>(a, threads, s);
+      case 5: return launch_fixed_n<DI, DO, MODE, 5, NW, WIRE>(a, threads, s);
+      case 6: return launch_fixed_n<DI, DO, MODE, 6, NW, WIRE>(a, threads, s);
+      case 7: return launch_fixed_n<DI, DO, MODE, 7, NW, WIRE>(a, threads, s);
+      default: break;
+    }
+  }
   switch (a.n) {
     case 2: return launch_fixed_n<DI, DO, MODE, 2, NW, WIRE>(a, threads, s);
     case 4: return launch_fixed_n<DI, DO, MODE, 4, NW, WIRE>(a, threads, s);

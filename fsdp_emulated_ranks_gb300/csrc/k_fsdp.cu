@@ -278,7 +278,11 @@ static cudaError_t fsdp_dispatch(const FsdpArgs& a, cudaStream_t s) {
   if (a.stash) return launch_flat(k_fsdp_vec<0, SW, true>, a, threads, s);
   switch (a.n) {
     case 2: return launch_flat(k_fsdp_vec4<2, SW>, a, threads, s);
+    case 3: return launch_flat(k_fsdp_vec4<3, SW>, a, threads, s);
     case 4: return launch_flat(k_fsdp_vec4<4, SW>, a, threads, s);
+    case 5: return launch_flat(k_fsdp_vec4<5, SW>, a, threads, s);
+    case 6: return launch_flat(k_fsdp_vec4<6, SW>, a, threads, s);
+    case 7: return launch_flat(k_fsdp_vec4<7, SW>, a, threads, s);
     case 8: return launch_flat(k_fsdp_vec4<8, SW>, a, threads, s);
     default: return launch_flat(k_fsdp_vec<0, SW>, a, threads, s);
   }
@@ -318,11 +322,17 @@ cudaError_t launch_fsdp_sumsq(const FsdpArgs& a, bool vec, double* partials,
                    : sumsq_launch<0, true, false, true>(a, partials, max_parts, nparts, s);
   }
   if (a.stash) {
-    if (a.n == 8) return sumsq_launch<8, true, true>(a, partials, max_parts, nparts, s);
-    return sumsq_launch<0, true, true>(a, partials, max_parts, nparts, s);
+    switch (a.n) {
+      case 5: return sumsq_launch<5, true, true>(a, partials, max_parts, nparts, s);
+      case 6: return sumsq_launch<6, true, true>(a, partials, max_parts, nparts, s);
+      case 7: return sumsq_launch<7, true, true>(a, partials, max_parts, nparts, s);
+      case 8: return sumsq_launch<8, true, true>(a, partials, max_parts, nparts, s);
+      default: return sumsq_launch<0, true, true>(a, partials, max_parts, nparts, s);
+    }
   }
   switch (a.n) {
     case 2: return sumsq_launch<2, true>(a, partials, max_parts, nparts, s);
+    case 3: return sumsq_launch<3, true>(a, partials, max_parts, nparts, s);
     case 4: return sumsq_launch<4, true>(a, partials, max_parts, nparts, s);
     case 8: return sumsq_launch<8, true>(a, partials, max_parts, nparts, s);
     default: return sumsq_launch<0, true>(a, partials, max_parts, nparts, s);

@@ -55,7 +55,7 @@ def host_inputs(n, count, dt, seed):
 
 # ---- reduce-scatter -------------------------------------------------------------
 
-@pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 16, 64])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 6, 7, 8, 16, 64])
 @pytest.mark.parametrize("pair", PAIRS)
 @pytest.mark.parametrize("offset", [0, 1, "16B"])
 def test_reduce_scatter(n, pair, offset):
@@ -91,7 +91,7 @@ def test_reduce_scatter_in_place(n, dt):
 
 # ---- all-reduce ----------------------------------------------------------------
 
-@pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 16, 64])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 6, 7, 8, 16, 64])
 @pytest.mark.parametrize("pair", PAIRS)
 @pytest.mark.parametrize("offset", [0, 1, "16B"])
 def test_all_reduce(n, pair, offset):
@@ -188,7 +188,7 @@ def fsdp_case(n, count, seed):
     return grads, master, m, v
 
 
-@pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 16, 33, 64])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 6, 7, 8, 16, 33, 64])
 @pytest.mark.parametrize("count_fn", [lambda n: 8 * n * 40, lambda n: 8 * n * 40 + 5, lambda n: 1,
                                       lambda n: 100])
 @pytest.mark.parametrize("offset", [0, 1, "16B"])
@@ -400,7 +400,7 @@ def test_bucket_all_reduce_fused(n, dt, op, offset):
 
 # ---- FSDP step with gradient-norm clipping ----------------------------------------
 
-@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 8, 16, 33, 64])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 6, 7, 8, 16, 33, 64])
 @pytest.mark.parametrize("count_fn", [lambda n: 8 * n * 40, lambda n: 8 * n * 40 + 5,
                                       lambda n: 8 * n * 40 - 3, lambda n: 3])
 @pytest.mark.parametrize("clip", ["active", "inactive"])

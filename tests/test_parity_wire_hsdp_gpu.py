@@ -49,7 +49,7 @@ def sizes(n):
 
 # ---- bf16 wire -------------------------------------------------------------------
 
-@pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 13, 64])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 7, 8, 13, 64])
 @pytest.mark.parametrize("pair", FLOAT_PAIRS)
 @pytest.mark.parametrize("offset", [0, 1, "16B"])
 @pytest.mark.parametrize("wire", ["bf16", "f32"])
