@@ -279,13 +279,14 @@ __device__ __forceinline__ void st_elem(void* p, uint64_t e,
 
 // Store of one vector's VEC results into a shard whose offsets are off the
 // vector grid (the reduce-scatters' out_scalar: L or a shard pointer not a
-// multiple of the vector).  Element stores from each thread
-// would hit a different 32-byte sector per lane; when the whole warp holds
-// VEC-element vectors that follow one another in one shard, the warp
-// instead passes its 32 * VEC results through shared memory and writes
-// them lane by lane, each store instruction covering 32 consecutive
-// elements.  Otherwise (a partial warp, a warp across a chunk boundary)
-// each thread stores its own elements.
+// multiple of the vector).  Element stores straight from each thread would
+// put every lane of a warp store in a different 32-byte sector.  When the
+// whole warp holds VEC-element vectors that follow one another in one
+// shard, the warp instead passes its 32 * VEC results through shared
+// memory and writes them lane by lane, each store instruction covering 32
+// consecutive elements.  Otherwise (a partial warp, a warp across a chunk
+// boundary) each thread stores its own elements.  e0: the vector's first
+// element in the rank buffers; k0: its offset in shard j.
 template <int DI, int DO, int NW>
 __device__ __forceinline__ void store_offgrid(void* out, uint64_t e0, uint64_t k0, int j,
                                                  const typename Elem<DI>::Acc* acc) {
