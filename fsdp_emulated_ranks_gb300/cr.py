@@ -204,7 +204,9 @@ def _ptr_array(xs: Sequence):
         ptrs, n = [0], 1
     pack = _PACK.get(n)
     if pack is None:
-        pack = _PACK[n] = struct.Struct(f"={n}Q").pack
+        pack = struct.Struct(f"={n}Q").pack
+        if len(_PACK) < 256:  # a bounded cache: callers use few table lengths
+            _PACK[n] = pack
     return pack(*ptrs)
 
 
