@@ -295,6 +295,38 @@ def test_fsdp2_plan_host_side(L):
     del plan, empty
 
 
+def test_range_forms_validation(L):
+    """The range forms check the range, the slab-local buffers and their
+    overlaps before anything else, and an empty range has nothing to do
+    (every pointer here is fake)."""
+    n, count = 4, 1000
+    L_ = cr.cr_chunk_len(count, n)
+    ins = [FAKE + r * (1 << 20) for r in range(n)]
+    outs = [FAKE + (1 << 30) + r * (1 << 20) for r in range(n)]
+    for lo, hi in ((5, 4), (0, count + 1), (count + 1, count + 1)):
+        expect(1, cr.cr_all_reduce_range, ins, count, lo, hi, "f32", "sum", outs, "f32", stream=0)
+        expect(1, cr.cr_reduce_scatter_range, ins, count, lo, hi, "f32", "sum", outs, "f32",
+               stream=0)
+        expect(1, cr.cr_fsdp_step_range, ins, count, lo, hi, outs, outs, outs, cr.adamw_cfg(),
+               ins, stream=0)
+    # element alignment of the slab pointers, NULL buffers, overlapping outputs
+    expect(3, cr.cr_all_reduce_range, [ins[0] + 2] + ins[1:], count, 0, 10, "f32", "sum", outs,
+           "f32", stream=0)
+    expect(1, cr.cr_all_reduce_range, [0] + ins[1:], count, 0, 10, "f32", "sum", outs, "f32",
+           stream=0)
+    expect(1, cr.cr_all_reduce_range, ins, count, 0, 10, "f32", "sum", [outs[0]] * n, "f32",
+           stream=0)
+    expect(2, cr.cr_all_reduce_range, ins, count, 0, 10, "i32", "avg", outs, "i32", stream=0)
+    # reduce-scatter parts: shard 0's part of [0, L + 5) is L elements, shard 1's 5
+    expect(1, cr.cr_reduce_scatter_range, ins, count, 0, L_ + 5, "f32", "sum",
+           [outs[0], 0, 0, 0], "f32", stream=0)
+    # empty ranges: valid, nothing launched
+    cr.cr_all_reduce_range(ins, count, 7, 7, "f32", "sum", outs, "f32", stream=0)
+    cr.cr_reduce_scatter_range(ins, count, 7, 7, "f32", "sum", [0] * n, "f32", stream=0)
+    cr.cr_fsdp_step_range(ins, count, 7, 7, [0] * n, [0] * n, [0] * n, cr.adamw_cfg(), outs,
+                          stream=0)
+
+
 def test_wire_validation(L):
     n = 4
     bufs = [FAKE + r * (1 << 20) for r in range(n)]
